@@ -1,0 +1,336 @@
+"""Pins of the CPU oracle to facts that do not come from the oracle itself.
+
+* the pages' worked rows (tests/golden/hand_rows.json, each with its citation);
+* the closed form of the correctness theorem, Pr[out = j] = p_j / Z, checked
+  exactly (rational arithmetic) against the dual-pivot algorithm's own recurrence;
+* brute-force membership by counting (no sort) against the sort-based sets;
+* Philox4x32-10 known-answer vectors of its published reference implementation;
+* special cases with textbook answers (k = 1 is arg-max, k = V is no filter,
+  top-p 1 keeps every positive entry, min-p 1 keeps the maximum, ...);
+* planted mistakes in the oracle that these pins must catch.
+"""
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from oracle import bruteforce, dual_pivot, filters, philox
+import workloads
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_rows.json")
+
+
+def _cases():
+    with open(GOLDEN) as fh:
+        return json.load(fh)["cases"]
+
+
+def _ratio(s: str) -> float:
+    a, b = s.split("/")
+    return float(a) / float(b)
+
+
+# ---------------------------------------------------------------- hand rows
+
+@pytest.mark.parametrize("case", _cases(), ids=lambda c: c["id"])
+def test_hand_row_sets_and_values(case):
+    p = np.array(case["probs"], np.float32)
+    args = (case["top_k"], case["top_p"], case["min_p"], case["order"])
+    S = filters.allowed_set(p, *args)
+    assert S.tolist() == case["expected_set"]
+    assert bruteforce.members(p, *args).tolist() == case["expected_set"]
+    pt, ok = filters.filtered_distribution(p, *args)
+    assert ok
+    for j, r in case["expected_ptilde"].items():
+        assert abs(pt[int(j)] - _ratio(r)) < 1e-6
+    assert abs(pt.sum() - 1.0) < 1e-12
+    law = dual_pivot.exact_output_law(p, *args)
+    assert sorted(law) == case["expected_set"]
+    for j, r in case["expected_ptilde"].items():
+        assert abs(float(law[int(j)]) - _ratio(r)) < 1e-6
+
+
+def test_drill_threshold_and_prefix_masses():
+    c = _cases()[0]
+    p = np.array(c["probs"], np.float32)
+    assert filters.top_p_threshold(p, c["top_p"]) == pytest.approx(np.float32(c["expected_threshold"]), abs=0)
+    vals = np.sort(p.astype(np.float64))[::-1]
+    assert np.allclose(np.cumsum(vals)[:3], c["expected_prefix_masses"], atol=1e-7)
+    c2 = _cases()[1]
+    assert filters.top_k_threshold(p, c2["top_k"]) == np.float32(c2["expected_threshold"])
+    out, ok = filters.top_p_renorm(p, 0.8)
+    assert ok and np.allclose(out, [0, 0.40 / 0.85, 0, 0.30 / 0.85, 0.15 / 0.85], atol=1e-7)
+    out, ok = filters.top_k_renorm(p, 2)
+    assert ok and np.allclose(out, [0, 0.40 / 0.70, 0, 0.30 / 0.70, 0], atol=1e-7)
+
+
+def test_explainer_topk_walkthrough_rounds():
+    """The explainer's walk-through: drawing D then C raises `low` to 0.12 then 0.18,
+    after which only A and B remain and every further draw is accepted."""
+    p = np.array([0.35, 0.28, 0.18, 0.12, 0.07], np.float32)
+    row = dual_pivot._Row(p, 2, None, None, "joint")
+    assert not row.f(np.float32(0.12)) and not row.f(np.float32(0.18))
+    assert row.f(np.float32(0.28)) and row.f(np.float32(0.35))
+    # From low = 0.18 only A and B are drawable; both are accepted.
+    for u in (0.0, 0.3, 0.6, 0.99):
+        j = dual_pivot.draw_inverse_transform(p.astype(np.float64), float(np.float32(0.18)), u)
+        assert j in (0, 1)
+
+
+# ---------------------------------------------------------------- brute force vs sort
+
+EDGE_K = [None, 0, 1, 2, 3, 5, 7, 8, 9]
+EDGE_P = [None, 0.0, 1e-3, 0.3, 0.5, 0.75, 0.9, 0.999, 1.0]
+EDGE_MINP = [None, 0.0, 0.05, 0.3, 0.7, 1.0, 1.5]
+
+
+def test_bruteforce_matches_sorted_sets():
+    rng = np.random.default_rng(5)
+    n_checked = 0
+    for V in (1, 2, 3, 5, 8):
+        rows = workloads.random_small_rows(60, V, seed=100 + V, zero_prob=0.2)
+        for p in rows:
+            if not (p > 0).any():
+                continue
+            for order in filters.ORDERS:
+                for _ in range(12):
+                    k = EDGE_K[rng.integers(len(EDGE_K))]
+                    tp = EDGE_P[rng.integers(len(EDGE_P))]
+                    mp = EDGE_MINP[rng.integers(len(EDGE_MINP))]
+                    if filters.topp_boundary_margin(p, k, tp, mp, order) < 1e-9:
+                        continue
+                    a = filters.allowed_set(p, k, tp, mp, order).tolist()
+                    b = bruteforce.members(p, k, tp, mp, order).tolist()
+                    assert a == b, (p, k, tp, mp, order)
+                    n_checked += 1
+    assert n_checked > 3000
+
+
+# ---------------------------------------------------------------- closed form of the theorem
+
+def _closed_form(p, k, tp, mp, order):
+    S = filters.allowed_set(p, k, tp, mp, order)
+    vals = {int(j): Fraction(float(np.float32(p[j]))) for j in S}
+    Z = sum(vals.values(), Fraction(0))
+    return {j: v / Z for j, v in vals.items()}
+
+
+@pytest.mark.parametrize("midpoint", ["exact", "fp32"])
+def test_exact_law_equals_pj_over_Z(midpoint):
+    rng = np.random.default_rng(7 if midpoint == "exact" else 8)
+    n = 0
+    for V in (1, 2, 3, 4, 5, 6):
+        rows = workloads.random_small_rows(8, V, seed=300 + V, zero_prob=0.15)
+        for p in rows:
+            if not (p > 0).any():
+                continue
+            for order in filters.ORDERS:
+                for _ in range(4):
+                    k = EDGE_K[rng.integers(len(EDGE_K))]
+                    tp = EDGE_P[rng.integers(len(EDGE_P))]
+                    mp = EDGE_MINP[rng.integers(len(EDGE_MINP))]
+                    if filters.topp_boundary_margin(p, k, tp, mp, order) < 1e-9:
+                        continue
+                    law = dual_pivot.exact_output_law(p, k, tp, mp, order, midpoint=midpoint)
+                    assert law == _closed_form(p, k, tp, mp, order), (p, k, tp, mp, order)
+                    n += 1
+    assert n > 150
+
+
+def test_exact_law_on_an_8_token_row_every_k():
+    p = workloads.random_small_rows(1, 8, seed=4242)[0]
+    for k in range(1, 9):
+        law = dual_pivot.exact_output_law(p, k, None, None)
+        assert law == _closed_form(p, k, None, None, "joint")
+        assert sum(law.values()) == 1
+
+
+# ---------------------------------------------------------------- special cases
+
+def test_special_cases():
+    p = workloads.random_small_rows(1, 7, seed=9)[0]
+    am = int(np.argmax(p))
+    pos = np.nonzero(p > 0)[0].tolist()
+    assert filters.allowed_set(p, 1).tolist() == [am]                      # k = 1 is greedy
+    assert filters.allowed_set(p, 7).tolist() == pos                       # k = V: no filter
+    assert filters.allowed_set(p, 0).tolist() == pos                       # k <= 0: no filter
+    assert filters.allowed_set(p, None, 1.0).tolist() == pos               # top-p 1 keeps all
+    assert filters.allowed_set(p, None, 0.0).tolist() == [am]              # top-p 0: arg-max
+    assert filters.allowed_set(p, None, None, 1.0).tolist() == [am]        # min-p 1: the max
+    assert filters.allowed_set(p, None, None, 1.5).tolist() == []          # min-p > 1: empty
+    pt, ok = filters.filtered_distribution(p)
+    assert ok and np.allclose(pt, p / p.astype(np.float64).sum())
+    # min-p is invariant to scaling the row (max and threshold scale together).
+    assert filters.allowed_set(p * 3, None, None, 0.3).tolist() == filters.allowed_set(p, None, None, 0.3).tolist()
+
+
+@pytest.mark.parametrize("bad", ["nan", "neg", "zero"])
+def test_invalid_rows(bad):
+    p = np.array([0.1, 0.2, 0.3, 0.4], np.float32)
+    if bad == "nan":
+        p[2] = np.nan
+    elif bad == "neg":
+        p[1] = -0.1
+    else:
+        p[:] = 0
+    assert filters.allowed_set(p, 2, 0.9).size == 0
+    assert bruteforce.members(p, 2, 0.9).size == 0
+    assert dual_pivot.sample(p, 2, 0.9, uniform=lambda r: 0.5) == (-1, False, 0)
+    assert dual_pivot.exact_output_law(p, 2, 0.9) == {}
+    out, ok = filters.top_k_renorm(p, 2)
+    assert not ok and not out.any()
+
+
+def test_renorm_and_mask_definitions():
+    rng = np.random.default_rng(3)
+    for _ in range(50):
+        V = int(rng.integers(2, 40))
+        p = workloads.random_small_rows(1, V, seed=int(rng.integers(1 << 30)))[0]
+        k = int(rng.integers(1, V))
+        out, ok = filters.top_k_renorm(p, k)
+        assert ok and np.count_nonzero(out) == k and abs(out.sum() - 1) < 1e-12
+        kept = out > 0
+        assert p[kept].min() > p[~kept].max()
+        tp = float(rng.uniform(0.05, 0.95))
+        out, ok = filters.top_p_renorm(p, tp)
+        kept = np.sort(p[out > 0].astype(np.float64))
+        M = p.astype(np.float64).sum()
+        assert kept.sum() >= np.float32(tp) * M                  # reaches p
+        assert kept[1:].sum() < np.float32(tp) * M               # and is the smallest such prefix
+        z = (rng.normal(size=V) * 3).astype(np.float32)
+        mz, ok = filters.top_k_mask_logits(z, k)
+        assert ok and np.isfinite(mz).sum() == k
+        assert set(np.nonzero(np.isfinite(mz))[0]) == set(np.argsort(-z)[:k])
+    z = np.array([1.0, np.nan, 2.0], np.float32)
+    mz, ok = filters.top_k_mask_logits(z, 1)
+    assert not ok and np.isneginf(mz).all()
+
+
+# ---------------------------------------------------------------- Philox
+
+# Known-answer vectors of the Random123 reference distribution (counter, key, output).
+PHILOX_KAT = [
+    ((0, 0, 0, 0), (0, 0), (0x6627E8D5, 0xE169C58D, 0xBC57AC4C, 0x9B00DBD8)),
+    ((0xFFFFFFFF,) * 4, (0xFFFFFFFF,) * 2, (0x408F276D, 0x41C83B0E, 0xA20BC7C6, 0x6D5451FD)),
+    ((0x243F6A88, 0x85A308D3, 0x13198A2E, 0x03707344), (0xA4093822, 0x299F31D0),
+     (0xD16CFE09, 0x94FDCCEB, 0x5001E420, 0x24126EA1)),
+]
+
+
+@pytest.mark.parametrize("ctr,key,out", PHILOX_KAT)
+def test_philox_known_answers(ctr, key, out):
+    assert philox.philox4x32_10(ctr, key) == out
+    got = philox.philox4x32_10_np(np.array([ctr], np.uint32), np.array([key], np.uint32))
+    assert tuple(int(x) for x in got[0]) == out
+
+
+def test_philox_uniform_grid_and_spread():
+    us = np.array([philox.sampler_uniform(123, 7, b, r) for b in range(200) for r in range(20)])
+    assert ((us >= 0) & (us < 1)).all()
+    assert np.all(us * 2 ** 24 == np.floor(us * 2 ** 24))
+    hist = np.histogram(us, bins=10, range=(0, 1))[0]
+    assert hist.min() > 300 and hist.max() < 500
+    # Different offsets (calls) and rows give different streams.
+    assert philox.sampler_uniform(1, 0, 0, 0) != philox.sampler_uniform(1, 1, 0, 0)
+    assert philox.sampler_uniform(1, 0, 0, 0) != philox.sampler_uniform(1, 0, 1, 0)
+
+
+# ---------------------------------------------------------------- replayed sampler
+
+def test_replayed_sampler_matches_law_and_round_bound():
+    p = workloads.random_small_rows(1, 16, seed=77)[0]
+    for k, tp, mp, order in [(5, None, None, "joint"), (8, 0.6, None, "top_k_first"),
+                             (None, 0.7, None, "joint"), (None, None, 0.3, "joint"),
+                             (12, 0.8, 0.1, "joint")]:
+        pt, _ = filters.filtered_distribution(p, k, tp, mp, order)
+        bound = filters.round_bound(p, k, tp, mp, order)
+        n = 6000
+        counts = np.zeros(16)
+        for b in range(n):
+            tok, ok, rounds = dual_pivot.sample_philox(p, k, tp, mp, order, seed=99, offset=3, row=b)
+            assert ok and pt[tok] > 0 and 1 <= rounds <= bound
+            counts[tok] += 1
+        tv = 0.5 * np.abs(counts / n - pt).sum()
+        assert tv < 0.03
+
+
+# ---------------------------------------------------------------- planted mistakes
+
+def _law_ok(p, args):
+    return dual_pivot.exact_output_law(p, *args) == _closed_form(p, *args)
+
+
+def test_pins_catch_planted_mistakes(monkeypatch):
+    """Each mutation of the oracle below is a plausible slip; a pin must fail on it."""
+    # A graded row, so that every case of the three-way update is reached.
+    p = np.array([0.30, 0.25, 0.20, 0.15, 0.10], np.float32)
+    cases = [(3, None, None, "joint"), (None, 0.6, None, "joint"), (4, 0.7, None, "top_k_first")]
+    assert all(_law_ok(p, c) for c in cases)
+    orig_f = dual_pivot._Row.f
+
+    def inclusive_mass(self, tau):          # top-p test counting the pivot's own mass
+        cnt, mass = self.count_mass_above(tau)
+        mass = mass + (Fraction(float(tau)) if self.exact else float(tau))
+        if self.k_on and not cnt < self.k:
+            return False
+        if self.p_on and not (cnt == 0 or mass < self.top_p * self.Mp):
+            return False
+        return True
+
+    def count_le(self, tau):                # top-k test with <= k
+        cnt, mass = self.count_mass_above(tau)
+        if self.k_on and not cnt <= self.k:
+            return False
+        return orig_f(self, tau) or (self.k_on and cnt == self.k)
+
+    for bad in (inclusive_mass, count_le):
+        monkeypatch.setattr(dual_pivot._Row, "f", bad)
+        assert not all(_law_ok(p, c) for c in cases), bad.__name__
+    monkeypatch.setattr(dual_pivot._Row, "f", orig_f)
+
+    # Swapped cases 2 and 3: `low` jumps to pivot2 although f(pivot2) = 1.
+    def swapped(row, pivot1, high, midpoint):
+        if row.f(pivot1):
+            return None
+        pivot2 = row.midpoint(pivot1, high, midpoint)
+        return (pivot2, high) if row.f(pivot2) else (pivot1, pivot2)
+
+    monkeypatch.setattr(dual_pivot, "three_cases", swapped)
+    assert not all(_law_ok(p, c) for c in cases)
+    monkeypatch.undo()
+    assert all(_law_ok(p, c) for c in cases)
+
+    # The order matters (explainer, filter-order section): on its row with top-p 0.75,
+    # top-k-first measures 0.75 * F_k = 0.675 and stops at {A,B} (0.70), while joint
+    # measures 0.75 * M = 0.75 and needs {A,B,C}.  Measuring top-k-first against M
+    # (a plausible slip) would make the two agree.
+    q = np.array([0.40, 0.30, 0.20, 0.10], np.float32)
+    assert filters.allowed_set(q, 3, 0.6, None, "top_k_first").tolist() == [0, 1]
+    assert filters.allowed_set(q, 3, 0.9, None, "top_k_first").tolist() == [0, 1, 2]
+    assert filters.allowed_set(q, 3, 0.9, None, "joint").tolist() == [0, 1, 2]
+    assert filters.allowed_set(q, 3, 0.75, None, "top_k_first").tolist() == [0, 1]
+    assert filters.allowed_set(q, 3, 0.75, None, "joint").tolist() == [0, 1, 2]
+    assert bruteforce.members(q, 3, 0.75, None, "top_k_first").tolist() == [0, 1]
+    assert bruteforce.members(q, 3, 0.75, None, "joint").tolist() == [0, 1, 2]
+
+
+# ---------------------------------------------------------------- generators
+
+def test_generators_tie_free_and_deterministic():
+    w = workloads.config1()
+    assert w.probs.shape == (4, 1024) and w.probs.dtype == np.float32
+    for r in w.probs:
+        assert not workloads.has_positive_ties(r)
+    w2 = workloads.config1()
+    assert np.array_equal(w.probs, w2.probs)
+    x, nb = workloads.detie(np.array([0.5, 0.5, 0.5, 0.0, 0.0, 0.25], np.float32))
+    assert nb == 2 and not workloads.has_positive_ties(x) and (x == 0).sum() == 2
+    w4 = workloads.config4(batch_in=2, vocab=4096)
+    assert w4.indices.tolist() == [0, 0, 0, 0, 1, 1, 1, 1]
+    w5 = workloads.config5(batch=40, vocab=2000)
+    assert len(w5.bad_rows) == 2
+    for r in w5.bad_rows:
+        assert not filters.row_is_valid(w5.probs[r])
