@@ -1,0 +1,179 @@
+/*
+ * fs_sampling.h -- sorting-free top-k / top-p / min-p sampling on GB300 (sm_103a).
+ *
+ * C ABI of libfs_sampling.so.  Sources of the operations (three web pages on one
+ * subject):
+ *   [blog]      "Sorting-Free GPU Kernels for LLM Sampling" (FlashInfer blog):
+ *               Top-K / Top-P / Min-P, inverse transform sampling, rejection
+ *               sampling, dual-pivot rejection sampling, correctness proof,
+ *               implementation details (guarded parallel prefix sums).
+ *   [drill]     "F4: top-k / top-p without sorting" (GPU kernel drills hint page):
+ *               sections 2-4 (threshold by bisection on count / mass, bisection on
+ *               the fp32 bit pattern), section 8 (signed values need their sign
+ *               handled before a bit-pattern comparison).
+ *   [explainer] FlashInfer sorting-free sampling explainer: the allowed set S and
+ *               renormalised distribution, top-k-first vs joint order, the API list
+ *               (direct sampling vs filter-only), seed/offset and RNG ownership,
+ *               degenerate rows.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every pointer argument is a DEVICE pointer owned by the caller, unless stated.
+ *    The library allocates no memory, keeps no per-call state and may be called
+ *    from several host threads at once.  Each call is asynchronous on `stream`
+ *    (a cudaStream_t passed as void*; NULL is the legacy default stream).
+ *  - `probs` / `logits` are row-major [batch_in, vocab] float32, contiguous (row
+ *    stride = vocab).  Rows are probabilities (or unnormalised non-negative scores;
+ *    every filter is scale-invariant, see top-p below).
+ *  - Sampling entries produce one token per OUTPUT row b in [0, batch_out).
+ *    `indices` (nullable) maps output row b to input row indices[b]; when NULL,
+ *    batch_out must equal batch_in and row b reads input row b.  Several output rows
+ *    may share an input row (parallel samples); each still draws its own numbers.
+ *  - Per-row parameter arrays are indexed by OUTPUT row (length batch_out):
+ *      top_k[b] <= 0 or >= vocab     : no top-k filter;
+ *      top_p[b] >= 1                 : no top-p filter; top_p[b] <= 0 keeps the arg-max;
+ *      min_p[b] <= 0                 : no min-p filter; min_p[b] > 1 keeps nothing.
+ *  - Random numbers: Philox4x32-10 (Salmon et al., SC'11) with
+ *      key = (seed lo, seed hi), counter = (round, output row b, offset lo, offset hi);
+ *    u = (first word >> 8) * 2^-24.  A caller must advance `offset` on every call
+ *    ([explainer] seed/offset: reusing it repeats the same draws).  The same inputs,
+ *    seed, offset and launch give the same tokens (no atomics decide a result).
+ *  - Outputs of sampling entries: out_token[b] (int32), out_valid[b] (uint8: 1 valid,
+ *    0 invalid) and, if out_rounds != NULL, out_rounds[b] = number of draws made.
+ *    A row is INVALID -- token -1, valid 0, never token 0 ([explainer] degenerate
+ *    rows) -- when its input row holds a NaN or a negative entry, sums to 0 (or its
+ *    float32 total overflows), keeps no token (e.g. min_p > 1), has a NaN parameter,
+ *    indices[b] is out of range, or FS_MAX_ROUNDS draws end without acceptance.
+ *  - Return value (fs_status): only what the host can check -- NULL required
+ *    pointers, vocab < 1, vocab > FS_MAX_VOCAB, batch < 0, indices == NULL with
+ *    batch_out != batch_in, a bad order value -- or a CUDA launch error
+ *    (FS_ERR_CUDA; fs_last_error_string() then holds the CUDA message).  A call
+ *    with batch_out == 0 (or batch == 0) does nothing and returns FS_OK.  Data
+ *    problems of single rows never become a status; they become valid = 0.
+ */
+#ifndef FS_SAMPLING_H
+#define FS_SAMPLING_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fs_status {
+    FS_OK = 0,
+    FS_ERR_INVALID_ARG = 1,
+    FS_ERR_UNSUPPORTED = 2,
+    FS_ERR_CUDA = 3
+} fs_status;
+
+/* Order of top-k and top-p ([explainer] filter order; [blog] footnote 1).
+ * TOP_K_FIRST: keep the top k, then apply top-p inside them with their mass
+ *              renormalised (top-p measured against F_k = mass of the k kept);
+ * JOINT:       the filters are checked together in every rejection round, each on
+ *              the original row (S = S_k intersect S_p intersect S_min). */
+typedef enum fs_order {
+    FS_ORDER_TOP_K_FIRST = 0,
+    FS_ORDER_JOINT = 1
+} fs_order;
+
+#define FS_MAX_VOCAB 2097152   /* largest supported vocab */
+#define FS_MAX_ROUNDS 256      /* rejection rounds before a row is reported invalid */
+
+/* Plain categorical sampling: one draw by inverse transform over the whole row.
+ * [blog] "inverse transform sampling": u ~ U[0,1), the token k with
+ * F_{k-1} <= u * M < F_k, located tile by tile with a guarded prefix sum
+ * ([blog] "implementation details"). */
+fs_status fs_sampling_from_probs(const float* probs, int32_t batch_in, int32_t vocab,
+                                 const int32_t* indices, int32_t batch_out,
+                                 uint64_t seed, uint64_t offset,
+                                 int32_t* out_token, uint8_t* out_valid,
+                                 int32_t* out_rounds, void* stream);
+
+/* Top-k sampling by dual-pivot rejection ([blog] "dual-pivot rejection sampling",
+ * proof section: Pr[out = j] = p_j / Z on the k largest).  top_k: [batch_out] int32. */
+fs_status fs_top_k_sampling(const float* probs, int32_t batch_in, int32_t vocab,
+                            const int32_t* indices, int32_t batch_out,
+                            const int32_t* top_k,
+                            uint64_t seed, uint64_t offset,
+                            int32_t* out_token, uint8_t* out_valid,
+                            int32_t* out_rounds, void* stream);
+
+/* Top-p (nucleus) sampling: S = the smallest descending prefix whose mass reaches
+ * top_p * M, M = the row's own total ([explainer] Top-p, ">=" form).
+ * top_p: [batch_out] float32. */
+fs_status fs_top_p_sampling(const float* probs, int32_t batch_in, int32_t vocab,
+                            const int32_t* indices, int32_t batch_out,
+                            const float* top_p,
+                            uint64_t seed, uint64_t offset,
+                            int32_t* out_token, uint8_t* out_valid,
+                            int32_t* out_rounds, void* stream);
+
+/* Min-p sampling: S = {i : p_i >= min_p * max_j p_j} ([blog] Min-P).  The threshold
+ * is the float32 rounded up from the exact product, so p_i >= threshold holds exactly
+ * when p_i >= min_p * max.  min_p: [batch_out] float32. */
+fs_status fs_min_p_sampling(const float* probs, int32_t batch_in, int32_t vocab,
+                            const int32_t* indices, int32_t batch_out,
+                            const float* min_p,
+                            uint64_t seed, uint64_t offset,
+                            int32_t* out_token, uint8_t* out_valid,
+                            int32_t* out_rounds, void* stream);
+
+/* Combined top-k + top-p (+ optional min-p) sampling, order = fs_order value
+ * ([explainer] filter order).  top_k and top_p are required ([batch_out] each);
+ * min_p is nullable and, when given, is intersected in either order. */
+fs_status fs_top_k_top_p_sampling(const float* probs, int32_t batch_in, int32_t vocab,
+                                  const int32_t* indices, int32_t batch_out,
+                                  const int32_t* top_k, const float* top_p,
+                                  const float* min_p, int32_t order,
+                                  uint64_t seed, uint64_t offset,
+                                  int32_t* out_token, uint8_t* out_valid,
+                                  int32_t* out_rounds, void* stream);
+
+/* Filter-only: keep x >= t, t = the largest threshold with count(x >= t) >= k, found
+ * exactly on the fp32 bit pattern ([drill] sections 2-4); write x / (kept mass), 0
+ * elsewhere.  top_k: [batch] int32 (<= 0 or >= vocab: keep all).  out_probs:
+ * [batch, vocab] float32, may equal probs (in place).  out_valid: [batch] uint8,
+ * nullable; an invalid row (NaN, negative, zero or overflowing total) is written as
+ * zeros. */
+fs_status fs_top_k_renorm_probs(const float* probs, int32_t batch, int32_t vocab,
+                                const int32_t* top_k, float* out_probs,
+                                uint8_t* out_valid, void* stream);
+
+/* Filter-only top-p: t = the largest threshold with mass(x >= t) >= top_p * M
+ * ([drill] sections 2-4); writes x / mass(x >= t) or 0.  top_p: [batch] float32
+ * (>= 1 keeps all, <= 0 keeps the arg-max, NaN makes the row invalid).  out_probs
+ * may equal probs. */
+fs_status fs_top_p_renorm_probs(const float* probs, int32_t batch, int32_t vocab,
+                                const float* top_p, float* out_probs,
+                                uint8_t* out_valid, void* stream);
+
+/* Filter-only on logits: keep the k largest, write -inf elsewhere.  The threshold is
+ * found on an order-preserving integer key of the signed float ([drill] section 8:
+ * negative bit patterns sort backwards, so the key flips them).  A row holding a NaN
+ * is invalid and written as -inf.  top_k: [batch] int32 (<= 0 or >= vocab: copy).
+ * out_logits may equal logits. */
+fs_status fs_top_k_mask_logits(const float* logits, int32_t batch, int32_t vocab,
+                               const int32_t* top_k, float* out_logits,
+                               uint8_t* out_valid, void* stream);
+
+/* The counter-based generator the samplers draw from, exposed for checking:
+ * out[4i..4i+3] = Philox4x32-10(counter = ctr[4i..4i+3], key = key[2i..2i+1]).
+ * ctr: [n,4] uint32, key: [n,2] uint32, out: [n,4] uint32 (device pointers). */
+fs_status fs_philox4x32_10(const uint32_t* ctr, const uint32_t* key, int64_t n,
+                           uint32_t* out, void* stream);
+
+/* Static description of a status code. */
+const char* fs_status_string(int32_t status);
+
+/* Message of the last FS_ERR_CUDA returned to the calling host thread ("" if none). */
+const char* fs_last_error_string(void);
+
+/* FS_MAX_VOCAB, for bindings that cannot read the macro. */
+int32_t fs_max_vocab(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FS_SAMPLING_H */

@@ -1,0 +1,126 @@
+// Status strings, launch planning and the Philox entry point.
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <set>
+#include <utility>
+
+#include "fs_host.h"
+
+namespace fsd {
+
+static thread_local char g_last_error[256] = "";
+
+fs_status cuda_fail(cudaError_t e) {
+    std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+    return FS_ERR_CUDA;
+}
+
+fs_status device_limits(int& sm_count, size_t& smem_optin) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    static std::mutex mu;
+    static int cached_sm[64] = {0};
+    static size_t cached_smem[64] = {0};
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev < 0 || dev >= 64) return FS_ERR_UNSUPPORTED;
+    if (cached_sm[dev] == 0) {
+        int v = 0;
+        e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e);
+        int s = 0;
+        e = cudaDeviceGetAttribute(&s, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e != cudaSuccess) return cuda_fail(e);
+        cached_sm[dev] = v;
+        cached_smem[dev] = size_t(s);
+    }
+    sm_count = cached_sm[dev];
+    smem_optin = cached_smem[dev];
+    return FS_OK;
+}
+
+fs_status make_plan(int rows, int vocab, Plan& p) {
+    int sms = 0;
+    size_t optin = 0;
+    fs_status st = device_limits(sms, optin);
+    if (st != FS_OK) return st;
+    p.ns = (vocab + SEG - 1) / SEG;
+    long long want = (2LL * sms + rows - 1) / rows;
+    int C = int(want < 1 ? 1 : (want > MAX_CLUSTER ? MAX_CLUSTER : want));
+    if (C > p.ns) C = p.ns;
+    if (p.ns < 8) C = 1;
+    if (C < 1) C = 1;
+    p.C = C;
+    p.nsc = (p.ns + C - 1) / C;
+    p.smem = Layout(p.nsc, p.ns).total;
+    if (p.smem > optin) return FS_ERR_UNSUPPORTED;
+    return FS_OK;
+}
+
+fs_status prepare_kernel(const void* fn, size_t smem) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    static std::mutex mu;
+    static std::set<std::pair<const void*, int>> done;
+    std::lock_guard<std::mutex> lock(mu);
+    if (done.count({fn, dev})) return FS_OK;
+    size_t optin = 0;
+    int sms = 0;
+    fs_status st = device_limits(sms, optin);
+    if (st != FS_OK) return st;
+    // Opt in to the device maximum once, so every later launch fits.
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(optin));
+    if (e != cudaSuccess) return cuda_fail(e);
+    (void)smem;
+    done.insert({fn, dev});
+    return FS_OK;
+}
+
+__global__ void philox_kernel(const uint32_t* __restrict__ ctr, const uint32_t* __restrict__ key, int64_t n,
+                              uint32_t* __restrict__ out) {
+    const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const uint4 c = make_uint4(ctr[4 * i], ctr[4 * i + 1], ctr[4 * i + 2], ctr[4 * i + 3]);
+    const uint2 k = make_uint2(key[2 * i], key[2 * i + 1]);
+    const uint4 o = philox4x32_10(c, k);
+    out[4 * i] = o.x;
+    out[4 * i + 1] = o.y;
+    out[4 * i + 2] = o.z;
+    out[4 * i + 3] = o.w;
+}
+
+}  // namespace fsd
+
+extern "C" {
+
+fs_status fs_philox4x32_10(const uint32_t* ctr, const uint32_t* key, int64_t n, uint32_t* out, void* stream) {
+    if (n < 0) return FS_ERR_INVALID_ARG;
+    if (n == 0) return FS_OK;
+    if (!ctr || !key || !out) return FS_ERR_INVALID_ARG;
+    const int64_t threads = 256;
+    const int64_t blocks = (n + threads - 1) / threads;
+    if (blocks > 0x7fffffffLL) return FS_ERR_UNSUPPORTED;
+    fsd::philox_kernel<<<unsigned(blocks), unsigned(threads), 0, static_cast<cudaStream_t>(stream)>>>(ctr, key, n,
+                                                                                                      out);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fsd::cuda_fail(e);
+    return FS_OK;
+}
+
+const char* fs_status_string(int32_t status) {
+    switch (status) {
+        case FS_OK: return "FS_OK";
+        case FS_ERR_INVALID_ARG: return "FS_ERR_INVALID_ARG: a required pointer is NULL or a size/enum is out of range";
+        case FS_ERR_UNSUPPORTED: return "FS_ERR_UNSUPPORTED: vocab or launch size beyond what this build supports";
+        case FS_ERR_CUDA: return "FS_ERR_CUDA: a CUDA call failed (see fs_last_error_string)";
+        default: return "unknown fs_status";
+    }
+}
+
+const char* fs_last_error_string(void) { return fsd::g_last_error; }
+
+int32_t fs_max_vocab(void) { return FS_MAX_VOCAB; }
+
+}  // extern "C"

@@ -1,0 +1,86 @@
+"""The C-ABI library: it builds, loads without a GPU, exports every symbol the
+header declares, and rejects bad host arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from tests.helpers import ROOT, ensure_built
+
+HEADER = os.path.join(ROOT, "include", "fs_sampling.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fs_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def so():
+    path = ensure_built()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for n in ["fs_sampling_from_probs", "fs_top_k_sampling", "fs_top_p_sampling", "fs_min_p_sampling",
+              "fs_top_k_top_p_sampling", "fs_top_k_renorm_probs", "fs_top_p_renorm_probs",
+              "fs_top_k_mask_logits", "fs_philox4x32_10", "fs_status_string"]:
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(so):
+    for name in _declared_functions():
+        assert hasattr(so, name), name
+
+
+def test_status_strings_and_limits(so):
+    so.fs_status_string.restype = ctypes.c_char_p
+    so.fs_max_vocab.restype = ctypes.c_int32
+    assert so.fs_status_string(0) == b"FS_OK"
+    assert b"INVALID" in so.fs_status_string(1)
+    assert so.fs_max_vocab() == 2097152
+
+
+P = ctypes.c_void_p
+FAKE = P(0x1000)   # never dereferenced: every call below is rejected on the host
+
+
+def _sample(so, probs=FAKE, b_in=4, V=16, idx=None, b_out=4, k=FAKE, p=FAKE, mp=None, order=0,
+            tok=FAKE, valid=FAKE):
+    f = so.fs_top_k_top_p_sampling
+    f.argtypes = [P, ctypes.c_int32, ctypes.c_int32, P, ctypes.c_int32, P, P, P, ctypes.c_int32,
+                  ctypes.c_uint64, ctypes.c_uint64, P, P, P, P]
+    return f(probs, b_in, V, idx, b_out, k, p, mp, order, 1, 2, tok, valid, None, None)
+
+
+def test_host_argument_checks(so):
+    assert _sample(so, probs=None) == 1
+    assert _sample(so, tok=None) == 1
+    assert _sample(so, valid=None) == 1
+    assert _sample(so, V=0) == 1
+    assert _sample(so, V=2097153) == 2
+    assert _sample(so, b_out=5) == 1            # no indices: batch_out must equal batch_in
+    assert _sample(so, order=7) == 1
+    assert _sample(so, k=None) == 1
+    assert _sample(so, b_out=-1) == 1
+    assert _sample(so, b_out=0, probs=None) == 0   # empty batch: nothing to do
+    f = so.fs_top_k_renorm_probs
+    f.argtypes = [P, ctypes.c_int32, ctypes.c_int32, P, P, P, P]
+    assert f(None, 2, 8, FAKE, FAKE, None, None) == 1
+    assert f(FAKE, 2, 8, None, FAKE, None, None) == 1
+    assert f(FAKE, 0, 8, FAKE, FAKE, None, None) == 0
+    g = so.fs_philox4x32_10
+    g.argtypes = [P, P, ctypes.c_int64, P, P]
+    assert g(None, FAKE, 4, FAKE, None) == 1
+    assert g(FAKE, FAKE, 0, FAKE, None) == 0
+
+
+def test_binding_imports_without_gpu():
+    ensure_built()
+    import min_sampling_gb300 as ms
+    assert ms.MAX_VOCAB == 2097152
+    with pytest.raises(ValueError):
+        ms._order("sideways")
