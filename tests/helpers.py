@@ -15,7 +15,8 @@ import numpy as np
 from oracle import filters
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-GUARD = 1e-5   # distance of decisive top-p prefix masses from the target
+GUARD = 1e-5        # distance of decisive top-p prefix masses from the target
+GUARD_DEEP = 2e-6   # used where the boundary token itself is lighter than 2 * GUARD
 
 
 def ensure_built() -> str:
@@ -25,12 +26,14 @@ def ensure_built() -> str:
     return lib
 
 
-def guard_accept(param_sets):
+def guard_accept(param_sets, delta: float = GUARD):
     """Accept callback for workloads: every (k, p, minp, order) use of row i must keep
-    its top-p boundary at least GUARD away from the target."""
+    its top-p boundary at least `delta` away from the target.  A use may carry its own
+    delta as a fifth element."""
     def accept(i, row):
         for ps in param_sets(i):
-            if filters.topp_boundary_margin(row, *ps) < GUARD:
+            d = ps[4] if len(ps) > 4 else delta
+            if filters.topp_boundary_margin(row, *ps[:4]) < d:
                 return False
         return True
     return accept

@@ -6,7 +6,7 @@ import pytest
 
 import workloads
 from oracle import filters
-from tests.helpers import GUARD, ensure_built, guard_accept
+from tests.helpers import GUARD_DEEP, ensure_built, guard_accept
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-6
@@ -153,7 +153,9 @@ def test_mask_special_values(ms):
 
 def test_config3_full_size(ms):
     """B=64, V=151936, z ~ N(0, 3^2): top-k 50, top-p 0.9 and the logit mask."""
-    acc = guard_accept(lambda i: [(None, 0.9, None, "joint"), (50, 0.9, None, "top_k_first"),
+    # Plain top-p 0.9 cuts at a token of mass ~1.3e-5 here, so no row can keep both
+    # neighbouring prefix masses 1e-5 from the target; that use gets the deep guard.
+    acc = guard_accept(lambda i: [(None, 0.9, None, "joint", GUARD_DEEP), (50, 0.9, None, "top_k_first"),
                                   (50, 0.9, None, "joint")])
     w = workloads.config3(accept=acc)
     out, valid = _run(ms, "top_k", w.probs, [50] * 64)
