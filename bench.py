@@ -1,0 +1,410 @@
+#!/usr/bin/env python
+"""Benchmark of the sorting-free sampling library on the pages' headline workload.
+
+Workload (one "step"): one call of fs_top_k_top_p_sampling in top-k-first order on a
+[64, 151936] float32 probability matrix, p = softmax(z), z ~ N(0, 3^2), top_k = 50,
+top_p = 0.9 (the Qwen-vocabulary batch of the F4 drill page).  Metric: rows/s and
+us/call, plus achieved HBM GB/s against the measured peak.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Every launch is timed with CUDA events on the stream it runs on; inputs rotate over
+enough copies to exceed three times the L2 cache, so each call reads HBM.  The other
+hot-path entries (joint sampler, renormalisers, logit mask, plain sampling) are
+timed the same way and reported under "entries".  "e2e" repeats the headline step
+through the C ABI with pinned host buffers (host->device copy of the probabilities
+and parameters, the call, device->host copy of tokens and flags) inside the timed
+region.  "cpu_baseline" times the CPU oracle (sort-based sampler) on a bounded
+sample of the same rows.  Under torchrun each rank runs the full workload on its own
+GPU (rows are independent: weak scaling, no collective on the data path); the
+timed region is bracketed by barriers and the slowest rank's time is used.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+B, V, K_TOP, P_TOP = 64, 151936, 50, 0.9
+WORKLOAD = ("top-k-first top-k+top-p sampling, B=64, V=151936 fp32 probs = softmax(z), "
+            "z~N(0,3^2), top_k=50, top_p=0.9")
+METRIC = "rows/s (top-k+top-p sample, B=64, V=151936)"
+FALLBACK_HBM_GBS = 6800.0
+SOURCES = ["fs_device.cuh", "sampling.cu", "renorm.cu", "api.cu", "fs_host.h"]
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-entries", action="store_true", help="time only the headline step")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-oracle sample")
+    return ap.parse_args()
+
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    for name in SOURCES:
+        with open(os.path.join(ROOT, "min_sampling_gb300", "csrc", name), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        e = d.get(kernel)
+        if e and e.get("source_hash") == source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class Clocks:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import min_sampling_gb300 as ms
+    import workloads
+
+    rank, world, local = dist_info()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    lib = ms.lib
+
+    w = workloads.config3(seed=workloads.cfg_seed(3) + rank, with_logits=True)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    per_copy = w.probs.nbytes
+    ncopy = max(4, math.ceil(3 * l2 / per_copy))
+    base = torch.from_numpy(w.probs).to(dev)
+    probs = [base.clone() for _ in range(ncopy)]
+    logits = [torch.from_numpy(w.logits).to(dev) for _ in range(min(ncopy, 4))]
+    logits += [logits[i % len(logits)].clone() for i in range(ncopy - len(logits))]
+    top_k = torch.full((B,), K_TOP, dtype=torch.int32, device=dev)
+    top_p = torch.full((B,), P_TOP, dtype=torch.float32, device=dev)
+    tok = torch.empty(B, dtype=torch.int32, device=dev)
+    valid = torch.empty(B, dtype=torch.uint8, device=dev)
+    rnd = torch.empty(B, dtype=torch.int32, device=dev)
+    outf = torch.empty((B, V), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sptr = ctypes.c_void_p(stream.cuda_stream)
+    P = ctypes.c_void_p
+    k_ptr, p_ptr = P(top_k.data_ptr()), P(top_p.data_ptr())
+    t_ptr, v_ptr, r_ptr, o_ptr = P(tok.data_ptr()), P(valid.data_ptr()), P(rnd.data_ptr()), P(outf.data_ptr())
+    pp = [P(x.data_ptr()) for x in probs]
+    lp = [P(x.data_ptr()) for x in logits]
+    seed = 20261202 + rank
+
+    def check(st):
+        if st != 0:
+            raise RuntimeError(lib.fs_status_string(st).decode() + " " + lib.fs_last_error_string().decode())
+
+    calls = {
+        "top_k_first": lambda i: check(lib.fs_top_k_top_p_sampling(pp[i % ncopy], B, V, None, B, k_ptr, p_ptr, None, 0,
+                                                                   seed, i, t_ptr, v_ptr, None, sptr)),
+        "joint": lambda i: check(lib.fs_top_k_top_p_sampling(pp[i % ncopy], B, V, None, B, k_ptr, p_ptr, None, 1,
+                                                             seed, i, t_ptr, v_ptr, None, sptr)),
+        "from_probs": lambda i: check(lib.fs_sampling_from_probs(pp[i % ncopy], B, V, None, B, seed, i, t_ptr, v_ptr,
+                                                                 None, sptr)),
+        "top_k_renorm": lambda i: check(lib.fs_top_k_renorm_probs(pp[i % ncopy], B, V, k_ptr, o_ptr, v_ptr, sptr)),
+        "top_p_renorm": lambda i: check(lib.fs_top_p_renorm_probs(pp[i % ncopy], B, V, p_ptr, o_ptr, v_ptr, sptr)),
+        "mask_logits": lambda i: check(lib.fs_top_k_mask_logits(lp[i % ncopy], B, V, k_ptr, o_ptr, v_ptr, sptr)),
+    }
+    read_bytes = B * V * 4
+    alg_bytes = {   # algorithmic bytes per launch
+        "top_k_first": read_bytes + B * (4 + 1 + 4 + 4),
+        "joint": read_bytes + B * (4 + 1 + 4 + 4),
+        "from_probs": read_bytes + B * (4 + 1),
+        "top_k_renorm": 2 * read_bytes + B * (4 + 1),
+        "top_p_renorm": 2 * read_bytes + B * (4 + 1),
+        "mask_logits": 2 * read_bytes + B * (4 + 1),
+    }
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    def timed(fn, steps, warmup, clocks=False):
+        for i in range(warmup):
+            fn(i)
+        barrier()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ctx = Clocks(local) if clocks else None
+        if ctx:
+            ctx.__enter__()
+        start.record(stream)
+        for i in range(steps):
+            ev[i][0].record(stream)
+            fn(warmup + i)
+            ev[i][1].record(stream)
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+        if ctx:
+            ctx.__exit__(None, None, None)
+        total_ms = start.elapsed_time(end)
+        per = [a.elapsed_time(b) for a, b in ev]
+        if world > 1:
+            import torch.distributed as dist
+            t = torch.tensor([total_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            total_ms = float(t.item())
+        return total_ms, per, (ctx.summary() if ctx else None)
+
+    K, W = args.steps, args.warmup
+    total_ms, per, clk = timed(calls["top_k_first"], K, W, clocks=True)
+    kern_ms = statistics.mean(per)
+    value = world * B * K / (total_ms / 1e3)
+    ms_step = total_ms / K
+
+    entries = {}
+    if not args.no_entries:
+        for name in ["joint", "from_probs", "top_k_renorm", "top_p_renorm", "mask_logits"]:
+            _, pe, _ = timed(calls[name], min(K, 100), 5)
+            us = statistics.mean(pe) * 1e3
+            entries[name] = {"us_per_call": round(us, 3), "p50_us": round(statistics.median(pe) * 1e3, 3),
+                             "p99_us": round(sorted(pe)[min(len(pe) - 1, int(0.99 * len(pe)))] * 1e3, 3),
+                             "gbps": round(alg_bytes[name] / (us * 1e-6) / 1e9, 1),
+                             "alg_bytes_per_call": alg_bytes[name]}
+    # Round counts of the headline step (one call) for the record.
+    check(lib.fs_top_k_top_p_sampling(pp[0], B, V, None, B, k_ptr, p_ptr, None, 0, seed, 12345, t_ptr, v_ptr, r_ptr,
+                                      sptr))
+    torch.cuda.synchronize(dev)
+    rounds = np.bincount(rnd.cpu().numpy()).tolist()
+
+    # End to end through the C ABI with host buffers.
+    host_p = torch.from_numpy(w.probs).pin_memory()
+    host_k = top_k.cpu().pin_memory()
+    host_pp = top_p.cpu().pin_memory()
+    host_tok = torch.empty(B, dtype=torch.int32).pin_memory()
+    host_val = torch.empty(B, dtype=torch.uint8).pin_memory()
+
+    def e2e(i):
+        dst = probs[i % ncopy]
+        dst.copy_(host_p, non_blocking=True)
+        top_k.copy_(host_k, non_blocking=True)
+        top_p.copy_(host_pp, non_blocking=True)
+        calls["top_k_first"](i)
+        host_tok.copy_(tok, non_blocking=True)
+        host_val.copy_(valid, non_blocking=True)
+
+    ke = max(10, min(K, 100))
+    e2e_ms, _, _ = timed(e2e, ke, 3)
+    h2d = host_p.numel() * 4 + host_k.numel() * 4 + host_pp.numel() * 4
+    d2h = host_tok.numel() * 4 + host_val.numel()
+    e2e_value = world * B * ke / (e2e_ms / 1e3)
+
+    peak, peak_kind = measured_peak()
+    achieved = alg_bytes["top_k_first"] / (kern_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "rows/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": round(ms_step, 5), "us_per_call": round(kern_ms * 1e3, 3),
+        "p50_us": round(statistics.median(per) * 1e3, 3),
+        "p99_us": round(sorted(per)[min(len(per) - 1, int(0.99 * len(per)))] * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "batch": B, "vocab": V, "top_k": K_TOP, "top_p": P_TOP,
+                   "entry": "fs_top_k_top_p_sampling(order=top_k_first)",
+                   "l2": f"inputs rotate over {ncopy} copies ({ncopy * per_copy / 1e6:.0f} MB > 3x L2 "
+                         f"{l2 / 1e6:.0f} MB)", "parallelism": f"rows independent, {world} GPU(s)"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                     "alg_bytes_per_launch": alg_bytes["top_k_first"],
+                     "traffic": recorded_traffic("sample_kernel")},
+        "e2e": {"value": round(e2e_value, 1), "unit": "rows/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / ke, 5)},
+        "gpu_launches": K,
+        "clocks": clk,
+        "rounds_histogram": rounds,
+        "entries": entries,
+    }
+    if rank == 0 and world == 1:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(w, budget_s: float):
+    """The CPU oracle (sort-based sampler) as it stands, on whole rows of the same
+    matrix, until `budget_s` of CPU time has been spent."""
+    import numpy as np
+
+    from oracle import baseline
+
+    rng = np.random.default_rng(0)
+    t0 = time.perf_counter()
+    rows = 0
+    while time.perf_counter() - t0 < budget_s and rows < 4 * B:
+        r = rows % B
+        baseline.sample_rows(w.probs[r:r + 1], w.top_k[r:r + 1], w.top_p[r:r + 1], None, "top_k_first", rng=rng)
+        rows += 1
+    dt = time.perf_counter() - t0
+    return {"value": round(rows / dt, 3), "unit": "rows/s", "cores": 1, "kind": "oracle",
+            "sample": f"{rows} rows of the same B=64 x V=151936 matrix, one sorted-row draw each, "
+                      f"numpy single-threaded, {dt:.1f} s"}
+
+
+# ---------------------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    """The CPU oracle as the reference arm: each step samples a bounded slice of the
+    workload's rows with the sort-based sampler."""
+    import numpy as np
+
+    import workloads
+    from oracle import baseline
+
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return
+    w = workloads.config3(with_logits=False)
+    rows_per_step = 2
+    rng = np.random.default_rng(1)
+
+    def step(i):
+        r = (i * rows_per_step) % B
+        baseline.sample_rows(w.probs[r:r + rows_per_step], w.top_k[r:r + rows_per_step],
+                             w.top_p[r:r + rows_per_step], None, "top_k_first", rng=rng)
+
+    for i in range(args.warmup):
+        step(i)
+    steps = max(1, min(args.steps, 40))
+    t0 = time.perf_counter()
+    for i in range(steps):
+        step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    value = rows_per_step * steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "rows/s", "n_gpus": world,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": round(dt / steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "batch": B, "vocab": V, "top_k": K_TOP, "top_p": P_TOP,
+                   "sample": f"{rows_per_step} rows per step"},
+        "cpu_baseline": {"value": round(value, 3), "unit": "rows/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{rows_per_step} of 64 rows per step, {steps} steps"},
+        "e2e": {"value": round(value, 3), "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

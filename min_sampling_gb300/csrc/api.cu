@@ -1,8 +1,10 @@
 // Status strings, launch planning and the Philox entry point.
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <mutex>
 #include <set>
+#include <tuple>
 #include <utility>
 
 #include "fs_host.h"
@@ -40,25 +42,7 @@ fs_status device_limits(int& sm_count, size_t& smem_optin) {
     return FS_OK;
 }
 
-fs_status make_plan(int rows, int vocab, Plan& p) {
-    int sms = 0;
-    size_t optin = 0;
-    fs_status st = device_limits(sms, optin);
-    if (st != FS_OK) return st;
-    p.ns = (vocab + SEG - 1) / SEG;
-    long long want = (2LL * sms + rows - 1) / rows;
-    int C = int(want < 1 ? 1 : (want > MAX_CLUSTER ? MAX_CLUSTER : want));
-    if (C > p.ns) C = p.ns;
-    if (p.ns < 8) C = 1;
-    if (C < 1) C = 1;
-    p.C = C;
-    p.nsc = (p.ns + C - 1) / C;
-    p.smem = Layout(p.nsc, p.ns).total;
-    if (p.smem > optin) return FS_ERR_UNSUPPORTED;
-    return FS_OK;
-}
-
-fs_status prepare_kernel(const void* fn, size_t smem) {
+fs_status prepare_kernel(const void* fn) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -70,11 +54,67 @@ fs_status prepare_kernel(const void* fn, size_t smem) {
     int sms = 0;
     fs_status st = device_limits(sms, optin);
     if (st != FS_OK) return st;
-    // Opt in to the device maximum once, so every later launch fits.
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(optin));
     if (e != cudaSuccess) return cuda_fail(e);
-    (void)smem;
     done.insert({fn, dev});
+    return FS_OK;
+}
+
+// Resident CTAs per SM for `fn` with `smem` bytes of dynamic shared memory (cached).
+static fs_status occupancy(const void* fn, size_t smem, int& occ) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    static std::mutex mu;
+    static std::map<std::tuple<const void*, int, size_t>, int> cache;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cache.find({fn, dev, smem});
+        if (it != cache.end()) {
+            occ = it->second;
+            return FS_OK;
+        }
+    }
+    int v = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, fn, NT, smem);
+    if (e != cudaSuccess) return cuda_fail(e);
+    std::lock_guard<std::mutex> lock(mu);
+    cache[{fn, dev, smem}] = v;
+    occ = v;
+    return FS_OK;
+}
+
+fs_status make_plan(int rows, int vocab, const void* fn, Plan& p) {
+    int sms = 0;
+    size_t optin = 0;
+    fs_status st = device_limits(sms, optin);
+    if (st != FS_OK) return st;
+    st = prepare_kernel(fn);
+    if (st != FS_OK) return st;
+    p.shift = seg_shift_for(vocab);
+    p.ns = (vocab + (BLK << p.shift) - 1) / (BLK << p.shift);
+    // Largest C (<= MAX_CLUSTER, >= 4 segments per CTA) whose grid fits in one wave.
+    int cmax = p.ns / 4;
+    if (cmax > MAX_CLUSTER) cmax = MAX_CLUSTER;
+    if (cmax < 1) cmax = 1;
+    int chosen = 1;
+    for (int C = cmax; C >= 1; --C) {
+        const int nsc = (p.ns + C - 1) / C;
+        const size_t smem = Layout(nsc).total;
+        if (smem > optin) continue;
+        int occ = 0;
+        st = occupancy(fn, smem, occ);
+        if (st != FS_OK) return st;
+        if (occ < 1) continue;
+        if (C == 1 || (long long)rows * C <= (long long)sms * occ) {
+            chosen = C;
+            break;
+        }
+    }
+    p.C = chosen;
+    p.nsc = (p.ns + chosen - 1) / chosen;
+    p.smem = Layout(p.nsc).total;
+    if (p.smem > optin) return FS_ERR_UNSUPPORTED;
     return FS_OK;
 }
 

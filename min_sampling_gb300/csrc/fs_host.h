@@ -9,12 +9,13 @@
 
 namespace fsd {
 
-// Cluster size, segments per CTA and shared-memory bytes of one launch.
+// Cluster size, segment geometry and shared-memory bytes of one launch.
 struct Plan {
-    int C;
-    int nsc;
-    int ns;
-    size_t smem;
+    int C;        // CTAs per row (cluster size)
+    int shift;    // log2(blocks per segment)
+    int ns;       // segments per row
+    int nsc;      // segments per CTA
+    size_t smem;  // dynamic shared memory per CTA
 };
 
 // Remember a CUDA error for fs_last_error_string() and turn it into a status.
@@ -23,17 +24,16 @@ fs_status cuda_fail(cudaError_t e);
 // Number of SMs and the opt-in shared-memory limit of the current device.
 fs_status device_limits(int& sm_count, size_t& smem_optin);
 
-// Choose the cluster size for `rows` rows of `vocab` elements: enough CTAs to give
-// every SM about two, at most MAX_CLUSTER per row and at least one segment each.
-fs_status make_plan(int rows, int vocab, Plan& p);
+// Choose the cluster size for `rows` rows of `vocab` elements so that the whole grid
+// is resident at once (rows * C <= SMs * CTAs-per-SM of `fn`), with at most
+// MAX_CLUSTER CTAs per row and at least four segments per CTA.
+fs_status make_plan(int rows, int vocab, const void* fn, Plan& p);
 
-// Opt the kernel into `smem` bytes of dynamic shared memory (once per device).
-fs_status prepare_kernel(const void* fn, size_t smem);
+// Opt the kernel into the device's maximum dynamic shared memory (once per device).
+fs_status prepare_kernel(const void* fn);
 
 template <typename Args>
 fs_status launch_cluster(void (*kernel)(Args), const Plan& p, int rows, void* stream, const Args& a) {
-    fs_status st = prepare_kernel(reinterpret_cast<const void*>(kernel), p.smem);
-    if (st != FS_OK) return st;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(rows) * unsigned(p.C), 1, 1);
     cfg.blockDim = dim3(NT, 1, 1);

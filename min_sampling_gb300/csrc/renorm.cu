@@ -5,9 +5,10 @@
 // ([drill] sections 2-4: the largest t with count(key >= t) >= k, or with
 // mass(key >= t) >= top_p * M), then writes the row once.  One cluster per row:
 //   pass 1   one HBM read: per-segment maximum key, the row total and a bad flag;
-//   search   top-k: candidates = every element at or above the k-th largest segment
-//            maximum (a lower bound of t), gathered into rank 0, where t is exact by
-//            counting; a bisection on the key takes over if they do not fit.
+//   search   top-k: every CTA bounds t from below by the k-th largest of its own
+//            segment maxima and keeps its elements at or above that bound; rank 0
+//            gathers the survivors of the best bound and counts t exactly among them;
+//            a bisection on the key takes over when they do not fit on chip.
 //            top-p: bisection on the key with three pivots per pass, each interval
 //            shrunk to the keys that exist in it;
 //   write    keep key >= t (x / kept mass, or the logit), else 0 / -inf.  Segments
@@ -28,202 +29,121 @@ struct FilterArgs {
     const int* top_k;
     const float* top_p;
     unsigned char* out_valid;
-    int nsc;
+    int shift;
     int ns;
+    int nsc;
 };
-
-struct KeyP {
-    __device__ __forceinline__ uint32_t operator()(float x) const { return prob_key(x); }
-};
-struct KeyL {
-    __device__ __forceinline__ uint32_t operator()(float x) const { return logit_key(x); }
-};
-
-// Mass (probabilities) and count of key >= t over this CTA's segments, cluster-wide.
-template <bool VEC, typename KEYF>
-__device__ void mass_count_ge(const float* __restrict__ row, int V, int s0, int nsc, const uint32_t* segkey,
-                              uint32_t t, KEYF keyf, const Smem& sm, int& buf, int C, int warp, int lane,
-                              int tid, float& mass, int& cnt) {
-    float wm = 0.f;
-    int wc = 0;
-    for (int ls = warp; ls < nsc; ls += NW) {
-        if (segkey[ls] < t) continue;
-        float v[SEG_IT][4];
-        load_segment<VEC, false>(row, V, s0 + ls, lane, 0.f, v);
-        float m = 0.f;
-        int c = 0;
-        const int base0 = (s0 + ls) * SEG + lane * 4;
-#pragma unroll
-        for (int it = 0; it < SEG_IT; ++it)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const bool g = keyf(v[it][q]) >= t && base0 + it * 128 + q < V;
-                m += g ? v[it][q] : 0.f;
-                c += g;
-            }
-        wm += warp_sum(m);
-        wc += warp_sum_i(c);
-    }
-    if (lane == 0) {
-        sm.redf[warp] = wm;
-        sm.redi[warp] = wc;
-    }
-    __syncthreads();
-    if (tid == 0) {
-        float s = 0.f;
-        int n = 0;
-        for (int w = 0; w < NW; ++w) { s += sm.redf[w]; n += sm.redi[w]; }
-        sm.slot[buf].f[0] = s;
-        sm.slot[buf].u[0] = uint32_t(n);
-    }
-    exchange(sm, buf, C, warp, lane);
-    buf ^= 1;
-    mass = 0.f;
-    cnt = 0;
-    for (int c = 0; c < C; ++c) {
-        mass += sm.gath[c].f[0];
-        cnt += int(sm.gath[c].u[0]);
-    }
-    __syncthreads();
-}
 
 template <bool VEC, int KIND>
-__global__ void __launch_bounds__(NT, 1) filter_kernel(const FilterArgs a) {
-    using KEYF = typename std::conditional<KIND == K_MASK, KeyL, KeyP>::type;
+__global__ void __launch_bounds__(NT, 4) filter_kernel(const FilterArgs a) {
+    using KEYF = typename std::conditional<KIND == K_MASK, KeyLogit, KeyProb>::type;
+    constexpr bool IS_PROB = KIND != K_MASK;
     const KEYF keyf;
     const int C = int(cluster_nctarank());
     const int rank = int(cluster_ctarank());
     const int b = int(cluster_id_x());
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const Layout L(a.nsc, a.ns);
+    const Layout L(a.nsc);
     const Smem sm(L);
-    const int V = a.V, NS = a.ns;
-    const int s0 = rank * a.nsc;
-    const int nsc = max(0, min(a.nsc, NS - s0));
+    const Geom g(a.V, a.shift, a.ns, a.nsc, rank);
+    const int V = a.V;
     const float* row = a.in + size_t(b) * size_t(V);
     float* orow = a.out + size_t(b) * size_t(V);
-    const bool is_prob = KIND != K_MASK;
+    const float fill = IS_PROB ? 0.f : __int_as_float(0xff800000);
+    const int k = (KIND != K_TOPP) ? a.top_k[b] : 0;
+    const float tp = (KIND == K_TOPP) ? a.top_p[b] : 1.f;
+    const bool k_on = KIND != K_TOPP && k > 0 && k < V;
 
     // ---- pass 1
-    if (tid == 0) sm.misc[1] = 0;
+    int pos = 0;
+    bool bad = false;
+    pass1<VEC, false, IS_PROB>(row, g, sm.segkey, sm.mass[0], warp, lane, pos, bad);
+    const int wbad = __any_sync(FULL, bad) ? 1 : 0;
+    if (lane == 0) sm.redi[NW + warp] = wbad;
     __syncthreads();
-    for (int ls = warp; ls < nsc; ls += NW) {
-        float v[SEG_IT][4];
-        load_segment<VEC, false>(row, V, s0 + ls, lane, is_prob ? 0.f : __int_as_float(0xff800000), v);
-        uint32_t kmax = 0;
-        float s = 0.f;
-        bool bad = false;
-        const int base0 = (s0 + ls) * SEG + lane * 4;
-#pragma unroll
-        for (int it = 0; it < SEG_IT; ++it)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float x = v[it][q];
-                const bool inr = base0 + it * 128 + q < V;
-                if (is_prob) {
-                    bad |= !(x >= 0.f);
-                    s += x;
-                } else {
-                    bad |= isnan(x);
-                }
-                kmax = max(kmax, inr ? keyf(x) : 0u);
-            }
-        kmax = warp_max_u(kmax);
-        if (is_prob) s = warp_sum(s);
-        if (__any_sync(FULL, bad) && lane == 0) sm.misc[1] = 1;
-        if (lane == 0) {
-            sm.segkey[ls] = kmax;
-            sm.mass[0][ls] = s;
-        }
+
+    // Local lower bound of the top-k threshold and the local candidates.
+    uint32_t L0c = 0;
+    int nloc = -1;
+    if (k_on && g.nsc >= k) {
+        L0c = max(IS_PROB ? 1u : 0u, kth_in_array(sm.segkey, g.nsc, k, sm, warp, lane, tid));
+        nloc = compact_ge<VEC, false>(row, g, L0c, keyf, fill, sm, warp, lane, tid);
+        if (nloc > CAP) nloc = -1;
     }
-    __syncthreads();
     if (warp == 0) {
-        uint32_t km = 0;
-        for (int base = 0; base < nsc; base += 32) km = max(km, base + lane < nsc ? sm.segkey[base + lane] : 0u);
-        km = warp_max_u(km);
-        const float s = ordered_sum(sm.mass[0], nsc, lane);
+        const uint32_t km = ordered_max_u(sm.segkey, g.nsc, lane);
+        const float s = IS_PROB ? ordered_sum(sm.mass[0], g.nsc, lane) : 0.f;
         if (lane == 0) {
+            int nb = 0;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) nb |= sm.redi[NW + w];
+            sm.slot[0].f[0] = s;
             sm.slot[0].u[0] = km;
-            sm.slot[0].f[1] = s;
-            sm.slot[0].u[1] = uint32_t(sm.misc[1]);
+            sm.slot[0].u[1] = uint32_t(nb);
+            sm.slot[0].u[3] = L0c;
+            sm.slot[0].u[4] = uint32_t(nloc);
         }
     }
     int buf = 0;
-    exchange(sm, buf, C, warp, lane);
+    exchange(sm, buf, C, tid, 13);
     buf ^= 1;
-    uint32_t maxkey = 0;
+    uint32_t maxkey = 0, L0 = 0;
     float M = 0.f;
-    bool bad = false;
+    bool any_bad = false, lists_ok = true;
+    int ncand = 0;
     for (int c = 0; c < C; ++c) {
-        maxkey = max(maxkey, sm.gath[c].u[0]);
-        M += sm.gath[c].f[1];
-        bad |= sm.gath[c].u[1] != 0;
+        const Slot& s = sm.gath[c];
+        M += s.f[0];
+        maxkey = max(maxkey, s.u[0]);
+        any_bad |= s.u[1] != 0;
+        L0 = max(L0, s.u[3]);
+        const int n = int(s.u[4]);
+        lists_ok = lists_ok && n >= 0;
+        ncand += max(n, 0);
     }
+    lists_ok = lists_ok && ncand <= CAP;
     __syncthreads();
 
-    bool valid = !bad;
-    if (is_prob) valid = valid && M > 0.f && M <= 3.402823466e38f;
-    const int k = (KIND != K_TOPP && a.top_k) ? a.top_k[b] : 0;
-    const float tp = (KIND == K_TOPP && a.top_p) ? a.top_p[b] : 1.f;
+    bool valid = !any_bad;
+    if (IS_PROB) valid = valid && M > 0.f && M <= 3.402823466e38f;
     if (KIND == K_TOPP && isnan(tp)) valid = false;
 
-    uint32_t t = 0;       // keep key >= t
-    float denom = M;      // kept mass (probabilities)
+    uint32_t t = 0;   // keep key >= t
+    float denom = M;  // kept mass (probabilities)
     if (valid) {
         if (KIND != K_TOPP) {
-            if (k > 0 && k < V) {
-                // Candidates: everything at or above the k-th largest segment maximum.
-                uint32_t L0 = is_prob ? 1u : 0u;
-                const bool pruned = k <= NS;
-                if (pruned) {
-                    gather_segkeys(sm, a.nsc, NS, tid);
-                    L0 = max(L0, kth_key_in_array(sm.segall, NS, k, sm, warp, lane, tid));
-                }
-                const int nloc = compact_ge<VEC, false>(row, V, s0, nsc, sm.segkey, L0, keyf,
-                                                        is_prob ? 0.f : __int_as_float(0xff800000), sm, warp,
-                                                        lane, tid);
-                if (tid == 0) sm.slot[buf].u[0] = uint32_t(nloc);
-                exchange(sm, buf, C, warp, lane);
-                buf ^= 1;
-                int ntot = 0;
-                for (int c = 0; c < C; ++c) ntot += int(sm.gath[c].u[0]);
-                __syncthreads();
-                if (ntot <= CAP) {
+            if (k_on) {
+                if (lists_ok) {
                     if (rank == 0) {
-                        gather_lists(sm, C, tid);
-                        uint32_t tk = kth_key_in_list(sm, ntot, k, keyf, warp, lane, tid);
+                        const int n = gather_lists(sm, C, 4, L0, keyf, warp, lane, tid);
+                        const uint32_t tk = kth_key_in_list(sm, n, k, keyf, warp, lane, tid);
                         if (warp == 0) {
                             float s = 0.f;
-                            for (int base = 0; base < ntot; base += 32) {
-                                const int i = base + lane;
-                                const bool g = i < ntot && keyf(sm.lv[i]) >= tk;
-                                s += warp_sum(g ? sm.lv[i] : 0.f);
-                            }
+                            for (int i = lane; i < n; i += 32) s += keyf(sm.lv[i]) >= tk ? sm.lv[i] : 0.f;
+                            s = warp_sum(s);
                             if (lane == 0) {
-                                sm.slot[buf].u[0] = tk;
                                 sm.slot[buf].f[0] = s;
+                                sm.slot[buf].u[0] = tk;
                             }
                         }
                     }
-                    exchange(sm, buf, C, warp, lane);
+                    exchange(sm, buf, C, tid, 9);
                     buf ^= 1;
                     t = sm.gath[0].u[0];
                     denom = sm.gath[0].f[0];
                     __syncthreads();
                 } else {
                     Bisect st;
-                    st.lo = pruned ? L0 : 0u;
+                    st.lo = L0;  // crit(L0) holds (L0 <= t_k), and crit(0) trivially
                     st.hi = uint64_t(maxkey) + 1;
                     st.cnt_lo = 0;
                     st.mass_lo = 0.f;
-                    bisect_run<VEC, false, false>(row, V, s0, nsc, sm.segkey, st, k, 0.f, keyf,
-                                                  is_prob ? 0.f : __int_as_float(0xff800000), sm, buf, C, warp,
-                                                  lane, tid);
+                    bisect_run<VEC, false, false>(row, g, &st, k, 0.f, keyf, fill, sm, &buf, C, warp, lane, tid);
                     t = uint32_t(st.lo);
-                    if (is_prob) {
+                    if (IS_PROB) {
                         int cnt;
-                        mass_count_ge<VEC>(row, V, s0, nsc, sm.segkey, t, keyf, sm, buf, C, warp, lane, tid,
-                                           denom, cnt);
+                        mass_count_ge<VEC, false>(row, g, t, keyf, nullptr, sm, &buf, C, warp, lane, tid, &denom,
+                                                  &cnt, nullptr);
                     }
                 }
             }
@@ -234,15 +154,15 @@ __global__ void __launch_bounds__(NT, 1) filter_kernel(const FilterArgs a) {
             } else if (tp <= 0.f) {
                 t = maxkey;
                 int cnt;
-                mass_count_ge<VEC>(row, V, s0, nsc, sm.segkey, t, keyf, sm, buf, C, warp, lane, tid, denom, cnt);
+                mass_count_ge<VEC, false>(row, g, t, keyf, nullptr, sm, &buf, C, warp, lane, tid, &denom, &cnt,
+                                          nullptr);
             } else {
                 Bisect st;
                 st.lo = 0;
                 st.hi = uint64_t(maxkey) + 1;
                 st.cnt_lo = 0;
                 st.mass_lo = M;
-                bisect_run<VEC, false, true>(row, V, s0, nsc, sm.segkey, st, 0, tp * M, keyf, 0.f, sm, buf, C,
-                                             warp, lane, tid);
+                bisect_run<VEC, false, true>(row, g, &st, 0, tp * M, keyf, 0.f, sm, &buf, C, warp, lane, tid);
                 t = uint32_t(st.lo);
                 denom = st.mass_lo;
             }
@@ -250,28 +170,15 @@ __global__ void __launch_bounds__(NT, 1) filter_kernel(const FilterArgs a) {
     }
 
     // ---- write this CTA's share of the row
-    const float fill = is_prob ? 0.f : __int_as_float(0xff800000);
     const bool vec_out = VEC && ((reinterpret_cast<uintptr_t>(orow) & 15) == 0);
-    for (int ls = warp; ls < nsc; ls += NW) {
-        const int s = s0 + ls;
-        const bool any_kept = valid && sm.segkey[ls] >= t;
-        float v[SEG_IT][4];
-        if (any_kept) {
-            load_segment<VEC, false>(row, V, s, lane, 0.f, v);
-        }
-#pragma unroll
-        for (int it = 0; it < SEG_IT; ++it) {
-            const int base = s * SEG + it * 128 + lane * 4;
+    visit<TRIP, VEC, false>(
+        row, g, fill, warp, lane, [&](int ls) { return valid && sm.segkey[ls] >= t; },
+        [&](int, int, int base, float4 x, bool on) {
             float o[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                if (!any_kept) {
-                    o[q] = fill;
-                } else {
-                    const float x = v[it][q];
-                    const bool keep = keyf(x) >= t;
-                    o[q] = keep ? (is_prob ? x / denom : x) : fill;
-                }
+                const float xv = q_at(x, q);
+                o[q] = (on && keyf(xv) >= t) ? (IS_PROB ? xv / denom : xv) : fill;
             }
             if (vec_out && base + 3 < V) {
                 *reinterpret_cast<float4*>(orow + base) = make_float4(o[0], o[1], o[2], o[3]);
@@ -280,10 +187,10 @@ __global__ void __launch_bounds__(NT, 1) filter_kernel(const FilterArgs a) {
                 for (int q = 0; q < 4; ++q)
                     if (base + q < V) orow[base + q] = o[q];
             }
-        }
-    }
+        },
+        [](int, bool) {});
     if (rank == 0 && tid == 0 && a.out_valid) a.out_valid[b] = valid ? 1 : 0;
-    cluster_sync();   // no CTA leaves while a peer may read its shared memory
+    cluster_sync();  // no CTA leaves while a peer may read its shared memory
 }
 
 template <int KIND>
@@ -295,8 +202,11 @@ static fs_status launch_filter(const float* in, int32_t batch, int32_t vocab, co
     if (KIND == K_TOPP ? !top_p : !top_k) return FS_ERR_INVALID_ARG;
     if (vocab < 1) return FS_ERR_INVALID_ARG;
     if (vocab > FS_MAX_VOCAB) return FS_ERR_UNSUPPORTED;
+    const bool vec = (vocab % 4 == 0) && ((reinterpret_cast<uintptr_t>(in) & 15) == 0);
+    const void* fn = vec ? reinterpret_cast<const void*>(filter_kernel<true, KIND>)
+                         : reinterpret_cast<const void*>(filter_kernel<false, KIND>);
     Plan p;
-    fs_status st = make_plan(batch, vocab, p);
+    fs_status st = make_plan(batch, vocab, fn, p);
     if (st != FS_OK) return st;
     FilterArgs a;
     a.in = in;
@@ -305,9 +215,9 @@ static fs_status launch_filter(const float* in, int32_t batch, int32_t vocab, co
     a.top_k = top_k;
     a.top_p = top_p;
     a.out_valid = out_valid;
-    a.nsc = p.nsc;
+    a.shift = p.shift;
     a.ns = p.ns;
-    const bool vec = (vocab % 4 == 0) && ((reinterpret_cast<uintptr_t>(in) & 15) == 0);
+    a.nsc = p.nsc;
     if (vec) return launch_cluster(filter_kernel<true, KIND>, p, batch, stream, a);
     return launch_cluster(filter_kernel<false, KIND>, p, batch, stream, a);
 }

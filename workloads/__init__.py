@@ -42,31 +42,42 @@ def softmax_fp32(z: np.ndarray) -> np.ndarray:
     return (e / e.sum()).astype(np.float32)
 
 
+def _order_key(x: np.ndarray) -> np.ndarray:
+    """Monotone map of float32 values to int64 keys (sign-aware bit pattern)."""
+    u = x.view(np.uint32).astype(np.int64)
+    neg = u >= 0x80000000
+    return np.where(neg, 0xFFFFFFFF - u, u + 0x80000000)
+
+
+def _from_order_key(k: np.ndarray) -> np.ndarray:
+    u = np.where(k >= 0x80000000, k - 0x80000000, 0xFFFFFFFF - k).astype(np.uint32)
+    return u.view(np.float32)
+
+
 def detie(x: np.ndarray, positive_only: bool = True) -> tuple[np.ndarray, int]:
     """Make the float32 values of ``x`` pairwise distinct.
 
-    Values are visited in ascending order; any value not strictly above its
-    predecessor is raised to the next float32 above the predecessor.  With
-    ``positive_only`` the zeros (and negatives) are left alone, since they can
-    never be sampled.  Returns the new array and the number of raised entries.
+    Values are visited in ascending order and each one is raised, if needed, to the
+    next representable float32 above its (already raised) predecessor:
+    key'[i] = max(key[i], key'[i-1] + 1), computed in closed form as
+    i + running-max(key[j] - j).  With ``positive_only`` zeros and negatives are left
+    alone (they are never sampled).  Returns the new array and the number of raised
+    entries.
     """
     x = np.array(x, dtype=np.float32, copy=True)
     order = np.argsort(x, kind="stable")
     s = x[order]
     start = int(np.searchsorted(s, np.float32(0.0), side="right")) if positive_only else 0
-    bumps = 0
-    while True:
-        body = s[start:]
-        if body.size < 2:
-            break
-        dup = np.nonzero(body[1:] <= body[:-1])[0] + 1 + start
-        if dup.size == 0:
-            break
-        # Fix the first member of every run; later members are fixed by the next sweep.
-        first = dup[np.concatenate(([True], np.diff(dup) > 1))]
-        s[first] = np.nextafter(s[first - 1], np.float32(np.inf))
-        bumps += int(first.size)
-    x[order] = s
+    body = s[start:]
+    if body.size < 2:
+        return x, 0
+    key = _order_key(body)
+    idx = np.arange(key.size, dtype=np.int64)
+    new = np.maximum.accumulate(key - idx) + idx
+    bumps = int(np.count_nonzero(new != key))
+    if bumps:
+        s[start:] = _from_order_key(new)
+        x[order] = s
     return x, bumps
 
 
