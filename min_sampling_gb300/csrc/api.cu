@@ -98,9 +98,8 @@ fs_status make_plan(int rows, int vocab, const void* fn, Plan& p) {
     if (cmax > MAX_CLUSTER) cmax = MAX_CLUSTER;
     if (cmax < 1) cmax = 1;
     int chosen = 1;
+    const size_t smem = Layout(p.ns).total;   // row-wide tables in every CTA
     for (int C = cmax; C >= 1; --C) {
-        const int nsc = (p.ns + C - 1) / C;
-        const size_t smem = Layout(nsc).total;
         if (smem > optin) continue;
         int occ = 0;
         st = occupancy(fn, smem, occ);
@@ -113,7 +112,7 @@ fs_status make_plan(int rows, int vocab, const void* fn, Plan& p) {
     }
     p.C = chosen;
     p.nsc = (p.ns + chosen - 1) / chosen;
-    p.smem = Layout(p.nsc).total;
+    p.smem = smem;
     if (p.smem > optin) return FS_ERR_UNSUPPORTED;
     return FS_OK;
 }

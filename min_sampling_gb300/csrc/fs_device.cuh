@@ -1,20 +1,20 @@
 // Device building blocks shared by the sampling and filter kernels (sm_103a).
 //
-// Execution model: one thread-block cluster per row.  A row is cut into segments of
-// 128 * 2^shift elements (128 = one float4 per lane of a warp); the C CTAs of a
-// cluster own contiguous ranges of segments.  Every CTA streams its range from HBM
-// exactly once (pass 1) and keeps, per segment, the maximum order key and the mass
-// above the current lower pivot in shared memory.  Later work (rejection rounds,
-// threshold searches, the filter write) visits only segments whose maximum can
-// matter, re-reading them through L2, and switches to a compact in-shared-memory
-// list of surviving tokens as soon as it is small.  Cross-CTA reductions go through
-// distributed shared memory (mapa + ld.shared::cluster) and hardware cluster
-// barriers; every CTA of a cluster executes the same sequence of cluster barriers,
-// because every branch around one depends only on cluster-wide reduced values.
+// Execution model: one thread-block cluster of C CTAs per row, rank 0 the leader.
+// A row is cut into segments of 128 * 2^shift elements (128 = one float4 per lane of
+// a warp).  Every CTA streams a contiguous share of the segments from HBM exactly
+// once (pass 1), and writes each segment's maximum order key and mass straight into
+// the leader's shared memory (distributed shared memory stores), so that after one
+// cluster barrier the leader holds the whole row's segment table.  From there the
+// leader drives the rest: it finishes alone when little data is left to touch (the
+// top-k candidates, a compact list of surviving tokens), and otherwise sends the
+// other CTAs commands (a two-pivot reduction pass, a three-pivot bisection pass, a
+// masked write) through their shared memory, each command bracketed by two cluster
+// barriers.  Every CTA executes the same sequence of cluster barriers: the peers
+// follow the leader's commands until an EXIT command.
 //
-// Code size matters as much as instruction count here: the per-row work after pass 1
-// runs once per CTA, so it executes from a cold instruction cache.  Hot loops are
-// written out explicitly; everything that runs once per phase is kept out of line.
+// Code size is kept small on purpose: the work after pass 1 runs once per CTA, from
+// a cold instruction cache, on every SM at the same moment.
 #pragma once
 
 #include <cstdint>
@@ -27,20 +27,18 @@ namespace fsd {
 constexpr int NT = 256;                 // threads per CTA
 constexpr int NW = NT / 32;             // warps per CTA
 constexpr int BLK = 128;                // elements per block (one float4 per lane)
-constexpr int TRIP = 8;                 // blocks a warp keeps in flight per trip
-constexpr int MAX_SEG_SHIFT = 2;        // at most 4 blocks per segment (V <= 2^21 needs 2)
-constexpr int NS_TARGET = 4096;         // segments per row (larger rows use longer segments)
-constexpr int CAP = 2048;               // compact-list capacity per CTA / per row
+constexpr int TB = 4;                   // blocks per trip (double-buffered in pass 1)
+constexpr int MAX_SEG_SHIFT = 2;        // at most 4 blocks per segment (V <= 2^21)
+constexpr int NS_TARGET = 4096;         // segments per row (longer rows use longer segments)
+constexpr int CAP = 2048;               // compact-list capacity (leader)
 constexpr int R_MAX = 256;              // rejection rounds before a row is invalid
 constexpr int MAX_CLUSTER = 8;
 constexpr unsigned FULL = 0xffffffffu;
 
-// ------------------------------------------------------------------ geometry
+// Commands from the leader to the other CTAs of the cluster.
+enum : int { CMD_EXIT = 0, CMD_PIVOT2 = 1, CMD_BISECT = 2, CMD_MASSGE = 3, CMD_WRITE = 4 };
 
-struct Slot {            // one cluster-exchange record (80 bytes)
-    float f[8];
-    uint32_t u[12];
-};
+// ------------------------------------------------------------------ geometry
 
 __host__ __device__ constexpr size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
@@ -51,21 +49,35 @@ __host__ __device__ inline int seg_shift_for(int V) {
     return s;
 }
 
-// Byte offsets of the dynamic shared-memory carve-up for `nsc` segments per CTA.
+// A command (written by the leader into every CTA's copy).
+struct Ctl {
+    int cmd;
+    int ia, ib;            // PIVOT2: which mass arrays receive the per-segment masses
+    int flag;              // WRITE: row valid
+    float f[4];            // pivots / denominator
+    uint32_t u[4];         // key pivots / threshold; u[3] = interval low (BISECT)
+    uint32_t hi_lo, hi_hi; // BISECT: 64-bit interval high
+};
+
+// One CTA's partial results, in the leader's shared memory (one record per rank).
+struct Part {
+    float f[4];
+    uint32_t u[12];
+};
+
+// Byte offsets of the dynamic shared-memory carve-up for `ns` segments per row.
 struct Layout {
-    size_t slot, gath, redf, redi, misc, segkey, mass0, mass1, mass2, off, lv, li, total;
-    __host__ __device__ explicit Layout(int nsc) {
+    size_t ctl, part, red, segkey, mass0, mass1, mass2, list, lv, li, total;
+    __host__ __device__ explicit Layout(int ns) {
         size_t o = 0;
-        slot = o;   o = align16(o + 2 * sizeof(Slot));
-        gath = o;   o = align16(o + MAX_CLUSTER * sizeof(Slot));
-        redf = o;   o = align16(o + NW * 4 * sizeof(float));
-        redi = o;   o = align16(o + NW * 4 * sizeof(int));
-        misc = o;   o = align16(o + 32 * sizeof(int));
-        segkey = o; o = align16(o + size_t(nsc) * 4);
-        mass0 = o;  o = align16(o + size_t(nsc) * 4);
-        mass1 = o;  o = align16(o + size_t(nsc) * 4);
-        mass2 = o;  o = align16(o + size_t(nsc) * 4);
-        off = o;    o = align16(o + size_t(nsc + 1) * 4);
+        ctl = o;    o = align16(o + sizeof(Ctl));
+        part = o;   o = align16(o + MAX_CLUSTER * sizeof(Part));
+        red = o;    o = align16(o + 64 * sizeof(int));
+        segkey = o; o = align16(o + size_t(ns) * 4);
+        mass0 = o;  o = align16(o + size_t(ns) * 4);
+        mass1 = o;  o = align16(o + size_t(ns) * 4);
+        mass2 = o;  o = align16(o + size_t(ns) * 4);
+        list = o;   o = align16(o + size_t(ns + 1) * 4);
         lv = o;     o = align16(o + size_t(CAP) * 4);
         li = o;     o = align16(o + size_t(CAP) * 4);
         total = o;
@@ -75,49 +87,42 @@ struct Layout {
 extern __shared__ __align__(16) unsigned char smem_raw[];
 
 struct Smem {
-    Slot* slot;          // [2] this CTA's exchange records (double-buffered)
-    Slot* gath;          // [C] everyone's records after an exchange
-    float* redf;         // [NW*4] per-warp scratch
-    int* redi;           // [NW*4]
-    int* misc;           // [32]
-    uint32_t* segkey;    // [nsc] maximum order key per segment
-    float* mass[3];      // [nsc] per-segment masses (current low / the two pivots)
-    int* off;            // [nsc+1] per-segment counts / offsets / live-segment list
-    float* lv;           // [CAP] compact list: values
-    int* li;             // [CAP] compact list: token indices
-    __device__ explicit Smem(const Layout& L) {
-        slot = reinterpret_cast<Slot*>(smem_raw + L.slot);
-        gath = reinterpret_cast<Slot*>(smem_raw + L.gath);
-        redf = reinterpret_cast<float*>(smem_raw + L.redf);
-        redi = reinterpret_cast<int*>(smem_raw + L.redi);
-        misc = reinterpret_cast<int*>(smem_raw + L.misc);
+    Ctl* ctl;            // the current command
+    Part* part;          // [MAX_CLUSTER] partial results (leader)
+    int* red;            // [64] block-reduction scratch
+    uint32_t* segkey;    // [ns] maximum order key per segment (row-wide on the leader)
+    float* mass[3];      // [ns] per-segment masses (row-wide on the leader)
+    int* list;           // [ns+1] live-segment list / offsets (leader)
+    float* lv;           // [CAP] compact list: values (leader)
+    int* li;             // [CAP] compact list: token indices (leader)
+    __device__ explicit Smem(int ns) {
+        const Layout L(ns);
+        ctl = reinterpret_cast<Ctl*>(smem_raw + L.ctl);
+        part = reinterpret_cast<Part*>(smem_raw + L.part);
+        red = reinterpret_cast<int*>(smem_raw + L.red);
         segkey = reinterpret_cast<uint32_t*>(smem_raw + L.segkey);
         mass[0] = reinterpret_cast<float*>(smem_raw + L.mass0);
         mass[1] = reinterpret_cast<float*>(smem_raw + L.mass1);
         mass[2] = reinterpret_cast<float*>(smem_raw + L.mass2);
-        off = reinterpret_cast<int*>(smem_raw + L.off);
+        list = reinterpret_cast<int*>(smem_raw + L.list);
         lv = reinterpret_cast<float*>(smem_raw + L.lv);
         li = reinterpret_cast<int*>(smem_raw + L.li);
     }
 };
 
-// Which part of the row this CTA owns.
+// The row, its segmentation and this CTA's share.  Segment indices are row-wide.
 struct Geom {
     int V;
     int shift;     // log2(blocks per segment)
     int ns;        // segments per row
-    int nsc_max;   // segments per CTA (the last CTA may own fewer)
-    int s0;        // first segment of this CTA
-    int nsc;       // segments owned by this CTA
-    __device__ Geom(int V_, int shift_, int ns_, int nsc_max_, int rank)
-        : V(V_), shift(shift_), ns(ns_), nsc_max(nsc_max_), s0(rank * nsc_max_) {
-        nsc = max(0, min(nsc_max, ns - s0));
+    int s0, s1;    // this CTA's segments [s0, s1)
+    __device__ Geom(int V_, int shift_, int ns_, int nsc, int rank) : V(V_), shift(shift_), ns(ns_) {
+        s0 = min(ns, rank * nsc);
+        s1 = min(ns, s0 + nsc);
     }
     __device__ int seg_it() const { return 1 << shift; }
-    // First element of block `it` of local segment `ls`, as seen by `lane`.
-    __device__ int base(int ls, int it, int lane) const {
-        return ((s0 + ls) << shift) * BLK + it * BLK + lane * 4;
-    }
+    // First element of block `it` of segment `s`, as seen by `lane`.
+    __device__ int base(int s, int it, int lane) const { return ((s << shift) + it) * BLK + lane * 4; }
 };
 
 // ------------------------------------------------------------------ cluster PTX
@@ -153,17 +158,23 @@ __device__ __forceinline__ uint32_t map_rank(uint32_t saddr, uint32_t rank) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
     return r;
 }
-__device__ __forceinline__ uint32_t ld_dsmem_u32(uint32_t addr) {
-    uint32_t v;
-    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-    return v;
+__device__ __forceinline__ void st_dsmem_u32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
-__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) { return __uint_as_float(ld_dsmem_u32(addr)); }
+// Store a word into the leader's copy of a shared-memory location (local store on the
+// leader itself).
+__device__ __forceinline__ void put_leader(void* local_addr, uint32_t v, bool leader) {
+    if (leader) {
+        *reinterpret_cast<uint32_t*>(local_addr) = v;
+    } else {
+        st_dsmem_u32(map_rank(smem_u32(local_addr), 0), v);
+    }
+}
 
 // ------------------------------------------------------------------ loads
 
-// Elements [base, base+4) that straddle or pass the row end (or an unaligned row):
-// element by element, `fill` past V.  Kept out of line: it is the cold path.
+// Elements [base, base+4) that straddle the row end, or of an unaligned row: element
+// by element, `fill` past V.  Out of line: the cold path.
 template <bool NC>
 FS_NOINLINE __device__ float4 load4_tail(const float* __restrict__ row, int V, int base, float fill) {
     float t[4];
@@ -194,41 +205,7 @@ __device__ __forceinline__ float q_at(const float4& v, int q) {
     return q == 0 ? v.x : (q == 1 ? v.y : (q == 2 ? v.z : v.w));
 }
 
-// Visit this warp's segments in trips of T blocks (all loads of a trip in flight
-// together).  Segments go to warps in runs of T / seg_it consecutive segments,
-// round-robin.  live(ls) decides whether segment ls is read (warp-uniform);
-// body(ls, it, base, x, on) sees block `it` of segment ls (x = fill when not live);
-// done(ls, on) runs after the last block of segment ls.
-template <int T, bool VEC, bool NC, typename LIVE, typename BODY, typename DONE>
-__device__ __forceinline__ void visit(const float* __restrict__ row, const Geom& g, float fill, int warp, int lane,
-                                      LIVE live, BODY body, DONE done) {
-    static_assert(T >= (1 << MAX_SEG_SHIFT), "a trip must hold a whole segment");
-    const int spt = T >> g.shift;
-    const int mask = g.seg_it() - 1;
-    const int per = spt << g.shift;  // blocks per trip actually used
-    for (int first = warp * spt; first < g.nsc; first += NW * spt) {
-        float4 v[T];
-        bool on[T];
-#pragma unroll
-        for (int j = 0; j < T; ++j) {
-            const int ls = first + (j >> g.shift);
-            on[j] = j < per && ls < g.nsc && live(ls);
-            v[j] = on[j] ? load4<VEC, NC>(row, g.V, g.base(ls, j & mask, lane), fill)
-                         : make_float4(fill, fill, fill, fill);
-        }
-#pragma unroll
-        for (int j = 0; j < T; ++j) {
-            const int ls = first + (j >> g.shift);
-            if (j < per && ls < g.nsc) {
-                const int it = j & mask;
-                body(ls, it, g.base(ls, it, lane), v[j], on[j]);
-                if (it == mask) done(ls, on[j]);
-            }
-        }
-    }
-}
-
-// ------------------------------------------------------------------ warp helpers
+// ------------------------------------------------------------------ warp / block helpers
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -255,17 +232,42 @@ __device__ __forceinline__ int warp_incl_scan_i(int v, int lane) {
     return v;
 }
 
-// Sum of a[0..n) in a fixed order: lane l accumulates a[l], a[l+32], ... in order,
-// then the 32 lane sums are tree-reduced.  Warp-collective; identical in all lanes.
-__device__ __forceinline__ float ordered_sum(const float* a, int n, int lane) {
-    float acc = 0.f;
-    for (int i = lane; i < n; i += 32) acc += a[i];
-    return warp_sum(acc);
+// Contiguous range of [0, n) handled by warp w of NW.
+__device__ __forceinline__ void warp_range(int n, int w, int& r0, int& r1) {
+    const int per = (n + NW - 1) / NW;
+    r0 = min(n, w * per);
+    r1 = min(n, r0 + per);
 }
-__device__ __forceinline__ uint32_t ordered_max_u(const uint32_t* a, int n, int lane) {
-    uint32_t acc = 0;
-    for (int i = lane; i < n; i += 32) acc = max(acc, a[i]);
-    return warp_max_u(acc);
+
+// Sum of a[0..n) in a fixed order, by the whole CTA: warp w sums its contiguous range
+// (lane-strided, then a tree), the NW range sums are added in warp order.  Every
+// thread gets the same value.  Uses red[0..NW) and two CTA barriers.
+FS_NOINLINE __device__ inline float block_ordered_sum(const float* a, int n, int* red, int warp, int lane) {
+    int r0, r1;
+    warp_range(n, warp, r0, r1);
+    float acc = 0.f;
+    for (int i = r0 + lane; i < r1; i += 32) acc += a[i];
+    acc = warp_sum(acc);
+    float* rf = reinterpret_cast<float*>(red);
+    if (lane == 0) rf[warp] = acc;
+    __syncthreads();
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) s += rf[w];
+    __syncthreads();
+    return s;
+}
+
+// Block-wide sum of a per-warp value (each warp passes its warp-uniform value);
+// fixed order, every thread gets the result.
+__device__ __forceinline__ int block_sum_warp_values(int v, int* red, int warp, int lane) {
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    int s = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) s += red[w];
+    __syncthreads();
+    return s;
 }
 
 // ------------------------------------------------------------------ keys
@@ -316,142 +318,296 @@ __device__ __forceinline__ float sampler_uniform(unsigned long long seed, unsign
 
 // ------------------------------------------------------------------ pass 1
 
-// One streaming pass over this CTA's segments: per-segment maximum order key and
-// (PROB) mass; per-lane positive count and a bad-value flag (NaN or negative for
-// probabilities, NaN for logits).  Each warp keeps TRIP blocks in flight; the warp
-// reductions of the TRIP blocks are interleaved.
+// One streaming pass over this CTA's segments.  Warp w takes a contiguous range of
+// them and reads it in trips of TB blocks with the next trip's loads in flight while
+// the current trip is reduced.  For every segment: the maximum order key and (PROB)
+// the mass, stored locally (segment key) and into the leader's table.  Per lane: the
+// positive count and a bad-value flag (NaN or negative for probabilities, NaN for
+// logits).
 template <bool VEC, bool NC, bool PROB>
-__device__ __forceinline__ void pass1(const float* __restrict__ row, const Geom& g, uint32_t* segkey,
-                                      float* segmass, int warp, int lane, int& pos, bool& bad) {
-    const int spt = TRIP >> g.shift;
+__device__ __forceinline__ void pass1(const float* __restrict__ row, const Geom& g, const Smem& sm, bool leader,
+                                      int warp, int lane, int& pos, bool& bad) {
+    int r0, r1;
+    warp_range(g.s1 - g.s0, warp, r0, r1);
+    r0 += g.s0;
+    r1 += g.s0;
+    const int nblk = (r1 - r0) << g.shift;
+    const int mask = g.seg_it() - 1;
     const float fill = PROB ? 0.f : __int_as_float(0xff800000);
-    for (int first = warp * spt; first < g.nsc; first += NW * spt) {
-        float4 v[TRIP];
+    float4 A[TB], Bv[TB];
 #pragma unroll
-        for (int j = 0; j < TRIP; ++j) {
-            const int ls = first + (j >> g.shift);
-            v[j] = ls < g.nsc ? load4<VEC, NC>(row, g.V, g.base(ls, j & (g.seg_it() - 1), lane), fill)
-                              : make_float4(fill, fill, fill, fill);
-        }
-        float s[TRIP];
-        uint32_t km[TRIP];
+    for (int j = 0; j < TB; ++j)
+        A[j] = j < nblk ? load4<VEC, NC>(row, g.V, g.base(r0 + (j >> g.shift), j & mask, lane), fill)
+                        : make_float4(fill, fill, fill, fill);
+    for (int b0 = 0; b0 < nblk; b0 += TB) {
+        const int nb = b0 + TB;
 #pragma unroll
-        for (int j = 0; j < TRIP; ++j) {
-            const int ls = first + (j >> g.shift);
-            const int base = g.base(ls, j & (g.seg_it() - 1), lane);
+        for (int j = 0; j < TB; ++j)
+            Bv[j] = nb + j < nblk
+                        ? load4<VEC, NC>(row, g.V, g.base(r0 + ((nb + j) >> g.shift), (nb + j) & mask, lane), fill)
+                        : make_float4(fill, fill, fill, fill);
+        float s[TB];
+        uint32_t km[TB];
+#pragma unroll
+        for (int j = 0; j < TB; ++j) {
+            const int blk = b0 + j;
+            const int base = g.base(r0 + (blk >> g.shift), blk & mask, lane);
             uint32_t k = 0;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const float x = q_at(v[j], q);
+                const float x = q_at(A[j], q);
                 if (PROB) {
                     bad |= !(x >= 0.f);
                     k = max(k, prob_key(x));
                     pos += x > 0.f;
                 } else {
                     bad |= isnan(x);
-                    k = max(k, (ls < g.nsc && base + q < g.V) ? logit_key(x) : 0u);
+                    k = max(k, (blk < nblk && base + q < g.V) ? logit_key(x) : 0u);
                 }
             }
-            km[j] = k;
-            s[j] = PROB ? (v[j].x + v[j].y) + (v[j].z + v[j].w) : 0.f;
+            km[j] = __reduce_max_sync(FULL, k);
+            s[j] = PROB ? (A[j].x + A[j].y) + (A[j].z + A[j].w) : 0.f;
         }
-#pragma unroll
-        for (int j = 0; j < TRIP; ++j) km[j] = __reduce_max_sync(FULL, km[j]);
         if (PROB) {
 #pragma unroll
             for (int m = 16; m; m >>= 1)
 #pragma unroll
-                for (int j = 0; j < TRIP; ++j) s[j] += __shfl_xor_sync(FULL, s[j], m);
+                for (int j = 0; j < TB; ++j) s[j] += __shfl_xor_sync(FULL, s[j], m);
         }
-        // Lane t stores segment first + t (its blocks combined in block order).
-        if (lane < spt && first + lane < g.nsc) {
+        // Lane t stores segment (b0 >> shift) + t, its blocks combined in order.
+        const int nseg = TB >> g.shift;
+        const int sg = r0 + (b0 >> g.shift) + lane;
+        if (lane < nseg && sg < r1) {
             float ss = 0.f;
             uint32_t kk = 0;
 #pragma unroll
-            for (int j = 0; j < TRIP; ++j) {
+            for (int j = 0; j < TB; ++j) {
                 const bool mine = (j >> g.shift) == lane;
                 ss += mine ? s[j] : 0.f;
                 kk = mine ? max(kk, km[j]) : kk;
             }
-            segkey[first + lane] = kk;
-            if (PROB) segmass[first + lane] = ss;
+            sm.segkey[sg] = kk;
+            if (!leader) put_leader(&sm.segkey[sg], kk, false);
+            if (PROB) put_leader(&sm.mass[0][sg], __float_as_uint(ss), leader);
         }
+#pragma unroll
+        for (int j = 0; j < TB; ++j) A[j] = Bv[j];
     }
 }
 
-// Fused (mass, count) above two pivots over the segments whose maximum exceeds p1
-// (the rejection round's reduction, [blog] dual pivot).  Per-segment masses go to
-// m1 / m2 (zero for skipped segments); per-lane counts accumulate into c1 / c2.
+// The rejection round's fused reduction ([blog] dual pivot) over this CTA's segments
+// whose maximum exceeds p1: per segment the mass above p1 and above p2 (stored into
+// the leader's mass[ia] / mass[ib]; zero for skipped segments); per lane the counts.
 template <bool VEC, bool NC>
-__device__ __forceinline__ void pivot_pass(const float* __restrict__ row, const Geom& g, const uint32_t* segkey,
-                                           float p1, float p2, float* m1, float* m2, int warp, int lane, int& c1,
-                                           int& c2) {
-    const int spt = TRIP >> g.shift;
+FS_NOINLINE __device__ void pivot_pass(const float* __restrict__ row, const Geom& g, const Smem& sm, bool leader,
+                                       float p1, float p2, int ia, int ib, int warp, int lane, int* c1o, int* c2o) {
+    int r0, r1;
+    warp_range(g.s1 - g.s0, warp, r0, r1);
+    r0 += g.s0;
+    r1 += g.s0;
     const uint32_t kp1 = prob_key(p1);
-    for (int first = warp * spt; first < g.nsc; first += NW * spt) {
-        float4 v[TRIP];
+    const int mask = g.seg_it() - 1;
+    int c1 = 0, c2 = 0;
+    for (int b0 = 0; b0 < ((r1 - r0) << g.shift); b0 += TB) {
+        float4 v[TB];
         bool any = false;
 #pragma unroll
-        for (int j = 0; j < TRIP; ++j) {
-            const int ls = first + (j >> g.shift);
-            const bool on = ls < g.nsc && segkey[ls] > kp1;
+        for (int j = 0; j < TB; ++j) {
+            const int blk = b0 + j;
+            const int sg = r0 + (blk >> g.shift);
+            const bool on = sg < r1 && sm.segkey[sg] > kp1;
             any |= on;
-            v[j] = on ? load4<VEC, NC>(row, g.V, g.base(ls, j & (g.seg_it() - 1), lane), 0.f)
-                      : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[j] = on ? load4<VEC, NC>(row, g.V, g.base(sg, blk & mask, lane), 0.f) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        float a[TRIP], b[TRIP];
+        float a[TB], b[TB];
 #pragma unroll
-        for (int j = 0; j < TRIP; ++j) {
+        for (int j = 0; j < TB; ++j) {
             float w1[4], w2[4];
-            int cc = 0;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const float x = q_at(v[j], q);
                 w1[q] = x > p1 ? x : 0.f;
                 w2[q] = x > p2 ? x : 0.f;
-                cc += int(x > p1) + (int(x > p2) << 16);
+                c1 += x > p1;
+                c2 += x > p2;
             }
             a[j] = (w1[0] + w1[1]) + (w1[2] + w1[3]);
             b[j] = (w2[0] + w2[1]) + (w2[2] + w2[3]);
-            c1 += cc & 0xffff;
-            c2 += cc >> 16;
         }
         if (any) {
 #pragma unroll
             for (int m = 16; m; m >>= 1)
 #pragma unroll
-                for (int j = 0; j < TRIP; ++j) {
+                for (int j = 0; j < TB; ++j) {
                     a[j] += __shfl_xor_sync(FULL, a[j], m);
                     b[j] += __shfl_xor_sync(FULL, b[j], m);
                 }
         }
-        if (lane < spt && first + lane < g.nsc) {
+        const int nseg = TB >> g.shift;
+        const int sg = r0 + (b0 >> g.shift) + lane;
+        if (lane < nseg && sg < r1) {
             float sa = 0.f, sb = 0.f;
 #pragma unroll
-            for (int j = 0; j < TRIP; ++j) {
+            for (int j = 0; j < TB; ++j) {
                 const bool mine = (j >> g.shift) == lane;
                 sa += mine ? a[j] : 0.f;
                 sb += mine ? b[j] : 0.f;
             }
-            m1[first + lane] = sa;
-            m2[first + lane] = sb;
+            put_leader(&sm.mass[ia][sg], __float_as_uint(sa), leader);
+            put_leader(&sm.mass[ib][sg], __float_as_uint(sb), leader);
         }
     }
+    *c1o = warp_sum_i(c1);
+    *c2o = warp_sum_i(c2);
 }
 
-// ------------------------------------------------------------------ cluster exchange
+// ------------------------------------------------------------------ leader-side helpers
 
-// Every CTA has filled the first `words` 32-bit words of slot[buf] (one thread).  After
-// the barrier, the C slots are copied (one word per thread) into gath in rank order,
-// and a CTA barrier publishes them.  Word i < 8 is f[i]; word 8 + i is u[i].
-__device__ __forceinline__ void exchange(const Smem& sm, int buf, int C, int tid, int words = 20) {
-    cluster_sync();
-    for (int w = tid; w < C * words; w += NT) {
-        const int c = w / words, o = w % words;
-        const uint32_t a = map_rank(smem_u32(reinterpret_cast<const uint32_t*>(&sm.slot[buf]) + o), c);
-        reinterpret_cast<uint32_t*>(&sm.gath[c])[o] = ld_dsmem_u32(a);
+// Ordered list of the segments s in [0, ns) with segkey[s] >= thr, into list[0..n).
+// Block-collective; returns n.
+FS_NOINLINE __device__ inline int live_list(const Smem& sm, int ns, uint32_t thr, int warp, int lane) {
+    int r0, r1;
+    warp_range(ns, warp, r0, r1);
+    int cnt = 0;
+    for (int base = r0; base < r1; base += 32) {
+        const int i = base + lane;
+        cnt += __popc(__ballot_sync(FULL, i < r1 && sm.segkey[i] >= thr));
+    }
+    if (lane == 0) sm.red[warp] = cnt;
+    __syncthreads();
+    int off = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+        if (w < warp) off += sm.red[w];
+        total += sm.red[w];
+    }
+    for (int base = r0; base < r1; base += 32) {
+        const int i = base + lane;
+        const bool live = i < r1 && sm.segkey[i] >= thr;
+        const unsigned bal = __ballot_sync(FULL, live);
+        if (live) sm.list[off + __popc(bal & ((1u << lane) - 1u))] = i;
+        off += __popc(bal);
     }
     __syncthreads();
+    return total;
+}
+
+// Leader: read the listed segments (list[0..nlive), in order) and collect, in index
+// order, every element with key >= thr into lv/li.  Returns the exact count (the
+// list holds at most CAP; more means overflow).  Each warp takes TB blocks of listed
+// segments per batch, so a batch is one L2 round trip.  Block-collective.
+template <bool VEC, bool NC, typename KEYF>
+FS_NOINLINE __device__ int collect(const float* __restrict__ row, const Geom& g, const Smem& sm, int nlive,
+                                   uint32_t thr, KEYF keyf, float fill, int warp, int lane) {
+    constexpr int CB = 8;              // blocks per warp per batch
+    const int spw = CB >> g.shift;   // listed segments per warp per batch
+    const int mask = g.seg_it() - 1;
+    int total = 0;
+    for (int b0 = 0; b0 < nlive; b0 += NW * spw) {
+        float4 v[CB];
+        int c = 0;
+#pragma unroll
+        for (int j = 0; j < CB; ++j) {
+            const int li = b0 + warp * spw + (j >> g.shift);
+            const bool on = li < nlive;
+            const int sg = on ? sm.list[li] : 0;
+            v[j] = on ? load4<VEC, NC>(row, g.V, g.base(sg, j & mask, lane), fill)
+                      : make_float4(fill, fill, fill, fill);
+        }
+#pragma unroll
+        for (int j = 0; j < CB; ++j) {
+            const int li = b0 + warp * spw + (j >> g.shift);
+            if (li < nlive) {
+                const int base = g.base(sm.list[li], j & mask, lane);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) c += __popc(__ballot_sync(FULL, keyf(q_at(v[j], q)) >= thr && base + q < g.V));
+            }
+        }
+        if (lane == 0) sm.red[warp] = c;
+        __syncthreads();
+        int pos = total, chunk = 0;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            if (w < warp) pos += sm.red[w];
+            chunk += sm.red[w];
+        }
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < CB; ++j) {
+            const int li = b0 + warp * spw + (j >> g.shift);
+            if (li < nlive) {
+                const int base = g.base(sm.list[li], j & mask, lane);
+                bool keep[4];
+                int k = 0;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    keep[q] = keyf(q_at(v[j], q)) >= thr && base + q < g.V;
+                    k += keep[q];
+                }
+                const int incl = warp_incl_scan_i(k, lane);
+                int p = pos + incl - k;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    if (keep[q]) {
+                        if (p < CAP) {
+                            sm.lv[p] = q_at(v[j], q);
+                            sm.li[p] = base + q;
+                        }
+                        ++p;
+                    }
+                }
+                pos += __shfl_sync(FULL, incl, 31);
+            }
+        }
+        total += chunk;
+    }
+    __syncthreads();
+    return total;
+}
+
+// Largest key t among the keys of lv[0..n) with #{key >= t} >= k; 0 if none.
+// Block-collective (rank counting; the list is short).
+template <typename KEYF>
+FS_NOINLINE __device__ uint32_t kth_key_in_list(const Smem& sm, int n, int k, KEYF keyf, int warp, int lane,
+                                                int tid) {
+    uint32_t best = 0;
+    for (int i = tid; i < n; i += NT) {
+        const uint32_t ki = keyf(sm.lv[i]);
+        int ge = 0;
+        for (int j = 0; j < n; ++j) ge += (keyf(sm.lv[j]) >= ki);
+        if (ge >= k) best = max(best, ki);
+    }
+    best = warp_max_u(best);
+    if (lane == 0) sm.red[warp] = int(best);
+    __syncthreads();
+    uint32_t r = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) r = max(r, uint32_t(sm.red[w]));
+    __syncthreads();
+    return r;
+}
+
+// In-place, order-preserving filter of lv/li[0..n) to key >= t by one warp.
+// Returns the new length (warp-uniform).
+template <typename KEYF>
+FS_NOINLINE __device__ int filter_list_warp(const Smem& sm, int n, uint32_t t, KEYF keyf, int lane) {
+    int w = 0;
+    for (int base = 0; base < n; base += 32) {
+        const int i = base + lane;
+        const bool keep = i < n && keyf(sm.lv[i]) >= t;
+        const float xv = keep ? sm.lv[i] : 0.f;
+        const int xi = keep ? sm.li[i] : 0;
+        const unsigned bal = __ballot_sync(FULL, keep);
+        const int pos = w + __popc(bal & ((1u << lane) - 1u));
+        __syncwarp();
+        if (keep) {
+            sm.lv[pos] = xv;
+            sm.li[pos] = xi;
+        }
+        __syncwarp();
+        w += __popc(bal);
+    }
+    return w;
 }
 
 // ------------------------------------------------------------------ draws
@@ -463,14 +619,13 @@ __device__ __forceinline__ void exchange(const Smem& sm, int buf, int C, int tid
 // eligible element whose running sum exceeds t, else the segment's last eligible
 // element.  The segment must hold an eligible element.
 template <bool VEC, bool NC>
-FS_NOINLINE __device__ void locate_in_segment(const float* __restrict__ row, const Geom& g, int ls, float low,
-                                              float t, int lane, int* j_out, float* x_out) {
+FS_NOINLINE __device__ void locate_in_segment(const float* __restrict__ row, const Geom& g, int s, float low, float t,
+                                              int lane, int* j_out, float* x_out) {
     float run = 0.f;
     int last_j = -1;
     float last_x = 0.f;
-#pragma unroll 1
     for (int it = 0; it < g.seg_it(); ++it) {
-        const int base = g.base(ls, it, lane);
+        const int base = g.base(s, it, lane);
         const float4 v = load4<VEC, NC>(row, g.V, base, 0.f);
         float w[4];
 #pragma unroll
@@ -516,30 +671,86 @@ FS_NOINLINE __device__ void locate_in_segment(const float* __restrict__ row, con
     *x_out = last_x;
 }
 
-// First segment (local index) whose running mass over mass[0..n) exceeds t, with the
-// mass before it in `before`; if none, the last segment with positive mass and
-// `force_last` set.  Warp-collective.
-FS_NOINLINE __device__ inline int locate_segment(const float* mass, int n, float t, int lane, float* before,
-                                                 bool* force_last) {
-    float run = 0.f;
-    int last = -1;
-    for (int base = 0; base < n; base += 32) {
-        const float m = (base + lane < n) ? mass[base + lane] : 0.f;
-        const float incl = warp_incl_scan(m, lane);
-        const unsigned hit = __ballot_sync(FULL, m > 0.f && run + incl > t);
-        const unsigned nz = __ballot_sync(FULL, m > 0.f);
-        if (nz) last = base + 31 - __clz(nz);
-        if (hit) {
-            const int l = __ffs(hit) - 1;
-            *before = run + __shfl_sync(FULL, incl - m, l);
-            *force_last = false;
-            return base + l;
+// The segment holding target t in the running mass over mass[0..n), by the whole CTA:
+// warp range sums (the same grouping block_ordered_sum uses), the range holding t,
+// then the segment inside it.  If no running mass exceeds t (rounding), the last
+// segment with positive mass.  Returns the segment and the mass before it; every
+// thread gets them.  Block-collective.
+FS_NOINLINE __device__ inline int locate_segment_block(const float* mass, int n, float t, int* red, int warp,
+                                                       int lane, float* before_out) {
+    int r0, r1;
+    warp_range(n, warp, r0, r1);
+    float acc = 0.f;
+    for (int i = r0 + lane; i < r1; i += 32) acc += mass[i];
+    acc = warp_sum(acc);
+    float* rf = reinterpret_cast<float*>(red);
+    if (lane == 0) rf[warp] = acc;
+    __syncthreads();
+    int res = -1;
+    float before = 0.f;
+    if (warp == 0) {
+        // Range holding t (guarded: the last range with positive mass).
+        float run = 0.f, lastb = 0.f;
+        int w_hit = -1, w_last = -1;
+        for (int w = 0; w < NW; ++w) {
+            const float m = rf[w];
+            if (m > 0.f) {
+                if (w_hit < 0 && run + m > t) {
+                    w_hit = w;
+                    before = run;
+                }
+                w_last = w;
+                lastb = run;
+            }
+            run += m;
         }
-        run += __shfl_sync(FULL, incl, 31);
+        bool force = false;
+        if (w_hit < 0) {
+            w_hit = w_last;
+            before = lastb;
+            force = true;
+        }
+        if (w_hit >= 0) {
+            int a0, a1;
+            warp_range(n, w_hit, a0, a1);
+            float tt = force ? __int_as_float(0x7f800000) : t - before;
+            float r = 0.f;
+            int last = -1;
+            float last_before = 0.f;
+            for (int base = a0; base < a1; base += 32) {
+                const float m = (base + lane < a1) ? mass[base + lane] : 0.f;
+                const float incl = warp_incl_scan(m, lane);
+                const unsigned hit = __ballot_sync(FULL, m > 0.f && r + incl > tt);
+                const unsigned nz = __ballot_sync(FULL, m > 0.f);
+                if (nz) {
+                    const int l = 31 - __clz(nz);
+                    last = base + l;
+                    last_before = r + __shfl_sync(FULL, incl - m, l);
+                }
+                if (hit) {
+                    const int l = __ffs(hit) - 1;
+                    res = base + l;
+                    before += r + __shfl_sync(FULL, incl - m, l);
+                    break;
+                }
+                r += __shfl_sync(FULL, incl, 31);
+            }
+            if (res < 0) {
+                res = last;
+                before += last_before;
+            }
+        }
+        if (lane == 0) {
+            red[NW] = res;
+            rf[NW + 1] = before;
+        }
     }
-    *before = 0.f;
-    *force_last = true;
-    return last;
+    __syncthreads();
+    res = red[NW];
+    before = rf[NW + 1];
+    __syncthreads();
+    *before_out = before;
+    return res;
 }
 
 // Locate inside a compact list lv[0..n) (index order), eligible x > low.  Warp-collective.
@@ -587,457 +798,307 @@ FS_NOINLINE __device__ inline int locate_in_list(const float* lv, int n, float l
     return last;
 }
 
-// ------------------------------------------------------------------ compaction
+// ------------------------------------------------------------------ commands
 
-// Ordered list of this CTA's segments whose maximum key is >= thr, into off[0..n).
-// Block-collective; returns n.
-FS_NOINLINE __device__ inline int live_segments(const Smem& sm, int nsc, uint32_t thr, int warp, int lane, int tid) {
-    int out = 0;
-    for (int base = 0; base < nsc; base += NT) {
-        const int ls = base + tid;
-        const bool live = ls < nsc && sm.segkey[ls] >= thr;
-        const unsigned bal = __ballot_sync(FULL, live);
-        if (lane == 0) sm.redi[warp] = __popc(bal);
-        __syncthreads();
-        int woff = out, chunk = 0;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-            const int c = sm.redi[w];
-            if (w < warp) woff += c;
-            chunk += c;
-        }
-        __syncthreads();
-        if (live) sm.off[woff + __popc(bal & ((1u << lane) - 1u))] = ls;
-        out += chunk;
-        __syncthreads();
-    }
-    return out;
-}
-
-// Collect, in index order, every element of this CTA's segments with key >= thr into
-// lv/li (values, row indices), at most CAP of them.  Returns the exact count (which
-// may exceed CAP; the caller treats that as overflow).  Block-collective.  Each
-// batch of live segments is read once (one L2 round trip): counted, offsets scanned,
-// then written from registers.
-template <bool VEC, bool NC, typename KEYF>
-FS_NOINLINE __device__ int compact_ge(const float* __restrict__ row, const Geom& g, uint32_t thr, KEYF keyf,
-                                      float fill, const Smem& sm, int warp, int lane, int tid) {
-    const int nlive = live_segments(sm, g.nsc, thr, warp, lane, tid);
-    const int spt = TRIP >> g.shift;   // live segments a warp takes per batch
-    int* cnt = sm.redi + 2 * NW;       // per-warp counts of the current batch (NW entries)
-    int total = 0;
-    for (int b0 = 0; b0 < nlive; b0 += NW * spt) {
-        float4 v[TRIP];
-        int c = 0;
-#pragma unroll
-        for (int j = 0; j < TRIP; ++j) {
-            const int li = b0 + warp * spt + (j >> g.shift);
-            const bool on = li < nlive;
-            const int ls = on ? sm.off[li] : 0;
-            v[j] = on ? load4<VEC, NC>(row, g.V, g.base(ls, j & (g.seg_it() - 1), lane), fill)
-                      : make_float4(fill, fill, fill, fill);
-            if (on) {
-                const int base = g.base(ls, j & (g.seg_it() - 1), lane);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) c += __popc(__ballot_sync(FULL, keyf(q_at(v[j], q)) >= thr && base + q < g.V));
-            }
-        }
-        if (lane == 0) cnt[warp] = c;
-        __syncthreads();
-        int pos = total, chunk = 0;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-            if (w < warp) pos += cnt[w];
-            chunk += cnt[w];
-        }
-        __syncthreads();
-#pragma unroll
-        for (int j = 0; j < TRIP; ++j) {
-            const int li = b0 + warp * spt + (j >> g.shift);
-            if (li < nlive) {
-                const int ls = sm.off[li];
-                const int base = g.base(ls, j & (g.seg_it() - 1), lane);
-                bool keep[4];
-                int k = 0;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    keep[q] = keyf(q_at(v[j], q)) >= thr && base + q < g.V;
-                    k += keep[q];
-                }
-                const int incl = warp_incl_scan_i(k, lane);
-                int p = pos + incl - k;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    if (keep[q]) {
-                        if (p < CAP) {
-                            sm.lv[p] = q_at(v[j], q);
-                            sm.li[p] = base + q;
-                        }
-                        ++p;
-                    }
-                }
-                pos += __shfl_sync(FULL, incl, 31);
-            }
-        }
-        total += chunk;
-    }
-    __syncthreads();
-    return total;
-}
-
-// Rank 0: append the lists of ranks 1..C-1 (lengths in gath[c].u[cnt_idx]) after its
-// own, keeping only entries with key >= keep_thr, in rank then index order.  Returns
-// the new length (at most CAP).  Block-collective on rank 0.  Entries are compacted
-// in place: a write never lands past the entry being read.
-template <typename KEYF>
-FS_NOINLINE __device__ int gather_lists(const Smem& sm, int C, int cnt_idx, uint32_t keep_thr, KEYF keyf, int warp,
-                                        int lane, int tid) {
-    int total = 0;
-    for (int c = 0; c < C; ++c) total += int(sm.gath[c].u[cnt_idx]);
-    int out = 0;
-    for (int base = 0; base < total; base += NT) {
-        const int e = base + tid;
-        float v = 0.f;
-        int ix = 0;
-        bool keep = false;
-        if (e < total) {
-            int c = 0, acc = 0;
-            while (c < C - 1 && e >= acc + int(sm.gath[c].u[cnt_idx])) {
-                acc += int(sm.gath[c].u[cnt_idx]);
-                ++c;
-            }
-            const int le = e - acc;
-            if (c == 0) {
-                v = sm.lv[le];
-                ix = sm.li[le];
-            } else {
-                v = ld_dsmem_f32(map_rank(smem_u32(sm.lv + le), c));
-                ix = int(ld_dsmem_u32(map_rank(smem_u32(sm.li + le), c)));
-            }
-            keep = keyf(v) >= keep_thr;
-        }
-        const unsigned bal = __ballot_sync(FULL, keep);
-        if (lane == 0) sm.redi[warp] = __popc(bal);
-        __syncthreads();
-        int woff = out;
-        int chunk = 0;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-            const int n = sm.redi[w];
-            if (w < warp) woff += n;
-            chunk += n;
-        }
-        const int p = woff + __popc(bal & ((1u << lane) - 1u));
-        if (keep && p < CAP) {
-            sm.lv[p] = v;
-            sm.li[p] = ix;
-        }
-        out += chunk;
-        __syncthreads();
-    }
-    return min(out, CAP);
-}
-
-// Largest key t among the keys of lv[0..n) with #{key >= t} >= k; 0 if none.
-// Block-collective (rank counting; the list is short).
-template <typename KEYF>
-FS_NOINLINE __device__ uint32_t kth_key_in_list(const Smem& sm, int n, int k, KEYF keyf, int warp, int lane, int tid) {
-    uint32_t best = 0;
-    for (int i = tid; i < n; i += NT) {
-        const uint32_t ki = keyf(sm.lv[i]);
-        int ge = 0;
-        for (int j = 0; j < n; ++j) ge += (keyf(sm.lv[j]) >= ki);
-        if (ge >= k) best = max(best, ki);
-    }
-    best = warp_max_u(best);
-    if (lane == 0) sm.redi[warp] = int(best);
-    __syncthreads();
-    uint32_t r = 0;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) r = max(r, uint32_t(sm.redi[w]));
-    __syncthreads();
-    return r;
-}
-
-// Largest value t among a[0..n) with #{a >= t} >= k; 0 if none.  Block-collective.
-FS_NOINLINE __device__ inline uint32_t kth_in_array(const uint32_t* a, int n, int k, const Smem& sm, int warp,
-                                                    int lane, int tid) {
-    uint32_t best = 0;
-    for (int i = tid; i < n; i += NT) {
-        const uint32_t ki = a[i];
-        int ge = 0;
-        for (int j = 0; j < n; ++j) ge += (a[j] >= ki);
-        if (ge >= k) best = max(best, ki);
-    }
-    best = warp_max_u(best);
-    if (lane == 0) sm.redi[warp] = int(best);
-    __syncthreads();
-    uint32_t r = 0;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) r = max(r, uint32_t(sm.redi[w]));
-    __syncthreads();
-    return r;
-}
-
-// In-place, order-preserving filter of lv/li[0..n) to key >= t by one warp.
-// Returns the new length (warp-uniform).
-template <typename KEYF>
-FS_NOINLINE __device__ int filter_list_warp(const Smem& sm, int n, uint32_t t, KEYF keyf, int lane) {
-    int w = 0;
-    for (int base = 0; base < n; base += 32) {
-        const int i = base + lane;
-        const bool keep = i < n && keyf(sm.lv[i]) >= t;
-        const float xv = keep ? sm.lv[i] : 0.f;
-        const int xi = keep ? sm.li[i] : 0;
-        const unsigned bal = __ballot_sync(FULL, keep);
-        const int pos = w + __popc(bal & ((1u << lane) - 1u));
-        __syncwarp();
-        if (keep) {
-            sm.lv[pos] = xv;
-            sm.li[pos] = xi;
-        }
-        __syncwarp();
-        w += __popc(bal);
-    }
-    return w;
-}
-
-// ------------------------------------------------------------------ bisection
-
-// Interval of a threshold search over order keys ([drill] sections 2-3: bisection on a
-// monotone count or mass, done on the integer bit pattern so that it ends exactly on
-// an existing value).  Invariant: crit(lo) holds and crit(hi) does not, where
-// crit(t) = count(key >= t) >= k  or  mass(key >= t) >= target.  Done when
-// hi = lo + 1; then lo is the threshold.
-struct Bisect {
-    uint64_t lo, hi;
-    int cnt_lo;       // count(key >= lo)
-    float mass_lo;    // mass(key >= lo) (probabilities only)
-};
-
-// Drive the search to the end with passes of three pivots ([drill] section 5: the
-// production kernel tries several pivots per pass and stops once a single value is
-// left).  Each pass counts (and sums, MASS) the elements at or above each pivot and
-// records the smallest and largest key inside each of the four sub-intervals, so the
-// next interval shrinks to the keys that exist in it.  All CTAs of the cluster call
-// it with identical state and leave with identical results.  At most 40 passes.
-template <bool VEC, bool NC, bool MASS, typename KEYF>
-FS_NOINLINE __device__ void bisect_run(const float* __restrict__ row, const Geom& g, Bisect* stp, int kcrit,
-                                       float target, KEYF keyf, float fill, const Smem& sm, int* bufp, int C,
-                                       int warp, int lane, int tid) {
-    Bisect st = *stp;
-    int buf = *bufp;
-    for (int iter = 0; iter < 40 && st.hi - st.lo > 1; ++iter) {
-        const uint64_t d = st.hi - st.lo;
-        uint32_t piv[3];
-        if (d >= 4) {
-#pragma unroll
-            for (int i = 0; i < 3; ++i) piv[i] = uint32_t(st.lo + (d * uint64_t(i + 1)) / 4);
+// Leader: publish a command into every CTA's Ctl (DSMEM stores), then the cluster
+// barrier after which the peers read it.  Block-collective on the leader.
+__device__ __forceinline__ void send_command(const Smem& sm, const Ctl& c, int C, int tid) {
+    constexpr int W = sizeof(Ctl) / 4;
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(&c);
+    if (tid < C * W) {
+        const int r = tid / W, o = tid % W;
+        uint32_t* dst = reinterpret_cast<uint32_t*>(sm.ctl) + o;
+        if (r == 0) {
+            *dst = src[o];
         } else {
-            piv[0] = uint32_t(st.lo + 1);
-            piv[1] = uint32_t(d == 3 ? st.lo + 2 : st.hi);
-            piv[2] = uint32_t(st.hi);
+            st_dsmem_u32(map_rank(smem_u32(dst), r), src[o]);
         }
-        const uint64_t lo = st.lo, hi = st.hi;
-        float m[3] = {0.f, 0.f, 0.f};
-        int c[3] = {0, 0, 0};
-        uint32_t mn[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
-        uint32_t mx[4] = {0u, 0u, 0u, 0u};
-        visit<4, VEC, NC>(
-            row, g, fill, warp, lane, [&](int ls) { return uint64_t(sm.segkey[ls]) >= lo; },
-            [&](int, int, int base, float4 x, bool on) {
-                if (!on) return;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float xv = q_at(x, q);
-                    const uint32_t key = keyf(xv);
-                    const bool inr = base + q < g.V;
-                    const bool g0 = inr && key >= piv[0], g1 = inr && key >= piv[1], g2 = inr && key >= piv[2];
-                    if (MASS) {
-                        m[0] += g0 ? xv : 0.f;
-                        m[1] += g1 ? xv : 0.f;
-                        m[2] += g2 ? xv : 0.f;
-                    }
-                    c[0] += g0;
-                    c[1] += g1;
-                    c[2] += g2;
-                    const bool inlo = inr && uint64_t(key) >= lo && uint64_t(key) < hi;
-                    const int bkt = int(g0) + int(g1) + int(g2);
-#pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        const bool sel = inlo && t == bkt;
-                        mn[t] = sel ? min(mn[t], key) : mn[t];
-                        mx[t] = sel ? max(mx[t], key) : mx[t];
-                    }
-                }
-            },
-            [&](int, bool) {});
-        // Warp, then block, then cluster reductions (fixed order).
-#pragma unroll
-        for (int i = 0; i < 3; ++i) {
-            m[i] = warp_sum(m[i]);
-            c[i] = warp_sum_i(c[i]);
-        }
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            mn[t] = warp_min_u(mn[t]);
-            mx[t] = warp_max_u(mx[t]);
-        }
-        if (lane == 0) {
-            for (int i = 0; i < 3; ++i) {
-                sm.redf[warp * 4 + i] = m[i];
-                sm.redi[warp * 4 + i] = c[i];
-            }
-        }
-        __syncthreads();
-        if (tid == 0) {
-            for (int i = 0; i < 3; ++i) {
-                float a = 0.f;
-                uint32_t b = 0;
-                for (int w = 0; w < NW; ++w) {
-                    a += sm.redf[w * 4 + i];
-                    b += uint32_t(sm.redi[w * 4 + i]);
-                }
-                sm.slot[buf].f[i] = a;
-                sm.slot[buf].u[i] = b;
-            }
-        }
-        __syncthreads();
-        if (lane == 0) {
-            for (int t = 0; t < 4; ++t) {
-                sm.redi[warp * 4 + t] = int(mn[t]);
-                reinterpret_cast<uint32_t*>(sm.redf)[warp * 4 + t] = mx[t];
-            }
-        }
-        __syncthreads();
-        if (tid == 0) {
-            for (int t = 0; t < 4; ++t) {
-                uint32_t a = 0xffffffffu, b = 0u;
-                for (int w = 0; w < NW; ++w) {
-                    a = min(a, uint32_t(sm.redi[w * 4 + t]));
-                    b = max(b, reinterpret_cast<const uint32_t*>(sm.redf)[w * 4 + t]);
-                }
-                sm.slot[buf].u[3 + t] = a;
-                sm.slot[buf].u[7 + t] = b;
-            }
-        }
-        exchange(sm, buf, C, tid);
-        buf ^= 1;
-        float mass[3] = {0.f, 0.f, 0.f};
-        int cnt[3] = {0, 0, 0};
-        uint32_t kmin[4], kmax[4];
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            kmin[t] = 0xffffffffu;
-            kmax[t] = 0u;
-        }
-        for (int cc = 0; cc < C; ++cc) {
-#pragma unroll
-            for (int i = 0; i < 3; ++i) {
-                mass[i] += sm.gath[cc].f[i];
-                cnt[i] += int(sm.gath[cc].u[i]);
-            }
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                kmin[t] = min(kmin[t], sm.gath[cc].u[3 + t]);
-                kmax[t] = max(kmax[t], sm.gath[cc].u[7 + t]);
-            }
-        }
-        // crit is monotone in the pivot: take the largest pivot where it holds.
-        int best = -1;
-#pragma unroll
-        for (int i = 0; i < 3; ++i) {
-            if (uint64_t(piv[i]) < hi) {
-                const bool ok = MASS ? (mass[i] >= target) : (cnt[i] >= kcrit);
-                if (ok) best = i;
-            }
-        }
-        uint64_t nlo = lo, nhi = hi;
-        int bkt = 0;
-        if (best >= 0) {
-            nlo = piv[best];
-            st.cnt_lo = cnt[best];
-            st.mass_lo = mass[best];
-            bkt = best + 1;
-        }
-        if (best + 1 < 3 && uint64_t(piv[best + 1]) < hi) nhi = piv[best + 1];
-        if (kmin[bkt] <= kmax[bkt]) {  // keys present in the new interval
-            nlo = max(nlo, uint64_t(kmin[bkt]));
-            nhi = min(nhi, uint64_t(kmax[bkt]) + 1);
-        }
-        st.lo = nlo;
-        st.hi = nhi;
-        __syncthreads();  // gath is rewritten by the next exchange
     }
-    *stp = st;
-    *bufp = buf;
+    cluster_sync();
 }
 
-// Count and mass (probabilities, x > 0) of key >= t over this CTA's segments, then
-// cluster-wide.  When seg_mass is given the per-segment masses are stored there and
-// the CTA mass is their ordered sum (what a later draw scans); per_rank (shared
-// memory, nullable) receives the C per-CTA masses.
-template <bool VEC, bool NC, typename KEYF>
-FS_NOINLINE __device__ void mass_count_ge(const float* __restrict__ row, const Geom& g, uint32_t t, KEYF keyf,
-                                          float* seg_mass, const Smem& sm, int* bufp, int C, int warp, int lane,
-                                          int tid, float* mass_out, int* cnt_out, float* per_rank) {
-    float wm = 0.f, ms = 0.f;
-    int wc = 0;
-    visit<4, VEC, NC>(
-        row, g, 0.f, warp, lane, [&](int ls) { return sm.segkey[ls] >= t; },
-        [&](int, int it, int base, float4 x, bool on) {
-            if (it == 0) ms = 0.f;
-            if (!on) return;
-            float s = 0.f;
-            int c = 0;
+// A three-pivot bisection pass ([drill] sections 3-5) over this CTA's segments whose
+// maximum key is >= lo: count and (MASS) mass of keys >= each pivot, and per
+// sub-interval [lo,p0) [p0,p1) [p1,p2) [p2,hi) the smallest and largest key present.
+// The CTA's record goes to the leader's part[rank]: f[0..2] masses, u[0..2] counts,
+// u[3..6] min keys, u[7..10] max keys.  Block-collective.
+template <bool VEC, bool NC, bool MASS, typename KEYF>
+FS_NOINLINE __device__ void bisect_pass(const float* __restrict__ row, const Geom& g, const Smem& sm, bool leader,
+                                        int rank, uint64_t lo, uint64_t hi, const uint32_t* piv, KEYF keyf,
+                                        float fill, int warp, int lane, int tid) {
+    int r0, r1;
+    warp_range(g.s1 - g.s0, warp, r0, r1);
+    r0 += g.s0;
+    r1 += g.s0;
+    const int mask = g.seg_it() - 1;
+    const uint32_t p0 = piv[0], p1 = piv[1], p2 = piv[2];
+    float m[3] = {0.f, 0.f, 0.f};
+    int c[3] = {0, 0, 0};
+    uint32_t mn[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+    uint32_t mx[4] = {0u, 0u, 0u, 0u};
+    for (int b0 = 0; b0 < ((r1 - r0) << g.shift); b0 += TB) {
+        float4 v[TB];
+        bool on[TB];
+#pragma unroll
+        for (int j = 0; j < TB; ++j) {
+            const int blk = b0 + j;
+            const int sg = r0 + (blk >> g.shift);
+            on[j] = sg < r1 && uint64_t(sm.segkey[sg]) >= lo;
+            v[j] = on[j] ? load4<VEC, NC>(row, g.V, g.base(sg, blk & mask, lane), fill)
+                         : make_float4(fill, fill, fill, fill);
+        }
+#pragma unroll
+        for (int j = 0; j < TB; ++j) {
+            if (!on[j]) continue;
+            const int blk = b0 + j;
+            const int base = g.base(r0 + (blk >> g.shift), blk & mask, lane);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const float xv = q_at(x, q);
-                const bool gq = keyf(xv) >= t && xv > 0.f && base + q < g.V;
-                s += gq ? xv : 0.f;
-                c += gq;
+                const float xv = q_at(v[j], q);
+                const uint32_t key = keyf(xv);
+                const bool inr = base + q < g.V;
+                const bool g0 = inr && key >= p0, g1 = inr && key >= p1, g2 = inr && key >= p2;
+                if (MASS) {
+                    m[0] += g0 ? xv : 0.f;
+                    m[1] += g1 ? xv : 0.f;
+                    m[2] += g2 ? xv : 0.f;
+                }
+                c[0] += g0;
+                c[1] += g1;
+                c[2] += g2;
+                const bool inlo = inr && uint64_t(key) >= lo && uint64_t(key) < hi;
+                const int bkt = int(g0) + int(g1) + int(g2);
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const bool sel = inlo && t == bkt;
+                    mn[t] = sel ? min(mn[t], key) : mn[t];
+                    mx[t] = sel ? max(mx[t], key) : mx[t];
+                }
             }
-            ms += warp_sum(s);
-            wc += warp_sum_i(c);
-        },
-        [&](int ls, bool) {
-            if (seg_mass && lane == 0) seg_mass[ls] = ms;
-            wm += ms;
-        });
+        }
+    }
+    // warp -> block (fixed order) -> the leader's part[rank]
+    float* rf = reinterpret_cast<float*>(sm.red);
+    uint32_t* ru = reinterpret_cast<uint32_t*>(sm.red);
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+        m[i] = warp_sum(m[i]);
+        c[i] = warp_sum_i(c[i]);
+    }
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        mn[t] = warp_min_u(mn[t]);
+        mx[t] = warp_max_u(mx[t]);
+    }
     if (lane == 0) {
-        sm.redf[warp] = wm;
-        sm.redi[warp] = wc;
+        for (int i = 0; i < 3; ++i) {
+            rf[i * NW + warp] = m[i];
+            ru[(3 + i) * NW + warp] = uint32_t(c[i]);
+        }
     }
     __syncthreads();
-    const int buf = *bufp;
-    if (warp == 0) {
-        float s = 0.f;
-        if (seg_mass) {
-            s = ordered_sum(seg_mass, g.nsc, lane);
-        } else {
-#pragma unroll
-            for (int w = 0; w < NW; ++w) s += sm.redf[w];
-        }
-        int n = 0;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) n += sm.redi[w];
-        if (lane == 0) {
-            sm.slot[buf].f[0] = s;
-            sm.slot[buf].u[0] = uint32_t(n);
+    uint32_t rec[6];
+    if (tid == 0) {
+        for (int i = 0; i < 3; ++i) {
+            float a = 0.f;
+            uint32_t b = 0;
+            for (int w = 0; w < NW; ++w) {
+                a += rf[i * NW + w];
+                b += ru[(3 + i) * NW + w];
+            }
+            rec[i] = __float_as_uint(a);
+            rec[3 + i] = b;
         }
     }
-    exchange(sm, buf, C, tid);
-    *bufp = buf ^ 1;
-    float mass = 0.f;
+    __syncthreads();
+    if (lane == 0) {
+        for (int t = 0; t < 4; ++t) {
+            ru[t * NW + warp] = mn[t];
+            ru[(4 + t) * NW + warp] = mx[t];
+        }
+    }
+    __syncthreads();
+    if (tid == 0) {
+        uint32_t* dst = reinterpret_cast<uint32_t*>(&sm.part[rank]);
+        for (int t = 0; t < 4; ++t) {
+            uint32_t a = 0xffffffffu, b = 0u;
+            for (int w = 0; w < NW; ++w) {
+                a = min(a, ru[t * NW + w]);
+                b = max(b, ru[(4 + t) * NW + w]);
+            }
+            put_leader(dst + 4 + 3 + t, a, leader);   // u[3 + t]
+            put_leader(dst + 4 + 7 + t, b, leader);   // u[7 + t]
+        }
+        for (int i = 0; i < 3; ++i) {
+            put_leader(dst + i, rec[i], leader);          // f[i]
+            put_leader(dst + 4 + i, rec[3 + i], leader);  // u[i]
+        }
+    }
+}
+
+// Count and mass (x > 0) of key >= t over this CTA's segments; the record goes to the
+// leader's part[rank] (f[0] mass, u[0] count).  Block-collective.
+template <bool VEC, bool NC, typename KEYF>
+FS_NOINLINE __device__ void massge_pass(const float* __restrict__ row, const Geom& g, const Smem& sm, bool leader,
+                                        int rank, uint32_t t, KEYF keyf, int warp, int lane, int tid) {
+    int r0, r1;
+    warp_range(g.s1 - g.s0, warp, r0, r1);
+    r0 += g.s0;
+    r1 += g.s0;
+    const int mask = g.seg_it() - 1;
+    float ms = 0.f;
     int cnt = 0;
-    for (int c = 0; c < C; ++c) {
-        mass += sm.gath[c].f[0];
-        cnt += int(sm.gath[c].u[0]);
+    for (int blk = 0; blk < ((r1 - r0) << g.shift); ++blk) {
+        const int sg = r0 + (blk >> g.shift);
+        if (sm.segkey[sg] < t) continue;
+        const int base = g.base(sg, blk & mask, lane);
+        const float4 v = load4<VEC, NC>(row, g.V, base, 0.f);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float xv = q_at(v, q);
+            const bool gq = keyf(xv) >= t && xv > 0.f && base + q < g.V;
+            ms += gq ? xv : 0.f;
+            cnt += gq;
+        }
     }
-    if (per_rank && tid < C) per_rank[tid] = sm.gath[tid].f[0];
+    ms = warp_sum(ms);
+    cnt = warp_sum_i(cnt);
+    float* rf = reinterpret_cast<float*>(sm.red);
+    if (lane == 0) {
+        rf[warp] = ms;
+        sm.red[NW + warp] = cnt;
+    }
     __syncthreads();
-    *mass_out = mass;
-    *cnt_out = cnt;
+    if (tid == 0) {
+        float a = 0.f;
+        int n = 0;
+        for (int w = 0; w < NW; ++w) {
+            a += rf[w];
+            n += sm.red[NW + w];
+        }
+        uint32_t* dst = reinterpret_cast<uint32_t*>(&sm.part[rank]);
+        put_leader(dst, __float_as_uint(a), leader);
+        put_leader(dst + 4, uint32_t(n), leader);
+    }
+}
+
+// Leader: one bisection step after all parts are in.  Updates the interval; returns
+// nothing (the state is replicated in the caller's registers on the leader only).
+struct Bisect {
+    uint64_t lo, hi;   // crit(lo) holds, crit(hi) does not; done when hi = lo + 1
+    float mass_lo;     // mass(key >= lo) (probabilities)
+};
+
+// Pivots of the next pass: three points splitting [lo, hi) into quarters (fewer when
+// the interval is short; unused pivots equal hi).
+__device__ __forceinline__ void bisect_pivots(const Bisect& st, uint32_t* piv) {
+    const uint64_t d = st.hi - st.lo;
+    if (d >= 4) {
+#pragma unroll
+        for (int i = 0; i < 3; ++i) piv[i] = uint32_t(st.lo + (d * uint64_t(i + 1)) / 4);
+    } else {
+        piv[0] = uint32_t(st.lo + 1);
+        piv[1] = uint32_t(d == 3 ? st.lo + 2 : st.hi);
+        piv[2] = uint32_t(st.hi);
+    }
+}
+
+// Fold the C parts of a bisection pass into the interval ([drill] section 5: take the
+// largest pivot where the criterion holds; shrink to the keys present).
+template <bool MASS>
+__device__ __forceinline__ void bisect_update(const Smem& sm, int C, Bisect& st, const uint32_t* piv, int kcrit,
+                                              float target) {
+    float mass[3] = {0.f, 0.f, 0.f};
+    int cnt[3] = {0, 0, 0};
+    uint32_t kmin[4], kmax[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        kmin[t] = 0xffffffffu;
+        kmax[t] = 0u;
+    }
+    for (int c = 0; c < C; ++c) {
+        const Part& p = sm.part[c];
+#pragma unroll
+        for (int i = 0; i < 3; ++i) {
+            mass[i] += p.f[i];
+            cnt[i] += int(p.u[i]);
+        }
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            kmin[t] = min(kmin[t], p.u[3 + t]);
+            kmax[t] = max(kmax[t], p.u[7 + t]);
+        }
+    }
+    int best = -1;
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+        if (uint64_t(piv[i]) < st.hi) {
+            const bool ok = MASS ? (mass[i] >= target) : (cnt[i] >= kcrit);
+            if (ok) best = i;
+        }
+    }
+    uint64_t nlo = st.lo, nhi = st.hi;
+    int bkt = 0;
+    if (best >= 0) {
+        nlo = piv[best];
+        st.mass_lo = mass[best];
+        bkt = best + 1;
+    }
+    if (best + 1 < 3 && uint64_t(piv[best + 1]) < st.hi) nhi = piv[best + 1];
+    if (kmin[bkt] <= kmax[bkt]) {  // keys present in the new interval
+        nlo = max(nlo, uint64_t(kmin[bkt]));
+        nhi = min(nhi, uint64_t(kmax[bkt]) + 1);
+    }
+    st.lo = nlo;
+    st.hi = nhi;
+}
+
+// Leader: drive a bisection to the end with the whole cluster (at most 40 passes).
+template <bool VEC, bool NC, bool MASS, typename KEYF>
+FS_NOINLINE __device__ void bisect_leader(const float* __restrict__ row, const Geom& g, const Smem& sm, int C,
+                                          Bisect* stp, int kcrit, float target, KEYF keyf, float fill, int warp,
+                                          int lane, int tid) {
+    Bisect st = *stp;
+    for (int iter = 0; iter < 40 && st.hi - st.lo > 1; ++iter) {
+        uint32_t piv[3];
+        bisect_pivots(st, piv);
+        Ctl c{};
+        c.cmd = CMD_BISECT;
+        c.u[0] = piv[0];
+        c.u[1] = piv[1];
+        c.u[2] = piv[2];
+        c.u[3] = uint32_t(st.lo);
+        c.hi_lo = uint32_t(st.hi);
+        c.hi_hi = uint32_t(st.hi >> 32);
+        send_command(sm, c, C, tid);
+        bisect_pass<VEC, NC, MASS>(row, g, sm, true, 0, st.lo, st.hi, piv, keyf, fill, warp, lane, tid);
+        cluster_sync();  // every part is in
+        bisect_update<MASS>(sm, C, st, piv, kcrit, target);
+        __syncthreads();
+    }
+    *stp = st;
+}
+
+// Leader: count and mass of key >= t over the whole row, with the cluster.
+template <bool VEC, bool NC, typename KEYF>
+FS_NOINLINE __device__ void massge_leader(const float* __restrict__ row, const Geom& g, const Smem& sm, int C,
+                                          uint32_t t, KEYF keyf, int warp, int lane, int tid, float* mass_out,
+                                          int* cnt_out) {
+    Ctl c{};
+    c.cmd = CMD_MASSGE;
+    c.u[0] = t;
+    send_command(sm, c, C, tid);
+    massge_pass<VEC, NC>(row, g, sm, true, 0, t, keyf, warp, lane, tid);
+    cluster_sync();
+    float m = 0.f;
+    int n = 0;
+    for (int r = 0; r < C; ++r) {
+        m += sm.part[r].f[0];
+        n += int(sm.part[r].u[0]);
+    }
+    __syncthreads();
+    *mass_out = m;
+    *cnt_out = n;
 }
 
 }  // namespace fsd

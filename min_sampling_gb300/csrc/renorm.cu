@@ -17,6 +17,7 @@
 
 #include "fs_device.cuh"
 #include "fs_host.h"
+#include "topk_bound.cuh"
 
 namespace fsd {
 
@@ -34,6 +35,80 @@ struct FilterArgs {
     int nsc;
 };
 
+// Write this CTA's segments: keep key >= t (x / denom, or the logit), else fill.
+// Segments whose maximum key is below t are written without being read.
+template <bool VEC, int KIND>
+FS_NOINLINE __device__ void write_pass(const float* __restrict__ row, float* __restrict__ orow, const Geom& g,
+                                       const Smem& sm, bool valid, uint32_t t, float denom, int warp, int lane) {
+    using KEYF = typename std::conditional<KIND == K_MASK, KeyLogit, KeyProb>::type;
+    constexpr bool IS_PROB = KIND != K_MASK;
+    const KEYF keyf;
+    const float fill = IS_PROB ? 0.f : __int_as_float(0xff800000);
+    const bool vec_out = VEC && ((reinterpret_cast<uintptr_t>(orow) & 15) == 0);
+    int r0, r1;
+    warp_range(g.s1 - g.s0, warp, r0, r1);
+    r0 += g.s0;
+    r1 += g.s0;
+    const int mask = g.seg_it() - 1;
+    for (int b0 = 0; b0 < ((r1 - r0) << g.shift); b0 += TB) {
+        float4 v[TB];
+        bool on[TB];
+#pragma unroll
+        for (int j = 0; j < TB; ++j) {
+            const int blk = b0 + j;
+            const int sg = r0 + (blk >> g.shift);
+            on[j] = sg < r1 && valid && sm.segkey[sg] >= t;
+            v[j] = on[j] ? load4<VEC, false>(row, g.V, g.base(sg, blk & mask, lane), fill)
+                         : make_float4(fill, fill, fill, fill);
+        }
+#pragma unroll
+        for (int j = 0; j < TB; ++j) {
+            const int blk = b0 + j;
+            const int sg = r0 + (blk >> g.shift);
+            if (sg >= r1) continue;
+            const int base = g.base(sg, blk & mask, lane);
+            float o[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float xv = q_at(v[j], q);
+                o[q] = (on[j] && keyf(xv) >= t) ? (IS_PROB ? xv / denom : xv) : fill;
+            }
+            if (vec_out && base + 3 < g.V) {
+                *reinterpret_cast<float4*>(orow + base) = make_float4(o[0], o[1], o[2], o[3]);
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (base + q < g.V) orow[base + q] = o[q];
+            }
+        }
+    }
+}
+
+// The other CTAs: follow the leader's commands until the write.
+template <bool VEC, int KIND>
+FS_NOINLINE __device__ void filter_peer(const float* __restrict__ row, float* __restrict__ orow, const Geom& g,
+                                        const Smem& sm, int rank, int warp, int lane, int tid) {
+    using KEYF = typename std::conditional<KIND == K_MASK, KeyLogit, KeyProb>::type;
+    const float fill = KIND == K_MASK ? __int_as_float(0xff800000) : 0.f;
+    for (;;) {
+        cluster_sync();  // the command is published
+        const Ctl c = *sm.ctl;
+        if (c.cmd == CMD_BISECT) {
+            const uint64_t hi = uint64_t(c.hi_lo) | (uint64_t(c.hi_hi) << 32);
+            bisect_pass<VEC, false, KIND == K_TOPP>(row, g, sm, false, rank, c.u[3], hi, c.u, KEYF(), fill, warp,
+                                                    lane, tid);
+        } else if (c.cmd == CMD_MASSGE) {
+            massge_pass<VEC, false>(row, g, sm, false, rank, c.u[0], KEYF(), warp, lane, tid);
+        } else if (c.cmd == CMD_WRITE) {
+            write_pass<VEC, KIND>(row, orow, g, sm, c.flag != 0, c.u[0], c.f[0], warp, lane);
+            return;
+        } else {
+            return;  // CMD_EXIT
+        }
+        cluster_sync();  // the results are in the leader
+    }
+}
+
 template <bool VEC, int KIND>
 __global__ void __launch_bounds__(NT, 4) filter_kernel(const FilterArgs a) {
     using KEYF = typename std::conditional<KIND == K_MASK, KeyLogit, KeyProb>::type;
@@ -43,67 +118,52 @@ __global__ void __launch_bounds__(NT, 4) filter_kernel(const FilterArgs a) {
     const int rank = int(cluster_ctarank());
     const int b = int(cluster_id_x());
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const Layout L(a.nsc);
-    const Smem sm(L);
+    const bool leader = rank == 0;
+    const Smem sm(a.ns);
     const Geom g(a.V, a.shift, a.ns, a.nsc, rank);
-    const int V = a.V;
+    const int V = a.V, ns = a.ns;
     const float* row = a.in + size_t(b) * size_t(V);
     float* orow = a.out + size_t(b) * size_t(V);
     const float fill = IS_PROB ? 0.f : __int_as_float(0xff800000);
-    const int k = (KIND != K_TOPP) ? a.top_k[b] : 0;
-    const float tp = (KIND == K_TOPP) ? a.top_p[b] : 1.f;
-    const bool k_on = KIND != K_TOPP && k > 0 && k < V;
 
     // ---- pass 1
     int pos = 0;
     bool bad = false;
-    pass1<VEC, false, IS_PROB>(row, g, sm.segkey, sm.mass[0], warp, lane, pos, bad);
-    const int wbad = __any_sync(FULL, bad) ? 1 : 0;
-    if (lane == 0) sm.redi[NW + warp] = wbad;
-    __syncthreads();
+    pass1<VEC, false, IS_PROB>(row, g, sm, leader, warp, lane, pos, bad);
+    pos = block_sum_warp_values(warp_sum_i(pos), sm.red, warp, lane);
+    const int nbad = block_sum_warp_values(__any_sync(FULL, bad) ? 1 : 0, sm.red, warp, lane);
+    if (tid == 0) {
+        uint32_t* dst = reinterpret_cast<uint32_t*>(&sm.part[rank]);
+        put_leader(dst + 4, uint32_t(pos), leader);
+        put_leader(dst + 5, uint32_t(nbad), leader);
+    }
+    cluster_sync();  // the leader's segment table and parts are complete
+    if (!leader) {
+        filter_peer<VEC, KIND>(row, orow, g, sm, rank, warp, lane, tid);
+        return;
+    }
 
-    // Local lower bound of the top-k threshold and the local candidates.
-    uint32_t L0c = 0;
-    int nloc = -1;
-    if (k_on && g.nsc >= k) {
-        L0c = max(IS_PROB ? 1u : 0u, kth_in_array(sm.segkey, g.nsc, k, sm, warp, lane, tid));
-        nloc = compact_ge<VEC, false>(row, g, L0c, keyf, fill, sm, warp, lane, tid);
-        if (nloc > CAP) nloc = -1;
-    }
-    if (warp == 0) {
-        const uint32_t km = ordered_max_u(sm.segkey, g.nsc, lane);
-        const float s = IS_PROB ? ordered_sum(sm.mass[0], g.nsc, lane) : 0.f;
-        if (lane == 0) {
-            int nb = 0;
-#pragma unroll
-            for (int w = 0; w < NW; ++w) nb |= sm.redi[NW + w];
-            sm.slot[0].f[0] = s;
-            sm.slot[0].u[0] = km;
-            sm.slot[0].u[1] = uint32_t(nb);
-            sm.slot[0].u[3] = L0c;
-            sm.slot[0].u[4] = uint32_t(nloc);
-        }
-    }
-    int buf = 0;
-    exchange(sm, buf, C, tid, 13);
-    buf ^= 1;
-    uint32_t maxkey = 0, L0 = 0;
-    float M = 0.f;
-    bool any_bad = false, lists_ok = true;
-    int ncand = 0;
+    // ---- leader
+    const int k = (KIND != K_TOPP) ? a.top_k[b] : 0;
+    const float tp = (KIND == K_TOPP) ? a.top_p[b] : 1.f;
+    const bool k_on = KIND != K_TOPP && k > 0 && k < V;
+    int npos = 0;
+    bool any_bad = false;
     for (int c = 0; c < C; ++c) {
-        const Slot& s = sm.gath[c];
-        M += s.f[0];
-        maxkey = max(maxkey, s.u[0]);
-        any_bad |= s.u[1] != 0;
-        L0 = max(L0, s.u[3]);
-        const int n = int(s.u[4]);
-        lists_ok = lists_ok && n >= 0;
-        ncand += max(n, 0);
+        npos += int(sm.part[c].u[0]);
+        any_bad |= sm.part[c].u[1] != 0;
     }
-    lists_ok = lists_ok && ncand <= CAP;
-    __syncthreads();
-
+    const float M = IS_PROB ? block_ordered_sum(sm.mass[0], ns, sm.red, warp, lane) : 0.f;
+    uint32_t maxkey = 0;
+    {
+        uint32_t km = 0;
+        for (int i = tid; i < ns; i += NT) km = max(km, sm.segkey[i]);
+        km = warp_max_u(km);
+        if (lane == 0) sm.red[warp] = int(km);
+        __syncthreads();
+        for (int w = 0; w < NW; ++w) maxkey = max(maxkey, uint32_t(sm.red[w]));
+        __syncthreads();
+    }
     bool valid = !any_bad;
     if (IS_PROB) valid = valid && M > 0.f && M <= 3.402823466e38f;
     if (KIND == K_TOPP && isnan(tp)) valid = false;
@@ -113,37 +173,35 @@ __global__ void __launch_bounds__(NT, 4) filter_kernel(const FilterArgs a) {
     if (valid) {
         if (KIND != K_TOPP) {
             if (k_on) {
-                if (lists_ok) {
-                    if (rank == 0) {
-                        const int n = gather_lists(sm, C, 4, L0, keyf, warp, lane, tid);
-                        const uint32_t tk = kth_key_in_list(sm, n, k, keyf, warp, lane, tid);
-                        if (warp == 0) {
-                            float s = 0.f;
-                            for (int i = lane; i < n; i += 32) s += keyf(sm.lv[i]) >= tk ? sm.lv[i] : 0.f;
-                            s = warp_sum(s);
-                            if (lane == 0) {
-                                sm.slot[buf].f[0] = s;
-                                sm.slot[buf].u[0] = tk;
-                            }
-                        }
+                uint32_t L0 = topk_bound(sm, ns, k, IS_PROB ? 21 : 22, warp, lane, tid);
+                if (IS_PROB) L0 = max(L0, 1u);
+                const int nlive = live_list(sm, ns, L0, warp, lane);
+                const int n = collect<VEC, false>(row, g, sm, nlive, L0, keyf, fill, warp, lane);
+                if (n <= CAP) {
+                    // Every element >= L0 (hence >= t) is in the list.
+                    t = kth_key_in_list(sm, n, k, keyf, warp, lane, tid);
+                    if (warp == 0) {
+                        float s = 0.f;
+                        for (int i = lane; i < n; i += 32) s += keyf(sm.lv[i]) >= t ? sm.lv[i] : 0.f;
+                        s = warp_sum(s);
+                        if (lane == 0) reinterpret_cast<float*>(sm.red)[40] = s;
                     }
-                    exchange(sm, buf, C, tid, 9);
-                    buf ^= 1;
-                    t = sm.gath[0].u[0];
-                    denom = sm.gath[0].f[0];
+                    __syncthreads();
+                    denom = reinterpret_cast<float*>(sm.red)[40];
                     __syncthreads();
                 } else {
                     Bisect st;
-                    st.lo = L0;  // crit(L0) holds (L0 <= t_k), and crit(0) trivially
+                    // crit(L0) holds when L0 came from the segment maxima; otherwise start
+                    // from 0 (count(key >= 0) = V >= k).
+                    st.lo = (IS_PROB && npos < k) ? 0u : L0;
+                    if (IS_PROB && L0 == 1u && npos < k) st.lo = 0;
                     st.hi = uint64_t(maxkey) + 1;
-                    st.cnt_lo = 0;
                     st.mass_lo = 0.f;
-                    bisect_run<VEC, false, false>(row, g, &st, k, 0.f, keyf, fill, sm, &buf, C, warp, lane, tid);
+                    bisect_leader<VEC, false, false>(row, g, sm, C, &st, k, 0.f, keyf, fill, warp, lane, tid);
                     t = uint32_t(st.lo);
                     if (IS_PROB) {
                         int cnt;
-                        mass_count_ge<VEC, false>(row, g, t, keyf, nullptr, sm, &buf, C, warp, lane, tid, &denom,
-                                                  &cnt, nullptr);
+                        massge_leader<VEC, false>(row, g, sm, C, t, keyf, warp, lane, tid, &denom, &cnt);
                     }
                 }
             }
@@ -154,43 +212,28 @@ __global__ void __launch_bounds__(NT, 4) filter_kernel(const FilterArgs a) {
             } else if (tp <= 0.f) {
                 t = maxkey;
                 int cnt;
-                mass_count_ge<VEC, false>(row, g, t, keyf, nullptr, sm, &buf, C, warp, lane, tid, &denom, &cnt,
-                                          nullptr);
+                massge_leader<VEC, false>(row, g, sm, C, t, keyf, warp, lane, tid, &denom, &cnt);
             } else {
                 Bisect st;
                 st.lo = 0;
                 st.hi = uint64_t(maxkey) + 1;
-                st.cnt_lo = 0;
                 st.mass_lo = M;
-                bisect_run<VEC, false, true>(row, g, &st, 0, tp * M, keyf, 0.f, sm, &buf, C, warp, lane, tid);
+                bisect_leader<VEC, false, true>(row, g, sm, C, &st, 0, tp * M, keyf, 0.f, warp, lane, tid);
                 t = uint32_t(st.lo);
                 denom = st.mass_lo;
             }
         }
     }
 
-    // ---- write this CTA's share of the row
-    const bool vec_out = VEC && ((reinterpret_cast<uintptr_t>(orow) & 15) == 0);
-    visit<TRIP, VEC, false>(
-        row, g, fill, warp, lane, [&](int ls) { return valid && sm.segkey[ls] >= t; },
-        [&](int, int, int base, float4 x, bool on) {
-            float o[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float xv = q_at(x, q);
-                o[q] = (on && keyf(xv) >= t) ? (IS_PROB ? xv / denom : xv) : fill;
-            }
-            if (vec_out && base + 3 < V) {
-                *reinterpret_cast<float4*>(orow + base) = make_float4(o[0], o[1], o[2], o[3]);
-            } else {
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    if (base + q < V) orow[base + q] = o[q];
-            }
-        },
-        [](int, bool) {});
-    if (rank == 0 && tid == 0 && a.out_valid) a.out_valid[b] = valid ? 1 : 0;
-    cluster_sync();  // no CTA leaves while a peer may read its shared memory
+    // ---- everyone writes its share of the row
+    Ctl c{};
+    c.cmd = CMD_WRITE;
+    c.flag = valid ? 1 : 0;
+    c.u[0] = t;
+    c.f[0] = denom;
+    send_command(sm, c, C, tid);
+    write_pass<VEC, KIND>(row, orow, g, sm, valid, t, denom, warp, lane);
+    if (tid == 0 && a.out_valid) a.out_valid[b] = valid ? 1 : 0;
 }
 
 template <int KIND>

@@ -1,25 +1,26 @@
 // Dual-pivot rejection sampler (sm_103a).
 //
-// One thread-block cluster per output row; see fs_device.cuh for the layout.
+// One thread-block cluster per output row; see fs_device.cuh for the execution model.
 // Steps, in the order the pages give them:
-//   pass 1   every CTA reads its share of the row once: per-segment maximum key and
-//            mass, the row total M, the positive count and a NaN/negative flag;
+//   pass 1   every CTA reads its share of the row once; the leader ends up with every
+//            segment's maximum key and mass, the row total M, the positive count and
+//            a NaN/negative flag;
 //   prologue (top-k-first only) the exact k-th largest value t_k and
-//            F_k = mass(x >= t_k) ([explainer] filter order).  Each CTA bounds t_k
-//            from below by the k-th largest of its own segment maxima (any subset's
-//            k-th largest is at most the row's), keeps its elements at or above that
-//            bound, and rank 0 gathers the survivors of the best bound and counts t_k
-//            exactly among them;
+//            F_k = mass(x >= t_k) ([explainer] filter order): a lower bound of t_k from
+//            the segment maxima (the k-th largest of any subset of the row is at most
+//            the row's), the elements at or above it gathered from the few segments
+//            that can hold them, and t_k counted exactly among them;
 //   rounds   ([blog] dual-pivot rejection sampling) draw j by inverse transform over
 //            {p > low}, pivot1 = p_j, pivot2 = (pivot1 + high) / 2, one fused
 //            reduction of (mass, count) above both pivots, then accept j, or
 //            (low, high) <- (pivot1, pivot2), or low <- pivot2.
-// While many tokens lie above `low` a round visits only segments whose maximum is
-// above pivot1 (read again through L2); once at most CAP tokens are left they are
-// gathered, in index order, into rank 0's shared memory and the remaining rounds run
-// there on one warp, with no further cluster traffic.
+// While many tokens lie above `low`, a round's reduction runs on the whole cluster
+// over the segments whose maximum exceeds pivot1 (read again through L2); once at most
+// CAP tokens are left, the leader gathers them in index order and finishes alone on
+// one warp.
 #include "fs_device.cuh"
 #include "fs_host.h"
+#include "topk_bound.cuh"
 
 namespace fsd {
 
@@ -57,28 +58,45 @@ struct Pred {
     }
 };
 
-// Rank 0 takes over the lists of all ranks (u[cnt_idx] of the last exchange holds
-// their lengths), keeping keys >= keep; then the cluster barrier after which the
-// other CTAs may leave.  Returns the list length on rank 0.
-__device__ __forceinline__ int handoff_to_rank0(const Smem& sm, int C, int rank, int cnt_idx, uint32_t keep,
-                                                int warp, int lane, int tid) {
-    int n = 0;
-    if (rank == 0) n = gather_lists(sm, C, cnt_idx, keep, KeyProb(), warp, lane, tid);
-    cluster_sync();  // the peers' lists have been read
-    return n;
+// The other CTAs: follow the leader's commands until EXIT.
+template <bool VEC>
+FS_NOINLINE __device__ void sample_peer(const float* __restrict__ row, const Geom& g, const Smem& sm, int rank,
+                                        int warp, int lane, int tid) {
+    for (;;) {
+        cluster_sync();  // the command is published
+        const Ctl c = *sm.ctl;
+        if (c.cmd == CMD_PIVOT2) {
+            int c1, c2;
+            pivot_pass<VEC, true>(row, g, sm, false, c.f[0], c.f[1], c.ia, c.ib, warp, lane, &c1, &c2);
+            c1 = block_sum_warp_values(c1, sm.red, warp, lane);
+            c2 = block_sum_warp_values(c2, sm.red, warp, lane);
+            if (tid == 0) {
+                uint32_t* dst = reinterpret_cast<uint32_t*>(&sm.part[rank]);
+                put_leader(dst + 4, uint32_t(c1), false);
+                put_leader(dst + 5, uint32_t(c2), false);
+            }
+        } else if (c.cmd == CMD_BISECT) {
+            const uint64_t hi = uint64_t(c.hi_lo) | (uint64_t(c.hi_hi) << 32);
+            bisect_pass<VEC, true, false>(row, g, sm, false, rank, c.u[3], hi, c.u, KeyProb(), 0.f, warp, lane,
+                                          tid);
+        } else {
+            return;  // CMD_EXIT
+        }
+        cluster_sync();  // the results are in the leader
+    }
 }
 
-// One compact round on rank 0's list (warp-collective): draw, reduce, decide.
+// One compact round on the leader's list (warp-collective): draw, reduce, decide.
 // Returns 1 if accepted (token in *j), 0 to continue, -1 if the list had no token
 // above low (cannot happen while S_low > 0).
-__device__ __forceinline__ int compact_round(const Smem& sm, int n_list, const Pred& f, bool any_filter, float u,
-                                             float& low, float& high, float& S_low, int lane, int* j) {
-    const int e = locate_in_list(sm.lv, n_list, low, u * S_low, lane);
+FS_NOINLINE __device__ int compact_round(const Smem& sm, int n_list, const Pred& f, bool any_filter, float u,
+                                         float* low, float* high, float* S_low, int lane, int* j) {
+    const int e = locate_in_list(sm.lv, n_list, *low, u * *S_low, lane);
     if (e < 0) return -1;
     *j = sm.li[e];
     const float pivot1 = sm.lv[e];
     if (!any_filter) return 1;
-    const float pivot2 = (pivot1 + high) * 0.5f;
+    const float pivot2 = (pivot1 + *high) * 0.5f;
     float M1 = 0.f, M2 = 0.f;
     int C1 = 0, C2 = 0;
     for (int i = lane; i < n_list; i += 32) {
@@ -95,12 +113,12 @@ __device__ __forceinline__ int compact_round(const Smem& sm, int n_list, const P
     C2 = warp_sum_i(C2);
     if (f(C1, M1, pivot1)) return 1;
     if (f(C2, M2, pivot2)) {
-        low = pivot1;
-        high = pivot2;
-        S_low = M1;
+        *low = pivot1;
+        *high = pivot2;
+        *S_low = M1;
     } else {
-        low = pivot2;
-        S_low = M2;
+        *low = pivot2;
+        *S_low = M2;
     }
     return 0;
 }
@@ -111,16 +129,35 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
     const int rank = int(cluster_ctarank());
     const int b = int(cluster_id_x());
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const Layout L(a.nsc);
-    const Smem sm(L);
+    const bool leader = rank == 0;
+    const Smem sm(a.ns);
     const Geom g(a.V, a.shift, a.ns, a.nsc, rank);
-    const int V = a.V;
+    const int V = a.V, ns = a.ns;
     const KeyProb keyf;
 
-    // ---- a1: row map and per-row parameters
+    // ---- a1: row map
     const int r = a.indices ? a.indices[b] : b;
     const bool row_ok = r >= 0 && r < a.batch_in;
     const float* row = a.probs + size_t(row_ok ? r : 0) * size_t(V);
+
+    // ---- a2: pass 1, the only HBM read of the row
+    int pos = 0;
+    bool bad = false;
+    if (row_ok) pass1<VEC, true, true>(row, g, sm, leader, warp, lane, pos, bad);
+    pos = block_sum_warp_values(warp_sum_i(pos), sm.red, warp, lane);
+    const int nbad = block_sum_warp_values(__any_sync(FULL, bad) ? 1 : 0, sm.red, warp, lane);
+    if (tid == 0) {
+        uint32_t* dst = reinterpret_cast<uint32_t*>(&sm.part[rank]);
+        put_leader(dst + 4, uint32_t(pos), leader);
+        put_leader(dst + 5, uint32_t(nbad), leader);
+    }
+    cluster_sync();  // the leader's segment table and parts are complete
+    if (!leader) {
+        sample_peer<VEC>(row, g, sm, rank, warp, lane, tid);
+        return;
+    }
+
+    // ---- leader from here on
     const int k = a.top_k ? a.top_k[b] : 0;
     const float tp = a.top_p ? a.top_p[b] : 1.f;
     const float mp = a.min_p ? a.min_p[b] : 0.f;
@@ -131,117 +168,98 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
     f.m_on = mp > 0.f;
     f.pthr = 0.f;
     f.t32 = 0.f;
-    const bool par_ok = !isnan(tp) && !isnan(mp);
     const bool any_filter = f.k_on || f.p_on || f.m_on;
     const bool kfirst = a.order == 0 && f.k_on;
 
-    // ---- a2: pass 1, the only HBM read of the row
-    int pos = 0;
-    bool bad = false;
-    if (row_ok) pass1<VEC, true, true>(row, g, sm.segkey, sm.mass[0], warp, lane, pos, bad);
-    pos = warp_sum_i(pos);
-    const int wbad = __any_sync(FULL, bad) ? 1 : 0;
-    if (lane == 0) {
-        sm.redi[warp] = pos;
-        sm.redi[NW + warp] = wbad;
-    }
-    __syncthreads();
-
-    // ---- a3 (part 1): local lower bound of t_k and the local candidates
-    uint32_t L0c = 0;
-    int nloc = -1;  // -1: no candidate list from this CTA
-    if (row_ok && kfirst && g.nsc >= k) {
-        L0c = max(1u, kth_in_array(sm.segkey, g.nsc, k, sm, warp, lane, tid));
-        nloc = compact_ge<VEC, true>(row, g, L0c, keyf, 0.f, sm, warp, lane, tid);
-        if (nloc > CAP) nloc = -1;
-    }
-    if (warp == 0) {
-        const int nown = row_ok ? g.nsc : 0;
-        const uint32_t km = ordered_max_u(sm.segkey, nown, lane);
-        const float s = ordered_sum(sm.mass[0], nown, lane);
-        if (lane == 0) {
-            int np = 0, nb = 0;
-#pragma unroll
-            for (int w = 0; w < NW; ++w) {
-                np += sm.redi[w];
-                nb |= sm.redi[NW + w];
-            }
-            sm.slot[0].f[0] = s;
-            sm.slot[0].u[0] = km;
-            sm.slot[0].u[1] = uint32_t(nb);
-            sm.slot[0].u[2] = uint32_t(np);
-            sm.slot[0].u[3] = L0c;
-            sm.slot[0].u[4] = uint32_t(nloc);
-        }
-    }
-    int buf = 0;
-    exchange(sm, buf, C, tid, 13);
-    buf ^= 1;
-    uint32_t maxkey = 0, L0 = 0;
-    float M = 0.f;
-    int npos = 0, ncand = 0;
-    bool any_bad = false, lists_ok = true;
-    float* cm = reinterpret_cast<float*>(sm.misc + 16);  // per-CTA mass above `low`, rank order
-    if (tid < C) cm[tid] = sm.gath[tid].f[0];
+    int npos = 0;
+    bool any_bad = false;
     for (int c = 0; c < C; ++c) {
-        const Slot& s = sm.gath[c];
-        M += s.f[0];
-        maxkey = max(maxkey, s.u[0]);
-        any_bad |= s.u[1] != 0;
-        npos += int(s.u[2]);
-        L0 = max(L0, s.u[3]);
-        const int n = int(s.u[4]);
-        lists_ok = lists_ok && n >= 0;
-        ncand += max(n, 0);
+        npos += int(sm.part[c].u[0]);
+        any_bad |= sm.part[c].u[1] != 0;
     }
-    lists_ok = lists_ok && ncand <= CAP;
-    __syncthreads();
+    float M = 0.f;
+    uint32_t maxkey = 0;
+    if (row_ok) {
+        M = block_ordered_sum(sm.mass[0], ns, sm.red, warp, lane);
+        uint32_t km = 0;
+        for (int i = tid; i < ns; i += NT) km = max(km, sm.segkey[i]);
+        km = warp_max_u(km);
+        if (lane == 0) sm.red[warp] = int(km);
+        __syncthreads();
+        for (int w = 0; w < NW; ++w) maxkey = max(maxkey, uint32_t(sm.red[w]));
+        __syncthreads();
+    }
     const float rowmax = __uint_as_float(maxkey);
-    bool valid = row_ok && par_ok && !any_bad && M > 0.f && M <= 3.402823466e38f;
+    bool valid = row_ok && !isnan(tp) && !isnan(mp) && !any_bad && M > 0.f && M <= 3.402823466e38f;
     if (f.m_on) {
         f.t32 = __double2float_ru(double(mp) * double(rowmax));
         if (!(rowmax >= f.t32)) valid = false;  // S is empty: f(max) = 0
     }
 
+    bool peers = true;  // the other CTAs still wait for commands
+    auto dismiss = [&]() {
+        if (peers) {
+            Ctl c{};
+            c.cmd = CMD_EXIT;
+            send_command(sm, c, C, tid);
+            peers = false;
+        }
+    };
+
     int token = -1, rounds = 0;
     bool accepted = false;
-    bool cluster_live = true;  // all CTAs of the cluster still run in lock-step
-
     if (valid) {
         float low = 0.f, high = rowmax, S_low = M;
-        int cur = 0;            // mass[cur][ls] = mass of segment ls above `low`
+        int cur = 0;            // mass[cur][s] = mass of segment s above `low`
         int count_low = npos;   // tokens above `low`
         int n_list = 0;
         bool compact = false;
         f.pthr = tp * M;
 
-        // ---- a3 (part 2): exact t_k and F_k
+        // ---- a3: top-k-first prologue
         if (kfirst) {
-            if (lists_ok) {
-                const int n = handoff_to_rank0(sm, C, rank, 4, L0, warp, lane, tid);
-                if (rank != 0) return;
-                cluster_live = false;
+            const uint32_t L0 = max(1u, topk_bound(sm, ns, k, 21, warp, lane, tid));
+            const int nlive = live_list(sm, ns, L0, warp, lane);
+            const int n = collect<VEC, true>(row, g, sm, nlive, L0, keyf, 0.f, warp, lane);
+            if (n <= CAP) {
+                dismiss();
                 compact = true;
                 // The list holds every element >= L0, hence every element >= t_k.
                 const uint32_t tk = kth_key_in_list(sm, n, k, keyf, warp, lane, tid);
                 if (warp == 0) {
                     n_list = filter_list_warp(sm, n, tk, keyf, lane);
-                    S_low = ordered_sum(sm.lv, n_list, lane);
+                    float s = 0.f;
+                    for (int i = lane; i < n_list; i += 32) s += sm.lv[i];
+                    S_low = warp_sum(s);
                 }
                 low = 0.f;
             } else {
-                // Too many candidates: exact t_k by bit-pattern bisection over the row.
+                // Too many candidates: t_k by bit-pattern bisection with the cluster.
                 Bisect st;
-                st.lo = L0;  // count(key >= L0) >= k when L0 > 0; count(key >= 0) = V otherwise
+                st.lo = L0;  // count(key >= L0) >= k (L0 = 1 counts every positive one)
                 st.hi = uint64_t(maxkey) + 1;
-                st.cnt_lo = 0;
                 st.mass_lo = 0.f;
-                bisect_run<VEC, true, false>(row, g, &st, k, 0.f, keyf, 0.f, sm, &buf, C, warp, lane, tid);
+                if (npos < k) st.lo = 0;  // fewer positives than k: t_k = 0 keeps them all
+                bisect_leader<VEC, true, false>(row, g, sm, C, &st, k, 0.f, keyf, 0.f, warp, lane, tid);
                 const uint32_t tk = uint32_t(st.lo);
-                mass_count_ge<VEC, true>(row, g, tk, keyf, sm.mass[0], sm, &buf, C, warp, lane, tid, &S_low,
-                                         &count_low, cm);
-                cur = 0;
                 low = tk >= 1u ? __uint_as_float(tk - 1u) : 0.f;  // x > low  <=>  key(x) >= t_k
+                // Per-segment masses above `low` for the draws (both pivots = low).
+                Ctl c{};
+                c.cmd = CMD_PIVOT2;
+                c.f[0] = low;
+                c.f[1] = low;
+                c.ia = 0;
+                c.ib = 1;
+                send_command(sm, c, C, tid);
+                int c1, c2;
+                pivot_pass<VEC, true>(row, g, sm, true, low, low, 0, 1, warp, lane, &c1, &c2);
+                c1 = block_sum_warp_values(c1, sm.red, warp, lane);
+                if (tid == 0) sm.part[0].u[0] = uint32_t(c1);
+                cluster_sync();
+                count_low = 0;
+                for (int cc = 0; cc < C; ++cc) count_low += int(sm.part[cc].u[0]);
+                S_low = block_ordered_sum(sm.mass[0], ns, sm.red, warp, lane);
+                cur = 0;
             }
             f.pthr = tp * S_low;  // top-p inside the k, measured against F_k
         }
@@ -249,24 +267,18 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
         // ---- a4..a7: rejection rounds
         for (int round = 0; round < R_MAX; ++round) {
             if (!compact && count_low <= CAP) {
-                // Few tokens left above `low`: gather them (index order) into rank 0.
+                // Few tokens left above `low`: the leader gathers them and goes on alone.
+                dismiss();
                 const uint32_t thr = prob_key(low) + 1u;
-                const int nl = compact_ge<VEC, true>(row, g, thr, keyf, 0.f, sm, warp, lane, tid);
-                if (tid == 0) sm.slot[buf].u[0] = uint32_t(min(nl, CAP));
-                exchange(sm, buf, C, tid, 9);
-                buf ^= 1;
-                const int n = handoff_to_rank0(sm, C, rank, 0, thr, warp, lane, tid);
-                if (rank != 0) return;
-                cluster_live = false;
+                const int nlive = live_list(sm, ns, thr, warp, lane);
+                n_list = min(CAP, collect<VEC, true>(row, g, sm, nlive, thr, keyf, 0.f, warp, lane));
                 compact = true;
-                n_list = n;
             }
             const float u = sampler_uniform(a.seed, a.offset, uint32_t(b), uint32_t(round));
             if (compact) {
-                // ---- compact rounds: warp 0 of rank 0 on the list
                 if (warp != 0) break;
                 int j = -1;
-                const int st = compact_round(sm, n_list, f, any_filter, u, low, high, S_low, lane, &j);
+                const int st = compact_round(sm, n_list, f, any_filter, u, &low, &high, &S_low, lane, &j);
                 if (st < 0) break;
                 if (st > 0) {
                     accepted = true;
@@ -276,50 +288,27 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
                 }
                 continue;
             }
-
-            // ---- a5: draw.  Owner CTA of the target, then segment, then element.
+            // ---- a5: draw over the leader's segment table, then inside the segment
+            float before;
             const float target = u * S_low;
-            float acc = 0.f, before = 0.f, lastb = 0.f;
-            int owner = -1, lastc = -1;
-            for (int c = 0; c < C; ++c) {
-                const float m = cm[c];
-                if (m > 0.f) {
-                    if (owner < 0 && acc + m > target) {
-                        owner = c;
-                        before = acc;
-                    }
-                    lastc = c;
-                    lastb = acc;
-                }
-                acc += m;
-            }
-            bool force = false;
-            if (owner < 0) {
-                owner = lastc;
-                before = lastb;
-                force = true;
-            }
-            if (owner < 0) break;  // no mass above `low` (cannot happen); uniform
-            if (rank == owner && warp == 0) {
-                const float inf = __int_as_float(0x7f800000);
-                const float t = force ? inf : target - before;
-                float bseg;
-                bool fl;
-                const int ls = locate_segment(sm.mass[cur], g.nsc, t, lane, &bseg, &fl);
-                const float t2 = (force || fl) ? inf : t - bseg;
+            const int s = locate_segment_block(sm.mass[cur], ns, target, sm.red, warp, lane, &before);
+            if (warp == 0) {
                 int jj = -1;
                 float xx = 0.f;
-                if (ls >= 0) locate_in_segment<VEC, true>(row, g, ls, low, t2, lane, &jj, &xx);
+                if (s >= 0) {
+                    const float t2 = (target - before < 0.f) ? 0.f : target - before;
+                    locate_in_segment<VEC, true>(row, g, s, low, t2, lane, &jj, &xx);
+                }
                 if (lane == 0) {
-                    sm.slot[buf].f[0] = xx;
-                    sm.slot[buf].u[0] = uint32_t(jj);
+                    sm.red[32] = jj;
+                    reinterpret_cast<float*>(sm.red)[33] = xx;
                 }
             }
-            exchange(sm, buf, C, tid, 9);
-            buf ^= 1;
-            const int j = int(sm.gath[owner].u[0]);
-            const float pivot1 = sm.gath[owner].f[0];
-            if (j < 0) break;  // uniform: every CTA read the same record
+            __syncthreads();
+            const int j = sm.red[32];
+            const float pivot1 = reinterpret_cast<float*>(sm.red)[33];
+            __syncthreads();
+            if (j < 0) break;
             if (!any_filter) {
                 accepted = true;
                 token = j;
@@ -328,44 +317,32 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
             }
             const float pivot2 = (pivot1 + high) * 0.5f;
 
-            // ---- a6: fused (mass, count) above pivot1 and pivot2
+            // ---- a6: fused (mass, count) above pivot1 and pivot2, on the whole cluster
             const int ia = cur == 0 ? 1 : 0;
             const int ib = cur == 2 ? 1 : 2;
-            int c1 = 0, c2 = 0;
-            pivot_pass<VEC, true>(row, g, sm.segkey, pivot1, pivot2, sm.mass[ia], sm.mass[ib], warp, lane, c1, c2);
-            c1 = warp_sum_i(c1);
-            c2 = warp_sum_i(c2);
-            if (lane == 0) {
-                sm.redi[warp] = c1;
-                sm.redi[NW + warp] = c2;
+            Ctl c{};
+            c.cmd = CMD_PIVOT2;
+            c.f[0] = pivot1;
+            c.f[1] = pivot2;
+            c.ia = ia;
+            c.ib = ib;
+            send_command(sm, c, C, tid);
+            int c1, c2;
+            pivot_pass<VEC, true>(row, g, sm, true, pivot1, pivot2, ia, ib, warp, lane, &c1, &c2);
+            c1 = block_sum_warp_values(c1, sm.red, warp, lane);
+            c2 = block_sum_warp_values(c2, sm.red, warp, lane);
+            if (tid == 0) {
+                sm.part[0].u[0] = uint32_t(c1);
+                sm.part[0].u[1] = uint32_t(c2);
             }
-            __syncthreads();
-            if (warp == 0) {
-                const float t1 = ordered_sum(sm.mass[ia], g.nsc, lane);
-                const float t2 = ordered_sum(sm.mass[ib], g.nsc, lane);
-                if (lane == 0) {
-                    int n1 = 0, n2 = 0;
-#pragma unroll
-                    for (int w = 0; w < NW; ++w) {
-                        n1 += sm.redi[w];
-                        n2 += sm.redi[NW + w];
-                    }
-                    sm.slot[buf].f[0] = t1;
-                    sm.slot[buf].f[1] = t2;
-                    sm.slot[buf].u[0] = uint32_t(n1);
-                    sm.slot[buf].u[1] = uint32_t(n2);
-                }
-            }
-            exchange(sm, buf, C, tid, 10);
-            buf ^= 1;
-            float M1 = 0.f, M2 = 0.f;
+            cluster_sync();  // every part is in
             int C1 = 0, C2 = 0;
-            for (int c = 0; c < C; ++c) {
-                M1 += sm.gath[c].f[0];
-                M2 += sm.gath[c].f[1];
-                C1 += int(sm.gath[c].u[0]);
-                C2 += int(sm.gath[c].u[1]);
+            for (int cc = 0; cc < C; ++cc) {
+                C1 += int(sm.part[cc].u[0]);
+                C2 += int(sm.part[cc].u[1]);
             }
+            const float M1 = block_ordered_sum(sm.mass[ia], ns, sm.red, warp, lane);
+            const float M2 = block_ordered_sum(sm.mass[ib], ns, sm.red, warp, lane);
 
             // ---- a7: the three cases
             if (f(C1, M1, pivot1)) {
@@ -380,22 +357,19 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
                 S_low = M1;
                 count_low = C1;
                 cur = ia;
-                if (tid < C) cm[tid] = sm.gath[tid].f[0];
             } else {
                 low = pivot2;
                 S_low = M2;
                 count_low = C2;
                 cur = ib;
-                if (tid < C) cm[tid] = sm.gath[tid].f[1];
             }
-            __syncthreads();  // cm is read and gath rewritten next round
         }
         if (!accepted) rounds = R_MAX;
     }
 
-    // ---- a8: outputs
-    if (cluster_live) cluster_sync();  // no CTA leaves while a peer may read its shared memory
-    if (rank == 0 && tid == 0) {
+    // ---- a8: outputs (the peers are let go first; warp 0 holds the result)
+    if (peers) dismiss();
+    if (tid == 0) {
         a.out_token[b] = accepted ? token : -1;
         a.out_valid[b] = accepted ? 1 : 0;
         if (a.out_rounds) a.out_rounds[b] = rounds;
