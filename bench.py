@@ -42,7 +42,7 @@ WORKLOAD = ("top-k-first top-k+top-p sampling, B=64, V=151936 fp32 probs = softm
             "z~N(0,3^2), top_k=50, top_p=0.9")
 METRIC = "rows/s (top-k+top-p sample, B=64, V=151936)"
 FALLBACK_HBM_GBS = 6800.0
-SOURCES = ["fs_device.cuh", "topk_bound.cuh", "sampling.cu", "renorm.cu", "api.cu", "fs_host.h"]
+SOURCES = ["fs_device.cuh", "sampling.cu", "renorm.cu", "api.cu", "fs_host.h"]
 
 
 def log(*a):

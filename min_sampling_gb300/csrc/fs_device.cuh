@@ -2,19 +2,19 @@
 //
 // Execution model: one thread-block cluster of C CTAs per row, rank 0 the leader.
 // A row is cut into segments of 128 * 2^shift elements (128 = one float4 per lane of
-// a warp).  Every CTA streams a contiguous share of the segments from HBM exactly
-// once (pass 1), and writes each segment's maximum order key and mass straight into
-// the leader's shared memory (distributed shared memory stores), so that after one
-// cluster barrier the leader holds the whole row's segment table.  From there the
-// leader drives the rest: it finishes alone when little data is left to touch (the
-// top-k candidates, a compact list of surviving tokens), and otherwise sends the
-// other CTAs commands (a two-pivot reduction pass, a three-pivot bisection pass, a
-// masked write) through their shared memory, each command bracketed by two cluster
-// barriers.  Every CTA executes the same sequence of cluster barriers: the peers
-// follow the leader's commands until an EXIT command.
+// a warp); CTA c owns a contiguous range of them.  Every CTA streams its range from
+// HBM exactly once (pass 1), keeps each segment's maximum order key and mass, and
+// also stores them into the leader's shared memory (distributed shared memory
+// stores), together with the CTA's totals and, when a top-k bound is needed, its share
+// of a histogram of the segment maxima (distributed shared memory atomics).  After
+// one cluster barrier the leader holds the row's segment table and totals.  From there
+// it drives the rest with commands written into the other CTAs' shared memory (a
+// candidate collection, a two-pivot reduction, a three-pivot bisection pass, a masked
+// write, exit), each bracketed by two cluster barriers; when little data is left it
+// finishes alone.  Every CTA executes the same sequence of cluster barriers.
 //
-// Code size is kept small on purpose: the work after pass 1 runs once per CTA, from
-// a cold instruction cache, on every SM at the same moment.
+// Code size is kept small on purpose: the work after pass 1 runs once per CTA, from a
+// cold instruction cache, on every SM at the same moment.
 #pragma once
 
 #include <cstdint>
@@ -31,12 +31,13 @@ constexpr int TB = 4;                   // blocks per trip (double-buffered in p
 constexpr int MAX_SEG_SHIFT = 2;        // at most 4 blocks per segment (V <= 2^21)
 constexpr int NS_TARGET = 4096;         // segments per row (longer rows use longer segments)
 constexpr int CAP = 2048;               // compact-list capacity (leader)
+constexpr int HBINS = 1024;             // histogram bins of the top-k bound
 constexpr int R_MAX = 256;              // rejection rounds before a row is invalid
 constexpr int MAX_CLUSTER = 8;
 constexpr unsigned FULL = 0xffffffffu;
 
 // Commands from the leader to the other CTAs of the cluster.
-enum : int { CMD_EXIT = 0, CMD_PIVOT2 = 1, CMD_BISECT = 2, CMD_MASSGE = 3, CMD_WRITE = 4 };
+enum : int { CMD_EXIT = 0, CMD_PIVOT2 = 1, CMD_BISECT = 2, CMD_MASSGE = 3, CMD_WRITE = 4, CMD_COLLECT = 5 };
 
 // ------------------------------------------------------------------ geometry
 
@@ -60,6 +61,7 @@ struct Ctl {
 };
 
 // One CTA's partial results, in the leader's shared memory (one record per rank).
+// Word i < 4 is f[i]; word 4 + i is u[i].
 struct Part {
     float f[4];
     uint32_t u[12];
@@ -67,12 +69,13 @@ struct Part {
 
 // Byte offsets of the dynamic shared-memory carve-up for `ns` segments per row.
 struct Layout {
-    size_t ctl, part, red, segkey, mass0, mass1, mass2, list, lv, li, total;
+    size_t ctl, part, red, misc, segkey, mass0, mass1, mass2, list, lv, li, total;
     __host__ __device__ explicit Layout(int ns) {
         size_t o = 0;
         ctl = o;    o = align16(o + sizeof(Ctl));
         part = o;   o = align16(o + MAX_CLUSTER * sizeof(Part));
         red = o;    o = align16(o + 64 * sizeof(int));
+        misc = o;   o = align16(o + 32 * sizeof(int));
         segkey = o; o = align16(o + size_t(ns) * 4);
         mass0 = o;  o = align16(o + size_t(ns) * 4);
         mass1 = o;  o = align16(o + size_t(ns) * 4);
@@ -90,16 +93,21 @@ struct Smem {
     Ctl* ctl;            // the current command
     Part* part;          // [MAX_CLUSTER] partial results (leader)
     int* red;            // [64] block-reduction scratch
-    uint32_t* segkey;    // [ns] maximum order key per segment (row-wide on the leader)
-    float* mass[3];      // [ns] per-segment masses (row-wide on the leader)
-    int* list;           // [ns+1] live-segment list / offsets (leader)
-    float* lv;           // [CAP] compact list: values (leader)
+    float* cmass;        // [MAX_CLUSTER] per-CTA mass above `low` (leader; misc[0..8))
+    int* misc;           // [32]
+    uint32_t* segkey;    // [ns] maximum order key per segment
+    float* mass[3];      // [ns] per-segment masses
+    int* list;           // [ns+1] live-segment list
+    float* lv;           // [CAP] compact list: values (leader); also the histogram
     int* li;             // [CAP] compact list: token indices (leader)
+    uint32_t* hist;      // [HBINS] aliases lv (used before any list is built)
     __device__ explicit Smem(int ns) {
         const Layout L(ns);
         ctl = reinterpret_cast<Ctl*>(smem_raw + L.ctl);
         part = reinterpret_cast<Part*>(smem_raw + L.part);
         red = reinterpret_cast<int*>(smem_raw + L.red);
+        misc = reinterpret_cast<int*>(smem_raw + L.misc);
+        cmass = reinterpret_cast<float*>(misc);
         segkey = reinterpret_cast<uint32_t*>(smem_raw + L.segkey);
         mass[0] = reinterpret_cast<float*>(smem_raw + L.mass0);
         mass[1] = reinterpret_cast<float*>(smem_raw + L.mass1);
@@ -107,6 +115,7 @@ struct Smem {
         list = reinterpret_cast<int*>(smem_raw + L.list);
         lv = reinterpret_cast<float*>(smem_raw + L.lv);
         li = reinterpret_cast<int*>(smem_raw + L.li);
+        hist = reinterpret_cast<uint32_t*>(lv);
     }
 };
 
@@ -115,14 +124,20 @@ struct Geom {
     int V;
     int shift;     // log2(blocks per segment)
     int ns;        // segments per row
+    int nsc;       // segments per CTA (the last may own fewer)
     int s0, s1;    // this CTA's segments [s0, s1)
-    __device__ Geom(int V_, int shift_, int ns_, int nsc, int rank) : V(V_), shift(shift_), ns(ns_) {
+    __device__ Geom(int V_, int shift_, int ns_, int nsc_, int rank) : V(V_), shift(shift_), ns(ns_), nsc(nsc_) {
         s0 = min(ns, rank * nsc);
         s1 = min(ns, s0 + nsc);
     }
     __device__ int seg_it() const { return 1 << shift; }
     // First element of block `it` of segment `s`, as seen by `lane`.
     __device__ int base(int s, int it, int lane) const { return ((s << shift) + it) * BLK + lane * 4; }
+    // The segment range of rank c.
+    __device__ void range_of(int c, int& a, int& b) const {
+        a = min(ns, c * nsc);
+        b = min(ns, a + nsc);
+    }
 };
 
 // ------------------------------------------------------------------ cluster PTX
@@ -144,11 +159,19 @@ __device__ __forceinline__ uint32_t cluster_id_x() {
 }
 // Hardware cluster barrier with release/acquire ordering of shared memory at cluster
 // scope.  Every thread of every CTA of the cluster must reach it; it also acts as a
-// CTA-wide barrier.
-__device__ __forceinline__ void cluster_sync() {
+// CTA-wide barrier.  The split form (arrive ... wait) lets independent work run
+// between the two halves.
+__device__ __forceinline__ void cluster_arrive() {
     __syncwarp();
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    __syncwarp();
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+    cluster_arrive();
+    cluster_wait();
 }
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -161,13 +184,21 @@ __device__ __forceinline__ uint32_t map_rank(uint32_t saddr, uint32_t rank) {
 __device__ __forceinline__ void st_dsmem_u32(uint32_t addr, uint32_t v) {
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
-// Store a word into the leader's copy of a shared-memory location (local store on the
-// leader itself).
+// Store a word into the leader's copy of a shared-memory location (a local store on
+// the leader itself).
 __device__ __forceinline__ void put_leader(void* local_addr, uint32_t v, bool leader) {
     if (leader) {
         *reinterpret_cast<uint32_t*>(local_addr) = v;
     } else {
         st_dsmem_u32(map_rank(smem_u32(local_addr), 0), v);
+    }
+}
+// Add 1 to a counter in the leader's shared memory.
+__device__ __forceinline__ void inc_leader(uint32_t* local_addr, bool leader) {
+    if (leader) {
+        atomicAdd(local_addr, 1u);
+    } else {
+        asm volatile("red.shared::cluster.add.u32 [%0], 1;" ::"r"(map_rank(smem_u32(local_addr), 0)) : "memory");
     }
 }
 
@@ -239,23 +270,12 @@ __device__ __forceinline__ void warp_range(int n, int w, int& r0, int& r1) {
     r1 = min(n, r0 + per);
 }
 
-// Sum of a[0..n) in a fixed order, by the whole CTA: warp w sums its contiguous range
-// (lane-strided, then a tree), the NW range sums are added in warp order.  Every
-// thread gets the same value.  Uses red[0..NW) and two CTA barriers.
-FS_NOINLINE __device__ inline float block_ordered_sum(const float* a, int n, int* red, int warp, int lane) {
-    int r0, r1;
-    warp_range(n, warp, r0, r1);
+// Sum of a[a0..a1) in a fixed order by one warp: lane-strided, then a tree.
+// Identical in all lanes.
+__device__ __forceinline__ float warp_ordered_sum(const float* a, int a0, int a1, int lane) {
     float acc = 0.f;
-    for (int i = r0 + lane; i < r1; i += 32) acc += a[i];
-    acc = warp_sum(acc);
-    float* rf = reinterpret_cast<float*>(red);
-    if (lane == 0) rf[warp] = acc;
-    __syncthreads();
-    float s = 0.f;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) s += rf[w];
-    __syncthreads();
-    return s;
+    for (int i = a0 + lane; i < a1; i += 32) acc += a[i];
+    return warp_sum(acc);
 }
 
 // Block-wide sum of a per-warp value (each warp passes its warp-uniform value);
@@ -319,14 +339,14 @@ __device__ __forceinline__ float sampler_uniform(unsigned long long seed, unsign
 // ------------------------------------------------------------------ pass 1
 
 // One streaming pass over this CTA's segments.  Warp w takes a contiguous range of
-// them and reads it in trips of TB blocks with the next trip's loads in flight while
-// the current trip is reduced.  For every segment: the maximum order key and (PROB)
-// the mass, stored locally (segment key) and into the leader's table.  Per lane: the
-// positive count and a bad-value flag (NaN or negative for probabilities, NaN for
-// logits).
+// them and reads it in trips of TB blocks, the next trip's loads in flight while the
+// current trip is reduced.  For every segment: the maximum order key and (PROB) the
+// mass, into this CTA's table.  Per lane: the positive count and a bad-value flag (NaN
+// or negative for probabilities, NaN for logits).  Touches no other CTA, so it may run
+// before the cluster's first barrier completes.
 template <bool VEC, bool NC, bool PROB>
-__device__ __forceinline__ void pass1(const float* __restrict__ row, const Geom& g, const Smem& sm, bool leader,
-                                      int warp, int lane, int& pos, bool& bad) {
+__device__ __forceinline__ void pass1(const float* __restrict__ row, const Geom& g, const Smem& sm, int warp,
+                                      int lane, int& pos, bool& bad) {
     int r0, r1;
     warp_range(g.s1 - g.s0, warp, r0, r1);
     r0 += g.s0;
@@ -387,20 +407,71 @@ __device__ __forceinline__ void pass1(const float* __restrict__ row, const Geom&
                 kk = mine ? max(kk, km[j]) : kk;
             }
             sm.segkey[sg] = kk;
-            if (!leader) put_leader(&sm.segkey[sg], kk, false);
-            if (PROB) put_leader(&sm.mass[0][sg], __float_as_uint(ss), leader);
+            if (PROB) sm.mass[0][sg] = ss;
         }
 #pragma unroll
         for (int j = 0; j < TB; ++j) A[j] = Bv[j];
     }
 }
 
+// After pass 1 and the cluster barrier that follows it, every CTA: its segments'
+// keys and (prob) masses into the leader's table, its totals into the leader's
+// part[rank] (f[0] ordered mass of its segments, u[0] positive count, u[1] bad flag,
+// u[2] maximum key) and, if `hist_shift` >= 0, one histogram count per segment maximum
+// into the leader's histogram (key >> hist_shift), which the leader cleared before
+// that barrier.  Block-collective.
+FS_NOINLINE __device__ inline void pass1_totals(const Geom& g, const Smem& sm, bool leader, int rank, int pos,
+                                                bool bad, int hist_shift, bool prob, int warp, int lane,
+                                                int tid) {
+    __syncthreads();  // the table written by pass 1
+    pos = warp_sum_i(pos);
+    const int b = __any_sync(FULL, bad) ? 1 : 0;
+    uint32_t km = 0;
+    for (int i = g.s0 + tid; i < g.s1; i += NT) {
+        const uint32_t key = sm.segkey[i];
+        km = max(km, key);
+        if (hist_shift >= 0) inc_leader(&sm.hist[min(uint32_t(HBINS - 1), key >> hist_shift)], leader);
+        if (!leader) {
+            put_leader(&sm.segkey[i], key, false);
+            if (prob) put_leader(&sm.mass[0][i], __float_as_uint(sm.mass[0][i]), false);
+        }
+    }
+    km = warp_max_u(km);
+    float* rf = reinterpret_cast<float*>(sm.red);
+    if (lane == 0) {
+        sm.red[warp] = pos;
+        sm.red[NW + warp] = b;
+        sm.red[2 * NW + warp] = int(km);
+    }
+    if (warp == 0) {
+        const float s = prob ? warp_ordered_sum(sm.mass[0], g.s0, g.s1, lane) : 0.f;
+        if (lane == 0) rf[3 * NW] = s;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int p = 0, nb = 0;
+        uint32_t mk = 0;
+        for (int w = 0; w < NW; ++w) {
+            p += sm.red[w];
+            nb |= sm.red[NW + w];
+            mk = max(mk, uint32_t(sm.red[2 * NW + w]));
+        }
+        uint32_t* dst = reinterpret_cast<uint32_t*>(&sm.part[rank]);
+        put_leader(dst + 0, __float_as_uint(rf[3 * NW]), leader);
+        put_leader(dst + 4, uint32_t(p), leader);
+        put_leader(dst + 5, uint32_t(nb), leader);
+        put_leader(dst + 6, mk, leader);
+    }
+}
+
 // The rejection round's fused reduction ([blog] dual pivot) over this CTA's segments
-// whose maximum exceeds p1: per segment the mass above p1 and above p2 (stored into
-// the leader's mass[ia] / mass[ib]; zero for skipped segments); per lane the counts.
+// whose maximum exceeds p1: per segment the mass above p1 and above p2 (local and in
+// the leader's mass[ia] / mass[ib]; zero for skipped segments); the CTA's ordered
+// sums and counts into the leader's part[rank] (f[0], f[1], u[0], u[1]).
+// Block-collective.
 template <bool VEC, bool NC>
 FS_NOINLINE __device__ void pivot_pass(const float* __restrict__ row, const Geom& g, const Smem& sm, bool leader,
-                                       float p1, float p2, int ia, int ib, int warp, int lane, int* c1o, int* c2o) {
+                                       int rank, float p1, float p2, int ia, int ib, int warp, int lane, int tid) {
     int r0, r1;
     warp_range(g.s1 - g.s0, warp, r0, r1);
     r0 += g.s0;
@@ -453,21 +524,49 @@ FS_NOINLINE __device__ void pivot_pass(const float* __restrict__ row, const Geom
                 sa += mine ? a[j] : 0.f;
                 sb += mine ? b[j] : 0.f;
             }
-            put_leader(&sm.mass[ia][sg], __float_as_uint(sa), leader);
-            put_leader(&sm.mass[ib][sg], __float_as_uint(sb), leader);
+            sm.mass[ia][sg] = sa;
+            sm.mass[ib][sg] = sb;
+            if (!leader) {
+                put_leader(&sm.mass[ia][sg], __float_as_uint(sa), false);
+                put_leader(&sm.mass[ib][sg], __float_as_uint(sb), false);
+            }
         }
     }
-    *c1o = warp_sum_i(c1);
-    *c2o = warp_sum_i(c2);
+    c1 = warp_sum_i(c1);
+    c2 = warp_sum_i(c2);
+    if (lane == 0) {
+        sm.red[warp] = c1;
+        sm.red[NW + warp] = c2;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const float t1 = warp_ordered_sum(sm.mass[ia], g.s0, g.s1, lane);
+        const float t2 = warp_ordered_sum(sm.mass[ib], g.s0, g.s1, lane);
+        if (lane == 0) {
+            int n1 = 0, n2 = 0;
+            for (int w = 0; w < NW; ++w) {
+                n1 += sm.red[w];
+                n2 += sm.red[NW + w];
+            }
+            uint32_t* dst = reinterpret_cast<uint32_t*>(&sm.part[rank]);
+            put_leader(dst + 0, __float_as_uint(t1), leader);
+            put_leader(dst + 1, __float_as_uint(t2), leader);
+            put_leader(dst + 4, uint32_t(n1), leader);
+            put_leader(dst + 5, uint32_t(n2), leader);
+        }
+    }
+    __syncthreads();
 }
 
-// ------------------------------------------------------------------ leader-side helpers
+// ------------------------------------------------------------------ candidate lists
 
-// Ordered list of the segments s in [0, ns) with segkey[s] >= thr, into list[0..n).
+// Ordered list of the segments s in [a, b) with segkey[s] >= thr, into list[0..n).
 // Block-collective; returns n.
-FS_NOINLINE __device__ inline int live_list(const Smem& sm, int ns, uint32_t thr, int warp, int lane) {
+FS_NOINLINE __device__ inline int live_list(const Smem& sm, int a, int b, uint32_t thr, int warp, int lane) {
     int r0, r1;
-    warp_range(ns, warp, r0, r1);
+    warp_range(b - a, warp, r0, r1);
+    r0 += a;
+    r1 += a;
     int cnt = 0;
     for (int base = r0; base < r1; base += 32) {
         const int i = base + lane;
@@ -492,15 +591,15 @@ FS_NOINLINE __device__ inline int live_list(const Smem& sm, int ns, uint32_t thr
     return total;
 }
 
-// Leader: read the listed segments (list[0..nlive), in order) and collect, in index
-// order, every element with key >= thr into lv/li.  Returns the exact count (the
-// list holds at most CAP; more means overflow).  Each warp takes TB blocks of listed
-// segments per batch, so a batch is one L2 round trip.  Block-collective.
-template <bool VEC, bool NC, typename KEYF>
-FS_NOINLINE __device__ int collect(const float* __restrict__ row, const Geom& g, const Smem& sm, int nlive,
-                                   uint32_t thr, KEYF keyf, float fill, int warp, int lane) {
+// Read the listed segments (list[0..nlive), in order) and emit, in index order, every
+// element with key >= thr: out(p, value, index) for p = 0, 1, ...  Returns the exact
+// count.  Each warp takes 8 blocks of listed segments per batch, so a batch is one L2
+// round trip.  Block-collective.
+template <bool VEC, bool NC, typename KEYF, typename OUT>
+__device__ __forceinline__ int collect(const float* __restrict__ row, const Geom& g, const Smem& sm, int nlive,
+                                       uint32_t thr, KEYF keyf, float fill, int warp, int lane, OUT out) {
     constexpr int CB = 8;              // blocks per warp per batch
-    const int spw = CB >> g.shift;   // listed segments per warp per batch
+    const int spw = CB >> g.shift;     // listed segments per warp per batch
     const int mask = g.seg_it() - 1;
     int total = 0;
     for (int b0 = 0; b0 < nlive; b0 += NW * spw) {
@@ -520,7 +619,8 @@ FS_NOINLINE __device__ int collect(const float* __restrict__ row, const Geom& g,
             if (li < nlive) {
                 const int base = g.base(sm.list[li], j & mask, lane);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) c += __popc(__ballot_sync(FULL, keyf(q_at(v[j], q)) >= thr && base + q < g.V));
+                for (int q = 0; q < 4; ++q)
+                    c += __popc(__ballot_sync(FULL, keyf(q_at(v[j], q)) >= thr && base + q < g.V));
             }
         }
         if (lane == 0) sm.red[warp] = c;
@@ -549,10 +649,7 @@ FS_NOINLINE __device__ int collect(const float* __restrict__ row, const Geom& g,
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     if (keep[q]) {
-                        if (p < CAP) {
-                            sm.lv[p] = q_at(v[j], q);
-                            sm.li[p] = base + q;
-                        }
+                        out(p, q_at(v[j], q), base + q);
                         ++p;
                     }
                 }
@@ -563,6 +660,75 @@ FS_NOINLINE __device__ int collect(const float* __restrict__ row, const Geom& g,
     }
     __syncthreads();
     return total;
+}
+
+// Every CTA: collect its own elements with key >= thr into its region of the leader's
+// list (entries [rank * rc, rank * rc + rc)), in index order; the exact count goes to
+// part[rank].u[4] of every CTA of the cluster, so that after the next cluster barrier
+// each CTA can tell whether all regions fit.  Block-collective.
+template <bool VEC, bool NC, typename KEYF>
+FS_NOINLINE __device__ void collect_own(const float* __restrict__ row, const Geom& g, const Smem& sm, bool leader,
+                                        int rank, int C, int rc, uint32_t thr, KEYF keyf, float fill, int warp,
+                                        int lane, int tid) {
+    const int nlive = live_list(sm, g.s0, g.s1, thr, warp, lane);
+    const int base = rank * rc;
+    const int n = collect<VEC, NC>(row, g, sm, nlive, thr, keyf, fill, warp, lane, [&](int p, float x, int ix) {
+        if (p < rc) {
+            put_leader(&sm.lv[base + p], __float_as_uint(x), leader);
+            put_leader(&sm.li[base + p], uint32_t(ix), leader);
+        }
+    });
+    if (tid < C) {
+        uint32_t* dst = reinterpret_cast<uint32_t*>(&sm.part[rank]) + 8;
+        if (tid == rank) {
+            *dst = uint32_t(n);
+        } else {
+            st_dsmem_u32(map_rank(smem_u32(dst), uint32_t(tid)), uint32_t(n));
+        }
+    }
+}
+
+// After the barrier that follows collect_own: whether every rank's candidates fit in
+// its region.  Any CTA (each holds every count).
+__device__ __forceinline__ bool regions_fit(const Smem& sm, int C, int rc) {
+    bool fits = true;
+    for (int r = 0; r < C; ++r) fits = fits && int(sm.part[r].u[4]) <= rc;
+    return fits;
+}
+__device__ __forceinline__ int regions_total(const Smem& sm, int C) {
+    int n = 0;
+    for (int r = 0; r < C; ++r) n += int(sm.part[r].u[4]);
+    return n;
+}
+
+// Leader: the candidate regions of all ranks, concatenated in rank order at the front
+// of lv/li.  Returns the total (the caller checked that every region fit).  Regions
+// move only towards the front, and every thread reads its entries before any write.
+FS_NOINLINE __device__ inline int join_regions(const Smem& sm, int C, int rc, int tid) {
+    int dst = 0;
+    for (int c = 0; c < C; ++c) {
+        const int n = int(sm.part[c].u[4]);
+        const int src = c * rc;
+        if (src != dst) {
+            for (int e0 = 0; e0 < n; e0 += NT) {
+                const int e = e0 + tid;
+                float v = 0.f;
+                int ix = 0;
+                if (e < n) {
+                    v = sm.lv[src + e];
+                    ix = sm.li[src + e];
+                }
+                __syncthreads();
+                if (e < n) {
+                    sm.lv[dst + e] = v;
+                    sm.li[dst + e] = ix;
+                }
+                __syncthreads();
+            }
+        }
+        dst += n;
+    }
+    return dst;
 }
 
 // Largest key t among the keys of lv[0..n) with #{key >= t} >= k; 0 if none.
@@ -608,6 +774,54 @@ FS_NOINLINE __device__ int filter_list_warp(const Smem& sm, int n, uint32_t t, K
         w += __popc(bal);
     }
     return w;
+}
+
+// Leader, block-collective: a lower bound L0 <= t_k of the row's k-th largest order
+// key from the histogram of the segment maxima (key >> bshift).  Scanning from the
+// top bin down, the bin in which the count reaches k holds the k-th largest segment
+// maximum, and its lower edge is at most that value.  The k-th largest of any subset
+// of the row (here, the segment maxima) is at most the row's own k-th largest, so
+// L0 <= t_k, and every segment holding an element >= t_k has its maximum >= L0.
+// Returns 0 when there are fewer than k segments.
+FS_NOINLINE __device__ inline uint32_t hist_bound(const Smem& sm, int ns, int k, int bshift, int warp, int lane,
+                                                  int tid) {
+    if (ns < k) return 0;
+    // Thread t owns positions 4t..4t+3 counted from the top bin (bins HBINS-1-pos).
+    uint32_t c[4];
+    uint32_t own = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        c[q] = sm.hist[HBINS - 1 - (4 * tid + q)];
+        own += c[q];
+    }
+    uint32_t incl = own;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t o = __shfl_up_sync(FULL, incl, d);
+        if (lane >= d) incl += o;
+    }
+    if (lane == 31) sm.red[warp] = int(incl);
+    __syncthreads();
+    uint32_t before = incl - own;
+    for (int w = 0; w < warp; ++w) before += uint32_t(sm.red[w]);
+    const uint32_t kk = uint32_t(k);
+    if (before < kk && before + own >= kk) {
+        uint32_t cum = before;
+        int pos = 4 * tid;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            cum += c[q];
+            if (cum >= kk) {
+                pos = 4 * tid + q;
+                break;
+            }
+        }
+        sm.red[NW] = HBINS - 1 - pos;
+    }
+    __syncthreads();
+    const uint32_t bin = uint32_t(sm.red[NW]);
+    __syncthreads();
+    return bin << bshift;
 }
 
 // ------------------------------------------------------------------ draws
@@ -671,86 +885,31 @@ FS_NOINLINE __device__ void locate_in_segment(const float* __restrict__ row, con
     *x_out = last_x;
 }
 
-// The segment holding target t in the running mass over mass[0..n), by the whole CTA:
-// warp range sums (the same grouping block_ordered_sum uses), the range holding t,
-// then the segment inside it.  If no running mass exceeds t (rounding), the last
-// segment with positive mass.  Returns the segment and the mass before it; every
-// thread gets them.  Block-collective.
-FS_NOINLINE __device__ inline int locate_segment_block(const float* mass, int n, float t, int* red, int warp,
-                                                       int lane, float* before_out) {
-    int r0, r1;
-    warp_range(n, warp, r0, r1);
-    float acc = 0.f;
-    for (int i = r0 + lane; i < r1; i += 32) acc += mass[i];
-    acc = warp_sum(acc);
-    float* rf = reinterpret_cast<float*>(red);
-    if (lane == 0) rf[warp] = acc;
-    __syncthreads();
-    int res = -1;
-    float before = 0.f;
-    if (warp == 0) {
-        // Range holding t (guarded: the last range with positive mass).
-        float run = 0.f, lastb = 0.f;
-        int w_hit = -1, w_last = -1;
-        for (int w = 0; w < NW; ++w) {
-            const float m = rf[w];
-            if (m > 0.f) {
-                if (w_hit < 0 && run + m > t) {
-                    w_hit = w;
-                    before = run;
-                }
-                w_last = w;
-                lastb = run;
-            }
-            run += m;
+// First segment in [a, b) whose running mass over mass[] exceeds t (the mass before
+// it in *before); if none, the last segment with positive mass.  Warp-collective.
+FS_NOINLINE __device__ inline int locate_segment(const float* mass, int a, int b, float t, int lane, float* before) {
+    float run = 0.f;
+    int last = -1;
+    float last_before = 0.f;
+    for (int base = a; base < b; base += 32) {
+        const float m = (base + lane < b) ? mass[base + lane] : 0.f;
+        const float incl = warp_incl_scan(m, lane);
+        const unsigned hit = __ballot_sync(FULL, m > 0.f && run + incl > t);
+        const unsigned nz = __ballot_sync(FULL, m > 0.f);
+        if (nz) {
+            const int l = 31 - __clz(nz);
+            last = base + l;
+            last_before = run + __shfl_sync(FULL, incl - m, l);
         }
-        bool force = false;
-        if (w_hit < 0) {
-            w_hit = w_last;
-            before = lastb;
-            force = true;
+        if (hit) {
+            const int l = __ffs(hit) - 1;
+            *before = run + __shfl_sync(FULL, incl - m, l);
+            return base + l;
         }
-        if (w_hit >= 0) {
-            int a0, a1;
-            warp_range(n, w_hit, a0, a1);
-            float tt = force ? __int_as_float(0x7f800000) : t - before;
-            float r = 0.f;
-            int last = -1;
-            float last_before = 0.f;
-            for (int base = a0; base < a1; base += 32) {
-                const float m = (base + lane < a1) ? mass[base + lane] : 0.f;
-                const float incl = warp_incl_scan(m, lane);
-                const unsigned hit = __ballot_sync(FULL, m > 0.f && r + incl > tt);
-                const unsigned nz = __ballot_sync(FULL, m > 0.f);
-                if (nz) {
-                    const int l = 31 - __clz(nz);
-                    last = base + l;
-                    last_before = r + __shfl_sync(FULL, incl - m, l);
-                }
-                if (hit) {
-                    const int l = __ffs(hit) - 1;
-                    res = base + l;
-                    before += r + __shfl_sync(FULL, incl - m, l);
-                    break;
-                }
-                r += __shfl_sync(FULL, incl, 31);
-            }
-            if (res < 0) {
-                res = last;
-                before += last_before;
-            }
-        }
-        if (lane == 0) {
-            red[NW] = res;
-            rf[NW + 1] = before;
-        }
+        run += __shfl_sync(FULL, incl, 31);
     }
-    __syncthreads();
-    res = red[NW];
-    before = rf[NW + 1];
-    __syncthreads();
-    *before_out = before;
-    return res;
+    *before = last_before;
+    return last;
 }
 
 // Locate inside a compact list lv[0..n) (index order), eligible x > low.  Warp-collective.
@@ -980,12 +1139,16 @@ FS_NOINLINE __device__ void massge_pass(const float* __restrict__ row, const Geo
         put_leader(dst, __float_as_uint(a), leader);
         put_leader(dst + 4, uint32_t(n), leader);
     }
+    __syncthreads();
 }
 
-// Leader: one bisection step after all parts are in.  Updates the interval; returns
-// nothing (the state is replicated in the caller's registers on the leader only).
+// Interval of a threshold search over order keys ([drill] sections 2-3: bisection on a
+// monotone count or mass, done on the integer bit pattern so that it ends exactly on
+// an existing value).  Invariant: crit(lo) holds and crit(hi) does not, where
+// crit(t) = count(key >= t) >= k  or  mass(key >= t) >= target.  Done when
+// hi = lo + 1; then lo is the threshold.
 struct Bisect {
-    uint64_t lo, hi;   // crit(lo) holds, crit(hi) does not; done when hi = lo + 1
+    uint64_t lo, hi;
     float mass_lo;     // mass(key >= lo) (probabilities)
 };
 
@@ -1099,6 +1262,52 @@ FS_NOINLINE __device__ void massge_leader(const float* __restrict__ row, const G
     __syncthreads();
     *mass_out = m;
     *cnt_out = n;
+}
+
+// Leader alone: every element of the row with key >= thr into lv/li[0..n) in index
+// order, read through the leader's full segment table.  Returns the exact count
+// (entries beyond CAP are dropped).  Block-collective.
+template <bool VEC, bool NC, typename KEYF>
+FS_NOINLINE __device__ int collect_all(const float* __restrict__ row, const Geom& g, const Smem& sm, uint32_t thr,
+                                       KEYF keyf, float fill, int warp, int lane) {
+    const int nlive = live_list(sm, 0, g.ns, thr, warp, lane);
+    return collect<VEC, NC>(row, g, sm, nlive, thr, keyf, fill, warp, lane, [&](int p, float x, int ix) {
+        if (p < CAP) {
+            sm.lv[p] = x;
+            sm.li[p] = ix;
+        }
+    });
+}
+
+// Leader: every element with key >= thr, in index order, into lv/li[0..n).  The whole
+// cluster collects (each CTA its own segments, into its region of the leader's list);
+// if a region overflowed but the total fits, the leader collects alone.  Returns n, or
+// -1 when more than CAP elements qualify (the peers then still wait for commands).
+// With `exit_if_fit` the peers leave once the list is complete (*peers = false).
+template <bool VEC, bool NC, typename KEYF>
+FS_NOINLINE __device__ int gather_leader(const float* __restrict__ row, const Geom& g, const Smem& sm, int C,
+                                         uint32_t thr, KEYF keyf, float fill, bool exit_if_fit, bool* peers,
+                                         int warp, int lane, int tid) {
+    const int rc = CAP / C;
+    Ctl c{};
+    c.cmd = CMD_COLLECT;
+    c.flag = exit_if_fit ? 1 : 0;
+    c.u[0] = thr;
+    send_command(sm, c, C, tid);
+    collect_own<VEC, NC>(row, g, sm, true, 0, C, rc, thr, keyf, fill, warp, lane, tid);
+    cluster_sync();  // every region and count is in
+    if (regions_fit(sm, C, rc)) {
+        if (exit_if_fit) *peers = false;
+        return join_regions(sm, C, rc, tid);
+    }
+    if (regions_total(sm, C) > CAP) return -1;
+    if (exit_if_fit) {
+        Ctl e{};
+        e.cmd = CMD_EXIT;
+        send_command(sm, e, C, tid);
+        *peers = false;
+    }
+    return collect_all<VEC, NC>(row, g, sm, thr, keyf, fill, warp, lane);
 }
 
 }  // namespace fsd

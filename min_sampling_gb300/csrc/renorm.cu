@@ -5,10 +5,11 @@
 // ([drill] sections 2-4: the largest t with count(key >= t) >= k, or with
 // mass(key >= t) >= top_p * M), then writes the row once.  One cluster per row:
 //   pass 1   one HBM read: per-segment maximum key, the row total and a bad flag;
-//   search   top-k: every CTA bounds t from below by the k-th largest of its own
-//            segment maxima and keeps its elements at or above that bound; rank 0
-//            gathers the survivors of the best bound and counts t exactly among them;
-//            a bisection on the key takes over when they do not fit on chip.
+//   search   top-k: a lower bound of t from a histogram of the segment maxima (the
+//            k-th largest of any subset of the row is at most the row's), every CTA's
+//            elements at or above it gathered into rank 0's list, and t counted
+//            exactly among them; a bisection on the key takes over when they do not
+//            fit on chip.
 //            top-p: bisection on the key with three pivots per pass, each interval
 //            shrunk to the keys that exist in it;
 //   write    keep key >= t (x / kept mass, or the logit), else 0 / -inf.  Segments
@@ -17,7 +18,6 @@
 
 #include "fs_device.cuh"
 #include "fs_host.h"
-#include "topk_bound.cuh"
 
 namespace fsd {
 
@@ -87,7 +87,7 @@ FS_NOINLINE __device__ void write_pass(const float* __restrict__ row, float* __r
 // The other CTAs: follow the leader's commands until the write.
 template <bool VEC, int KIND>
 FS_NOINLINE __device__ void filter_peer(const float* __restrict__ row, float* __restrict__ orow, const Geom& g,
-                                        const Smem& sm, int rank, int warp, int lane, int tid) {
+                                        const Smem& sm, int rank, int C, int warp, int lane, int tid) {
     using KEYF = typename std::conditional<KIND == K_MASK, KeyLogit, KeyProb>::type;
     const float fill = KIND == K_MASK ? __int_as_float(0xff800000) : 0.f;
     for (;;) {
@@ -102,6 +102,8 @@ FS_NOINLINE __device__ void filter_peer(const float* __restrict__ row, float* __
         } else if (c.cmd == CMD_WRITE) {
             write_pass<VEC, KIND>(row, orow, g, sm, c.flag != 0, c.u[0], c.f[0], warp, lane);
             return;
+        } else if (c.cmd == CMD_COLLECT) {
+            collect_own<VEC, false>(row, g, sm, false, rank, C, CAP / C, c.u[0], KEYF(), fill, warp, lane, tid);
         } else {
             return;  // CMD_EXIT
         }
@@ -126,43 +128,36 @@ __global__ void __launch_bounds__(NT, 4) filter_kernel(const FilterArgs a) {
     float* orow = a.out + size_t(b) * size_t(V);
     const float fill = IS_PROB ? 0.f : __int_as_float(0xff800000);
 
-    // ---- pass 1
+    const int k = (KIND != K_TOPP) ? a.top_k[b] : 0;
+    const bool k_on = KIND != K_TOPP && k > 0 && k < V;
+    const bool need_hist = k_on && ns >= k;
+
+    // ---- pass 1, inside a split cluster barrier
+    if (leader && need_hist)
+        for (int i = tid; i < HBINS; i += NT) sm.hist[i] = 0u;
+    cluster_arrive();
     int pos = 0;
     bool bad = false;
-    pass1<VEC, false, IS_PROB>(row, g, sm, leader, warp, lane, pos, bad);
-    pos = block_sum_warp_values(warp_sum_i(pos), sm.red, warp, lane);
-    const int nbad = block_sum_warp_values(__any_sync(FULL, bad) ? 1 : 0, sm.red, warp, lane);
-    if (tid == 0) {
-        uint32_t* dst = reinterpret_cast<uint32_t*>(&sm.part[rank]);
-        put_leader(dst + 4, uint32_t(pos), leader);
-        put_leader(dst + 5, uint32_t(nbad), leader);
-    }
-    cluster_sync();  // the leader's segment table and parts are complete
+    pass1<VEC, false, IS_PROB>(row, g, sm, warp, lane, pos, bad);
+    cluster_wait();  // every CTA has started and the leader's histogram is clear
+    pass1_totals(g, sm, leader, rank, pos, bad, need_hist ? (IS_PROB ? 21 : 22) : -1, IS_PROB, warp, lane, tid);
+    cluster_sync();  // the leader's segment table, histogram and parts are complete
     if (!leader) {
-        filter_peer<VEC, KIND>(row, orow, g, sm, rank, warp, lane, tid);
+        filter_peer<VEC, KIND>(row, orow, g, sm, rank, C, warp, lane, tid);
         return;
     }
 
     // ---- leader
-    const int k = (KIND != K_TOPP) ? a.top_k[b] : 0;
     const float tp = (KIND == K_TOPP) ? a.top_p[b] : 1.f;
-    const bool k_on = KIND != K_TOPP && k > 0 && k < V;
     int npos = 0;
     bool any_bad = false;
+    float M = 0.f;
+    uint32_t maxkey = 0;
     for (int c = 0; c < C; ++c) {
         npos += int(sm.part[c].u[0]);
         any_bad |= sm.part[c].u[1] != 0;
-    }
-    const float M = IS_PROB ? block_ordered_sum(sm.mass[0], ns, sm.red, warp, lane) : 0.f;
-    uint32_t maxkey = 0;
-    {
-        uint32_t km = 0;
-        for (int i = tid; i < ns; i += NT) km = max(km, sm.segkey[i]);
-        km = warp_max_u(km);
-        if (lane == 0) sm.red[warp] = int(km);
-        __syncthreads();
-        for (int w = 0; w < NW; ++w) maxkey = max(maxkey, uint32_t(sm.red[w]));
-        __syncthreads();
+        M += sm.part[c].f[0];
+        maxkey = max(maxkey, sm.part[c].u[2]);
     }
     bool valid = !any_bad;
     if (IS_PROB) valid = valid && M > 0.f && M <= 3.402823466e38f;
@@ -173,11 +168,12 @@ __global__ void __launch_bounds__(NT, 4) filter_kernel(const FilterArgs a) {
     if (valid) {
         if (KIND != K_TOPP) {
             if (k_on) {
-                uint32_t L0 = topk_bound(sm, ns, k, IS_PROB ? 21 : 22, warp, lane, tid);
+                uint32_t L0 = need_hist ? hist_bound(sm, ns, k, IS_PROB ? 21 : 22, warp, lane, tid) : 0u;
                 if (IS_PROB) L0 = max(L0, 1u);
-                const int nlive = live_list(sm, ns, L0, warp, lane);
-                const int n = collect<VEC, false>(row, g, sm, nlive, L0, keyf, fill, warp, lane);
-                if (n <= CAP) {
+                bool peers = true;
+                const int n = gather_leader<VEC, false>(row, g, sm, C, L0, keyf, fill, false, &peers, warp, lane,
+                                                        tid);
+                if (n >= 0) {
                     // Every element >= L0 (hence >= t) is in the list.
                     t = kth_key_in_list(sm, n, k, keyf, warp, lane, tid);
                     if (warp == 0) {

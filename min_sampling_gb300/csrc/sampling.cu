@@ -3,13 +3,13 @@
 // One thread-block cluster per output row; see fs_device.cuh for the execution model.
 // Steps, in the order the pages give them:
 //   pass 1   every CTA reads its share of the row once; the leader ends up with every
-//            segment's maximum key and mass, the row total M, the positive count and
-//            a NaN/negative flag;
+//            segment's maximum key and mass, each CTA's mass, the row total M, the
+//            positive count and a NaN/negative flag;
 //   prologue (top-k-first only) the exact k-th largest value t_k and
 //            F_k = mass(x >= t_k) ([explainer] filter order): a lower bound of t_k from
-//            the segment maxima (the k-th largest of any subset of the row is at most
-//            the row's), the elements at or above it gathered from the few segments
-//            that can hold them, and t_k counted exactly among them;
+//            a histogram of the segment maxima (the k-th largest of any subset of the
+//            row is at most the row's), every CTA's elements at or above it gathered
+//            into the leader's list, and t_k counted exactly among them;
 //   rounds   ([blog] dual-pivot rejection sampling) draw j by inverse transform over
 //            {p > low}, pivot1 = p_j, pivot2 = (pivot1 + high) / 2, one fused
 //            reduction of (mass, count) above both pivots, then accept j, or
@@ -20,7 +20,6 @@
 // one warp.
 #include "fs_device.cuh"
 #include "fs_host.h"
-#include "topk_bound.cuh"
 
 namespace fsd {
 
@@ -58,31 +57,27 @@ struct Pred {
     }
 };
 
-// The other CTAs: follow the leader's commands until EXIT.
+// The other CTAs: follow the leader's commands until EXIT (or until a collection that
+// completed the leader's list).
 template <bool VEC>
 FS_NOINLINE __device__ void sample_peer(const float* __restrict__ row, const Geom& g, const Smem& sm, int rank,
-                                        int warp, int lane, int tid) {
+                                        int C, int warp, int lane, int tid) {
     for (;;) {
         cluster_sync();  // the command is published
         const Ctl c = *sm.ctl;
         if (c.cmd == CMD_PIVOT2) {
-            int c1, c2;
-            pivot_pass<VEC, true>(row, g, sm, false, c.f[0], c.f[1], c.ia, c.ib, warp, lane, &c1, &c2);
-            c1 = block_sum_warp_values(c1, sm.red, warp, lane);
-            c2 = block_sum_warp_values(c2, sm.red, warp, lane);
-            if (tid == 0) {
-                uint32_t* dst = reinterpret_cast<uint32_t*>(&sm.part[rank]);
-                put_leader(dst + 4, uint32_t(c1), false);
-                put_leader(dst + 5, uint32_t(c2), false);
-            }
+            pivot_pass<VEC, true>(row, g, sm, false, rank, c.f[0], c.f[1], c.ia, c.ib, warp, lane, tid);
         } else if (c.cmd == CMD_BISECT) {
             const uint64_t hi = uint64_t(c.hi_lo) | (uint64_t(c.hi_hi) << 32);
             bisect_pass<VEC, true, false>(row, g, sm, false, rank, c.u[3], hi, c.u, KeyProb(), 0.f, warp, lane,
                                           tid);
+        } else if (c.cmd == CMD_COLLECT) {
+            collect_own<VEC, true>(row, g, sm, false, rank, C, CAP / C, c.u[0], KeyProb(), 0.f, warp, lane, tid);
         } else {
             return;  // CMD_EXIT
         }
         cluster_sync();  // the results are in the leader
+        if (c.cmd == CMD_COLLECT && c.flag && regions_fit(sm, C, CAP / C)) return;
     }
 }
 
@@ -123,6 +118,44 @@ FS_NOINLINE __device__ int compact_round(const Smem& sm, int n_list, const Pred&
     return 0;
 }
 
+// Inverse-transform draw over the whole row while its tokens are spread over the
+// cluster (warp-collective, leader): the owning CTA from the per-CTA masses cmass[]
+// (summed in rank order, as S_low was), the segment inside the owner's range from
+// mass[cur], then the token inside the segment.  Returns the token, its value in *x.
+template <bool VEC>
+FS_NOINLINE __device__ int draw_full(const float* __restrict__ row, const Geom& g, const Smem& sm, int C, int cur,
+                                     float low, float target, int lane, float* x) {
+    float run = 0.f, before = 0.f, last_before = 0.f;
+    int owner = -1, last = -1;
+    for (int c = 0; c < C; ++c) {
+        const float m = sm.cmass[c];
+        if (m > 0.f) {
+            if (owner < 0 && run + m > target) {
+                owner = c;
+                before = run;
+            }
+            last = c;
+            last_before = run;
+        }
+        run += m;
+    }
+    if (owner < 0) {
+        owner = last;
+        before = last_before;
+    }
+    if (owner < 0) return -1;
+    int a0, a1;
+    g.range_of(owner, a0, a1);
+    float t = target - before;
+    float bs = 0.f;
+    const int s = locate_segment(sm.mass[cur], a0, a1, t, lane, &bs);
+    if (s < 0) return -1;
+    t = (t - bs < 0.f) ? 0.f : t - bs;
+    int j = -1;
+    locate_in_segment<VEC, true>(row, g, s, low, t, lane, &j, x);
+    return j;
+}
+
 template <bool VEC>
 __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
     const int C = int(cluster_nctarank());
@@ -135,66 +168,67 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
     const int V = a.V, ns = a.ns;
     const KeyProb keyf;
 
-    // ---- a1: row map
+    // ---- a1: row map and parameters (every CTA reads them)
     const int r = a.indices ? a.indices[b] : b;
     const bool row_ok = r >= 0 && r < a.batch_in;
     const float* row = a.probs + size_t(row_ok ? r : 0) * size_t(V);
+    const int k = a.top_k ? a.top_k[b] : 0;
+    const bool k_on = k > 0 && k < V;
+    const bool kfirst = a.order == 0 && k_on;
+    const bool need_hist = kfirst && ns >= k;
 
-    // ---- a2: pass 1, the only HBM read of the row
+    // ---- a2: pass 1, the only HBM read of the row, inside a split cluster barrier
+    if (leader && need_hist)
+        for (int i = tid; i < HBINS; i += NT) sm.hist[i] = 0u;
+    cluster_arrive();
     int pos = 0;
     bool bad = false;
-    if (row_ok) pass1<VEC, true, true>(row, g, sm, leader, warp, lane, pos, bad);
-    pos = block_sum_warp_values(warp_sum_i(pos), sm.red, warp, lane);
-    const int nbad = block_sum_warp_values(__any_sync(FULL, bad) ? 1 : 0, sm.red, warp, lane);
-    if (tid == 0) {
-        uint32_t* dst = reinterpret_cast<uint32_t*>(&sm.part[rank]);
-        put_leader(dst + 4, uint32_t(pos), leader);
-        put_leader(dst + 5, uint32_t(nbad), leader);
+    if (row_ok) {
+        pass1<VEC, true, true>(row, g, sm, warp, lane, pos, bad);
+    } else {
+        for (int i = g.s0 + tid; i < g.s1; i += NT) {
+            sm.segkey[i] = 0u;
+            sm.mass[0][i] = 0.f;
+        }
     }
-    cluster_sync();  // the leader's segment table and parts are complete
+    cluster_wait();  // every CTA has started and the leader's histogram is clear
+    pass1_totals(g, sm, leader, rank, pos, bad, need_hist ? 21 : -1, true, warp, lane, tid);
+    cluster_sync();  // the leader's segment table, histogram and parts are complete
     if (!leader) {
-        sample_peer<VEC>(row, g, sm, rank, warp, lane, tid);
+        sample_peer<VEC>(row, g, sm, rank, C, warp, lane, tid);
         return;
     }
 
     // ---- leader from here on
-    const int k = a.top_k ? a.top_k[b] : 0;
     const float tp = a.top_p ? a.top_p[b] : 1.f;
     const float mp = a.min_p ? a.min_p[b] : 0.f;
     Pred f;
-    f.k_on = k > 0 && k < V;
+    f.k_on = k_on;
     f.k = k;
     f.p_on = tp < 1.f;
     f.m_on = mp > 0.f;
     f.pthr = 0.f;
     f.t32 = 0.f;
     const bool any_filter = f.k_on || f.p_on || f.m_on;
-    const bool kfirst = a.order == 0 && f.k_on;
 
     int npos = 0;
     bool any_bad = false;
+    float M = 0.f;           // sum of the per-CTA ordered sums, in rank order
+    uint32_t maxkey = 0;
     for (int c = 0; c < C; ++c) {
         npos += int(sm.part[c].u[0]);
         any_bad |= sm.part[c].u[1] != 0;
+        M += sm.part[c].f[0];
+        maxkey = max(maxkey, sm.part[c].u[2]);
     }
-    float M = 0.f;
-    uint32_t maxkey = 0;
-    if (row_ok) {
-        M = block_ordered_sum(sm.mass[0], ns, sm.red, warp, lane);
-        uint32_t km = 0;
-        for (int i = tid; i < ns; i += NT) km = max(km, sm.segkey[i]);
-        km = warp_max_u(km);
-        if (lane == 0) sm.red[warp] = int(km);
-        __syncthreads();
-        for (int w = 0; w < NW; ++w) maxkey = max(maxkey, uint32_t(sm.red[w]));
-        __syncthreads();
-    }
+    if (tid < C) sm.cmass[tid] = sm.part[tid].f[0];
     const float rowmax = __uint_as_float(maxkey);
     bool valid = row_ok && !isnan(tp) && !isnan(mp) && !any_bad && M > 0.f && M <= 3.402823466e38f;
     if (f.m_on) {
         f.t32 = __double2float_ru(double(mp) * double(rowmax));
         if (!(rowmax >= f.t32)) valid = false;  // S is empty: f(max) = 0
     }
+    __syncthreads();
 
     bool peers = true;  // the other CTAs still wait for commands
     auto dismiss = [&]() {
@@ -218,10 +252,9 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
 
         // ---- a3: top-k-first prologue
         if (kfirst) {
-            const uint32_t L0 = max(1u, topk_bound(sm, ns, k, 21, warp, lane, tid));
-            const int nlive = live_list(sm, ns, L0, warp, lane);
-            const int n = collect<VEC, true>(row, g, sm, nlive, L0, keyf, 0.f, warp, lane);
-            if (n <= CAP) {
+            const uint32_t L0 = max(1u, need_hist ? hist_bound(sm, ns, k, 21, warp, lane, tid) : 0u);
+            const int n = gather_leader<VEC, true>(row, g, sm, C, L0, keyf, 0.f, true, &peers, warp, lane, tid);
+            if (n >= 0) {
                 dismiss();
                 compact = true;
                 // The list holds every element >= L0, hence every element >= t_k.
@@ -243,7 +276,7 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
                 bisect_leader<VEC, true, false>(row, g, sm, C, &st, k, 0.f, keyf, 0.f, warp, lane, tid);
                 const uint32_t tk = uint32_t(st.lo);
                 low = tk >= 1u ? __uint_as_float(tk - 1u) : 0.f;  // x > low  <=>  key(x) >= t_k
-                // Per-segment masses above `low` for the draws (both pivots = low).
+                // Per-segment and per-CTA masses above `low` for the draws (both pivots = low).
                 Ctl c{};
                 c.cmd = CMD_PIVOT2;
                 c.f[0] = low;
@@ -251,14 +284,16 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
                 c.ia = 0;
                 c.ib = 1;
                 send_command(sm, c, C, tid);
-                int c1, c2;
-                pivot_pass<VEC, true>(row, g, sm, true, low, low, 0, 1, warp, lane, &c1, &c2);
-                c1 = block_sum_warp_values(c1, sm.red, warp, lane);
-                if (tid == 0) sm.part[0].u[0] = uint32_t(c1);
+                pivot_pass<VEC, true>(row, g, sm, true, 0, low, low, 0, 1, warp, lane, tid);
                 cluster_sync();
                 count_low = 0;
-                for (int cc = 0; cc < C; ++cc) count_low += int(sm.part[cc].u[0]);
-                S_low = block_ordered_sum(sm.mass[0], ns, sm.red, warp, lane);
+                S_low = 0.f;
+                for (int cc = 0; cc < C; ++cc) {
+                    count_low += int(sm.part[cc].u[0]);
+                    S_low += sm.part[cc].f[0];
+                }
+                if (tid < C) sm.cmass[tid] = sm.part[tid].f[0];
+                __syncthreads();
                 cur = 0;
             }
             f.pthr = tp * S_low;  // top-p inside the k, measured against F_k
@@ -267,11 +302,11 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
         // ---- a4..a7: rejection rounds
         for (int round = 0; round < R_MAX; ++round) {
             if (!compact && count_low <= CAP) {
-                // Few tokens left above `low`: the leader gathers them and goes on alone.
+                // Few tokens left above `low`: gather them; the leader goes on alone.
+                n_list = gather_leader<VEC, true>(row, g, sm, C, prob_key(low) + 1u, keyf, 0.f, true, &peers, warp,
+                                                  lane, tid);
                 dismiss();
-                const uint32_t thr = prob_key(low) + 1u;
-                const int nlive = live_list(sm, ns, thr, warp, lane);
-                n_list = min(CAP, collect<VEC, true>(row, g, sm, nlive, thr, keyf, 0.f, warp, lane));
+                if (n_list < 0) break;
                 compact = true;
             }
             const float u = sampler_uniform(a.seed, a.offset, uint32_t(b), uint32_t(round));
@@ -288,17 +323,10 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
                 }
                 continue;
             }
-            // ---- a5: draw over the leader's segment table, then inside the segment
-            float before;
-            const float target = u * S_low;
-            const int s = locate_segment_block(sm.mass[cur], ns, target, sm.red, warp, lane, &before);
+            // ---- a5: draw (warp 0): owner CTA, segment, token
             if (warp == 0) {
-                int jj = -1;
                 float xx = 0.f;
-                if (s >= 0) {
-                    const float t2 = (target - before < 0.f) ? 0.f : target - before;
-                    locate_in_segment<VEC, true>(row, g, s, low, t2, lane, &jj, &xx);
-                }
+                const int jj = draw_full<VEC>(row, g, sm, C, cur, low, u * S_low, lane, &xx);
                 if (lane == 0) {
                     sm.red[32] = jj;
                     reinterpret_cast<float*>(sm.red)[33] = xx;
@@ -327,22 +355,16 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
             c.ia = ia;
             c.ib = ib;
             send_command(sm, c, C, tid);
-            int c1, c2;
-            pivot_pass<VEC, true>(row, g, sm, true, pivot1, pivot2, ia, ib, warp, lane, &c1, &c2);
-            c1 = block_sum_warp_values(c1, sm.red, warp, lane);
-            c2 = block_sum_warp_values(c2, sm.red, warp, lane);
-            if (tid == 0) {
-                sm.part[0].u[0] = uint32_t(c1);
-                sm.part[0].u[1] = uint32_t(c2);
-            }
+            pivot_pass<VEC, true>(row, g, sm, true, 0, pivot1, pivot2, ia, ib, warp, lane, tid);
             cluster_sync();  // every part is in
             int C1 = 0, C2 = 0;
+            float M1 = 0.f, M2 = 0.f;
             for (int cc = 0; cc < C; ++cc) {
                 C1 += int(sm.part[cc].u[0]);
                 C2 += int(sm.part[cc].u[1]);
+                M1 += sm.part[cc].f[0];
+                M2 += sm.part[cc].f[1];
             }
-            const float M1 = block_ordered_sum(sm.mass[ia], ns, sm.red, warp, lane);
-            const float M2 = block_ordered_sum(sm.mass[ib], ns, sm.red, warp, lane);
 
             // ---- a7: the three cases
             if (f(C1, M1, pivot1)) {
@@ -351,7 +373,8 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
                 rounds = round + 1;
                 break;
             }
-            if (f(C2, M2, pivot2)) {
+            const bool narrow = f(C2, M2, pivot2);
+            if (narrow) {
                 low = pivot1;
                 high = pivot2;
                 S_low = M1;
@@ -363,6 +386,8 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
                 count_low = C2;
                 cur = ib;
             }
+            if (tid < C) sm.cmass[tid] = narrow ? sm.part[tid].f[0] : sm.part[tid].f[1];
+            __syncthreads();
         }
         if (!accepted) rounds = R_MAX;
     }
