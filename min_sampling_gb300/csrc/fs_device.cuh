@@ -30,7 +30,8 @@ constexpr int BLK = 128;                // elements per block (one float4 per la
 constexpr int TB = 4;                   // blocks per trip (double-buffered in pass 1)
 constexpr int MAX_SEG_SHIFT = 2;        // at most 4 blocks per segment (V <= 2^21)
 constexpr int NS_TARGET = 4096;         // segments per row (longer rows use longer segments)
-constexpr int CAP = 2048;               // compact-list capacity (leader)
+constexpr int CAP = 1024;               // compact-list capacity (leader)
+constexpr int SBH = 2;                  // blocks per half of a warp's staging buffer
 constexpr int HBINS = 1024;             // histogram bins of the top-k bound
 constexpr int R_MAX = 256;              // rejection rounds before a row is invalid
 constexpr int MAX_CLUSTER = 8;
@@ -69,7 +70,7 @@ struct Part {
 
 // Byte offsets of the dynamic shared-memory carve-up for `ns` segments per row.
 struct Layout {
-    size_t ctl, part, red, misc, segkey, mass0, mass1, mass2, list, lv, li, total;
+    size_t ctl, part, red, misc, segkey, mass0, mass1, mass2, list, lv, li, stage, total;
     __host__ __device__ explicit Layout(int ns) {
         size_t o = 0;
         ctl = o;    o = align16(o + sizeof(Ctl));
@@ -83,6 +84,7 @@ struct Layout {
         list = o;   o = align16(o + size_t(ns + 1) * 4);
         lv = o;     o = align16(o + size_t(CAP) * 4);
         li = o;     o = align16(o + size_t(CAP) * 4);
+        stage = o;  o = align16(o + size_t(NW) * 2 * SBH * BLK * 4);
         total = o;
     }
 };
@@ -101,6 +103,7 @@ struct Smem {
     float* lv;           // [CAP] compact list: values (leader); also the histogram
     int* li;             // [CAP] compact list: token indices (leader)
     uint32_t* hist;      // [HBINS] aliases lv (used before any list is built)
+    float* stage;        // [NW][2][SBH][BLK] per-warp staging of blocks read from global memory
     __device__ explicit Smem(int ns) {
         const Layout L(ns);
         ctl = reinterpret_cast<Ctl*>(smem_raw + L.ctl);
@@ -116,6 +119,7 @@ struct Smem {
         lv = reinterpret_cast<float*>(smem_raw + L.lv);
         li = reinterpret_cast<int*>(smem_raw + L.li);
         hist = reinterpret_cast<uint32_t*>(lv);
+        stage = reinterpret_cast<float*>(smem_raw + L.stage);
     }
 };
 
@@ -193,12 +197,13 @@ __device__ __forceinline__ void put_leader(void* local_addr, uint32_t v, bool le
         st_dsmem_u32(map_rank(smem_u32(local_addr), 0), v);
     }
 }
-// Add 1 to a counter in the leader's shared memory.
-__device__ __forceinline__ void inc_leader(uint32_t* local_addr, bool leader) {
+// Add n to a counter in the leader's shared memory.
+__device__ __forceinline__ void add_leader(uint32_t* local_addr, uint32_t n, bool leader) {
     if (leader) {
-        atomicAdd(local_addr, 1u);
+        atomicAdd(local_addr, n);
     } else {
-        asm volatile("red.shared::cluster.add.u32 [%0], 1;" ::"r"(map_rank(smem_u32(local_addr), 0)) : "memory");
+        asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(map_rank(smem_u32(local_addr), 0)), "r"(n)
+                     : "memory");
     }
 }
 
@@ -234,6 +239,37 @@ __device__ __forceinline__ float4 load4(const float* __restrict__ row, int V, in
 
 __device__ __forceinline__ float q_at(const float4& v, int q) {
     return q == 0 ? v.x : (q == 1 ? v.y : (q == 2 ? v.z : v.w));
+}
+
+// Asynchronous copies global -> shared (cp.async, completed per thread by
+// cp.async.wait_group).  `bytes` < the copy size zero-fills the rest, and 0 reads
+// nothing; the source address is then the row start, which is always valid.
+__device__ __forceinline__ void cp_async16(float* dst, const float* src, int bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async4(float* dst, const float* src, int bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Stage the lane's four elements [base, base+4) of a row into dst[0..4); zeros past V.
+// VEC: the row start is 16-byte aligned and V % 4 == 0, so base < V implies base + 4 <= V.
+template <bool VEC>
+__device__ __forceinline__ void stage4(float* dst, const float* __restrict__ row, int V, int base) {
+    if (VEC) {
+        const bool in = base < V;
+        cp_async16(dst, in ? row + base : row, in ? 16 : 0);
+    } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const bool in = base + q < V;
+            cp_async4(dst + q, in ? row + base + q : row, in ? 4 : 0);
+        }
+    }
 }
 
 // ------------------------------------------------------------------ warp / block helpers
@@ -336,6 +372,55 @@ __device__ __forceinline__ float sampler_uniform(unsigned long long seed, unsign
     return float(philox4x32_10(ctr, key).x >> 8) * 0x1p-24f;
 }
 
+// This warp's contiguous share of the CTA's segments, streamed from global memory (in
+// practice L2, after pass 1) through the warp's staging buffer, two chunks of SBH
+// blocks in flight.  Blocks of segments with live(sg) false are not read.  Then, in
+// block order, body(sg, it, on, v, base): `it` the block's index inside segment sg,
+// `on` = live(sg), v the lane's four values (zeros when not on or past V), base the
+// index of v.x.  Each lane reads back only what it copied itself, so no warp barrier is
+// needed between the copies and their use.
+template <bool VEC, typename LIVE, typename BODY>
+__device__ __forceinline__ void stream_warp(const float* __restrict__ row, const Geom& g, const Smem& sm, int warp,
+                                            int lane, LIVE live, BODY body) {
+    int r0, r1;
+    warp_range(g.s1 - g.s0, warp, r0, r1);
+    r0 += g.s0;
+    r1 += g.s0;
+    const int nblk = (r1 - r0) << g.shift;
+    const int mask = g.seg_it() - 1;
+    float* st = sm.stage + warp * (2 * SBH * BLK) + lane * 4;
+    const int nch = (nblk + SBH - 1) / SBH;
+    auto issue = [&](int c) {
+        float* dst = st + (c & 1) * (SBH * BLK);
+#pragma unroll 1
+        for (int j = 0; j < SBH && c * SBH + j < nblk; ++j) {
+            const int blk = c * SBH + j;
+            const int sg = r0 + (blk >> g.shift);
+            if (live(sg)) stage4<VEC>(dst + j * BLK, row, g.V, g.base(sg, blk & mask, lane));
+        }
+        cp_async_commit();
+    };
+    if (nch > 0) issue(0);
+#pragma unroll 1
+    for (int c = 0; c < nch; ++c) {
+        if (c + 1 < nch) {
+            issue(c + 1);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        const float* src = st + (c & 1) * (SBH * BLK);
+#pragma unroll 1
+        for (int j = 0; j < SBH && c * SBH + j < nblk; ++j) {
+            const int blk = c * SBH + j;
+            const int sg = r0 + (blk >> g.shift);
+            const bool on = live(sg);
+            const float4 v = on ? *reinterpret_cast<const float4*>(src + j * BLK) : make_float4(0.f, 0.f, 0.f, 0.f);
+            body(sg, blk & mask, on, v, g.base(sg, blk & mask, lane));
+        }
+    }
+}
+
 // ------------------------------------------------------------------ pass 1
 
 // One streaming pass over this CTA's segments.  Warp w takes a contiguous range of
@@ -419,7 +504,8 @@ __device__ __forceinline__ void pass1(const float* __restrict__ row, const Geom&
 // part[rank] (f[0] ordered mass of its segments, u[0] positive count, u[1] bad flag,
 // u[2] maximum key) and, if `hist_shift` >= 0, one histogram count per segment maximum
 // into the leader's histogram (key >> hist_shift), which the leader cleared before
-// that barrier.  Block-collective.
+// that barrier.  Histogram updates are combined per warp (equal bins of a warp add
+// once).  Block-collective.
 FS_NOINLINE __device__ inline void pass1_totals(const Geom& g, const Smem& sm, bool leader, int rank, int pos,
                                                 bool bad, int hist_shift, bool prob, int warp, int lane,
                                                 int tid) {
@@ -427,11 +513,18 @@ FS_NOINLINE __device__ inline void pass1_totals(const Geom& g, const Smem& sm, b
     pos = warp_sum_i(pos);
     const int b = __any_sync(FULL, bad) ? 1 : 0;
     uint32_t km = 0;
-    for (int i = g.s0 + tid; i < g.s1; i += NT) {
-        const uint32_t key = sm.segkey[i];
+#pragma unroll 1
+    for (int i0 = g.s0 + warp * 32; i0 < g.s1; i0 += NT) {
+        const int i = i0 + lane;
+        const bool in = i < g.s1;
+        const uint32_t key = in ? sm.segkey[i] : 0u;
         km = max(km, key);
-        if (hist_shift >= 0) inc_leader(&sm.hist[min(uint32_t(HBINS - 1), key >> hist_shift)], leader);
-        if (!leader) {
+        if (hist_shift >= 0) {
+            const uint32_t bin = in ? min(uint32_t(HBINS - 1), key >> hist_shift) : 0xffffffffu;
+            const unsigned same = __match_any_sync(FULL, bin);
+            if (in && lane == __ffs(same) - 1) add_leader(&sm.hist[bin], uint32_t(__popc(same)), leader);
+        }
+        if (in && !leader) {
             put_leader(&sm.segkey[i], key, false);
             if (prob) put_leader(&sm.mass[0][i], __float_as_uint(sm.mass[0][i]), false);
         }
@@ -451,6 +544,7 @@ FS_NOINLINE __device__ inline void pass1_totals(const Geom& g, const Smem& sm, b
     if (tid == 0) {
         int p = 0, nb = 0;
         uint32_t mk = 0;
+#pragma unroll 1
         for (int w = 0; w < NW; ++w) {
             p += sm.red[w];
             nb |= sm.red[NW + w];
@@ -469,69 +563,41 @@ FS_NOINLINE __device__ inline void pass1_totals(const Geom& g, const Smem& sm, b
 // the leader's mass[ia] / mass[ib]; zero for skipped segments); the CTA's ordered
 // sums and counts into the leader's part[rank] (f[0], f[1], u[0], u[1]).
 // Block-collective.
-template <bool VEC, bool NC>
+template <bool VEC>
 FS_NOINLINE __device__ void pivot_pass(const float* __restrict__ row, const Geom& g, const Smem& sm, bool leader,
                                        int rank, float p1, float p2, int ia, int ib, int warp, int lane, int tid) {
-    int r0, r1;
-    warp_range(g.s1 - g.s0, warp, r0, r1);
-    r0 += g.s0;
-    r1 += g.s0;
     const uint32_t kp1 = prob_key(p1);
-    const int mask = g.seg_it() - 1;
+    const int last = g.seg_it() - 1;
     int c1 = 0, c2 = 0;
-    for (int b0 = 0; b0 < ((r1 - r0) << g.shift); b0 += TB) {
-        float4 v[TB];
-        bool any = false;
+    float sa = 0.f, sb = 0.f;
+    stream_warp<VEC>(
+        row, g, sm, warp, lane, [&](int sg) { return sm.segkey[sg] > kp1; },
+        [&](int sg, int it, bool on, const float4& v, int) {
+            float a = 0.f, b = 0.f;
+            if (on) {
+                float w1[4], w2[4];
 #pragma unroll
-        for (int j = 0; j < TB; ++j) {
-            const int blk = b0 + j;
-            const int sg = r0 + (blk >> g.shift);
-            const bool on = sg < r1 && sm.segkey[sg] > kp1;
-            any |= on;
-            v[j] = on ? load4<VEC, NC>(row, g.V, g.base(sg, blk & mask, lane), 0.f) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        float a[TB], b[TB];
-#pragma unroll
-        for (int j = 0; j < TB; ++j) {
-            float w1[4], w2[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float x = q_at(v[j], q);
-                w1[q] = x > p1 ? x : 0.f;
-                w2[q] = x > p2 ? x : 0.f;
-                c1 += x > p1;
-                c2 += x > p2;
-            }
-            a[j] = (w1[0] + w1[1]) + (w1[2] + w1[3]);
-            b[j] = (w2[0] + w2[1]) + (w2[2] + w2[3]);
-        }
-        if (any) {
-#pragma unroll
-            for (int m = 16; m; m >>= 1)
-#pragma unroll
-                for (int j = 0; j < TB; ++j) {
-                    a[j] += __shfl_xor_sync(FULL, a[j], m);
-                    b[j] += __shfl_xor_sync(FULL, b[j], m);
+                for (int q = 0; q < 4; ++q) {
+                    const float x = q_at(v, q);
+                    w1[q] = x > p1 ? x : 0.f;
+                    w2[q] = x > p2 ? x : 0.f;
+                    c1 += x > p1;
+                    c2 += x > p2;
                 }
-        }
-        const int nseg = TB >> g.shift;
-        const int sg = r0 + (b0 >> g.shift) + lane;
-        if (lane < nseg && sg < r1) {
-            float sa = 0.f, sb = 0.f;
-#pragma unroll
-            for (int j = 0; j < TB; ++j) {
-                const bool mine = (j >> g.shift) == lane;
-                sa += mine ? a[j] : 0.f;
-                sb += mine ? b[j] : 0.f;
+                a = warp_sum((w1[0] + w1[1]) + (w1[2] + w1[3]));
+                b = warp_sum((w2[0] + w2[1]) + (w2[2] + w2[3]));
             }
-            sm.mass[ia][sg] = sa;
-            sm.mass[ib][sg] = sb;
-            if (!leader) {
-                put_leader(&sm.mass[ia][sg], __float_as_uint(sa), false);
-                put_leader(&sm.mass[ib][sg], __float_as_uint(sb), false);
+            sa = it ? sa + a : a;
+            sb = it ? sb + b : b;
+            if (it == last && lane == 0) {
+                sm.mass[ia][sg] = sa;
+                sm.mass[ib][sg] = sb;
+                if (!leader) {
+                    put_leader(&sm.mass[ia][sg], __float_as_uint(sa), false);
+                    put_leader(&sm.mass[ib][sg], __float_as_uint(sb), false);
+                }
             }
-        }
-    }
+        });
     c1 = warp_sum_i(c1);
     c2 = warp_sum_i(c2);
     if (lane == 0) {
@@ -544,6 +610,7 @@ FS_NOINLINE __device__ void pivot_pass(const float* __restrict__ row, const Geom
         const float t2 = warp_ordered_sum(sm.mass[ib], g.s0, g.s1, lane);
         if (lane == 0) {
             int n1 = 0, n2 = 0;
+#pragma unroll 1
             for (int w = 0; w < NW; ++w) {
                 n1 += sm.red[w];
                 n2 += sm.red[NW + w];
@@ -568,6 +635,7 @@ FS_NOINLINE __device__ inline int live_list(const Smem& sm, int a, int b, uint32
     r0 += a;
     r1 += a;
     int cnt = 0;
+#pragma unroll 1
     for (int base = r0; base < r1; base += 32) {
         const int i = base + lane;
         cnt += __popc(__ballot_sync(FULL, i < r1 && sm.segkey[i] >= thr));
@@ -575,11 +643,12 @@ FS_NOINLINE __device__ inline int live_list(const Smem& sm, int a, int b, uint32
     if (lane == 0) sm.red[warp] = cnt;
     __syncthreads();
     int off = 0, total = 0;
-#pragma unroll
+#pragma unroll 1
     for (int w = 0; w < NW; ++w) {
         if (w < warp) off += sm.red[w];
         total += sm.red[w];
     }
+#pragma unroll 1
     for (int base = r0; base < r1; base += 32) {
         const int i = base + lane;
         const bool live = i < r1 && sm.segkey[i] >= thr;
@@ -593,72 +662,63 @@ FS_NOINLINE __device__ inline int live_list(const Smem& sm, int a, int b, uint32
 
 // Read the listed segments (list[0..nlive), in order) and emit, in index order, every
 // element with key >= thr: out(p, value, index) for p = 0, 1, ...  Returns the exact
-// count.  Each warp takes 8 blocks of listed segments per batch, so a batch is one L2
-// round trip.  Block-collective.
-template <bool VEC, bool NC, typename KEYF, typename OUT>
+// count.  Each batch stages 2*SBH listed blocks per warp (cp.async), counts, fixes the
+// warps' output offsets, then emits.  Block-collective.
+template <bool VEC, typename KEYF, typename OUT>
 __device__ __forceinline__ int collect(const float* __restrict__ row, const Geom& g, const Smem& sm, int nlive,
-                                       uint32_t thr, KEYF keyf, float fill, int warp, int lane, OUT out) {
-    constexpr int CB = 8;              // blocks per warp per batch
-    const int spw = CB >> g.shift;     // listed segments per warp per batch
+                                       uint32_t thr, KEYF keyf, int warp, int lane, OUT out) {
+    constexpr int WB = 2 * SBH;
+    const int nblk = nlive << g.shift;
     const int mask = g.seg_it() - 1;
+    float* st = sm.stage + warp * (WB * BLK) + lane * 4;
     int total = 0;
-    for (int b0 = 0; b0 < nlive; b0 += NW * spw) {
-        float4 v[CB];
-        int c = 0;
-#pragma unroll
-        for (int j = 0; j < CB; ++j) {
-            const int li = b0 + warp * spw + (j >> g.shift);
-            const bool on = li < nlive;
-            const int sg = on ? sm.list[li] : 0;
-            v[j] = on ? load4<VEC, NC>(row, g.V, g.base(sg, j & mask, lane), fill)
-                      : make_float4(fill, fill, fill, fill);
+#pragma unroll 1
+    for (int c0 = 0; c0 < nblk; c0 += NW * WB) {
+        const int w0 = c0 + warp * WB;
+        const int nb = max(0, min(WB, nblk - w0));
+#pragma unroll 1
+        for (int j = 0; j < nb; ++j) {
+            const int lb = w0 + j;
+            stage4<VEC>(st + j * BLK, row, g.V, g.base(sm.list[lb >> g.shift], lb & mask, lane));
         }
+        cp_async_commit();
+        cp_async_wait<0>();
+        int cnt = 0;
+#pragma unroll 1
+        for (int j = 0; j < nb; ++j) {
+            const int lb = w0 + j;
+            const int base = g.base(sm.list[lb >> g.shift], lb & mask, lane);
 #pragma unroll
-        for (int j = 0; j < CB; ++j) {
-            const int li = b0 + warp * spw + (j >> g.shift);
-            if (li < nlive) {
-                const int base = g.base(sm.list[li], j & mask, lane);
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    c += __popc(__ballot_sync(FULL, keyf(q_at(v[j], q)) >= thr && base + q < g.V));
-            }
+            for (int q = 0; q < 4; ++q) cnt += (keyf(st[j * BLK + q]) >= thr && base + q < g.V);
         }
-        if (lane == 0) sm.red[warp] = c;
+        cnt = warp_sum_i(cnt);
+        if (lane == 0) sm.red[warp] = cnt;
         __syncthreads();
         int pos = total, chunk = 0;
-#pragma unroll
+#pragma unroll 1
         for (int w = 0; w < NW; ++w) {
             if (w < warp) pos += sm.red[w];
             chunk += sm.red[w];
         }
         __syncthreads();
+#pragma unroll 1
+        for (int j = 0; j < nb; ++j) {
+            const int lb = w0 + j;
+            const int base = g.base(sm.list[lb >> g.shift], lb & mask, lane);
+            int k = 0;
 #pragma unroll
-        for (int j = 0; j < CB; ++j) {
-            const int li = b0 + warp * spw + (j >> g.shift);
-            if (li < nlive) {
-                const int base = g.base(sm.list[li], j & mask, lane);
-                bool keep[4];
-                int k = 0;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    keep[q] = keyf(q_at(v[j], q)) >= thr && base + q < g.V;
-                    k += keep[q];
-                }
-                const int incl = warp_incl_scan_i(k, lane);
-                int p = pos + incl - k;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    if (keep[q]) {
-                        out(p, q_at(v[j], q), base + q);
-                        ++p;
-                    }
-                }
-                pos += __shfl_sync(FULL, incl, 31);
+            for (int q = 0; q < 4; ++q) k += (keyf(st[j * BLK + q]) >= thr && base + q < g.V);
+            const int incl = warp_incl_scan_i(k, lane);
+            int p = pos + incl - k;
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {
+                const float x = st[j * BLK + q];
+                if (keyf(x) >= thr && base + q < g.V) out(p++, x, base + q);
             }
+            pos += __shfl_sync(FULL, incl, 31);
         }
         total += chunk;
     }
-    __syncthreads();
     return total;
 }
 
@@ -666,13 +726,13 @@ __device__ __forceinline__ int collect(const float* __restrict__ row, const Geom
 // list (entries [rank * rc, rank * rc + rc)), in index order; the exact count goes to
 // part[rank].u[4] of every CTA of the cluster, so that after the next cluster barrier
 // each CTA can tell whether all regions fit.  Block-collective.
-template <bool VEC, bool NC, typename KEYF>
+template <bool VEC, typename KEYF>
 FS_NOINLINE __device__ void collect_own(const float* __restrict__ row, const Geom& g, const Smem& sm, bool leader,
-                                        int rank, int C, int rc, uint32_t thr, KEYF keyf, float fill, int warp,
-                                        int lane, int tid) {
+                                        int rank, int C, int rc, uint32_t thr, KEYF keyf, int warp, int lane,
+                                        int tid) {
     const int nlive = live_list(sm, g.s0, g.s1, thr, warp, lane);
     const int base = rank * rc;
-    const int n = collect<VEC, NC>(row, g, sm, nlive, thr, keyf, fill, warp, lane, [&](int p, float x, int ix) {
+    const int n = collect<VEC>(row, g, sm, nlive, thr, keyf, warp, lane, [&](int p, float x, int ix) {
         if (p < rc) {
             put_leader(&sm.lv[base + p], __float_as_uint(x), leader);
             put_leader(&sm.li[base + p], uint32_t(ix), leader);
@@ -692,11 +752,13 @@ FS_NOINLINE __device__ void collect_own(const float* __restrict__ row, const Geo
 // its region.  Any CTA (each holds every count).
 __device__ __forceinline__ bool regions_fit(const Smem& sm, int C, int rc) {
     bool fits = true;
+#pragma unroll 1
     for (int r = 0; r < C; ++r) fits = fits && int(sm.part[r].u[4]) <= rc;
     return fits;
 }
 __device__ __forceinline__ int regions_total(const Smem& sm, int C) {
     int n = 0;
+#pragma unroll 1
     for (int r = 0; r < C; ++r) n += int(sm.part[r].u[4]);
     return n;
 }
@@ -706,10 +768,12 @@ __device__ __forceinline__ int regions_total(const Smem& sm, int C) {
 // move only towards the front, and every thread reads its entries before any write.
 FS_NOINLINE __device__ inline int join_regions(const Smem& sm, int C, int rc, int tid) {
     int dst = 0;
+#pragma unroll 1
     for (int c = 0; c < C; ++c) {
         const int n = int(sm.part[c].u[4]);
         const int src = c * rc;
         if (src != dst) {
+#pragma unroll 1
             for (int e0 = 0; e0 < n; e0 += NT) {
                 const int e = e0 + tid;
                 float v = 0.f;
@@ -737,9 +801,11 @@ template <typename KEYF>
 FS_NOINLINE __device__ uint32_t kth_key_in_list(const Smem& sm, int n, int k, KEYF keyf, int warp, int lane,
                                                 int tid) {
     uint32_t best = 0;
+#pragma unroll 1
     for (int i = tid; i < n; i += NT) {
         const uint32_t ki = keyf(sm.lv[i]);
         int ge = 0;
+#pragma unroll 4
         for (int j = 0; j < n; ++j) ge += (keyf(sm.lv[j]) >= ki);
         if (ge >= k) best = max(best, ki);
     }
@@ -747,7 +813,7 @@ FS_NOINLINE __device__ uint32_t kth_key_in_list(const Smem& sm, int n, int k, KE
     if (lane == 0) sm.red[warp] = int(best);
     __syncthreads();
     uint32_t r = 0;
-#pragma unroll
+#pragma unroll 1
     for (int w = 0; w < NW; ++w) r = max(r, uint32_t(sm.red[w]));
     __syncthreads();
     return r;
@@ -758,6 +824,7 @@ FS_NOINLINE __device__ uint32_t kth_key_in_list(const Smem& sm, int n, int k, KE
 template <typename KEYF>
 FS_NOINLINE __device__ int filter_list_warp(const Smem& sm, int n, uint32_t t, KEYF keyf, int lane) {
     int w = 0;
+#pragma unroll 1
     for (int base = 0; base < n; base += 32) {
         const int i = base + lane;
         const bool keep = i < n && keyf(sm.lv[i]) >= t;
@@ -803,6 +870,7 @@ FS_NOINLINE __device__ inline uint32_t hist_bound(const Smem& sm, int ns, int k,
     if (lane == 31) sm.red[warp] = int(incl);
     __syncthreads();
     uint32_t before = incl - own;
+#pragma unroll 1
     for (int w = 0; w < warp; ++w) before += uint32_t(sm.red[w]);
     const uint32_t kk = uint32_t(k);
     if (before < kk && before + own >= kk) {
@@ -838,6 +906,7 @@ FS_NOINLINE __device__ void locate_in_segment(const float* __restrict__ row, con
     float run = 0.f;
     int last_j = -1;
     float last_x = 0.f;
+#pragma unroll 1
     for (int it = 0; it < g.seg_it(); ++it) {
         const int base = g.base(s, it, lane);
         const float4 v = load4<VEC, NC>(row, g.V, base, 0.f);
@@ -891,6 +960,7 @@ FS_NOINLINE __device__ inline int locate_segment(const float* mass, int a, int b
     float run = 0.f;
     int last = -1;
     float last_before = 0.f;
+#pragma unroll 1
     for (int base = a; base < b; base += 32) {
         const float m = (base + lane < b) ? mass[base + lane] : 0.f;
         const float incl = warp_incl_scan(m, lane);
@@ -916,6 +986,7 @@ FS_NOINLINE __device__ inline int locate_segment(const float* mass, int a, int b
 FS_NOINLINE __device__ inline int locate_in_list(const float* lv, int n, float low, float t, int lane) {
     float run = 0.f;
     int last = -1;
+#pragma unroll 1
     for (int base = 0; base < n; base += 128) {
         float w[4];
 #pragma unroll
@@ -981,39 +1052,22 @@ __device__ __forceinline__ void send_command(const Smem& sm, const Ctl& c, int C
 // sub-interval [lo,p0) [p0,p1) [p1,p2) [p2,hi) the smallest and largest key present.
 // The CTA's record goes to the leader's part[rank]: f[0..2] masses, u[0..2] counts,
 // u[3..6] min keys, u[7..10] max keys.  Block-collective.
-template <bool VEC, bool NC, bool MASS, typename KEYF>
+template <bool VEC, bool MASS, typename KEYF>
 FS_NOINLINE __device__ void bisect_pass(const float* __restrict__ row, const Geom& g, const Smem& sm, bool leader,
                                         int rank, uint64_t lo, uint64_t hi, const uint32_t* piv, KEYF keyf,
-                                        float fill, int warp, int lane, int tid) {
-    int r0, r1;
-    warp_range(g.s1 - g.s0, warp, r0, r1);
-    r0 += g.s0;
-    r1 += g.s0;
-    const int mask = g.seg_it() - 1;
+                                        int warp, int lane, int tid) {
     const uint32_t p0 = piv[0], p1 = piv[1], p2 = piv[2];
     float m[3] = {0.f, 0.f, 0.f};
     int c[3] = {0, 0, 0};
     uint32_t mn[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
     uint32_t mx[4] = {0u, 0u, 0u, 0u};
-    for (int b0 = 0; b0 < ((r1 - r0) << g.shift); b0 += TB) {
-        float4 v[TB];
-        bool on[TB];
-#pragma unroll
-        for (int j = 0; j < TB; ++j) {
-            const int blk = b0 + j;
-            const int sg = r0 + (blk >> g.shift);
-            on[j] = sg < r1 && uint64_t(sm.segkey[sg]) >= lo;
-            v[j] = on[j] ? load4<VEC, NC>(row, g.V, g.base(sg, blk & mask, lane), fill)
-                         : make_float4(fill, fill, fill, fill);
-        }
-#pragma unroll
-        for (int j = 0; j < TB; ++j) {
-            if (!on[j]) continue;
-            const int blk = b0 + j;
-            const int base = g.base(r0 + (blk >> g.shift), blk & mask, lane);
-#pragma unroll
+    stream_warp<VEC>(
+        row, g, sm, warp, lane, [&](int sg) { return uint64_t(sm.segkey[sg]) >= lo; },
+        [&](int, int, bool on, const float4& v, int base) {
+            if (!on) return;
+#pragma unroll 1
             for (int q = 0; q < 4; ++q) {
-                const float xv = q_at(v[j], q);
+                const float xv = q_at(v, q);
                 const uint32_t key = keyf(xv);
                 const bool inr = base + q < g.V;
                 const bool g0 = inr && key >= p0, g1 = inr && key >= p1, g2 = inr && key >= p2;
@@ -1034,8 +1088,7 @@ FS_NOINLINE __device__ void bisect_pass(const float* __restrict__ row, const Geo
                     mx[t] = sel ? max(mx[t], key) : mx[t];
                 }
             }
-        }
-    }
+        });
     // warp -> block (fixed order) -> the leader's part[rank]
     float* rf = reinterpret_cast<float*>(sm.red);
     uint32_t* ru = reinterpret_cast<uint32_t*>(sm.red);
@@ -1050,6 +1103,7 @@ FS_NOINLINE __device__ void bisect_pass(const float* __restrict__ row, const Geo
         mx[t] = warp_max_u(mx[t]);
     }
     if (lane == 0) {
+#pragma unroll
         for (int i = 0; i < 3; ++i) {
             rf[i * NW + warp] = m[i];
             ru[(3 + i) * NW + warp] = uint32_t(c[i]);
@@ -1058,9 +1112,11 @@ FS_NOINLINE __device__ void bisect_pass(const float* __restrict__ row, const Geo
     __syncthreads();
     uint32_t rec[6];
     if (tid == 0) {
+#pragma unroll
         for (int i = 0; i < 3; ++i) {
             float a = 0.f;
             uint32_t b = 0;
+#pragma unroll 1
             for (int w = 0; w < NW; ++w) {
                 a += rf[i * NW + w];
                 b += ru[(3 + i) * NW + w];
@@ -1071,6 +1127,7 @@ FS_NOINLINE __device__ void bisect_pass(const float* __restrict__ row, const Geo
     }
     __syncthreads();
     if (lane == 0) {
+#pragma unroll
         for (int t = 0; t < 4; ++t) {
             ru[t * NW + warp] = mn[t];
             ru[(4 + t) * NW + warp] = mx[t];
@@ -1079,8 +1136,10 @@ FS_NOINLINE __device__ void bisect_pass(const float* __restrict__ row, const Geo
     __syncthreads();
     if (tid == 0) {
         uint32_t* dst = reinterpret_cast<uint32_t*>(&sm.part[rank]);
+#pragma unroll 1
         for (int t = 0; t < 4; ++t) {
             uint32_t a = 0xffffffffu, b = 0u;
+#pragma unroll 1
             for (int w = 0; w < NW; ++w) {
                 a = min(a, ru[t * NW + w]);
                 b = max(b, ru[(4 + t) * NW + w]);
@@ -1088,6 +1147,7 @@ FS_NOINLINE __device__ void bisect_pass(const float* __restrict__ row, const Geo
             put_leader(dst + 4 + 3 + t, a, leader);   // u[3 + t]
             put_leader(dst + 4 + 7 + t, b, leader);   // u[7 + t]
         }
+#pragma unroll
         for (int i = 0; i < 3; ++i) {
             put_leader(dst + i, rec[i], leader);          // f[i]
             put_leader(dst + 4 + i, rec[3 + i], leader);  // u[i]
@@ -1097,29 +1157,23 @@ FS_NOINLINE __device__ void bisect_pass(const float* __restrict__ row, const Geo
 
 // Count and mass (x > 0) of key >= t over this CTA's segments; the record goes to the
 // leader's part[rank] (f[0] mass, u[0] count).  Block-collective.
-template <bool VEC, bool NC, typename KEYF>
+template <bool VEC, typename KEYF>
 FS_NOINLINE __device__ void massge_pass(const float* __restrict__ row, const Geom& g, const Smem& sm, bool leader,
                                         int rank, uint32_t t, KEYF keyf, int warp, int lane, int tid) {
-    int r0, r1;
-    warp_range(g.s1 - g.s0, warp, r0, r1);
-    r0 += g.s0;
-    r1 += g.s0;
-    const int mask = g.seg_it() - 1;
     float ms = 0.f;
     int cnt = 0;
-    for (int blk = 0; blk < ((r1 - r0) << g.shift); ++blk) {
-        const int sg = r0 + (blk >> g.shift);
-        if (sm.segkey[sg] < t) continue;
-        const int base = g.base(sg, blk & mask, lane);
-        const float4 v = load4<VEC, NC>(row, g.V, base, 0.f);
+    stream_warp<VEC>(
+        row, g, sm, warp, lane, [&](int sg) { return sm.segkey[sg] >= t; },
+        [&](int, int, bool on, const float4& v, int base) {
+            if (!on) return;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float xv = q_at(v, q);
-            const bool gq = keyf(xv) >= t && xv > 0.f && base + q < g.V;
-            ms += gq ? xv : 0.f;
-            cnt += gq;
-        }
-    }
+            for (int q = 0; q < 4; ++q) {
+                const float xv = q_at(v, q);
+                const bool gq = keyf(xv) >= t && xv > 0.f && base + q < g.V;
+                ms += gq ? xv : 0.f;
+                cnt += gq;
+            }
+        });
     ms = warp_sum(ms);
     cnt = warp_sum_i(cnt);
     float* rf = reinterpret_cast<float*>(sm.red);
@@ -1131,6 +1185,7 @@ FS_NOINLINE __device__ void massge_pass(const float* __restrict__ row, const Geo
     if (tid == 0) {
         float a = 0.f;
         int n = 0;
+#pragma unroll 1
         for (int w = 0; w < NW; ++w) {
             a += rf[w];
             n += sm.red[NW + w];
@@ -1217,10 +1272,10 @@ __device__ __forceinline__ void bisect_update(const Smem& sm, int C, Bisect& st,
 }
 
 // Leader: drive a bisection to the end with the whole cluster (at most 40 passes).
-template <bool VEC, bool NC, bool MASS, typename KEYF>
+template <bool VEC, bool MASS, typename KEYF>
 FS_NOINLINE __device__ void bisect_leader(const float* __restrict__ row, const Geom& g, const Smem& sm, int C,
-                                          Bisect* stp, int kcrit, float target, KEYF keyf, float fill, int warp,
-                                          int lane, int tid) {
+                                          Bisect* stp, int kcrit, float target, KEYF keyf, int warp, int lane,
+                                          int tid) {
     Bisect st = *stp;
     for (int iter = 0; iter < 40 && st.hi - st.lo > 1; ++iter) {
         uint32_t piv[3];
@@ -1234,7 +1289,7 @@ FS_NOINLINE __device__ void bisect_leader(const float* __restrict__ row, const G
         c.hi_lo = uint32_t(st.hi);
         c.hi_hi = uint32_t(st.hi >> 32);
         send_command(sm, c, C, tid);
-        bisect_pass<VEC, NC, MASS>(row, g, sm, true, 0, st.lo, st.hi, piv, keyf, fill, warp, lane, tid);
+        bisect_pass<VEC, MASS>(row, g, sm, true, 0, st.lo, st.hi, piv, keyf, warp, lane, tid);
         cluster_sync();  // every part is in
         bisect_update<MASS>(sm, C, st, piv, kcrit, target);
         __syncthreads();
@@ -1243,7 +1298,7 @@ FS_NOINLINE __device__ void bisect_leader(const float* __restrict__ row, const G
 }
 
 // Leader: count and mass of key >= t over the whole row, with the cluster.
-template <bool VEC, bool NC, typename KEYF>
+template <bool VEC, typename KEYF>
 FS_NOINLINE __device__ void massge_leader(const float* __restrict__ row, const Geom& g, const Smem& sm, int C,
                                           uint32_t t, KEYF keyf, int warp, int lane, int tid, float* mass_out,
                                           int* cnt_out) {
@@ -1251,7 +1306,7 @@ FS_NOINLINE __device__ void massge_leader(const float* __restrict__ row, const G
     c.cmd = CMD_MASSGE;
     c.u[0] = t;
     send_command(sm, c, C, tid);
-    massge_pass<VEC, NC>(row, g, sm, true, 0, t, keyf, warp, lane, tid);
+    massge_pass<VEC>(row, g, sm, true, 0, t, keyf, warp, lane, tid);
     cluster_sync();
     float m = 0.f;
     int n = 0;
@@ -1267,11 +1322,11 @@ FS_NOINLINE __device__ void massge_leader(const float* __restrict__ row, const G
 // Leader alone: every element of the row with key >= thr into lv/li[0..n) in index
 // order, read through the leader's full segment table.  Returns the exact count
 // (entries beyond CAP are dropped).  Block-collective.
-template <bool VEC, bool NC, typename KEYF>
+template <bool VEC, typename KEYF>
 FS_NOINLINE __device__ int collect_all(const float* __restrict__ row, const Geom& g, const Smem& sm, uint32_t thr,
-                                       KEYF keyf, float fill, int warp, int lane) {
+                                       KEYF keyf, int warp, int lane) {
     const int nlive = live_list(sm, 0, g.ns, thr, warp, lane);
-    return collect<VEC, NC>(row, g, sm, nlive, thr, keyf, fill, warp, lane, [&](int p, float x, int ix) {
+    return collect<VEC>(row, g, sm, nlive, thr, keyf, warp, lane, [&](int p, float x, int ix) {
         if (p < CAP) {
             sm.lv[p] = x;
             sm.li[p] = ix;
@@ -1284,17 +1339,17 @@ FS_NOINLINE __device__ int collect_all(const float* __restrict__ row, const Geom
 // if a region overflowed but the total fits, the leader collects alone.  Returns n, or
 // -1 when more than CAP elements qualify (the peers then still wait for commands).
 // With `exit_if_fit` the peers leave once the list is complete (*peers = false).
-template <bool VEC, bool NC, typename KEYF>
+template <bool VEC, typename KEYF>
 FS_NOINLINE __device__ int gather_leader(const float* __restrict__ row, const Geom& g, const Smem& sm, int C,
-                                         uint32_t thr, KEYF keyf, float fill, bool exit_if_fit, bool* peers,
-                                         int warp, int lane, int tid) {
+                                         uint32_t thr, KEYF keyf, bool exit_if_fit, bool* peers, int warp, int lane,
+                                         int tid) {
     const int rc = CAP / C;
     Ctl c{};
     c.cmd = CMD_COLLECT;
     c.flag = exit_if_fit ? 1 : 0;
     c.u[0] = thr;
     send_command(sm, c, C, tid);
-    collect_own<VEC, NC>(row, g, sm, true, 0, C, rc, thr, keyf, fill, warp, lane, tid);
+    collect_own<VEC>(row, g, sm, true, 0, C, rc, thr, keyf, warp, lane, tid);
     cluster_sync();  // every region and count is in
     if (regions_fit(sm, C, rc)) {
         if (exit_if_fit) *peers = false;
@@ -1307,7 +1362,7 @@ FS_NOINLINE __device__ int gather_leader(const float* __restrict__ row, const Ge
         send_command(sm, e, C, tid);
         *peers = false;
     }
-    return collect_all<VEC, NC>(row, g, sm, thr, keyf, fill, warp, lane);
+    return collect_all<VEC>(row, g, sm, thr, keyf, warp, lane);
 }
 
 }  // namespace fsd

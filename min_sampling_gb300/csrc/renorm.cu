@@ -45,43 +45,23 @@ FS_NOINLINE __device__ void write_pass(const float* __restrict__ row, float* __r
     const KEYF keyf;
     const float fill = IS_PROB ? 0.f : __int_as_float(0xff800000);
     const bool vec_out = VEC && ((reinterpret_cast<uintptr_t>(orow) & 15) == 0);
-    int r0, r1;
-    warp_range(g.s1 - g.s0, warp, r0, r1);
-    r0 += g.s0;
-    r1 += g.s0;
-    const int mask = g.seg_it() - 1;
-    for (int b0 = 0; b0 < ((r1 - r0) << g.shift); b0 += TB) {
-        float4 v[TB];
-        bool on[TB];
-#pragma unroll
-        for (int j = 0; j < TB; ++j) {
-            const int blk = b0 + j;
-            const int sg = r0 + (blk >> g.shift);
-            on[j] = sg < r1 && valid && sm.segkey[sg] >= t;
-            v[j] = on[j] ? load4<VEC, false>(row, g.V, g.base(sg, blk & mask, lane), fill)
-                         : make_float4(fill, fill, fill, fill);
-        }
-#pragma unroll
-        for (int j = 0; j < TB; ++j) {
-            const int blk = b0 + j;
-            const int sg = r0 + (blk >> g.shift);
-            if (sg >= r1) continue;
-            const int base = g.base(sg, blk & mask, lane);
+    stream_warp<VEC>(
+        row, g, sm, warp, lane, [&](int sg) { return valid && sm.segkey[sg] >= t; },
+        [&](int, int, bool on, const float4& v, int base) {
             float o[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const float xv = q_at(v[j], q);
-                o[q] = (on[j] && keyf(xv) >= t) ? (IS_PROB ? xv / denom : xv) : fill;
+                const float xv = q_at(v, q);
+                o[q] = (on && keyf(xv) >= t) ? (IS_PROB ? xv / denom : xv) : fill;
             }
             if (vec_out && base + 3 < g.V) {
                 *reinterpret_cast<float4*>(orow + base) = make_float4(o[0], o[1], o[2], o[3]);
             } else {
-#pragma unroll
+#pragma unroll 1
                 for (int q = 0; q < 4; ++q)
                     if (base + q < g.V) orow[base + q] = o[q];
             }
-        }
-    }
+        });
 }
 
 // The other CTAs: follow the leader's commands until the write.
@@ -89,21 +69,19 @@ template <bool VEC, int KIND>
 FS_NOINLINE __device__ void filter_peer(const float* __restrict__ row, float* __restrict__ orow, const Geom& g,
                                         const Smem& sm, int rank, int C, int warp, int lane, int tid) {
     using KEYF = typename std::conditional<KIND == K_MASK, KeyLogit, KeyProb>::type;
-    const float fill = KIND == K_MASK ? __int_as_float(0xff800000) : 0.f;
     for (;;) {
         cluster_sync();  // the command is published
         const Ctl c = *sm.ctl;
         if (c.cmd == CMD_BISECT) {
             const uint64_t hi = uint64_t(c.hi_lo) | (uint64_t(c.hi_hi) << 32);
-            bisect_pass<VEC, false, KIND == K_TOPP>(row, g, sm, false, rank, c.u[3], hi, c.u, KEYF(), fill, warp,
-                                                    lane, tid);
+            bisect_pass<VEC, KIND == K_TOPP>(row, g, sm, false, rank, c.u[3], hi, c.u, KEYF(), warp, lane, tid);
         } else if (c.cmd == CMD_MASSGE) {
-            massge_pass<VEC, false>(row, g, sm, false, rank, c.u[0], KEYF(), warp, lane, tid);
+            massge_pass<VEC>(row, g, sm, false, rank, c.u[0], KEYF(), warp, lane, tid);
         } else if (c.cmd == CMD_WRITE) {
             write_pass<VEC, KIND>(row, orow, g, sm, c.flag != 0, c.u[0], c.f[0], warp, lane);
             return;
         } else if (c.cmd == CMD_COLLECT) {
-            collect_own<VEC, false>(row, g, sm, false, rank, C, CAP / C, c.u[0], KEYF(), fill, warp, lane, tid);
+            collect_own<VEC>(row, g, sm, false, rank, C, CAP / C, c.u[0], KEYF(), warp, lane, tid);
         } else {
             return;  // CMD_EXIT
         }
@@ -126,7 +104,6 @@ __global__ void __launch_bounds__(NT, 4) filter_kernel(const FilterArgs a) {
     const int V = a.V, ns = a.ns;
     const float* row = a.in + size_t(b) * size_t(V);
     float* orow = a.out + size_t(b) * size_t(V);
-    const float fill = IS_PROB ? 0.f : __int_as_float(0xff800000);
 
     const int k = (KIND != K_TOPP) ? a.top_k[b] : 0;
     const bool k_on = KIND != K_TOPP && k > 0 && k < V;
@@ -171,8 +148,7 @@ __global__ void __launch_bounds__(NT, 4) filter_kernel(const FilterArgs a) {
                 uint32_t L0 = need_hist ? hist_bound(sm, ns, k, IS_PROB ? 21 : 22, warp, lane, tid) : 0u;
                 if (IS_PROB) L0 = max(L0, 1u);
                 bool peers = true;
-                const int n = gather_leader<VEC, false>(row, g, sm, C, L0, keyf, fill, false, &peers, warp, lane,
-                                                        tid);
+                const int n = gather_leader<VEC>(row, g, sm, C, L0, keyf, false, &peers, warp, lane, tid);
                 if (n >= 0) {
                     // Every element >= L0 (hence >= t) is in the list.
                     t = kth_key_in_list(sm, n, k, keyf, warp, lane, tid);
@@ -193,11 +169,11 @@ __global__ void __launch_bounds__(NT, 4) filter_kernel(const FilterArgs a) {
                     if (IS_PROB && L0 == 1u && npos < k) st.lo = 0;
                     st.hi = uint64_t(maxkey) + 1;
                     st.mass_lo = 0.f;
-                    bisect_leader<VEC, false, false>(row, g, sm, C, &st, k, 0.f, keyf, fill, warp, lane, tid);
+                    bisect_leader<VEC, false>(row, g, sm, C, &st, k, 0.f, keyf, warp, lane, tid);
                     t = uint32_t(st.lo);
                     if (IS_PROB) {
                         int cnt;
-                        massge_leader<VEC, false>(row, g, sm, C, t, keyf, warp, lane, tid, &denom, &cnt);
+                        massge_leader<VEC>(row, g, sm, C, t, keyf, warp, lane, tid, &denom, &cnt);
                     }
                 }
             }
@@ -208,13 +184,13 @@ __global__ void __launch_bounds__(NT, 4) filter_kernel(const FilterArgs a) {
             } else if (tp <= 0.f) {
                 t = maxkey;
                 int cnt;
-                massge_leader<VEC, false>(row, g, sm, C, t, keyf, warp, lane, tid, &denom, &cnt);
+                massge_leader<VEC>(row, g, sm, C, t, keyf, warp, lane, tid, &denom, &cnt);
             } else {
                 Bisect st;
                 st.lo = 0;
                 st.hi = uint64_t(maxkey) + 1;
                 st.mass_lo = M;
-                bisect_leader<VEC, false, true>(row, g, sm, C, &st, 0, tp * M, keyf, 0.f, warp, lane, tid);
+                bisect_leader<VEC, true>(row, g, sm, C, &st, 0, tp * M, keyf, warp, lane, tid);
                 t = uint32_t(st.lo);
                 denom = st.mass_lo;
             }

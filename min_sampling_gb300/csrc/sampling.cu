@@ -66,13 +66,12 @@ FS_NOINLINE __device__ void sample_peer(const float* __restrict__ row, const Geo
         cluster_sync();  // the command is published
         const Ctl c = *sm.ctl;
         if (c.cmd == CMD_PIVOT2) {
-            pivot_pass<VEC, true>(row, g, sm, false, rank, c.f[0], c.f[1], c.ia, c.ib, warp, lane, tid);
+            pivot_pass<VEC>(row, g, sm, false, rank, c.f[0], c.f[1], c.ia, c.ib, warp, lane, tid);
         } else if (c.cmd == CMD_BISECT) {
             const uint64_t hi = uint64_t(c.hi_lo) | (uint64_t(c.hi_hi) << 32);
-            bisect_pass<VEC, true, false>(row, g, sm, false, rank, c.u[3], hi, c.u, KeyProb(), 0.f, warp, lane,
-                                          tid);
+            bisect_pass<VEC, false>(row, g, sm, false, rank, c.u[3], hi, c.u, KeyProb(), warp, lane, tid);
         } else if (c.cmd == CMD_COLLECT) {
-            collect_own<VEC, true>(row, g, sm, false, rank, C, CAP / C, c.u[0], KeyProb(), 0.f, warp, lane, tid);
+            collect_own<VEC>(row, g, sm, false, rank, C, CAP / C, c.u[0], KeyProb(), warp, lane, tid);
         } else {
             return;  // CMD_EXIT
         }
@@ -253,7 +252,7 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
         // ---- a3: top-k-first prologue
         if (kfirst) {
             const uint32_t L0 = max(1u, need_hist ? hist_bound(sm, ns, k, 21, warp, lane, tid) : 0u);
-            const int n = gather_leader<VEC, true>(row, g, sm, C, L0, keyf, 0.f, true, &peers, warp, lane, tid);
+            const int n = gather_leader<VEC>(row, g, sm, C, L0, keyf, true, &peers, warp, lane, tid);
             if (n >= 0) {
                 dismiss();
                 compact = true;
@@ -273,7 +272,7 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
                 st.hi = uint64_t(maxkey) + 1;
                 st.mass_lo = 0.f;
                 if (npos < k) st.lo = 0;  // fewer positives than k: t_k = 0 keeps them all
-                bisect_leader<VEC, true, false>(row, g, sm, C, &st, k, 0.f, keyf, 0.f, warp, lane, tid);
+                bisect_leader<VEC, false>(row, g, sm, C, &st, k, 0.f, keyf, warp, lane, tid);
                 const uint32_t tk = uint32_t(st.lo);
                 low = tk >= 1u ? __uint_as_float(tk - 1u) : 0.f;  // x > low  <=>  key(x) >= t_k
                 // Per-segment and per-CTA masses above `low` for the draws (both pivots = low).
@@ -284,7 +283,7 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
                 c.ia = 0;
                 c.ib = 1;
                 send_command(sm, c, C, tid);
-                pivot_pass<VEC, true>(row, g, sm, true, 0, low, low, 0, 1, warp, lane, tid);
+                pivot_pass<VEC>(row, g, sm, true, 0, low, low, 0, 1, warp, lane, tid);
                 cluster_sync();
                 count_low = 0;
                 S_low = 0.f;
@@ -303,8 +302,7 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
         for (int round = 0; round < R_MAX; ++round) {
             if (!compact && count_low <= CAP) {
                 // Few tokens left above `low`: gather them; the leader goes on alone.
-                n_list = gather_leader<VEC, true>(row, g, sm, C, prob_key(low) + 1u, keyf, 0.f, true, &peers, warp,
-                                                  lane, tid);
+                n_list = gather_leader<VEC>(row, g, sm, C, prob_key(low) + 1u, keyf, true, &peers, warp, lane, tid);
                 dismiss();
                 if (n_list < 0) break;
                 compact = true;
@@ -355,7 +353,7 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
             c.ia = ia;
             c.ib = ib;
             send_command(sm, c, C, tid);
-            pivot_pass<VEC, true>(row, g, sm, true, 0, pivot1, pivot2, ia, ib, warp, lane, tid);
+            pivot_pass<VEC>(row, g, sm, true, 0, pivot1, pivot2, ia, ib, warp, lane, tid);
             cluster_sync();  // every part is in
             int C1 = 0, C2 = 0;
             float M1 = 0.f, M2 = 0.f;
