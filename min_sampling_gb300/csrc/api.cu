@@ -98,7 +98,7 @@ fs_status make_plan(int rows, int vocab, const void* fn, Plan& p) {
     if (cmax > MAX_CLUSTER) cmax = MAX_CLUSTER;
     if (cmax < 1) cmax = 1;
     int chosen = 1;
-    const size_t smem = Layout(p.ns).total;   // row-wide tables in every CTA
+    const size_t smem = Layout(p.ns).total();   // row-wide tables in every CTA
     for (int C = cmax; C >= 1; --C) {
         if (smem > optin) continue;
         int occ = 0;
@@ -111,7 +111,7 @@ fs_status make_plan(int rows, int vocab, const void* fn, Plan& p) {
         }
     }
     p.C = chosen;
-    p.nsc = (p.ns + chosen - 1) / chosen;
+    p.nsc = ((p.ns + chosen - 1) / chosen + 3) & ~3;   // a multiple of 4 segments per CTA
     p.smem = smem;
     if (p.smem > optin) return FS_ERR_UNSUPPORTED;
     return FS_OK;

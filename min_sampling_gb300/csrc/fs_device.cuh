@@ -20,7 +20,10 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
-#define FS_NOINLINE __noinline__
+// Everything on the path of a call is inlined: an out-of-line call saves and restores
+// live registers through the stack, and with most of the SM's on-chip memory given to
+// shared memory those accesses miss L1.  Only rarely taken fallbacks stay out of line.
+#define FS_COLD __noinline__
 
 namespace fsd {
 
@@ -38,6 +41,15 @@ constexpr int MAX_CLUSTER = 8;
 constexpr unsigned FULL = 0xffffffffu;
 
 // Commands from the leader to the other CTAs of the cluster.
+static_assert(HBINS <= NW * 2 * SBH * BLK, "the histogram lives in the staging buffers");
+
+// A (token index, value) pair packed into one 64-bit register.
+__device__ __forceinline__ unsigned long long pack_jx(int j, float x) {
+    return (static_cast<unsigned long long>(static_cast<uint32_t>(j)) << 32) | __float_as_uint(x);
+}
+__device__ __forceinline__ int unpack_j(unsigned long long p) { return static_cast<int>(p >> 32); }
+__device__ __forceinline__ float unpack_x(unsigned long long p) { return __uint_as_float(static_cast<uint32_t>(p)); }
+
 enum : int { CMD_EXIT = 0, CMD_PIVOT2 = 1, CMD_BISECT = 2, CMD_MASSGE = 3, CMD_WRITE = 4, CMD_COLLECT = 5 };
 
 // ------------------------------------------------------------------ geometry
@@ -52,75 +64,62 @@ __host__ __device__ inline int seg_shift_for(int V) {
 }
 
 // A command (written by the leader into every CTA's copy).
-struct Ctl {
+struct alignas(16) Ctl {
     int cmd;
     int ia, ib;            // PIVOT2: which mass arrays receive the per-segment masses
     int flag;              // WRITE: row valid
     float f[4];            // pivots / denominator
     uint32_t u[4];         // key pivots / threshold; u[3] = interval low (BISECT)
     uint32_t hi_lo, hi_hi; // BISECT: 64-bit interval high
+    uint32_t pad[2];
 };
 
 // One CTA's partial results, in the leader's shared memory (one record per rank).
 // Word i < 4 is f[i]; word 4 + i is u[i].
-struct Part {
+struct alignas(16) Part {
     float f[4];
     uint32_t u[12];
 };
 
-// Byte offsets of the dynamic shared-memory carve-up for `ns` segments per row.
+// The dynamic shared-memory carve-up for `ns` segments per row: a fixed header (the
+// command, the parts, reduction scratch), five per-segment arrays of nsp words each,
+// the compact list and the per-warp staging buffers.
 struct Layout {
-    size_t ctl, part, red, misc, segkey, mass0, mass1, mass2, list, lv, li, stage, total;
-    __host__ __device__ explicit Layout(int ns) {
-        size_t o = 0;
-        ctl = o;    o = align16(o + sizeof(Ctl));
-        part = o;   o = align16(o + MAX_CLUSTER * sizeof(Part));
-        red = o;    o = align16(o + 64 * sizeof(int));
-        misc = o;   o = align16(o + 32 * sizeof(int));
-        segkey = o; o = align16(o + size_t(ns) * 4);
-        mass0 = o;  o = align16(o + size_t(ns) * 4);
-        mass1 = o;  o = align16(o + size_t(ns) * 4);
-        mass2 = o;  o = align16(o + size_t(ns) * 4);
-        list = o;   o = align16(o + size_t(ns + 1) * 4);
-        lv = o;     o = align16(o + size_t(CAP) * 4);
-        li = o;     o = align16(o + size_t(CAP) * 4);
-        stage = o;  o = align16(o + size_t(NW) * 2 * SBH * BLK * 4);
-        total = o;
-    }
+    static constexpr size_t CTL = 0;
+    static constexpr size_t PART = align16(CTL + sizeof(Ctl));
+    static constexpr size_t RED = align16(PART + MAX_CLUSTER * sizeof(Part));
+    static constexpr size_t MISC = align16(RED + 64 * sizeof(int));
+    static constexpr size_t ARR = align16(MISC + 32 * sizeof(int));
+    size_t nsp;   // words per per-segment array (ns + 1, rounded up to 4)
+    __host__ __device__ explicit Layout(int ns) : nsp((size_t(ns) + 4) & ~size_t(3)) {}
+    __host__ __device__ size_t arr(int i) const { return ARR + size_t(i) * nsp * 4; }
+    __host__ __device__ size_t lv() const { return arr(5); }
+    __host__ __device__ size_t li() const { return lv() + size_t(CAP) * 4; }
+    __host__ __device__ size_t stage() const { return li() + size_t(CAP) * 4; }
+    __host__ __device__ size_t total() const { return stage() + size_t(NW) * 2 * SBH * BLK * 4; }
 };
 
 extern __shared__ __align__(16) unsigned char smem_raw[];
 
+// Views of the carve-up.  Holds only the segment count, so that it travels in a
+// register: every pointer is recomputed from the shared-memory base.
 struct Smem {
-    Ctl* ctl;            // the current command
-    Part* part;          // [MAX_CLUSTER] partial results (leader)
-    int* red;            // [64] block-reduction scratch
-    float* cmass;        // [MAX_CLUSTER] per-CTA mass above `low` (leader; misc[0..8))
-    int* misc;           // [32]
-    uint32_t* segkey;    // [ns] maximum order key per segment
-    float* mass[3];      // [ns] per-segment masses
-    int* list;           // [ns+1] live-segment list
-    float* lv;           // [CAP] compact list: values (leader); also the histogram
-    int* li;             // [CAP] compact list: token indices (leader)
-    uint32_t* hist;      // [HBINS] aliases lv (used before any list is built)
-    float* stage;        // [NW][2][SBH][BLK] per-warp staging of blocks read from global memory
-    __device__ explicit Smem(int ns) {
-        const Layout L(ns);
-        ctl = reinterpret_cast<Ctl*>(smem_raw + L.ctl);
-        part = reinterpret_cast<Part*>(smem_raw + L.part);
-        red = reinterpret_cast<int*>(smem_raw + L.red);
-        misc = reinterpret_cast<int*>(smem_raw + L.misc);
-        cmass = reinterpret_cast<float*>(misc);
-        segkey = reinterpret_cast<uint32_t*>(smem_raw + L.segkey);
-        mass[0] = reinterpret_cast<float*>(smem_raw + L.mass0);
-        mass[1] = reinterpret_cast<float*>(smem_raw + L.mass1);
-        mass[2] = reinterpret_cast<float*>(smem_raw + L.mass2);
-        list = reinterpret_cast<int*>(smem_raw + L.list);
-        lv = reinterpret_cast<float*>(smem_raw + L.lv);
-        li = reinterpret_cast<int*>(smem_raw + L.li);
-        hist = reinterpret_cast<uint32_t*>(lv);
-        stage = reinterpret_cast<float*>(smem_raw + L.stage);
-    }
+    int ns;
+    __device__ explicit Smem(int ns_) : ns(ns_) {}
+    template <typename T>
+    __device__ __forceinline__ T* at(size_t off) const { return reinterpret_cast<T*>(smem_raw + off); }
+    __device__ __forceinline__ Ctl* ctl() const { return at<Ctl>(Layout::CTL); }            // current command
+    __device__ __forceinline__ Part* part() const { return at<Part>(Layout::PART); }        // [MAX_CLUSTER]
+    __device__ __forceinline__ int* red() const { return at<int>(Layout::RED); }            // [64] scratch
+    __device__ __forceinline__ float* cmass() const { return at<float>(Layout::MISC); }     // [MAX_CLUSTER]
+    __device__ __forceinline__ uint32_t* segkey() const { return at<uint32_t>(Layout(ns).arr(0)); }
+    __device__ __forceinline__ float* mass(int i) const { return at<float>(Layout(ns).arr(1 + i)); }  // i < 3
+    __device__ __forceinline__ int* list() const { return at<int>(Layout(ns).arr(4)); }     // live segments
+    __device__ __forceinline__ float* lv() const { return at<float>(Layout(ns).lv()); }     // [CAP] values
+    __device__ __forceinline__ int* li() const { return at<int>(Layout(ns).li()); }         // [CAP] indices
+    // [HBINS] aliases the staging buffers: written (by every CTA) and read before any staging
+    __device__ __forceinline__ uint32_t* hist() const { return at<uint32_t>(Layout(ns).stage()); }
+    __device__ __forceinline__ float* stage() const { return at<float>(Layout(ns).stage()); }
 };
 
 // The row, its segmentation and this CTA's share.  Segment indices are row-wide.
@@ -212,7 +211,7 @@ __device__ __forceinline__ void add_leader(uint32_t* local_addr, uint32_t n, boo
 // Elements [base, base+4) that straddle the row end, or of an unaligned row: element
 // by element, `fill` past V.  Out of line: the cold path.
 template <bool NC>
-FS_NOINLINE __device__ float4 load4_tail(const float* __restrict__ row, int V, int base, float fill) {
+FS_COLD __device__ float4 load4_tail(const float* __restrict__ row, int V, int base, float fill) {
     float t[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) t[q] = (base + q < V) ? (NC ? __ldg(row + base + q) : row[base + q]) : fill;
@@ -380,7 +379,7 @@ __device__ __forceinline__ float sampler_uniform(unsigned long long seed, unsign
 // index of v.x.  Each lane reads back only what it copied itself, so no warp barrier is
 // needed between the copies and their use.
 template <bool VEC, typename LIVE, typename BODY>
-__device__ __forceinline__ void stream_warp(const float* __restrict__ row, const Geom& g, const Smem& sm, int warp,
+__device__ __forceinline__ void stream_warp(const float* __restrict__ row, Geom g, Smem sm, int warp,
                                             int lane, LIVE live, BODY body) {
     int r0, r1;
     warp_range(g.s1 - g.s0, warp, r0, r1);
@@ -388,7 +387,7 @@ __device__ __forceinline__ void stream_warp(const float* __restrict__ row, const
     r1 += g.s0;
     const int nblk = (r1 - r0) << g.shift;
     const int mask = g.seg_it() - 1;
-    float* st = sm.stage + warp * (2 * SBH * BLK) + lane * 4;
+    float* st = sm.stage() + warp * (2 * SBH * BLK) + lane * 4;
     const int nch = (nblk + SBH - 1) / SBH;
     auto issue = [&](int c) {
         float* dst = st + (c & 1) * (SBH * BLK);
@@ -430,7 +429,7 @@ __device__ __forceinline__ void stream_warp(const float* __restrict__ row, const
 // or negative for probabilities, NaN for logits).  Touches no other CTA, so it may run
 // before the cluster's first barrier completes.
 template <bool VEC, bool NC, bool PROB>
-__device__ __forceinline__ void pass1(const float* __restrict__ row, const Geom& g, const Smem& sm, int warp,
+__device__ __forceinline__ void pass1(const float* __restrict__ row, Geom g, Smem sm, int warp,
                                       int lane, int& pos, bool& bad) {
     int r0, r1;
     warp_range(g.s1 - g.s0, warp, r0, r1);
@@ -491,70 +490,105 @@ __device__ __forceinline__ void pass1(const float* __restrict__ row, const Geom&
                 ss += mine ? s[j] : 0.f;
                 kk = mine ? max(kk, km[j]) : kk;
             }
-            sm.segkey[sg] = kk;
-            if (PROB) sm.mass[0][sg] = ss;
+            sm.segkey()[sg] = kk;
+            if (PROB) sm.mass(0)[sg] = ss;
         }
 #pragma unroll
         for (int j = 0; j < TB; ++j) A[j] = Bv[j];
     }
 }
 
+// Store a 16-byte word into rank r's copy of a shared-memory location.
+__device__ __forceinline__ void st_rank_v4(void* local_addr, uint4 v, uint32_t r, uint32_t self) {
+    if (r == self) {
+        *reinterpret_cast<uint4*>(local_addr) = v;
+    } else {
+        asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(map_rank(smem_u32(local_addr), r)),
+                     "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                     : "memory");
+    }
+}
+
 // After pass 1 and the cluster barrier that follows it, every CTA: its segments'
-// keys and (prob) masses into the leader's table, its totals into the leader's
-// part[rank] (f[0] ordered mass of its segments, u[0] positive count, u[1] bad flag,
-// u[2] maximum key) and, if `hist_shift` >= 0, one histogram count per segment maximum
-// into the leader's histogram (key >> hist_shift), which the leader cleared before
-// that barrier.  Histogram updates are combined per warp (equal bins of a warp add
-// once).  Block-collective.
-FS_NOINLINE __device__ inline void pass1_totals(const Geom& g, const Smem& sm, bool leader, int rank, int pos,
-                                                bool bad, int hist_shift, bool prob, int warp, int lane,
-                                                int tid) {
+// keys and (prob) masses into the leader's table, its totals into part[rank] of every
+// CTA (f[0] ordered mass of its segments, u[0] positive count, u[1] bad flag, u[2]
+// maximum key) and, if `hist_shift` >= 0, one count per segment maximum into the
+// histogram (key >> hist_shift) of every CTA of the cluster, each of which cleared its
+// own before that barrier.  Histogram updates are combined per warp (equal bins of a
+// warp add once).  The CTA's first segment is a multiple of 4, so the table moves in
+// 16-byte words.  Block-collective.
+__device__ __forceinline__ void pass1_totals(Geom g, Smem sm, bool leader, int rank, int C, int pos, bool bad,
+                                             int hist_shift, bool prob, int warp, int lane, int tid) {
     __syncthreads();  // the table written by pass 1
     pos = warp_sum_i(pos);
     const int b = __any_sync(FULL, bad) ? 1 : 0;
     uint32_t km = 0;
+    if (hist_shift >= 0) {
 #pragma unroll 1
-    for (int i0 = g.s0 + warp * 32; i0 < g.s1; i0 += NT) {
-        const int i = i0 + lane;
-        const bool in = i < g.s1;
-        const uint32_t key = in ? sm.segkey[i] : 0u;
-        km = max(km, key);
-        if (hist_shift >= 0) {
+        for (int i0 = g.s0 + warp * 32; i0 < g.s1; i0 += NT) {
+            const int i = i0 + lane;
+            const bool in = i < g.s1;
+            const uint32_t key = in ? sm.segkey()[i] : 0u;
             const uint32_t bin = in ? min(uint32_t(HBINS - 1), key >> hist_shift) : 0xffffffffu;
             const unsigned same = __match_any_sync(FULL, bin);
-            if (in && lane == __ffs(same) - 1) add_leader(&sm.hist[bin], uint32_t(__popc(same)), leader);
+            if (in && lane == __ffs(same) - 1) {
+                uint32_t* h = &sm.hist()[bin];
+                const uint32_t n = uint32_t(__popc(same));
+#pragma unroll 1
+                for (int r = 0; r < C; ++r) {
+                    if (r == rank) {
+                        atomicAdd(h, n);
+                    } else {
+                        asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(map_rank(smem_u32(h), uint32_t(r))),
+                                     "r"(n)
+                                     : "memory");
+                    }
+                }
+            }
         }
-        if (in && !leader) {
-            put_leader(&sm.segkey[i], key, false);
-            if (prob) put_leader(&sm.mass[0][i], __float_as_uint(sm.mass[0][i]), false);
+    }
+#pragma unroll 1
+    for (int i = g.s0 + 4 * tid; i < g.s1; i += 4 * NT) {
+        const uint4 kv = *reinterpret_cast<const uint4*>(&sm.segkey()[i]);
+        const int nv = min(4, g.s1 - i);
+        km = max(km, max(max(kv.x, nv > 1 ? kv.y : 0u), max(nv > 2 ? kv.z : 0u, nv > 3 ? kv.w : 0u)));
+        if (!leader) {
+            if (nv == 4) {
+                st_rank_v4(&sm.segkey()[i], kv, 0, 1);
+                if (prob) st_rank_v4(&sm.mass(0)[i], *reinterpret_cast<const uint4*>(&sm.mass(0)[i]), 0, 1);
+            } else {  // the row's last, partial word: never past this CTA's range
+#pragma unroll 1
+                for (int q = 0; q < nv; ++q) {
+                    put_leader(&sm.segkey()[i + q], sm.segkey()[i + q], false);
+                    if (prob) put_leader(&sm.mass(0)[i + q], __float_as_uint(sm.mass(0)[i + q]), false);
+                }
+            }
         }
     }
     km = warp_max_u(km);
-    float* rf = reinterpret_cast<float*>(sm.red);
+    float* rf = reinterpret_cast<float*>(sm.red());
     if (lane == 0) {
-        sm.red[warp] = pos;
-        sm.red[NW + warp] = b;
-        sm.red[2 * NW + warp] = int(km);
+        sm.red()[warp] = pos;
+        sm.red()[NW + warp] = b;
+        sm.red()[2 * NW + warp] = int(km);
     }
     if (warp == 0) {
-        const float s = prob ? warp_ordered_sum(sm.mass[0], g.s0, g.s1, lane) : 0.f;
+        const float s = prob ? warp_ordered_sum(sm.mass(0), g.s0, g.s1, lane) : 0.f;
         if (lane == 0) rf[3 * NW] = s;
     }
     __syncthreads();
-    if (tid == 0) {
+    if (tid < C) {
         int p = 0, nb = 0;
         uint32_t mk = 0;
 #pragma unroll 1
         for (int w = 0; w < NW; ++w) {
-            p += sm.red[w];
-            nb |= sm.red[NW + w];
-            mk = max(mk, uint32_t(sm.red[2 * NW + w]));
+            p += sm.red()[w];
+            nb |= sm.red()[NW + w];
+            mk = max(mk, uint32_t(sm.red()[2 * NW + w]));
         }
-        uint32_t* dst = reinterpret_cast<uint32_t*>(&sm.part[rank]);
-        put_leader(dst + 0, __float_as_uint(rf[3 * NW]), leader);
-        put_leader(dst + 4, uint32_t(p), leader);
-        put_leader(dst + 5, uint32_t(nb), leader);
-        put_leader(dst + 6, mk, leader);
+        st_rank_v4(&sm.part()[rank].u[0], make_uint4(uint32_t(p), uint32_t(nb), mk, 0u), uint32_t(tid), uint32_t(rank));
+        st_rank_v4(&sm.part()[rank].f[0], make_uint4(__float_as_uint(rf[3 * NW]), 0u, 0u, 0u), uint32_t(tid),
+                   uint32_t(rank));
     }
 }
 
@@ -564,14 +598,14 @@ FS_NOINLINE __device__ inline void pass1_totals(const Geom& g, const Smem& sm, b
 // sums and counts into the leader's part[rank] (f[0], f[1], u[0], u[1]).
 // Block-collective.
 template <bool VEC>
-FS_NOINLINE __device__ void pivot_pass(const float* __restrict__ row, const Geom& g, const Smem& sm, bool leader,
+__device__ __forceinline__ void pivot_pass(const float* __restrict__ row, Geom g, Smem sm, bool leader,
                                        int rank, float p1, float p2, int ia, int ib, int warp, int lane, int tid) {
     const uint32_t kp1 = prob_key(p1);
     const int last = g.seg_it() - 1;
     int c1 = 0, c2 = 0;
     float sa = 0.f, sb = 0.f;
     stream_warp<VEC>(
-        row, g, sm, warp, lane, [&](int sg) { return sm.segkey[sg] > kp1; },
+        row, g, sm, warp, lane, [&](int sg) { return sm.segkey()[sg] > kp1; },
         [&](int sg, int it, bool on, const float4& v, int) {
             float a = 0.f, b = 0.f;
             if (on) {
@@ -590,32 +624,32 @@ FS_NOINLINE __device__ void pivot_pass(const float* __restrict__ row, const Geom
             sa = it ? sa + a : a;
             sb = it ? sb + b : b;
             if (it == last && lane == 0) {
-                sm.mass[ia][sg] = sa;
-                sm.mass[ib][sg] = sb;
+                sm.mass(ia)[sg] = sa;
+                sm.mass(ib)[sg] = sb;
                 if (!leader) {
-                    put_leader(&sm.mass[ia][sg], __float_as_uint(sa), false);
-                    put_leader(&sm.mass[ib][sg], __float_as_uint(sb), false);
+                    put_leader(&sm.mass(ia)[sg], __float_as_uint(sa), false);
+                    put_leader(&sm.mass(ib)[sg], __float_as_uint(sb), false);
                 }
             }
         });
     c1 = warp_sum_i(c1);
     c2 = warp_sum_i(c2);
     if (lane == 0) {
-        sm.red[warp] = c1;
-        sm.red[NW + warp] = c2;
+        sm.red()[warp] = c1;
+        sm.red()[NW + warp] = c2;
     }
     __syncthreads();
     if (warp == 0) {
-        const float t1 = warp_ordered_sum(sm.mass[ia], g.s0, g.s1, lane);
-        const float t2 = warp_ordered_sum(sm.mass[ib], g.s0, g.s1, lane);
+        const float t1 = warp_ordered_sum(sm.mass(ia), g.s0, g.s1, lane);
+        const float t2 = warp_ordered_sum(sm.mass(ib), g.s0, g.s1, lane);
         if (lane == 0) {
             int n1 = 0, n2 = 0;
 #pragma unroll 1
             for (int w = 0; w < NW; ++w) {
-                n1 += sm.red[w];
-                n2 += sm.red[NW + w];
+                n1 += sm.red()[w];
+                n2 += sm.red()[NW + w];
             }
-            uint32_t* dst = reinterpret_cast<uint32_t*>(&sm.part[rank]);
+            uint32_t* dst = reinterpret_cast<uint32_t*>(&sm.part()[rank]);
             put_leader(dst + 0, __float_as_uint(t1), leader);
             put_leader(dst + 1, __float_as_uint(t2), leader);
             put_leader(dst + 4, uint32_t(n1), leader);
@@ -629,7 +663,7 @@ FS_NOINLINE __device__ void pivot_pass(const float* __restrict__ row, const Geom
 
 // Ordered list of the segments s in [a, b) with segkey[s] >= thr, into list[0..n).
 // Block-collective; returns n.
-FS_NOINLINE __device__ inline int live_list(const Smem& sm, int a, int b, uint32_t thr, int warp, int lane) {
+__device__ __forceinline__ int live_list(Smem sm, int a, int b, uint32_t thr, int warp, int lane) {
     int r0, r1;
     warp_range(b - a, warp, r0, r1);
     r0 += a;
@@ -638,22 +672,22 @@ FS_NOINLINE __device__ inline int live_list(const Smem& sm, int a, int b, uint32
 #pragma unroll 1
     for (int base = r0; base < r1; base += 32) {
         const int i = base + lane;
-        cnt += __popc(__ballot_sync(FULL, i < r1 && sm.segkey[i] >= thr));
+        cnt += __popc(__ballot_sync(FULL, i < r1 && sm.segkey()[i] >= thr));
     }
-    if (lane == 0) sm.red[warp] = cnt;
+    if (lane == 0) sm.red()[warp] = cnt;
     __syncthreads();
     int off = 0, total = 0;
 #pragma unroll 1
     for (int w = 0; w < NW; ++w) {
-        if (w < warp) off += sm.red[w];
-        total += sm.red[w];
+        if (w < warp) off += sm.red()[w];
+        total += sm.red()[w];
     }
 #pragma unroll 1
     for (int base = r0; base < r1; base += 32) {
         const int i = base + lane;
-        const bool live = i < r1 && sm.segkey[i] >= thr;
+        const bool live = i < r1 && sm.segkey()[i] >= thr;
         const unsigned bal = __ballot_sync(FULL, live);
-        if (live) sm.list[off + __popc(bal & ((1u << lane) - 1u))] = i;
+        if (live) sm.list()[off + __popc(bal & ((1u << lane) - 1u))] = i;
         off += __popc(bal);
     }
     __syncthreads();
@@ -665,12 +699,12 @@ FS_NOINLINE __device__ inline int live_list(const Smem& sm, int a, int b, uint32
 // count.  Each batch stages 2*SBH listed blocks per warp (cp.async), counts, fixes the
 // warps' output offsets, then emits.  Block-collective.
 template <bool VEC, typename KEYF, typename OUT>
-__device__ __forceinline__ int collect(const float* __restrict__ row, const Geom& g, const Smem& sm, int nlive,
+__device__ __forceinline__ int collect(const float* __restrict__ row, Geom g, Smem sm, int nlive,
                                        uint32_t thr, KEYF keyf, int warp, int lane, OUT out) {
     constexpr int WB = 2 * SBH;
     const int nblk = nlive << g.shift;
     const int mask = g.seg_it() - 1;
-    float* st = sm.stage + warp * (WB * BLK) + lane * 4;
+    float* st = sm.stage() + warp * (WB * BLK) + lane * 4;
     int total = 0;
 #pragma unroll 1
     for (int c0 = 0; c0 < nblk; c0 += NW * WB) {
@@ -679,7 +713,7 @@ __device__ __forceinline__ int collect(const float* __restrict__ row, const Geom
 #pragma unroll 1
         for (int j = 0; j < nb; ++j) {
             const int lb = w0 + j;
-            stage4<VEC>(st + j * BLK, row, g.V, g.base(sm.list[lb >> g.shift], lb & mask, lane));
+            stage4<VEC>(st + j * BLK, row, g.V, g.base(sm.list()[lb >> g.shift], lb & mask, lane));
         }
         cp_async_commit();
         cp_async_wait<0>();
@@ -687,24 +721,24 @@ __device__ __forceinline__ int collect(const float* __restrict__ row, const Geom
 #pragma unroll 1
         for (int j = 0; j < nb; ++j) {
             const int lb = w0 + j;
-            const int base = g.base(sm.list[lb >> g.shift], lb & mask, lane);
+            const int base = g.base(sm.list()[lb >> g.shift], lb & mask, lane);
 #pragma unroll
             for (int q = 0; q < 4; ++q) cnt += (keyf(st[j * BLK + q]) >= thr && base + q < g.V);
         }
         cnt = warp_sum_i(cnt);
-        if (lane == 0) sm.red[warp] = cnt;
+        if (lane == 0) sm.red()[warp] = cnt;
         __syncthreads();
         int pos = total, chunk = 0;
 #pragma unroll 1
         for (int w = 0; w < NW; ++w) {
-            if (w < warp) pos += sm.red[w];
-            chunk += sm.red[w];
+            if (w < warp) pos += sm.red()[w];
+            chunk += sm.red()[w];
         }
         __syncthreads();
 #pragma unroll 1
         for (int j = 0; j < nb; ++j) {
             const int lb = w0 + j;
-            const int base = g.base(sm.list[lb >> g.shift], lb & mask, lane);
+            const int base = g.base(sm.list()[lb >> g.shift], lb & mask, lane);
             int k = 0;
 #pragma unroll
             for (int q = 0; q < 4; ++q) k += (keyf(st[j * BLK + q]) >= thr && base + q < g.V);
@@ -723,23 +757,37 @@ __device__ __forceinline__ int collect(const float* __restrict__ row, const Geom
 }
 
 // Every CTA: collect its own elements with key >= thr into its region of the leader's
-// list (entries [rank * rc, rank * rc + rc)), in index order; the exact count goes to
-// part[rank].u[4] of every CTA of the cluster, so that after the next cluster barrier
-// each CTA can tell whether all regions fit.  Block-collective.
+// list (entries [rank * rc, rank * rc + rc)), in index order, or with `to_all` into
+// that region of every CTA's list; the exact count goes to part[rank].u[4] of every CTA
+// of the cluster, so that after the next cluster barrier each CTA can tell whether all
+// regions fit.  Block-collective.
 template <bool VEC, typename KEYF>
-FS_NOINLINE __device__ void collect_own(const float* __restrict__ row, const Geom& g, const Smem& sm, bool leader,
-                                        int rank, int C, int rc, uint32_t thr, KEYF keyf, int warp, int lane,
-                                        int tid) {
+__device__ __forceinline__ void collect_own(const float* __restrict__ row, Geom g, Smem sm, bool leader, int rank,
+                                            int C, int rc, uint32_t thr, KEYF keyf, bool to_all, int warp, int lane,
+                                            int tid) {
     const int nlive = live_list(sm, g.s0, g.s1, thr, warp, lane);
     const int base = rank * rc;
     const int n = collect<VEC>(row, g, sm, nlive, thr, keyf, warp, lane, [&](int p, float x, int ix) {
         if (p < rc) {
-            put_leader(&sm.lv[base + p], __float_as_uint(x), leader);
-            put_leader(&sm.li[base + p], uint32_t(ix), leader);
+            if (to_all) {
+#pragma unroll 1
+                for (int r = 0; r < C; ++r) {
+                    if (r == rank) {
+                        sm.lv()[base + p] = x;
+                        sm.li()[base + p] = ix;
+                    } else {
+                        st_dsmem_u32(map_rank(smem_u32(&sm.lv()[base + p]), uint32_t(r)), __float_as_uint(x));
+                        st_dsmem_u32(map_rank(smem_u32(&sm.li()[base + p]), uint32_t(r)), uint32_t(ix));
+                    }
+                }
+            } else {
+                put_leader(&sm.lv()[base + p], __float_as_uint(x), leader);
+                put_leader(&sm.li()[base + p], uint32_t(ix), leader);
+            }
         }
     });
     if (tid < C) {
-        uint32_t* dst = reinterpret_cast<uint32_t*>(&sm.part[rank]) + 8;
+        uint32_t* dst = reinterpret_cast<uint32_t*>(&sm.part()[rank]) + 8;
         if (tid == rank) {
             *dst = uint32_t(n);
         } else {
@@ -750,44 +798,45 @@ FS_NOINLINE __device__ void collect_own(const float* __restrict__ row, const Geo
 
 // After the barrier that follows collect_own: whether every rank's candidates fit in
 // its region.  Any CTA (each holds every count).
-__device__ __forceinline__ bool regions_fit(const Smem& sm, int C, int rc) {
+__device__ __forceinline__ bool regions_fit(Smem sm, int C, int rc) {
     bool fits = true;
 #pragma unroll 1
-    for (int r = 0; r < C; ++r) fits = fits && int(sm.part[r].u[4]) <= rc;
+    for (int r = 0; r < C; ++r) fits = fits && int(sm.part()[r].u[4]) <= rc;
     return fits;
 }
-__device__ __forceinline__ int regions_total(const Smem& sm, int C) {
+__device__ __forceinline__ int regions_total(Smem sm, int C) {
     int n = 0;
 #pragma unroll 1
-    for (int r = 0; r < C; ++r) n += int(sm.part[r].u[4]);
+    for (int r = 0; r < C; ++r) n += int(sm.part()[r].u[4]);
     return n;
 }
 
-// Leader: the candidate regions of all ranks, concatenated in rank order at the front
-// of lv/li.  Returns the total (the caller checked that every region fit).  Regions
-// move only towards the front, and every thread reads its entries before any write.
-FS_NOINLINE __device__ inline int join_regions(const Smem& sm, int C, int rc, int tid) {
+// The candidate regions of all ranks, concatenated in rank order at the front of
+// lv/li, by one warp.  Returns the total (the caller checked that every region fit).
+// Regions only move towards the front and each chunk of 32 is read before it is
+// written, so no entry is overwritten before it has been read.
+__device__ __forceinline__ int join_regions_warp(Smem sm, int C, int rc, int lane) {
     int dst = 0;
 #pragma unroll 1
     for (int c = 0; c < C; ++c) {
-        const int n = int(sm.part[c].u[4]);
+        const int n = int(sm.part()[c].u[4]);
         const int src = c * rc;
         if (src != dst) {
 #pragma unroll 1
-            for (int e0 = 0; e0 < n; e0 += NT) {
-                const int e = e0 + tid;
+            for (int e0 = 0; e0 < n; e0 += 32) {
+                const int e = e0 + lane;
                 float v = 0.f;
                 int ix = 0;
                 if (e < n) {
-                    v = sm.lv[src + e];
-                    ix = sm.li[src + e];
+                    v = sm.lv()[src + e];
+                    ix = sm.li()[src + e];
                 }
-                __syncthreads();
+                __syncwarp();
                 if (e < n) {
-                    sm.lv[dst + e] = v;
-                    sm.li[dst + e] = ix;
+                    sm.lv()[dst + e] = v;
+                    sm.li()[dst + e] = ix;
                 }
-                __syncthreads();
+                __syncwarp();
             }
         }
         dst += n;
@@ -795,47 +844,57 @@ FS_NOINLINE __device__ inline int join_regions(const Smem& sm, int C, int rc, in
     return dst;
 }
 
-// Largest key t among the keys of lv[0..n) with #{key >= t} >= k; 0 if none.
-// Block-collective (rank counting; the list is short).
+// The k-th largest order key among lv[0..n) (0 if n < k), by one warp: the largest t
+// with #{key >= t} >= k, built bit by bit from the top (a count is monotone in t, so
+// each bit is kept when the count at the raised threshold still reaches k).  The
+// result is a key present in the list.
 template <typename KEYF>
-FS_NOINLINE __device__ uint32_t kth_key_in_list(const Smem& sm, int n, int k, KEYF keyf, int warp, int lane,
-                                                int tid) {
-    uint32_t best = 0;
+__device__ __forceinline__ uint32_t kth_key_warp(Smem sm, int n, int k, KEYF keyf, int lane) {
+    if (n < k) return 0u;
+    uint32_t lo = 0xffffffffu, hi = 0u;
 #pragma unroll 1
-    for (int i = tid; i < n; i += NT) {
-        const uint32_t ki = keyf(sm.lv[i]);
-        int ge = 0;
-#pragma unroll 4
-        for (int j = 0; j < n; ++j) ge += (keyf(sm.lv[j]) >= ki);
-        if (ge >= k) best = max(best, ki);
+    for (int i = lane; i < n; i += 32) {
+        const uint32_t key = keyf(sm.lv()[i]);
+        lo = min(lo, key);
+        hi = max(hi, key);
     }
-    best = warp_max_u(best);
-    if (lane == 0) sm.red[warp] = int(best);
-    __syncthreads();
-    uint32_t r = 0;
+    lo = warp_min_u(lo);
+    hi = warp_max_u(hi);
+    // Every key shares the bits above the highest bit where lo and hi differ.
+    const int top = 31 - __clz(int(lo ^ hi) | 1);
+    uint32_t t = lo & ~((2u << top) - 1u);
+    if ((lo ^ hi) == 0u) return lo;
 #pragma unroll 1
-    for (int w = 0; w < NW; ++w) r = max(r, uint32_t(sm.red[w]));
-    __syncthreads();
-    return r;
+    for (int bit = top; bit >= 0; --bit) {
+        const uint32_t cand = t | (1u << bit);
+        int cnt = 0;
+#pragma unroll 1
+        for (int i0 = 0; i0 < n; i0 += 32) {
+            const int i = i0 + lane;
+            cnt += __popc(__ballot_sync(FULL, i < n && keyf(sm.lv()[i]) >= cand));
+        }
+        if (cnt >= k) t = cand;
+    }
+    return t;
 }
 
 // In-place, order-preserving filter of lv/li[0..n) to key >= t by one warp.
 // Returns the new length (warp-uniform).
 template <typename KEYF>
-FS_NOINLINE __device__ int filter_list_warp(const Smem& sm, int n, uint32_t t, KEYF keyf, int lane) {
+__device__ __forceinline__ int filter_list_warp(Smem sm, int n, uint32_t t, KEYF keyf, int lane) {
     int w = 0;
 #pragma unroll 1
     for (int base = 0; base < n; base += 32) {
         const int i = base + lane;
-        const bool keep = i < n && keyf(sm.lv[i]) >= t;
-        const float xv = keep ? sm.lv[i] : 0.f;
-        const int xi = keep ? sm.li[i] : 0;
+        const bool keep = i < n && keyf(sm.lv()[i]) >= t;
+        const float xv = keep ? sm.lv()[i] : 0.f;
+        const int xi = keep ? sm.li()[i] : 0;
         const unsigned bal = __ballot_sync(FULL, keep);
         const int pos = w + __popc(bal & ((1u << lane) - 1u));
         __syncwarp();
         if (keep) {
-            sm.lv[pos] = xv;
-            sm.li[pos] = xi;
+            sm.lv()[pos] = xv;
+            sm.li()[pos] = xi;
         }
         __syncwarp();
         w += __popc(bal);
@@ -850,7 +909,7 @@ FS_NOINLINE __device__ int filter_list_warp(const Smem& sm, int n, uint32_t t, K
 // of the row (here, the segment maxima) is at most the row's own k-th largest, so
 // L0 <= t_k, and every segment holding an element >= t_k has its maximum >= L0.
 // Returns 0 when there are fewer than k segments.
-FS_NOINLINE __device__ inline uint32_t hist_bound(const Smem& sm, int ns, int k, int bshift, int warp, int lane,
+__device__ __forceinline__ uint32_t hist_bound(Smem sm, int ns, int k, int bshift, int warp, int lane,
                                                   int tid) {
     if (ns < k) return 0;
     // Thread t owns positions 4t..4t+3 counted from the top bin (bins HBINS-1-pos).
@@ -858,7 +917,7 @@ FS_NOINLINE __device__ inline uint32_t hist_bound(const Smem& sm, int ns, int k,
     uint32_t own = 0;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        c[q] = sm.hist[HBINS - 1 - (4 * tid + q)];
+        c[q] = sm.hist()[HBINS - 1 - (4 * tid + q)];
         own += c[q];
     }
     uint32_t incl = own;
@@ -867,11 +926,11 @@ FS_NOINLINE __device__ inline uint32_t hist_bound(const Smem& sm, int ns, int k,
         const uint32_t o = __shfl_up_sync(FULL, incl, d);
         if (lane >= d) incl += o;
     }
-    if (lane == 31) sm.red[warp] = int(incl);
+    if (lane == 31) sm.red()[warp] = int(incl);
     __syncthreads();
     uint32_t before = incl - own;
 #pragma unroll 1
-    for (int w = 0; w < warp; ++w) before += uint32_t(sm.red[w]);
+    for (int w = 0; w < warp; ++w) before += uint32_t(sm.red()[w]);
     const uint32_t kk = uint32_t(k);
     if (before < kk && before + own >= kk) {
         uint32_t cum = before;
@@ -884,10 +943,10 @@ FS_NOINLINE __device__ inline uint32_t hist_bound(const Smem& sm, int ns, int k,
                 break;
             }
         }
-        sm.red[NW] = HBINS - 1 - pos;
+        sm.red()[NW] = HBINS - 1 - pos;
     }
     __syncthreads();
-    const uint32_t bin = uint32_t(sm.red[NW]);
+    const uint32_t bin = uint32_t(sm.red()[NW]);
     __syncthreads();
     return bin << bshift;
 }
@@ -899,10 +958,10 @@ FS_NOINLINE __device__ inline uint32_t hist_bound(const Smem& sm, int ns, int k,
 // monotone, so the result is always forced onto an eligible token).  Eligible: x >
 // low.  `t` is the target measured from the segment start.  Returns the first
 // eligible element whose running sum exceeds t, else the segment's last eligible
-// element.  The segment must hold an eligible element.
+// element (-1 if none), packed with its value.
 template <bool VEC, bool NC>
-FS_NOINLINE __device__ void locate_in_segment(const float* __restrict__ row, const Geom& g, int s, float low, float t,
-                                              int lane, int* j_out, float* x_out) {
+__device__ __forceinline__ unsigned long long locate_in_segment(const float* __restrict__ row, Geom g, int s, float low,
+                                                            float t, int lane) {
     float run = 0.f;
     int last_j = -1;
     float last_x = 0.f;
@@ -944,19 +1003,17 @@ FS_NOINLINE __device__ void locate_in_segment(const float* __restrict__ row, con
                 }
             }
             if (pq < 0) pq = lastq;
-            *j_out = __shfl_sync(FULL, base + pq, l);
-            *x_out = __shfl_sync(FULL, q_at(v, pq), l);
-            return;
+            return pack_jx(__shfl_sync(FULL, base + pq, l), __shfl_sync(FULL, q_at(v, pq), l));
         }
         run += __shfl_sync(FULL, incl, 31);
     }
-    *j_out = last_j;
-    *x_out = last_x;
+    return pack_jx(last_j, last_x);
 }
 
-// First segment in [a, b) whose running mass over mass[] exceeds t (the mass before
-// it in *before); if none, the last segment with positive mass.  Warp-collective.
-FS_NOINLINE __device__ inline int locate_segment(const float* mass, int a, int b, float t, int lane, float* before) {
+// First segment in [a, b) whose running mass over mass[] exceeds t; if none, the last
+// segment with positive mass (-1 if none).  Packed with the mass before it.
+// Warp-collective.
+__device__ __forceinline__ unsigned long long locate_segment(const float* mass, int a, int b, float t, int lane) {
     float run = 0.f;
     int last = -1;
     float last_before = 0.f;
@@ -973,17 +1030,15 @@ FS_NOINLINE __device__ inline int locate_segment(const float* mass, int a, int b
         }
         if (hit) {
             const int l = __ffs(hit) - 1;
-            *before = run + __shfl_sync(FULL, incl - m, l);
-            return base + l;
+            return pack_jx(base + l, run + __shfl_sync(FULL, incl - m, l));
         }
         run += __shfl_sync(FULL, incl, 31);
     }
-    *before = last_before;
-    return last;
+    return pack_jx(last, last_before);
 }
 
 // Locate inside a compact list lv[0..n) (index order), eligible x > low.  Warp-collective.
-FS_NOINLINE __device__ inline int locate_in_list(const float* lv, int n, float low, float t, int lane) {
+__device__ __forceinline__ int locate_in_list(const float* lv, int n, float low, float t, int lane) {
     float run = 0.f;
     int last = -1;
 #pragma unroll 1
@@ -1030,18 +1085,29 @@ FS_NOINLINE __device__ inline int locate_in_list(const float* lv, int n, float l
 
 // ------------------------------------------------------------------ commands
 
-// Leader: publish a command into every CTA's Ctl (DSMEM stores), then the cluster
-// barrier after which the peers read it.  Block-collective on the leader.
-__device__ __forceinline__ void send_command(const Smem& sm, const Ctl& c, int C, int tid) {
-    constexpr int W = sizeof(Ctl) / 4;
-    const uint32_t* src = reinterpret_cast<const uint32_t*>(&c);
-    if (tid < C * W) {
-        const int r = tid / W, o = tid % W;
-        uint32_t* dst = reinterpret_cast<uint32_t*>(sm.ctl) + o;
-        if (r == 0) {
-            *dst = src[o];
-        } else {
-            st_dsmem_u32(map_rank(smem_u32(dst), r), src[o]);
+// Leader: publish a command into every CTA's Ctl (thread r writes rank r's copy, four
+// 16-byte stores), then the cluster barrier after which the peers read it.
+// Block-collective on the leader.
+__device__ __forceinline__ void send_command(Smem sm, const Ctl& c, int C, int tid) {
+    static_assert(sizeof(Ctl) == 64, "Ctl is four 16-byte words");
+    if (tid < C) {
+        const uint4 w[4] = {
+            make_uint4(uint32_t(c.cmd), uint32_t(c.ia), uint32_t(c.ib), uint32_t(c.flag)),
+            make_uint4(__float_as_uint(c.f[0]), __float_as_uint(c.f[1]), __float_as_uint(c.f[2]),
+                       __float_as_uint(c.f[3])),
+            make_uint4(c.u[0], c.u[1], c.u[2], c.u[3]),
+            make_uint4(c.hi_lo, c.hi_hi, 0u, 0u)};
+        uint4* dst = reinterpret_cast<uint4*>(sm.ctl());
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (tid == 0) {
+                dst[i] = w[i];
+            } else {
+                asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                 map_rank(smem_u32(dst + i), uint32_t(tid))),
+                             "r"(w[i].x), "r"(w[i].y), "r"(w[i].z), "r"(w[i].w)
+                             : "memory");
+            }
         }
     }
     cluster_sync();
@@ -1053,16 +1119,15 @@ __device__ __forceinline__ void send_command(const Smem& sm, const Ctl& c, int C
 // The CTA's record goes to the leader's part[rank]: f[0..2] masses, u[0..2] counts,
 // u[3..6] min keys, u[7..10] max keys.  Block-collective.
 template <bool VEC, bool MASS, typename KEYF>
-FS_NOINLINE __device__ void bisect_pass(const float* __restrict__ row, const Geom& g, const Smem& sm, bool leader,
-                                        int rank, uint64_t lo, uint64_t hi, const uint32_t* piv, KEYF keyf,
-                                        int warp, int lane, int tid) {
-    const uint32_t p0 = piv[0], p1 = piv[1], p2 = piv[2];
+FS_COLD __device__ void bisect_pass(const float* __restrict__ row, Geom g, Smem sm, bool leader,
+                                        int rank, uint64_t lo, uint64_t hi, uint32_t p0, uint32_t p1, uint32_t p2,
+                                        KEYF keyf, int warp, int lane, int tid) {
     float m[3] = {0.f, 0.f, 0.f};
     int c[3] = {0, 0, 0};
     uint32_t mn[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
     uint32_t mx[4] = {0u, 0u, 0u, 0u};
     stream_warp<VEC>(
-        row, g, sm, warp, lane, [&](int sg) { return uint64_t(sm.segkey[sg]) >= lo; },
+        row, g, sm, warp, lane, [&](int sg) { return uint64_t(sm.segkey()[sg]) >= lo; },
         [&](int, int, bool on, const float4& v, int base) {
             if (!on) return;
 #pragma unroll 1
@@ -1090,8 +1155,8 @@ FS_NOINLINE __device__ void bisect_pass(const float* __restrict__ row, const Geo
             }
         });
     // warp -> block (fixed order) -> the leader's part[rank]
-    float* rf = reinterpret_cast<float*>(sm.red);
-    uint32_t* ru = reinterpret_cast<uint32_t*>(sm.red);
+    float* rf = reinterpret_cast<float*>(sm.red());
+    uint32_t* ru = reinterpret_cast<uint32_t*>(sm.red());
 #pragma unroll
     for (int i = 0; i < 3; ++i) {
         m[i] = warp_sum(m[i]);
@@ -1135,7 +1200,7 @@ FS_NOINLINE __device__ void bisect_pass(const float* __restrict__ row, const Geo
     }
     __syncthreads();
     if (tid == 0) {
-        uint32_t* dst = reinterpret_cast<uint32_t*>(&sm.part[rank]);
+        uint32_t* dst = reinterpret_cast<uint32_t*>(&sm.part()[rank]);
 #pragma unroll 1
         for (int t = 0; t < 4; ++t) {
             uint32_t a = 0xffffffffu, b = 0u;
@@ -1158,12 +1223,12 @@ FS_NOINLINE __device__ void bisect_pass(const float* __restrict__ row, const Geo
 // Count and mass (x > 0) of key >= t over this CTA's segments; the record goes to the
 // leader's part[rank] (f[0] mass, u[0] count).  Block-collective.
 template <bool VEC, typename KEYF>
-FS_NOINLINE __device__ void massge_pass(const float* __restrict__ row, const Geom& g, const Smem& sm, bool leader,
+FS_COLD __device__ void massge_pass(const float* __restrict__ row, Geom g, Smem sm, bool leader,
                                         int rank, uint32_t t, KEYF keyf, int warp, int lane, int tid) {
     float ms = 0.f;
     int cnt = 0;
     stream_warp<VEC>(
-        row, g, sm, warp, lane, [&](int sg) { return sm.segkey[sg] >= t; },
+        row, g, sm, warp, lane, [&](int sg) { return sm.segkey()[sg] >= t; },
         [&](int, int, bool on, const float4& v, int base) {
             if (!on) return;
 #pragma unroll
@@ -1176,10 +1241,10 @@ FS_NOINLINE __device__ void massge_pass(const float* __restrict__ row, const Geo
         });
     ms = warp_sum(ms);
     cnt = warp_sum_i(cnt);
-    float* rf = reinterpret_cast<float*>(sm.red);
+    float* rf = reinterpret_cast<float*>(sm.red());
     if (lane == 0) {
         rf[warp] = ms;
-        sm.red[NW + warp] = cnt;
+        sm.red()[NW + warp] = cnt;
     }
     __syncthreads();
     if (tid == 0) {
@@ -1188,9 +1253,9 @@ FS_NOINLINE __device__ void massge_pass(const float* __restrict__ row, const Geo
 #pragma unroll 1
         for (int w = 0; w < NW; ++w) {
             a += rf[w];
-            n += sm.red[NW + w];
+            n += sm.red()[NW + w];
         }
-        uint32_t* dst = reinterpret_cast<uint32_t*>(&sm.part[rank]);
+        uint32_t* dst = reinterpret_cast<uint32_t*>(&sm.part()[rank]);
         put_leader(dst, __float_as_uint(a), leader);
         put_leader(dst + 4, uint32_t(n), leader);
     }
@@ -1224,7 +1289,7 @@ __device__ __forceinline__ void bisect_pivots(const Bisect& st, uint32_t* piv) {
 // Fold the C parts of a bisection pass into the interval ([drill] section 5: take the
 // largest pivot where the criterion holds; shrink to the keys present).
 template <bool MASS>
-__device__ __forceinline__ void bisect_update(const Smem& sm, int C, Bisect& st, const uint32_t* piv, int kcrit,
+__device__ __forceinline__ void bisect_update(Smem sm, int C, Bisect& st, const uint32_t* piv, int kcrit,
                                               float target) {
     float mass[3] = {0.f, 0.f, 0.f};
     int cnt[3] = {0, 0, 0};
@@ -1235,7 +1300,7 @@ __device__ __forceinline__ void bisect_update(const Smem& sm, int C, Bisect& st,
         kmax[t] = 0u;
     }
     for (int c = 0; c < C; ++c) {
-        const Part& p = sm.part[c];
+        const Part& p = sm.part()[c];
 #pragma unroll
         for (int i = 0; i < 3; ++i) {
             mass[i] += p.f[i];
@@ -1273,10 +1338,8 @@ __device__ __forceinline__ void bisect_update(const Smem& sm, int C, Bisect& st,
 
 // Leader: drive a bisection to the end with the whole cluster (at most 40 passes).
 template <bool VEC, bool MASS, typename KEYF>
-FS_NOINLINE __device__ void bisect_leader(const float* __restrict__ row, const Geom& g, const Smem& sm, int C,
-                                          Bisect* stp, int kcrit, float target, KEYF keyf, int warp, int lane,
-                                          int tid) {
-    Bisect st = *stp;
+__device__ __forceinline__ void bisect_leader(const float* __restrict__ row, Geom g, Smem sm, int C, Bisect& st,
+                                              int kcrit, float target, KEYF keyf, int warp, int lane, int tid) {
     for (int iter = 0; iter < 40 && st.hi - st.lo > 1; ++iter) {
         uint32_t piv[3];
         bisect_pivots(st, piv);
@@ -1289,19 +1352,18 @@ FS_NOINLINE __device__ void bisect_leader(const float* __restrict__ row, const G
         c.hi_lo = uint32_t(st.hi);
         c.hi_hi = uint32_t(st.hi >> 32);
         send_command(sm, c, C, tid);
-        bisect_pass<VEC, MASS>(row, g, sm, true, 0, st.lo, st.hi, piv, keyf, warp, lane, tid);
+        bisect_pass<VEC, MASS>(row, g, sm, true, 0, st.lo, st.hi, piv[0], piv[1], piv[2], keyf, warp, lane, tid);
         cluster_sync();  // every part is in
         bisect_update<MASS>(sm, C, st, piv, kcrit, target);
         __syncthreads();
     }
-    *stp = st;
 }
 
-// Leader: count and mass of key >= t over the whole row, with the cluster.
+// Leader: mass of the positive elements with key >= t over the whole row, with the
+// cluster.
 template <bool VEC, typename KEYF>
-FS_NOINLINE __device__ void massge_leader(const float* __restrict__ row, const Geom& g, const Smem& sm, int C,
-                                          uint32_t t, KEYF keyf, int warp, int lane, int tid, float* mass_out,
-                                          int* cnt_out) {
+FS_COLD __device__ float massge_leader(const float* __restrict__ row, Geom g, Smem sm, int C, uint32_t t,
+                                           KEYF keyf, int warp, int lane, int tid) {
     Ctl c{};
     c.cmd = CMD_MASSGE;
     c.u[0] = t;
@@ -1309,58 +1371,54 @@ FS_NOINLINE __device__ void massge_leader(const float* __restrict__ row, const G
     massge_pass<VEC>(row, g, sm, true, 0, t, keyf, warp, lane, tid);
     cluster_sync();
     float m = 0.f;
-    int n = 0;
-    for (int r = 0; r < C; ++r) {
-        m += sm.part[r].f[0];
-        n += int(sm.part[r].u[0]);
-    }
+#pragma unroll 1
+    for (int r = 0; r < C; ++r) m += sm.part()[r].f[0];
     __syncthreads();
-    *mass_out = m;
-    *cnt_out = n;
+    return m;
 }
 
 // Leader alone: every element of the row with key >= thr into lv/li[0..n) in index
 // order, read through the leader's full segment table.  Returns the exact count
 // (entries beyond CAP are dropped).  Block-collective.
 template <bool VEC, typename KEYF>
-FS_NOINLINE __device__ int collect_all(const float* __restrict__ row, const Geom& g, const Smem& sm, uint32_t thr,
+FS_COLD __device__ int collect_all(const float* __restrict__ row, Geom g, Smem sm, uint32_t thr,
                                        KEYF keyf, int warp, int lane) {
     const int nlive = live_list(sm, 0, g.ns, thr, warp, lane);
     return collect<VEC>(row, g, sm, nlive, thr, keyf, warp, lane, [&](int p, float x, int ix) {
         if (p < CAP) {
-            sm.lv[p] = x;
-            sm.li[p] = ix;
+            sm.lv()[p] = x;
+            sm.li()[p] = ix;
         }
     });
 }
 
-// Leader: every element with key >= thr, in index order, into lv/li[0..n).  The whole
-// cluster collects (each CTA its own segments, into its region of the leader's list);
-// if a region overflowed but the total fits, the leader collects alone.  Returns n, or
-// -1 when more than CAP elements qualify (the peers then still wait for commands).
-// With `exit_if_fit` the peers leave once the list is complete (*peers = false).
+// Leader: every element with key >= thr, in index order, into lv/li[0..n), on the
+// leader's command.  The whole cluster collects (each CTA its own segments, into its
+// region of the leader's list); if a region overflowed but the total fits, the leader
+// collects alone.  Returns n, or -1 when more than CAP elements qualify (the peers then
+// still wait for commands).  With `exit_if_fit` the peers have left whenever n >= 0.
 template <bool VEC, typename KEYF>
-FS_NOINLINE __device__ int gather_leader(const float* __restrict__ row, const Geom& g, const Smem& sm, int C,
-                                         uint32_t thr, KEYF keyf, bool exit_if_fit, bool* peers, int warp, int lane,
-                                         int tid) {
+__device__ __forceinline__ int gather_leader(const float* __restrict__ row, Geom g, Smem sm, int C, uint32_t thr,
+                                         KEYF keyf, bool exit_if_fit, int warp, int lane, int tid) {
     const int rc = CAP / C;
     Ctl c{};
     c.cmd = CMD_COLLECT;
     c.flag = exit_if_fit ? 1 : 0;
     c.u[0] = thr;
     send_command(sm, c, C, tid);
-    collect_own<VEC>(row, g, sm, true, 0, C, rc, thr, keyf, warp, lane, tid);
+    collect_own<VEC>(row, g, sm, true, 0, C, rc, thr, keyf, false, warp, lane, tid);
     cluster_sync();  // every region and count is in
+    const int n = regions_total(sm, C);
     if (regions_fit(sm, C, rc)) {
-        if (exit_if_fit) *peers = false;
-        return join_regions(sm, C, rc, tid);
+        if (warp == 0) join_regions_warp(sm, C, rc, lane);
+        __syncthreads();
+        return n;
     }
-    if (regions_total(sm, C) > CAP) return -1;
+    if (n > CAP) return -1;
     if (exit_if_fit) {
         Ctl e{};
         e.cmd = CMD_EXIT;
         send_command(sm, e, C, tid);
-        *peers = false;
     }
     return collect_all<VEC>(row, g, sm, thr, keyf, warp, lane);
 }

@@ -38,15 +38,15 @@ struct FilterArgs {
 // Write this CTA's segments: keep key >= t (x / denom, or the logit), else fill.
 // Segments whose maximum key is below t are written without being read.
 template <bool VEC, int KIND>
-FS_NOINLINE __device__ void write_pass(const float* __restrict__ row, float* __restrict__ orow, const Geom& g,
-                                       const Smem& sm, bool valid, uint32_t t, float denom, int warp, int lane) {
+__device__ __forceinline__ void write_pass(const float* __restrict__ row, float* __restrict__ orow, Geom g,
+                                       Smem sm, bool valid, uint32_t t, float denom, int warp, int lane) {
     using KEYF = typename std::conditional<KIND == K_MASK, KeyLogit, KeyProb>::type;
     constexpr bool IS_PROB = KIND != K_MASK;
     const KEYF keyf;
     const float fill = IS_PROB ? 0.f : __int_as_float(0xff800000);
     const bool vec_out = VEC && ((reinterpret_cast<uintptr_t>(orow) & 15) == 0);
     stream_warp<VEC>(
-        row, g, sm, warp, lane, [&](int sg) { return valid && sm.segkey[sg] >= t; },
+        row, g, sm, warp, lane, [&](int sg) { return valid && sm.segkey()[sg] >= t; },
         [&](int, int, bool on, const float4& v, int base) {
             float o[4];
 #pragma unroll
@@ -66,22 +66,23 @@ FS_NOINLINE __device__ void write_pass(const float* __restrict__ row, float* __r
 
 // The other CTAs: follow the leader's commands until the write.
 template <bool VEC, int KIND>
-FS_NOINLINE __device__ void filter_peer(const float* __restrict__ row, float* __restrict__ orow, const Geom& g,
-                                        const Smem& sm, int rank, int C, int warp, int lane, int tid) {
+__device__ __forceinline__ void filter_peer(const float* __restrict__ row, float* __restrict__ orow, Geom g,
+                                        Smem sm, int rank, int C, int warp, int lane, int tid) {
     using KEYF = typename std::conditional<KIND == K_MASK, KeyLogit, KeyProb>::type;
     for (;;) {
         cluster_sync();  // the command is published
-        const Ctl c = *sm.ctl;
+        const Ctl c = *sm.ctl();
         if (c.cmd == CMD_BISECT) {
             const uint64_t hi = uint64_t(c.hi_lo) | (uint64_t(c.hi_hi) << 32);
-            bisect_pass<VEC, KIND == K_TOPP>(row, g, sm, false, rank, c.u[3], hi, c.u, KEYF(), warp, lane, tid);
+            bisect_pass<VEC, KIND == K_TOPP>(row, g, sm, false, rank, c.u[3], hi, c.u[0], c.u[1], c.u[2], KEYF(),
+                                             warp, lane, tid);
         } else if (c.cmd == CMD_MASSGE) {
             massge_pass<VEC>(row, g, sm, false, rank, c.u[0], KEYF(), warp, lane, tid);
         } else if (c.cmd == CMD_WRITE) {
             write_pass<VEC, KIND>(row, orow, g, sm, c.flag != 0, c.u[0], c.f[0], warp, lane);
             return;
         } else if (c.cmd == CMD_COLLECT) {
-            collect_own<VEC>(row, g, sm, false, rank, C, CAP / C, c.u[0], KEYF(), warp, lane, tid);
+            collect_own<VEC>(row, g, sm, false, rank, C, CAP / C, c.u[0], KEYF(), false, warp, lane, tid);
         } else {
             return;  // CMD_EXIT
         }
@@ -110,71 +111,103 @@ __global__ void __launch_bounds__(NT, 4) filter_kernel(const FilterArgs a) {
     const bool need_hist = k_on && ns >= k;
 
     // ---- pass 1, inside a split cluster barrier
-    if (leader && need_hist)
-        for (int i = tid; i < HBINS; i += NT) sm.hist[i] = 0u;
+    if (need_hist)
+        for (int i = tid; i < HBINS; i += NT) sm.hist()[i] = 0u;
     cluster_arrive();
     int pos = 0;
     bool bad = false;
     pass1<VEC, false, IS_PROB>(row, g, sm, warp, lane, pos, bad);
-    cluster_wait();  // every CTA has started and the leader's histogram is clear
-    pass1_totals(g, sm, leader, rank, pos, bad, need_hist ? (IS_PROB ? 21 : 22) : -1, IS_PROB, warp, lane, tid);
-    cluster_sync();  // the leader's segment table, histogram and parts are complete
-    if (!leader) {
-        filter_peer<VEC, KIND>(row, orow, g, sm, rank, C, warp, lane, tid);
-        return;
-    }
+    cluster_wait();  // every CTA has started and cleared its histogram
+    pass1_totals(g, sm, leader, rank, C, pos, bad, need_hist ? (IS_PROB ? 21 : 22) : -1, IS_PROB, warp, lane, tid);
+    cluster_sync();  // the leader's segment table, every CTA's parts and histogram, are complete
 
-    // ---- leader
     const float tp = (KIND == K_TOPP) ? a.top_p[b] : 1.f;
     int npos = 0;
     bool any_bad = false;
     float M = 0.f;
     uint32_t maxkey = 0;
+#pragma unroll 1
     for (int c = 0; c < C; ++c) {
-        npos += int(sm.part[c].u[0]);
-        any_bad |= sm.part[c].u[1] != 0;
-        M += sm.part[c].f[0];
-        maxkey = max(maxkey, sm.part[c].u[2]);
+        npos += int(sm.part()[c].u[0]);
+        any_bad |= sm.part()[c].u[1] != 0;
+        M += sm.part()[c].f[0];
+        maxkey = max(maxkey, sm.part()[c].u[2]);
     }
     bool valid = !any_bad;
     if (IS_PROB) valid = valid && M > 0.f && M <= 3.402823466e38f;
     if (KIND == K_TOPP && isnan(tp)) valid = false;
 
+    // ---- top-k: every CTA derives the same lower bound L0 <= t from its copy of the
+    // histogram and sends its elements >= L0 to its region of every CTA's list.  When
+    // every region fits, each CTA finds t and the kept mass itself and writes its share.
+    uint32_t L0 = 0u;
+    bool fits = false;
+    if (k_on) {
+        L0 = need_hist ? hist_bound(sm, ns, k, IS_PROB ? 21 : 22, warp, lane, tid) : 0u;
+        if (IS_PROB) L0 = max(L0, 1u);
+        collect_own<VEC>(row, g, sm, leader, rank, C, CAP / C, L0, keyf, true, warp, lane, tid);
+        cluster_sync();  // every region and count is in every CTA
+        fits = regions_fit(sm, C, CAP / C);
+    }
+    if (fits) {
+        // Every element >= L0 (hence >= t) is in the list.
+        if (warp == 0) {
+            const int n = join_regions_warp(sm, C, CAP / C, lane);
+            const uint32_t t = kth_key_warp(sm, n, k, keyf, lane);
+            float s = 0.f;
+            for (int i = lane; i < n; i += 32) s += keyf(sm.lv()[i]) >= t ? sm.lv()[i] : 0.f;
+            s = warp_sum(s);
+            if (lane == 0) {
+                sm.red()[40] = int(t);
+                reinterpret_cast<float*>(sm.red())[41] = s;
+            }
+        }
+        __syncthreads();
+        const uint32_t t = uint32_t(sm.red()[40]);
+        const float denom = reinterpret_cast<float*>(sm.red())[41];
+        write_pass<VEC, KIND>(row, orow, g, sm, valid, t, denom, warp, lane);
+        if (leader && tid == 0 && a.out_valid) a.out_valid[b] = valid ? 1 : 0;
+        return;
+    }
+    if (!leader) {
+        filter_peer<VEC, KIND>(row, orow, g, sm, rank, C, warp, lane, tid);
+        return;
+    }
+
+    // ---- leader: the threshold with the cluster's help, then everyone writes
     uint32_t t = 0;   // keep key >= t
     float denom = M;  // kept mass (probabilities)
     if (valid) {
         if (KIND != K_TOPP) {
             if (k_on) {
-                uint32_t L0 = need_hist ? hist_bound(sm, ns, k, IS_PROB ? 21 : 22, warp, lane, tid) : 0u;
-                if (IS_PROB) L0 = max(L0, 1u);
-                bool peers = true;
-                const int n = gather_leader<VEC>(row, g, sm, C, L0, keyf, false, &peers, warp, lane, tid);
+                int n = -1;
+                if (regions_total(sm, C) <= CAP) n = collect_all<VEC>(row, g, sm, L0, keyf, warp, lane);
                 if (n >= 0) {
                     // Every element >= L0 (hence >= t) is in the list.
-                    t = kth_key_in_list(sm, n, k, keyf, warp, lane, tid);
                     if (warp == 0) {
+                        const uint32_t tt = kth_key_warp(sm, n, k, keyf, lane);
                         float s = 0.f;
-                        for (int i = lane; i < n; i += 32) s += keyf(sm.lv[i]) >= t ? sm.lv[i] : 0.f;
+                        for (int i = lane; i < n; i += 32) s += keyf(sm.lv()[i]) >= tt ? sm.lv()[i] : 0.f;
                         s = warp_sum(s);
-                        if (lane == 0) reinterpret_cast<float*>(sm.red)[40] = s;
+                        if (lane == 0) {
+                            sm.red()[40] = int(tt);
+                            reinterpret_cast<float*>(sm.red())[41] = s;
+                        }
                     }
                     __syncthreads();
-                    denom = reinterpret_cast<float*>(sm.red)[40];
+                    t = uint32_t(sm.red()[40]);
+                    denom = reinterpret_cast<float*>(sm.red())[41];
                     __syncthreads();
                 } else {
                     Bisect st;
                     // crit(L0) holds when L0 came from the segment maxima; otherwise start
                     // from 0 (count(key >= 0) = V >= k).
                     st.lo = (IS_PROB && npos < k) ? 0u : L0;
-                    if (IS_PROB && L0 == 1u && npos < k) st.lo = 0;
                     st.hi = uint64_t(maxkey) + 1;
                     st.mass_lo = 0.f;
-                    bisect_leader<VEC, false>(row, g, sm, C, &st, k, 0.f, keyf, warp, lane, tid);
+                    bisect_leader<VEC, false>(row, g, sm, C, st, k, 0.f, keyf, warp, lane, tid);
                     t = uint32_t(st.lo);
-                    if (IS_PROB) {
-                        int cnt;
-                        massge_leader<VEC>(row, g, sm, C, t, keyf, warp, lane, tid, &denom, &cnt);
-                    }
+                    if (IS_PROB) denom = massge_leader<VEC>(row, g, sm, C, t, keyf, warp, lane, tid);
                 }
             }
         } else {
@@ -183,14 +216,13 @@ __global__ void __launch_bounds__(NT, 4) filter_kernel(const FilterArgs a) {
                 denom = M;
             } else if (tp <= 0.f) {
                 t = maxkey;
-                int cnt;
-                massge_leader<VEC>(row, g, sm, C, t, keyf, warp, lane, tid, &denom, &cnt);
+                denom = massge_leader<VEC>(row, g, sm, C, t, keyf, warp, lane, tid);
             } else {
                 Bisect st;
                 st.lo = 0;
                 st.hi = uint64_t(maxkey) + 1;
                 st.mass_lo = M;
-                bisect_leader<VEC, true>(row, g, sm, C, &st, 0, tp * M, keyf, warp, lane, tid);
+                bisect_leader<VEC, true>(row, g, sm, C, st, 0, tp * M, keyf, warp, lane, tid);
                 t = uint32_t(st.lo);
                 denom = st.mass_lo;
             }

@@ -60,18 +60,19 @@ struct Pred {
 // The other CTAs: follow the leader's commands until EXIT (or until a collection that
 // completed the leader's list).
 template <bool VEC>
-FS_NOINLINE __device__ void sample_peer(const float* __restrict__ row, const Geom& g, const Smem& sm, int rank,
+__device__ __forceinline__ void sample_peer(const float* __restrict__ row, Geom g, Smem sm, int rank,
                                         int C, int warp, int lane, int tid) {
     for (;;) {
         cluster_sync();  // the command is published
-        const Ctl c = *sm.ctl;
+        const Ctl c = *sm.ctl();
         if (c.cmd == CMD_PIVOT2) {
             pivot_pass<VEC>(row, g, sm, false, rank, c.f[0], c.f[1], c.ia, c.ib, warp, lane, tid);
         } else if (c.cmd == CMD_BISECT) {
             const uint64_t hi = uint64_t(c.hi_lo) | (uint64_t(c.hi_hi) << 32);
-            bisect_pass<VEC, false>(row, g, sm, false, rank, c.u[3], hi, c.u, KeyProb(), warp, lane, tid);
+            bisect_pass<VEC, false>(row, g, sm, false, rank, c.u[3], hi, c.u[0], c.u[1], c.u[2], KeyProb(), warp,
+                                    lane, tid);
         } else if (c.cmd == CMD_COLLECT) {
-            collect_own<VEC>(row, g, sm, false, rank, C, CAP / C, c.u[0], KeyProb(), warp, lane, tid);
+            collect_own<VEC>(row, g, sm, false, rank, C, CAP / C, c.u[0], KeyProb(), false, warp, lane, tid);
         } else {
             return;  // CMD_EXIT
         }
@@ -81,20 +82,20 @@ FS_NOINLINE __device__ void sample_peer(const float* __restrict__ row, const Geo
 }
 
 // One compact round on the leader's list (warp-collective): draw, reduce, decide.
-// Returns 1 if accepted (token in *j), 0 to continue, -1 if the list had no token
+// Returns 1 if accepted (token in j), 0 to continue, -1 if the list had no token
 // above low (cannot happen while S_low > 0).
-FS_NOINLINE __device__ int compact_round(const Smem& sm, int n_list, const Pred& f, bool any_filter, float u,
-                                         float* low, float* high, float* S_low, int lane, int* j) {
-    const int e = locate_in_list(sm.lv, n_list, *low, u * *S_low, lane);
+__device__ __forceinline__ int compact_round(Smem sm, int n_list, const Pred& f, bool any_filter, float u, float& low,
+                                             float& high, float& S_low, int lane, int& j) {
+    const int e = locate_in_list(sm.lv(), n_list, low, u * S_low, lane);
     if (e < 0) return -1;
-    *j = sm.li[e];
-    const float pivot1 = sm.lv[e];
+    j = sm.li()[e];
+    const float pivot1 = sm.lv()[e];
     if (!any_filter) return 1;
-    const float pivot2 = (pivot1 + *high) * 0.5f;
+    const float pivot2 = (pivot1 + high) * 0.5f;
     float M1 = 0.f, M2 = 0.f;
     int C1 = 0, C2 = 0;
     for (int i = lane; i < n_list; i += 32) {
-        const float x = sm.lv[i];
+        const float x = sm.lv()[i];
         const bool g1 = x > pivot1, g2 = x > pivot2;
         M1 += g1 ? x : 0.f;
         M2 += g2 ? x : 0.f;
@@ -107,12 +108,12 @@ FS_NOINLINE __device__ int compact_round(const Smem& sm, int n_list, const Pred&
     C2 = warp_sum_i(C2);
     if (f(C1, M1, pivot1)) return 1;
     if (f(C2, M2, pivot2)) {
-        *low = pivot1;
-        *high = pivot2;
-        *S_low = M1;
+        low = pivot1;
+        high = pivot2;
+        S_low = M1;
     } else {
-        *low = pivot2;
-        *S_low = M2;
+        low = pivot2;
+        S_low = M2;
     }
     return 0;
 }
@@ -120,14 +121,15 @@ FS_NOINLINE __device__ int compact_round(const Smem& sm, int n_list, const Pred&
 // Inverse-transform draw over the whole row while its tokens are spread over the
 // cluster (warp-collective, leader): the owning CTA from the per-CTA masses cmass[]
 // (summed in rank order, as S_low was), the segment inside the owner's range from
-// mass[cur], then the token inside the segment.  Returns the token, its value in *x.
+// mass[cur], then the token inside the segment.  Returns the token (-1 if none) packed
+// with its value.
 template <bool VEC>
-FS_NOINLINE __device__ int draw_full(const float* __restrict__ row, const Geom& g, const Smem& sm, int C, int cur,
-                                     float low, float target, int lane, float* x) {
+__device__ __forceinline__ unsigned long long draw_full(const float* __restrict__ row, Geom g, Smem sm, int C, int cur,
+                                                   float low, float target, int lane) {
     float run = 0.f, before = 0.f, last_before = 0.f;
     int owner = -1, last = -1;
     for (int c = 0; c < C; ++c) {
-        const float m = sm.cmass[c];
+        const float m = sm.cmass()[c];
         if (m > 0.f) {
             if (owner < 0 && run + m > target) {
                 owner = c;
@@ -142,17 +144,15 @@ FS_NOINLINE __device__ int draw_full(const float* __restrict__ row, const Geom& 
         owner = last;
         before = last_before;
     }
-    if (owner < 0) return -1;
+    if (owner < 0) return pack_jx(-1, 0.f);
     int a0, a1;
     g.range_of(owner, a0, a1);
     float t = target - before;
-    float bs = 0.f;
-    const int s = locate_segment(sm.mass[cur], a0, a1, t, lane, &bs);
-    if (s < 0) return -1;
-    t = (t - bs < 0.f) ? 0.f : t - bs;
-    int j = -1;
-    locate_in_segment<VEC, true>(row, g, s, low, t, lane, &j, x);
-    return j;
+    const unsigned long long ls = locate_segment(sm.mass(cur), a0, a1, t, lane);
+    const int s = unpack_j(ls);
+    if (s < 0) return pack_jx(-1, 0.f);
+    t = (t - unpack_x(ls) < 0.f) ? 0.f : t - unpack_x(ls);
+    return locate_in_segment<VEC, true>(row, g, s, low, t, lane);
 }
 
 template <bool VEC>
@@ -177,8 +177,8 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
     const bool need_hist = kfirst && ns >= k;
 
     // ---- a2: pass 1, the only HBM read of the row, inside a split cluster barrier
-    if (leader && need_hist)
-        for (int i = tid; i < HBINS; i += NT) sm.hist[i] = 0u;
+    if (need_hist)
+        for (int i = tid; i < HBINS; i += NT) sm.hist()[i] = 0u;
     cluster_arrive();
     int pos = 0;
     bool bad = false;
@@ -186,15 +186,27 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
         pass1<VEC, true, true>(row, g, sm, warp, lane, pos, bad);
     } else {
         for (int i = g.s0 + tid; i < g.s1; i += NT) {
-            sm.segkey[i] = 0u;
-            sm.mass[0][i] = 0.f;
+            sm.segkey()[i] = 0u;
+            sm.mass(0)[i] = 0.f;
         }
     }
-    cluster_wait();  // every CTA has started and the leader's histogram is clear
-    pass1_totals(g, sm, leader, rank, pos, bad, need_hist ? 21 : -1, true, warp, lane, tid);
-    cluster_sync();  // the leader's segment table, histogram and parts are complete
+    cluster_wait();  // every CTA has started and cleared its histogram
+    pass1_totals(g, sm, leader, rank, C, pos, bad, need_hist ? 21 : -1, true, warp, lane, tid);
+    cluster_sync();  // the leader's segment table, every CTA's parts and histogram, are complete
+
+    // ---- a3 (first half, every CTA): top-k-first candidates.  Every CTA derives the
+    // same lower bound L0 <= t_k from its copy of the histogram and sends its elements
+    // >= L0 to its region of the leader's list.
+    bool fits = false;
+    uint32_t L0 = 1u;
+    if (kfirst) {
+        L0 = max(1u, need_hist ? hist_bound(sm, ns, k, 21, warp, lane, tid) : 0u);
+        collect_own<VEC>(row, g, sm, leader, rank, C, CAP / C, L0, keyf, false, warp, lane, tid);
+        cluster_sync();  // every region and count is in
+        fits = regions_fit(sm, C, CAP / C);
+    }
     if (!leader) {
-        sample_peer<VEC>(row, g, sm, rank, C, warp, lane, tid);
+        if (!fits) sample_peer<VEC>(row, g, sm, rank, C, warp, lane, tid);
         return;
     }
 
@@ -214,22 +226,23 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
     bool any_bad = false;
     float M = 0.f;           // sum of the per-CTA ordered sums, in rank order
     uint32_t maxkey = 0;
+#pragma unroll 1
     for (int c = 0; c < C; ++c) {
-        npos += int(sm.part[c].u[0]);
-        any_bad |= sm.part[c].u[1] != 0;
-        M += sm.part[c].f[0];
-        maxkey = max(maxkey, sm.part[c].u[2]);
+        npos += int(sm.part()[c].u[0]);
+        any_bad |= sm.part()[c].u[1] != 0;
+        M += sm.part()[c].f[0];
+        maxkey = max(maxkey, sm.part()[c].u[2]);
     }
-    if (tid < C) sm.cmass[tid] = sm.part[tid].f[0];
+    if (tid < C) sm.cmass()[tid] = sm.part()[tid].f[0];
     const float rowmax = __uint_as_float(maxkey);
     bool valid = row_ok && !isnan(tp) && !isnan(mp) && !any_bad && M > 0.f && M <= 3.402823466e38f;
     if (f.m_on) {
         f.t32 = __double2float_ru(double(mp) * double(rowmax));
         if (!(rowmax >= f.t32)) valid = false;  // S is empty: f(max) = 0
     }
-    __syncthreads();
+    if (!fits) __syncthreads();
 
-    bool peers = true;  // the other CTAs still wait for commands
+    bool peers = !fits;  // the other CTAs still wait for commands
     auto dismiss = [&]() {
         if (peers) {
             Ctl c{};
@@ -243,25 +256,31 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
     bool accepted = false;
     if (valid) {
         float low = 0.f, high = rowmax, S_low = M;
-        int cur = 0;            // mass[cur][s] = mass of segment s above `low`
+        int cur = 0;            // mass(cur)[s] = mass of segment s above `low`
         int count_low = npos;   // tokens above `low`
         int n_list = 0;
         bool compact = false;
         f.pthr = tp * M;
 
-        // ---- a3: top-k-first prologue
+        // ---- a3 (second half, leader): t_k and F_k
         if (kfirst) {
-            const uint32_t L0 = max(1u, need_hist ? hist_bound(sm, ns, k, 21, warp, lane, tid) : 0u);
-            const int n = gather_leader<VEC>(row, g, sm, C, L0, keyf, true, &peers, warp, lane, tid);
-            if (n >= 0) {
+            int n = -1;
+            if (fits) {
+                n = regions_total(sm, C);
+                if (warp == 0) join_regions_warp(sm, C, CAP / C, lane);
+            } else if (regions_total(sm, C) <= CAP) {
+                // A region overflowed: the leader collects the candidates alone.
                 dismiss();
+                n = collect_all<VEC>(row, g, sm, L0, keyf, warp, lane);
+            }
+            if (n >= 0) {
                 compact = true;
                 // The list holds every element >= L0, hence every element >= t_k.
-                const uint32_t tk = kth_key_in_list(sm, n, k, keyf, warp, lane, tid);
                 if (warp == 0) {
+                    const uint32_t tk = kth_key_warp(sm, n, k, keyf, lane);
                     n_list = filter_list_warp(sm, n, tk, keyf, lane);
                     float s = 0.f;
-                    for (int i = lane; i < n_list; i += 32) s += sm.lv[i];
+                    for (int i = lane; i < n_list; i += 32) s += sm.lv()[i];
                     S_low = warp_sum(s);
                 }
                 low = 0.f;
@@ -272,7 +291,7 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
                 st.hi = uint64_t(maxkey) + 1;
                 st.mass_lo = 0.f;
                 if (npos < k) st.lo = 0;  // fewer positives than k: t_k = 0 keeps them all
-                bisect_leader<VEC, false>(row, g, sm, C, &st, k, 0.f, keyf, warp, lane, tid);
+                bisect_leader<VEC, false>(row, g, sm, C, st, k, 0.f, keyf, warp, lane, tid);
                 const uint32_t tk = uint32_t(st.lo);
                 low = tk >= 1u ? __uint_as_float(tk - 1u) : 0.f;  // x > low  <=>  key(x) >= t_k
                 // Per-segment and per-CTA masses above `low` for the draws (both pivots = low).
@@ -287,11 +306,12 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
                 cluster_sync();
                 count_low = 0;
                 S_low = 0.f;
+#pragma unroll 1
                 for (int cc = 0; cc < C; ++cc) {
-                    count_low += int(sm.part[cc].u[0]);
-                    S_low += sm.part[cc].f[0];
+                    count_low += int(sm.part()[cc].u[0]);
+                    S_low += sm.part()[cc].f[0];
                 }
-                if (tid < C) sm.cmass[tid] = sm.part[tid].f[0];
+                if (tid < C) sm.cmass()[tid] = sm.part()[tid].f[0];
                 __syncthreads();
                 cur = 0;
             }
@@ -302,7 +322,8 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
         for (int round = 0; round < R_MAX; ++round) {
             if (!compact && count_low <= CAP) {
                 // Few tokens left above `low`: gather them; the leader goes on alone.
-                n_list = gather_leader<VEC>(row, g, sm, C, prob_key(low) + 1u, keyf, true, &peers, warp, lane, tid);
+                n_list = gather_leader<VEC>(row, g, sm, C, prob_key(low) + 1u, keyf, true, warp, lane, tid);
+                if (n_list >= 0) peers = false;  // they left with the completed list
                 dismiss();
                 if (n_list < 0) break;
                 compact = true;
@@ -311,7 +332,7 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
             if (compact) {
                 if (warp != 0) break;
                 int j = -1;
-                const int st = compact_round(sm, n_list, f, any_filter, u, &low, &high, &S_low, lane, &j);
+                const int st = compact_round(sm, n_list, f, any_filter, u, low, high, S_low, lane, j);
                 if (st < 0) break;
                 if (st > 0) {
                     accepted = true;
@@ -323,16 +344,15 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
             }
             // ---- a5: draw (warp 0): owner CTA, segment, token
             if (warp == 0) {
-                float xx = 0.f;
-                const int jj = draw_full<VEC>(row, g, sm, C, cur, low, u * S_low, lane, &xx);
+                const unsigned long long jx = draw_full<VEC>(row, g, sm, C, cur, low, u * S_low, lane);
                 if (lane == 0) {
-                    sm.red[32] = jj;
-                    reinterpret_cast<float*>(sm.red)[33] = xx;
+                    sm.red()[32] = unpack_j(jx);
+                    reinterpret_cast<float*>(sm.red())[33] = unpack_x(jx);
                 }
             }
             __syncthreads();
-            const int j = sm.red[32];
-            const float pivot1 = reinterpret_cast<float*>(sm.red)[33];
+            const int j = sm.red()[32];
+            const float pivot1 = reinterpret_cast<float*>(sm.red())[33];
             __syncthreads();
             if (j < 0) break;
             if (!any_filter) {
@@ -358,10 +378,10 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
             int C1 = 0, C2 = 0;
             float M1 = 0.f, M2 = 0.f;
             for (int cc = 0; cc < C; ++cc) {
-                C1 += int(sm.part[cc].u[0]);
-                C2 += int(sm.part[cc].u[1]);
-                M1 += sm.part[cc].f[0];
-                M2 += sm.part[cc].f[1];
+                C1 += int(sm.part()[cc].u[0]);
+                C2 += int(sm.part()[cc].u[1]);
+                M1 += sm.part()[cc].f[0];
+                M2 += sm.part()[cc].f[1];
             }
 
             // ---- a7: the three cases
@@ -384,7 +404,7 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
                 count_low = C2;
                 cur = ib;
             }
-            if (tid < C) sm.cmass[tid] = narrow ? sm.part[tid].f[0] : sm.part[tid].f[1];
+            if (tid < C) sm.cmass()[tid] = narrow ? sm.part()[tid].f[0] : sm.part()[tid].f[1];
             __syncthreads();
         }
         if (!accepted) rounds = R_MAX;
