@@ -57,6 +57,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-entries", action="store_true", help="time only the headline step")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-oracle sample")
+    ap.add_argument("--profile", action="store_true",
+                    help="only run the headline step (warmup + steps launches) for a profiler; prints a short line")
     return ap.parse_args()
 
 
@@ -259,6 +261,13 @@ def run_ours(args):
         return total_ms, per, (ctx.summary() if ctx else None)
 
     K, W = args.steps, args.warmup
+    if args.profile:
+        for i in range(W + K):
+            calls["top_k_first"](i)
+        torch.cuda.synchronize(dev)
+        if rank == 0:
+            print(json.dumps({"profile": "top_k_first", "launches": W + K, "batch": B, "vocab": V}), flush=True)
+        return
     total_ms, per, clk = timed(calls["top_k_first"], K, W, clocks=True)
     kern_ms = statistics.mean(per)
     value = world * B * K / (total_ms / 1e3)

@@ -112,6 +112,7 @@ struct Smem {
     __device__ __forceinline__ Part* part() const { return at<Part>(Layout::PART); }        // [MAX_CLUSTER]
     __device__ __forceinline__ int* red() const { return at<int>(Layout::RED); }            // [64] scratch
     __device__ __forceinline__ float* cmass() const { return at<float>(Layout::MISC); }     // [MAX_CLUSTER]
+    __device__ __forceinline__ int* ctr() const { return at<int>(Layout::MISC + 64); }      // pass-1 trip counter
     __device__ __forceinline__ uint32_t* segkey() const { return at<uint32_t>(Layout(ns).arr(0)); }
     __device__ __forceinline__ float* mass(int i) const { return at<float>(Layout(ns).arr(1 + i)); }  // i < 3
     __device__ __forceinline__ int* list() const { return at<int>(Layout(ns).arr(4)); }     // live segments
@@ -422,40 +423,44 @@ __device__ __forceinline__ void stream_warp(const float* __restrict__ row, Geom 
 
 // ------------------------------------------------------------------ pass 1
 
-// One streaming pass over this CTA's segments.  Warp w takes a contiguous range of
-// them and reads it in trips of TB blocks, the next trip's loads in flight while the
-// current trip is reduced.  For every segment: the maximum order key and (PROB) the
+// One streaming pass over this CTA's segments, in trips of TB blocks (whole segments):
+// warp w starts with trip w and then takes the next untaken trip from a shared counter
+// (initialised to NW), so that warps finishing early take more; the next trip's loads
+// are in flight while the current trip is reduced.  For every segment: the maximum order key and (PROB) the
 // mass, into this CTA's table.  Per lane: the positive count and a bad-value flag (NaN
 // or negative for probabilities, NaN for logits).  Touches no other CTA, so it may run
 // before the cluster's first barrier completes.
 template <bool VEC, bool NC, bool PROB>
-__device__ __forceinline__ void pass1(const float* __restrict__ row, Geom g, Smem sm, int warp,
-                                      int lane, int& pos, bool& bad) {
-    int r0, r1;
-    warp_range(g.s1 - g.s0, warp, r0, r1);
-    r0 += g.s0;
-    r1 += g.s0;
-    const int nblk = (r1 - r0) << g.shift;
+__device__ __forceinline__ void pass1(const float* __restrict__ row, Geom g, Smem sm, int warp, int lane, int& pos,
+                                      bool& bad) {
+    const int spt = TB >> g.shift;  // segments per trip
+    const int ntrip = (g.s1 - g.s0 + spt - 1) / spt;
     const int mask = g.seg_it() - 1;
     const float fill = PROB ? 0.f : __int_as_float(0xff800000);
+    auto load_trip = [&](int t, float4* v) {
+#pragma unroll
+        for (int j = 0; j < TB; ++j) {
+            const int sg = g.s0 + t * spt + (j >> g.shift);
+            v[j] = (t < ntrip && sg < g.s1) ? load4<VEC, NC>(row, g.V, g.base(sg, j & mask, lane), fill)
+                                            : make_float4(fill, fill, fill, fill);
+        }
+    };
     float4 A[TB], Bv[TB];
-#pragma unroll
-    for (int j = 0; j < TB; ++j)
-        A[j] = j < nblk ? load4<VEC, NC>(row, g.V, g.base(r0 + (j >> g.shift), j & mask, lane), fill)
-                        : make_float4(fill, fill, fill, fill);
-    for (int b0 = 0; b0 < nblk; b0 += TB) {
-        const int nb = b0 + TB;
-#pragma unroll
-        for (int j = 0; j < TB; ++j)
-            Bv[j] = nb + j < nblk
-                        ? load4<VEC, NC>(row, g.V, g.base(r0 + ((nb + j) >> g.shift), (nb + j) & mask, lane), fill)
-                        : make_float4(fill, fill, fill, fill);
+    int t = warp;  // the first NW trips are fixed; later ones are taken from the counter
+    load_trip(t, A);
+#pragma unroll 1
+    while (t < ntrip) {
+        int tn = 0;
+        if (lane == 0) tn = atomicAdd(sm.ctr(), 1);
+        tn = __shfl_sync(FULL, tn, 0);
+        load_trip(tn, Bv);
+        const int sg0 = g.s0 + t * spt;
         float s[TB];
         uint32_t km[TB];
 #pragma unroll
         for (int j = 0; j < TB; ++j) {
-            const int blk = b0 + j;
-            const int base = g.base(r0 + (blk >> g.shift), blk & mask, lane);
+            const int sg = sg0 + (j >> g.shift);
+            const int base = g.base(sg, j & mask, lane);
             uint32_t k = 0;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -466,7 +471,7 @@ __device__ __forceinline__ void pass1(const float* __restrict__ row, Geom g, Sme
                     pos += x > 0.f;
                 } else {
                     bad |= isnan(x);
-                    k = max(k, (blk < nblk && base + q < g.V) ? logit_key(x) : 0u);
+                    k = max(k, (sg < g.s1 && base + q < g.V) ? logit_key(x) : 0u);
                 }
             }
             km[j] = __reduce_max_sync(FULL, k);
@@ -478,10 +483,9 @@ __device__ __forceinline__ void pass1(const float* __restrict__ row, Geom g, Sme
 #pragma unroll
                 for (int j = 0; j < TB; ++j) s[j] += __shfl_xor_sync(FULL, s[j], m);
         }
-        // Lane t stores segment (b0 >> shift) + t, its blocks combined in order.
-        const int nseg = TB >> g.shift;
-        const int sg = r0 + (b0 >> g.shift) + lane;
-        if (lane < nseg && sg < r1) {
+        // Lane l stores segment sg0 + l, its blocks combined in order.
+        const int sg = sg0 + lane;
+        if (lane < spt && sg < g.s1) {
             float ss = 0.f;
             uint32_t kk = 0;
 #pragma unroll
@@ -495,6 +499,7 @@ __device__ __forceinline__ void pass1(const float* __restrict__ row, Geom g, Sme
         }
 #pragma unroll
         for (int j = 0; j < TB; ++j) A[j] = Bv[j];
+        t = tn;
     }
 }
 
@@ -514,9 +519,9 @@ __device__ __forceinline__ void st_rank_v4(void* local_addr, uint4 v, uint32_t r
 // CTA (f[0] ordered mass of its segments, u[0] positive count, u[1] bad flag, u[2]
 // maximum key) and, if `hist_shift` >= 0, one count per segment maximum into the
 // histogram (key >> hist_shift) of every CTA of the cluster, each of which cleared its
-// own before that barrier.  Histogram updates are combined per warp (equal bins of a
-// warp add once).  The CTA's first segment is a multiple of 4, so the table moves in
-// 16-byte words.  Block-collective.
+// own (and its lv, used here for its local counts) before that barrier.  The CTA's
+// first segment is a multiple of 4, so the table moves in 16-byte words.
+// Block-collective.
 __device__ __forceinline__ void pass1_totals(Geom g, Smem sm, bool leader, int rank, int C, int pos, bool bad,
                                              int hist_shift, bool prob, int warp, int lane, int tid) {
     __syncthreads();  // the table written by pass 1
@@ -524,16 +529,18 @@ __device__ __forceinline__ void pass1_totals(Geom g, Smem sm, bool leader, int r
     const int b = __any_sync(FULL, bad) ? 1 : 0;
     uint32_t km = 0;
     if (hist_shift >= 0) {
+        // This CTA's counts in lv (cleared with the histogram), then every non-empty bin
+        // added once into each CTA's histogram.
+        uint32_t* loc = reinterpret_cast<uint32_t*>(sm.lv());
 #pragma unroll 1
-        for (int i0 = g.s0 + warp * 32; i0 < g.s1; i0 += NT) {
-            const int i = i0 + lane;
-            const bool in = i < g.s1;
-            const uint32_t key = in ? sm.segkey()[i] : 0u;
-            const uint32_t bin = in ? min(uint32_t(HBINS - 1), key >> hist_shift) : 0xffffffffu;
-            const unsigned same = __match_any_sync(FULL, bin);
-            if (in && lane == __ffs(same) - 1) {
+        for (int i = g.s0 + tid; i < g.s1; i += NT) atomicAdd(&loc[min(uint32_t(HBINS - 1), sm.segkey()[i] >> hist_shift)], 1u);
+        __syncthreads();
+#pragma unroll
+        for (int q = 0; q < HBINS / NT; ++q) {
+            const int bin = q * NT + tid;
+            const uint32_t n = loc[bin];
+            if (n) {
                 uint32_t* h = &sm.hist()[bin];
-                const uint32_t n = uint32_t(__popc(same));
 #pragma unroll 1
                 for (int r = 0; r < C; ++r) {
                     if (r == rank) {
@@ -696,60 +703,60 @@ __device__ __forceinline__ int live_list(Smem sm, int a, int b, uint32_t thr, in
 
 // Read the listed segments (list[0..nlive), in order) and emit, in index order, every
 // element with key >= thr: out(p, value, index) for p = 0, 1, ...  Returns the exact
-// count.  Each batch stages 2*SBH listed blocks per warp (cp.async), counts, fixes the
-// warps' output offsets, then emits.  Block-collective.
+// count.  Listed blocks go in batches of NW * 2 * SBH; block j of a batch to warp
+// j % NW (staged with cp.async), so that a short list spreads over all warps; per-block
+// counts fix every block's output offset.  Block-collective.
 template <bool VEC, typename KEYF, typename OUT>
-__device__ __forceinline__ int collect(const float* __restrict__ row, Geom g, Smem sm, int nlive,
-                                       uint32_t thr, KEYF keyf, int warp, int lane, OUT out) {
-    constexpr int WB = 2 * SBH;
+__device__ __forceinline__ int collect(const float* __restrict__ row, Geom g, Smem sm, int nlive, uint32_t thr,
+                                       KEYF keyf, int warp, int lane, OUT out) {
+    constexpr int WB = 2 * SBH;        // blocks per warp per batch
+    constexpr int NB = NW * WB;        // blocks per batch (<= 32: one per lane of a scan)
+    static_assert(NB <= 32, "a batch's block counts are scanned by one warp");
     const int nblk = nlive << g.shift;
     const int mask = g.seg_it() - 1;
     float* st = sm.stage() + warp * (WB * BLK) + lane * 4;
     int total = 0;
 #pragma unroll 1
-    for (int c0 = 0; c0 < nblk; c0 += NW * WB) {
-        const int w0 = c0 + warp * WB;
-        const int nb = max(0, min(WB, nblk - w0));
+    for (int c0 = 0; c0 < nblk; c0 += NB) {
+        const int nb = min(NB, nblk - c0);
+        // block c0 + warp + NW * i is this warp's slot i
 #pragma unroll 1
-        for (int j = 0; j < nb; ++j) {
-            const int lb = w0 + j;
-            stage4<VEC>(st + j * BLK, row, g.V, g.base(sm.list()[lb >> g.shift], lb & mask, lane));
+        for (int i = 0; i < WB && warp + NW * i < nb; ++i) {
+            const int lb = c0 + warp + NW * i;
+            stage4<VEC>(st + i * BLK, row, g.V, g.base(sm.list()[lb >> g.shift], lb & mask, lane));
         }
         cp_async_commit();
         cp_async_wait<0>();
-        int cnt = 0;
 #pragma unroll 1
-        for (int j = 0; j < nb; ++j) {
-            const int lb = w0 + j;
+        for (int i = 0; i < WB && warp + NW * i < nb; ++i) {
+            const int lb = c0 + warp + NW * i;
             const int base = g.base(sm.list()[lb >> g.shift], lb & mask, lane);
+            int cnt = 0;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) cnt += (keyf(st[j * BLK + q]) >= thr && base + q < g.V);
-        }
-        cnt = warp_sum_i(cnt);
-        if (lane == 0) sm.red()[warp] = cnt;
-        __syncthreads();
-        int pos = total, chunk = 0;
-#pragma unroll 1
-        for (int w = 0; w < NW; ++w) {
-            if (w < warp) pos += sm.red()[w];
-            chunk += sm.red()[w];
+            for (int q = 0; q < 4; ++q) cnt += (keyf(st[i * BLK + q]) >= thr && base + q < g.V);
+            cnt = warp_sum_i(cnt);
+            if (lane == 0) sm.red()[warp + NW * i] = cnt;
         }
         __syncthreads();
+        const int bc = lane < nb ? sm.red()[lane] : 0;
+        const int bincl = warp_incl_scan_i(bc, lane);
+        const int chunk = __shfl_sync(FULL, bincl, 31);
+        __syncthreads();
 #pragma unroll 1
-        for (int j = 0; j < nb; ++j) {
-            const int lb = w0 + j;
+        for (int i = 0; i < WB && warp + NW * i < nb; ++i) {
+            const int jb = warp + NW * i;
+            const int lb = c0 + jb;
             const int base = g.base(sm.list()[lb >> g.shift], lb & mask, lane);
             int k = 0;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) k += (keyf(st[j * BLK + q]) >= thr && base + q < g.V);
+            for (int q = 0; q < 4; ++q) k += (keyf(st[i * BLK + q]) >= thr && base + q < g.V);
             const int incl = warp_incl_scan_i(k, lane);
-            int p = pos + incl - k;
+            int p = total + __shfl_sync(FULL, bincl - bc, jb) + incl - k;
 #pragma unroll 1
             for (int q = 0; q < 4; ++q) {
-                const float x = st[j * BLK + q];
+                const float x = st[i * BLK + q];
                 if (keyf(x) >= thr && base + q < g.V) out(p++, x, base + q);
             }
-            pos += __shfl_sync(FULL, incl, 31);
         }
         total += chunk;
     }
@@ -797,18 +804,34 @@ __device__ __forceinline__ void collect_own(const float* __restrict__ row, Geom 
 }
 
 // After the barrier that follows collect_own: whether every rank's candidates fit in
-// its region.  Any CTA (each holds every count).
+// its region, and their total.  Any CTA (each holds every count); warp-parallel, every
+// lane of every warp gets the result.
 __device__ __forceinline__ bool regions_fit(Smem sm, int C, int rc) {
-    bool fits = true;
-#pragma unroll 1
-    for (int r = 0; r < C; ++r) fits = fits && int(sm.part()[r].u[4]) <= rc;
-    return fits;
+    const int lane = threadIdx.x & 31;
+    return __all_sync(FULL, lane >= C || int(sm.part()[lane].u[4]) <= rc);
 }
 __device__ __forceinline__ int regions_total(Smem sm, int C) {
-    int n = 0;
-#pragma unroll 1
-    for (int r = 0; r < C; ++r) n += int(sm.part()[r].u[4]);
-    return n;
+    const int lane = threadIdx.x & 31;
+    return warp_sum_i(lane < C ? int(sm.part()[lane].u[4]) : 0);
+}
+
+// The cluster's totals from the parts written by pass1_totals (lane c reads part c).
+struct Totals {
+    int npos;
+    bool any_bad;
+    float M;
+    uint32_t maxkey;
+};
+__device__ __forceinline__ Totals cluster_totals(Smem sm, int C) {
+    const int lane = threadIdx.x & 31;
+    const bool in = lane < C;
+    const Part& p = sm.part()[in ? lane : 0];
+    Totals t;
+    t.npos = warp_sum_i(in ? int(p.u[0]) : 0);
+    t.any_bad = __any_sync(FULL, in && p.u[1] != 0u);
+    t.M = warp_sum(in ? p.f[0] : 0.f);
+    t.maxkey = warp_max_u(in ? p.u[2] : 0u);
+    return t;
 }
 
 // The candidate regions of all ranks, concatenated in rank order at the front of
@@ -876,6 +899,84 @@ __device__ __forceinline__ uint32_t kth_key_warp(Smem sm, int n, int k, KEYF key
         if (cnt >= k) t = cand;
     }
     return t;
+}
+
+// A candidate list of at most SMALL entries held by one warp in registers: entry
+// e = 32 r + lane in slot r (x[r], i[r]); in[r] marks entries below n.
+constexpr int SR = 4;              // slots per lane
+constexpr int SMALL = 32 * SR;
+struct Small {
+    float x[SR];
+    int i[SR];
+    bool in[SR];
+    int n;
+};
+
+// Gather the joined candidate list (regions of rc entries, counts in part[r].u[4], in
+// rank order) straight from the regions, n <= SMALL.  Warp-collective.
+__device__ __forceinline__ Small small_gather(Smem sm, int C, int rc, int lane) {
+    // Exclusive prefix of the region counts, region r's offset in lane r.
+    const int cnt = lane < C ? int(sm.part()[lane].u[4]) : 0;
+    const int off = warp_incl_scan_i(cnt, lane) - cnt;
+    Small s;
+    s.n = __shfl_sync(FULL, off + cnt, 31);
+    int rr[SR], oo[SR];
+#pragma unroll
+    for (int r = 0; r < SR; ++r) {
+        rr[r] = 0;
+        oo[r] = 0;
+    }
+#pragma unroll 1
+    for (int c = 0; c < C; ++c) {
+        const int o = __shfl_sync(FULL, off, c);
+        const int m = __shfl_sync(FULL, cnt, c);
+#pragma unroll
+        for (int r = 0; r < SR; ++r) {
+            if (m > 0 && o <= 32 * r + lane) {
+                rr[r] = c;
+                oo[r] = o;
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < SR; ++r) {
+        const int e = 32 * r + lane;
+        s.in[r] = e < s.n;
+        const int a = rr[r] * rc + (e - oo[r]);
+        s.x[r] = s.in[r] ? sm.lv()[a] : 0.f;
+        s.i[r] = s.in[r] ? sm.li()[a] : 0;
+    }
+    return s;
+}
+
+// The k-th largest order key of a small list (0 if it has fewer than k entries): the
+// largest key v with #{keys >= v} >= k, counting for each entry how many entries are
+// at least as large (every entry visits every other through shuffles).
+// Warp-collective.  Entries of the list have non-zero keys.
+template <typename KEYF>
+__device__ __forceinline__ uint32_t small_kth(const Small& s, int k, KEYF keyf) {
+    if (s.n < k) return 0u;
+    uint32_t key[SR];
+    int ge[SR];
+#pragma unroll
+    for (int r = 0; r < SR; ++r) {
+        key[r] = s.in[r] ? keyf(s.x[r]) : 0u;
+        ge[r] = 0;
+    }
+#pragma unroll
+    for (int r2 = 0; r2 < SR; ++r2) {
+        if (32 * r2 >= s.n) break;
+#pragma unroll 4
+        for (int l = 0; l < 32; ++l) {
+            const uint32_t a = __shfl_sync(FULL, key[r2], l);
+#pragma unroll
+            for (int r = 0; r < SR; ++r) ge[r] += int(a >= key[r]);
+        }
+    }
+    uint32_t best = 0u;
+#pragma unroll
+    for (int r = 0; r < SR; ++r) best = max(best, s.in[r] && ge[r] >= k ? key[r] : 0u);
+    return warp_max_u(best);
 }
 
 // In-place, order-preserving filter of lv/li[0..n) to key >= t by one warp.

@@ -107,12 +107,18 @@ __global__ void __launch_bounds__(NT, 4) filter_kernel(const FilterArgs a) {
     float* orow = a.out + size_t(b) * size_t(V);
 
     const int k = (KIND != K_TOPP) ? a.top_k[b] : 0;
+    const float tp = (KIND == K_TOPP) ? a.top_p[b] : 1.f;
     const bool k_on = KIND != K_TOPP && k > 0 && k < V;
     const bool need_hist = k_on && ns >= k;
 
     // ---- pass 1, inside a split cluster barrier
     if (need_hist)
-        for (int i = tid; i < HBINS; i += NT) sm.hist()[i] = 0u;
+        for (int i = tid; i < HBINS; i += NT) {
+            sm.hist()[i] = 0u;
+            reinterpret_cast<uint32_t*>(sm.lv())[i] = 0u;
+        }
+    if (tid == 0) *sm.ctr() = NW;
+    __syncthreads();
     cluster_arrive();
     int pos = 0;
     bool bad = false;
@@ -121,18 +127,11 @@ __global__ void __launch_bounds__(NT, 4) filter_kernel(const FilterArgs a) {
     pass1_totals(g, sm, leader, rank, C, pos, bad, need_hist ? (IS_PROB ? 21 : 22) : -1, IS_PROB, warp, lane, tid);
     cluster_sync();  // the leader's segment table, every CTA's parts and histogram, are complete
 
-    const float tp = (KIND == K_TOPP) ? a.top_p[b] : 1.f;
-    int npos = 0;
-    bool any_bad = false;
-    float M = 0.f;
-    uint32_t maxkey = 0;
-#pragma unroll 1
-    for (int c = 0; c < C; ++c) {
-        npos += int(sm.part()[c].u[0]);
-        any_bad |= sm.part()[c].u[1] != 0;
-        M += sm.part()[c].f[0];
-        maxkey = max(maxkey, sm.part()[c].u[2]);
-    }
+    const Totals tot = cluster_totals(sm, C);
+    const int npos = tot.npos;
+    const bool any_bad = tot.any_bad;
+    const float M = tot.M;
+    const uint32_t maxkey = tot.maxkey;
     bool valid = !any_bad;
     if (IS_PROB) valid = valid && M > 0.f && M <= 3.402823466e38f;
     if (KIND == K_TOPP && isnan(tp)) valid = false;
@@ -152,10 +151,18 @@ __global__ void __launch_bounds__(NT, 4) filter_kernel(const FilterArgs a) {
     if (fits) {
         // Every element >= L0 (hence >= t) is in the list.
         if (warp == 0) {
-            const int n = join_regions_warp(sm, C, CAP / C, lane);
-            const uint32_t t = kth_key_warp(sm, n, k, keyf, lane);
+            uint32_t t;
             float s = 0.f;
-            for (int i = lane; i < n; i += 32) s += keyf(sm.lv()[i]) >= t ? sm.lv()[i] : 0.f;
+            if (regions_total(sm, C) <= SMALL) {  // the usual case: in registers
+                const Small sl = small_gather(sm, C, CAP / C, lane);
+                t = small_kth(sl, k, keyf);
+#pragma unroll
+                for (int r = 0; r < SR; ++r) s += sl.in[r] && keyf(sl.x[r]) >= t ? sl.x[r] : 0.f;
+            } else {
+                const int n = join_regions_warp(sm, C, CAP / C, lane);
+                t = kth_key_warp(sm, n, k, keyf, lane);
+                for (int i = lane; i < n; i += 32) s += keyf(sm.lv()[i]) >= t ? sm.lv()[i] : 0.f;
+            }
             s = warp_sum(s);
             if (lane == 0) {
                 sm.red()[40] = int(t);

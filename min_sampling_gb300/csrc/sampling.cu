@@ -120,7 +120,7 @@ __device__ __forceinline__ int compact_round(Smem sm, int n_list, const Pred& f,
 
 // Inverse-transform draw over the whole row while its tokens are spread over the
 // cluster (warp-collective, leader): the owning CTA from the per-CTA masses cmass[]
-// (summed in rank order, as S_low was), the segment inside the owner's range from
+// (the first CTA whose running mass passes the target), the segment inside its range from
 // mass[cur], then the token inside the segment.  Returns the token (-1 if none) packed
 // with its value.
 template <bool VEC>
@@ -155,6 +155,72 @@ __device__ __forceinline__ unsigned long long draw_full(const float* __restrict_
     return locate_in_segment<VEC, true>(row, g, s, low, t, lane);
 }
 
+// The rounds on a short candidate list held in warp 0's registers (kept[r] marks the
+// filtered set; S_low its mass): the same draw, fused reduction and three cases as
+// compact_round, on registers.  Returns the token (-1 after R_MAX rounds or with
+// nothing eligible); the number of rounds in `rounds`.
+__device__ __forceinline__ int small_rounds(const Small& s, const bool* kept, const Pred& f, float S_low, float high,
+                                            unsigned long long seed, unsigned long long offset, uint32_t b, int lane,
+                                            int& rounds) {
+    float low = 0.f;
+#pragma unroll 1
+    for (int round = 0; round < R_MAX; ++round) {
+        const float target = sampler_uniform(seed, offset, b, uint32_t(round)) * S_low;
+        // Inverse transform over the list in index order: slot by slot, a lane scan each.
+        int e = -1, last = -1;
+        float run = 0.f;
+#pragma unroll
+        for (int r = 0; r < SR; ++r) {
+            const float w = kept[r] && s.x[r] > low ? s.x[r] : 0.f;
+            const float c = run + warp_incl_scan(w, lane);
+            const unsigned hit = __ballot_sync(FULL, w > 0.f && c > target);
+            const unsigned el = __ballot_sync(FULL, w > 0.f);
+            if (e < 0 && hit) e = 32 * r + __ffs(hit) - 1;
+            if (el) last = 32 * r + 31 - __clz(el);
+            run = __shfl_sync(FULL, c, 31);
+        }
+        if (e < 0) e = last;  // the running sum never passed the target
+        if (e < 0) break;
+        float pivot1 = 0.f;
+        int j = 0;
+#pragma unroll
+        for (int r = 0; r < SR; ++r) {
+            const float xv = __shfl_sync(FULL, s.x[r], e & 31);
+            const int iv = __shfl_sync(FULL, s.i[r], e & 31);
+            if ((e >> 5) == r) {
+                pivot1 = xv;
+                j = iv;
+            }
+        }
+        const float pivot2 = (pivot1 + high) * 0.5f;
+        float m1 = 0.f, m2 = 0.f;
+        int C1 = 0, C2 = 0;
+#pragma unroll
+        for (int r = 0; r < SR; ++r) {
+            const bool a1 = kept[r] && s.x[r] > pivot1, a2 = kept[r] && s.x[r] > pivot2;
+            m1 += a1 ? s.x[r] : 0.f;
+            m2 += a2 ? s.x[r] : 0.f;
+            C1 += __popc(__ballot_sync(FULL, a1));
+            C2 += __popc(__ballot_sync(FULL, a2));
+        }
+        const float M1 = warp_sum(m1), M2 = warp_sum(m2);
+        if (f(C1, M1, pivot1)) {
+            rounds = round + 1;
+            return j;
+        }
+        if (f(C2, M2, pivot2)) {
+            low = pivot1;
+            high = pivot2;
+            S_low = M1;
+        } else {
+            low = pivot2;
+            S_low = M2;
+        }
+    }
+    rounds = R_MAX;
+    return -1;
+}
+
 template <bool VEC>
 __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
     const int C = int(cluster_nctarank());
@@ -172,13 +238,20 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
     const bool row_ok = r >= 0 && r < a.batch_in;
     const float* row = a.probs + size_t(row_ok ? r : 0) * size_t(V);
     const int k = a.top_k ? a.top_k[b] : 0;
+    const float tp = a.top_p ? a.top_p[b] : 1.f;
+    const float mp = a.min_p ? a.min_p[b] : 0.f;
     const bool k_on = k > 0 && k < V;
     const bool kfirst = a.order == 0 && k_on;
     const bool need_hist = kfirst && ns >= k;
 
     // ---- a2: pass 1, the only HBM read of the row, inside a split cluster barrier
     if (need_hist)
-        for (int i = tid; i < HBINS; i += NT) sm.hist()[i] = 0u;
+        for (int i = tid; i < HBINS; i += NT) {
+            sm.hist()[i] = 0u;
+            reinterpret_cast<uint32_t*>(sm.lv())[i] = 0u;
+        }
+    if (tid == 0) *sm.ctr() = NW;
+    __syncthreads();
     cluster_arrive();
     int pos = 0;
     bool bad = false;
@@ -211,8 +284,6 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
     }
 
     // ---- leader from here on
-    const float tp = a.top_p ? a.top_p[b] : 1.f;
-    const float mp = a.min_p ? a.min_p[b] : 0.f;
     Pred f;
     f.k_on = k_on;
     f.k = k;
@@ -222,17 +293,11 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
     f.t32 = 0.f;
     const bool any_filter = f.k_on || f.p_on || f.m_on;
 
-    int npos = 0;
-    bool any_bad = false;
-    float M = 0.f;           // sum of the per-CTA ordered sums, in rank order
-    uint32_t maxkey = 0;
-#pragma unroll 1
-    for (int c = 0; c < C; ++c) {
-        npos += int(sm.part()[c].u[0]);
-        any_bad |= sm.part()[c].u[1] != 0;
-        M += sm.part()[c].f[0];
-        maxkey = max(maxkey, sm.part()[c].u[2]);
-    }
+    const Totals tot = cluster_totals(sm, C);
+    const int npos = tot.npos;
+    const bool any_bad = tot.any_bad;
+    const float M = tot.M;   // sum of the per-CTA ordered sums
+    const uint32_t maxkey = tot.maxkey;
     if (tid < C) sm.cmass()[tid] = sm.part()[tid].f[0];
     const float rowmax = __uint_as_float(maxkey);
     bool valid = row_ok && !isnan(tp) && !isnan(mp) && !any_bad && M > 0.f && M <= 3.402823466e38f;
@@ -263,6 +328,24 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
         f.pthr = tp * M;
 
         // ---- a3 (second half, leader): t_k and F_k
+        if (kfirst && fits && regions_total(sm, C) <= SMALL) {
+            // The usual case: a short candidate list, finished in warp 0's registers.
+            if (warp == 0) {
+                const Small sl = small_gather(sm, C, CAP / C, lane);
+                const uint32_t tk = small_kth(sl, k, keyf);
+                bool kept[SR];
+                float fk = 0.f;
+#pragma unroll
+                for (int r = 0; r < SR; ++r) {
+                    kept[r] = sl.in[r] && keyf(sl.x[r]) >= tk;
+                    fk += kept[r] ? sl.x[r] : 0.f;
+                }
+                const float Fk = warp_sum(fk);
+                f.pthr = tp * Fk;  // top-p inside the k, measured against F_k
+                token = small_rounds(sl, kept, f, Fk, high, a.seed, a.offset, uint32_t(b), lane, rounds);
+                accepted = token >= 0;
+            }
+        } else {
         if (kfirst) {
             int n = -1;
             if (fits) {
@@ -304,12 +387,11 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
                 send_command(sm, c, C, tid);
                 pivot_pass<VEC>(row, g, sm, true, 0, low, low, 0, 1, warp, lane, tid);
                 cluster_sync();
-                count_low = 0;
-                S_low = 0.f;
-#pragma unroll 1
-                for (int cc = 0; cc < C; ++cc) {
-                    count_low += int(sm.part()[cc].u[0]);
-                    S_low += sm.part()[cc].f[0];
+                {
+                    const bool inC = lane < C;
+                    const Part& pc = sm.part()[inC ? lane : 0];
+                    count_low = warp_sum_i(inC ? int(pc.u[0]) : 0);
+                    S_low = warp_sum(inC ? pc.f[0] : 0.f);
                 }
                 if (tid < C) sm.cmass()[tid] = sm.part()[tid].f[0];
                 __syncthreads();
@@ -375,14 +457,12 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
             send_command(sm, c, C, tid);
             pivot_pass<VEC>(row, g, sm, true, 0, pivot1, pivot2, ia, ib, warp, lane, tid);
             cluster_sync();  // every part is in
-            int C1 = 0, C2 = 0;
-            float M1 = 0.f, M2 = 0.f;
-            for (int cc = 0; cc < C; ++cc) {
-                C1 += int(sm.part()[cc].u[0]);
-                C2 += int(sm.part()[cc].u[1]);
-                M1 += sm.part()[cc].f[0];
-                M2 += sm.part()[cc].f[1];
-            }
+            const bool inC = lane < C;
+            const Part& pc = sm.part()[inC ? lane : 0];
+            const int C1 = warp_sum_i(inC ? int(pc.u[0]) : 0);
+            const int C2 = warp_sum_i(inC ? int(pc.u[1]) : 0);
+            const float M1 = warp_sum(inC ? pc.f[0] : 0.f);
+            const float M2 = warp_sum(inC ? pc.f[1] : 0.f);
 
             // ---- a7: the three cases
             if (f(C1, M1, pivot1)) {
@@ -408,6 +488,7 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
             __syncthreads();
         }
         if (!accepted) rounds = R_MAX;
+        }
     }
 
     // ---- a8: outputs (the peers are let go first; warp 0 holds the result)
