@@ -49,7 +49,11 @@ def log(*a):
     print(*a, file=sys.stderr, flush=True)
 
 
-def parse_args():
+def parse_args(argv=None):
+    return parse_args_from(argv)
+
+
+def parse_args_from(argv):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
@@ -59,7 +63,7 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-oracle sample")
     ap.add_argument("--profile", action="store_true",
                     help="only run the headline step (warmup + steps launches) for a profiler; prints a short line")
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 def dist_info():
@@ -67,6 +71,28 @@ def dist_info():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return rank, world, local
+
+
+def rank_seed(rank: int) -> int:
+    """Input seed of a rank: every rank samples rows of its own (weak scaling)."""
+    import workloads
+    return workloads.cfg_seed(3) + rank
+
+
+def slowest(total_ms: float, device=None) -> float:
+    """The timed region of the slowest rank (MAX all-reduce); unchanged on one rank."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return total_ms
+    t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_value(world: int, rows_per_rank: int, steps: int, total_ms: float) -> float:
+    """Rows of all ranks per second of the slowest rank."""
+    return world * rows_per_rank * steps / (total_ms / 1e3)
 
 
 def measured_peak():
@@ -178,7 +204,7 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=dev)
     lib = ms.lib
 
-    w = workloads.config3(seed=workloads.cfg_seed(3) + rank, with_logits=True)
+    w = workloads.config3(seed=rank_seed(rank), with_logits=True)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     per_copy = w.probs.nbytes
     ncopy = max(4, math.ceil(3 * l2 / per_copy))
@@ -251,13 +277,8 @@ def run_ours(args):
         torch.cuda.synchronize(dev)
         if ctx:
             ctx.__exit__(None, None, None)
-        total_ms = start.elapsed_time(end)
+        total_ms = slowest(start.elapsed_time(end), dev)
         per = [a.elapsed_time(b) for a, b in ev]
-        if world > 1:
-            import torch.distributed as dist
-            t = torch.tensor([total_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            total_ms = float(t.item())
         return total_ms, per, (ctx.summary() if ctx else None)
 
     K, W = args.steps, args.warmup
@@ -270,7 +291,7 @@ def run_ours(args):
         return
     total_ms, per, clk = timed(calls["top_k_first"], K, W, clocks=True)
     kern_ms = statistics.mean(per)
-    value = world * B * K / (total_ms / 1e3)
+    value = weak_value(world, B, K, total_ms)
     ms_step = total_ms / K
 
     entries = {}
@@ -308,7 +329,7 @@ def run_ours(args):
     e2e_ms, _, _ = timed(e2e, ke, 3)
     h2d = host_p.numel() * 4 + host_k.numel() * 4 + host_pp.numel() * 4
     d2h = host_tok.numel() * 4 + host_val.numel()
-    e2e_value = world * B * ke / (e2e_ms / 1e3)
+    e2e_value = weak_value(world, B, ke, e2e_ms)
 
     peak, peak_kind = measured_peak()
     achieved = alg_bytes["top_k_first"] / (kern_ms * 1e-3) / 1e9
