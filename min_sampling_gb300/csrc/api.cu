@@ -60,27 +60,40 @@ fs_status prepare_kernel(const void* fn) {
     return FS_OK;
 }
 
-// Resident CTAs per SM for `fn` with `smem` bytes of dynamic shared memory (cached).
-static fs_status occupancy(const void* fn, size_t smem, int& occ) {
+// How many clusters of C CTAs of `fn` (with `smem` bytes of dynamic shared memory)
+// can be resident at once on the current device (cached).  This accounts for the
+// placement of a cluster inside one GPC, which a per-SM occupancy count does not.
+static fs_status active_clusters(const void* fn, size_t smem, int C, int& n) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e);
     static std::mutex mu;
-    static std::map<std::tuple<const void*, int, size_t>, int> cache;
+    static std::map<std::tuple<const void*, int, size_t, int>, int> cache;
     {
         std::lock_guard<std::mutex> lock(mu);
-        auto it = cache.find({fn, dev, smem});
+        auto it = cache.find({fn, dev, smem, C});
         if (it != cache.end()) {
-            occ = it->second;
+            n = it->second;
             return FS_OK;
         }
     }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(C), 1, 1);
+    cfg.blockDim = dim3(NT, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = unsigned(C);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     int v = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, fn, NT, smem);
+    e = cudaOccupancyMaxActiveClusters(&v, fn, &cfg);
     if (e != cudaSuccess) return cuda_fail(e);
     std::lock_guard<std::mutex> lock(mu);
-    cache[{fn, dev, smem}] = v;
-    occ = v;
+    cache[{fn, dev, smem, C}] = v;
+    n = v;
     return FS_OK;
 }
 
@@ -93,27 +106,25 @@ fs_status make_plan(int rows, int vocab, const void* fn, Plan& p) {
     if (st != FS_OK) return st;
     p.shift = seg_shift_for(vocab);
     p.ns = (vocab + (BLK << p.shift) - 1) / (BLK << p.shift);
-    // Largest C (<= MAX_CLUSTER, >= 4 segments per CTA) whose grid fits in one wave.
+    p.smem = Layout(p.ns).total();   // row-wide tables in every CTA
+    if (p.smem > optin) return FS_ERR_UNSUPPORTED;
+    // Largest C (<= MAX_CLUSTER, >= 4 segments per CTA) whose clusters are all
+    // resident at once (one wave); C = 1 when none is.
     int cmax = p.ns / 4;
     if (cmax > MAX_CLUSTER) cmax = MAX_CLUSTER;
     if (cmax < 1) cmax = 1;
     int chosen = 1;
-    const size_t smem = Layout(p.ns).total();   // row-wide tables in every CTA
-    for (int C = cmax; C >= 1; --C) {
-        if (smem > optin) continue;
-        int occ = 0;
-        st = occupancy(fn, smem, occ);
+    for (int C = cmax; C >= 2; --C) {
+        int n = 0;
+        st = active_clusters(fn, p.smem, C, n);
         if (st != FS_OK) return st;
-        if (occ < 1) continue;
-        if (C == 1 || (long long)rows * C <= (long long)sms * occ) {
+        if (rows <= n) {
             chosen = C;
             break;
         }
     }
     p.C = chosen;
     p.nsc = ((p.ns + chosen - 1) / chosen + 3) & ~3;   // a multiple of 4 segments per CTA
-    p.smem = smem;
-    if (p.smem > optin) return FS_ERR_UNSUPPORTED;
     return FS_OK;
 }
 

@@ -113,6 +113,7 @@ struct Smem {
     __device__ __forceinline__ int* red() const { return at<int>(Layout::RED); }            // [64] scratch
     __device__ __forceinline__ float* cmass() const { return at<float>(Layout::MISC); }     // [MAX_CLUSTER]
     __device__ __forceinline__ int* ctr() const { return at<int>(Layout::MISC + 64); }      // pass-1 trip counter
+    __device__ __forceinline__ int* bcast() const { return at<int>(Layout::MISC + 80); }    // [4] CTA broadcast
     __device__ __forceinline__ uint32_t* segkey() const { return at<uint32_t>(Layout(ns).arr(0)); }
     __device__ __forceinline__ float* mass(int i) const { return at<float>(Layout(ns).arr(1 + i)); }  // i < 3
     __device__ __forceinline__ int* list() const { return at<int>(Layout(ns).arr(4)); }     // live segments
@@ -432,7 +433,7 @@ __device__ __forceinline__ void stream_warp(const float* __restrict__ row, Geom 
 // before the cluster's first barrier completes.
 template <bool VEC, bool NC, bool PROB>
 __device__ __forceinline__ void pass1(const float* __restrict__ row, Geom g, Smem sm, int warp, int lane, int& pos,
-                                      bool& bad) {
+                                      bool& bad, uint32_t& kmax) {
     const int spt = TB >> g.shift;  // segments per trip
     const int ntrip = (g.s1 - g.s0 + spt - 1) / spt;
     const int mask = g.seg_it() - 1;
@@ -475,6 +476,7 @@ __device__ __forceinline__ void pass1(const float* __restrict__ row, Geom g, Sme
                 }
             }
             km[j] = __reduce_max_sync(FULL, k);
+            kmax = max(kmax, km[j]);
             s[j] = PROB ? (A[j].x + A[j].y) + (A[j].z + A[j].w) : 0.f;
         }
         if (PROB) {
@@ -514,27 +516,54 @@ __device__ __forceinline__ void st_rank_v4(void* local_addr, uint4 v, uint32_t r
     }
 }
 
-// After pass 1 and the cluster barrier that follows it, every CTA: its segments'
-// keys and (prob) masses into the leader's table, its totals into part[rank] of every
-// CTA (f[0] ordered mass of its segments, u[0] positive count, u[1] bad flag, u[2]
-// maximum key) and, if `hist_shift` >= 0, one count per segment maximum into the
-// histogram (key >> hist_shift) of every CTA of the cluster, each of which cleared its
-// own (and its lv, used here for its local counts) before that barrier.  The CTA's
-// first segment is a multiple of 4, so the table moves in 16-byte words.
-// Block-collective.
+// After pass 1 and the cluster barrier that follows it, every CTA: with `publish`, its
+// segments' masses into the leader's mass table (for draws over the whole row); its
+// totals into part[rank] of every CTA (f[0] ordered mass of its segments, u[0]
+// positive count, u[1] bad flag, u[2] maximum key); and, if `hist_shift` >= 0, one
+// count per segment maximum into the histogram (key >> hist_shift) of every CTA of the
+// cluster, each of which cleared its own (and its lv, used here for its local counts)
+// before that barrier.  The CTA's first segment is a multiple of 4, so the table moves
+// in 16-byte words.  Block-collective.
 __device__ __forceinline__ void pass1_totals(Geom g, Smem sm, bool leader, int rank, int C, int pos, bool bad,
-                                             int hist_shift, bool prob, int warp, int lane, int tid) {
+                                             uint32_t kmax, int hist_shift, bool prob, bool publish, int warp,
+                                             int lane, int tid) {
     __syncthreads();  // the table written by pass 1
+    uint32_t* loc = reinterpret_cast<uint32_t*>(sm.lv());
+    if (hist_shift >= 0) {  // this CTA's counts in lv (cleared with the histogram)
+#pragma unroll 1
+        for (int i = g.s0 + tid; i < g.s1; i += NT)
+            atomicAdd(&loc[min(uint32_t(HBINS - 1), sm.segkey()[i] >> hist_shift)], 1u);
+    }
+    if (publish && !leader) {
+#pragma unroll 1
+        for (int i = g.s0 + 4 * tid; i < g.s1; i += 4 * NT) {
+            const int nv = min(4, g.s1 - i);
+            if (nv == 4) {
+                st_rank_v4(&sm.mass(0)[i], *reinterpret_cast<const uint4*>(&sm.mass(0)[i]), 0, 1);
+            } else {  // the row's last, partial word: never past this CTA's range
+#pragma unroll 1
+                for (int q = 0; q < nv; ++q) put_leader(&sm.mass(0)[i + q], __float_as_uint(sm.mass(0)[i + q]), false);
+            }
+        }
+    }
+    // Per warp: counts, flags, maximum and the ordered mass of a fixed share of segments.
+    float ms = 0.f;
+    if (prob) {
+        int r0, r1;
+        warp_range(g.s1 - g.s0, warp, r0, r1);
+        ms = warp_ordered_sum(sm.mass(0), g.s0 + r0, g.s0 + r1, lane);
+    }
     pos = warp_sum_i(pos);
     const int b = __any_sync(FULL, bad) ? 1 : 0;
-    uint32_t km = 0;
-    if (hist_shift >= 0) {
-        // This CTA's counts in lv (cleared with the histogram), then every non-empty bin
-        // added once into each CTA's histogram.
-        uint32_t* loc = reinterpret_cast<uint32_t*>(sm.lv());
-#pragma unroll 1
-        for (int i = g.s0 + tid; i < g.s1; i += NT) atomicAdd(&loc[min(uint32_t(HBINS - 1), sm.segkey()[i] >> hist_shift)], 1u);
-        __syncthreads();
+    float* rf = reinterpret_cast<float*>(sm.red());
+    if (lane == 0) {
+        sm.red()[warp] = pos;
+        sm.red()[NW + warp] = b;
+        sm.red()[2 * NW + warp] = int(kmax);
+        rf[3 * NW + warp] = ms;
+    }
+    __syncthreads();
+    if (hist_shift >= 0) {  // every non-empty bin added once into each CTA's histogram
 #pragma unroll
         for (int q = 0; q < HBINS / NT; ++q) {
             const int bin = q * NT + tid;
@@ -554,48 +583,19 @@ __device__ __forceinline__ void pass1_totals(Geom g, Smem sm, bool leader, int r
             }
         }
     }
-#pragma unroll 1
-    for (int i = g.s0 + 4 * tid; i < g.s1; i += 4 * NT) {
-        const uint4 kv = *reinterpret_cast<const uint4*>(&sm.segkey()[i]);
-        const int nv = min(4, g.s1 - i);
-        km = max(km, max(max(kv.x, nv > 1 ? kv.y : 0u), max(nv > 2 ? kv.z : 0u, nv > 3 ? kv.w : 0u)));
-        if (!leader) {
-            if (nv == 4) {
-                st_rank_v4(&sm.segkey()[i], kv, 0, 1);
-                if (prob) st_rank_v4(&sm.mass(0)[i], *reinterpret_cast<const uint4*>(&sm.mass(0)[i]), 0, 1);
-            } else {  // the row's last, partial word: never past this CTA's range
-#pragma unroll 1
-                for (int q = 0; q < nv; ++q) {
-                    put_leader(&sm.segkey()[i + q], sm.segkey()[i + q], false);
-                    if (prob) put_leader(&sm.mass(0)[i + q], __float_as_uint(sm.mass(0)[i + q]), false);
-                }
-            }
-        }
-    }
-    km = warp_max_u(km);
-    float* rf = reinterpret_cast<float*>(sm.red());
-    if (lane == 0) {
-        sm.red()[warp] = pos;
-        sm.red()[NW + warp] = b;
-        sm.red()[2 * NW + warp] = int(km);
-    }
-    if (warp == 0) {
-        const float s = prob ? warp_ordered_sum(sm.mass(0), g.s0, g.s1, lane) : 0.f;
-        if (lane == 0) rf[3 * NW] = s;
-    }
-    __syncthreads();
     if (tid < C) {
         int p = 0, nb = 0;
         uint32_t mk = 0;
-#pragma unroll 1
+        float m = 0.f;
+#pragma unroll
         for (int w = 0; w < NW; ++w) {
             p += sm.red()[w];
             nb |= sm.red()[NW + w];
             mk = max(mk, uint32_t(sm.red()[2 * NW + w]));
+            m += rf[3 * NW + w];
         }
         st_rank_v4(&sm.part()[rank].u[0], make_uint4(uint32_t(p), uint32_t(nb), mk, 0u), uint32_t(tid), uint32_t(rank));
-        st_rank_v4(&sm.part()[rank].f[0], make_uint4(__float_as_uint(rf[3 * NW]), 0u, 0u, 0u), uint32_t(tid),
-                   uint32_t(rank));
+        st_rank_v4(&sm.part()[rank].f[0], make_uint4(__float_as_uint(m), 0u, 0u, 0u), uint32_t(tid), uint32_t(rank));
     }
 }
 
@@ -668,114 +668,96 @@ __device__ __forceinline__ void pivot_pass(const float* __restrict__ row, Geom g
 
 // ------------------------------------------------------------------ candidate lists
 
-// Ordered list of the segments s in [a, b) with segkey[s] >= thr, into list[0..n).
-// Block-collective; returns n.
-__device__ __forceinline__ int live_list(Smem sm, int a, int b, uint32_t thr, int warp, int lane) {
+// Every element with key >= thr of the segments [a, b), in index order:
+// out(p, value, index) for p = 0, 1, ...  Returns the exact count.  Warp w takes the
+// w-th contiguous share of [a, b), lists its segments whose maximum key is >= thr
+// (into list[], inside its own share), stages their blocks 2*SBH at a time
+// (cp.async) and counts; one block barrier turns the warps' counts into output
+// offsets; then each warp emits (from the staged blocks, or staging again when it
+// had more than one batch).  Block-collective; red[0..NW) is used.
+template <bool VEC, typename KEYF, typename OUT>
+__device__ __forceinline__ int collect_range(const float* __restrict__ row, Geom g, Smem sm, int a, int b,
+                                             uint32_t thr, KEYF keyf, int warp, int lane, OUT out) {
+    constexpr int WB = 2 * SBH;  // blocks per batch
     int r0, r1;
     warp_range(b - a, warp, r0, r1);
     r0 += a;
     r1 += a;
-    int cnt = 0;
+    // This warp's live segments, in order, into list[r0 ..).
+    int nl = 0;
 #pragma unroll 1
-    for (int base = r0; base < r1; base += 32) {
-        const int i = base + lane;
-        cnt += __popc(__ballot_sync(FULL, i < r1 && sm.segkey()[i] >= thr));
-    }
-    if (lane == 0) sm.red()[warp] = cnt;
-    __syncthreads();
-    int off = 0, total = 0;
-#pragma unroll 1
-    for (int w = 0; w < NW; ++w) {
-        if (w < warp) off += sm.red()[w];
-        total += sm.red()[w];
-    }
-#pragma unroll 1
-    for (int base = r0; base < r1; base += 32) {
-        const int i = base + lane;
+    for (int b0 = r0; b0 < r1; b0 += 32) {
+        const int i = b0 + lane;
         const bool live = i < r1 && sm.segkey()[i] >= thr;
         const unsigned bal = __ballot_sync(FULL, live);
-        if (live) sm.list()[off + __popc(bal & ((1u << lane) - 1u))] = i;
-        off += __popc(bal);
+        if (live) sm.list()[r0 + nl + __popc(bal & ((1u << lane) - 1u))] = i;
+        nl += __popc(bal);
     }
-    __syncthreads();
-    return total;
-}
-
-// Read the listed segments (list[0..nlive), in order) and emit, in index order, every
-// element with key >= thr: out(p, value, index) for p = 0, 1, ...  Returns the exact
-// count.  Listed blocks go in batches of NW * 2 * SBH; block j of a batch to warp
-// j % NW (staged with cp.async), so that a short list spreads over all warps; per-block
-// counts fix every block's output offset.  Block-collective.
-template <bool VEC, typename KEYF, typename OUT>
-__device__ __forceinline__ int collect(const float* __restrict__ row, Geom g, Smem sm, int nlive, uint32_t thr,
-                                       KEYF keyf, int warp, int lane, OUT out) {
-    constexpr int WB = 2 * SBH;        // blocks per warp per batch
-    constexpr int NB = NW * WB;        // blocks per batch (<= 32: one per lane of a scan)
-    static_assert(NB <= 32, "a batch's block counts are scanned by one warp");
-    const int nblk = nlive << g.shift;
+    __syncwarp();
+    const int nblk = nl << g.shift;
     const int mask = g.seg_it() - 1;
     float* st = sm.stage() + warp * (WB * BLK) + lane * 4;
-    int total = 0;
+    auto block_base = [&](int lb) { return g.base(sm.list()[r0 + (lb >> g.shift)], lb & mask, lane); };
+    auto stage = [&](int c0) {
 #pragma unroll 1
-    for (int c0 = 0; c0 < nblk; c0 += NB) {
-        const int nb = min(NB, nblk - c0);
-        // block c0 + warp + NW * i is this warp's slot i
-#pragma unroll 1
-        for (int i = 0; i < WB && warp + NW * i < nb; ++i) {
-            const int lb = c0 + warp + NW * i;
-            stage4<VEC>(st + i * BLK, row, g.V, g.base(sm.list()[lb >> g.shift], lb & mask, lane));
-        }
+        for (int j = 0; j < WB && c0 + j < nblk; ++j) stage4<VEC>(st + j * BLK, row, g.V, block_base(c0 + j));
         cp_async_commit();
         cp_async_wait<0>();
+    };
+    auto keep = [&](int j, int base, int q) { return keyf(st[j * BLK + q]) >= thr && base + q < g.V; };
+    int cnt = 0;
 #pragma unroll 1
-        for (int i = 0; i < WB && warp + NW * i < nb; ++i) {
-            const int lb = c0 + warp + NW * i;
-            const int base = g.base(sm.list()[lb >> g.shift], lb & mask, lane);
-            int cnt = 0;
+    for (int c0 = 0; c0 < nblk; c0 += WB) {
+        stage(c0);
+#pragma unroll 1
+        for (int j = 0; j < WB && c0 + j < nblk; ++j) {
+            const int base = block_base(c0 + j);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) cnt += (keyf(st[i * BLK + q]) >= thr && base + q < g.V);
-            cnt = warp_sum_i(cnt);
-            if (lane == 0) sm.red()[warp + NW * i] = cnt;
+            for (int q = 0; q < 4; ++q) cnt += keep(j, base, q);
         }
-        __syncthreads();
-        const int bc = lane < nb ? sm.red()[lane] : 0;
-        const int bincl = warp_incl_scan_i(bc, lane);
-        const int chunk = __shfl_sync(FULL, bincl, 31);
-        __syncthreads();
+    }
+    cnt = warp_sum_i(cnt);
+    if (lane == 0) sm.red()[warp] = cnt;
+    __syncthreads();
+    int pos = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+        const int c = sm.red()[w];
+        pos += w < warp ? c : 0;
+        total += c;
+    }
+    __syncthreads();
 #pragma unroll 1
-        for (int i = 0; i < WB && warp + NW * i < nb; ++i) {
-            const int jb = warp + NW * i;
-            const int lb = c0 + jb;
-            const int base = g.base(sm.list()[lb >> g.shift], lb & mask, lane);
+    for (int c0 = 0; c0 < nblk; c0 += WB) {
+        if (nblk > WB) stage(c0);  // one batch is still staged from the count
+#pragma unroll 1
+        for (int j = 0; j < WB && c0 + j < nblk; ++j) {
+            const int base = block_base(c0 + j);
             int k = 0;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) k += (keyf(st[i * BLK + q]) >= thr && base + q < g.V);
+            for (int q = 0; q < 4; ++q) k += keep(j, base, q);
             const int incl = warp_incl_scan_i(k, lane);
-            int p = total + __shfl_sync(FULL, bincl - bc, jb) + incl - k;
+            int p = pos + incl - k;
 #pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
-                const float x = st[i * BLK + q];
-                if (keyf(x) >= thr && base + q < g.V) out(p++, x, base + q);
-            }
+            for (int q = 0; q < 4; ++q)
+                if (keep(j, base, q)) out(p++, st[j * BLK + q], base + q);
+            pos += __shfl_sync(FULL, incl, 31);
         }
-        total += chunk;
     }
     return total;
 }
 
-// Every CTA: collect its own elements with key >= thr into its region of the leader's
-// list (entries [rank * rc, rank * rc + rc)), in index order, or with `to_all` into
-// that region of every CTA's list; the exact count goes to part[rank].u[4] of every CTA
-// of the cluster, so that after the next cluster barrier each CTA can tell whether all
-// regions fit.  Block-collective.
+// Every CTA: collect its own elements with key >= thr, in index order, into entries
+// [base, base + cap) of the leader's list, or with `to_all` of every CTA's list; with
+// `bcast`, the exact count goes to part[rank].u[4] of every CTA of the cluster, so that
+// after the next cluster barrier each CTA can tell whether all regions fit and where
+// each rank's candidates start.  Block-collective.
 template <bool VEC, typename KEYF>
 __device__ __forceinline__ void collect_own(const float* __restrict__ row, Geom g, Smem sm, bool leader, int rank,
-                                            int C, int rc, uint32_t thr, KEYF keyf, bool to_all, int warp, int lane,
-                                            int tid) {
-    const int nlive = live_list(sm, g.s0, g.s1, thr, warp, lane);
-    const int base = rank * rc;
-    const int n = collect<VEC>(row, g, sm, nlive, thr, keyf, warp, lane, [&](int p, float x, int ix) {
-        if (p < rc) {
+                                            int C, int base, int cap, uint32_t thr, KEYF keyf, bool to_all,
+                                            bool bcast, int warp, int lane, int tid) {
+    const int n = collect_range<VEC>(row, g, sm, g.s0, g.s1, thr, keyf, warp, lane, [&](int p, float x, int ix) {
+        if (p < cap) {
             if (to_all) {
 #pragma unroll 1
                 for (int r = 0; r < C; ++r) {
@@ -793,7 +775,7 @@ __device__ __forceinline__ void collect_own(const float* __restrict__ row, Geom 
             }
         }
     });
-    if (tid < C) {
+    if (bcast && tid < C) {
         uint32_t* dst = reinterpret_cast<uint32_t*>(&sm.part()[rank]) + 8;
         if (tid == rank) {
             *dst = uint32_t(n);
@@ -832,6 +814,30 @@ __device__ __forceinline__ Totals cluster_totals(Smem sm, int C) {
     t.M = warp_sum(in ? p.f[0] : 0.f);
     t.maxkey = warp_max_u(in ? p.u[2] : 0u);
     return t;
+}
+
+// Start of rank r's candidates in the list: r * rc in region layout, or the count of
+// the lower ranks when the list is contiguous.  Warp-parallel (lane r reads count r).
+__device__ __forceinline__ int exact_base(Smem sm, int rank) {
+    const int lane = threadIdx.x & 31;
+    return warp_sum_i(lane < rank ? int(sm.part()[lane].u[4]) : 0);
+}
+
+// After a region collection and the cluster barrier that follows it, on every CTA
+// alike: 0 when every region fit (the list stays in regions of CAP / C); 1 when a
+// region overflowed but the total fits, after every CTA collected again at exact
+// offsets and the cluster synchronised (the list is contiguous, in index order); -1
+// when more than CAP elements qualify.  Block-collective on every CTA.
+template <bool VEC, typename KEYF>
+__device__ __forceinline__ int settle_list(const float* __restrict__ row, Geom g, Smem sm, bool leader, int rank,
+                                           int C, uint32_t thr, KEYF keyf, bool to_all, int warp, int lane,
+                                           int tid) {
+    if (regions_fit(sm, C, CAP / C)) return 0;
+    if (regions_total(sm, C) > CAP) return -1;
+    const int base = exact_base(sm, rank);
+    collect_own<VEC>(row, g, sm, leader, rank, C, base, CAP - base, thr, keyf, to_all, false, warp, lane, tid);
+    cluster_sync();
+    return 1;
 }
 
 // The candidate regions of all ranks, concatenated in rank order at the front of
@@ -912,9 +918,10 @@ struct Small {
     int n;
 };
 
-// Gather the joined candidate list (regions of rc entries, counts in part[r].u[4], in
-// rank order) straight from the regions, n <= SMALL.  Warp-collective.
-__device__ __forceinline__ Small small_gather(Smem sm, int C, int rc, int lane) {
+// Gather the candidate list (counts in part[r].u[4], in rank order; rank r's entries
+// start at r * rc, or with `exact` right after the lower ranks') n <= SMALL.
+// Warp-collective.
+__device__ __forceinline__ Small small_gather(Smem sm, int C, int rc, bool exact, int lane) {
     // Exclusive prefix of the region counts, region r's offset in lane r.
     const int cnt = lane < C ? int(sm.part()[lane].u[4]) : 0;
     const int off = warp_incl_scan_i(cnt, lane) - cnt;
@@ -942,7 +949,7 @@ __device__ __forceinline__ Small small_gather(Smem sm, int C, int rc, int lane) 
     for (int r = 0; r < SR; ++r) {
         const int e = 32 * r + lane;
         s.in[r] = e < s.n;
-        const int a = rr[r] * rc + (e - oo[r]);
+        const int a = exact ? e : rr[r] * rc + (e - oo[r]);
         s.x[r] = s.in[r] ? sm.lv()[a] : 0.f;
         s.i[r] = s.in[r] ? sm.li()[a] : 0;
     }
@@ -1003,53 +1010,52 @@ __device__ __forceinline__ int filter_list_warp(Smem sm, int n, uint32_t t, KEYF
     return w;
 }
 
-// Leader, block-collective: a lower bound L0 <= t_k of the row's k-th largest order
-// key from the histogram of the segment maxima (key >> bshift).  Scanning from the
-// top bin down, the bin in which the count reaches k holds the k-th largest segment
-// maximum, and its lower edge is at most that value.  The k-th largest of any subset
-// of the row (here, the segment maxima) is at most the row's own k-th largest, so
-// L0 <= t_k, and every segment holding an element >= t_k has its maximum >= L0.
-// Returns 0 when there are fewer than k segments.
-__device__ __forceinline__ uint32_t hist_bound(Smem sm, int ns, int k, int bshift, int warp, int lane,
-                                                  int tid) {
+// Block-collective: a lower bound L0 <= t_k of the row's k-th largest order key from
+// the histogram of the segment maxima (key >> bshift).  Scanning from the top bin
+// down, the bin in which the count reaches k holds the k-th largest segment maximum,
+// and its lower edge is at most that value.  The k-th largest of any subset of the
+// row (here, the segment maxima) is at most the row's own k-th largest, so L0 <= t_k,
+// and every segment holding an element >= t_k has its maximum >= L0.  Warp 0 scans
+// 128 bins at a time from the bin of the row maximum `maxkey` down; the result is
+// broadcast through shared memory.  Returns 0 when there are fewer than k segments.
+__device__ __forceinline__ uint32_t hist_bound(Smem sm, int ns, int k, int bshift, uint32_t maxkey, int warp,
+                                               int lane) {
     if (ns < k) return 0;
-    // Thread t owns positions 4t..4t+3 counted from the top bin (bins HBINS-1-pos).
-    uint32_t c[4];
-    uint32_t own = 0;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        c[q] = sm.hist()[HBINS - 1 - (4 * tid + q)];
-        own += c[q];
-    }
-    uint32_t incl = own;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        const uint32_t o = __shfl_up_sync(FULL, incl, d);
-        if (lane >= d) incl += o;
-    }
-    if (lane == 31) sm.red()[warp] = int(incl);
-    __syncthreads();
-    uint32_t before = incl - own;
+    if (warp == 0) {
+        const uint32_t kk = uint32_t(k);
+        uint32_t before = 0;
+        int found = 0;
 #pragma unroll 1
-    for (int w = 0; w < warp; ++w) before += uint32_t(sm.red()[w]);
-    const uint32_t kk = uint32_t(k);
-    if (before < kk && before + own >= kk) {
-        uint32_t cum = before;
-        int pos = 4 * tid;
+        for (int top = int(min(uint32_t(HBINS - 1), maxkey >> bshift)); top >= 0; top -= 128) {
+            // Lane l holds bins top - 4l, top - 4l - 1, ... (descending).
+            uint32_t c[4], own = 0;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            cum += c[q];
-            if (cum >= kk) {
-                pos = 4 * tid + q;
+            for (int q = 0; q < 4; ++q) {
+                const int bin = top - 4 * lane - q;
+                c[q] = bin >= 0 ? sm.hist()[bin] : 0u;
+                own += c[q];
+            }
+            const uint32_t incl = uint32_t(warp_incl_scan_i(int(own), lane));
+            const uint32_t total = __shfl_sync(FULL, incl, 31);
+            if (before + total >= kk) {
+                const bool cross = before + incl - own < kk && before + incl >= kk;
+                const int l = __ffs(__ballot_sync(FULL, cross)) - 1;
+                uint32_t cum = before + incl - own;
+                int q = 0;  // the first of the lane's bins where the running count reaches k
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    cum += c[t];
+                    if (cum < kk) q = t + 1;
+                }
+                found = __shfl_sync(FULL, top - 4 * lane - q, l);
                 break;
             }
+            before += total;
         }
-        sm.red()[NW] = HBINS - 1 - pos;
+        if (lane == 0) *sm.bcast() = found;
     }
     __syncthreads();
-    const uint32_t bin = uint32_t(sm.red()[NW]);
-    __syncthreads();
-    return bin << bshift;
+    return uint32_t(*sm.bcast()) << bshift;
 }
 
 // ------------------------------------------------------------------ draws
@@ -1478,50 +1484,30 @@ FS_COLD __device__ float massge_leader(const float* __restrict__ row, Geom g, Sm
     return m;
 }
 
-// Leader alone: every element of the row with key >= thr into lv/li[0..n) in index
-// order, read through the leader's full segment table.  Returns the exact count
-// (entries beyond CAP are dropped).  Block-collective.
-template <bool VEC, typename KEYF>
-FS_COLD __device__ int collect_all(const float* __restrict__ row, Geom g, Smem sm, uint32_t thr,
-                                       KEYF keyf, int warp, int lane) {
-    const int nlive = live_list(sm, 0, g.ns, thr, warp, lane);
-    return collect<VEC>(row, g, sm, nlive, thr, keyf, warp, lane, [&](int p, float x, int ix) {
-        if (p < CAP) {
-            sm.lv()[p] = x;
-            sm.li()[p] = ix;
-        }
-    });
-}
-
 // Leader: every element with key >= thr, in index order, into lv/li[0..n), on the
 // leader's command.  The whole cluster collects (each CTA its own segments, into its
-// region of the leader's list); if a region overflowed but the total fits, the leader
-// collects alone.  Returns n, or -1 when more than CAP elements qualify (the peers then
-// still wait for commands).  With `exit_if_fit` the peers have left whenever n >= 0.
+// region of the leader's list; again at exact offsets if a region overflowed).
+// Returns n, or -1 when more than CAP elements qualify (the peers then still wait for
+// commands).  With `exit_if_fit` the peers have left whenever n >= 0.
 template <bool VEC, typename KEYF>
 __device__ __forceinline__ int gather_leader(const float* __restrict__ row, Geom g, Smem sm, int C, uint32_t thr,
-                                         KEYF keyf, bool exit_if_fit, int warp, int lane, int tid) {
+                                             KEYF keyf, bool exit_if_fit, int warp, int lane, int tid) {
     const int rc = CAP / C;
     Ctl c{};
     c.cmd = CMD_COLLECT;
     c.flag = exit_if_fit ? 1 : 0;
     c.u[0] = thr;
     send_command(sm, c, C, tid);
-    collect_own<VEC>(row, g, sm, true, 0, C, rc, thr, keyf, false, warp, lane, tid);
+    collect_own<VEC>(row, g, sm, true, 0, C, 0, rc, thr, keyf, false, true, warp, lane, tid);
     cluster_sync();  // every region and count is in
+    const int mode = settle_list<VEC>(row, g, sm, true, 0, C, thr, keyf, false, warp, lane, tid);
+    if (mode < 0) return -1;
     const int n = regions_total(sm, C);
-    if (regions_fit(sm, C, rc)) {
+    if (mode == 0) {
         if (warp == 0) join_regions_warp(sm, C, rc, lane);
         __syncthreads();
-        return n;
     }
-    if (n > CAP) return -1;
-    if (exit_if_fit) {
-        Ctl e{};
-        e.cmd = CMD_EXIT;
-        send_command(sm, e, C, tid);
-    }
-    return collect_all<VEC>(row, g, sm, thr, keyf, warp, lane);
+    return n;
 }
 
 }  // namespace fsd

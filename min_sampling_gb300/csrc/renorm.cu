@@ -81,8 +81,6 @@ __device__ __forceinline__ void filter_peer(const float* __restrict__ row, float
         } else if (c.cmd == CMD_WRITE) {
             write_pass<VEC, KIND>(row, orow, g, sm, c.flag != 0, c.u[0], c.f[0], warp, lane);
             return;
-        } else if (c.cmd == CMD_COLLECT) {
-            collect_own<VEC>(row, g, sm, false, rank, C, CAP / C, c.u[0], KEYF(), false, warp, lane, tid);
         } else {
             return;  // CMD_EXIT
         }
@@ -122,9 +120,11 @@ __global__ void __launch_bounds__(NT, 4) filter_kernel(const FilterArgs a) {
     cluster_arrive();
     int pos = 0;
     bool bad = false;
-    pass1<VEC, false, IS_PROB>(row, g, sm, warp, lane, pos, bad);
+    uint32_t kmax = 0;
+    pass1<VEC, false, IS_PROB>(row, g, sm, warp, lane, pos, bad, kmax);
     cluster_wait();  // every CTA has started and cleared its histogram
-    pass1_totals(g, sm, leader, rank, C, pos, bad, need_hist ? (IS_PROB ? 21 : 22) : -1, IS_PROB, warp, lane, tid);
+    pass1_totals(g, sm, leader, rank, C, pos, bad, kmax, need_hist ? (IS_PROB ? 21 : 22) : -1, IS_PROB, false, warp,
+                 lane, tid);
     cluster_sync();  // the leader's segment table, every CTA's parts and histogram, are complete
 
     const Totals tot = cluster_totals(sm, C);
@@ -138,28 +138,30 @@ __global__ void __launch_bounds__(NT, 4) filter_kernel(const FilterArgs a) {
 
     // ---- top-k: every CTA derives the same lower bound L0 <= t from its copy of the
     // histogram and sends its elements >= L0 to its region of every CTA's list.  When
-    // every region fits, each CTA finds t and the kept mass itself and writes its share.
+    // the list is complete, each CTA finds t and the kept mass itself and writes its
+    // share.
     uint32_t L0 = 0u;
-    bool fits = false;
+    int list_mode = -1;  // 0: regions fit, 1: contiguous, -1: no list
     if (k_on) {
-        L0 = need_hist ? hist_bound(sm, ns, k, IS_PROB ? 21 : 22, warp, lane, tid) : 0u;
+        L0 = need_hist ? hist_bound(sm, ns, k, IS_PROB ? 21 : 22, maxkey, warp, lane) : 0u;
         if (IS_PROB) L0 = max(L0, 1u);
-        collect_own<VEC>(row, g, sm, leader, rank, C, CAP / C, L0, keyf, true, warp, lane, tid);
+        collect_own<VEC>(row, g, sm, leader, rank, C, rank * (CAP / C), CAP / C, L0, keyf, true, true, warp, lane,
+                         tid);
         cluster_sync();  // every region and count is in every CTA
-        fits = regions_fit(sm, C, CAP / C);
+        list_mode = settle_list<VEC>(row, g, sm, leader, rank, C, L0, keyf, true, warp, lane, tid);
     }
-    if (fits) {
+    if (list_mode >= 0) {
         // Every element >= L0 (hence >= t) is in the list.
         if (warp == 0) {
             uint32_t t;
             float s = 0.f;
             if (regions_total(sm, C) <= SMALL) {  // the usual case: in registers
-                const Small sl = small_gather(sm, C, CAP / C, lane);
+                const Small sl = small_gather(sm, C, CAP / C, list_mode == 1, lane);
                 t = small_kth(sl, k, keyf);
 #pragma unroll
                 for (int r = 0; r < SR; ++r) s += sl.in[r] && keyf(sl.x[r]) >= t ? sl.x[r] : 0.f;
             } else {
-                const int n = join_regions_warp(sm, C, CAP / C, lane);
+                const int n = list_mode == 0 ? join_regions_warp(sm, C, CAP / C, lane) : regions_total(sm, C);
                 t = kth_key_warp(sm, n, k, keyf, lane);
                 for (int i = lane; i < n; i += 32) s += keyf(sm.lv()[i]) >= t ? sm.lv()[i] : 0.f;
             }
@@ -187,25 +189,8 @@ __global__ void __launch_bounds__(NT, 4) filter_kernel(const FilterArgs a) {
     if (valid) {
         if (KIND != K_TOPP) {
             if (k_on) {
-                int n = -1;
-                if (regions_total(sm, C) <= CAP) n = collect_all<VEC>(row, g, sm, L0, keyf, warp, lane);
-                if (n >= 0) {
-                    // Every element >= L0 (hence >= t) is in the list.
-                    if (warp == 0) {
-                        const uint32_t tt = kth_key_warp(sm, n, k, keyf, lane);
-                        float s = 0.f;
-                        for (int i = lane; i < n; i += 32) s += keyf(sm.lv()[i]) >= tt ? sm.lv()[i] : 0.f;
-                        s = warp_sum(s);
-                        if (lane == 0) {
-                            sm.red()[40] = int(tt);
-                            reinterpret_cast<float*>(sm.red())[41] = s;
-                        }
-                    }
-                    __syncthreads();
-                    t = uint32_t(sm.red()[40]);
-                    denom = reinterpret_cast<float*>(sm.red())[41];
-                    __syncthreads();
-                } else {
+                {
+                    // More than CAP candidates: the threshold by bisection with the cluster.
                     Bisect st;
                     // crit(L0) holds when L0 came from the segment maxima; otherwise start
                     // from 0 (count(key >= 0) = V >= k).

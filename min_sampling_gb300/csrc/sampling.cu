@@ -72,12 +72,16 @@ __device__ __forceinline__ void sample_peer(const float* __restrict__ row, Geom 
             bisect_pass<VEC, false>(row, g, sm, false, rank, c.u[3], hi, c.u[0], c.u[1], c.u[2], KeyProb(), warp,
                                     lane, tid);
         } else if (c.cmd == CMD_COLLECT) {
-            collect_own<VEC>(row, g, sm, false, rank, C, CAP / C, c.u[0], KeyProb(), false, warp, lane, tid);
+            collect_own<VEC>(row, g, sm, false, rank, C, rank * (CAP / C), CAP / C, c.u[0], KeyProb(), false, true,
+                             warp, lane, tid);
         } else {
             return;  // CMD_EXIT
         }
         cluster_sync();  // the results are in the leader
-        if (c.cmd == CMD_COLLECT && c.flag && regions_fit(sm, C, CAP / C)) return;
+        if (c.cmd == CMD_COLLECT) {
+            const int mode = settle_list<VEC>(row, g, sm, false, rank, C, c.u[0], KeyProb(), false, warp, lane, tid);
+            if (c.flag && mode >= 0) return;
+        }
     }
 }
 
@@ -255,8 +259,9 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
     cluster_arrive();
     int pos = 0;
     bool bad = false;
+    uint32_t kmax = 0;
     if (row_ok) {
-        pass1<VEC, true, true>(row, g, sm, warp, lane, pos, bad);
+        pass1<VEC, true, true>(row, g, sm, warp, lane, pos, bad, kmax);
     } else {
         for (int i = g.s0 + tid; i < g.s1; i += NT) {
             sm.segkey()[i] = 0u;
@@ -264,22 +269,34 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
         }
     }
     cluster_wait();  // every CTA has started and cleared its histogram
-    pass1_totals(g, sm, leader, rank, C, pos, bad, need_hist ? 21 : -1, true, warp, lane, tid);
+    pass1_totals(g, sm, leader, rank, C, pos, bad, kmax, need_hist ? 21 : -1, true, !kfirst, warp, lane, tid);
     cluster_sync();  // the leader's segment table, every CTA's parts and histogram, are complete
 
     // ---- a3 (first half, every CTA): top-k-first candidates.  Every CTA derives the
     // same lower bound L0 <= t_k from its copy of the histogram and sends its elements
     // >= L0 to its region of the leader's list.
-    bool fits = false;
+    int list_mode = -1;  // 0: regions fit, 1: contiguous, -1: no list (too many / not top-k-first)
     uint32_t L0 = 1u;
+    Totals tot;
     if (kfirst) {
-        L0 = max(1u, need_hist ? hist_bound(sm, ns, k, 21, warp, lane, tid) : 0u);
-        collect_own<VEC>(row, g, sm, leader, rank, C, CAP / C, L0, keyf, false, warp, lane, tid);
-        cluster_sync();  // every region and count is in
-        fits = regions_fit(sm, C, CAP / C);
+        const uint32_t mk = warp_max_u(lane < C ? sm.part()[lane].u[2] : 0u);
+        L0 = max(1u, need_hist ? hist_bound(sm, ns, k, 21, mk, warp, lane) : 0u);
+        collect_own<VEC>(row, g, sm, leader, rank, C, rank * (CAP / C), CAP / C, L0, keyf, false, true, warp, lane,
+                         tid);
+        if (leader) {  // the row's totals while the other CTAs finish their candidates
+            cluster_arrive();
+            tot = cluster_totals(sm, C);
+            cluster_wait();
+        } else {
+            cluster_sync();
+        }
+        // every region and count is in
+        list_mode = settle_list<VEC>(row, g, sm, leader, rank, C, L0, keyf, false, warp, lane, tid);
+    } else if (leader) {
+        tot = cluster_totals(sm, C);
     }
     if (!leader) {
-        if (!fits) sample_peer<VEC>(row, g, sm, rank, C, warp, lane, tid);
+        if (list_mode < 0) sample_peer<VEC>(row, g, sm, rank, C, warp, lane, tid);
         return;
     }
 
@@ -293,7 +310,6 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
     f.t32 = 0.f;
     const bool any_filter = f.k_on || f.p_on || f.m_on;
 
-    const Totals tot = cluster_totals(sm, C);
     const int npos = tot.npos;
     const bool any_bad = tot.any_bad;
     const float M = tot.M;   // sum of the per-CTA ordered sums
@@ -305,9 +321,9 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
         f.t32 = __double2float_ru(double(mp) * double(rowmax));
         if (!(rowmax >= f.t32)) valid = false;  // S is empty: f(max) = 0
     }
-    if (!fits) __syncthreads();
+    if (list_mode < 0) __syncthreads();
 
-    bool peers = !fits;  // the other CTAs still wait for commands
+    bool peers = list_mode < 0;  // the other CTAs still wait for commands
     auto dismiss = [&]() {
         if (peers) {
             Ctl c{};
@@ -328,10 +344,10 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
         f.pthr = tp * M;
 
         // ---- a3 (second half, leader): t_k and F_k
-        if (kfirst && fits && regions_total(sm, C) <= SMALL) {
+        if (kfirst && list_mode >= 0 && regions_total(sm, C) <= SMALL) {
             // The usual case: a short candidate list, finished in warp 0's registers.
             if (warp == 0) {
-                const Small sl = small_gather(sm, C, CAP / C, lane);
+                const Small sl = small_gather(sm, C, CAP / C, list_mode == 1, lane);
                 const uint32_t tk = small_kth(sl, k, keyf);
                 bool kept[SR];
                 float fk = 0.f;
@@ -348,13 +364,9 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
         } else {
         if (kfirst) {
             int n = -1;
-            if (fits) {
+            if (list_mode >= 0) {
                 n = regions_total(sm, C);
-                if (warp == 0) join_regions_warp(sm, C, CAP / C, lane);
-            } else if (regions_total(sm, C) <= CAP) {
-                // A region overflowed: the leader collects the candidates alone.
-                dismiss();
-                n = collect_all<VEC>(row, g, sm, L0, keyf, warp, lane);
+                if (list_mode == 0 && warp == 0) join_regions_warp(sm, C, CAP / C, lane);
             }
             if (n >= 0) {
                 compact = true;

@@ -184,6 +184,21 @@ def test_large_k_bisection_path(ms):
             assert np.array_equal(out[i], exp)
 
 
+def test_candidates_concentrated_in_one_cta(ms):
+    """Most large values inside the first eighth of the row: the CTA that owns it has
+    more top-k candidates than its share of the on-chip list, but the total fits, so
+    every CTA collects again at exact offsets."""
+    Z = workloads.concentrated_logits(2, 151936, 1000, 19000, seed=31)
+    P = np.stack([workloads.detie(workloads.softmax_fp32(z))[0] for z in Z])
+    for k in (100, 400):
+        out, valid = _run(ms, "top_k", P, [k, k])
+        _check_renorm(P, [k, k], out, valid, filters.top_k_renorm)
+        out, valid = _run(ms, "mask", Z, [k, k])
+        for i in range(2):
+            exp, ok = filters.top_k_mask_logits(Z[i], k)
+            assert np.array_equal(out[i], exp)
+
+
 def test_max_vocab_row(ms):
     V = 2097152
     acc = guard_accept(lambda i: [(None, 0.5, None, "joint")])

@@ -301,6 +301,27 @@ def test_determinism_and_offsets(ms):
     assert not np.array_equal(a[0], c[0]) and not np.array_equal(a[0], d[0])
 
 
+def test_candidates_concentrated_in_one_cta(ms):
+    """Most large values inside the first eighth of the row, so that one CTA holds more
+    candidates than its share of the on-chip list (top-k-first prologue, joint
+    compaction): membership of every draw."""
+    import torch
+    Z = workloads.concentrated_logits(2, 151936, 1000, 19000, seed=31)
+    P = np.stack([workloads.detie(workloads.softmax_fp32(z))[0] for z in Z])
+    acc = guard_accept(lambda i: [(100, 0.9, None, "top_k_first"), (400, 0.95, None, "joint")])
+    for i in range(2):
+        assert acc(i, P[i]), "the fixed rows sit too close to a top-p boundary"
+    Pt = _t(P, torch.float32)
+    idx = np.repeat(np.arange(2, dtype=np.int32), 32)
+    for entry, k, p in (("top_k_first", 100, 0.9), ("joint", 400, 0.95)):
+        ks = np.full(64, k, np.int32)
+        ps = np.full(64, p, np.float32)
+        masks, vref = allowed_masks(P[idx], ks, ps, None, entry)
+        for call in range(4):
+            tok, valid, rounds = _call(ms, entry, Pt, ks, ps, None, indices=idx, seed=5, offset=call)
+            _membership(masks, vref, tok, valid)
+
+
 def test_misaligned_rows_and_large_k_first(ms):
     """A base address that is not 16-byte aligned (scalar path) and a top-k-first k
     whose candidates exceed the on-chip list (bisection prologue)."""

@@ -315,3 +315,17 @@ def random_small_rows(n: int, vocab: int, seed: int, zero_prob: float = 0.0) -> 
                 break
         out[i] = row
     return out
+
+
+def concentrated_logits(n: int, vocab: int, n_big: int, span: int, seed: int, shift: float = 8.0) -> np.ndarray:
+    """``n`` tie-free logit rows, z ~ N(0, 1), in which ``n_big`` entries at distinct
+    random positions inside ``[0, span)`` are raised by ``shift``: most of a row's
+    large values then sit in one part of it (a stress case for work split by index
+    ranges)."""
+    out = np.empty((n, vocab), np.float32)
+    for i in range(n):
+        rng = row_rng(seed, i)
+        z = rng.normal(0.0, 1.0, vocab)
+        z[rng.choice(span, size=n_big, replace=False)] += shift
+        out[i] = detie(z.astype(np.float32), positive_only=False)[0]
+    return out
