@@ -208,6 +208,14 @@ __device__ __forceinline__ void add_leader(uint32_t* local_addr, uint32_t n, boo
     }
 }
 
+// Programmatic dependent launch.  grid_dependency_wait() returns once every kernel
+// this grid depends on (the previous kernel of the stream) has completed and its
+// memory operations are visible; it must precede the first global-memory access.
+// allow_dependents() lets the next kernel of the stream be scheduled on SMs this grid
+// leaves free; that kernel still waits for this grid's completion before it reads.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------------ loads
 
 // Elements [base, base+4) that straddle the row end, or of an unaligned row: element
@@ -256,6 +264,22 @@ __device__ __forceinline__ void cp_async4(float* dst, const float* src, int byte
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Ask the memory system to bring elements [e0, e1) of a row into L2 (bulk L2 prefetch,
+// no destination, nothing to wait for), split over the lanes of one warp in pieces of
+// whole 16-byte words.  The row start must be 16-byte aligned and e0 % 4 == 0; the
+// last piece ends at e1 rounded down to a multiple of 4 (a partial word is left to the
+// ordinary loads).  Warp-collective.
+__device__ __forceinline__ void l2_prefetch_range(const float* row, int e0, int e1, int lane) {
+    const int words = max(0, (e1 - e0) >> 2);       // 16-byte words
+    const int per = (words + 31) / 32;
+    const int w0 = min(words, lane * per);
+    const int w1 = min(words, w0 + per);
+    if (w1 > w0) {
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(row + e0 + 4 * w0), "r"(uint32_t(w1 - w0) * 16u)
+                     : "memory");
+    }
+}
 
 // Stage the lane's four elements [base, base+4) of a row into dst[0..4); zeros past V.
 // VEC: the row start is 16-byte aligned and V % 4 == 0, so base < V implies base + 4 <= V.
@@ -446,6 +470,8 @@ __device__ __forceinline__ void pass1(const float* __restrict__ row, Geom g, Sme
                                             : make_float4(fill, fill, fill, fill);
         }
     };
+    if (VEC && warp == 0)  // the CTA's whole share towards L2 at once; the loads below then mostly hit L2
+        l2_prefetch_range(row, g.s0 * (BLK << g.shift), min(g.V, g.s1 * (BLK << g.shift)), lane);
     float4 A[TB], Bv[TB];
     int t = warp;  // the first NW trips are fixed; later ones are taken from the counter
     load_trip(t, A);

@@ -39,13 +39,18 @@ fs_status launch_cluster(void (*kernel)(Args), const Plan& p, int rows, void* st
     cfg.blockDim = dim3(NT, 1, 1);
     cfg.dynamicSmemBytes = p.smem;
     cfg.stream = static_cast<cudaStream_t>(stream);
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = unsigned(p.C);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // Programmatic dependent launch: the grid may be scheduled while the previous
+    // kernel of the stream is still finishing; the kernel waits for that kernel's
+    // completion (griddepcontrol.wait) before it touches global memory.
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, a);
     if (e != cudaSuccess) return cuda_fail(e);
     return FS_OK;

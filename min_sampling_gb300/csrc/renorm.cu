@@ -101,6 +101,8 @@ __global__ void __launch_bounds__(NT, 4) filter_kernel(const FilterArgs a) {
     const Smem sm(a.ns);
     const Geom g(a.V, a.shift, a.ns, a.nsc, rank);
     const int V = a.V, ns = a.ns;
+    grid_dependency_wait();
+    allow_dependents();
     const float* row = a.in + size_t(b) * size_t(V);
     float* orow = a.out + size_t(b) * size_t(V);
 

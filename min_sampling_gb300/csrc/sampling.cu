@@ -237,6 +237,8 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
     const int V = a.V, ns = a.ns;
     const KeyProb keyf;
 
+    grid_dependency_wait();
+    allow_dependents();
     // ---- a1: row map and parameters (every CTA reads them)
     const int r = a.indices ? a.indices[b] : b;
     const bool row_ok = r >= 0 && r < a.batch_in;
