@@ -452,12 +452,14 @@ __device__ __forceinline__ void stream_warp(const float* __restrict__ row, Geom 
 // warp w starts with trip w and then takes the next untaken trip from a shared counter
 // (initialised to NW), so that warps finishing early take more; the next trip's loads
 // are in flight while the current trip is reduced.  For every segment: the maximum order key and (PROB) the
-// mass, into this CTA's table.  Per lane: the positive count and a bad-value flag (NaN
-// or negative for probabilities, NaN for logits).  Touches no other CTA, so it may run
-// before the cluster's first barrier completes.
+// mass, into this CTA's table.  Per lane: the positive count, a bad-value flag (NaN
+// or negative for probabilities, NaN for logits) and the largest key seen.  With
+// `hist_shift` >= 0 every segment maximum is also counted into the CTA's local
+// histogram (lv, cleared beforehand) at bin key >> hist_shift.  Touches no other CTA,
+// so it may run before the cluster's first barrier completes.
 template <bool VEC, bool NC, bool PROB>
-__device__ __forceinline__ void pass1(const float* __restrict__ row, Geom g, Smem sm, int warp, int lane, int& pos,
-                                      bool& bad, uint32_t& kmax) {
+__device__ __forceinline__ void pass1(const float* __restrict__ row, Geom g, Smem sm, int hist_shift, int warp,
+                                      int lane, int& pos, bool& bad, uint32_t& kmax) {
     const int spt = TB >> g.shift;  // segments per trip
     const int ntrip = (g.s1 - g.s0 + spt - 1) / spt;
     const int mask = g.seg_it() - 1;
@@ -524,6 +526,8 @@ __device__ __forceinline__ void pass1(const float* __restrict__ row, Geom g, Sme
             }
             sm.segkey()[sg] = kk;
             if (PROB) sm.mass(0)[sg] = ss;
+            if (hist_shift >= 0)  // this CTA's histogram counts, in lv
+                atomicAdd(reinterpret_cast<uint32_t*>(sm.lv()) + min(uint32_t(HBINS - 1), kk >> hist_shift), 1u);
         }
 #pragma unroll
         for (int j = 0; j < TB; ++j) A[j] = Bv[j];
@@ -545,21 +549,16 @@ __device__ __forceinline__ void st_rank_v4(void* local_addr, uint4 v, uint32_t r
 // After pass 1 and the cluster barrier that follows it, every CTA: with `publish`, its
 // segments' masses into the leader's mass table (for draws over the whole row); its
 // totals into part[rank] of every CTA (f[0] ordered mass of its segments, u[0]
-// positive count, u[1] bad flag, u[2] maximum key); and, if `hist_shift` >= 0, one
-// count per segment maximum into the histogram (key >> hist_shift) of every CTA of the
-// cluster, each of which cleared its own (and its lv, used here for its local counts)
+// positive count, u[1] bad flag, u[2] maximum key); and, if `hist_shift` >= 0, the
+// CTA's counts of its segment maxima (key >> hist_shift, made by pass 1 in lv) into the
+// histogram of every CTA of the cluster, each of which cleared its own (and its lv)
 // before that barrier.  The CTA's first segment is a multiple of 4, so the table moves
 // in 16-byte words.  Block-collective.
 __device__ __forceinline__ void pass1_totals(Geom g, Smem sm, bool leader, int rank, int C, int pos, bool bad,
                                              uint32_t kmax, int hist_shift, bool prob, bool publish, int warp,
                                              int lane, int tid) {
-    __syncthreads();  // the table written by pass 1
-    uint32_t* loc = reinterpret_cast<uint32_t*>(sm.lv());
-    if (hist_shift >= 0) {  // this CTA's counts in lv (cleared with the histogram)
-#pragma unroll 1
-        for (int i = g.s0 + tid; i < g.s1; i += NT)
-            atomicAdd(&loc[min(uint32_t(HBINS - 1), sm.segkey()[i] >> hist_shift)], 1u);
-    }
+    __syncthreads();  // the table and the local histogram counts written by pass 1
+    const uint32_t* loc = reinterpret_cast<const uint32_t*>(sm.lv());
     if (publish && !leader) {
 #pragma unroll 1
         for (int i = g.s0 + 4 * tid; i < g.s1; i += 4 * NT) {
@@ -933,8 +932,8 @@ __device__ __forceinline__ uint32_t kth_key_warp(Smem sm, int n, int k, KEYF key
     return t;
 }
 
-// A candidate list of at most SMALL entries held by one warp in registers: entry
-// e = 32 r + lane in slot r (x[r], i[r]); in[r] marks entries below n.
+// A candidate list of at most SMALL entries held by one warp in registers, lane-major:
+// entry e = SR * lane + r in slot r (x[r], i[r]); in[r] marks entries below n.
 constexpr int SR = 4;              // slots per lane
 constexpr int SMALL = 32 * SR;
 struct Small {
@@ -965,7 +964,7 @@ __device__ __forceinline__ Small small_gather(Smem sm, int C, int rc, bool exact
         const int m = __shfl_sync(FULL, cnt, c);
 #pragma unroll
         for (int r = 0; r < SR; ++r) {
-            if (m > 0 && o <= 32 * r + lane) {
+            if (m > 0 && o <= SR * lane + r) {
                 rr[r] = c;
                 oo[r] = o;
             }
@@ -973,7 +972,7 @@ __device__ __forceinline__ Small small_gather(Smem sm, int C, int rc, bool exact
     }
 #pragma unroll
     for (int r = 0; r < SR; ++r) {
-        const int e = 32 * r + lane;
+        const int e = SR * lane + r;
         s.in[r] = e < s.n;
         const int a = exact ? e : rr[r] * rc + (e - oo[r]);
         s.x[r] = s.in[r] ? sm.lv()[a] : 0.f;
@@ -996,11 +995,11 @@ __device__ __forceinline__ uint32_t small_kth(const Small& s, int k, KEYF keyf) 
         key[r] = s.in[r] ? keyf(s.x[r]) : 0u;
         ge[r] = 0;
     }
+    const int lanes = (s.n + SR - 1) / SR;  // lanes holding entries
+#pragma unroll 1
+    for (int l = 0; l < lanes; ++l) {
 #pragma unroll
-    for (int r2 = 0; r2 < SR; ++r2) {
-        if (32 * r2 >= s.n) break;
-#pragma unroll 4
-        for (int l = 0; l < 32; ++l) {
+        for (int r2 = 0; r2 < SR; ++r2) {
             const uint32_t a = __shfl_sync(FULL, key[r2], l);
 #pragma unroll
             for (int r = 0; r < SR; ++r) ge[r] += int(a >= key[r]);

@@ -123,7 +123,8 @@ __global__ void __launch_bounds__(NT, 4) filter_kernel(const FilterArgs a) {
     int pos = 0;
     bool bad = false;
     uint32_t kmax = 0;
-    pass1<VEC, false, IS_PROB>(row, g, sm, warp, lane, pos, bad, kmax);
+    pass1<VEC, false, IS_PROB>(row, g, sm, need_hist ? (IS_PROB ? 21 : 22) : -1, warp, lane, pos, bad,
+                               kmax);
     cluster_wait();  // every CTA has started and cleared its histogram
     pass1_totals(g, sm, leader, rank, C, pos, bad, kmax, need_hist ? (IS_PROB ? 21 : 22) : -1, IS_PROB, false, warp,
                  lane, tid);

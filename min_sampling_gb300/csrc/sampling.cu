@@ -170,44 +170,55 @@ __device__ __forceinline__ int small_rounds(const Small& s, const bool* kept, co
 #pragma unroll 1
     for (int round = 0; round < R_MAX; ++round) {
         const float target = sampler_uniform(seed, offset, b, uint32_t(round)) * S_low;
-        // Inverse transform over the list in index order: slot by slot, a lane scan each.
-        int e = -1, last = -1;
-        float run = 0.f;
+        // Inverse transform over the list in index order (lane-major): the lane whose
+        // running sum passes the target, then the slot inside it.
+        float w[SR], lsum = 0.f;
 #pragma unroll
         for (int r = 0; r < SR; ++r) {
-            const float w = kept[r] && s.x[r] > low ? s.x[r] : 0.f;
-            const float c = run + warp_incl_scan(w, lane);
-            const unsigned hit = __ballot_sync(FULL, w > 0.f && c > target);
-            const unsigned el = __ballot_sync(FULL, w > 0.f);
-            if (e < 0 && hit) e = 32 * r + __ffs(hit) - 1;
-            if (el) last = 32 * r + 31 - __clz(el);
-            run = __shfl_sync(FULL, c, 31);
+            w[r] = kept[r] && s.x[r] > low ? s.x[r] : 0.f;
+            lsum += w[r];
         }
-        if (e < 0) e = last;  // the running sum never passed the target
-        if (e < 0) break;
-        float pivot1 = 0.f;
-        int j = 0;
+        const float incl = warp_incl_scan(lsum, lane);
+        const unsigned hit = __ballot_sync(FULL, lsum > 0.f && incl > target);
+        const unsigned elig = __ballot_sync(FULL, lsum > 0.f);
+        if (!elig) break;
+        // In the chosen lane: the first eligible slot whose running sum passes the
+        // target, else its last eligible slot (also when no lane passed it).
+        const int l = hit ? __ffs(hit) - 1 : 31 - __clz(elig);
+        int pick = -1, last = 0;
+        float run = incl - lsum;
 #pragma unroll
         for (int r = 0; r < SR; ++r) {
-            const float xv = __shfl_sync(FULL, s.x[r], e & 31);
-            const int iv = __shfl_sync(FULL, s.i[r], e & 31);
-            if ((e >> 5) == r) {
-                pivot1 = xv;
-                j = iv;
+            if (w[r] > 0.f) {
+                run += w[r];
+                last = r;
+                if (pick < 0 && run > target) pick = r;
             }
         }
+        if (pick < 0 || !hit) pick = last;
+        pick = __shfl_sync(FULL, pick, l);
+        float xv = 0.f;
+        int iv = 0;
+#pragma unroll
+        for (int r = 0; r < SR; ++r) {
+            xv = r == pick ? s.x[r] : xv;
+            iv = r == pick ? s.i[r] : iv;
+        }
+        const float pivot1 = __shfl_sync(FULL, xv, l);
+        const int j = __shfl_sync(FULL, iv, l);
         const float pivot2 = (pivot1 + high) * 0.5f;
         float m1 = 0.f, m2 = 0.f;
-        int C1 = 0, C2 = 0;
+        int c1 = 0, c2 = 0;
 #pragma unroll
         for (int r = 0; r < SR; ++r) {
             const bool a1 = kept[r] && s.x[r] > pivot1, a2 = kept[r] && s.x[r] > pivot2;
             m1 += a1 ? s.x[r] : 0.f;
             m2 += a2 ? s.x[r] : 0.f;
-            C1 += __popc(__ballot_sync(FULL, a1));
-            C2 += __popc(__ballot_sync(FULL, a2));
+            c1 += a1;
+            c2 += a2;
         }
         const float M1 = warp_sum(m1), M2 = warp_sum(m2);
+        const int C1 = warp_sum_i(c1), C2 = warp_sum_i(c2);
         if (f(C1, M1, pivot1)) {
             rounds = round + 1;
             return j;
@@ -263,7 +274,7 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
     bool bad = false;
     uint32_t kmax = 0;
     if (row_ok) {
-        pass1<VEC, true, true>(row, g, sm, warp, lane, pos, bad, kmax);
+        pass1<VEC, true, true>(row, g, sm, need_hist ? 21 : -1, warp, lane, pos, bad, kmax);
     } else {
         for (int i = g.s0 + tid; i < g.s1; i += NT) {
             sm.segkey()[i] = 0u;
