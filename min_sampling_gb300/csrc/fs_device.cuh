@@ -38,6 +38,8 @@ constexpr int SBH = 2;                  // blocks per half of a warp's staging b
 constexpr int HBINS = 1024;             // histogram bins of the top-k bound
 constexpr int R_MAX = 256;              // rejection rounds before a row is invalid
 constexpr int MAX_CLUSTER = 8;
+constexpr int REDW = 128;               // words of block-reduction scratch
+constexpr uint64_t NO_LIMIT = uint64_t(1) << 32;  // an upper key bound that excludes nothing
 constexpr unsigned FULL = 0xffffffffu;
 
 // Commands from the leader to the other CTAs of the cluster.
@@ -50,7 +52,7 @@ __device__ __forceinline__ unsigned long long pack_jx(int j, float x) {
 __device__ __forceinline__ int unpack_j(unsigned long long p) { return static_cast<int>(p >> 32); }
 __device__ __forceinline__ float unpack_x(unsigned long long p) { return __uint_as_float(static_cast<uint32_t>(p)); }
 
-enum : int { CMD_EXIT = 0, CMD_PIVOT2 = 1, CMD_BISECT = 2, CMD_MASSGE = 3, CMD_WRITE = 4, CMD_COLLECT = 5 };
+enum : int { CMD_EXIT = 0, CMD_PIVOT2 = 1, CMD_SEARCH = 2, CMD_WRITE = 4, CMD_COLLECT = 5 };
 
 // ------------------------------------------------------------------ geometry
 
@@ -88,7 +90,7 @@ struct Layout {
     static constexpr size_t CTL = 0;
     static constexpr size_t PART = align16(CTL + sizeof(Ctl));
     static constexpr size_t RED = align16(PART + MAX_CLUSTER * sizeof(Part));
-    static constexpr size_t MISC = align16(RED + 64 * sizeof(int));
+    static constexpr size_t MISC = align16(RED + REDW * sizeof(int));
     static constexpr size_t ARR = align16(MISC + 32 * sizeof(int));
     size_t nsp;   // words per per-segment array (ns + 1, rounded up to 4)
     __host__ __device__ explicit Layout(int ns) : nsp((size_t(ns) + 4) & ~size_t(3)) {}
@@ -110,7 +112,7 @@ struct Smem {
     __device__ __forceinline__ T* at(size_t off) const { return reinterpret_cast<T*>(smem_raw + off); }
     __device__ __forceinline__ Ctl* ctl() const { return at<Ctl>(Layout::CTL); }            // current command
     __device__ __forceinline__ Part* part() const { return at<Part>(Layout::PART); }        // [MAX_CLUSTER]
-    __device__ __forceinline__ int* red() const { return at<int>(Layout::RED); }            // [64] scratch
+    __device__ __forceinline__ int* red() const { return at<int>(Layout::RED); }            // [REDW] scratch
     __device__ __forceinline__ float* cmass() const { return at<float>(Layout::MISC); }     // [MAX_CLUSTER]
     __device__ __forceinline__ int* ctr() const { return at<int>(Layout::MISC + 64); }      // pass-1 trip counter
     __device__ __forceinline__ int* bcast() const { return at<int>(Layout::MISC + 80); }    // [4] CTA broadcast
@@ -397,52 +399,46 @@ __device__ __forceinline__ float sampler_uniform(unsigned long long seed, unsign
     return float(philox4x32_10(ctr, key).x >> 8) * 0x1p-24f;
 }
 
-// This warp's contiguous share of the CTA's segments, streamed from global memory (in
-// practice L2, after pass 1) through the warp's staging buffer, two chunks of SBH
-// blocks in flight.  Blocks of segments with live(sg) false are not read.  Then, in
-// block order, body(sg, it, on, v, base): `it` the block's index inside segment sg,
-// `on` = live(sg), v the lane's four values (zeros when not on or past V), base the
-// index of v.x.  Each lane reads back only what it copied itself, so no warp barrier is
-// needed between the copies and their use.
-template <bool VEC, typename LIVE, typename BODY>
-__device__ __forceinline__ void stream_warp(const float* __restrict__ row, Geom g, Smem sm, int warp,
-                                            int lane, LIVE live, BODY body) {
+// This warp's contiguous share of the CTA's segments, read again from global memory
+// (in practice L2, after pass 1) in chunks of TB blocks held in registers, the next
+// chunk's loads in flight while the current one is processed.  Blocks of segments
+// with live(sg) false are not read.  Then, in block order, body(sg, it, on, v, base):
+// `it` the block's index inside segment sg, `on` = live(sg), v the lane's four values
+// (zeros when not on or past V), base the index of v.x.  NC: read-only loads (the row
+// is not written during the kernel).
+template <bool VEC, bool NC, typename LIVE, typename BODY>
+__device__ __forceinline__ void stream_warp(const float* __restrict__ row, Geom g, Smem sm, int warp, int lane,
+                                            LIVE live, BODY body) {
     int r0, r1;
     warp_range(g.s1 - g.s0, warp, r0, r1);
     r0 += g.s0;
     r1 += g.s0;
     const int nblk = (r1 - r0) << g.shift;
     const int mask = g.seg_it() - 1;
-    float* st = sm.stage() + warp * (2 * SBH * BLK) + lane * 4;
-    const int nch = (nblk + SBH - 1) / SBH;
-    auto issue = [&](int c) {
-        float* dst = st + (c & 1) * (SBH * BLK);
-#pragma unroll 1
-        for (int j = 0; j < SBH && c * SBH + j < nblk; ++j) {
-            const int blk = c * SBH + j;
+    auto load_chunk = [&](int b0, float4* v) {
+#pragma unroll
+        for (int j = 0; j < TB; ++j) {
+            const int blk = b0 + j;
             const int sg = r0 + (blk >> g.shift);
-            if (live(sg)) stage4<VEC>(dst + j * BLK, row, g.V, g.base(sg, blk & mask, lane));
+            v[j] = (blk < nblk && live(sg)) ? load4<VEC, NC>(row, g.V, g.base(sg, blk & mask, lane), 0.f)
+                                            : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        cp_async_commit();
     };
-    if (nch > 0) issue(0);
+    float4 A[TB], Bv[TB];
+    load_chunk(0, A);
 #pragma unroll 1
-    for (int c = 0; c < nch; ++c) {
-        if (c + 1 < nch) {
-            issue(c + 1);
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
+    for (int b0 = 0; b0 < nblk; b0 += TB) {
+        load_chunk(b0 + TB, Bv);
+#pragma unroll
+        for (int j = 0; j < TB; ++j) {
+            const int blk = b0 + j;
+            if (blk < nblk) {
+                const int sg = r0 + (blk >> g.shift);
+                body(sg, blk & mask, live(sg), A[j], g.base(sg, blk & mask, lane));
+            }
         }
-        const float* src = st + (c & 1) * (SBH * BLK);
-#pragma unroll 1
-        for (int j = 0; j < SBH && c * SBH + j < nblk; ++j) {
-            const int blk = c * SBH + j;
-            const int sg = r0 + (blk >> g.shift);
-            const bool on = live(sg);
-            const float4 v = on ? *reinterpret_cast<const float4*>(src + j * BLK) : make_float4(0.f, 0.f, 0.f, 0.f);
-            body(sg, blk & mask, on, v, g.base(sg, blk & mask, lane));
-        }
+#pragma unroll
+        for (int j = 0; j < TB; ++j) A[j] = Bv[j];
     }
 }
 
@@ -636,7 +632,7 @@ __device__ __forceinline__ void pivot_pass(const float* __restrict__ row, Geom g
     const int last = g.seg_it() - 1;
     int c1 = 0, c2 = 0;
     float sa = 0.f, sb = 0.f;
-    stream_warp<VEC>(
+    stream_warp<VEC, true>(
         row, g, sm, warp, lane, [&](int sg) { return sm.segkey()[sg] > kp1; },
         [&](int sg, int it, bool on, const float4& v, int) {
             float a = 0.f, b = 0.f;
@@ -693,7 +689,7 @@ __device__ __forceinline__ void pivot_pass(const float* __restrict__ row, Geom g
 
 // ------------------------------------------------------------------ candidate lists
 
-// Every element with key >= thr of the segments [a, b), in index order:
+// Every element with thr <= key < thr_hi of the segments [a, b), in index order:
 // out(p, value, index) for p = 0, 1, ...  Returns the exact count.  Warp w takes the
 // w-th contiguous share of [a, b), lists its segments whose maximum key is >= thr
 // (into list[], inside its own share), stages their blocks 2*SBH at a time
@@ -702,7 +698,8 @@ __device__ __forceinline__ void pivot_pass(const float* __restrict__ row, Geom g
 // had more than one batch).  Block-collective; red[0..NW) is used.
 template <bool VEC, typename KEYF, typename OUT>
 __device__ __forceinline__ int collect_range(const float* __restrict__ row, Geom g, Smem sm, int a, int b,
-                                             uint32_t thr, KEYF keyf, int warp, int lane, OUT out) {
+                                             uint32_t thr, uint64_t thr_hi, KEYF keyf, int warp, int lane,
+                                             OUT out) {
     constexpr int WB = 2 * SBH;  // blocks per batch
     int r0, r1;
     warp_range(b - a, warp, r0, r1);
@@ -729,7 +726,10 @@ __device__ __forceinline__ int collect_range(const float* __restrict__ row, Geom
         cp_async_commit();
         cp_async_wait<0>();
     };
-    auto keep = [&](int j, int base, int q) { return keyf(st[j * BLK + q]) >= thr && base + q < g.V; };
+    auto keep = [&](int j, int base, int q) {
+        const uint32_t key = keyf(st[j * BLK + q]);
+        return key >= thr && uint64_t(key) < thr_hi && base + q < g.V;
+    };
     int cnt = 0;
 #pragma unroll 1
     for (int c0 = 0; c0 < nblk; c0 += WB) {
@@ -772,16 +772,17 @@ __device__ __forceinline__ int collect_range(const float* __restrict__ row, Geom
     return total;
 }
 
-// Every CTA: collect its own elements with key >= thr, in index order, into entries
+// Every CTA: collect its own elements with thr <= key < thr_hi, in index order, into entries
 // [base, base + cap) of the leader's list, or with `to_all` of every CTA's list; with
 // `bcast`, the exact count goes to part[rank].u[4] of every CTA of the cluster, so that
 // after the next cluster barrier each CTA can tell whether all regions fit and where
 // each rank's candidates start.  Block-collective.
 template <bool VEC, typename KEYF>
 __device__ __forceinline__ void collect_own(const float* __restrict__ row, Geom g, Smem sm, bool leader, int rank,
-                                            int C, int base, int cap, uint32_t thr, KEYF keyf, bool to_all,
-                                            bool bcast, int warp, int lane, int tid) {
-    const int n = collect_range<VEC>(row, g, sm, g.s0, g.s1, thr, keyf, warp, lane, [&](int p, float x, int ix) {
+                                            int C, int base, int cap, uint32_t thr, uint64_t thr_hi, KEYF keyf,
+                                            bool to_all, bool bcast, int warp, int lane, int tid) {
+    const int n = collect_range<VEC>(row, g, sm, g.s0, g.s1, thr, thr_hi, keyf, warp, lane, [&](int p, float x,
+                                                                                                  int ix) {
         if (p < cap) {
             if (to_all) {
 #pragma unroll 1
@@ -855,12 +856,13 @@ __device__ __forceinline__ int exact_base(Smem sm, int rank) {
 // when more than CAP elements qualify.  Block-collective on every CTA.
 template <bool VEC, typename KEYF>
 __device__ __forceinline__ int settle_list(const float* __restrict__ row, Geom g, Smem sm, bool leader, int rank,
-                                           int C, uint32_t thr, KEYF keyf, bool to_all, int warp, int lane,
-                                           int tid) {
+                                           int C, uint32_t thr, uint64_t thr_hi, KEYF keyf, bool to_all, int warp,
+                                           int lane, int tid) {
     if (regions_fit(sm, C, CAP / C)) return 0;
     if (regions_total(sm, C) > CAP) return -1;
     const int base = exact_base(sm, rank);
-    collect_own<VEC>(row, g, sm, leader, rank, C, base, CAP - base, thr, keyf, to_all, false, warp, lane, tid);
+    collect_own<VEC>(row, g, sm, leader, rank, C, base, CAP - base, thr, thr_hi, keyf, to_all, false, warp, lane,
+                     tid);
     cluster_sync();
     return 1;
 }
@@ -1245,287 +1247,231 @@ __device__ __forceinline__ void send_command(Smem sm, const Ctl& c, int C, int t
     cluster_sync();
 }
 
-// A three-pivot bisection pass ([drill] sections 3-5) over this CTA's segments whose
-// maximum key is >= lo: count and (MASS) mass of keys >= each pivot, and per
-// sub-interval [lo,p0) [p0,p1) [p1,p2) [p2,hi) the smallest and largest key present.
-// The CTA's record goes to the leader's part[rank]: f[0..2] masses, u[0..2] counts,
-// u[3..6] min keys, u[7..10] max keys.  Block-collective.
-template <bool VEC, bool MASS, typename KEYF>
-FS_COLD __device__ void bisect_pass(const float* __restrict__ row, Geom g, Smem sm, bool leader,
-                                        int rank, uint64_t lo, uint64_t hi, uint32_t p0, uint32_t p1, uint32_t p2,
-                                        KEYF keyf, int warp, int lane, int tid) {
-    float m[3] = {0.f, 0.f, 0.f};
-    int c[3] = {0, 0, 0};
-    uint32_t mn[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
-    uint32_t mx[4] = {0u, 0u, 0u, 0u};
-    stream_warp<VEC>(
-        row, g, sm, warp, lane, [&](int sg) { return uint64_t(sm.segkey()[sg]) >= lo; },
-        [&](int, int, bool on, const float4& v, int base) {
-            if (!on) return;
-#pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
-                const float xv = q_at(v, q);
-                const uint32_t key = keyf(xv);
-                const bool inr = base + q < g.V;
-                const bool g0 = inr && key >= p0, g1 = inr && key >= p1, g2 = inr && key >= p2;
-                if (MASS) {
-                    m[0] += g0 ? xv : 0.f;
-                    m[1] += g1 ? xv : 0.f;
-                    m[2] += g2 ? xv : 0.f;
-                }
-                c[0] += g0;
-                c[1] += g1;
-                c[2] += g2;
-                const bool inlo = inr && uint64_t(key) >= lo && uint64_t(key) < hi;
-                const int bkt = int(g0) + int(g1) + int(g2);
+// ------------------------------------------------------------------ threshold search
+
+// Search for the threshold of a filter over the integer order keys ([drill] sections
+// 2-4: a count or a mass that is monotone in the threshold, searched on the fp32 bit
+// pattern so that it ends exactly on a value of the row): the largest t with
+// crit(t) = count(key >= t) >= k, or mass(key >= t) >= target.  Invariant: crit(lo)
+// holds, crit(hi) does not; the counts and masses of keys >= hi are known.  Each pass
+// splits [lo, hi) at NP pivots and measures, for every pivot, the count and mass of the
+// keys in [pivot, hi).  Once at most CAP keys lie in [lo, hi) they are gathered on chip
+// and the search ends there.
+constexpr int NP = 7;
+constexpr int INT_BIG = 0x7fffffff;
+
+struct Search {
+    uint64_t lo, hi;
+    float mass_lo;   // mass(key >= lo)
+    float mass_hi;   // mass(key >= hi)
+    int cnt_hi;      // count(key >= hi)
+    int cnt_in;      // count(lo <= key < hi), INT_BIG if not known
+};
+
+// Pivot i (0 <= i < NP) of [lo, hi): evenly spread; when the interval is short, lo + 1,
+// lo + 2, ... (those reaching hi are inert: nothing in [lo, hi) is >= hi).
+__device__ __forceinline__ uint64_t search_pivot(uint64_t lo, uint64_t hi, int i) {
+    const uint64_t d = hi - lo;
+    return d > uint64_t(NP) ? lo + (d * uint64_t(i + 1)) / uint64_t(NP + 1) : min(lo + uint64_t(i + 1), hi);
+}
+
+// Per-thread accumulation of one element into the NP pivot sums (mass when MASS;
+// counts always).
+// Keys, bounds and pivots are 32-bit here: hi <= maxkey + 1 and a valid row's largest
+// key is below 0xffffffff (that pattern is a NaN), so min(hi, 0xffffffff) loses nothing.
+template <bool MASS>
+__device__ __forceinline__ void search_add(uint32_t key, float x, uint32_t lo, uint32_t hi, const uint32_t* piv,
+                                           float* m, int* c) {
+    if (key < lo || key >= hi) return;
 #pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const bool sel = inlo && t == bkt;
-                    mn[t] = sel ? min(mn[t], key) : mn[t];
-                    mx[t] = sel ? max(mx[t], key) : mx[t];
-                }
-            }
-        });
-    // warp -> block (fixed order) -> the leader's part[rank]
+    for (int i = 0; i < NP; ++i) {
+        const bool ge = key >= piv[i];
+        if (MASS) m[i] += ge ? x : 0.f;
+        c[i] += ge;
+    }
+}
+__device__ __forceinline__ uint32_t clamp32(uint64_t v) { return uint32_t(min(v, uint64_t(0xffffffffu))); }
+
+// Block: the NP sums of every thread, reduced in a fixed order, into the 2 * NP words
+// of dst (masses as float bits, then counts), written by thread 0 through `put`.
+template <typename PUT>
+__device__ __forceinline__ void search_reduce(Smem sm, float* m, int* c, int warp, int lane, int tid, PUT put) {
     float* rf = reinterpret_cast<float*>(sm.red());
-    uint32_t* ru = reinterpret_cast<uint32_t*>(sm.red());
 #pragma unroll
-    for (int i = 0; i < 3; ++i) {
+    for (int i = 0; i < NP; ++i) {
         m[i] = warp_sum(m[i]);
         c[i] = warp_sum_i(c[i]);
     }
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-        mn[t] = warp_min_u(mn[t]);
-        mx[t] = warp_max_u(mx[t]);
-    }
     if (lane == 0) {
 #pragma unroll
-        for (int i = 0; i < 3; ++i) {
+        for (int i = 0; i < NP; ++i) {
             rf[i * NW + warp] = m[i];
-            ru[(3 + i) * NW + warp] = uint32_t(c[i]);
+            sm.red()[(NP + i) * NW + warp] = c[i];
         }
     }
     __syncthreads();
-    uint32_t rec[6];
-    if (tid == 0) {
-#pragma unroll
-        for (int i = 0; i < 3; ++i) {
+    if (tid < 2 * NP) {
+        uint32_t v;
+        if (tid < NP) {
             float a = 0.f;
-            uint32_t b = 0;
-#pragma unroll 1
-            for (int w = 0; w < NW; ++w) {
-                a += rf[i * NW + w];
-                b += ru[(3 + i) * NW + w];
-            }
-            rec[i] = __float_as_uint(a);
-            rec[3 + i] = b;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) a += rf[tid * NW + w];
+            v = __float_as_uint(a);
+        } else {
+            int a = 0;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) a += sm.red()[tid * NW + w];
+            v = uint32_t(a);
         }
+        put(tid, v);
     }
     __syncthreads();
-    if (lane == 0) {
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            ru[t * NW + warp] = mn[t];
-            ru[(4 + t) * NW + warp] = mx[t];
-        }
-    }
-    __syncthreads();
-    if (tid == 0) {
-        uint32_t* dst = reinterpret_cast<uint32_t*>(&sm.part()[rank]);
-#pragma unroll 1
-        for (int t = 0; t < 4; ++t) {
-            uint32_t a = 0xffffffffu, b = 0u;
-#pragma unroll 1
-            for (int w = 0; w < NW; ++w) {
-                a = min(a, ru[t * NW + w]);
-                b = max(b, ru[(4 + t) * NW + w]);
-            }
-            put_leader(dst + 4 + 3 + t, a, leader);   // u[3 + t]
-            put_leader(dst + 4 + 7 + t, b, leader);   // u[7 + t]
-        }
-#pragma unroll
-        for (int i = 0; i < 3; ++i) {
-            put_leader(dst + i, rec[i], leader);          // f[i]
-            put_leader(dst + 4 + i, rec[3 + i], leader);  // u[i]
-        }
-    }
 }
+static_assert(2 * NP * NW <= REDW, "search sums fit the reduction scratch");
 
-// Count and mass (x > 0) of key >= t over this CTA's segments; the record goes to the
-// leader's part[rank] (f[0] mass, u[0] count).  Block-collective.
-template <bool VEC, typename KEYF>
-FS_COLD __device__ void massge_pass(const float* __restrict__ row, Geom g, Smem sm, bool leader,
-                                        int rank, uint32_t t, KEYF keyf, int warp, int lane, int tid) {
-    float ms = 0.f;
-    int cnt = 0;
-    stream_warp<VEC>(
-        row, g, sm, warp, lane, [&](int sg) { return sm.segkey()[sg] >= t; },
+// One pass of the search over this CTA's segments whose maximum key is >= lo; the
+// record (words 0..NP-1 masses (when MASS), NP..2NP-1 counts) goes to the leader's
+// part[rank].  Block-collective.
+template <bool VEC, bool NC, bool MASS, typename KEYF>
+__device__ __forceinline__ void search_pass(const float* __restrict__ row, Geom g, Smem sm, bool leader, int rank,
+                                            uint64_t lo, uint64_t hi, KEYF keyf, int warp, int lane, int tid) {
+    uint32_t piv[NP];
+#pragma unroll
+    for (int i = 0; i < NP; ++i) piv[i] = clamp32(search_pivot(lo, hi, i));
+    const uint32_t lo32 = uint32_t(lo), hi32 = clamp32(hi);
+    float m[NP];
+    int c[NP];
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {
+        m[i] = 0.f;
+        c[i] = 0;
+    }
+    stream_warp<VEC, NC>(
+        row, g, sm, warp, lane, [&](int sg) { return sm.segkey()[sg] >= lo32; },
         [&](int, int, bool on, const float4& v, int base) {
             if (!on) return;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const float xv = q_at(v, q);
-                const bool gq = keyf(xv) >= t && xv > 0.f && base + q < g.V;
-                ms += gq ? xv : 0.f;
-                cnt += gq;
+                if (base + q < g.V) search_add<MASS>(keyf(q_at(v, q)), q_at(v, q), lo32, hi32, piv, m, c);
             }
         });
-    ms = warp_sum(ms);
-    cnt = warp_sum_i(cnt);
-    float* rf = reinterpret_cast<float*>(sm.red());
-    if (lane == 0) {
-        rf[warp] = ms;
-        sm.red()[NW + warp] = cnt;
-    }
-    __syncthreads();
-    if (tid == 0) {
-        float a = 0.f;
-        int n = 0;
-#pragma unroll 1
-        for (int w = 0; w < NW; ++w) {
-            a += rf[w];
-            n += sm.red()[NW + w];
-        }
-        uint32_t* dst = reinterpret_cast<uint32_t*>(&sm.part()[rank]);
-        put_leader(dst, __float_as_uint(a), leader);
-        put_leader(dst + 4, uint32_t(n), leader);
-    }
-    __syncthreads();
+    uint32_t* dst = reinterpret_cast<uint32_t*>(&sm.part()[rank]);
+    search_reduce(sm, m, c, warp, lane, tid, [&](int w, uint32_t v) { put_leader(dst + w, v, leader); });
 }
 
-// Interval of a threshold search over order keys ([drill] sections 2-3: bisection on a
-// monotone count or mass, done on the integer bit pattern so that it ends exactly on
-// an existing value).  Invariant: crit(lo) holds and crit(hi) does not, where
-// crit(t) = count(key >= t) >= k  or  mass(key >= t) >= target.  Done when
-// hi = lo + 1; then lo is the threshold.
-struct Bisect {
-    uint64_t lo, hi;
-    float mass_lo;     // mass(key >= lo) (probabilities)
-};
-
-// Pivots of the next pass: three points splitting [lo, hi) into quarters (fewer when
-// the interval is short; unused pivots equal hi).
-__device__ __forceinline__ void bisect_pivots(const Bisect& st, uint32_t* piv) {
-    const uint64_t d = st.hi - st.lo;
-    if (d >= 4) {
-#pragma unroll
-        for (int i = 0; i < 3; ++i) piv[i] = uint32_t(st.lo + (d * uint64_t(i + 1)) / 4);
-    } else {
-        piv[0] = uint32_t(st.lo + 1);
-        piv[1] = uint32_t(d == 3 ? st.lo + 2 : st.hi);
-        piv[2] = uint32_t(st.hi);
-    }
-}
-
-// Fold the C parts of a bisection pass into the interval ([drill] section 5: take the
-// largest pivot where the criterion holds; shrink to the keys present).
-template <bool MASS>
-__device__ __forceinline__ void bisect_update(Smem sm, int C, Bisect& st, const uint32_t* piv, int kcrit,
-                                              float target) {
-    float mass[3] = {0.f, 0.f, 0.f};
-    int cnt[3] = {0, 0, 0};
-    uint32_t kmin[4], kmax[4];
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-        kmin[t] = 0xffffffffu;
-        kmax[t] = 0u;
-    }
-    for (int c = 0; c < C; ++c) {
-        const Part& p = sm.part()[c];
-#pragma unroll
-        for (int i = 0; i < 3; ++i) {
-            mass[i] += p.f[i];
-            cnt[i] += int(p.u[i]);
-        }
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            kmin[t] = min(kmin[t], p.u[3 + t]);
-            kmax[t] = max(kmax[t], p.u[7 + t]);
-        }
-    }
+// Fold the sums of a pass (masses M[i], counts N[i] of keys in [pivot i, hi)) into
+// the search state; the criterion is on the mass (CRIT_MASS) or on the count.
+template <bool CRIT_MASS>
+__device__ __forceinline__ void search_update(Search& st, const float* M, const int* N, int kcrit, float target) {
     int best = -1;
 #pragma unroll
-    for (int i = 0; i < 3; ++i) {
-        if (uint64_t(piv[i]) < st.hi) {
-            const bool ok = MASS ? (mass[i] >= target) : (cnt[i] >= kcrit);
-            if (ok) best = i;
-        }
+    for (int i = 0; i < NP; ++i) {
+        const bool ok = CRIT_MASS ? (st.mass_hi + M[i] >= target) : (st.cnt_hi + N[i] >= kcrit);
+        if (ok) best = i;
     }
-    uint64_t nlo = st.lo, nhi = st.hi;
-    int bkt = 0;
+    const uint64_t lo = st.lo, hi = st.hi;
+    const int nxt = best + 1;  // the pivot that becomes hi (NP: hi stays)
+    int cnt_lo_in = st.cnt_in;  // count of [new lo, old hi)
     if (best >= 0) {
-        nlo = piv[best];
-        st.mass_lo = mass[best];
-        bkt = best + 1;
+        st.lo = search_pivot(lo, hi, best);
+        st.mass_lo = st.mass_hi + M[best];
+        cnt_lo_in = N[best];
     }
-    if (best + 1 < 3 && uint64_t(piv[best + 1]) < st.hi) nhi = piv[best + 1];
-    if (kmin[bkt] <= kmax[bkt]) {  // keys present in the new interval
-        nlo = max(nlo, uint64_t(kmin[bkt]));
-        nhi = min(nhi, uint64_t(kmax[bkt]) + 1);
+    if (nxt < NP) {
+        st.hi = search_pivot(lo, hi, nxt);
+        st.mass_hi += M[nxt];
+        st.cnt_hi += N[nxt];
+        st.cnt_in = cnt_lo_in == INT_BIG ? INT_BIG : cnt_lo_in - N[nxt];
+    } else {
+        st.cnt_in = cnt_lo_in;
     }
-    st.lo = nlo;
-    st.hi = nhi;
 }
 
-// Leader: drive a bisection to the end with the whole cluster (at most 40 passes).
-template <bool VEC, bool MASS, typename KEYF>
-__device__ __forceinline__ void bisect_leader(const float* __restrict__ row, Geom g, Smem sm, int C, Bisect& st,
-                                              int kcrit, float target, KEYF keyf, int warp, int lane, int tid) {
-    for (int iter = 0; iter < 40 && st.hi - st.lo > 1; ++iter) {
-        uint32_t piv[3];
-        bisect_pivots(st, piv);
+// Leader, with the cluster: passes over the row until the interval is exact or holds
+// at most CAP keys (at most 40 passes).  MASS: masses are measured (probabilities);
+// CRIT_MASS: the criterion is on them.  Block-collective on the leader.
+template <bool VEC, bool NC, bool CRIT_MASS, bool MASS, typename KEYF>
+__device__ __forceinline__ void search_row(const float* __restrict__ row, Geom g, Smem sm, int C, Search& st,
+                                           int kcrit, float target, KEYF keyf, int warp, int lane, int tid) {
+#pragma unroll 1
+    for (int iter = 0; iter < 40 && st.hi - st.lo > 1 && st.cnt_in > CAP; ++iter) {
         Ctl c{};
-        c.cmd = CMD_BISECT;
-        c.u[0] = piv[0];
-        c.u[1] = piv[1];
-        c.u[2] = piv[2];
-        c.u[3] = uint32_t(st.lo);
+        c.cmd = CMD_SEARCH;
+        c.flag = MASS ? 1 : 0;
+        c.u[0] = uint32_t(st.lo);
         c.hi_lo = uint32_t(st.hi);
         c.hi_hi = uint32_t(st.hi >> 32);
         send_command(sm, c, C, tid);
-        bisect_pass<VEC, MASS>(row, g, sm, true, 0, st.lo, st.hi, piv[0], piv[1], piv[2], keyf, warp, lane, tid);
+        search_pass<VEC, NC, MASS>(row, g, sm, true, 0, st.lo, st.hi, keyf, warp, lane, tid);
         cluster_sync();  // every part is in
-        bisect_update<MASS>(sm, C, st, piv, kcrit, target);
+        float M[NP];
+        int N[NP];
+#pragma unroll
+        for (int i = 0; i < NP; ++i) {
+            const bool in = lane < C;
+            const uint32_t* w = reinterpret_cast<const uint32_t*>(&sm.part()[in ? lane : 0]);
+            M[i] = warp_sum(in ? __uint_as_float(w[i]) : 0.f);
+            N[i] = warp_sum_i(in ? int(w[NP + i]) : 0);
+        }
+        search_update<CRIT_MASS>(st, M, N, kcrit, target);
+        __syncthreads();  // the parts are read before the next pass writes them
+    }
+}
+
+// The search over a list lv/li[0..n) that holds every key of [lo, hi) (and no other),
+// block-collective, until the interval is exact.
+template <bool CRIT_MASS, bool MASS, typename KEYF>
+__device__ __forceinline__ void search_list(Smem sm, int n, Search& st, int kcrit, float target, KEYF keyf,
+                                            int warp, int lane, int tid) {
+#pragma unroll 1
+    for (int iter = 0; iter < 40 && st.hi - st.lo > 1; ++iter) {
+        uint32_t piv[NP];
+#pragma unroll
+        for (int i = 0; i < NP; ++i) piv[i] = clamp32(search_pivot(st.lo, st.hi, i));
+        const uint32_t lo32 = uint32_t(st.lo), hi32 = clamp32(st.hi);
+        float m[NP];
+        int c[NP];
+#pragma unroll
+        for (int i = 0; i < NP; ++i) {
+            m[i] = 0.f;
+            c[i] = 0;
+        }
+#pragma unroll 1
+        for (int e = tid; e < n; e += NT) search_add<MASS>(keyf(sm.lv()[e]), sm.lv()[e], lo32, hi32, piv, m, c);
+        uint32_t* dst = reinterpret_cast<uint32_t*>(&sm.part()[0]);  // 2 * NP words (free once gathered)
+        search_reduce(sm, m, c, warp, lane, tid, [&](int w, uint32_t v) { dst[w] = v; });
+        float M[NP];
+        int N[NP];
+#pragma unroll
+        for (int i = 0; i < NP; ++i) {
+            M[i] = __uint_as_float(dst[i]);
+            N[i] = int(dst[NP + i]);
+        }
+        search_update<CRIT_MASS>(st, M, N, kcrit, target);
         __syncthreads();
     }
 }
 
-// Leader: mass of the positive elements with key >= t over the whole row, with the
-// cluster.
-template <bool VEC, typename KEYF>
-FS_COLD __device__ float massge_leader(const float* __restrict__ row, Geom g, Smem sm, int C, uint32_t t,
-                                           KEYF keyf, int warp, int lane, int tid) {
-    Ctl c{};
-    c.cmd = CMD_MASSGE;
-    c.u[0] = t;
-    send_command(sm, c, C, tid);
-    massge_pass<VEC>(row, g, sm, true, 0, t, keyf, warp, lane, tid);
-    cluster_sync();
-    float m = 0.f;
-#pragma unroll 1
-    for (int r = 0; r < C; ++r) m += sm.part()[r].f[0];
-    __syncthreads();
-    return m;
-}
-
-// Leader: every element with key >= thr, in index order, into lv/li[0..n), on the
+// Leader: every element with thr <= key < thr_hi, in index order, into lv/li[0..n), on the
 // leader's command.  The whole cluster collects (each CTA its own segments, into its
 // region of the leader's list; again at exact offsets if a region overflowed).
 // Returns n, or -1 when more than CAP elements qualify (the peers then still wait for
 // commands).  With `exit_if_fit` the peers have left whenever n >= 0.
 template <bool VEC, typename KEYF>
 __device__ __forceinline__ int gather_leader(const float* __restrict__ row, Geom g, Smem sm, int C, uint32_t thr,
-                                             KEYF keyf, bool exit_if_fit, int warp, int lane, int tid) {
+                                             uint64_t thr_hi, KEYF keyf, bool exit_if_fit, int warp, int lane,
+                                             int tid) {
     const int rc = CAP / C;
     Ctl c{};
     c.cmd = CMD_COLLECT;
     c.flag = exit_if_fit ? 1 : 0;
     c.u[0] = thr;
+    c.hi_lo = uint32_t(thr_hi);
+    c.hi_hi = uint32_t(thr_hi >> 32);
     send_command(sm, c, C, tid);
-    collect_own<VEC>(row, g, sm, true, 0, C, 0, rc, thr, keyf, false, true, warp, lane, tid);
+    collect_own<VEC>(row, g, sm, true, 0, C, 0, rc, thr, thr_hi, keyf, false, true, warp, lane, tid);
     cluster_sync();  // every region and count is in
-    const int mode = settle_list<VEC>(row, g, sm, true, 0, C, thr, keyf, false, warp, lane, tid);
+    const int mode = settle_list<VEC>(row, g, sm, true, 0, C, thr, thr_hi, keyf, false, warp, lane, tid);
     if (mode < 0) return -1;
     const int n = regions_total(sm, C);
     if (mode == 0) {
@@ -1533,6 +1479,32 @@ __device__ __forceinline__ int gather_leader(const float* __restrict__ row, Geom
         __syncthreads();
     }
     return n;
+}
+
+// Leader: the threshold of a count (k) or mass (target) criterion over the row, from
+// the state `st` (crit(st.lo) holds), with the cluster: passes over the row, then the
+// remaining keys gathered on chip.  Returns with st.hi = st.lo + 1 (st.lo the
+// threshold, st.mass_lo its mass), unless more than 40 passes were needed.
+template <bool VEC, bool NC, bool CRIT_MASS, bool MASS, typename KEYF>
+__device__ __forceinline__ void threshold_search(const float* __restrict__ row, Geom g, Smem sm, int C, Search& st,
+                                                 int kcrit, float target, KEYF keyf, int warp, int lane, int tid) {
+    search_row<VEC, NC, CRIT_MASS, MASS>(row, g, sm, C, st, kcrit, target, keyf, warp, lane, tid);
+    if (st.hi - st.lo <= 1 || st.cnt_in > CAP) return;
+    const int n = gather_leader<VEC>(row, g, sm, C, uint32_t(st.lo), st.hi, keyf, false, warp, lane, tid);
+    if (n < 0) return;
+    search_list<CRIT_MASS, MASS>(sm, n, st, kcrit, target, keyf, warp, lane, tid);
+}
+
+// The starting state of a search over a whole row: [0, maxkey + 1), everything in it.
+__device__ __forceinline__ Search search_start(uint32_t maxkey, float M, int V) {
+    Search st;
+    st.lo = 0;
+    st.hi = uint64_t(maxkey) + 1;
+    st.mass_lo = M;
+    st.mass_hi = 0.f;
+    st.cnt_hi = 0;
+    st.cnt_in = V;
+    return st;
 }
 
 }  // namespace fsd

@@ -45,7 +45,7 @@ __device__ __forceinline__ void write_pass(const float* __restrict__ row, float*
     const KEYF keyf;
     const float fill = IS_PROB ? 0.f : __int_as_float(0xff800000);
     const bool vec_out = VEC && ((reinterpret_cast<uintptr_t>(orow) & 15) == 0);
-    stream_warp<VEC>(
+    stream_warp<VEC, false>(
         row, g, sm, warp, lane, [&](int sg) { return valid && sm.segkey()[sg] >= t; },
         [&](int, int, bool on, const float4& v, int base) {
             float o[4];
@@ -67,17 +67,18 @@ __device__ __forceinline__ void write_pass(const float* __restrict__ row, float*
 // The other CTAs: follow the leader's commands until the write.
 template <bool VEC, int KIND>
 __device__ __forceinline__ void filter_peer(const float* __restrict__ row, float* __restrict__ orow, Geom g,
-                                        Smem sm, int rank, int C, int warp, int lane, int tid) {
+                                            Smem sm, int rank, int C, int warp, int lane, int tid) {
     using KEYF = typename std::conditional<KIND == K_MASK, KeyLogit, KeyProb>::type;
+    constexpr bool IS_PROB = KIND != K_MASK;
     for (;;) {
         cluster_sync();  // the command is published
         const Ctl c = *sm.ctl();
-        if (c.cmd == CMD_BISECT) {
-            const uint64_t hi = uint64_t(c.hi_lo) | (uint64_t(c.hi_hi) << 32);
-            bisect_pass<VEC, KIND == K_TOPP>(row, g, sm, false, rank, c.u[3], hi, c.u[0], c.u[1], c.u[2], KEYF(),
-                                             warp, lane, tid);
-        } else if (c.cmd == CMD_MASSGE) {
-            massge_pass<VEC>(row, g, sm, false, rank, c.u[0], KEYF(), warp, lane, tid);
+        const uint64_t hi = uint64_t(c.hi_lo) | (uint64_t(c.hi_hi) << 32);
+        if (c.cmd == CMD_SEARCH) {
+            search_pass<VEC, false, IS_PROB>(row, g, sm, false, rank, c.u[0], hi, KEYF(), warp, lane, tid);
+        } else if (c.cmd == CMD_COLLECT) {
+            collect_own<VEC>(row, g, sm, false, rank, C, rank * (CAP / C), CAP / C, c.u[0], hi, KEYF(), false, true,
+                             warp, lane, tid);
         } else if (c.cmd == CMD_WRITE) {
             write_pass<VEC, KIND>(row, orow, g, sm, c.flag != 0, c.u[0], c.f[0], warp, lane);
             return;
@@ -85,6 +86,7 @@ __device__ __forceinline__ void filter_peer(const float* __restrict__ row, float
             return;  // CMD_EXIT
         }
         cluster_sync();  // the results are in the leader
+        if (c.cmd == CMD_COLLECT) settle_list<VEC>(row, g, sm, false, rank, C, c.u[0], hi, KEYF(), false, warp, lane, tid);
     }
 }
 
@@ -148,10 +150,10 @@ __global__ void __launch_bounds__(NT, 4) filter_kernel(const FilterArgs a) {
     if (k_on) {
         L0 = need_hist ? hist_bound(sm, ns, k, IS_PROB ? 21 : 22, maxkey, warp, lane) : 0u;
         if (IS_PROB) L0 = max(L0, 1u);
-        collect_own<VEC>(row, g, sm, leader, rank, C, rank * (CAP / C), CAP / C, L0, keyf, true, true, warp, lane,
-                         tid);
+        collect_own<VEC>(row, g, sm, leader, rank, C, rank * (CAP / C), CAP / C, L0, NO_LIMIT, keyf, true, true,
+                         warp, lane, tid);
         cluster_sync();  // every region and count is in every CTA
-        list_mode = settle_list<VEC>(row, g, sm, leader, rank, C, L0, keyf, true, warp, lane, tid);
+        list_mode = settle_list<VEC>(row, g, sm, leader, rank, C, L0, NO_LIMIT, keyf, true, warp, lane, tid);
     }
     if (list_mode >= 0) {
         // Every element >= L0 (hence >= t) is in the list.
@@ -192,35 +194,20 @@ __global__ void __launch_bounds__(NT, 4) filter_kernel(const FilterArgs a) {
     if (valid) {
         if (KIND != K_TOPP) {
             if (k_on) {
-                {
-                    // More than CAP candidates: the threshold by bisection with the cluster.
-                    Bisect st;
-                    // crit(L0) holds when L0 came from the segment maxima; otherwise start
-                    // from 0 (count(key >= 0) = V >= k).
-                    st.lo = (IS_PROB && npos < k) ? 0u : L0;
-                    st.hi = uint64_t(maxkey) + 1;
-                    st.mass_lo = 0.f;
-                    bisect_leader<VEC, false>(row, g, sm, C, st, k, 0.f, keyf, warp, lane, tid);
-                    t = uint32_t(st.lo);
-                    if (IS_PROB) denom = massge_leader<VEC>(row, g, sm, C, t, keyf, warp, lane, tid);
-                }
-            }
-        } else {
-            if (tp >= 1.f) {
-                t = 0;
-                denom = M;
-            } else if (tp <= 0.f) {
-                t = maxkey;
-                denom = massge_leader<VEC>(row, g, sm, C, t, keyf, warp, lane, tid);
-            } else {
-                Bisect st;
-                st.lo = 0;
-                st.hi = uint64_t(maxkey) + 1;
-                st.mass_lo = M;
-                bisect_leader<VEC, true>(row, g, sm, C, st, 0, tp * M, keyf, warp, lane, tid);
+                // More than CAP candidates: the threshold by a search with the cluster.
+                Search st = search_start(maxkey, M, V);
+                threshold_search<VEC, false, false, IS_PROB>(row, g, sm, C, st, k, 0.f, keyf, warp, lane, tid);
                 t = uint32_t(st.lo);
                 denom = st.mass_lo;
             }
+        } else if (tp < 1.f) {
+            // Top-p: the largest t with mass(key >= t) >= top_p * M; top_p <= 0 keeps the
+            // maximum alone (the smallest positive target).
+            Search st = search_start(maxkey, M, V);
+            const float target = tp > 0.f ? tp * M : __uint_as_float(1u);
+            threshold_search<VEC, false, true, true>(row, g, sm, C, st, 0, target, keyf, warp, lane, tid);
+            t = uint32_t(st.lo);
+            denom = st.mass_lo;
         }
     }
 

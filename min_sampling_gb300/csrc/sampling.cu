@@ -67,19 +67,21 @@ __device__ __forceinline__ void sample_peer(const float* __restrict__ row, Geom 
         const Ctl c = *sm.ctl();
         if (c.cmd == CMD_PIVOT2) {
             pivot_pass<VEC>(row, g, sm, false, rank, c.f[0], c.f[1], c.ia, c.ib, warp, lane, tid);
-        } else if (c.cmd == CMD_BISECT) {
+        } else if (c.cmd == CMD_SEARCH) {
             const uint64_t hi = uint64_t(c.hi_lo) | (uint64_t(c.hi_hi) << 32);
-            bisect_pass<VEC, false>(row, g, sm, false, rank, c.u[3], hi, c.u[0], c.u[1], c.u[2], KeyProb(), warp,
-                                    lane, tid);
+            search_pass<VEC, true, false>(row, g, sm, false, rank, c.u[0], hi, KeyProb(), warp, lane, tid);
         } else if (c.cmd == CMD_COLLECT) {
-            collect_own<VEC>(row, g, sm, false, rank, C, rank * (CAP / C), CAP / C, c.u[0], KeyProb(), false, true,
-                             warp, lane, tid);
+            const uint64_t hi = uint64_t(c.hi_lo) | (uint64_t(c.hi_hi) << 32);
+            collect_own<VEC>(row, g, sm, false, rank, C, rank * (CAP / C), CAP / C, c.u[0], hi, KeyProb(), false,
+                             true, warp, lane, tid);
         } else {
             return;  // CMD_EXIT
         }
         cluster_sync();  // the results are in the leader
         if (c.cmd == CMD_COLLECT) {
-            const int mode = settle_list<VEC>(row, g, sm, false, rank, C, c.u[0], KeyProb(), false, warp, lane, tid);
+            const uint64_t hi = uint64_t(c.hi_lo) | (uint64_t(c.hi_hi) << 32);
+            const int mode = settle_list<VEC>(row, g, sm, false, rank, C, c.u[0], hi, KeyProb(), false, warp, lane,
+                                              tid);
             if (c.flag && mode >= 0) return;
         }
     }
@@ -294,8 +296,8 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
     if (kfirst) {
         const uint32_t mk = warp_max_u(lane < C ? sm.part()[lane].u[2] : 0u);
         L0 = max(1u, need_hist ? hist_bound(sm, ns, k, 21, mk, warp, lane) : 0u);
-        collect_own<VEC>(row, g, sm, leader, rank, C, rank * (CAP / C), CAP / C, L0, keyf, false, true, warp, lane,
-                         tid);
+        collect_own<VEC>(row, g, sm, leader, rank, C, rank * (CAP / C), CAP / C, L0, NO_LIMIT, keyf, false, true,
+                         warp, lane, tid);
         if (leader) {  // the row's totals while the other CTAs finish their candidates
             cluster_arrive();
             tot = cluster_totals(sm, C);
@@ -304,7 +306,7 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
             cluster_sync();
         }
         // every region and count is in
-        list_mode = settle_list<VEC>(row, g, sm, leader, rank, C, L0, keyf, false, warp, lane, tid);
+        list_mode = settle_list<VEC>(row, g, sm, leader, rank, C, L0, NO_LIMIT, keyf, false, warp, lane, tid);
     } else if (leader) {
         tot = cluster_totals(sm, C);
     }
@@ -393,13 +395,9 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
                 }
                 low = 0.f;
             } else {
-                // Too many candidates: t_k by bit-pattern bisection with the cluster.
-                Bisect st;
-                st.lo = L0;  // count(key >= L0) >= k (L0 = 1 counts every positive one)
-                st.hi = uint64_t(maxkey) + 1;
-                st.mass_lo = 0.f;
-                if (npos < k) st.lo = 0;  // fewer positives than k: t_k = 0 keeps them all
-                bisect_leader<VEC, false>(row, g, sm, C, st, k, 0.f, keyf, warp, lane, tid);
+                // Too many candidates: t_k by a threshold search with the cluster.
+                Search st = search_start(maxkey, M, V);
+                threshold_search<VEC, true, false, false>(row, g, sm, C, st, k, 0.f, keyf, warp, lane, tid);
                 const uint32_t tk = uint32_t(st.lo);
                 low = tk >= 1u ? __uint_as_float(tk - 1u) : 0.f;  // x > low  <=>  key(x) >= t_k
                 // Per-segment and per-CTA masses above `low` for the draws (both pivots = low).
@@ -429,7 +427,7 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
         for (int round = 0; round < R_MAX; ++round) {
             if (!compact && count_low <= CAP) {
                 // Few tokens left above `low`: gather them; the leader goes on alone.
-                n_list = gather_leader<VEC>(row, g, sm, C, prob_key(low) + 1u, keyf, true, warp, lane, tid);
+                n_list = gather_leader<VEC>(row, g, sm, C, prob_key(low) + 1u, NO_LIMIT, keyf, true, warp, lane, tid);
                 if (n_list >= 0) peers = false;  // they left with the completed list
                 dismiss();
                 if (n_list < 0) break;
