@@ -130,6 +130,34 @@ fs_status fs_top_k_top_p_sampling(const float* probs, int32_t batch_in, int32_t 
                                   int32_t* out_token, uint8_t* out_valid,
                                   int32_t* out_rounds, void* stream);
 
+/* Sampling with caller-owned generator state ([explainer] RNG ownership: per-request
+ * seed / offset, and a device-resident offset so that a captured CUDA graph advances
+ * its own state between replays).  Arguments as fs_top_k_top_p_sampling, except:
+ *   top_k, top_p   nullable here (NULL: that filter is off);
+ *   seeds          [batch_out] uint64, nullable: Philox key of output row b;
+ *   offsets        [batch_out] uint64, nullable: counter offset of output row b;
+ *   offset_dev     one uint64 in device memory, nullable: added to every row's offset
+ *                  (read when the kernel runs, after earlier work on the stream);
+ *   seed, offset   used for rows whose seeds / offsets array is NULL.
+ * Row b draws Philox4x32-10 with key = seed_b and counter = (round, s_b, lo, hi) of
+ * offset_b + *offset_dev, where s_b = b when `seeds` is NULL and 0 otherwise: with
+ * per-request seeds a request's draws do not depend on its position in the batch.
+ * Nothing is advanced by this call; see fs_advance_offset. */
+fs_status fs_top_k_top_p_sampling_rng(const float* probs, int32_t batch_in, int32_t vocab,
+                                      const int32_t* indices, int32_t batch_out,
+                                      const int32_t* top_k, const float* top_p,
+                                      const float* min_p, int32_t order,
+                                      const uint64_t* seeds, const uint64_t* offsets,
+                                      const uint64_t* offset_dev,
+                                      uint64_t seed, uint64_t offset,
+                                      int32_t* out_token, uint8_t* out_valid,
+                                      int32_t* out_rounds, void* stream);
+
+/* *offset_dev += delta on the device, ordered on `stream` (one thread; no status
+ * beyond launch errors).  Placed after the sampling call inside a captured graph it
+ * gives every replay fresh draws.  offset_dev must not be NULL. */
+fs_status fs_advance_offset(uint64_t* offset_dev, uint64_t delta, void* stream);
+
 /* Filter-only: keep x >= t, t = the largest threshold with count(x >= t) >= k, found
  * exactly on the fp32 bit pattern ([drill] sections 2-4); write x / (kept mass), 0
  * elsewhere.  top_k: [batch] int32 (<= 0 or >= vocab: keep all).  out_probs:

@@ -19,7 +19,7 @@ import torch
 __all__ = [
     "FsError", "lib", "LIB_PATH", "ORDER_TOP_K_FIRST", "ORDER_JOINT", "MAX_ROUNDS",
     "sampling_from_probs", "top_k_sampling", "top_p_sampling", "min_p_sampling",
-    "top_k_top_p_sampling", "top_k_renorm_probs", "top_p_renorm_probs",
+    "top_k_top_p_sampling", "top_k_top_p_sampling_rng", "advance_offset", "top_k_renorm_probs", "top_p_renorm_probs",
     "top_k_mask_logits", "philox4x32_10",
 ]
 
@@ -39,6 +39,9 @@ _SIGNATURES = {
     "fs_top_p_sampling": [_P, _I32, _I32, _P, _I32, _P, _U64, _U64, _P, _P, _P, _P],
     "fs_min_p_sampling": [_P, _I32, _I32, _P, _I32, _P, _U64, _U64, _P, _P, _P, _P],
     "fs_top_k_top_p_sampling": [_P, _I32, _I32, _P, _I32, _P, _P, _P, _I32, _U64, _U64, _P, _P, _P, _P],
+    "fs_top_k_top_p_sampling_rng": [_P, _I32, _I32, _P, _I32, _P, _P, _P, _I32, _P, _P, _P, _U64, _U64, _P, _P, _P,
+                                    _P],
+    "fs_advance_offset": [_P, _U64, _P],
     "fs_top_k_renorm_probs": [_P, _I32, _I32, _P, _P, _P, _P],
     "fs_top_p_renorm_probs": [_P, _I32, _I32, _P, _P, _P, _P],
     "fs_top_k_mask_logits": [_P, _I32, _I32, _P, _P, _P, _P],
@@ -187,6 +190,52 @@ def top_k_top_p_sampling(probs, top_k, top_p, min_p=None, order="top_k_first", i
     return _sample("fs_top_k_top_p_sampling", probs, indices, seed, offset,
                    [(top_k, torch.int32, "top_k"), (top_p, torch.float32, "top_p"),
                     (min_p, torch.float32, "min_p")], return_rounds, order=_order(order))
+
+
+def top_k_top_p_sampling_rng(probs, top_k=None, top_p=None, min_p=None, order="joint", indices=None, *,
+                             seeds=None, offsets=None, offset_dev=None, seed: int = 0, offset: int = 0,
+                             return_rounds: bool = False):
+    """Sampling with caller-owned generator state: per-request ``seeds`` / ``offsets``
+    ([batch_out] uint64 tensors) and/or a device-resident ``offset_dev`` (one uint64,
+    advanced with :func:`advance_offset`, e.g. inside a captured CUDA graph)."""
+    probs = _matrix(probs, "probs")
+    b_in, V = probs.shape
+    dev = probs.device
+    if indices is not None:
+        if not (isinstance(indices, torch.Tensor) and indices.dim() == 1 and indices.dtype == torch.int32
+                and indices.device == dev and indices.is_contiguous()):
+            raise ValueError("indices must be a contiguous 1-D int32 tensor on the probs' device")
+        b_out = indices.shape[0]
+    else:
+        b_out = b_in
+
+    def u64(t, n, name):
+        if t is None:
+            return None
+        if not (isinstance(t, torch.Tensor) and t.dtype == torch.uint64 and t.device == dev and t.is_contiguous()
+                and t.numel() == n):
+            raise ValueError(f"{name} must be a contiguous uint64 tensor of {n} elements on the probs' device")
+        return t
+
+    seeds, offsets = u64(seeds, b_out, "seeds"), u64(offsets, b_out, "offsets")
+    offset_dev = u64(offset_dev, 1, "offset_dev")
+    ps = [None if v is None else _rows(v, b_out, dt, dev, n)
+          for v, dt, n in ((top_k, torch.int32, "top_k"), (top_p, torch.float32, "top_p"),
+                           (min_p, torch.float32, "min_p"))]
+    tok, valid, rounds = _outputs(b_out, dev)
+    _check(_lib().fs_top_k_top_p_sampling_rng(
+        _ptr(probs), b_in, V, _ptr(indices), b_out, *[_ptr(t) for t in ps], _order(order), _ptr(seeds),
+        _ptr(offsets), _ptr(offset_dev), int(seed) & (2 ** 64 - 1), int(offset) & (2 ** 64 - 1), _ptr(tok),
+        _ptr(valid), _ptr(rounds) if return_rounds else None, _stream()))
+    return (tok, valid, rounds) if return_rounds else (tok, valid)
+
+
+def advance_offset(offset_dev, delta: int = 1) -> None:
+    """*offset_dev += delta on the current stream."""
+    if not (isinstance(offset_dev, torch.Tensor) and offset_dev.dtype == torch.uint64 and offset_dev.is_cuda
+            and offset_dev.numel() == 1):
+        raise ValueError("offset_dev must be a CUDA uint64 tensor of one element")
+    _check(_lib().fs_advance_offset(_ptr(offset_dev), int(delta) & (2 ** 64 - 1), _stream()))
 
 
 def _filter(fn_name, x, param, dtype, pname, out):

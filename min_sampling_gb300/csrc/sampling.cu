@@ -33,6 +33,9 @@ struct SampleArgs {
     const float* min_p;
     int order;                // 0 top_k_first, 1 joint
     unsigned long long seed, offset;
+    const unsigned long long* seeds;       // per output row, nullable
+    const unsigned long long* offsets;     // per output row, nullable
+    const unsigned long long* offset_dev;  // added to every row's offset, nullable
     int* out_token;
     unsigned char* out_valid;
     int* out_rounds;
@@ -258,6 +261,10 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
     const float* row = a.probs + size_t(row_ok ? r : 0) * size_t(V);
     const int k = a.top_k ? a.top_k[b] : 0;
     const float tp = a.top_p ? a.top_p[b] : 1.f;
+    // The row's generator state ([explainer] RNG ownership).
+    const unsigned long long seed_b = a.seeds ? a.seeds[b] : a.seed;
+    const unsigned long long offset_b = (a.offsets ? a.offsets[b] : a.offset) + (a.offset_dev ? *a.offset_dev : 0ull);
+    const uint32_t stream_b = a.seeds ? 0u : uint32_t(b);
     const float mp = a.min_p ? a.min_p[b] : 0.f;
     const bool k_on = k > 0 && k < V;
     const bool kfirst = a.order == 0 && k_on;
@@ -373,7 +380,7 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
                 }
                 const float Fk = warp_sum(fk);
                 f.pthr = tp * Fk;  // top-p inside the k, measured against F_k
-                token = small_rounds(sl, kept, f, Fk, high, a.seed, a.offset, uint32_t(b), lane, rounds);
+                token = small_rounds(sl, kept, f, Fk, high, seed_b, offset_b, stream_b, lane, rounds);
                 accepted = token >= 0;
             }
         } else {
@@ -433,7 +440,7 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
                 if (n_list < 0) break;
                 compact = true;
             }
-            const float u = sampler_uniform(a.seed, a.offset, uint32_t(b), uint32_t(round));
+            const float u = sampler_uniform(seed_b, offset_b, stream_b, uint32_t(round));
             if (compact) {
                 if (warp != 0) break;
                 int j = -1;
@@ -528,7 +535,8 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
 static fs_status launch_sample(const float* probs, int32_t batch_in, int32_t vocab, const int32_t* indices,
                                int32_t batch_out, const int32_t* top_k, const float* top_p, const float* min_p,
                                int32_t order, uint64_t seed, uint64_t offset, int32_t* out_token, uint8_t* out_valid,
-                               int32_t* out_rounds, void* stream) {
+                               int32_t* out_rounds, void* stream, const uint64_t* seeds = nullptr,
+                               const uint64_t* offsets = nullptr, const uint64_t* offset_dev = nullptr) {
     if (batch_out < 0 || batch_in < 0) return FS_ERR_INVALID_ARG;
     if (batch_out == 0) return FS_OK;
     if (!probs || !out_token || !out_valid) return FS_ERR_INVALID_ARG;
@@ -554,6 +562,9 @@ static fs_status launch_sample(const float* probs, int32_t batch_in, int32_t voc
     a.order = order == FS_ORDER_TOP_K_FIRST ? 0 : 1;
     a.seed = seed;
     a.offset = offset;
+    a.seeds = reinterpret_cast<const unsigned long long*>(seeds);
+    a.offsets = reinterpret_cast<const unsigned long long*>(offsets);
+    a.offset_dev = reinterpret_cast<const unsigned long long*>(offset_dev);
     a.out_token = out_token;
     a.out_valid = out_valid;
     a.out_rounds = out_rounds;
@@ -562,6 +573,11 @@ static fs_status launch_sample(const float* probs, int32_t batch_in, int32_t voc
     a.nsc = p.nsc;
     if (vec) return launch_cluster(sample_kernel<true>, p, batch_out, stream, a);
     return launch_cluster(sample_kernel<false>, p, batch_out, stream, a);
+}
+
+__global__ void advance_kernel(unsigned long long* offset_dev, unsigned long long delta) {
+    grid_dependency_wait();
+    *offset_dev += delta;
 }
 
 }  // namespace fsd
@@ -606,6 +622,24 @@ fs_status fs_top_k_top_p_sampling(const float* probs, int32_t batch_in, int32_t 
     if ((!top_k || !top_p) && batch_out > 0) return FS_ERR_INVALID_ARG;
     return fsd::launch_sample(probs, batch_in, vocab, indices, batch_out, top_k, top_p, min_p, order, seed, offset,
                               out_token, out_valid, out_rounds, stream);
+}
+
+fs_status fs_top_k_top_p_sampling_rng(const float* probs, int32_t batch_in, int32_t vocab, const int32_t* indices,
+                                      int32_t batch_out, const int32_t* top_k, const float* top_p, const float* min_p,
+                                      int32_t order, const uint64_t* seeds, const uint64_t* offsets,
+                                      const uint64_t* offset_dev, uint64_t seed, uint64_t offset, int32_t* out_token,
+                                      uint8_t* out_valid, int32_t* out_rounds, void* stream) {
+    return fsd::launch_sample(probs, batch_in, vocab, indices, batch_out, top_k, top_p, min_p, order, seed, offset,
+                              out_token, out_valid, out_rounds, stream, seeds, offsets, offset_dev);
+}
+
+fs_status fs_advance_offset(uint64_t* offset_dev, uint64_t delta, void* stream) {
+    if (!offset_dev) return FS_ERR_INVALID_ARG;
+    fsd::advance_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(
+        reinterpret_cast<unsigned long long*>(offset_dev), static_cast<unsigned long long>(delta));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fsd::cuda_fail(e);
+    return FS_OK;
 }
 
 }  // extern "C"
