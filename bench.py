@@ -241,6 +241,8 @@ def run_ours(args):
         "top_k_renorm": lambda i: check(lib.fs_top_k_renorm_probs(pp[i % ncopy], B, V, k_ptr, o_ptr, v_ptr, sptr)),
         "top_p_renorm": lambda i: check(lib.fs_top_p_renorm_probs(pp[i % ncopy], B, V, p_ptr, o_ptr, v_ptr, sptr)),
         "mask_logits": lambda i: check(lib.fs_top_k_mask_logits(lp[i % ncopy], B, V, k_ptr, o_ptr, v_ptr, sptr)),
+        "joint_single_pivot": lambda i: check(lib.fs_top_k_top_p_sampling_pivots(
+            pp[i % ncopy], B, V, None, B, k_ptr, p_ptr, None, 1, 1, seed, i, t_ptr, v_ptr, None, sptr)),
     }
     read_bytes = B * V * 4
     alg_bytes = {   # algorithmic bytes per launch
@@ -250,6 +252,7 @@ def run_ours(args):
         "top_k_renorm": 2 * read_bytes + B * (4 + 1),
         "top_p_renorm": 2 * read_bytes + B * (4 + 1),
         "mask_logits": 2 * read_bytes + B * (4 + 1),
+        "joint_single_pivot": read_bytes + B * (4 + 1 + 4 + 4),
     }
 
     def barrier():
@@ -303,18 +306,33 @@ def run_ours(args):
 
     entries = {}
     if not args.no_entries:
-        for name in ["joint", "from_probs", "top_k_renorm", "top_p_renorm", "mask_logits"]:
+        for name in ["joint", "from_probs", "top_k_renorm", "top_p_renorm", "mask_logits", "joint_single_pivot"]:
             tot, pe, _ = timed(calls[name], min(K, 100), 5)
             us = tot / min(K, 100) * 1e3
             entries[name] = {"us_per_call": round(us, 3), "p50_us": round(statistics.median(pe) * 1e3, 3),
                              "p99_us": round(sorted(pe)[min(len(pe) - 1, int(0.99 * len(pe)))] * 1e3, 3),
                              "gbps": round(alg_bytes[name] / (us * 1e-6) / 1e9, 1),
                              "alg_bytes_per_call": alg_bytes[name]}
-    # Round counts of the headline step (one call) for the record.
+    # Round counts of the headline step (one call) for the record, and of the joint
+    # order under the dual- and one-pivot rules over many calls (the pivot ablation).
     check(lib.fs_top_k_top_p_sampling(pp[0], B, V, None, B, k_ptr, p_ptr, None, 0, seed, 12345, t_ptr, v_ptr, r_ptr,
                                       sptr))
     torch.cuda.synchronize(dev)
     rounds = np.bincount(rnd.cpu().numpy()).tolist()
+    ablation = {}
+    for piv in (2, 1):
+        rs = []
+        for i in range(64):
+            check(lib.fs_top_k_top_p_sampling_pivots(pp[i % ncopy], B, V, None, B, k_ptr, p_ptr, None, 1, piv, seed,
+                                                     50000 + i, t_ptr, v_ptr, r_ptr, sptr))
+            rs.append(rnd.clone())
+        r = torch.cat(rs).cpu().numpy()
+        ablation["dual" if piv == 2 else "single"] = {
+            "rounds_mean": round(float(r.mean()), 3), "rounds_p99": int(np.percentile(r, 99)),
+            "rounds_max": int(r.max()), "draws": int(r.size)}
+    if "joint" in entries and "joint_single_pivot" in entries:
+        ablation["dual"]["us_per_call"] = entries["joint"]["us_per_call"]
+        ablation["single"]["us_per_call"] = entries["joint_single_pivot"]["us_per_call"]
 
     # End to end through the C ABI with host buffers.
     host_p = torch.from_numpy(w.probs).pin_memory()
@@ -361,6 +379,7 @@ def run_ours(args):
         "gpu_launches": K,
         "clocks": clk,
         "rounds_histogram": rounds,
+        "pivot_ablation": {"workload": "joint top-k 50 + top-p 0.9, B=64, V=151936", **ablation},
         "entries": entries,
     }
     if rank == 0 and world == 1:

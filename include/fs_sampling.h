@@ -153,6 +153,19 @@ fs_status fs_top_k_top_p_sampling_rng(const float* probs, int32_t batch_in, int3
                                       int32_t* out_token, uint8_t* out_valid,
                                       int32_t* out_rounds, void* stream);
 
+/* Ablation of the pivot rule: as fs_top_k_top_p_sampling (top_k and top_p nullable),
+ * with pivots = 2 the dual-pivot sampler and pivots = 1 the one-pivot rejection
+ * sampler of [blog] "rejection sampling" (after a rejection low <- pivot1; no second
+ * pivot).  Both draw from the same distribution; the one-pivot rule needs more rounds
+ * when many tokens lie below the cut.  pivots outside {1, 2}: FS_ERR_INVALID_ARG. */
+fs_status fs_top_k_top_p_sampling_pivots(const float* probs, int32_t batch_in, int32_t vocab,
+                                         const int32_t* indices, int32_t batch_out,
+                                         const int32_t* top_k, const float* top_p,
+                                         const float* min_p, int32_t order, int32_t pivots,
+                                         uint64_t seed, uint64_t offset,
+                                         int32_t* out_token, uint8_t* out_valid,
+                                         int32_t* out_rounds, void* stream);
+
 /* *offset_dev += delta on the device, ordered on `stream` (one thread; no status
  * beyond launch errors).  Placed after the sampling call inside a captured graph it
  * gives every replay fresh draws.  offset_dev must not be NULL. */

@@ -36,6 +36,7 @@ struct SampleArgs {
     const unsigned long long* seeds;       // per output row, nullable
     const unsigned long long* offsets;     // per output row, nullable
     const unsigned long long* offset_dev;  // added to every row's offset, nullable
+    int single_pivot;         // 1: the one-pivot rule (ablation)
     int* out_token;
     unsigned char* out_valid;
     int* out_rounds;
@@ -48,10 +49,15 @@ struct SampleArgs {
 // the pivot; [explainer] Top-k, Top-p, Min-p), from the count and the mass of the
 // tokens strictly above tau.
 struct Pred {
+    bool single;  // the one-pivot rule: pivot2 = pivot1 (after a rejection, low <- pivot1)
     bool k_on, p_on, m_on;
     int k;
     float pthr;   // top_p * M'   (M' = M, or F_k for top-k-first)
     float t32;    // min-p threshold: float32 rounded up from min_p * max
+    // The second pivot ([blog] dual pivot): the fp32 midpoint of pivot1 and high.
+    __device__ __forceinline__ float pivot2(float pivot1, float high) const {
+        return single ? pivot1 : (pivot1 + high) * 0.5f;
+    }
     __device__ __forceinline__ bool operator()(int cnt, float mass, float tau) const {
         if (k_on && !(cnt < k)) return false;
         if (p_on && !(cnt == 0 || mass < pthr)) return false;
@@ -100,7 +106,7 @@ __device__ __forceinline__ int compact_round(Smem sm, int n_list, const Pred& f,
     j = sm.li()[e];
     const float pivot1 = sm.lv()[e];
     if (!any_filter) return 1;
-    const float pivot2 = (pivot1 + high) * 0.5f;
+    const float pivot2 = f.pivot2(pivot1, high);
     float M1 = 0.f, M2 = 0.f;
     int C1 = 0, C2 = 0;
     for (int i = lane; i < n_list; i += 32) {
@@ -211,7 +217,7 @@ __device__ __forceinline__ int small_rounds(const Small& s, const bool* kept, co
         }
         const float pivot1 = __shfl_sync(FULL, xv, l);
         const int j = __shfl_sync(FULL, iv, l);
-        const float pivot2 = (pivot1 + high) * 0.5f;
+        const float pivot2 = f.pivot2(pivot1, high);
         float m1 = 0.f, m2 = 0.f;
         int c1 = 0, c2 = 0;
 #pragma unroll
@@ -324,6 +330,7 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
 
     // ---- leader from here on
     Pred f;
+    f.single = a.single_pivot != 0;
     f.k_on = k_on;
     f.k = k;
     f.p_on = tp < 1.f;
@@ -473,7 +480,7 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
                 rounds = round + 1;
                 break;
             }
-            const float pivot2 = (pivot1 + high) * 0.5f;
+            const float pivot2 = f.pivot2(pivot1, high);
 
             // ---- a6: fused (mass, count) above pivot1 and pivot2, on the whole cluster
             const int ia = cur == 0 ? 1 : 0;
@@ -536,7 +543,8 @@ static fs_status launch_sample(const float* probs, int32_t batch_in, int32_t voc
                                int32_t batch_out, const int32_t* top_k, const float* top_p, const float* min_p,
                                int32_t order, uint64_t seed, uint64_t offset, int32_t* out_token, uint8_t* out_valid,
                                int32_t* out_rounds, void* stream, const uint64_t* seeds = nullptr,
-                               const uint64_t* offsets = nullptr, const uint64_t* offset_dev = nullptr) {
+                               const uint64_t* offsets = nullptr, const uint64_t* offset_dev = nullptr,
+                               int32_t pivots = 2) {
     if (batch_out < 0 || batch_in < 0) return FS_ERR_INVALID_ARG;
     if (batch_out == 0) return FS_OK;
     if (!probs || !out_token || !out_valid) return FS_ERR_INVALID_ARG;
@@ -544,6 +552,7 @@ static fs_status launch_sample(const float* probs, int32_t batch_in, int32_t voc
     if (vocab > FS_MAX_VOCAB) return FS_ERR_UNSUPPORTED;
     if (!indices && batch_out != batch_in) return FS_ERR_INVALID_ARG;
     if (order != FS_ORDER_TOP_K_FIRST && order != FS_ORDER_JOINT) return FS_ERR_INVALID_ARG;
+    if (pivots != 1 && pivots != 2) return FS_ERR_INVALID_ARG;
 
     const bool vec = (vocab % 4 == 0) && ((reinterpret_cast<uintptr_t>(probs) & 15) == 0);
     const void* fn = vec ? reinterpret_cast<const void*>(sample_kernel<true>)
@@ -565,6 +574,7 @@ static fs_status launch_sample(const float* probs, int32_t batch_in, int32_t voc
     a.seeds = reinterpret_cast<const unsigned long long*>(seeds);
     a.offsets = reinterpret_cast<const unsigned long long*>(offsets);
     a.offset_dev = reinterpret_cast<const unsigned long long*>(offset_dev);
+    a.single_pivot = pivots == 1 ? 1 : 0;
     a.out_token = out_token;
     a.out_valid = out_valid;
     a.out_rounds = out_rounds;
@@ -640,6 +650,15 @@ fs_status fs_advance_offset(uint64_t* offset_dev, uint64_t delta, void* stream) 
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fsd::cuda_fail(e);
     return FS_OK;
+}
+
+fs_status fs_top_k_top_p_sampling_pivots(const float* probs, int32_t batch_in, int32_t vocab, const int32_t* indices,
+                                         int32_t batch_out, const int32_t* top_k, const float* top_p,
+                                         const float* min_p, int32_t order, int32_t pivots, uint64_t seed,
+                                         uint64_t offset, int32_t* out_token, uint8_t* out_valid, int32_t* out_rounds,
+                                         void* stream) {
+    return fsd::launch_sample(probs, batch_in, vocab, indices, batch_out, top_k, top_p, min_p, order, seed, offset,
+                              out_token, out_valid, out_rounds, stream, nullptr, nullptr, nullptr, pivots);
 }
 
 }  // extern "C"

@@ -30,6 +30,8 @@ exceeds the target.
 
 Readings: the midpoint is rounded to float32 like the probabilities it is
 compared with ("fp32"); "exact" keeps it rational for the Markov evaluation.
+"single" is the one-pivot sampler of the [blog] rejection-sampling section (after a
+rejection, low <- pivot1; no second pivot), kept for the ablation.
 "Repeat steps 3 and 4" (garbled in [blog]) is read as "repeat from the draw".
 A row is invalid when f(high) = 0 at the start (S empty) or when r_max draws pass
 without acceptance.
@@ -118,6 +120,8 @@ def three_cases(row: _Row, pivot1, high, midpoint: str):
     """
     if row.f(pivot1):
         return None
+    if midpoint == "single":
+        return pivot1, high
     pivot2 = row.midpoint(pivot1, high, midpoint)
     if row.f(pivot2):
         return pivot1, pivot2
@@ -162,10 +166,10 @@ def sample(p, top_k=None, top_p=None, min_p=None, order="joint",
 
 
 def sample_philox(p, top_k=None, top_p=None, min_p=None, order="joint", *,
-                  seed: int, offset: int, row: int, r_max: int = 256):
+                  seed: int, offset: int, row: int, r_max: int = 256, midpoint: str = "fp32"):
     """``sample`` driven by the Philox stream of output row ``row`` (see oracle.philox)."""
     return sample(p, top_k, top_p, min_p, order,
-                  uniform=lambda r: sampler_uniform(seed, offset, row, r), r_max=r_max)
+                  uniform=lambda r: sampler_uniform(seed, offset, row, r), r_max=r_max, midpoint=midpoint)
 
 
 def exact_output_law(p, top_k=None, top_p=None, min_p=None, order="joint",

@@ -338,3 +338,43 @@ def test_misaligned_rows_and_large_k_first(ms):
         for call in range(3):
             tok, valid, rounds = _call(ms, "top_k_first", P, ks, ps, None, seed=9, offset=call)
             _membership(masks, vref, tok, valid)
+
+
+def test_single_pivot_ablation(ms):
+    """The one-pivot rule ([blog] rejection sampling) through the ablation entry: the
+    same law (TV, chi-square, every draw in S), the oracle's one-pivot run replayed on
+    the same Philox stream, and more rounds than the dual-pivot rule where the second
+    pivot matters."""
+    import torch
+    w = _config1()
+    P = torch.from_numpy(w.probs).cuda()
+    for r in (0, 1):
+        k, p = int(w.top_k[r]), float(w.top_p[r])
+        pt, ok = filters.filtered_distribution(w.probs[r], k, p, None, "joint")
+        n = draws_for_tv(pt)
+        idx = torch.from_numpy(np.full(n, r, np.int32)).cuda()
+        kk = torch.full((n,), k, dtype=torch.int32, device="cuda")
+        pp = torch.full((n,), p, dtype=torch.float32, device="cuda")
+        out = {}
+        for piv in (1, 2):
+            tok, valid, rounds = ms.top_k_top_p_sampling_pivots(P, kk, pp, None, "joint", idx, pivots=piv,
+                                                                 seed=99 + r, offset=4, return_rounds=True)
+            tok, valid, rounds = tok.cpu().numpy(), valid.cpu().numpy(), rounds.cpu().numpy()
+            assert valid.all() and (pt[tok] > 0).all()
+            counts = np.bincount(tok, minlength=w.vocab).astype(np.float64)
+            assert tv_distance(counts, pt) <= 0.005
+            assert chi2_pvalue(counts, pt) > 1e-3
+            out[piv] = (tok, rounds)
+        # Row 0 keeps the arg-max alone (k = 1): there the second pivot skips most of the
+        # rejections (the oracle's one-pivot run averages about 2.6 draws, dual 2.0).
+        if r == 0:
+            assert out[1][1].mean() > out[2][1].mean() + 0.3
+        assert out[1][1].max() >= out[2][1].max()
+        agree = 0
+        for b in range(400):
+            t_ref, _, r_ref = dual_pivot.sample_philox(w.probs[r], k, p, None, "joint", seed=99 + r, offset=4, row=b,
+                                                       midpoint="single")
+            agree += int(t_ref == out[1][0][b] and r_ref == out[1][1][b])
+        assert agree >= 0.99 * 400, agree
+    with pytest.raises(ms.FsError):
+        ms.top_k_top_p_sampling_pivots(P, 10, 0.9, None, "joint", pivots=3, seed=1, offset=0)

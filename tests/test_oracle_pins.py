@@ -140,6 +140,35 @@ def test_exact_law_equals_pj_over_Z(midpoint):
     assert n > 150
 
 
+def test_single_pivot_law_is_exact_and_never_faster():
+    """The one-pivot sampler of the [blog] rejection-sampling section is also exact
+    (p_j / Z on S), and on a row where the dual-pivot rule skips several rejections its
+    expected number of draws is larger."""
+    p = np.array([0.02, 0.03, 0.05, 0.10, 0.15, 0.20, 0.45], np.float32)
+    for k, tp in [(1, None), (2, None), (None, 0.5), (3, 0.9)]:
+        law = dual_pivot.exact_output_law(p, k, tp, None, "joint", midpoint="single")
+        S = filters.allowed_set(p, k, tp, None, "joint")
+        Z = sum(Fraction(float(p[i])) for i in S)
+        assert set(law) == set(int(i) for i in S)
+        for i in S:
+            assert law[int(i)] == Fraction(float(p[i])) / Z
+    # Expected draws from the start state, by the same recursion with a draw counter.
+    def expected_draws(midpoint):
+        row = dual_pivot._Row(p, 1, None, None, "joint", exact=True)
+
+        def go(low, high):
+            elig = [i for i in range(row.V) if row.p[i] > low]
+            S_ = sum((row.p[i] for i in elig), Fraction(0))
+            e = Fraction(1)
+            for i in elig:
+                nxt = dual_pivot.three_cases(row, row.p[i], high, midpoint)
+                if nxt is not None:
+                    e += row.p[i] / S_ * go(*nxt)
+            return e
+        return go(row.low0, row.high0)
+    assert expected_draws("single") > expected_draws("exact")
+
+
 def test_exact_law_on_an_8_token_row_every_k():
     p = workloads.random_small_rows(1, 8, seed=4242)[0]
     for k in range(1, 9):
