@@ -241,6 +241,8 @@ def run_ours(args):
         "top_k_renorm": lambda i: check(lib.fs_top_k_renorm_probs(pp[i % ncopy], B, V, k_ptr, o_ptr, v_ptr, sptr)),
         "top_p_renorm": lambda i: check(lib.fs_top_p_renorm_probs(pp[i % ncopy], B, V, p_ptr, o_ptr, v_ptr, sptr)),
         "mask_logits": lambda i: check(lib.fs_top_k_mask_logits(lp[i % ncopy], B, V, k_ptr, o_ptr, v_ptr, sptr)),
+        "top_k_first_from_logits": lambda i: check(lib.fs_top_k_top_p_sampling_from_logits(
+            lp[i % ncopy], B, V, None, B, None, k_ptr, p_ptr, None, 0, seed, i, t_ptr, v_ptr, None, sptr)),
         "joint_single_pivot": lambda i: check(lib.fs_top_k_top_p_sampling_pivots(
             pp[i % ncopy], B, V, None, B, k_ptr, p_ptr, None, 1, 1, seed, i, t_ptr, v_ptr, None, sptr)),
     }
@@ -253,6 +255,7 @@ def run_ours(args):
         "top_p_renorm": 2 * read_bytes + B * (4 + 1),
         "mask_logits": 2 * read_bytes + B * (4 + 1),
         "joint_single_pivot": read_bytes + B * (4 + 1 + 4 + 4),
+        "top_k_first_from_logits": read_bytes + B * (4 + 1 + 4 + 4),
     }
 
     def barrier():
@@ -306,7 +309,8 @@ def run_ours(args):
 
     entries = {}
     if not args.no_entries:
-        for name in ["joint", "from_probs", "top_k_renorm", "top_p_renorm", "mask_logits", "joint_single_pivot"]:
+        for name in ["joint", "from_probs", "top_k_renorm", "top_p_renorm", "mask_logits", "joint_single_pivot",
+                     "top_k_first_from_logits"]:
             tot, pe, _ = timed(calls[name], min(K, 100), 5)
             us = tot / min(K, 100) * 1e3
             entries[name] = {"us_per_call": round(us, 3), "p50_us": round(statistics.median(pe) * 1e3, 3),

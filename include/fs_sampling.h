@@ -153,6 +153,25 @@ fs_status fs_top_k_top_p_sampling_rng(const float* probs, int32_t batch_in, int3
                                       int32_t* out_token, uint8_t* out_valid,
                                       int32_t* out_rounds, void* stream);
 
+/* Sampling from logits with the softmax fused in ([explainer] the sampling pipeline:
+ * p = softmax(z / T) before the filters).  logits: [batch_in, vocab] float32.  The row
+ * is read once for its maximum m; the rest of the path (every filter, order and the
+ * dual-pivot rounds, exactly as fs_top_k_top_p_sampling) then runs on the weights
+ * w = exp((z - m) / T) in float32 -- the unnormalised softmax, read again from L2 --
+ * so no probability matrix is written.  temperature: [batch_out] float32, nullable
+ * (1); T <= 0 or NaN makes the row invalid.  top_k, top_p, min_p: nullable.  A NaN
+ * or +inf logit makes the row invalid; -inf logits have weight 0.  Top-k and top-p
+ * are decided on the float32 weights (two logits whose weights round to the same
+ * float32 count as equal). */
+fs_status fs_top_k_top_p_sampling_from_logits(const float* logits, int32_t batch_in, int32_t vocab,
+                                              const int32_t* indices, int32_t batch_out,
+                                              const float* temperature,
+                                              const int32_t* top_k, const float* top_p,
+                                              const float* min_p, int32_t order,
+                                              uint64_t seed, uint64_t offset,
+                                              int32_t* out_token, uint8_t* out_valid,
+                                              int32_t* out_rounds, void* stream);
+
 /* Ablation of the pivot rule: as fs_top_k_top_p_sampling (top_k and top_p nullable),
  * with pivots = 2 the dual-pivot sampler and pivots = 1 the one-pivot rejection
  * sampler of [blog] "rejection sampling" (after a rejection low <- pivot1; no second

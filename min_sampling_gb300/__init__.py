@@ -20,7 +20,7 @@ __all__ = [
     "FsError", "lib", "LIB_PATH", "ORDER_TOP_K_FIRST", "ORDER_JOINT", "MAX_ROUNDS",
     "sampling_from_probs", "top_k_sampling", "top_p_sampling", "min_p_sampling",
     "top_k_top_p_sampling", "top_k_top_p_sampling_rng", "advance_offset",
-    "top_k_top_p_sampling_pivots", "top_k_renorm_probs", "top_p_renorm_probs",
+    "top_k_top_p_sampling_pivots", "top_k_top_p_sampling_from_logits", "top_k_renorm_probs", "top_p_renorm_probs",
     "top_k_mask_logits", "philox4x32_10",
 ]
 
@@ -43,6 +43,8 @@ _SIGNATURES = {
     "fs_top_k_top_p_sampling_rng": [_P, _I32, _I32, _P, _I32, _P, _P, _P, _I32, _P, _P, _P, _U64, _U64, _P, _P, _P,
                                     _P],
     "fs_advance_offset": [_P, _U64, _P],
+    "fs_top_k_top_p_sampling_from_logits": [_P, _I32, _I32, _P, _I32, _P, _P, _P, _P, _I32, _U64, _U64, _P, _P, _P,
+                                            _P],
     "fs_top_k_top_p_sampling_pivots": [_P, _I32, _I32, _P, _I32, _P, _P, _P, _I32, _I32, _U64, _U64, _P, _P, _P,
                                        _P],
     "fs_top_k_renorm_probs": [_P, _I32, _I32, _P, _P, _P, _P],
@@ -246,6 +248,24 @@ def top_k_top_p_sampling_pivots(probs, top_k=None, top_p=None, min_p=None, order
     tok, valid, rounds = _outputs(b_out, dev)
     _check(_lib().fs_top_k_top_p_sampling_pivots(
         _ptr(probs), b_in, V, _ptr(indices), b_out, *[_ptr(t) for t in ps], _order(order), int(pivots),
+        int(seed) & (2 ** 64 - 1), int(offset) & (2 ** 64 - 1), _ptr(tok), _ptr(valid),
+        _ptr(rounds) if return_rounds else None, _stream()))
+    return (tok, valid, rounds) if return_rounds else (tok, valid)
+
+
+def top_k_top_p_sampling_from_logits(logits, temperature=None, top_k=None, top_p=None, min_p=None, order="joint",
+                                     indices=None, *, seed: int, offset: int, return_rounds: bool = False):
+    """Sampling from logits with the softmax (temperature) fused into the kernel."""
+    logits = _matrix(logits, "logits")
+    b_in, V = logits.shape
+    dev = logits.device
+    b_out = b_in if indices is None else indices.shape[0]
+    ps = [None if v is None else _rows(v, b_out, dt, dev, n)
+          for v, dt, n in ((temperature, torch.float32, "temperature"), (top_k, torch.int32, "top_k"),
+                           (top_p, torch.float32, "top_p"), (min_p, torch.float32, "min_p"))]
+    tok, valid, rounds = _outputs(b_out, dev)
+    _check(_lib().fs_top_k_top_p_sampling_from_logits(
+        _ptr(logits), b_in, V, _ptr(indices), b_out, *[_ptr(t) for t in ps], _order(order),
         int(seed) & (2 ** 64 - 1), int(offset) & (2 ** 64 - 1), _ptr(tok), _ptr(valid),
         _ptr(rounds) if return_rounds else None, _stream()))
     return (tok, valid, rounds) if return_rounds else (tok, valid)

@@ -145,6 +145,18 @@ struct Geom {
         a = min(ns, c * nsc);
         b = min(ns, a + nsc);
     }
+    // Rows of logits sampled through a softmax: every value read from the row after the
+    // row maximum vm is known is turned into its weight w = exp((z - vm) / T) (vinv =
+    // 1 / T), so that the rest of the path works on unnormalised probabilities.  For
+    // rows of probabilities (soft = false) values are used as they are.
+    bool soft = false;
+    float vm = 0.f, vinv = 1.f;
+    __device__ __forceinline__ float val(float x) const { return soft ? expf((x - vm) * vinv) : x; }
+    __device__ __forceinline__ float4 val4(float4 v) const {
+        return soft ? make_float4(val(v.x), val(v.y), val(v.z), val(v.w)) : v;
+    }
+    // The raw value past the row end that stands for weight 0.
+    __device__ __forceinline__ float fill0() const { return soft ? __int_as_float(0xff800000) : 0.f; }
 };
 
 // ------------------------------------------------------------------ cluster PTX
@@ -420,7 +432,7 @@ __device__ __forceinline__ void stream_warp(const float* __restrict__ row, Geom 
         for (int j = 0; j < TB; ++j) {
             const int blk = b0 + j;
             const int sg = r0 + (blk >> g.shift);
-            v[j] = (blk < nblk && live(sg)) ? load4<VEC, NC>(row, g.V, g.base(sg, blk & mask, lane), 0.f)
+            v[j] = (blk < nblk && live(sg)) ? g.val4(load4<VEC, NC>(row, g.V, g.base(sg, blk & mask, lane), g.fill0()))
                                             : make_float4(0.f, 0.f, 0.f, 0.f);
         }
     };
@@ -464,8 +476,9 @@ __device__ __forceinline__ void pass1(const float* __restrict__ row, Geom g, Sme
 #pragma unroll
         for (int j = 0; j < TB; ++j) {
             const int sg = g.s0 + t * spt + (j >> g.shift);
-            v[j] = (t < ntrip && sg < g.s1) ? load4<VEC, NC>(row, g.V, g.base(sg, j & mask, lane), fill)
-                                            : make_float4(fill, fill, fill, fill);
+            v[j] = (t < ntrip && sg < g.s1)
+                       ? g.val4(load4<VEC, NC>(row, g.V, g.base(sg, j & mask, lane), g.soft ? g.fill0() : fill))
+                       : make_float4(fill, fill, fill, fill);
         }
     };
     if (VEC && warp == 0)  // the CTA's whole share towards L2 at once; the loads below then mostly hit L2
@@ -727,7 +740,7 @@ __device__ __forceinline__ int collect_range(const float* __restrict__ row, Geom
         cp_async_wait<0>();
     };
     auto keep = [&](int j, int base, int q) {
-        const uint32_t key = keyf(st[j * BLK + q]);
+        const uint32_t key = keyf(g.val(st[j * BLK + q]));
         return key >= thr && uint64_t(key) < thr_hi && base + q < g.V;
     };
     int cnt = 0;
@@ -765,7 +778,7 @@ __device__ __forceinline__ int collect_range(const float* __restrict__ row, Geom
             int p = pos + incl - k;
 #pragma unroll 1
             for (int q = 0; q < 4; ++q)
-                if (keep(j, base, q)) out(p++, st[j * BLK + q], base + q);
+                if (keep(j, base, q)) out(p++, g.val(st[j * BLK + q]), base + q);
             pos += __shfl_sync(FULL, incl, 31);
         }
     }
@@ -1102,7 +1115,7 @@ __device__ __forceinline__ unsigned long long locate_in_segment(const float* __r
 #pragma unroll 1
     for (int it = 0; it < g.seg_it(); ++it) {
         const int base = g.base(s, it, lane);
-        const float4 v = load4<VEC, NC>(row, g.V, base, 0.f);
+        const float4 v = g.val4(load4<VEC, NC>(row, g.V, base, g.fill0()));
         float w[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {

@@ -37,6 +37,7 @@ struct SampleArgs {
     const unsigned long long* offsets;     // per output row, nullable
     const unsigned long long* offset_dev;  // added to every row's offset, nullable
     int single_pivot;         // 1: the one-pivot rule (ablation)
+    const float* temperature; // rows of logits: per output row, nullable (1)
     int* out_token;
     unsigned char* out_valid;
     int* out_rounds;
@@ -247,7 +248,48 @@ __device__ __forceinline__ int small_rounds(const Small& s, const bool* kept, co
     return -1;
 }
 
+// Largest order key of this CTA's segments of a row of logits (first read of the row),
+// block-collective; every thread gets it.
 template <bool VEC>
+__device__ __forceinline__ uint32_t row_max_key(const float* __restrict__ row, Geom g, Smem sm, int warp, int lane) {
+    int r0, r1;
+    warp_range(g.s1 - g.s0, warp, r0, r1);
+    r0 += g.s0;
+    r1 += g.s0;
+    const int nblk = (r1 - r0) << g.shift;
+    const int mask = g.seg_it() - 1;
+    const float ninf = __int_as_float(0xff800000);
+    uint32_t km = 0;
+#pragma unroll 1
+    for (int b0 = 0; b0 < nblk; b0 += TB) {
+        float4 v[TB];
+#pragma unroll
+        for (int j = 0; j < TB; ++j) {
+            const int blk = b0 + j;
+            v[j] = blk < nblk ? load4<VEC, true>(row, g.V, g.base(r0 + (blk >> g.shift), blk & mask, lane), ninf)
+                              : make_float4(ninf, ninf, ninf, ninf);
+        }
+#pragma unroll
+        for (int j = 0; j < TB; ++j)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) km = max(km, logit_key(q_at(v[j], q)));
+    }
+    km = warp_max_u(km);
+    if (lane == 0) sm.red()[warp] = int(km);
+    __syncthreads();
+    uint32_t r = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) r = max(r, uint32_t(sm.red()[w]));
+    __syncthreads();
+    return r;
+}
+
+// The float whose order key (logit_key) is k.
+__device__ __forceinline__ float from_logit_key(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+template <bool VEC, bool SOFT>
 __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
     const int C = int(cluster_nctarank());
     const int rank = int(cluster_ctarank());
@@ -255,7 +297,7 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool leader = rank == 0;
     const Smem sm(a.ns);
-    const Geom g(a.V, a.shift, a.ns, a.nsc, rank);
+    Geom g(a.V, a.shift, a.ns, a.nsc, rank);
     const int V = a.V, ns = a.ns;
     const KeyProb keyf;
 
@@ -275,8 +317,31 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
     const bool k_on = k > 0 && k < V;
     const bool kfirst = a.order == 0 && k_on;
     const bool need_hist = kfirst && ns >= k;
+    const float temp = SOFT && a.temperature ? a.temperature[b] : 1.f;
 
-    // ---- a2: pass 1, the only HBM read of the row, inside a split cluster barrier
+    if (SOFT) {
+        // Rows of logits: the row maximum first (the one HBM read), exchanged through
+        // every CTA's part[].u[3]; pass 1 then reads the row again (from L2) as weights
+        // w = exp((z - max) / T), i.e. the softmax without its normalisation.
+        cluster_arrive();
+        const uint32_t zk = row_ok ? row_max_key<VEC>(row, g, sm, warp, lane) : 0u;
+        cluster_wait();  // every CTA has started
+        if (tid < C) {
+            uint32_t* dst = &sm.part()[rank].u[3];
+            if (tid == rank) {
+                *dst = zk;
+            } else {
+                st_dsmem_u32(map_rank(smem_u32(dst), uint32_t(tid)), zk);
+            }
+        }
+        cluster_sync();
+        g.soft = true;
+        g.vm = from_logit_key(warp_max_u(lane < C ? sm.part()[lane].u[3] : 0u));
+        g.vinv = 1.f / temp;
+    }
+
+    // ---- a2: pass 1, the only HBM read of the row (of probabilities), inside a split
+    // cluster barrier
     if (need_hist)
         for (int i = tid; i < HBINS; i += NT) {
             sm.hist()[i] = 0u;
@@ -345,7 +410,8 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
     const uint32_t maxkey = tot.maxkey;
     if (tid < C) sm.cmass()[tid] = sm.part()[tid].f[0];
     const float rowmax = __uint_as_float(maxkey);
-    bool valid = row_ok && !isnan(tp) && !isnan(mp) && !any_bad && M > 0.f && M <= 3.402823466e38f;
+    bool valid = row_ok && !isnan(tp) && !isnan(mp) && !any_bad && M > 0.f && M <= 3.402823466e38f &&
+                 (!SOFT || temp > 0.f);
     if (f.m_on) {
         f.t32 = __double2float_ru(double(mp) * double(rowmax));
         if (!(rowmax >= f.t32)) valid = false;  // S is empty: f(max) = 0
@@ -544,7 +610,7 @@ static fs_status launch_sample(const float* probs, int32_t batch_in, int32_t voc
                                int32_t order, uint64_t seed, uint64_t offset, int32_t* out_token, uint8_t* out_valid,
                                int32_t* out_rounds, void* stream, const uint64_t* seeds = nullptr,
                                const uint64_t* offsets = nullptr, const uint64_t* offset_dev = nullptr,
-                               int32_t pivots = 2) {
+                               int32_t pivots = 2, bool soft = false, const float* temperature = nullptr) {
     if (batch_out < 0 || batch_in < 0) return FS_ERR_INVALID_ARG;
     if (batch_out == 0) return FS_OK;
     if (!probs || !out_token || !out_valid) return FS_ERR_INVALID_ARG;
@@ -555,8 +621,10 @@ static fs_status launch_sample(const float* probs, int32_t batch_in, int32_t voc
     if (pivots != 1 && pivots != 2) return FS_ERR_INVALID_ARG;
 
     const bool vec = (vocab % 4 == 0) && ((reinterpret_cast<uintptr_t>(probs) & 15) == 0);
-    const void* fn = vec ? reinterpret_cast<const void*>(sample_kernel<true>)
-                         : reinterpret_cast<const void*>(sample_kernel<false>);
+    const void* fn = soft ? (vec ? reinterpret_cast<const void*>(sample_kernel<true, true>)
+                                 : reinterpret_cast<const void*>(sample_kernel<false, true>))
+                          : (vec ? reinterpret_cast<const void*>(sample_kernel<true, false>)
+                                 : reinterpret_cast<const void*>(sample_kernel<false, false>));
     Plan p;
     fs_status st = make_plan(batch_out, vocab, fn, p);
     if (st != FS_OK) return st;
@@ -575,14 +643,19 @@ static fs_status launch_sample(const float* probs, int32_t batch_in, int32_t voc
     a.offsets = reinterpret_cast<const unsigned long long*>(offsets);
     a.offset_dev = reinterpret_cast<const unsigned long long*>(offset_dev);
     a.single_pivot = pivots == 1 ? 1 : 0;
+    a.temperature = temperature;
     a.out_token = out_token;
     a.out_valid = out_valid;
     a.out_rounds = out_rounds;
     a.shift = p.shift;
     a.ns = p.ns;
     a.nsc = p.nsc;
-    if (vec) return launch_cluster(sample_kernel<true>, p, batch_out, stream, a);
-    return launch_cluster(sample_kernel<false>, p, batch_out, stream, a);
+    if (soft) {
+        if (vec) return launch_cluster(sample_kernel<true, true>, p, batch_out, stream, a);
+        return launch_cluster(sample_kernel<false, true>, p, batch_out, stream, a);
+    }
+    if (vec) return launch_cluster(sample_kernel<true, false>, p, batch_out, stream, a);
+    return launch_cluster(sample_kernel<false, false>, p, batch_out, stream, a);
 }
 
 __global__ void advance_kernel(unsigned long long* offset_dev, unsigned long long delta) {
@@ -659,6 +732,16 @@ fs_status fs_top_k_top_p_sampling_pivots(const float* probs, int32_t batch_in, i
                                          void* stream) {
     return fsd::launch_sample(probs, batch_in, vocab, indices, batch_out, top_k, top_p, min_p, order, seed, offset,
                               out_token, out_valid, out_rounds, stream, nullptr, nullptr, nullptr, pivots);
+}
+
+fs_status fs_top_k_top_p_sampling_from_logits(const float* logits, int32_t batch_in, int32_t vocab,
+                                              const int32_t* indices, int32_t batch_out, const float* temperature,
+                                              const int32_t* top_k, const float* top_p, const float* min_p,
+                                              int32_t order, uint64_t seed, uint64_t offset, int32_t* out_token,
+                                              uint8_t* out_valid, int32_t* out_rounds, void* stream) {
+    return fsd::launch_sample(logits, batch_in, vocab, indices, batch_out, top_k, top_p, min_p, order, seed, offset,
+                              out_token, out_valid, out_rounds, stream, nullptr, nullptr, nullptr, 2, true,
+                              temperature);
 }
 
 }  // extern "C"

@@ -297,3 +297,12 @@ def top_k_mask_logits(z, k: int):
         return z.copy(), True
     t = np.sort(z.astype(np.float64))[::-1][int(k) - 1]
     return np.where(z.astype(np.float64) >= t, z, np.float32(-np.inf)).astype(np.float32), True
+
+
+def softmax(z, temperature: float = 1.0) -> np.ndarray:
+    """p = softmax(z / T) in float64 ([explainer] the sampling pipeline: temperature
+    then softmax before the filters), from the float32 logits converted exactly:
+    exp((z_i - max z) / T) / sum_j exp((z_j - max z) / T).  -inf logits get 0."""
+    z64 = np.asarray(z, dtype=np.float32).astype(np.float64)
+    e = np.exp((z64 - z64.max()) / float(temperature))
+    return e / e.sum()

@@ -169,6 +169,22 @@ def test_single_pivot_law_is_exact_and_never_faster():
     assert expected_draws("single") > expected_draws("exact")
 
 
+def test_softmax_definition():
+    """Shift invariance, the uniform row, the ratio exp((z_i - z_j) / T), T = 1 against
+    a hand value, and weight 0 for -inf."""
+    z = np.array([0.0, 1.0, -2.0, 3.5], np.float32)
+    for T in (0.5, 1.0, 2.0):
+        p = filters.softmax(z, T)
+        assert abs(p.sum() - 1.0) < 1e-15
+        np.testing.assert_allclose(filters.softmax(z + np.float32(7.0), T), p, rtol=1e-13)
+        assert math.isclose(p[1] / p[0], math.exp(1.0 / T), rel_tol=1e-13)
+    np.testing.assert_allclose(filters.softmax(np.zeros(5, np.float32)), np.full(5, 0.2), rtol=1e-15)
+    q = filters.softmax(np.array([0.0, math.log(3.0)], np.float32))
+    assert math.isclose(q[1], 0.75, rel_tol=1e-7)          # e^{ln 3} / (1 + e^{ln 3}) with z rounded to float32
+    r = filters.softmax(np.array([1.0, -np.inf, 1.0], np.float32))
+    assert r[1] == 0.0 and r[0] == r[2] == 0.5
+
+
 def test_exact_law_on_an_8_token_row_every_k():
     p = workloads.random_small_rows(1, 8, seed=4242)[0]
     for k in range(1, 9):
