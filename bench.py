@@ -59,7 +59,8 @@ def parse_args_from(argv):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--no-entries", action="store_true", help="time only the headline step")
+    ap.add_argument("--no-entries", action="store_true",
+                    help="time only the headline step (no other entries, no pivot ablation)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-oracle sample")
     ap.add_argument("--profile", action="store_true",
                     help="only run the headline step (warmup + steps launches) for a profiler; prints a short line")
@@ -324,7 +325,7 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     rounds = np.bincount(rnd.cpu().numpy()).tolist()
     ablation = {}
-    for piv in (2, 1):
+    for piv in ((2, 1) if not args.no_entries else ()):
         rs = []
         for i in range(64):
             check(lib.fs_top_k_top_p_sampling_pivots(pp[i % ncopy], B, V, None, B, k_ptr, p_ptr, None, 1, piv, seed,
@@ -383,7 +384,8 @@ def run_ours(args):
         "gpu_launches": K,
         "clocks": clk,
         "rounds_histogram": rounds,
-        "pivot_ablation": {"workload": "joint top-k 50 + top-p 0.9, B=64, V=151936", **ablation},
+        "pivot_ablation": ({"workload": "joint top-k 50 + top-p 0.9, B=64, V=151936", **ablation}
+                           if ablation else None),
         "entries": entries,
     }
     if rank == 0 and world == 1:
