@@ -372,7 +372,7 @@ def run_ours(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "batch": B, "vocab": V, "top_k": K_TOP, "top_p": P_TOP,
-                   "entry": "fs_top_k_top_p_sampling(order=top_k_first)",
+                   "entry": "fs_top_k_top_p_sampling(order=top_k_first)", "plan": ms.sampling_plan(B, V),
                    "l2": f"inputs rotate over {ncopy} copies ({ncopy * per_copy / 1e6:.0f} MB > 3x L2 "
                          f"{l2 / 1e6:.0f} MB)", "parallelism": f"rows independent, {world} GPU(s)"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",

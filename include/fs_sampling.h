@@ -217,6 +217,12 @@ fs_status fs_top_k_mask_logits(const float* logits, int32_t batch, int32_t vocab
                                const int32_t* top_k, float* out_logits,
                                uint8_t* out_valid, void* stream);
 
+/* The launch plan of the sampling kernels for `batch_out` rows of `vocab` elements on
+ * the current device: CTAs per row (*cluster), elements per segment and segments per
+ * CTA.  Host only; nothing is launched. */
+fs_status fs_sampling_plan(int32_t batch_out, int32_t vocab, int32_t* cluster, int32_t* segment_len,
+                           int32_t* segments_per_cta);
+
 /* The counter-based generator the samplers draw from, exposed for checking:
  * out[4i..4i+3] = Philox4x32-10(counter = ctr[4i..4i+3], key = key[2i..2i+1]).
  * ctr: [n,4] uint32, key: [n,2] uint32, out: [n,4] uint32 (device pointers). */

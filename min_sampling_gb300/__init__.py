@@ -20,7 +20,7 @@ __all__ = [
     "FsError", "lib", "LIB_PATH", "ORDER_TOP_K_FIRST", "ORDER_JOINT", "MAX_ROUNDS",
     "sampling_from_probs", "top_k_sampling", "top_p_sampling", "min_p_sampling",
     "top_k_top_p_sampling", "top_k_top_p_sampling_rng", "advance_offset",
-    "top_k_top_p_sampling_pivots", "top_k_top_p_sampling_from_logits", "top_k_renorm_probs", "top_p_renorm_probs",
+    "top_k_top_p_sampling_pivots", "top_k_top_p_sampling_from_logits", "sampling_plan", "top_k_renorm_probs", "top_p_renorm_probs",
     "top_k_mask_logits", "philox4x32_10",
 ]
 
@@ -43,6 +43,8 @@ _SIGNATURES = {
     "fs_top_k_top_p_sampling_rng": [_P, _I32, _I32, _P, _I32, _P, _P, _P, _I32, _P, _P, _P, _U64, _U64, _P, _P, _P,
                                     _P],
     "fs_advance_offset": [_P, _U64, _P],
+    "fs_sampling_plan": [_I32, _I32, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
+                         ctypes.POINTER(ctypes.c_int32)],
     "fs_top_k_top_p_sampling_from_logits": [_P, _I32, _I32, _P, _I32, _P, _P, _P, _P, _I32, _U64, _U64, _P, _P, _P,
                                             _P],
     "fs_top_k_top_p_sampling_pivots": [_P, _I32, _I32, _P, _I32, _P, _P, _P, _I32, _I32, _U64, _U64, _P, _P, _P,
@@ -269,6 +271,13 @@ def top_k_top_p_sampling_from_logits(logits, temperature=None, top_k=None, top_p
         int(seed) & (2 ** 64 - 1), int(offset) & (2 ** 64 - 1), _ptr(tok), _ptr(valid),
         _ptr(rounds) if return_rounds else None, _stream()))
     return (tok, valid, rounds) if return_rounds else (tok, valid)
+
+
+def sampling_plan(batch_out: int, vocab: int) -> dict:
+    """CTAs per row, elements per segment and segments per CTA the samplers use."""
+    vals = [ctypes.c_int32(0) for _ in range(3)]
+    _check(_lib().fs_sampling_plan(int(batch_out), int(vocab), *[ctypes.byref(v) for v in vals]))
+    return {"cluster": vals[0].value, "segment_len": vals[1].value, "segments_per_cta": vals[2].value}
 
 
 def advance_offset(offset_dev, delta: int = 1) -> None:

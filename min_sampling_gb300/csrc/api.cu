@@ -56,6 +56,10 @@ fs_status prepare_kernel(const void* fn) {
     if (st != FS_OK) return st;
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(optin));
     if (e != cudaSuccess) return cuda_fail(e);
+    // Clusters of up to 16 CTAs (more than the portable 8) where the device has them;
+    // make_plan only picks sizes the occupancy query says fit.
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return cuda_fail(e);
     done.insert({fn, dev});
     return FS_OK;
 }

@@ -37,7 +37,7 @@ constexpr int CAP = 1024;               // compact-list capacity (leader)
 constexpr int SBH = 2;                  // blocks per half of a warp's staging buffer
 constexpr int HBINS = 1024;             // histogram bins of the top-k bound
 constexpr int R_MAX = 256;              // rejection rounds before a row is invalid
-constexpr int MAX_CLUSTER = 8;
+constexpr int MAX_CLUSTER = 16;         // CTAs per row (above 8: non-portable cluster sizes)
 constexpr int REDW = 128;               // words of block-reduction scratch
 constexpr uint64_t NO_LIMIT = uint64_t(1) << 32;  // an upper key bound that excludes nothing
 constexpr unsigned FULL = 0xffffffffu;

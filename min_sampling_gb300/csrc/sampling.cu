@@ -744,4 +744,17 @@ fs_status fs_top_k_top_p_sampling_from_logits(const float* logits, int32_t batch
                               temperature);
 }
 
+fs_status fs_sampling_plan(int32_t batch_out, int32_t vocab, int32_t* cluster, int32_t* segment_len,
+                           int32_t* segments_per_cta) {
+    if (batch_out < 1 || vocab < 1 || !cluster || !segment_len || !segments_per_cta) return FS_ERR_INVALID_ARG;
+    if (vocab > FS_MAX_VOCAB) return FS_ERR_UNSUPPORTED;
+    fsd::Plan p;
+    const fs_status st = fsd::make_plan(batch_out, vocab, reinterpret_cast<const void*>(fsd::sample_kernel<true, false>), p);
+    if (st != FS_OK) return st;
+    *cluster = p.C;
+    *segment_len = fsd::BLK << p.shift;
+    *segments_per_cta = p.nsc;
+    return FS_OK;
+}
+
 }  // extern "C"
