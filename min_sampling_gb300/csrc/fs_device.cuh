@@ -35,7 +35,7 @@ constexpr int MAX_SEG_SHIFT = 2;        // at most 4 blocks per segment (V <= 2^
 constexpr int NS_TARGET = 4096;         // segments per row (longer rows use longer segments)
 constexpr int CAP = 1024;               // compact-list capacity (leader)
 constexpr int SBH = 2;                  // blocks per half of a warp's staging buffer
-constexpr int HBINS = 1024;             // histogram bins of the top-k bound
+constexpr int HBINS = 2048;             // histogram bins of the top-k bound (key >> 21)
 constexpr int R_MAX = 256;              // rejection rounds before a row is invalid
 constexpr int MAX_CLUSTER = 16;         // CTAs per row (above 8: non-portable cluster sizes)
 constexpr int REDW = 128;               // words of block-reduction scratch
@@ -44,6 +44,7 @@ constexpr unsigned FULL = 0xffffffffu;
 
 // Commands from the leader to the other CTAs of the cluster.
 static_assert(HBINS <= NW * 2 * SBH * BLK, "the histogram lives in the staging buffers");
+static_assert(HBINS <= 2 * CAP, "a CTA's own histogram counts live in the compact list (values, then indices)");
 
 // A (token index, value) pair packed into one 64-bit register.
 __device__ __forceinline__ unsigned long long pack_jx(int j, float x) {
@@ -997,19 +998,40 @@ __device__ __forceinline__ Small small_gather(Smem sm, int C, int rc, bool exact
 }
 
 // The k-th largest order key of a small list (0 if it has fewer than k entries): the
-// largest key v with #{keys >= v} >= k, counting for each entry how many entries are
-// at least as large (every entry visits every other through shuffles).
+// largest key v with #{keys >= v} >= k.  When few entries lie below it (n - k < 32),
+// the smallest keys are taken away one distinct value at a time (a warp minimum per
+// step) until fewer than k would remain; otherwise every entry counts how many
+// entries are at least as large (every entry visits every other through shuffles).
 // Warp-collective.  Entries of the list have non-zero keys.
 template <typename KEYF>
 __device__ __forceinline__ uint32_t small_kth(const Small& s, int k, KEYF keyf) {
     if (s.n < k) return 0u;
     uint32_t key[SR];
+#pragma unroll
+    for (int r = 0; r < SR; ++r) key[r] = s.in[r] ? keyf(s.x[r]) : 0u;
+    const int drop = s.n - k;  // entries strictly below the answer, at most
+    if (drop < 32) {
+        uint32_t floor_ = 0u;  // keys <= floor_ are taken away
+        int gone = 0;
+#pragma unroll 1
+        for (int it = 0; it <= drop; ++it) {
+            uint32_t m = 0xffffffffu;
+#pragma unroll
+            for (int r = 0; r < SR; ++r) m = (s.in[r] && key[r] > floor_) ? min(m, key[r]) : m;
+            m = warp_min_u(m);
+            int c = 0;
+#pragma unroll
+            for (int r = 0; r < SR; ++r) c += (s.in[r] && key[r] == m);
+            c = warp_sum_i(c);
+            if (gone + c > drop) return m;  // fewer than k would remain above m
+            gone += c;
+            floor_ = m;
+        }
+        return floor_;  // not reached: the loop ends by the return above
+    }
     int ge[SR];
 #pragma unroll
-    for (int r = 0; r < SR; ++r) {
-        key[r] = s.in[r] ? keyf(s.x[r]) : 0u;
-        ge[r] = 0;
-    }
+    for (int r = 0; r < SR; ++r) ge[r] = 0;
     const int lanes = (s.n + SR - 1) / SR;  // lanes holding entries
 #pragma unroll 1
     for (int l = 0; l < lanes; ++l) {

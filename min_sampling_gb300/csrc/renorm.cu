@@ -125,10 +125,10 @@ __global__ void __launch_bounds__(NT, 4) filter_kernel(const FilterArgs a) {
     int pos = 0;
     bool bad = false;
     uint32_t kmax = 0;
-    pass1<VEC, false, IS_PROB>(row, g, sm, need_hist ? (IS_PROB ? 21 : 22) : -1, warp, lane, pos, bad,
+    pass1<VEC, false, IS_PROB>(row, g, sm, need_hist ? 21 : -1, warp, lane, pos, bad,
                                kmax);
     cluster_wait();  // every CTA has started and cleared its histogram
-    pass1_totals(g, sm, leader, rank, C, pos, bad, kmax, need_hist ? (IS_PROB ? 21 : 22) : -1, IS_PROB, false, warp,
+    pass1_totals(g, sm, leader, rank, C, pos, bad, kmax, need_hist ? 21 : -1, IS_PROB, false, warp,
                  lane, tid);
     cluster_sync();  // the leader's segment table, every CTA's parts and histogram, are complete
 
@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(NT, 4) filter_kernel(const FilterArgs a) {
     uint32_t L0 = 0u;
     int list_mode = -1;  // 0: regions fit, 1: contiguous, -1: no list
     if (k_on) {
-        L0 = need_hist ? hist_bound(sm, ns, k, IS_PROB ? 21 : 22, maxkey, warp, lane) : 0u;
+        L0 = need_hist ? hist_bound(sm, ns, k, 21, maxkey, warp, lane) : 0u;
         if (IS_PROB) L0 = max(L0, 1u);
         collect_own<VEC>(row, g, sm, leader, rank, C, rank * (CAP / C), CAP / C, L0, NO_LIMIT, keyf, true, true,
                          warp, lane, tid);

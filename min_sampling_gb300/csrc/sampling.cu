@@ -179,9 +179,12 @@ __device__ __forceinline__ int small_rounds(const Small& s, const bool* kept, co
                                             unsigned long long seed, unsigned long long offset, uint32_t b, int lane,
                                             int& rounds) {
     float low = 0.f;
+    // Lane l holds the uniform of round l: 32 rounds of the stream at the cost of one.
+    const float u_lane = sampler_uniform(seed, offset, b, uint32_t(lane));
 #pragma unroll 1
     for (int round = 0; round < R_MAX; ++round) {
-        const float target = sampler_uniform(seed, offset, b, uint32_t(round)) * S_low;
+        const float u = round < 32 ? __shfl_sync(FULL, u_lane, round) : sampler_uniform(seed, offset, b, uint32_t(round));
+        const float target = u * S_low;
         // Inverse transform over the list in index order (lane-major): the lane whose
         // running sum passes the target, then the slot inside it.
         float w[SR], lsum = 0.f;
