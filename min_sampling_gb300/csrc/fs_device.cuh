@@ -43,7 +43,7 @@ constexpr uint64_t NO_LIMIT = uint64_t(1) << 32;  // an upper key bound that exc
 constexpr unsigned FULL = 0xffffffffu;
 
 // Commands from the leader to the other CTAs of the cluster.
-static_assert(HBINS <= NW * 2 * SBH * BLK, "the histogram lives in the staging buffers");
+static_assert(2 * HBINS <= NW * 2 * SBH * BLK, "both top-k histograms live in the staging buffers");
 static_assert(HBINS <= 2 * CAP, "a CTA's own histogram counts live in the compact list (values, then indices)");
 
 // A (token index, value) pair packed into one 64-bit register.
@@ -914,40 +914,6 @@ __device__ __forceinline__ int join_regions_warp(Smem sm, int C, int rc, int lan
     return dst;
 }
 
-// The k-th largest order key among lv[0..n) (0 if n < k), by one warp: the largest t
-// with #{key >= t} >= k, built bit by bit from the top (a count is monotone in t, so
-// each bit is kept when the count at the raised threshold still reaches k).  The
-// result is a key present in the list.
-template <typename KEYF>
-__device__ __forceinline__ uint32_t kth_key_warp(Smem sm, int n, int k, KEYF keyf, int lane) {
-    if (n < k) return 0u;
-    uint32_t lo = 0xffffffffu, hi = 0u;
-#pragma unroll 1
-    for (int i = lane; i < n; i += 32) {
-        const uint32_t key = keyf(sm.lv()[i]);
-        lo = min(lo, key);
-        hi = max(hi, key);
-    }
-    lo = warp_min_u(lo);
-    hi = warp_max_u(hi);
-    // Every key shares the bits above the highest bit where lo and hi differ.
-    const int top = 31 - __clz(int(lo ^ hi) | 1);
-    uint32_t t = lo & ~((2u << top) - 1u);
-    if ((lo ^ hi) == 0u) return lo;
-#pragma unroll 1
-    for (int bit = top; bit >= 0; --bit) {
-        const uint32_t cand = t | (1u << bit);
-        int cnt = 0;
-#pragma unroll 1
-        for (int i0 = 0; i0 < n; i0 += 32) {
-            const int i = i0 + lane;
-            cnt += __popc(__ballot_sync(FULL, i < n && keyf(sm.lv()[i]) >= cand));
-        }
-        if (cnt >= k) t = cand;
-    }
-    return t;
-}
-
 // A candidate list of at most SMALL entries held by one warp in registers, lane-major:
 // entry e = SR * lane + r in slot r (x[r], i[r]); in[r] marks entries below n.
 constexpr int SR = 4;              // slots per lane
@@ -1072,52 +1038,176 @@ __device__ __forceinline__ int filter_list_warp(Smem sm, int n, uint32_t t, KEYF
     return w;
 }
 
-// Block-collective: a lower bound L0 <= t_k of the row's k-th largest order key from
-// the histogram of the segment maxima (key >> bshift).  Scanning from the top bin
-// down, the bin in which the count reaches k holds the k-th largest segment maximum,
-// and its lower edge is at most that value.  The k-th largest of any subset of the
-// row (here, the segment maxima) is at most the row's own k-th largest, so L0 <= t_k,
-// and every segment holding an element >= t_k has its maximum >= L0.  Warp 0 scans
-// 128 bins at a time from the bin of the row maximum `maxkey` down; the result is
-// broadcast through shared memory.  Returns 0 when there are fewer than k segments.
-__device__ __forceinline__ uint32_t hist_bound(Smem sm, int ns, int k, int bshift, uint32_t maxkey, int warp,
-                                               int lane) {
-    if (ns < k) return 0;
-    if (warp == 0) {
-        const uint32_t kk = uint32_t(k);
-        uint32_t before = 0;
-        int found = 0;
+// Warp-collective: scanning the bins h[top], h[top - 1], ... h[0] from the top down,
+// the first bin at which the running count reaches kk (-1 when it never does), and in
+// `above` the count of the bins scanned before it.  Lane l holds four consecutive bins
+// of each window of 128.
+__device__ __forceinline__ int scan_bins_down(const uint32_t* h, int top, uint32_t kk, int lane, uint32_t& above) {
+    uint32_t before = 0;
+    above = 0;
 #pragma unroll 1
-        for (int top = int(min(uint32_t(HBINS - 1), maxkey >> bshift)); top >= 0; top -= 128) {
-            // Lane l holds bins top - 4l, top - 4l - 1, ... (descending).
-            uint32_t c[4], own = 0;
+    for (; top >= 0; top -= 128) {
+        uint32_t c[4], own = 0;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int bin = top - 4 * lane - q;
-                c[q] = bin >= 0 ? sm.hist()[bin] : 0u;
+        for (int q = 0; q < 4; ++q) {
+            const int bin = top - 4 * lane - q;
+            c[q] = bin >= 0 ? h[bin] : 0u;
+            own += c[q];
+        }
+        const uint32_t incl = uint32_t(warp_incl_scan_i(int(own), lane));
+        const uint32_t total = __shfl_sync(FULL, incl, 31);
+        if (before + total >= kk) {
+            const uint32_t excl = before + incl - own;
+            const int l = __ffs(__ballot_sync(FULL, excl < kk && excl + own >= kk)) - 1;
+            uint32_t cum = excl;
+            int q = 0;  // the first of the lane's bins where the running count reaches kk
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                cum += c[t];
+                if (cum < kk) q = t + 1;
+            }
+            uint32_t ab = excl;
+#pragma unroll
+            for (int t = 0; t < 4; ++t) ab += t < q ? c[t] : 0u;
+            above = __shfl_sync(FULL, ab, l);
+            return __shfl_sync(FULL, top - 4 * lane - q, l);
+        }
+        before += total;
+    }
+    return -1;
+}
+
+// Block- and cluster-collective (every CTA of the cluster calls it with the same row,
+// k and histogram): a lower bound L <= t_k of the row's k-th largest order key from
+// the histogram of the segment maxima (key >> 21) that pass 1 left in every CTA.
+// Scanning from the bin of the row maximum `maxkey` down, the bin B in which the
+// count reaches k holds the k-th largest segment maximum, and its lower edge is at
+// most that value.  The k-th largest of any subset of the row (here, the segment
+// maxima) is at most the row's own k-th largest, so B's edge is <= t_k, and every
+// segment holding an element >= t_k has its maximum >= the edge.
+//
+// A bin spans a quarter of a binade, which for logits of a few units is several units
+// wide: when more than SMALL segment maxima are at or above B's edge, the bound is
+// refined inside B.  Each CTA counts its own segment maxima that fall in B by the key
+// bits 20..10 (in lv), adds the non-empty counts into every CTA's second histogram
+// (which is zero since the kernel cleared it before its first cluster barrier), and
+// after one cluster barrier every CTA scans B's 2048 sub-bins for the remaining k
+// minus the count above B: the same argument, at 1/2048 of the width.  lv is free:
+// no CTA writes candidates before the barrier.  Returns 0 when fewer than k
+// segments exist.
+__device__ __forceinline__ uint32_t hist_bound(Smem sm, Geom g, int rank, int C, int k, uint32_t maxkey, int warp,
+                                               int lane, int tid) {
+    if (g.ns < k) return 0;
+    const uint32_t* h = sm.hist();
+    if (warp == 0) {
+        uint32_t above;
+        const int B = scan_bins_down(h, int(maxkey >> 21), uint32_t(k), lane, above);
+        if (lane == 0) {
+            sm.bcast()[0] = max(B, 0);
+            sm.bcast()[1] = int(above);
+            sm.bcast()[2] = B >= 0 ? int(above + h[B]) : 0;
+        }
+    }
+    __syncthreads();
+    const uint32_t B = uint32_t(sm.bcast()[0]);
+    const int above = sm.bcast()[1];
+    const int at = sm.bcast()[2];
+    if (at <= SMALL) return B << 21;
+    // ---- refinement inside bin B
+    uint32_t* loc = reinterpret_cast<uint32_t*>(sm.lv());
+    uint32_t* h2 = sm.hist() + HBINS;
+#pragma unroll
+    for (int q = 0; q < HBINS / NT; ++q) loc[q * NT + tid] = 0u;
+    __syncthreads();
+#pragma unroll 1
+    for (int i = g.s0 + tid; i < g.s1; i += NT) {
+        const uint32_t key = sm.segkey()[i];
+        if ((key >> 21) == B) atomicAdd(&loc[(key >> 10) & (HBINS - 1)], 1u);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < HBINS / NT; ++q) {
+        const int bin = q * NT + tid;
+        const uint32_t n = loc[bin];
+        if (n) {
+#pragma unroll 1
+            for (int r = 0; r < C; ++r) {
+                if (r == rank) {
+                    atomicAdd(&h2[bin], n);
+                } else {
+                    asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(map_rank(smem_u32(&h2[bin]), uint32_t(r))),
+                                 "r"(n)
+                                 : "memory");
+                }
+            }
+        }
+    }
+    cluster_sync();  // every CTA's counts are in every second histogram
+    if (warp == 0) {
+        uint32_t above2;
+        const int top = (maxkey >> 21) == B ? int((maxkey >> 10) & (HBINS - 1)) : HBINS - 1;
+        const int b2 = scan_bins_down(h2, top, uint32_t(k - above), lane, above2);
+        if (lane == 0) sm.bcast()[3] = max(b2, 0);
+    }
+    __syncthreads();
+    return (B << 21) | (uint32_t(sm.bcast()[3]) << 10);
+}
+
+// Block-collective: the k-th largest order key of the list lv[0, n) (0 when n < k), by
+// a most-significant-digit radix select over 8-bit digits: each round counts the
+// keys that match the digits chosen so far into 256 counters (the histogram area of
+// shared memory), warp 0 finds the digit at which the count from the top reaches
+// the remaining rank, and the keys above that digit leave the rank.  The result is
+// the same key as the warp's bit-by-bit search: the largest t with
+// #{key >= t} >= k, which is a key of the list.
+template <typename KEYF>
+__device__ __forceinline__ uint32_t kth_key_cta(Smem sm, int n, int k, KEYF keyf, int warp, int lane, int tid) {
+    static_assert(NT == 256, "one counter per thread");
+    if (n < k) return 0u;
+    uint32_t* h = sm.hist();
+    uint32_t prefix = 0, pmask = 0, kk = uint32_t(k);
+#pragma unroll 1
+    for (int shift = 24; shift >= 0; shift -= 8) {
+        h[tid] = 0u;
+        __syncthreads();
+#pragma unroll 1
+        for (int i = tid; i < n; i += NT) {
+            const uint32_t key = keyf(sm.lv()[i]);
+            if ((key & pmask) == prefix) atomicAdd(&h[(key >> shift) & 255u], 1u);
+        }
+        __syncthreads();
+        if (warp == 0) {
+            uint32_t c[8], own = 0;  // lane l: digits 255 - 8l down to 248 - 8l
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                c[q] = h[255 - 8 * lane - q];
                 own += c[q];
             }
             const uint32_t incl = uint32_t(warp_incl_scan_i(int(own), lane));
-            const uint32_t total = __shfl_sync(FULL, incl, 31);
-            if (before + total >= kk) {
-                const bool cross = before + incl - own < kk && before + incl >= kk;
-                const int l = __ffs(__ballot_sync(FULL, cross)) - 1;
-                uint32_t cum = before + incl - own;
-                int q = 0;  // the first of the lane's bins where the running count reaches k
+            const uint32_t excl = incl - own;
+            const int l = __ffs(__ballot_sync(FULL, excl < kk && incl >= kk)) - 1;
+            uint32_t cum = excl, ab = excl;
+            int q = 0;
 #pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    cum += c[t];
-                    if (cum < kk) q = t + 1;
-                }
-                found = __shfl_sync(FULL, top - 4 * lane - q, l);
-                break;
+            for (int t = 0; t < 8; ++t) {
+                cum += c[t];
+                if (cum < kk) q = t + 1;
             }
-            before += total;
+#pragma unroll
+            for (int t = 0; t < 8; ++t) ab += t < q ? c[t] : 0u;
+            const int d = __shfl_sync(FULL, 255 - 8 * lane - q, l);
+            ab = __shfl_sync(FULL, ab, l);
+            if (lane == 0) {
+                sm.bcast()[0] = d;
+                sm.bcast()[1] = int(ab);
+            }
         }
-        if (lane == 0) *sm.bcast() = found;
+        __syncthreads();
+        prefix |= uint32_t(sm.bcast()[0]) << shift;
+        pmask |= 255u << shift;
+        kk -= uint32_t(sm.bcast()[1]);
     }
-    __syncthreads();
-    return uint32_t(*sm.bcast()) << bshift;
+    return prefix;
 }
 
 // ------------------------------------------------------------------ draws

@@ -117,6 +117,7 @@ __global__ void __launch_bounds__(NT, 4) filter_kernel(const FilterArgs a) {
     if (need_hist)
         for (int i = tid; i < HBINS; i += NT) {
             sm.hist()[i] = 0u;
+            sm.hist()[HBINS + i] = 0u;
             reinterpret_cast<uint32_t*>(sm.lv())[i] = 0u;
         }
     if (tid == 0) *sm.ctr() = NW;
@@ -148,7 +149,7 @@ __global__ void __launch_bounds__(NT, 4) filter_kernel(const FilterArgs a) {
     uint32_t L0 = 0u;
     int list_mode = -1;  // 0: regions fit, 1: contiguous, -1: no list
     if (k_on) {
-        L0 = need_hist ? hist_bound(sm, ns, k, 21, maxkey, warp, lane) : 0u;
+        L0 = need_hist ? hist_bound(sm, g, rank, C, k, maxkey, warp, lane, tid) : 0u;
         if (IS_PROB) L0 = max(L0, 1u);
         collect_own<VEC>(row, g, sm, leader, rank, C, rank * (CAP / C), CAP / C, L0, NO_LIMIT, keyf, true, true,
                          warp, lane, tid);
@@ -157,23 +158,32 @@ __global__ void __launch_bounds__(NT, 4) filter_kernel(const FilterArgs a) {
     }
     if (list_mode >= 0) {
         // Every element >= L0 (hence >= t) is in the list.
-        if (warp == 0) {
-            uint32_t t;
-            float s = 0.f;
-            if (regions_total(sm, C) <= SMALL) {  // the usual case: in registers
+        const int n = regions_total(sm, C);
+        if (n <= SMALL) {  // the usual case: in warp 0's registers
+            if (warp == 0) {
                 const Small sl = small_gather(sm, C, CAP / C, list_mode == 1, lane);
-                t = small_kth(sl, k, keyf);
+                const uint32_t t = small_kth(sl, k, keyf);
+                float s = 0.f;
 #pragma unroll
                 for (int r = 0; r < SR; ++r) s += sl.in[r] && keyf(sl.x[r]) >= t ? sl.x[r] : 0.f;
-            } else {
-                const int n = list_mode == 0 ? join_regions_warp(sm, C, CAP / C, lane) : regions_total(sm, C);
-                t = kth_key_warp(sm, n, k, keyf, lane);
-                for (int i = lane; i < n; i += 32) s += keyf(sm.lv()[i]) >= t ? sm.lv()[i] : 0.f;
+                s = warp_sum(s);
+                if (lane == 0) {
+                    sm.red()[40] = int(t);
+                    reinterpret_cast<float*>(sm.red())[41] = s;
+                }
             }
-            s = warp_sum(s);
-            if (lane == 0) {
-                sm.red()[40] = int(t);
-                reinterpret_cast<float*>(sm.red())[41] = s;
+        } else {  // a longer list: joined, then a radix select by the whole CTA
+            if (list_mode == 0 && warp == 0) join_regions_warp(sm, C, CAP / C, lane);
+            __syncthreads();
+            const uint32_t t = kth_key_cta(sm, n, k, keyf, warp, lane, tid);
+            if (warp == 0) {
+                float s = 0.f;
+                for (int i = lane; i < n; i += 32) s += keyf(sm.lv()[i]) >= t ? sm.lv()[i] : 0.f;
+                s = warp_sum(s);
+                if (lane == 0) {
+                    sm.red()[40] = int(t);
+                    reinterpret_cast<float*>(sm.red())[41] = s;
+                }
             }
         }
         __syncthreads();

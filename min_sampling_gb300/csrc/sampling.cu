@@ -348,6 +348,7 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
     if (need_hist)
         for (int i = tid; i < HBINS; i += NT) {
             sm.hist()[i] = 0u;
+            sm.hist()[HBINS + i] = 0u;
             reinterpret_cast<uint32_t*>(sm.lv())[i] = 0u;
         }
     if (tid == 0) *sm.ctr() = NW;
@@ -376,7 +377,7 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
     Totals tot;
     if (kfirst) {
         const uint32_t mk = warp_max_u(lane < C ? sm.part()[lane].u[2] : 0u);
-        L0 = max(1u, need_hist ? hist_bound(sm, ns, k, 21, mk, warp, lane) : 0u);
+        L0 = max(1u, need_hist ? hist_bound(sm, g, rank, C, k, mk, warp, lane, tid) : 0u);
         collect_own<VEC>(row, g, sm, leader, rank, C, rank * (CAP / C), CAP / C, L0, NO_LIMIT, keyf, false, true,
                          warp, lane, tid);
         if (leader) {  // the row's totals while the other CTAs finish their candidates
@@ -469,8 +470,9 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
             if (n >= 0) {
                 compact = true;
                 // The list holds every element >= L0, hence every element >= t_k.
+                __syncthreads();  // the joined list
+                const uint32_t tk = kth_key_cta(sm, n, k, keyf, warp, lane, tid);
                 if (warp == 0) {
-                    const uint32_t tk = kth_key_warp(sm, n, k, keyf, lane);
                     n_list = filter_list_warp(sm, n, tk, keyf, lane);
                     float s = 0.f;
                     for (int i = lane; i < n_list; i += 32) s += sm.lv()[i];

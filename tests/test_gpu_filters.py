@@ -207,3 +207,34 @@ def test_max_vocab_row(ms):
     _check_renorm(P, [100], out, valid, filters.top_k_renorm)
     out, valid = _run(ms, "top_p", P, [0.5])
     _check_renorm(P, [0.5], out, valid, filters.top_p_renorm)
+
+
+def _crowded_rows(V, seed):
+    """Rows whose top values crowd into a few quarter-binade bins of the segment-maximum
+    histogram, so that the coarse top-k bound admits more than 128 segments and is
+    refined inside its bin: logits 12 + N(0, 1) (all in [8, 16) but the far tails),
+    log-softmax logits of N(0, 3^2) (all negative), and near-flat probabilities
+    softmax(N(0, 0.05^2)) (all within a few percent of 1/V)."""
+    rng = np.random.default_rng([seed, V])
+    z1 = workloads.detie((12.0 + rng.normal(0, 1, V)).astype(np.float32), positive_only=False)[0]
+    z = rng.normal(0, 3, V)
+    z2 = workloads.detie((z - (np.log(np.sum(np.exp(z - z.max()))) + z.max())).astype(np.float32),
+                         positive_only=False)[0]
+    p3 = workloads.detie(workloads.softmax_fp32(rng.normal(0, 0.05, V)))[0]
+    return np.stack([z1, z2]), p3
+
+
+@pytest.mark.parametrize("k", [1, 50, 300, 900])
+def test_refined_bound_crowded_rows(ms, k):
+    """The refined top-k bound (second histogram inside the boundary bin) and, for
+    k = 300 and 900, candidate lists longer than the register path (the CTA's radix
+    select): masks and renormalised rows against the oracle."""
+    Z, p3 = _crowded_rows(151936, 5)
+    out, valid = _run(ms, "mask", Z, [k, k])
+    for i in range(2):
+        exp, ok = filters.top_k_mask_logits(Z[i], k)
+        assert ok and valid[i] and np.array_equal(out[i], exp), (k, i)
+    P = np.stack([workloads.detie(workloads.softmax_fp32(Z[0]))[0], p3])
+    out, valid = _run(ms, "top_k", P, [k, k])
+    _check_renorm(P, [k, k], out, valid, filters.top_k_renorm)
+    assert (np.count_nonzero(out, axis=1) == k).all()

@@ -378,3 +378,37 @@ def test_single_pivot_ablation(ms):
         assert agree >= 0.99 * 400, agree
     with pytest.raises(ms.FsError):
         ms.top_k_top_p_sampling_pivots(P, 10, 0.9, None, "joint", pivots=3, seed=1, offset=0)
+
+
+def test_refined_bound_and_long_list_law(ms):
+    """Top-k-first draws where the top-k bound is refined inside its histogram bin
+    (a near-flat row, k = 50) and where the candidate list is longer than the
+    register path (an N(0, 3^2) softmax row, k = 300, top-p 0.95): every draw in S,
+    TV <= 0.005 and chi-square p > 1e-3 against the oracle's filtered law."""
+    import torch
+    V = 151936
+    rng = np.random.default_rng([17, V])
+    flat = workloads.detie(workloads.softmax_fp32(rng.normal(0, 0.05, V)))[0]
+    acc = guard_accept(lambda i: [(300, 0.95, None, "top_k_first")])
+    steep = None
+    for att in range(64):
+        cand = workloads.detie(workloads.softmax_fp32(workloads.row_rng(18, 0, att).normal(0, 3, V)))[0]
+        if acc(0, cand):
+            steep = cand
+            break
+    assert steep is not None
+    P = np.stack([flat, steep])
+    Pt = _t(P, torch.float32)
+    for r, (k, p) in enumerate([(50, 1.0), (300, 0.95)]):
+        pt, ok = filters.filtered_distribution(P[r], k, p, None, "top_k_first")
+        assert ok
+        n = draws_for_tv(pt)
+        idx = np.full(n, r, np.int32)
+        tok, valid, rounds = _call(ms, "top_k_first", Pt, np.full(n, k, np.int32), np.full(n, p, np.float32),
+                                   None, indices=idx, seed=4321 + r, offset=3)
+        assert valid.all() and (tok >= 0).all()
+        assert (pt[tok] > 0).all(), "a draw outside S"
+        counts = np.bincount(tok, minlength=V).astype(np.float64)
+        tv = tv_distance(counts, pt)
+        assert tv <= 0.005, (r, tv, expected_null_tv(pt, n))
+        assert chi2_pvalue(counts, pt) > 1e-3, r
