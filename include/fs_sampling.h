@@ -218,10 +218,17 @@ fs_status fs_top_k_mask_logits(const float* logits, int32_t batch, int32_t vocab
                                uint8_t* out_valid, void* stream);
 
 /* The launch plan of the sampling kernels for `batch_out` rows of `vocab` elements on
- * the current device: CTAs per row (*cluster), elements per segment and segments per
- * CTA.  Host only; nothing is launched. */
-fs_status fs_sampling_plan(int32_t batch_out, int32_t vocab, int32_t* cluster, int32_t* segment_len,
-                           int32_t* segments_per_cta);
+ * the current device.  order = FS_ORDER_TOP_K_FIRST gives the plan of the
+ * top-k-first entries (fs_top_k_top_p_sampling*, order top-k-first) and of
+ * fs_sampling_from_probs, which stream each row about once; FS_ORDER_JOINT that of
+ * the joint order and of fs_top_k_sampling, fs_top_p_sampling and fs_min_p_sampling,
+ * whose rejection rounds pass over the row several times.  Outputs (host pointers):
+ * CTAs per row (*cluster), elements per segment, segments per CTA and the most CTAs
+ * resident on one SM (*ctas_per_sm; below the occupancy limit when the plan caps it
+ * through its shared-memory request).  Host only; nothing is launched.
+ * FS_ERR_INVALID_ARG: batch_out or vocab < 1, a null output, an unknown order. */
+fs_status fs_sampling_plan(int32_t batch_out, int32_t vocab, int32_t order, int32_t* cluster,
+                           int32_t* segment_len, int32_t* segments_per_cta, int32_t* ctas_per_sm);
 
 /* The counter-based generator the samplers draw from, exposed for checking:
  * out[4i..4i+3] = Philox4x32-10(counter = ctr[4i..4i+3], key = key[2i..2i+1]).

@@ -43,8 +43,8 @@ _SIGNATURES = {
     "fs_top_k_top_p_sampling_rng": [_P, _I32, _I32, _P, _I32, _P, _P, _P, _I32, _P, _P, _P, _U64, _U64, _P, _P, _P,
                                     _P],
     "fs_advance_offset": [_P, _U64, _P],
-    "fs_sampling_plan": [_I32, _I32, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
-                         ctypes.POINTER(ctypes.c_int32)],
+    "fs_sampling_plan": [_I32, _I32, _I32, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
+                         ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)],
     "fs_top_k_top_p_sampling_from_logits": [_P, _I32, _I32, _P, _I32, _P, _P, _P, _P, _I32, _U64, _U64, _P, _P, _P,
                                             _P],
     "fs_top_k_top_p_sampling_pivots": [_P, _I32, _I32, _P, _I32, _P, _P, _P, _I32, _I32, _U64, _U64, _P, _P, _P,
@@ -273,11 +273,15 @@ def top_k_top_p_sampling_from_logits(logits, temperature=None, top_k=None, top_p
     return (tok, valid, rounds) if return_rounds else (tok, valid)
 
 
-def sampling_plan(batch_out: int, vocab: int) -> dict:
-    """CTAs per row, elements per segment and segments per CTA the samplers use."""
-    vals = [ctypes.c_int32(0) for _ in range(3)]
-    _check(_lib().fs_sampling_plan(int(batch_out), int(vocab), *[ctypes.byref(v) for v in vals]))
-    return {"cluster": vals[0].value, "segment_len": vals[1].value, "segments_per_cta": vals[2].value}
+def sampling_plan(batch_out: int, vocab: int, order: str = "top_k_first") -> dict:
+    """CTAs per row, elements per segment, segments per CTA and CTAs per SM (at most)
+    of the samplers' launch: order "top_k_first" for the top-k-first entries and
+    sampling_from_probs, "joint" for the joint order and the top-k / top-p / min-p
+    samplers."""
+    vals = [ctypes.c_int32(0) for _ in range(4)]
+    _check(_lib().fs_sampling_plan(int(batch_out), int(vocab), _order(order), *[ctypes.byref(v) for v in vals]))
+    return {"cluster": vals[0].value, "segment_len": vals[1].value, "segments_per_cta": vals[2].value,
+            "ctas_per_sm": vals[3].value}
 
 
 def advance_offset(offset_dev, delta: int = 1) -> None:

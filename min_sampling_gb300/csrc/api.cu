@@ -1,5 +1,6 @@
 // Status strings, launch planning and the Philox entry point.
 #include <cstdio>
+#include <algorithm>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -101,7 +102,64 @@ static fs_status active_clusters(const void* fn, size_t smem, int C, int& n) {
     return FS_OK;
 }
 
-fs_status make_plan(int rows, int vocab, const void* fn, Plan& p) {
+// Shared memory of one SM and the per-CTA reservation (cached per device).
+static fs_status smem_per_sm(int& per_sm, int& reserved) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    static std::mutex mu;
+    static std::map<int, std::pair<int, int>> cache;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(dev);
+    if (it == cache.end()) {
+        int a = 0, b = 0;
+        e = cudaDeviceGetAttribute(&a, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+        if (e != cudaSuccess) return cuda_fail(e);
+        e = cudaDeviceGetAttribute(&b, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+        if (e != cudaSuccess) return cuda_fail(e);
+        it = cache.insert({dev, {a, b}}).first;
+    }
+    per_sm = it->second.first;
+    reserved = it->second.second;
+    return FS_OK;
+}
+
+// The launch plan of `fn` for `rows` rows of `vocab` values.  The row-wide tables fix
+// the shared memory a CTA needs.
+//
+// Kernels that stream the row about once (`single_pass`: the top-k-first samplers,
+// sampling without filters, the top-k renormaliser and the logit mask) follow
+// measurements of the top-k-first sampler on GB300 over 8..192 rows of 32000 to
+// 256000 values: the fastest plans keep about 2.5 CTAs per SM (C near 2.5 x SMs /
+// rows) with at most 3 CTAs per SM (a cap below the occupancy limit is enforced by
+// asking for more shared memory than a 4th CTA leaves room for: with 4 per SM
+// allowed, the block scheduler stacks 4 on some SMs and those SMs set the pass
+// time), and clusters above 12 CTAs only pay off for 4 rows or fewer.  So C starts
+// at ceil(2.5 x SMs / rows), capped at 12 (16 up to 4 rows), and steps down until
+// all clusters are resident at once (one wave) at 3 per SM, else at the occupancy
+// limit.
+//
+// Kernels that pass over the row several times with the whole cluster (rejection
+// rounds of the joint order, top-p threshold searches) gain more from CTAs per row
+// than from balance: the largest C (at most 16) whose clusters are all resident at
+// the occupancy limit.
+//
+// C = 1 at the occupancy limit when no cluster size fits in one wave.  Plans are
+// cached per (kernel, device, rows, vocab, kind).
+fs_status make_plan(int rows, int vocab, const void* fn, bool single_pass, Plan& p) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    static std::mutex mu;
+    static std::map<std::tuple<const void*, int, int, int, bool>, Plan> cache;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cache.find({fn, dev, rows, vocab, single_pass});
+        if (it != cache.end()) {
+            p = it->second;
+            return FS_OK;
+        }
+    }
     int sms = 0;
     size_t optin = 0;
     fs_status st = device_limits(sms, optin);
@@ -110,25 +168,56 @@ fs_status make_plan(int rows, int vocab, const void* fn, Plan& p) {
     if (st != FS_OK) return st;
     p.shift = seg_shift_for(vocab);
     p.ns = (vocab + (BLK << p.shift) - 1) / (BLK << p.shift);
-    p.smem = Layout(p.ns).total();   // row-wide tables in every CTA
-    if (p.smem > optin) return FS_ERR_UNSUPPORTED;
-    // Largest C (<= MAX_CLUSTER, >= 4 segments per CTA) whose clusters are all
-    // resident at once (one wave); C = 1 when none is.
-    int cmax = p.ns / 4;
+    const size_t need = Layout(p.ns).total();   // row-wide tables in every CTA
+    if (need > optin) return FS_ERR_UNSUPPORTED;
+    int per_sm = 0, reserved = 0;
+    st = smem_per_sm(per_sm, reserved);
+    if (st != FS_OK) return st;
+    int natural = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&natural, fn, NT, need);
+    if (e != cudaSuccess) return cuda_fail(e);
+    int cmax = p.ns / 4;   // >= 4 segments per CTA
     if (cmax > MAX_CLUSTER) cmax = MAX_CLUSTER;
-    if (cmax < 1) cmax = 1;
-    int chosen = 1;
-    for (int C = cmax; C >= 2; --C) {
-        int n = 0;
-        st = active_clusters(fn, p.smem, C, n);
-        if (st != FS_OK) return st;
-        if (rows <= n) {
-            chosen = C;
-            break;
+    auto nsc_of = [&](int C) { return ((p.ns + C - 1) / C + 3) & ~3; };   // a multiple of 4
+    p.C = 1;
+    p.smem = need;
+    if (single_pass) {
+        if (rows > 4 && cmax > 12) cmax = 12;
+        int c0 = int((5L * sms + 2L * rows - 1) / (2L * rows));   // ceil(2.5 x SMs / rows)
+        if (c0 > cmax) c0 = cmax;
+        // The smallest request (a multiple of 16 bytes) that leaves no room for a 4th CTA.
+        const size_t smem3 = std::max(need, (size_t(per_sm / 4 - reserved) + 16) & ~size_t(15));
+        const bool cap3 = natural > 3 && smem3 <= optin;
+        bool done = false;
+        for (int C = c0; C >= 2 && !done; --C) {
+            for (int pass = cap3 ? 0 : 1; pass < 2 && !done; ++pass) {
+                const size_t smem = pass == 0 ? smem3 : need;
+                int n = 0;
+                st = active_clusters(fn, smem, C, n);
+                if (st != FS_OK) return st;
+                if (rows <= n) {
+                    p.C = C;
+                    p.smem = smem;
+                    done = true;
+                }
+            }
+        }
+    } else {
+        for (int C = cmax; C >= 2; --C) {
+            int n = 0;
+            st = active_clusters(fn, need, C, n);
+            if (st != FS_OK) return st;
+            if (rows <= n) {
+                p.C = C;
+                break;
+            }
         }
     }
-    p.C = chosen;
-    p.nsc = ((p.ns + chosen - 1) / chosen + 3) & ~3;   // a multiple of 4 segments per CTA
+    p.nsc = nsc_of(p.C);
+    p.per_sm = p.C == 1 ? natural : int(per_sm / (p.smem + reserved));
+    if (p.per_sm > natural) p.per_sm = natural;
+    std::lock_guard<std::mutex> lock(mu);
+    cache[{fn, dev, rows, vocab, single_pass}] = p;
     return FS_OK;
 }
 

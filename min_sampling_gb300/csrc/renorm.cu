@@ -245,7 +245,7 @@ static fs_status launch_filter(const float* in, int32_t batch, int32_t vocab, co
     const void* fn = vec ? reinterpret_cast<const void*>(filter_kernel<true, KIND>)
                          : reinterpret_cast<const void*>(filter_kernel<false, KIND>);
     Plan p;
-    fs_status st = make_plan(batch, vocab, fn, p);
+    fs_status st = make_plan(batch, vocab, fn, KIND != K_TOPP, p);
     if (st != FS_OK) return st;
     FilterArgs a;
     a.in = in;

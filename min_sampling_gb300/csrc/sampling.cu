@@ -630,8 +630,10 @@ static fs_status launch_sample(const float* probs, int32_t batch_in, int32_t voc
                                  : reinterpret_cast<const void*>(sample_kernel<false, true>))
                           : (vec ? reinterpret_cast<const void*>(sample_kernel<true, false>)
                                  : reinterpret_cast<const void*>(sample_kernel<false, false>));
+    // One streaming pass per row: the top-k-first order, and sampling without filters.
+    const bool single_pass = (order == FS_ORDER_TOP_K_FIRST && top_k) || (!top_k && !top_p && !min_p);
     Plan p;
-    fs_status st = make_plan(batch_out, vocab, fn, p);
+    fs_status st = make_plan(batch_out, vocab, fn, single_pass, p);
     if (st != FS_OK) return st;
     SampleArgs a;
     a.probs = probs;
@@ -749,16 +751,20 @@ fs_status fs_top_k_top_p_sampling_from_logits(const float* logits, int32_t batch
                               temperature);
 }
 
-fs_status fs_sampling_plan(int32_t batch_out, int32_t vocab, int32_t* cluster, int32_t* segment_len,
-                           int32_t* segments_per_cta) {
-    if (batch_out < 1 || vocab < 1 || !cluster || !segment_len || !segments_per_cta) return FS_ERR_INVALID_ARG;
+fs_status fs_sampling_plan(int32_t batch_out, int32_t vocab, int32_t order, int32_t* cluster,
+                           int32_t* segment_len, int32_t* segments_per_cta, int32_t* ctas_per_sm) {
+    if (batch_out < 1 || vocab < 1 || !cluster || !segment_len || !segments_per_cta || !ctas_per_sm)
+        return FS_ERR_INVALID_ARG;
+    if (order != FS_ORDER_TOP_K_FIRST && order != FS_ORDER_JOINT) return FS_ERR_INVALID_ARG;
     if (vocab > FS_MAX_VOCAB) return FS_ERR_UNSUPPORTED;
     fsd::Plan p;
-    const fs_status st = fsd::make_plan(batch_out, vocab, reinterpret_cast<const void*>(fsd::sample_kernel<true, false>), p);
+    const fs_status st = fsd::make_plan(batch_out, vocab, reinterpret_cast<const void*>(fsd::sample_kernel<true, false>),
+                                       order == FS_ORDER_TOP_K_FIRST, p);
     if (st != FS_OK) return st;
     *cluster = p.C;
     *segment_len = fsd::BLK << p.shift;
     *segments_per_cta = p.nsc;
+    *ctas_per_sm = p.per_sm;
     return FS_OK;
 }
 

@@ -412,3 +412,28 @@ def test_refined_bound_and_long_list_law(ms):
         tv = tv_distance(counts, pt)
         assert tv <= 0.005, (r, tv, expected_null_tv(pt, n))
         assert chi2_pvalue(counts, pt) > 1e-3, r
+
+
+@pytest.mark.parametrize("V", [32000, 151936, 256000])
+def test_launch_plan_fits_one_wave(ms, V):
+    """The launch plans of both kinds: a cluster of 1..16 CTAs covering the row's
+    segments, at most the occupancy limit of CTAs per SM, every cluster resident at
+    once whenever C > 1 (rows x C <= SMs x CTAs per SM), and the multi-pass kind
+    never with fewer CTAs per row than the single-pass kind."""
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for B in (1, 8, 32, 64, 128, 192, 256, 4096):
+        plans = {}
+        for order in ("top_k_first", "joint"):
+            pl = ms.sampling_plan(B, V, order)
+            C, per_sm = pl["cluster"], pl["ctas_per_sm"]
+            assert 1 <= C <= 16 and 1 <= per_sm <= 8, pl
+            assert C * pl["segments_per_cta"] * pl["segment_len"] >= V, pl
+            assert pl["segments_per_cta"] % 4 == 0
+            if C > 1:
+                assert B * C <= sms * per_sm, (B, pl)
+            assert ms.sampling_plan(B, V, order) == pl   # cached, stable
+            plans[order] = pl
+        assert plans["joint"]["cluster"] >= plans["top_k_first"]["cluster"], plans
+    with pytest.raises(ValueError):
+        ms.sampling_plan(8, V, "sorted")
