@@ -146,7 +146,7 @@ static fs_status smem_per_sm(int& per_sm, int& reserved) {
 //
 // C = 1 at the occupancy limit when no cluster size fits in one wave.  Plans are
 // cached per (kernel, device, rows, vocab, kind).
-fs_status make_plan(int rows, int vocab, const void* fn, bool single_pass, Plan& p) {
+fs_status make_plan(int rows, int vocab, const void* fn, bool single_pass, Plan& p, bool topp_hist) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -168,7 +168,8 @@ fs_status make_plan(int rows, int vocab, const void* fn, bool single_pass, Plan&
     if (st != FS_OK) return st;
     p.shift = seg_shift_for(vocab);
     p.ns = (vocab + (BLK << p.shift) - 1) / (BLK << p.shift);
-    const size_t need = Layout(p.ns).total();   // row-wide tables in every CTA
+    // row-wide tables in every CTA (and the top-p histograms of that filter)
+    const size_t need = topp_hist ? Layout(p.ns).topp_total() : Layout(p.ns).total();
     if (need > optin) return FS_ERR_UNSUPPORTED;
     int per_sm = 0, reserved = 0;
     st = smem_per_sm(per_sm, reserved);

@@ -100,6 +100,19 @@ struct Layout {
     __host__ __device__ size_t li() const { return lv() + size_t(CAP) * 4; }
     __host__ __device__ size_t stage() const { return li() + size_t(CAP) * 4; }
     __host__ __device__ size_t total() const { return stage() + size_t(NW) * 2 * SBH * BLK * 4; }
+    // Top-p histograms (filter kernels only, after pass 1): two receive buffers of
+    // TOPPW 64-bit words (HBINS bins and two totals) over the per-segment arrays from
+    // arr(1) on (the masses and the live list, unused on that path), and a local one
+    // in the staging buffers, or after the receive buffers when those reach into them.
+    static constexpr size_t TOPPW = HBINS + 2;
+    __host__ __device__ size_t topp_recv(int i) const { return arr(1) + size_t(i) * TOPPW * 8; }
+    __host__ __device__ size_t topp_local() const {
+        return topp_recv(2) <= stage() ? stage() : topp_recv(2);
+    }
+    __host__ __device__ size_t topp_total() const {
+        const size_t end = topp_local() + TOPPW * 8;
+        return end > total() ? end : total();
+    }
 };
 
 extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -125,6 +138,12 @@ struct Smem {
     // [HBINS] aliases the staging buffers: written (by every CTA) and read before any staging
     __device__ __forceinline__ uint32_t* hist() const { return at<uint32_t>(Layout(ns).stage()); }
     __device__ __forceinline__ float* stage() const { return at<float>(Layout(ns).stage()); }
+    __device__ __forceinline__ unsigned long long* topp_recv(int i) const {
+        return at<unsigned long long>(Layout(ns).topp_recv(i));
+    }
+    __device__ __forceinline__ unsigned long long* topp_local() const {
+        return at<unsigned long long>(Layout(ns).topp_local());
+    }
 };
 
 // The row, its segmentation and this CTA's share.  Segment indices are row-wide.
@@ -314,6 +333,11 @@ __device__ __forceinline__ void stage4(float* dst, const float* __restrict__ row
 
 // ------------------------------------------------------------------ warp / block helpers
 
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
+#pragma unroll
+    for (int m = 16; m; m >>= 1) v += __shfl_xor_sync(FULL, v, m);
+    return v;
+}
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int m = 16; m; m >>= 1) v += __shfl_xor_sync(FULL, v, m);
@@ -372,6 +396,20 @@ __device__ __forceinline__ int block_sum_warp_values(int v, int* red, int warp, 
 // non-negative floats the integer order of the pattern is the numeric order
 // ([drill] section 3).
 __device__ __forceinline__ uint32_t prob_key(float x) { return x > 0.f ? __float_as_uint(x) : 0u; }
+
+// x * 2^sh rounded to the nearest integer (halves up), for x >= 0, computed from the
+// bits of x (x = m * 2^(e - 150) with the implicit bit in m; subnormals have e = 1 and
+// no implicit bit).  The caller keeps x * 2^sh below 2^63, so m << s fits.
+__device__ __forceinline__ unsigned long long fixed_point(float x, int sh) {
+    const uint32_t b = __float_as_uint(x);
+    int e = int(b >> 23);
+    unsigned long long m = b & 0x7fffffu;
+    if (e) m |= 0x800000u; else e = 1;
+    const int s = e - 150 + sh;
+    if (s >= 0) return m << s;
+    if (s < -25) return 0ull;  // below one half
+    return (m + (1ull << (-s - 1))) >> (-s);
+}
 
 // Order-preserving key of a signed float ([drill] section 8: negative patterns sort
 // backwards, so they are flipped; non-negative ones get the sign bit set).
@@ -1038,37 +1076,52 @@ __device__ __forceinline__ int filter_list_warp(Smem sm, int n, uint32_t t, KEYF
     return w;
 }
 
+// Warp-collective inclusive prefix sum of 64-bit words.
+__device__ __forceinline__ unsigned long long warp_incl_scan_u64(unsigned long long v, int lane) {
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const unsigned long long o = __shfl_up_sync(FULL, v, d);
+        if (lane >= d) v += o;
+    }
+    return v;
+}
+__device__ __forceinline__ uint32_t warp_incl_scan_t(uint32_t v, int lane) { return uint32_t(warp_incl_scan_i(int(v), lane)); }
+__device__ __forceinline__ unsigned long long warp_incl_scan_t(unsigned long long v, int lane) {
+    return warp_incl_scan_u64(v, lane);
+}
+
 // Warp-collective: scanning the bins h[top], h[top - 1], ... h[0] from the top down,
-// the first bin at which the running count reaches kk (-1 when it never does), and in
-// `above` the count of the bins scanned before it.  Lane l holds four consecutive bins
-// of each window of 128.
-__device__ __forceinline__ int scan_bins_down(const uint32_t* h, int top, uint32_t kk, int lane, uint32_t& above) {
-    uint32_t before = 0;
+// the first bin at which the running count (or mass) reaches kk (-1 when it never
+// does), and in `above` the sum of the bins scanned before it.  Lane l holds four
+// consecutive bins of each window of 128.
+template <typename T>
+__device__ __forceinline__ int scan_bins_down(const T* h, int top, T kk, int lane, T& above) {
+    T before = 0;
     above = 0;
 #pragma unroll 1
     for (; top >= 0; top -= 128) {
-        uint32_t c[4], own = 0;
+        T c[4], own = 0;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int bin = top - 4 * lane - q;
-            c[q] = bin >= 0 ? h[bin] : 0u;
+            c[q] = bin >= 0 ? h[bin] : T(0);
             own += c[q];
         }
-        const uint32_t incl = uint32_t(warp_incl_scan_i(int(own), lane));
-        const uint32_t total = __shfl_sync(FULL, incl, 31);
+        const T incl = warp_incl_scan_t(own, lane);
+        const T total = __shfl_sync(FULL, incl, 31);
         if (before + total >= kk) {
-            const uint32_t excl = before + incl - own;
+            const T excl = before + incl - own;
             const int l = __ffs(__ballot_sync(FULL, excl < kk && excl + own >= kk)) - 1;
-            uint32_t cum = excl;
-            int q = 0;  // the first of the lane's bins where the running count reaches kk
+            T cum = excl;
+            int q = 0;  // the first of the lane's bins where the running sum reaches kk
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
                 cum += c[t];
                 if (cum < kk) q = t + 1;
             }
-            uint32_t ab = excl;
+            T ab = excl;
 #pragma unroll
-            for (int t = 0; t < 4; ++t) ab += t < q ? c[t] : 0u;
+            for (int t = 0; t < 4; ++t) ab += t < q ? c[t] : T(0);
             above = __shfl_sync(FULL, ab, l);
             return __shfl_sync(FULL, top - 4 * lane - q, l);
         }
@@ -1101,7 +1154,7 @@ __device__ __forceinline__ uint32_t hist_bound(Smem sm, Geom g, int rank, int C,
     const uint32_t* h = sm.hist();
     if (warp == 0) {
         uint32_t above;
-        const int B = scan_bins_down(h, int(maxkey >> 21), uint32_t(k), lane, above);
+        const int B = scan_bins_down<uint32_t>(h, int(maxkey >> 21), uint32_t(k), lane, above);
         if (lane == 0) {
             sm.bcast()[0] = max(B, 0);
             sm.bcast()[1] = int(above);
@@ -1146,7 +1199,7 @@ __device__ __forceinline__ uint32_t hist_bound(Smem sm, Geom g, int rank, int C,
     if (warp == 0) {
         uint32_t above2;
         const int top = (maxkey >> 21) == B ? int((maxkey >> 10) & (HBINS - 1)) : HBINS - 1;
-        const int b2 = scan_bins_down(h2, top, uint32_t(k - above), lane, above2);
+        const int b2 = scan_bins_down<uint32_t>(h2, top, uint32_t(k - above), lane, above2);
         if (lane == 0) sm.bcast()[3] = max(b2, 0);
     }
     __syncthreads();

@@ -28,7 +28,7 @@ fs_status device_limits(int& sm_count, size_t& smem_optin);
 // Choose the cluster size for `rows` rows of `vocab` elements so that the whole grid
 // is resident at once (rows <= the device's resident clusters of that size for `fn`),
 // with at most MAX_CLUSTER CTAs per row and at least four segments per CTA.
-fs_status make_plan(int rows, int vocab, const void* fn, bool single_pass, Plan& p);
+fs_status make_plan(int rows, int vocab, const void* fn, bool single_pass, Plan& p, bool topp_hist = false);
 
 // Opt the kernel into the device's maximum dynamic shared memory (once per device).
 fs_status prepare_kernel(const void* fn);

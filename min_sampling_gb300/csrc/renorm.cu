@@ -10,8 +10,10 @@
 //            elements at or above it gathered into rank 0's list, and t counted
 //            exactly among them; a bisection on the key takes over when they do not
 //            fit on chip.
-//            top-p: bisection on the key with three pivots per pass, each interval
-//            shrunk to the keys that exist in it;
+//            top-p: a histogram of integer masses over the key's top 11 bits picks
+//            the bin where the prefix mass crosses top_p * M, the elements of that
+//            bin are gathered to rank 0, which finishes with two radix rounds over
+//            them (topp_threshold);
 //   write    keep key >= t (x / kept mass, or the logit), else 0 / -inf.  Segments
 //            whose maximum is below t are written without being read.
 #include <type_traits>
@@ -90,6 +92,361 @@ __device__ __forceinline__ void filter_peer(const float* __restrict__ row, float
     }
 }
 
+// Add the non-zero words of the local histogram L[0, nb) into every CTA's copy of R.
+__device__ __forceinline__ void push_bins_u64(const unsigned long long* L, unsigned long long* R, int nb, int rank,
+                                              int C, int tid) {
+#pragma unroll 1
+    for (int bin = tid; bin < nb; bin += NT) {
+        const unsigned long long v = L[bin];
+        if (!v) continue;
+#pragma unroll 1
+        for (int r = 0; r < C; ++r) {
+            if (r == rank) {
+                atomicAdd(&R[bin], v);
+            } else {
+                asm volatile("red.shared::cluster.add.u64 [%0], %1;" ::"r"(map_rank(smem_u32(&R[bin]), uint32_t(r))),
+                             "l"(v)
+                             : "memory");
+            }
+        }
+    }
+}
+
+// Add the 32-bit words of the local histogram L[0, nb) into every CTA's copy of R.
+__device__ __forceinline__ void push_bins_u32(const uint32_t* L, uint32_t* R, int nb, int rank, int C, int tid) {
+#pragma unroll 1
+    for (int bin = tid; bin < nb; bin += NT) {
+        const uint32_t v = L[bin];
+        if (!v) continue;
+#pragma unroll 1
+        for (int r = 0; r < C; ++r) {
+            if (r == rank) {
+                atomicAdd(&R[bin], v);
+            } else {
+                asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(map_rank(smem_u32(&R[bin]), uint32_t(r))),
+                             "r"(v)
+                             : "memory");
+            }
+        }
+    }
+}
+
+constexpr int TOPP_LIST = 2048;  // entries of the leader's list of crossing-bin elements
+
+// Exact 64-bit histogram passes over the keys of the window [lo, hi), narrowing it to
+// the key where the prefix mass from the top reaches the target: the fallback of
+// topp_threshold when the crossing bin holds more elements than the leader's list.
+// Masses x * 2^sh are rounded to integers, with the row maximum below 2^42 (the row's
+// sum stays below 2^63); the first pass also sums, in registers, the row total (the
+// target is ceil(top_p * total)) and the mass above the window.  Each pass keeps the
+// bin where the prefix reaches the target, until a bin is one key wide.  Block- and
+// cluster-collective; both receive buffers are zero on entry and no CTA adds to them
+// before the cluster barrier that precedes the call.
+template <bool VEC>
+__device__ __forceinline__ void topp_exact_levels(const float* __restrict__ row, Geom g, Smem sm, int rank, int C,
+                                                  uint32_t maxkey, float tp, unsigned long long lo,
+                                                  unsigned long long hi, int warp, int lane, int tid, uint32_t& t_out,
+                                                  float& denom_out) {
+    using u64 = unsigned long long;
+    constexpr int TW = int(Layout::TOPPW);
+    u64* L = sm.topp_local();
+    u64* b64 = reinterpret_cast<u64*>(sm.red() + 64);  // [6] broadcast words
+    const int sh = 168 - int((maxkey >> 23) & 255u);     // the maximum * 2^sh < 2^42
+    u64 A = 0, T = 1;  // the mass above the window, the target
+    uint32_t t = uint32_t(lo);
+    u64 kept = 0;
+#pragma unroll 1
+    for (int lev = 0; lev < 4; ++lev) {
+        const bool first = lev == 0;
+        int lw = 0;
+        while (((hi - lo + (1ull << lw) - 1) >> lw) > u64(HBINS)) ++lw;
+        const int nb = int((hi - lo + (1ull << lw) - 1) >> lw);
+        u64* R = sm.topp_recv(lev & 1);
+        for (int i = tid; i < TW; i += NT) L[i] = 0ull;
+        __syncthreads();
+        u64 a_above = 0, a_total = 0;
+        const uint32_t live_lo = first ? 1u : uint32_t(lo);
+        stream_warp<VEC, true>(
+            row, g, sm, warp, lane, [&](int sg) { return sm.segkey()[sg] >= live_lo; },
+            [&](int, int, bool on, const float4& v, int) {
+                if (!on) return;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float x = q_at(v, q);
+                    const u64 key = prob_key(x);
+                    if (first) {
+                        const u64 m = fixed_point(x, sh);
+                        a_total += m;
+                        if (key >= hi) a_above += m;
+                    }
+                    if (key >= lo && key < hi) atomicAdd(&L[(key - lo) >> lw], fixed_point(x, sh));
+                }
+            });
+        if (first) {
+            a_above = warp_sum_u64(a_above);
+            a_total = warp_sum_u64(a_total);
+            if (lane == 0) {
+                atomicAdd(&L[HBINS], a_above);
+                atomicAdd(&L[HBINS + 1], a_total);
+            }
+        }
+        __syncthreads();
+        push_bins_u64(L, R, nb, rank, C, tid);
+        if (first) push_bins_u64(L + HBINS, R + HBINS, 2, rank, C, tid);
+        if (lev >= 1)  // the other buffer, for the next pass: read before this pass began
+            for (int i = tid; i < TW; i += NT) sm.topp_recv((lev + 1) & 1)[i] = 0ull;
+        cluster_sync();  // this pass's sums in every R
+        if (warp == 0) {
+            if (first) {
+                const u64 total = R[HBINS + 1];
+                A = R[HBINS];
+                if (tp > 0.f) {
+                    const double tt = ceil(double(tp) * double(total));
+                    T = tt < 1.0 ? 1ull : u64(tt);
+                }
+            }
+            const int top = int(min(u64(nb - 1), (u64(maxkey) - lo) >> lw));
+            u64 above;
+            const int j = max(0, scan_bins_down<u64>(R, top, T > A ? T - A : 1ull, lane, above));
+            if (lane == 0) {
+                const u64 nlo = lo + (u64(j) << lw);
+                b64[0] = nlo;
+                b64[1] = min(hi, nlo + (1ull << lw));
+                b64[2] = A + above;
+                b64[3] = T;
+                b64[4] = A + above + R[j];
+                b64[5] = lw == 0 ? 1ull : 0ull;
+            }
+        }
+        __syncthreads();
+        lo = b64[0];
+        hi = b64[1];
+        A = b64[2];
+        T = b64[3];
+        t = uint32_t(lo);
+        kept = b64[4];
+        if (b64[5]) break;
+        __syncthreads();  // b64 is rewritten by the next pass
+    }
+    t_out = t;
+    denom_out = float(double(kept) * ldexp(1.0, -sh));
+}
+
+// Block- and cluster-collective top-p threshold of a valid row of probabilities: the
+// largest key t with mass(key >= t) >= top_p * M ([drill] section 4; top_p <= 0 keeps
+// the maximum alone).  Returns t and the kept mass, the same in every CTA.
+//   level 0   every CTA counts its share of the row (which pass 1 left in L2) into
+//             bins of key bits 31..21 with 32-bit masses x * 2^s rounded to integers
+//             (M * 2^s < 2^31, so no sum overflows; integer sums do not depend on the
+//             order of the additions) and adds them into every CTA's copy; every CTA
+//             then picks the bin B where the prefix mass from the top reaches
+//             top_p times the row's sum of those masses.
+//   collect   every CTA sums (fp32, in its own fixed order) its elements above B and
+//             appends the elements inside B, as (key, x * 2^sh rounded, the maximum *
+//             2^sh < 2^42), to the leader's list (slots reserved per warp with one
+//             cluster-shared atomic).
+//   finish    the leader: the mass above B (the CTAs' sums added in rank order) and
+//             the target top_p * M, in units of 2^-sh, then two radix rounds over the
+//             list (key bits 20..10, then 9..0) with 64-bit mass histograms; the
+//             result goes to every CTA before one cluster barrier.  If rounding put
+//             the target outside B's range of masses, the crossing is at B's edge:
+//             t = the key above B (the target was reached there) or B's lowest key.
+// When B holds more elements than the list, every CTA runs topp_exact_levels on B.
+// The receive buffers are zero on entry (cleared before the cluster barrier after
+// pass 1), and so is the leader's list count, red[100].
+template <bool VEC>
+__device__ __forceinline__ void topp_threshold(const float* __restrict__ row, Geom g, Smem sm, bool leader, int rank,
+                                               int C, uint32_t maxkey, float M, float tp, int warp, int lane, int tid,
+                                               uint32_t& t_out, float& denom_out) {
+    using u64 = unsigned long long;
+    constexpr int TW = int(Layout::TOPPW);
+    u64* L = sm.topp_local();
+    u64* b64 = reinterpret_cast<u64*>(sm.red() + 64);  // [6] broadcast words
+    uint32_t* list_n = reinterpret_cast<uint32_t*>(sm.red() + 100);
+    u64* list_q = sm.topp_recv(0);                                                      // [TOPP_LIST] masses
+    uint32_t* list_k = reinterpret_cast<uint32_t*>(sm.topp_recv(1)) + HBINS;            // [TOPP_LIST] keys
+    uint32_t* R32 = reinterpret_cast<uint32_t*>(sm.topp_recv(1));                       // [HBINS] level 0
+    // ---- level 0
+    {
+        const int s0 = 157 - int(__float_as_uint(M) >> 23);  // M * 2^s0 < 2^31
+        const int s0a = s0 > 126 ? 126 : s0;
+        const float f0a = __int_as_float((s0a + 127) << 23), f0b = __int_as_float((s0 - s0a + 127) << 23);
+        uint32_t* L32 = reinterpret_cast<uint32_t*>(L);
+        for (int i = tid; i < HBINS; i += NT) L32[i] = 0u;
+        __syncthreads();
+        stream_warp<VEC, true>(
+            row, g, sm, warp, lane, [&](int sg) { return sm.segkey()[sg] != 0u; },
+            [&](int, int, bool on, const float4& v, int) {
+                if (!on) return;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float x = q_at(v, q);
+                    if (x > 0.f) atomicAdd(&L32[__float_as_uint(x) >> 21], __float2uint_rn((x * f0a) * f0b));
+                }
+            });
+        __syncthreads();
+        push_bins_u32(L32, R32, HBINS, rank, C, tid);
+        cluster_sync();  // level-0 sums in every R32
+        if (warp == 0) {
+            u64 q = 0;
+            for (int i = lane; i < HBINS; i += 32) q += R32[i];
+            q = warp_sum_u64(q);
+            const double T0 = tp > 0.f ? ceil(double(tp) * double(q)) : 1.0;
+            uint32_t ab;
+            const int B = scan_bins_down<uint32_t>(R32, int(maxkey >> 21), uint32_t(T0 < 1.0 ? 1.0 : T0), lane, ab);
+            if (lane == 0) b64[0] = u64(max(B, 0));
+        }
+        __syncthreads();
+    }
+    const uint32_t B = uint32_t(b64[0]);
+    const uint32_t lo = B << 21;
+    const u64 hi = u64(B + 1) << 21;
+    const int sh = 168 - int((maxkey >> 23) & 255u);
+    // ---- collect
+    float a_f = 0.f;
+    const uint32_t cnt_addr = map_rank(smem_u32(list_n), 0);
+    stream_warp<VEC, true>(
+        row, g, sm, warp, lane, [&](int sg) { return sm.segkey()[sg] >= lo; },
+        [&](int, int, bool on, const float4& v, int) {
+            if (!on) return;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float x = q_at(v, q);
+                const uint32_t key = prob_key(x);
+                if (key >= hi) a_f += x;
+                const bool in = key >= lo && u64(key) < hi;
+                const unsigned bal = __ballot_sync(FULL, in);
+                if (bal) {
+                    uint32_t base = 0;
+                    if (lane == 0)  // the same cluster-scoped atomic in every CTA, the leader included
+                        asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;"
+                                     : "=r"(base)
+                                     : "r"(cnt_addr), "r"(uint32_t(__popc(bal)))
+                                     : "memory");
+                    base = __shfl_sync(FULL, base, 0);
+                    const uint32_t pos = base + uint32_t(__popc(bal & ((1u << lane) - 1u)));
+                    if (in && pos < uint32_t(TOPP_LIST)) {
+                        const u64 m = fixed_point(x, sh);
+                        if (leader) {
+                            list_k[pos] = key;
+                            list_q[pos] = m;
+                        } else {
+                            st_dsmem_u32(map_rank(smem_u32(&list_k[pos]), 0), key);
+                            asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(map_rank(smem_u32(&list_q[pos]), 0)),
+                                         "l"(m)
+                                         : "memory");
+                        }
+                    }
+                }
+            }
+        });
+    a_f = warp_sum(a_f);
+    if (lane == 0) reinterpret_cast<float*>(sm.red())[warp] = a_f;
+    __syncthreads();
+    if (tid == 0) {
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) s += reinterpret_cast<float*>(sm.red())[w];
+        put_leader(&sm.part()[rank].f[3], __float_as_uint(s), leader);
+    }
+    cluster_sync();  // the list, its count and the CTAs' sums are in the leader
+    uint32_t n_all;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(n_all) : "r"(cnt_addr) : "memory");
+    if (n_all > uint32_t(TOPP_LIST)) {  // the fallback, in every CTA alike
+        cluster_sync();                  // every CTA has read the count
+        for (int i = tid; i < 2 * TW; i += NT) sm.topp_recv(0)[i] = 0ull;
+        cluster_sync();                  // every receive buffer is clear
+        topp_exact_levels<VEC>(row, g, sm, rank, C, maxkey, tp, lo, hi, warp, lane, tid, t_out, denom_out);
+        return;
+    }
+    // ---- finish (leader)
+    if (leader) {
+        const int n = int(n_all);
+        if (tid == 0) {
+            float af = 0.f;
+            for (int r = 0; r < C; ++r) af += sm.part()[r].f[3];
+            const double sc = ldexp(1.0, sh);
+            const u64 A = u64(rint(double(af) * sc));
+            const double tt = tp > 0.f ? ceil(double(tp) * double(M) * sc) : 1.0;
+            b64[0] = A;
+            b64[1] = tt < 1.0 ? 1ull : u64(tt);
+            reinterpret_cast<float*>(sm.red())[96] = af;
+        }
+        for (int i = tid; i < HBINS; i += NT) L[i] = 0ull;
+        __syncthreads();
+        const u64 A = b64[0], T = b64[1];
+        for (int i = tid; i < n; i += NT) atomicAdd(&L[(list_k[i] >> 10) & (HBINS - 1)], list_q[i]);
+        __syncthreads();
+        // round 1: bits 20..10
+        if (warp == 0) {
+            u64 w = 0;
+            for (int i = lane; i < HBINS; i += 32) w += L[i];
+            w = warp_sum_u64(w);
+            int d1 = -1;  // -1: the target is reached above B; -2: only below B's lowest key
+            u64 ab = 0;
+            if (T > A && T <= A + w) {
+                const int top = (maxkey >> 21) == B ? int((maxkey >> 10) & (HBINS - 1)) : HBINS - 1;
+                d1 = max(0, scan_bins_down<u64>(L, top, T - A, lane, ab));
+            } else if (T > A) {
+                d1 = -2;
+            }
+            if (lane == 0) {
+                b64[2] = u64(int64_t(d1));
+                b64[3] = ab;
+                b64[4] = w;
+            }
+        }
+        __syncthreads();
+        const int d1 = int(int64_t(b64[2]));
+        uint32_t t;
+        u64 kept_in;  // mass of the list at or above t
+        if (d1 >= 0) {
+            const uint32_t pre = (B << 11) | uint32_t(d1);
+            const u64 ab1 = b64[3];
+            for (int i = tid; i < 1024; i += NT) L[HBINS - 1024 + i] = 0ull;  // round-2 bins after round 1's
+            __syncthreads();
+            u64* L2 = L + (HBINS - 1024);
+            for (int i = tid; i < n; i += NT)
+                if ((list_k[i] >> 10) == pre) atomicAdd(&L2[list_k[i] & 1023u], list_q[i]);
+            __syncthreads();
+            if (warp == 0) {
+                const int top = (maxkey >> 10) == pre ? int(maxkey & 1023u) : 1023;
+                u64 ab2;
+                const int d2 = max(0, scan_bins_down<u64>(L2, top, T - A - ab1, lane, ab2));
+                if (lane == 0) {
+                    b64[5] = u64(d2);
+                    b64[3] = ab1 + ab2 + L2[d2];
+                }
+            }
+            __syncthreads();
+            t = (pre << 10) | uint32_t(b64[5]);
+            kept_in = b64[3];
+        } else if (d1 == -1) {
+            t = uint32_t(min(hi, u64(0xffffffffu)));  // keep what lies above B
+            kept_in = 0;
+        } else {
+            t = lo;  // keep all of B
+            kept_in = b64[4];
+        }
+        if (tid == 0) {
+            const float af = reinterpret_cast<float*>(sm.red())[96];
+            const float denom = af + float(double(kept_in) * ldexp(1.0, -sh));
+            for (int r = 0; r < C; ++r) {  // into every CTA's own slot
+                if (r == 0) {
+                    sm.part()[0].u[8] = t;
+                    sm.part()[0].u[9] = __float_as_uint(denom);
+                } else {
+                    st_dsmem_u32(map_rank(smem_u32(&sm.part()[r].u[8]), uint32_t(r)), t);
+                    st_dsmem_u32(map_rank(smem_u32(&sm.part()[r].u[9]), uint32_t(r)), __float_as_uint(denom));
+                }
+            }
+        }
+    }
+    cluster_sync();  // t and the kept mass are in every CTA
+    t_out = sm.part()[rank].u[8];
+    denom_out = __uint_as_float(sm.part()[rank].u[9]);
+}
+
 template <bool VEC, int KIND>
 __global__ void __launch_bounds__(NT, 4) filter_kernel(const FilterArgs a) {
     using KEYF = typename std::conditional<KIND == K_MASK, KeyLogit, KeyProb>::type;
@@ -131,10 +488,13 @@ __global__ void __launch_bounds__(NT, 4) filter_kernel(const FilterArgs a) {
     cluster_wait();  // every CTA has started and cleared its histogram
     pass1_totals(g, sm, leader, rank, C, pos, bad, kmax, need_hist ? 21 : -1, IS_PROB, false, warp,
                  lane, tid);
-    cluster_sync();  // the leader's segment table, every CTA's parts and histogram, are complete
+    if (KIND == K_TOPP) {  // the top-p receive buffers (over the segment masses, now read) and list count
+        for (int i = tid; i < 2 * int(Layout::TOPPW); i += NT) sm.topp_recv(0)[i] = 0ull;
+        if (tid == 0) sm.red()[100] = 0;
+    }
+    cluster_sync();  // every CTA's parts and histogram are complete
 
     const Totals tot = cluster_totals(sm, C);
-    const int npos = tot.npos;
     const bool any_bad = tot.any_bad;
     const float M = tot.M;
     const uint32_t maxkey = tot.maxkey;
@@ -193,6 +553,14 @@ __global__ void __launch_bounds__(NT, 4) filter_kernel(const FilterArgs a) {
         if (leader && tid == 0 && a.out_valid) a.out_valid[b] = valid ? 1 : 0;
         return;
     }
+    if (KIND == K_TOPP) {  // every CTA alike: the threshold, then its share of the row
+        uint32_t t = 0;   // keep key >= t
+        float denom = M;  // kept mass
+        if (valid && tp < 1.f) topp_threshold<VEC>(row, g, sm, leader, rank, C, maxkey, M, tp, warp, lane, tid, t, denom);
+        write_pass<VEC, KIND>(row, orow, g, sm, valid, t, denom, warp, lane);
+        if (leader && tid == 0 && a.out_valid) a.out_valid[b] = valid ? 1 : 0;
+        return;
+    }
     if (!leader) {
         filter_peer<VEC, KIND>(row, orow, g, sm, rank, C, warp, lane, tid);
         return;
@@ -210,14 +578,6 @@ __global__ void __launch_bounds__(NT, 4) filter_kernel(const FilterArgs a) {
                 t = uint32_t(st.lo);
                 denom = st.mass_lo;
             }
-        } else if (tp < 1.f) {
-            // Top-p: the largest t with mass(key >= t) >= top_p * M; top_p <= 0 keeps the
-            // maximum alone (the smallest positive target).
-            Search st = search_start(maxkey, M, V);
-            const float target = tp > 0.f ? tp * M : __uint_as_float(1u);
-            threshold_search<VEC, false, true, true>(row, g, sm, C, st, 0, target, keyf, warp, lane, tid);
-            t = uint32_t(st.lo);
-            denom = st.mass_lo;
         }
     }
 
@@ -245,7 +605,7 @@ static fs_status launch_filter(const float* in, int32_t batch, int32_t vocab, co
     const void* fn = vec ? reinterpret_cast<const void*>(filter_kernel<true, KIND>)
                          : reinterpret_cast<const void*>(filter_kernel<false, KIND>);
     Plan p;
-    fs_status st = make_plan(batch, vocab, fn, KIND != K_TOPP, p);
+    fs_status st = make_plan(batch, vocab, fn, KIND != K_TOPP, p, KIND == K_TOPP);
     if (st != FS_OK) return st;
     FilterArgs a;
     a.in = in;

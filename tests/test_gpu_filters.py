@@ -238,3 +238,52 @@ def test_refined_bound_crowded_rows(ms, k):
     out, valid = _run(ms, "top_k", P, [k, k])
     _check_renorm(P, [k, k], out, valid, filters.top_k_renorm)
     assert (np.count_nonzero(out, axis=1) == k).all()
+
+
+def test_top_p_scales_and_extremes(ms):
+    """Top-p renormalisation of rows scaled by exact powers of two (2^100, 2^-80:
+    the integer mass scale follows the row maximum), of a row pushed into the
+    subnormal range, and top_p from 0 (the maximum alone) to 0.95: kept sets
+    bit-exact, values within 1e-6 of the oracle's."""
+    ps = [0.0, 1e-4, 0.3, 0.5, 0.8, 0.95]
+    acc = guard_accept(lambda i: [(None, p, None, "joint", GUARD_DEEP if p > 0.9 else 1e-5) for p in ps if p > 0])
+    base = _softmax_rows(3, 50_000, 3.0, 77, acc)
+    assert all(acc(i, base[i]) for i in range(3))
+    for scale in (2.0 ** 100, 2.0 ** -80, 1.0):
+        P = (base.astype(np.float64) * scale).astype(np.float32)
+        assert np.array_equal(P.astype(np.float64) / scale, base.astype(np.float64))   # exact scaling
+        for p in ps:
+            out, valid = _run(ms, "top_p", P, [p] * 3)
+            for i in range(3):
+                exp, ok = filters.top_p_renorm(P[i], p)
+                assert bool(valid[i]) == ok
+                assert np.array_equal(out[i] != 0, exp != 0), (scale, p, i)
+                assert np.max(np.abs(out[i].astype(np.float64) - exp)) <= TOL, (scale, p, i)
+    # Subnormal values: the scaled row differs from `base` by rounding, so its own
+    # boundary margins decide which top_p are checked.
+    S = (base[:1].astype(np.float64) * 2.0 ** -135).astype(np.float32)
+    M = float(S.astype(np.float64).sum())
+    for p in (0.0, 0.3, 0.5, 0.8):
+        if p > 0 and filters.topp_boundary_margin(S[0], None, p, None, "joint") < 1e-5 * M:
+            continue
+        out, valid = _run(ms, "top_p", S, [p])
+        exp, ok = filters.top_p_renorm(S[0], p)
+        assert ok and valid[0]
+        assert np.array_equal(out[0] != 0, exp != 0), p
+        assert np.max(np.abs(out[0].astype(np.float64) - exp)) <= TOL, p
+
+
+def test_top_p_crowded_crossing_bin(ms):
+    """Near-flat rows (softmax of N(0, 0.05^2), V = 20000): the bin of the top-p
+    crossing holds thousands of elements, more than the leader's list, so every CTA
+    finishes with the exact histogram passes.  Kept sets bit-exact, values within
+    1e-6."""
+    ps = [0.2, 0.5, 0.8]
+    acc = guard_accept(lambda i: [(None, p, None, "joint") for p in ps])
+    P = _softmax_rows(4, 20_000, 0.05, 91, acc)
+    assert all(acc(i, P[i]) for i in range(4))
+    keys = P.view(np.uint32) >> 21
+    assert max(np.bincount(keys[i]).max() for i in range(4)) > 2048   # the crowded bin
+    for p in ps:
+        out, valid = _run(ms, "top_p", P, [p] * 4)
+        _check_renorm(P, [p] * 4, out, valid, filters.top_p_renorm)
