@@ -27,4 +27,5 @@ Modules:
   dual_pivot   the dual-pivot rejection sampler as the pages state it; exact
                Markov-chain evaluation of its output law (small V)
   baseline     sort-based reference sampler used as the timed CPU baseline
+  speculative  chain speculative-sampling verification (Leviathan et al. 2023; Chen et al. 2023)
 """
