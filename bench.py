@@ -310,8 +310,32 @@ def run_ours(args):
 
     entries = {}
     if not args.no_entries:
+        # Chain speculative verification, B rows of L = 4 drafts: targets softmax(3 z),
+        # drafts softmax(3 z + N(0, 1)), draft tokens drawn from the drafts (seeded, on the
+        # device); 5 copies rotate so that the rows each call streams are not in L2.
+        LD = 4
+        gsp = torch.Generator(device=dev)
+        gsp.manual_seed(rank_seed(rank) + 17)
+        sp_in = []
+        for _ in range(5):
+            zt = torch.randn((B, LD + 1, V), generator=gsp, device=dev) * 3.0
+            tgt = torch.softmax(zt, dim=-1).contiguous()
+            dft = torch.softmax(zt[:, :LD] + torch.randn((B, LD, V), generator=gsp, device=dev), dim=-1).contiguous()
+            tks = torch.multinomial(dft.reshape(-1, V), 1, generator=gsp).reshape(B, LD).to(torch.int32).contiguous()
+            sp_in.append((P(dft.data_ptr()), P(tks.data_ptr()), P(tgt.data_ptr()), dft, tks, tgt))
+            del zt
+        sp_tok = torch.empty((B, LD + 1), dtype=torch.int32, device=dev)
+        sp_acc = torch.empty(B, dtype=torch.int32, device=dev)
+        sp_emi = torch.empty(B, dtype=torch.int32, device=dev)
+        calls["chain_speculative"] = lambda i: check(lib.fs_chain_speculative_sampling(
+            sp_in[i % 5][0], sp_in[i % 5][1], sp_in[i % 5][2], B, LD, V, seed, i, P(sp_tok.data_ptr()),
+            P(sp_acc.data_ptr()), P(sp_emi.data_ptr()), sptr))
+        calls["chain_speculative"](0)
+        torch.cuda.synchronize(dev)
+        rejected = int((sp_acc < LD).sum().item())   # rows that stream target and draft rows
+        alg_bytes["chain_speculative"] = (rejected * 2 + (B - rejected)) * V * 4 + B * (LD * 12 + (LD + 1) * 4 + 8)
         for name in ["joint", "from_probs", "top_k_renorm", "top_p_renorm", "mask_logits", "joint_single_pivot",
-                     "top_k_first_from_logits"]:
+                     "top_k_first_from_logits", "chain_speculative"]:
             tot, pe, _ = timed(calls[name], min(K, 100), 5)
             us = tot / min(K, 100) * 1e3
             entries[name] = {"us_per_call": round(us, 3), "p50_us": round(statistics.median(pe) * 1e3, 3),

@@ -217,6 +217,35 @@ fs_status fs_top_k_mask_logits(const float* logits, int32_t batch, int32_t vocab
                                const int32_t* top_k, float* out_logits,
                                uint8_t* out_valid, void* stream);
 
+/* Chain speculative-sampling verification (speculative decoding), one cluster per
+ * batch row.  The pages name it as a use of the sampler ([blog] community adoption)
+ * without an algorithm; this follows Leviathan et al. 2023, Algorithm 1 / Chen et
+ * al. 2023, Algorithm 2.  For row b, draft token d_i (drawn by the caller from draft
+ * row q_i) is accepted while u_i * q_i(d_i) < p_i(d_i); at the first rejection i the
+ * emitted token is drawn from the residual max(p_i - q_i, 0), and after num_draft
+ * acceptances from p_{num_draft+1}.  Rows are used as given (not renormalised); a
+ * draft token outside [0, vocab) is rejected.  The draw is the sampler's inverse
+ * transform over the weights.  Randomness: the Philox stream of row b as in the
+ * samplers (key = seed, counter = (round, b, offset)): round i for the test of draft
+ * i, round num_draft for the draw.
+ *   draft_probs  [batch, num_draft, vocab] float32, device (may be null if num_draft = 0)
+ *   draft_tokens [batch, num_draft] int32, device (idem)
+ *   target_probs [batch, num_draft + 1, vocab] float32, device
+ *   out_tokens   [batch, num_draft + 1] int32, device: the accepted draft tokens, then
+ *                the emitted token, then -1
+ *   out_accepted [batch] int32: accepted draft tokens
+ *   out_emitted  [batch] int32: accepted + 1, or accepted when the draw's weights are
+ *                not a valid row (a NaN or infinite value, a negative value in the
+ *                bonus row, or no positive mass); the emitted slot is then -1
+ * Pointers are device memory owned by the caller; nothing is allocated.  Errors:
+ * FS_ERR_INVALID_ARG for negative sizes, vocab < 1 or a required null pointer;
+ * FS_ERR_UNSUPPORTED for vocab > FS_MAX_VOCAB or batch * (num_draft + 1) >= 2^31. */
+fs_status fs_chain_speculative_sampling(const float* draft_probs, const int32_t* draft_tokens,
+                                        const float* target_probs, int32_t batch, int32_t num_draft,
+                                        int32_t vocab, uint64_t seed, uint64_t offset,
+                                        int32_t* out_tokens, int32_t* out_accepted, int32_t* out_emitted,
+                                        void* stream);
+
 /* The launch plan of the sampling kernels for `batch_out` rows of `vocab` elements on
  * the current device.  order = FS_ORDER_TOP_K_FIRST gives the plan of the
  * top-k-first entries (fs_top_k_top_p_sampling*, order top-k-first) and of

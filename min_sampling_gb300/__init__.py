@@ -20,7 +20,8 @@ __all__ = [
     "FsError", "lib", "LIB_PATH", "ORDER_TOP_K_FIRST", "ORDER_JOINT", "MAX_ROUNDS",
     "sampling_from_probs", "top_k_sampling", "top_p_sampling", "min_p_sampling",
     "top_k_top_p_sampling", "top_k_top_p_sampling_rng", "advance_offset",
-    "top_k_top_p_sampling_pivots", "top_k_top_p_sampling_from_logits", "sampling_plan", "top_k_renorm_probs", "top_p_renorm_probs",
+    "top_k_top_p_sampling_pivots", "top_k_top_p_sampling_from_logits", "sampling_plan",
+    "chain_speculative_sampling", "top_k_renorm_probs", "top_p_renorm_probs",
     "top_k_mask_logits", "philox4x32_10",
 ]
 
@@ -43,6 +44,7 @@ _SIGNATURES = {
     "fs_top_k_top_p_sampling_rng": [_P, _I32, _I32, _P, _I32, _P, _P, _P, _I32, _P, _P, _P, _U64, _U64, _P, _P, _P,
                                     _P],
     "fs_advance_offset": [_P, _U64, _P],
+    "fs_chain_speculative_sampling": [_P, _P, _P, _I32, _I32, _I32, _U64, _U64, _P, _P, _P, _P],
     "fs_sampling_plan": [_I32, _I32, _I32, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
                          ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)],
     "fs_top_k_top_p_sampling_from_logits": [_P, _I32, _I32, _P, _I32, _P, _P, _P, _P, _I32, _U64, _U64, _P, _P, _P,
@@ -271,6 +273,40 @@ def top_k_top_p_sampling_from_logits(logits, temperature=None, top_k=None, top_p
         int(seed) & (2 ** 64 - 1), int(offset) & (2 ** 64 - 1), _ptr(tok), _ptr(valid),
         _ptr(rounds) if return_rounds else None, _stream()))
     return (tok, valid, rounds) if return_rounds else (tok, valid)
+
+
+def chain_speculative_sampling(draft_probs, draft_tokens, target_probs, *, seed: int, offset: int):
+    """Chain speculative-sampling verification: draft_probs [B, L, V] float32,
+    draft_tokens [B, L] int32, target_probs [B, L + 1, V] float32 (CUDA, contiguous).
+    Returns (tokens [B, L + 1] int32: the accepted drafts, the emitted token, then -1;
+    accepted [B] int32; emitted [B] int32)."""
+    def check3(x, name):
+        if not isinstance(x, torch.Tensor) or x.dim() != 3 or x.dtype != torch.float32 or not x.is_cuda \
+                or not x.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 3-D float32 CUDA tensor")
+    check3(target_probs, "target_probs")
+    B, L1, V = target_probs.shape
+    L = L1 - 1
+    if L < 0:
+        raise ValueError("target_probs needs at least one row per batch entry")
+    if L > 0:
+        check3(draft_probs, "draft_probs")
+        if tuple(draft_probs.shape) != (B, L, V):
+            raise ValueError("draft_probs must be [B, L, V] with target_probs [B, L + 1, V]")
+        if not isinstance(draft_tokens, torch.Tensor) or tuple(draft_tokens.shape) != (B, L) \
+                or draft_tokens.device != target_probs.device:
+            raise ValueError("draft_tokens must be a [B, L] tensor on the same device")
+        draft_tokens = draft_tokens.to(torch.int32).contiguous()
+    else:
+        draft_probs = draft_tokens = None
+    dev = target_probs.device
+    tok = torch.empty((B, L + 1), dtype=torch.int32, device=dev)
+    acc = torch.empty(B, dtype=torch.int32, device=dev)
+    emi = torch.empty(B, dtype=torch.int32, device=dev)
+    _check(_lib().fs_chain_speculative_sampling(
+        _ptr(draft_probs), _ptr(draft_tokens), _ptr(target_probs), B, L, V,
+        int(seed) & (2 ** 64 - 1), int(offset) & (2 ** 64 - 1), _ptr(tok), _ptr(acc), _ptr(emi), _stream()))
+    return tok, acc, emi
 
 
 def sampling_plan(batch_out: int, vocab: int, order: str = "top_k_first") -> dict:

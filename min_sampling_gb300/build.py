@@ -22,7 +22,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfs_sampling.so")
-SOURCES = ["sampling.cu", "renorm.cu", "api.cu"]
+SOURCES = ["sampling.cu", "renorm.cu", "speculative.cu", "api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -171,6 +171,9 @@ struct Geom {
     // rows of probabilities (soft = false) values are used as they are.
     bool soft = false;
     float vm = 0.f, vinv = 1.f;
+    // Chain speculative verification: values are the residual max(x - y, 0) of the
+    // row against this second row at the same index (null: the row itself).
+    const float* qrow = nullptr;
     __device__ __forceinline__ float val(float x) const { return soft ? expf((x - vm) * vinv) : x; }
     __device__ __forceinline__ float4 val4(float4 v) const {
         return soft ? make_float4(val(v.x), val(v.y), val(v.z), val(v.w)) : v;
@@ -282,6 +285,25 @@ __device__ __forceinline__ float4 load4(const float* __restrict__ row, int V, in
 
 __device__ __forceinline__ float q_at(const float4& v, int q) {
     return q == 0 ? v.x : (q == 1 ? v.y : (q == 2 ? v.z : v.w));
+}
+
+// max(x - y, 0), keeping a NaN difference so that the row shows as bad.
+__device__ __forceinline__ float residual_of(float x, float y) {
+    const float d = x - y;
+    return (d > 0.f || d != d) ? d : 0.f;
+}
+
+// The lane's four values of the row at `base` as the path sees them: the row's own
+// values or, with a second row, their residual against it; then the weight transform
+// of rows of logits.
+template <bool VEC, bool NC>
+__device__ __forceinline__ float4 row4(const float* __restrict__ row, const Geom& g, int base, float fill) {
+    float4 v = load4<VEC, NC>(row, g.V, base, fill);
+    if (g.qrow) {
+        const float4 y = load4<VEC, NC>(g.qrow, g.V, base, 0.f);
+        v = make_float4(residual_of(v.x, y.x), residual_of(v.y, y.y), residual_of(v.z, y.z), residual_of(v.w, y.w));
+    }
+    return g.val4(v);
 }
 
 // Asynchronous copies global -> shared (cp.async, completed per thread by
@@ -471,7 +493,7 @@ __device__ __forceinline__ void stream_warp(const float* __restrict__ row, Geom 
         for (int j = 0; j < TB; ++j) {
             const int blk = b0 + j;
             const int sg = r0 + (blk >> g.shift);
-            v[j] = (blk < nblk && live(sg)) ? g.val4(load4<VEC, NC>(row, g.V, g.base(sg, blk & mask, lane), g.fill0()))
+            v[j] = (blk < nblk && live(sg)) ? row4<VEC, NC>(row, g, g.base(sg, blk & mask, lane), g.fill0())
                                             : make_float4(0.f, 0.f, 0.f, 0.f);
         }
     };
@@ -516,7 +538,7 @@ __device__ __forceinline__ void pass1(const float* __restrict__ row, Geom g, Sme
         for (int j = 0; j < TB; ++j) {
             const int sg = g.s0 + t * spt + (j >> g.shift);
             v[j] = (t < ntrip && sg < g.s1)
-                       ? g.val4(load4<VEC, NC>(row, g.V, g.base(sg, j & mask, lane), g.soft ? g.fill0() : fill))
+                       ? row4<VEC, NC>(row, g, g.base(sg, j & mask, lane), g.soft ? g.fill0() : fill)
                        : make_float4(fill, fill, fill, fill);
         }
     };
@@ -1280,7 +1302,7 @@ __device__ __forceinline__ unsigned long long locate_in_segment(const float* __r
 #pragma unroll 1
     for (int it = 0; it < g.seg_it(); ++it) {
         const int base = g.base(s, it, lane);
-        const float4 v = g.val4(load4<VEC, NC>(row, g.V, base, g.fill0()));
+        const float4 v = row4<VEC, NC>(row, g, base, g.fill0());
         float w[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -1393,6 +1415,43 @@ __device__ __forceinline__ int locate_in_list(const float* lv, int n, float low,
         run += __shfl_sync(FULL, incl, 31);
     }
     return last;
+}
+
+// Inverse-transform draw over the whole row while its tokens are spread over the
+// cluster (warp-collective, leader): the owning CTA from the per-CTA masses cmass[]
+// (the first CTA whose running mass passes the target), the segment inside its range from
+// mass[cur], then the token inside the segment.  Returns the token (-1 if none) packed
+// with its value.
+template <bool VEC>
+__device__ __forceinline__ unsigned long long draw_full(const float* __restrict__ row, Geom g, Smem sm, int C, int cur,
+                                                   float low, float target, int lane) {
+    float run = 0.f, before = 0.f, last_before = 0.f;
+    int owner = -1, last = -1;
+    for (int c = 0; c < C; ++c) {
+        const float m = sm.cmass()[c];
+        if (m > 0.f) {
+            if (owner < 0 && run + m > target) {
+                owner = c;
+                before = run;
+            }
+            last = c;
+            last_before = run;
+        }
+        run += m;
+    }
+    if (owner < 0) {
+        owner = last;
+        before = last_before;
+    }
+    if (owner < 0) return pack_jx(-1, 0.f);
+    int a0, a1;
+    g.range_of(owner, a0, a1);
+    float t = target - before;
+    const unsigned long long ls = locate_segment(sm.mass(cur), a0, a1, t, lane);
+    const int s = unpack_j(ls);
+    if (s < 0) return pack_jx(-1, 0.f);
+    t = (t - unpack_x(ls) < 0.f) ? 0.f : t - unpack_x(ls);
+    return locate_in_segment<VEC, true>(row, g, s, low, t, lane);
 }
 
 // ------------------------------------------------------------------ commands

@@ -134,42 +134,6 @@ __device__ __forceinline__ int compact_round(Smem sm, int n_list, const Pred& f,
     return 0;
 }
 
-// Inverse-transform draw over the whole row while its tokens are spread over the
-// cluster (warp-collective, leader): the owning CTA from the per-CTA masses cmass[]
-// (the first CTA whose running mass passes the target), the segment inside its range from
-// mass[cur], then the token inside the segment.  Returns the token (-1 if none) packed
-// with its value.
-template <bool VEC>
-__device__ __forceinline__ unsigned long long draw_full(const float* __restrict__ row, Geom g, Smem sm, int C, int cur,
-                                                   float low, float target, int lane) {
-    float run = 0.f, before = 0.f, last_before = 0.f;
-    int owner = -1, last = -1;
-    for (int c = 0; c < C; ++c) {
-        const float m = sm.cmass()[c];
-        if (m > 0.f) {
-            if (owner < 0 && run + m > target) {
-                owner = c;
-                before = run;
-            }
-            last = c;
-            last_before = run;
-        }
-        run += m;
-    }
-    if (owner < 0) {
-        owner = last;
-        before = last_before;
-    }
-    if (owner < 0) return pack_jx(-1, 0.f);
-    int a0, a1;
-    g.range_of(owner, a0, a1);
-    float t = target - before;
-    const unsigned long long ls = locate_segment(sm.mass(cur), a0, a1, t, lane);
-    const int s = unpack_j(ls);
-    if (s < 0) return pack_jx(-1, 0.f);
-    t = (t - unpack_x(ls) < 0.f) ? 0.f : t - unpack_x(ls);
-    return locate_in_segment<VEC, true>(row, g, s, low, t, lane);
-}
 
 // The rounds on a short candidate list held in warp 0's registers (kept[r] marks the
 // filtered set; S_low its mass): the same draw, fused reduction and three cases as

@@ -329,3 +329,25 @@ def concentrated_logits(n: int, vocab: int, n_big: int, span: int, seed: int, sh
         z[rng.choice(span, size=n_big, replace=False)] += shift
         out[i] = detie(z.astype(np.float32), positive_only=False)[0]
     return out
+
+
+def speculative_batch(batch: int, num_draft: int, vocab: int, seed: int, sigma: float = 3.0,
+                      drift: float = 1.0):
+    """Synthetic chain-verification inputs: target rows p = softmax(z), draft rows
+    q = softmax(z + drift * N(0, 1)) (a draft model close to the target), and draft
+    tokens drawn from q.  Returns (draft [B, L, V], tokens [B, L] int32, target
+    [B, L + 1, V]), all float32 rows de-tied like the other workloads."""
+    rng = np.random.default_rng([seed, batch, num_draft, vocab])
+    target = np.empty((batch, num_draft + 1, vocab), np.float32)
+    draft = np.empty((batch, num_draft, vocab), np.float32)
+    tokens = np.empty((batch, num_draft), np.int32)
+    for b in range(batch):
+        for i in range(num_draft + 1):
+            z = rng.normal(0.0, sigma, vocab)
+            target[b, i] = detie(softmax_fp32(z))[0]
+            if i < num_draft:
+                q = detie(softmax_fp32(z + drift * rng.normal(0.0, 1.0, vocab)))[0]
+                draft[b, i] = q
+                q64 = q.astype(np.float64)
+                tokens[b, i] = rng.choice(vocab, p=q64 / q64.sum())
+    return draft, tokens, target
