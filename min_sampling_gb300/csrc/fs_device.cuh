@@ -439,6 +439,10 @@ __device__ __forceinline__ uint32_t logit_key(float x) {
     const uint32_t u = __float_as_uint(x);
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
+// The float whose order key (logit_key) is k.
+__device__ __forceinline__ float from_logit_key(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
 
 struct KeyProb {
     __device__ __forceinline__ uint32_t operator()(float x) const { return prob_key(x); }
@@ -526,7 +530,14 @@ __device__ __forceinline__ void stream_warp(const float* __restrict__ row, Geom 
 // `hist_shift` >= 0 every segment maximum is also counted into the CTA's local
 // histogram (lv, cleared beforehand) at bin key >> hist_shift.  Touches no other CTA,
 // so it may run before the cluster's first barrier completes.
-template <bool VEC, bool NC, bool PROB>
+//
+// SOFT (rows of logits sampled through a softmax, read once; PROB false): keys are
+// logit keys, the positive count is the count of logits above -inf, and +inf is a bad
+// value as well as NaN.  SOFT = 2 also keeps a segment's mass as sum exp((z - zmax) / T)
+// relative to its own largest logit zmax (1/T = g.vinv), the running maximum of an
+// online softmax; pass1_totals moves the masses to the CTA's maximum and the sampler to
+// the row's.  SOFT = 1 keeps no masses (paths that draw only from gathered candidates).
+template <bool VEC, bool NC, bool PROB, int SOFT = 0>
 __device__ __forceinline__ void pass1(const float* __restrict__ row, Geom g, Smem sm, int hist_shift, int warp,
                                       int lane, int& pos, bool& bad, uint32_t& kmax) {
     const int spt = TB >> g.shift;  // segments per trip
@@ -569,15 +580,31 @@ __device__ __forceinline__ void pass1(const float* __restrict__ row, Geom g, Sme
                     k = max(k, prob_key(x));
                     pos += x > 0.f;
                 } else {
+                    const bool in = sg < g.s1 && base + q < g.V;
                     bad |= isnan(x);
-                    k = max(k, (sg < g.s1 && base + q < g.V) ? logit_key(x) : 0u);
+                    if (SOFT) {
+                        bad |= in && x == __int_as_float(0x7f800000);
+                        pos += in && x > __int_as_float(0xff800000);
+                    }
+                    k = max(k, in ? logit_key(x) : 0u);
                 }
             }
             km[j] = __reduce_max_sync(FULL, k);
             kmax = max(kmax, km[j]);
             s[j] = PROB ? (A[j].x + A[j].y) + (A[j].z + A[j].w) : 0.f;
         }
-        if (PROB) {
+        if (SOFT == 2) {  // weights relative to each block's largest logit, all blocks at once
+#pragma unroll
+            for (int j = 0; j < TB; ++j) {
+                // a block of -inf or padding has no finite maximum: +inf makes its weights 0
+                const float zb = km[j] > 0x007fffffu ? from_logit_key(km[j]) : __int_as_float(0x7f800000);
+                float e = 0.f;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) e += expf((q_at(A[j], q) - zb) * g.vinv);
+                s[j] = e;
+            }
+        }
+        if (PROB || SOFT == 2) {
 #pragma unroll
             for (int m = 16; m; m >>= 1)
 #pragma unroll
@@ -594,8 +621,16 @@ __device__ __forceinline__ void pass1(const float* __restrict__ row, Geom g, Sme
                 ss += mine ? s[j] : 0.f;
                 kk = mine ? max(kk, km[j]) : kk;
             }
+            if (SOFT == 2 && g.shift > 0) {  // blocks of one segment: each to the segment's largest logit
+                ss = 0.f;
+                const float zs = from_logit_key(kk);
+#pragma unroll
+                for (int j = 0; j < TB; ++j)
+                    if ((j >> g.shift) == lane && km[j] > 0x007fffffu)
+                        ss += s[j] * expf((from_logit_key(km[j]) - zs) * g.vinv);
+            }
             sm.segkey()[sg] = kk;
-            if (PROB) sm.mass(0)[sg] = ss;
+            if (PROB || SOFT == 2) sm.mass(0)[sg] = ss;
             if (hist_shift >= 0)  // this CTA's histogram counts, in lv
                 atomicAdd(reinterpret_cast<uint32_t*>(sm.lv()) + min(uint32_t(HBINS - 1), kk >> hist_shift), 1u);
         }
@@ -623,11 +658,29 @@ __device__ __forceinline__ void st_rank_v4(void* local_addr, uint4 v, uint32_t r
 // CTA's counts of its segment maxima (key >> hist_shift, made by pass 1 in lv) into the
 // histogram of every CTA of the cluster, each of which cleared its own (and its lv)
 // before that barrier.  The CTA's first segment is a multiple of 4, so the table moves
-// in 16-byte words.  Block-collective.
+// in 16-byte words.  With `online` (pass 1 SOFT = 2) the segment masses are first moved
+// from each segment's largest logit to the CTA's (times exp((zmax - zcta) / T)), so
+// the table and f[0] are relative to the CTA's maximum logit, u[2].  Block-collective.
 __device__ __forceinline__ void pass1_totals(Geom g, Smem sm, bool leader, int rank, int C, int pos, bool bad,
                                              uint32_t kmax, int hist_shift, bool prob, bool publish, int warp,
-                                             int lane, int tid) {
+                                             int lane, int tid, bool online = false) {
     __syncthreads();  // the table and the local histogram counts written by pass 1
+    if (online) {
+        if (lane == 0) sm.red()[warp] = int(kmax);  // kmax is the same in every lane of a warp
+        __syncthreads();
+        uint32_t mk = 0;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) mk = max(mk, uint32_t(sm.red()[w]));
+        if (mk > 0x007fffffu) {  // a logit above -inf
+            const float zc = from_logit_key(mk);
+#pragma unroll 1
+            for (int i = g.s0 + tid; i < g.s1; i += NT) {
+                const uint32_t kk = sm.segkey()[i];
+                sm.mass(0)[i] = kk > 0x007fffffu ? sm.mass(0)[i] * expf((from_logit_key(kk) - zc) * g.vinv) : 0.f;
+            }
+        }
+        __syncthreads();
+    }
     const uint32_t* loc = reinterpret_cast<const uint32_t*>(sm.lv());
     if (publish && !leader) {
 #pragma unroll 1
@@ -759,6 +812,30 @@ __device__ __forceinline__ void pivot_pass(const float* __restrict__ row, Geom g
         }
     }
     __syncthreads();
+}
+
+// Rows of logits sampled through a softmax, once the row maximum g.vm is known: this
+// CTA's segment keys (logit keys of each segment's largest logit) become keys of the
+// weights w = exp((z - vm) / T), raised by 4 units in the last place so that no weight
+// of the segment exceeds its key whatever the last-place error of expf (within 2
+// units; (z - vm) / T is correctly rounded, hence non-decreasing in z).
+// Block-collective; the caller synchronises before the keys are read.
+__device__ __forceinline__ uint32_t soft_weight_key(const Geom& g, uint32_t lk) {
+    return lk > 0x007fffffu ? prob_key(expf((from_logit_key(lk) - g.vm) * g.vinv)) : 0u;
+}
+__device__ __forceinline__ void soft_segment_keys(const Geom& g, Smem sm, int tid) {
+#pragma unroll 1
+    for (int i = g.s0 + tid; i < g.s1; i += NT) {
+        const uint32_t w = soft_weight_key(g, sm.segkey()[i]);
+        sm.segkey()[i] = w == 0u ? 0u : min(w + 4u, 0x7f7fffffu);
+    }
+}
+// The weight key of a lower bound L on logit keys, lowered by 8 units in the last
+// place (at least 1): every weight whose logit is at least L, and the k-th largest
+// weight when L is at most the k-th largest logit, lie at or above it.
+__device__ __forceinline__ uint32_t soft_bound(const Geom& g, uint32_t L) {
+    const uint32_t w = soft_weight_key(g, L);
+    return w > 9u ? w - 8u : 1u;
 }
 
 // ------------------------------------------------------------------ candidate lists

@@ -215,46 +215,7 @@ __device__ __forceinline__ int small_rounds(const Small& s, const bool* kept, co
     return -1;
 }
 
-// Largest order key of this CTA's segments of a row of logits (first read of the row),
-// block-collective; every thread gets it.
-template <bool VEC>
-__device__ __forceinline__ uint32_t row_max_key(const float* __restrict__ row, Geom g, Smem sm, int warp, int lane) {
-    int r0, r1;
-    warp_range(g.s1 - g.s0, warp, r0, r1);
-    r0 += g.s0;
-    r1 += g.s0;
-    const int nblk = (r1 - r0) << g.shift;
-    const int mask = g.seg_it() - 1;
-    const float ninf = __int_as_float(0xff800000);
-    uint32_t km = 0;
-#pragma unroll 1
-    for (int b0 = 0; b0 < nblk; b0 += TB) {
-        float4 v[TB];
-#pragma unroll
-        for (int j = 0; j < TB; ++j) {
-            const int blk = b0 + j;
-            v[j] = blk < nblk ? load4<VEC, true>(row, g.V, g.base(r0 + (blk >> g.shift), blk & mask, lane), ninf)
-                              : make_float4(ninf, ninf, ninf, ninf);
-        }
-#pragma unroll
-        for (int j = 0; j < TB; ++j)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) km = max(km, logit_key(q_at(v[j], q)));
-    }
-    km = warp_max_u(km);
-    if (lane == 0) sm.red()[warp] = int(km);
-    __syncthreads();
-    uint32_t r = 0;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) r = max(r, uint32_t(sm.red()[w]));
-    __syncthreads();
-    return r;
-}
 
-// The float whose order key (logit_key) is k.
-__device__ __forceinline__ float from_logit_key(uint32_t k) {
-    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
 
 template <bool VEC, bool SOFT>
 __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
@@ -286,29 +247,12 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
     const bool need_hist = kfirst && ns >= k;
     const float temp = SOFT && a.temperature ? a.temperature[b] : 1.f;
 
-    if (SOFT) {
-        // Rows of logits: the row maximum first (the one HBM read), exchanged through
-        // every CTA's part[].u[3]; pass 1 then reads the row again (from L2) as weights
-        // w = exp((z - max) / T), i.e. the softmax without its normalisation.
-        cluster_arrive();
-        const uint32_t zk = row_ok ? row_max_key<VEC>(row, g, sm, warp, lane) : 0u;
-        cluster_wait();  // every CTA has started
-        if (tid < C) {
-            uint32_t* dst = &sm.part()[rank].u[3];
-            if (tid == rank) {
-                *dst = zk;
-            } else {
-                st_dsmem_u32(map_rank(smem_u32(dst), uint32_t(tid)), zk);
-            }
-        }
-        cluster_sync();
-        g.soft = true;
-        g.vm = from_logit_key(warp_max_u(lane < C ? sm.part()[lane].u[3] : 0u));
-        g.vinv = 1.f / temp;
-    }
+    // Rows of logits are read once too: pass 1 keeps, per segment, its largest logit and
+    // its mass relative to it (an online softmax); the row's maximum follows from the
+    // CTAs' after the barrier.
+    if (SOFT) g.vinv = 1.f / temp;
 
-    // ---- a2: pass 1, the only HBM read of the row (of probabilities), inside a split
-    // cluster barrier
+    // ---- a2: pass 1, the only HBM read of the row, inside a split cluster barrier
     if (need_hist)
         for (int i = tid; i < HBINS; i += NT) {
             sm.hist()[i] = 0u;
@@ -322,7 +266,12 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
     bool bad = false;
     uint32_t kmax = 0;
     if (row_ok) {
-        pass1<VEC, true, true>(row, g, sm, need_hist ? 21 : -1, warp, lane, pos, bad, kmax);
+        if (SOFT && kfirst)  // draws come from the gathered candidates: keys only
+            pass1<VEC, true, false, 1>(row, g, sm, need_hist ? 21 : -1, warp, lane, pos, bad, kmax);
+        else if (SOFT)
+            pass1<VEC, true, false, 2>(row, g, sm, -1, warp, lane, pos, bad, kmax);
+        else
+            pass1<VEC, true, true>(row, g, sm, need_hist ? 21 : -1, warp, lane, pos, bad, kmax);
     } else {
         for (int i = g.s0 + tid; i < g.s1; i += NT) {
             sm.segkey()[i] = 0u;
@@ -330,8 +279,27 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
         }
     }
     cluster_wait();  // every CTA has started and cleared its histogram
-    pass1_totals(g, sm, leader, rank, C, pos, bad, kmax, need_hist ? 21 : -1, true, !kfirst, warp, lane, tid);
+    pass1_totals(g, sm, leader, rank, C, pos, bad, kmax, need_hist ? 21 : -1, !(SOFT && kfirst), !kfirst, warp, lane,
+                 tid, SOFT && !kfirst);
     cluster_sync();  // the leader's segment table, every CTA's parts and histogram, are complete
+
+    // Rows of logits: the row's largest logit m (the CTAs' maxima are logit keys in
+    // part[].u[2]) and each CTA's factor exp((m_c - m) / T) from its maximum to the row's,
+    // in scale[c].  From here on the row is read as the weights w = exp((z - m) / T).
+    float* scale = reinterpret_cast<float*>(sm.red() + 112);  // [MAX_CLUSTER], past the search scratch
+    uint32_t row_mkey = 0;
+    if (SOFT) {
+        row_mkey = warp_max_u(lane < C ? sm.part()[lane].u[2] : 0u);
+        const bool fin = row_mkey > 0x007fffffu && row_mkey < 0xff800000u;
+        g.vm = from_logit_key(row_mkey);
+        g.soft = true;
+        if (tid < C) {
+            const uint32_t kc = sm.part()[tid].u[2];
+            scale[tid] = (fin && kc > 0x007fffffu) ? expf((from_logit_key(kc) - g.vm) * g.vinv) : 0.f;
+        }
+        if (!kfirst) soft_segment_keys(g, sm, tid);
+        __syncthreads();
+    }
 
     // ---- a3 (first half, every CTA): top-k-first candidates.  Every CTA derives the
     // same lower bound L0 <= t_k from its copy of the histogram and sends its elements
@@ -342,6 +310,11 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
     if (kfirst) {
         const uint32_t mk = warp_max_u(lane < C ? sm.part()[lane].u[2] : 0u);
         L0 = max(1u, need_hist ? hist_bound(sm, g, rank, C, k, mk, warp, lane, tid) : 0u);
+        if (SOFT) {  // the segment keys and the bound, from logits to weights
+            soft_segment_keys(g, sm, tid);
+            L0 = soft_bound(g, L0);
+            __syncthreads();
+        }
         collect_own<VEC>(row, g, sm, leader, rank, C, rank * (CAP / C), CAP / C, L0, NO_LIMIT, keyf, false, true,
                          warp, lane, tid);
         if (leader) {  // the row's totals while the other CTAs finish their candidates
@@ -372,11 +345,21 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
     f.t32 = 0.f;
     const bool any_filter = f.k_on || f.p_on || f.m_on;
 
+    if (SOFT) {  // the CTAs' masses to the row's maximum; the largest weight is exp(0) = 1
+        const bool inC = lane < C;
+        const bool fin = row_mkey > 0x007fffffu && row_mkey < 0xff800000u;
+        // top-k-first kept no masses: the row's mass only decides validity there, and is
+        // at least the largest weight, 1
+        tot.M = kfirst ? (fin ? 1.f : 0.f) : warp_sum(inC ? scale[lane] * sm.part()[lane].f[0] : 0.f);
+        tot.maxkey = fin ? 0x3f800000u : 0u;
+        if (!kfirst)  // the segment table for draws over the whole row, from each CTA's maximum to the row's
+            for (int i = tid; i < ns; i += NT) sm.mass(0)[i] *= scale[i / a.nsc];
+    }
     const int npos = tot.npos;
     const bool any_bad = tot.any_bad;
     const float M = tot.M;   // sum of the per-CTA ordered sums
     const uint32_t maxkey = tot.maxkey;
-    if (tid < C) sm.cmass()[tid] = sm.part()[tid].f[0];
+    if (tid < C) sm.cmass()[tid] = SOFT ? scale[tid] * sm.part()[tid].f[0] : sm.part()[tid].f[0];
     const float rowmax = __uint_as_float(maxkey);
     bool valid = row_ok && !isnan(tp) && !isnan(mp) && !any_bad && M > 0.f && M <= 3.402823466e38f &&
                  (!SOFT || temp > 0.f);

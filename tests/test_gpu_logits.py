@@ -99,3 +99,32 @@ def test_invalid_rows_and_neg_inf(ms):
     assert not valid[1].any() and not valid[2].any() and not valid[3].any()
     assert (tok[1:4] == -1).all()
     assert (tok[4] % 2 == 1).all()
+
+
+def test_long_rows_and_underflow(ms):
+    """Rows long enough that a segment spans several blocks (V = 600001: the online
+    softmax combines the blocks of a segment), logits far below the maximum (weights
+    that underflow to 0) and whole segments of -inf: membership of every draw in both
+    orders against the oracle's sets, and the law on the short row."""
+    import torch
+    rng = np.random.default_rng(2025)
+    V = 600_001
+    uses = lambda i: [(40, 0.8, None, "top_k_first"), (40, 0.8, None, "joint")]
+    Z = _logit_rows(2, V, 3.0, 4242, uses)
+    Z[1, :300_000] -= 200.0            # weights exp(-200 - ...) underflow to 0
+    Z[1, 400_000:420_000] = -np.inf     # whole segments of -inf
+    P = np.stack([filters.softmax(z) for z in Z])
+    for i in range(2):
+        assert guard_accept(uses)(i, P[i])
+    k = np.full(2, 40, np.int32)
+    p = np.full(2, 0.8, np.float32)
+    Zt = torch.from_numpy(Z).cuda()
+    for order in ("top_k_first", "joint"):
+        masks, vref = allowed_masks(P, k, p, None, order)
+        for call in range(4):
+            tok, valid = ms.top_k_top_p_sampling_from_logits(Zt, None, torch.from_numpy(k).cuda(),
+                                                             torch.from_numpy(p).cuda(), None, order,
+                                                             seed=17, offset=call)
+            tok, valid = tok.cpu().numpy(), valid.cpu().numpy()
+            assert np.array_equal(valid.astype(bool), vref)
+            assert masks[np.arange(2), tok].all(), "a draw outside S"
