@@ -37,11 +37,41 @@ struct FilterArgs {
     int nsc;
 };
 
+// Write `fill` over this CTA's segments whose largest key is below `floor`: their
+// output is fill whatever the threshold, as long as it is at least `floor`.  No
+// reads; streaming stores (the zeros are not read again).
+template <bool VEC>
+__device__ __forceinline__ void fill_below(float* __restrict__ orow, Geom g, Smem sm, uint32_t floor, float fill,
+                                           int warp, int lane) {
+    int r0, r1;
+    warp_range(g.s1 - g.s0, warp, r0, r1);
+    r0 += g.s0;
+    r1 += g.s0;
+    const bool vec_out = VEC && ((reinterpret_cast<uintptr_t>(orow) & 15) == 0);
+#pragma unroll 1
+    for (int sg = r0; sg < r1; ++sg) {
+        if (sm.segkey()[sg] >= floor) continue;
+#pragma unroll 1
+        for (int it = 0; it < g.seg_it(); ++it) {
+            const int base = g.base(sg, it, lane);
+            if (vec_out && base + 3 < g.V) {
+                __stcs(reinterpret_cast<float4*>(orow + base), make_float4(fill, fill, fill, fill));
+            } else {
+#pragma unroll 1
+                for (int q = 0; q < 4; ++q)
+                    if (base + q < g.V) __stcs(orow + base + q, fill);
+            }
+        }
+    }
+}
+
 // Write this CTA's segments: keep key >= t (x / denom, or the logit), else fill.
-// Segments whose maximum key is below t are written without being read.
+// Segments whose maximum key is below t are written without being read; those below
+// `floor` were written already (fill_below) and are skipped.
 template <bool VEC, int KIND>
 __device__ __forceinline__ void write_pass(const float* __restrict__ row, float* __restrict__ orow, Geom g,
-                                       Smem sm, bool valid, uint32_t t, float denom, int warp, int lane) {
+                                       Smem sm, bool valid, uint32_t t, float denom, int warp, int lane,
+                                       uint32_t floor = 0u) {
     using KEYF = typename std::conditional<KIND == K_MASK, KeyLogit, KeyProb>::type;
     constexpr bool IS_PROB = KIND != K_MASK;
     const KEYF keyf;
@@ -49,7 +79,8 @@ __device__ __forceinline__ void write_pass(const float* __restrict__ row, float*
     const bool vec_out = VEC && ((reinterpret_cast<uintptr_t>(orow) & 15) == 0);
     stream_warp<VEC, false>(
         row, g, sm, warp, lane, [&](int sg) { return valid && sm.segkey()[sg] >= t; },
-        [&](int, int, bool on, const float4& v, int base) {
+        [&](int sg, int, bool on, const float4& v, int base) {
+            if (sm.segkey()[sg] < floor) return;
             float o[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -508,12 +539,18 @@ __global__ void __launch_bounds__(NT, 4) filter_kernel(const FilterArgs a) {
     // share.
     uint32_t L0 = 0u;
     int list_mode = -1;  // 0: regions fit, 1: contiguous, -1: no list
+    const bool early = valid && need_hist && orow != row;  // fill the sure part of the output early
     if (k_on) {
         L0 = need_hist ? hist_bound(sm, g, rank, C, k, maxkey, warp, lane, tid) : 0u;
         if (IS_PROB) L0 = max(L0, 1u);
         collect_own<VEC>(row, g, sm, leader, rank, C, rank * (CAP / C), CAP / C, L0, NO_LIMIT, keyf, true, true,
                          warp, lane, tid);
-        cluster_sync();  // every region and count is in every CTA
+        // While the other CTAs finish their candidates: the output of the segments whose
+        // maximum is below L0 (<= t) is the fill, written now when it does not alias the
+        // input (an in-place call keeps the row intact for the fallback search).
+        cluster_arrive();
+        if (early) fill_below<VEC>(orow, g, sm, L0, IS_PROB ? 0.f : __int_as_float(0xff800000), warp, lane);
+        cluster_wait();  // every region and count is in every CTA
         list_mode = settle_list<VEC>(row, g, sm, leader, rank, C, L0, NO_LIMIT, keyf, true, warp, lane, tid);
     }
     if (list_mode >= 0) {
@@ -549,7 +586,7 @@ __global__ void __launch_bounds__(NT, 4) filter_kernel(const FilterArgs a) {
         __syncthreads();
         const uint32_t t = uint32_t(sm.red()[40]);
         const float denom = reinterpret_cast<float*>(sm.red())[41];
-        write_pass<VEC, KIND>(row, orow, g, sm, valid, t, denom, warp, lane);
+        write_pass<VEC, KIND>(row, orow, g, sm, valid, t, denom, warp, lane, early ? L0 : 0u);
         if (leader && tid == 0 && a.out_valid) a.out_valid[b] = valid ? 1 : 0;
         return;
     }
