@@ -437,3 +437,33 @@ def test_launch_plan_fits_one_wave(ms, V):
         assert plans["joint"]["cluster"] >= plans["top_k_first"]["cluster"], plans
     with pytest.raises(ValueError):
         ms.sampling_plan(8, V, "sorted")
+
+
+def test_batch_sizes_and_cluster_sizes(ms):
+    """Batch sizes whose launch plans use clusters of many sizes (16 down to 2 CTAs per
+    row, odd sizes included), V = 32000: top-k-first membership of every draw,
+    top-k / top-p renormalisation and the logit mask exactly as the oracle's."""
+    import torch
+    from tests.test_gpu_filters import _check_renorm, _run as run_filter
+    V = 32000
+    seen = set()
+    for B in (3, 33, 45, 60, 77, 100, 130, 300):
+        acc = guard_accept(lambda i: [(50, 0.9, None, "top_k_first"), (None, 0.9, None, "joint")])
+        w = workloads.config3(batch=B, vocab=V, accept=acc, seed=9000 + B)
+        seen.add(ms.sampling_plan(B, V, "top_k_first")["cluster"])
+        P = torch.from_numpy(w.probs).cuda()
+        ks = np.full(B, 50, np.int32)
+        ps = np.full(B, 0.9, np.float32)
+        masks, vref = allowed_masks(w.probs, ks, ps, None, "top_k_first")
+        for call in range(2):
+            tok, valid, rounds = _call(ms, "top_k_first", P, ks, ps, None, seed=B, offset=call)
+            _membership(masks, vref, tok, valid)
+        out, valid = run_filter(ms, "top_k", w.probs, list(ks))
+        _check_renorm(w.probs, list(ks), out, valid, filters.top_k_renorm)
+        out, valid = run_filter(ms, "top_p", w.probs, list(ps))
+        _check_renorm(w.probs, list(ps), out, valid, filters.top_p_renorm)
+        out, valid = run_filter(ms, "mask", w.logits, list(ks))
+        for i in range(B):
+            exp, ok = filters.top_k_mask_logits(w.logits[i], 50)
+            assert ok and valid[i] and np.array_equal(out[i], exp), (B, i)
+    assert len(seen) >= 5, seen
