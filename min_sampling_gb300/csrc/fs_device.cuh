@@ -519,6 +519,60 @@ __device__ __forceinline__ void stream_warp(const float* __restrict__ row, Geom 
     }
 }
 
+// Warp-collective inclusive prefix sum of 64-bit words.
+__device__ __forceinline__ unsigned long long warp_incl_scan_u64(unsigned long long v, int lane) {
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const unsigned long long o = __shfl_up_sync(FULL, v, d);
+        if (lane >= d) v += o;
+    }
+    return v;
+}
+__device__ __forceinline__ uint32_t warp_incl_scan_t(uint32_t v, int lane) { return uint32_t(warp_incl_scan_i(int(v), lane)); }
+__device__ __forceinline__ unsigned long long warp_incl_scan_t(unsigned long long v, int lane) {
+    return warp_incl_scan_u64(v, lane);
+}
+
+// Warp-collective: scanning the bins h[top], h[top - 1], ... h[0] from the top down,
+// the first bin at which the running count (or mass) reaches kk (-1 when it never
+// does), and in `above` the sum of the bins scanned before it.  Lane l holds four
+// consecutive bins of each window of 128.
+template <typename T>
+__device__ __forceinline__ int scan_bins_down(const T* h, int top, T kk, int lane, T& above) {
+    T before = 0;
+    above = 0;
+#pragma unroll 1
+    for (; top >= 0; top -= 128) {
+        T c[4], own = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int bin = top - 4 * lane - q;
+            c[q] = bin >= 0 ? h[bin] : T(0);
+            own += c[q];
+        }
+        const T incl = warp_incl_scan_t(own, lane);
+        const T total = __shfl_sync(FULL, incl, 31);
+        if (before + total >= kk) {
+            const T excl = before + incl - own;
+            const int l = __ffs(__ballot_sync(FULL, excl < kk && excl + own >= kk)) - 1;
+            T cum = excl;
+            int q = 0;  // the first of the lane's bins where the running sum reaches kk
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                cum += c[t];
+                if (cum < kk) q = t + 1;
+            }
+            T ab = excl;
+#pragma unroll
+            for (int t = 0; t < 4; ++t) ab += t < q ? c[t] : T(0);
+            above = __shfl_sync(FULL, ab, l);
+            return __shfl_sync(FULL, top - 4 * lane - q, l);
+        }
+        before += total;
+    }
+    return -1;
+}
+
 // ------------------------------------------------------------------ pass 1
 
 // One streaming pass over this CTA's segments, in trips of TB blocks (whole segments):
@@ -657,13 +711,16 @@ __device__ __forceinline__ void st_rank_v4(void* local_addr, uint4 v, uint32_t r
 // positive count, u[1] bad flag, u[2] maximum key); and, if `hist_shift` >= 0, the
 // CTA's counts of its segment maxima (key >> hist_shift, made by pass 1 in lv) into the
 // histogram of every CTA of the cluster, each of which cleared its own (and its lv)
-// before that barrier.  The CTA's first segment is a multiple of 4, so the table moves
-// in 16-byte words.  With `online` (pass 1 SOFT = 2) the segment masses are first moved
+// before that barrier.  With `hist_k` > 0 only the CTA's bins from its largest down to
+// the one where its own count reaches hist_k are added: the cluster's count reaches
+// hist_k at or above the highest such bin of any CTA, and every bin from there up is
+// exact, so the top-k bound is the same.  The CTA's first segment is a multiple of 4,
+// so the table moves in 16-byte words.  With `online` (pass 1 SOFT = 2) the segment masses are first moved
 // from each segment's largest logit to the CTA's (times exp((zmax - zcta) / T)), so
 // the table and f[0] are relative to the CTA's maximum logit, u[2].  Block-collective.
 __device__ __forceinline__ void pass1_totals(Geom g, Smem sm, bool leader, int rank, int C, int pos, bool bad,
                                              uint32_t kmax, int hist_shift, bool prob, bool publish, int warp,
-                                             int lane, int tid, bool online = false) {
+                                             int lane, int tid, bool online = false, int hist_k = 0) {
     __syncthreads();  // the table and the local histogram counts written by pass 1
     if (online) {
         if (lane == 0) sm.red()[warp] = int(kmax);  // kmax is the same in every lane of a warp
@@ -711,10 +768,27 @@ __device__ __forceinline__ void pass1_totals(Geom g, Smem sm, bool leader, int r
         rf[3 * NW + warp] = ms;
     }
     __syncthreads();
-    if (hist_shift >= 0) {  // every non-empty bin added once into each CTA's histogram
+    if (hist_shift >= 0) {  // every non-empty bin (of the top ones) added once into each CTA's histogram
+        int top = HBINS - 1, lowest = 0;
+        if (hist_k > 0) {
+            if (warp == 0) {
+                uint32_t mk = 0;
 #pragma unroll
-        for (int q = 0; q < HBINS / NT; ++q) {
-            const int bin = q * NT + tid;
+                for (int w = 0; w < NW; ++w) mk = max(mk, uint32_t(sm.red()[2 * NW + w]));
+                const int tb = int(min(uint32_t(HBINS - 1), mk >> hist_shift));
+                uint32_t ab;
+                const int br = scan_bins_down<uint32_t>(loc, tb, uint32_t(hist_k), lane, ab);
+                if (lane == 0) {
+                    sm.bcast()[0] = tb;
+                    sm.bcast()[1] = max(br, 0);
+                }
+            }
+            __syncthreads();
+            top = sm.bcast()[0];
+            lowest = sm.bcast()[1];
+        }
+#pragma unroll 1
+        for (int bin = lowest + tid; bin <= top; bin += NT) {
             const uint32_t n = loc[bin];
             if (n) {
                 uint32_t* h = &sm.hist()[bin];
@@ -1173,60 +1247,6 @@ __device__ __forceinline__ int filter_list_warp(Smem sm, int n, uint32_t t, KEYF
         w += __popc(bal);
     }
     return w;
-}
-
-// Warp-collective inclusive prefix sum of 64-bit words.
-__device__ __forceinline__ unsigned long long warp_incl_scan_u64(unsigned long long v, int lane) {
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        const unsigned long long o = __shfl_up_sync(FULL, v, d);
-        if (lane >= d) v += o;
-    }
-    return v;
-}
-__device__ __forceinline__ uint32_t warp_incl_scan_t(uint32_t v, int lane) { return uint32_t(warp_incl_scan_i(int(v), lane)); }
-__device__ __forceinline__ unsigned long long warp_incl_scan_t(unsigned long long v, int lane) {
-    return warp_incl_scan_u64(v, lane);
-}
-
-// Warp-collective: scanning the bins h[top], h[top - 1], ... h[0] from the top down,
-// the first bin at which the running count (or mass) reaches kk (-1 when it never
-// does), and in `above` the sum of the bins scanned before it.  Lane l holds four
-// consecutive bins of each window of 128.
-template <typename T>
-__device__ __forceinline__ int scan_bins_down(const T* h, int top, T kk, int lane, T& above) {
-    T before = 0;
-    above = 0;
-#pragma unroll 1
-    for (; top >= 0; top -= 128) {
-        T c[4], own = 0;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int bin = top - 4 * lane - q;
-            c[q] = bin >= 0 ? h[bin] : T(0);
-            own += c[q];
-        }
-        const T incl = warp_incl_scan_t(own, lane);
-        const T total = __shfl_sync(FULL, incl, 31);
-        if (before + total >= kk) {
-            const T excl = before + incl - own;
-            const int l = __ffs(__ballot_sync(FULL, excl < kk && excl + own >= kk)) - 1;
-            T cum = excl;
-            int q = 0;  // the first of the lane's bins where the running sum reaches kk
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                cum += c[t];
-                if (cum < kk) q = t + 1;
-            }
-            T ab = excl;
-#pragma unroll
-            for (int t = 0; t < 4; ++t) ab += t < q ? c[t] : T(0);
-            above = __shfl_sync(FULL, ab, l);
-            return __shfl_sync(FULL, top - 4 * lane - q, l);
-        }
-        before += total;
-    }
-    return -1;
 }
 
 // Block- and cluster-collective (every CTA of the cluster calls it with the same row,

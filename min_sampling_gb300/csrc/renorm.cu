@@ -518,7 +518,7 @@ __global__ void __launch_bounds__(NT, 4) filter_kernel(const FilterArgs a) {
                                kmax);
     cluster_wait();  // every CTA has started and cleared its histogram
     pass1_totals(g, sm, leader, rank, C, pos, bad, kmax, need_hist ? 21 : -1, IS_PROB, false, warp,
-                 lane, tid);
+                 lane, tid, false, need_hist ? k : 0);
     if (KIND == K_TOPP) {  // the top-p receive buffers (over the segment masses, now read) and list count
         for (int i = tid; i < 2 * int(Layout::TOPPW); i += NT) sm.topp_recv(0)[i] = 0ull;
         if (tid == 0) sm.red()[100] = 0;

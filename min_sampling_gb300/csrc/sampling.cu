@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
     }
     cluster_wait();  // every CTA has started and cleared its histogram
     pass1_totals(g, sm, leader, rank, C, pos, bad, kmax, need_hist ? 21 : -1, !(SOFT && kfirst), !kfirst, warp, lane,
-                 tid, SOFT && !kfirst);
+                 tid, SOFT && !kfirst, need_hist ? k : 0);
     cluster_sync();  // the leader's segment table, every CTA's parts and histogram, are complete
 
     // Rows of logits: the row's largest logit m (the CTAs' maxima are logit keys in
