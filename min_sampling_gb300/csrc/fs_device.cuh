@@ -3,15 +3,18 @@
 // Execution model: one thread-block cluster of C CTAs per row, rank 0 the leader.
 // A row is cut into segments of 128 * 2^shift elements (128 = one float4 per lane of
 // a warp); CTA c owns a contiguous range of them.  Every CTA streams its range from
-// HBM exactly once (pass 1), keeps each segment's maximum order key and mass, and
-// also stores them into the leader's shared memory (distributed shared memory
-// stores), together with the CTA's totals and, when a top-k bound is needed, its share
-// of a histogram of the segment maxima (distributed shared memory atomics).  After
-// one cluster barrier the leader holds the row's segment table and totals.  From there
-// it drives the rest with commands written into the other CTAs' shared memory (a
-// candidate collection, a two-pivot reduction, a three-pivot bisection pass, a masked
-// write, exit), each bracketed by two cluster barriers; when little data is left it
-// finishes alone.  Every CTA executes the same sequence of cluster barriers.
+// HBM exactly once (pass 1) and keeps each segment's maximum order key and mass; it
+// sends its totals to every CTA, its segment masses into the leader's shared memory
+// when a draw over the whole row may need them (distributed shared memory stores),
+// and, when a top-k bound is needed, the top of its histogram of segment maxima into
+// every CTA's (distributed shared memory atomics).  After one cluster barrier every
+// CTA can derive the same top-k bound and gather its candidates.  Paths that need the
+// whole cluster afterwards are driven by the leader through commands written into the
+// other CTAs' shared memory (a candidate collection, a two-pivot reduction, a 7-pivot
+// threshold-search pass, a masked write, exit), each bracketed by two cluster
+// barriers; when little data is left the leader finishes alone.  The top-p filter
+// runs symmetric histogram passes instead (renorm.cu).  Every CTA executes the same
+// sequence of cluster barriers.
 //
 // Code size is kept small on purpose: the work after pass 1 runs once per CTA, from a
 // cold instruction cache, on every SM at the same moment.

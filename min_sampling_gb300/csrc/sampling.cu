@@ -18,6 +18,10 @@
 // over the segments whose maximum exceeds pivot1 (read again through L2); once at most
 // CAP tokens are left, the leader gathers them in index order and finishes alone on
 // one warp.
+// Rows of logits (the from-logits entry, temperature T) are read once as well: pass 1
+// keeps logit keys and, where draws over the whole row need them, each segment's mass
+// relative to its own largest logit (an online softmax); after the first barrier the
+// row's maximum m is known and every later read sees the weights exp((z - m) / T).
 #include "fs_device.cuh"
 #include "fs_host.h"
 
