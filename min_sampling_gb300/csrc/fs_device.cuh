@@ -1794,10 +1794,16 @@ __device__ __forceinline__ void search_list(Smem sm, int n, Search& st, int kcri
 // region of the leader's list; again at exact offsets if a region overflowed).
 // Returns n, or -1 when more than CAP elements qualify (the peers then still wait for
 // commands).  With `exit_if_fit` the peers have left whenever n >= 0.
+//
+// With `count_u` >= 0 the leader already holds each CTA's exact count of those
+// elements, in part[r].u[count_u] (from the last reduction, with at most CAP in all):
+// CTA r's base offset (the sum of the counts before it) goes into its bcast[2] with
+// the command (ib = 1), so the CTAs write one contiguous list at once and nothing
+// overflows or needs collecting again.
 template <bool VEC, typename KEYF>
 __device__ __forceinline__ int gather_leader(const float* __restrict__ row, Geom g, Smem sm, int C, uint32_t thr,
                                              uint64_t thr_hi, KEYF keyf, bool exit_if_fit, int warp, int lane,
-                                             int tid) {
+                                             int tid, int count_u = -1) {
     const int rc = CAP / C;
     Ctl c{};
     c.cmd = CMD_COLLECT;
@@ -1805,6 +1811,26 @@ __device__ __forceinline__ int gather_leader(const float* __restrict__ row, Geom
     c.u[0] = thr;
     c.hi_lo = uint32_t(thr_hi);
     c.hi_hi = uint32_t(thr_hi >> 32);
+    if (count_u >= 0) {
+        c.ib = 1;
+        if (tid < C) {  // thread r: rank r's base offset, into rank r's bcast[2]
+            int base = 0;
+#pragma unroll 1
+            for (int r = 0; r < tid; ++r) base += int(sm.part()[r].u[count_u]);
+            if (tid == 0) {
+                sm.bcast()[2] = base;
+            } else {
+                st_dsmem_u32(map_rank(smem_u32(&sm.bcast()[2]), uint32_t(tid)), uint32_t(base));
+            }
+        }
+        int total = 0;
+#pragma unroll 1
+        for (int r = 0; r < C; ++r) total += int(sm.part()[r].u[count_u]);
+        send_command(sm, c, C, tid);  // its barrier also publishes the bases
+        collect_own<VEC>(row, g, sm, true, 0, C, 0, CAP, thr, thr_hi, keyf, false, false, warp, lane, tid);
+        cluster_sync();  // every CTA's elements are in place
+        return total;
+    }
     send_command(sm, c, C, tid);
     collect_own<VEC>(row, g, sm, true, 0, C, 0, rc, thr, thr_hi, keyf, false, true, warp, lane, tid);
     cluster_sync();  // every region and count is in

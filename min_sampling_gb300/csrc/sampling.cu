@@ -86,17 +86,23 @@ __device__ __forceinline__ void sample_peer(const float* __restrict__ row, Geom 
             search_pass<VEC, true, false>(row, g, sm, false, rank, c.u[0], hi, KeyProb(), warp, lane, tid);
         } else if (c.cmd == CMD_COLLECT) {
             const uint64_t hi = uint64_t(c.hi_lo) | (uint64_t(c.hi_hi) << 32);
-            collect_own<VEC>(row, g, sm, false, rank, C, rank * (CAP / C), CAP / C, c.u[0], hi, KeyProb(), false,
-                             true, warp, lane, tid);
+            // ib = 1: exact offsets (this CTA's base in bcast[2]); else a region of CAP / C
+            const int base = c.ib ? sm.bcast()[2] : rank * (CAP / C);
+            collect_own<VEC>(row, g, sm, false, rank, C, base, c.ib ? CAP - base : CAP / C, c.u[0], hi, KeyProb(),
+                             false, c.ib == 0, warp, lane, tid);
         } else {
             return;  // CMD_EXIT
         }
         cluster_sync();  // the results are in the leader
         if (c.cmd == CMD_COLLECT) {
-            const uint64_t hi = uint64_t(c.hi_lo) | (uint64_t(c.hi_hi) << 32);
-            const int mode = settle_list<VEC>(row, g, sm, false, rank, C, c.u[0], hi, KeyProb(), false, warp, lane,
-                                              tid);
-            if (c.flag && mode >= 0) return;
+            if (c.ib) {
+                if (c.flag) return;
+            } else {
+                const uint64_t hi = uint64_t(c.hi_lo) | (uint64_t(c.hi_hi) << 32);
+                const int mode = settle_list<VEC>(row, g, sm, false, rank, C, c.u[0], hi, KeyProb(), false, warp,
+                                                  lane, tid);
+                if (c.flag && mode >= 0) return;
+            }
         }
     }
 }
@@ -389,6 +395,7 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
         float low = 0.f, high = rowmax, S_low = M;
         int cur = 0;            // mass(cur)[s] = mass of segment s above `low`
         int count_low = npos;   // tokens above `low`
+        int low_u = -1;         // part[c].u[low_u]: CTA c's exact count above `low` (-1: not known)
         int n_list = 0;
         bool compact = false;
         f.pthr = tp * M;
@@ -450,6 +457,7 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
                     const bool inC = lane < C;
                     const Part& pc = sm.part()[inC ? lane : 0];
                     count_low = warp_sum_i(inC ? int(pc.u[0]) : 0);
+                    low_u = 0;
                     S_low = warp_sum(inC ? pc.f[0] : 0.f);
                 }
                 if (tid < C) sm.cmass()[tid] = sm.part()[tid].f[0];
@@ -463,7 +471,8 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
         for (int round = 0; round < R_MAX; ++round) {
             if (!compact && count_low <= CAP) {
                 // Few tokens left above `low`: gather them; the leader goes on alone.
-                n_list = gather_leader<VEC>(row, g, sm, C, prob_key(low) + 1u, NO_LIMIT, keyf, true, warp, lane, tid);
+                n_list = gather_leader<VEC>(row, g, sm, C, prob_key(low) + 1u, NO_LIMIT, keyf, true, warp, lane, tid,
+                                            low_u);
                 if (n_list >= 0) peers = false;  // they left with the completed list
                 dismiss();
                 if (n_list < 0) break;
@@ -536,11 +545,13 @@ __global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
                 high = pivot2;
                 S_low = M1;
                 count_low = C1;
+                low_u = 0;
                 cur = ia;
             } else {
                 low = pivot2;
                 S_low = M2;
                 count_low = C2;
+                low_u = 1;
                 cur = ib;
             }
             if (tid < C) sm.cmass()[tid] = narrow ? sm.part()[tid].f[0] : sm.part()[tid].f[1];
