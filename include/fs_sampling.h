@@ -155,8 +155,10 @@ fs_status fs_top_k_top_p_sampling_rng(const float* probs, int32_t batch_in, int3
 
 /* Sampling from logits with the softmax fused in ([explainer] the sampling pipeline:
  * p = softmax(z / T) before the filters).  logits: [batch_in, vocab] float32.  The row
- * is read once for its maximum m; the rest of the path (every filter, order and the
- * dual-pivot rounds, exactly as fs_top_k_top_p_sampling) then runs on the weights
+ * is read from HBM once (an online softmax: the first pass keeps each segment's
+ * largest logit and, where needed, its mass relative to it; the row maximum m follows
+ * from the CTAs'); the rest of the path (every filter, order and the dual-pivot
+ * rounds, exactly as fs_top_k_top_p_sampling) then runs on the weights
  * w = exp((z - m) / T) in float32 -- the unnormalised softmax, read again from L2 --
  * so no probability matrix is written.  temperature: [batch_out] float32, nullable
  * (1); T <= 0 or NaN makes the row invalid.  top_k, top_p, min_p: nullable.  A NaN
