@@ -64,6 +64,9 @@ def parse_args_from(argv):
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-oracle sample")
     ap.add_argument("--profile", action="store_true",
                     help="only run the headline step (warmup + steps launches) for a profiler; prints a short line")
+    ap.add_argument("--profile-entry", default="top_k_first",
+                    help="with --profile: the entry to launch (top_k_first, joint, from_probs, top_k_renorm, "
+                         "top_p_renorm, mask_logits, top_k_first_from_logits, joint_single_pivot)")
     return ap.parse_args(argv)
 
 
@@ -302,11 +305,13 @@ def run_ours(args):
 
     K, W = args.steps, args.warmup
     if args.profile:
+        if args.profile_entry not in calls:
+            raise SystemExit(f"unknown --profile-entry {args.profile_entry!r}")
         for i in range(W + K):
-            calls["top_k_first"](i)
+            calls[args.profile_entry](i)
         torch.cuda.synchronize(dev)
         if rank == 0:
-            print(json.dumps({"profile": "top_k_first", "launches": W + K, "batch": B, "vocab": V}), flush=True)
+            print(json.dumps({"profile": args.profile_entry, "launches": W + K, "batch": B, "vocab": V}), flush=True)
         return
     total_ms, per, clk = timed(calls["top_k_first"], K, W, clocks=True)
     kern_ms = total_ms / K   # average launch duration in the back-to-back timed region
