@@ -228,7 +228,7 @@ __device__ __forceinline__ int small_rounds(const Small& s, const bool* kept, co
 
 
 template <bool VEC, bool SOFT>
-__global__ void __launch_bounds__(NT, 4) sample_kernel(const SampleArgs a) {
+__global__ void __launch_bounds__(NT, 3) sample_kernel(const SampleArgs a) {
     const int C = int(cluster_nctarank());
     const int rank = int(cluster_ctarank());
     const int b = int(cluster_id_x());
