@@ -918,17 +918,22 @@ __device__ __forceinline__ uint32_t soft_bound(const Geom& g, uint32_t L) {
 // ------------------------------------------------------------------ candidate lists
 
 // Every element with thr <= key < thr_hi of the segments [a, b), in index order:
-// out(p, value, index) for p = 0, 1, ...  Returns the exact count.  Warp w takes the
-// w-th contiguous share of [a, b), lists its segments whose maximum key is >= thr
-// (into list[], inside its own share), stages their blocks 2*SBH at a time
-// (cp.async) and counts; one block barrier turns the warps' counts into output
-// offsets; then each warp emits (from the staged blocks, or staging again when it
-// had more than one batch).  Block-collective; red[0..NW) is used.
+// out(p, value, index) for p = 0, 1, ...  Returns the exact count (the same in every
+// thread).  Each warp lists the segments of its contiguous share of [a, b) whose
+// maximum key is >= thr (into list[], inside its share); after one block barrier the
+// live blocks, in index order, are dealt round-robin to the warps, CB at a time, so
+// that every warp stages at most CB / NW of them at once (cp.async, into its part of
+// the staging area; a crowded share no longer serialises its warp); the blocks' counts
+// meet in red[] and a second barrier turns them into output offsets.  Block-collective;
+// red[0, NW + CB) is used, and the caller has synchronised the block since its own
+// last use of red.
 template <bool VEC, typename KEYF, typename OUT>
 __device__ __forceinline__ int collect_range(const float* __restrict__ row, Geom g, Smem sm, int a, int b,
                                              uint32_t thr, uint64_t thr_hi, KEYF keyf, int warp, int lane,
                                              OUT out) {
-    constexpr int WB = 2 * SBH;  // blocks per batch
+    constexpr int PW = 2 * SBH;  // blocks per warp in flight: its staging buffer
+    constexpr int CB = NW * PW;  // blocks per batch (one count per lane of a warp)
+    static_assert(CB == 32 && NW + CB <= REDW, "a batch's counts fit one warp and the scratch");
     int r0, r1;
     warp_range(b - a, warp, r0, r1);
     r0 += a;
@@ -943,59 +948,72 @@ __device__ __forceinline__ int collect_range(const float* __restrict__ row, Geom
         if (live) sm.list()[r0 + nl + __popc(bal & ((1u << lane) - 1u))] = i;
         nl += __popc(bal);
     }
-    __syncwarp();
-    const int nblk = nl << g.shift;
+    if (lane == 0) sm.red()[warp] = nl;
+    __syncthreads();
+    // Lane w < NW: warp w's live count, the inclusive prefix over warps, and its share's start.
+    const int wn = lane < NW ? sm.red()[lane] : 0;
+    const int wincl = warp_incl_scan_i(wn, lane);
+    int ws0, ws1;
+    warp_range(b - a, lane < NW ? lane : 0, ws0, ws1);
+    const int nblk = __shfl_sync(FULL, wincl, NW - 1) << g.shift;
     const int mask = g.seg_it() - 1;
-    float* st = sm.stage() + warp * (WB * BLK) + lane * 4;
-    auto block_base = [&](int lb) { return g.base(sm.list()[r0 + (lb >> g.shift)], lb & mask, lane); };
-    auto stage = [&](int c0) {
-#pragma unroll 1
-        for (int j = 0; j < WB && c0 + j < nblk; ++j) stage4<VEC>(st + j * BLK, row, g.V, block_base(c0 + j));
-        cp_async_commit();
-        cp_async_wait<0>();
+    // The element base of live block j (in index order) for this lane.
+    auto block_base = [&](int j) {
+        const int s = j >> g.shift;  // its ordinal among the live segments
+        const int w = __popc(__ballot_sync(FULL, lane < NW && wincl <= s));
+        const int first = __shfl_sync(FULL, wincl - wn, w);
+        const int start = __shfl_sync(FULL, ws0, w) + a;
+        return g.base(sm.list()[start + s - first], j & mask, lane);
     };
-    auto keep = [&](int j, int base, int q) {
-        const uint32_t key = keyf(g.val(st[j * BLK + q]));
+    auto keep = [&](float x, int base, int q) {
+        const uint32_t key = keyf(g.val(x));
         return key >= thr && uint64_t(key) < thr_hi && base + q < g.V;
     };
-    int cnt = 0;
+    float* st = sm.stage() + warp * (PW * BLK) + lane * 4;
+    int total = 0;
 #pragma unroll 1
-    for (int c0 = 0; c0 < nblk; c0 += WB) {
-        stage(c0);
-#pragma unroll 1
-        for (int j = 0; j < WB && c0 + j < nblk; ++j) {
-            const int base = block_base(c0 + j);
+    for (int c0 = 0; c0 < nblk; c0 += CB) {
+        if (c0) __syncthreads();  // every warp has read the previous batch's counts
+        int bs[PW];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) cnt += keep(j, base, q);
+        for (int i = 0; i < PW; ++i) {
+            const int j = c0 + warp + NW * i;
+            bs[i] = j < nblk ? block_base(j) : 0;
+            if (j < nblk) stage4<VEC>(st + i * BLK, row, g.V, bs[i]);
         }
-    }
-    cnt = warp_sum_i(cnt);
-    if (lane == 0) sm.red()[warp] = cnt;
-    __syncthreads();
-    int pos = 0, total = 0;
+        cp_async_commit();
+        cp_async_wait<0>();  // each lane reads back only the words it staged
 #pragma unroll
-    for (int w = 0; w < NW; ++w) {
-        const int c = sm.red()[w];
-        pos += w < warp ? c : 0;
-        total += c;
-    }
-    __syncthreads();
-#pragma unroll 1
-    for (int c0 = 0; c0 < nblk; c0 += WB) {
-        if (nblk > WB) stage(c0);  // one batch is still staged from the count
-#pragma unroll 1
-        for (int j = 0; j < WB && c0 + j < nblk; ++j) {
-            const int base = block_base(c0 + j);
-            int k = 0;
+        for (int i = 0; i < PW; ++i) {
+            const int j = c0 + warp + NW * i;
+            if (j < nblk) {
+                int k = 0;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) k += keep(j, base, q);
-            const int incl = warp_incl_scan_i(k, lane);
-            int p = pos + incl - k;
-#pragma unroll 1
-            for (int q = 0; q < 4; ++q)
-                if (keep(j, base, q)) out(p++, g.val(st[j * BLK + q]), base + q);
-            pos += __shfl_sync(FULL, incl, 31);
+                for (int q = 0; q < 4; ++q) k += keep(st[i * BLK + q], bs[i], q);
+                k = warp_sum_i(k);
+                if (lane == 0) sm.red()[NW + (j - c0)] = k;
+            }
         }
+        __syncthreads();
+        // Lane l: the count of the batch's block l and the inclusive prefix.
+        const int bc = c0 + lane < nblk ? sm.red()[NW + lane] : 0;
+        const int bincl = warp_incl_scan_i(bc, lane);
+#pragma unroll 1
+        for (int i = 0; i < PW; ++i) {
+            const int jl = warp + NW * i;
+            if (c0 + jl < nblk) {
+                int p = total + __shfl_sync(FULL, bincl - bc, jl);
+                int k = 0;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) k += keep(st[i * BLK + q], bs[i], q);
+                const int incl = warp_incl_scan_i(k, lane);
+                p += incl - k;
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (keep(st[i * BLK + q], bs[i], q)) out(p++, g.val(st[i * BLK + q]), bs[i] + q);
+            }
+        }
+        total += __shfl_sync(FULL, bincl, 31);
     }
     return total;
 }

@@ -478,8 +478,11 @@ __device__ __forceinline__ void topp_threshold(const float* __restrict__ row, Ge
     denom_out = __uint_as_float(sm.part()[rank].u[9]);
 }
 
+// The single-pass kinds run at most 3 CTAs per SM (the launch plan's cap), so they are
+// compiled for 3 and keep their working set in registers; top-p renorm takes the
+// occupancy limit for its multi-pass plan.
 template <bool VEC, int KIND>
-__global__ void __launch_bounds__(NT, 4) filter_kernel(const FilterArgs a) {
+__global__ void __launch_bounds__(NT, KIND == K_TOPP ? 4 : 3) filter_kernel(const FilterArgs a) {
     using KEYF = typename std::conditional<KIND == K_MASK, KeyLogit, KeyProb>::type;
     constexpr bool IS_PROB = KIND != K_MASK;
     const KEYF keyf;
