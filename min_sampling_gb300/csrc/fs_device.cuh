@@ -133,6 +133,7 @@ struct Smem {
     __device__ __forceinline__ float* cmass() const { return at<float>(Layout::MISC); }     // [MAX_CLUSTER]
     __device__ __forceinline__ int* ctr() const { return at<int>(Layout::MISC + 64); }      // pass-1 trip counter
     __device__ __forceinline__ int* bcast() const { return at<int>(Layout::MISC + 80); }    // [4] CTA broadcast
+    __device__ __forceinline__ uint32_t* prm() const { return at<uint32_t>(Layout::MISC + 96); }  // [8] row parameters
     __device__ __forceinline__ uint32_t* segkey() const { return at<uint32_t>(Layout(ns).arr(0)); }
     __device__ __forceinline__ float* mass(int i) const { return at<float>(Layout(ns).arr(1 + i)); }  // i < 3
     __device__ __forceinline__ int* list() const { return at<int>(Layout(ns).arr(4)); }     // live segments
@@ -586,7 +587,10 @@ __device__ __forceinline__ int scan_bins_down(const T* h, int top, T kk, int lan
 // or negative for probabilities, NaN for logits) and the largest key seen.  With
 // `hist_shift` >= 0 every segment maximum is also counted into the CTA's local
 // histogram (lv, cleared beforehand) at bin key >> hist_shift.  Touches no other CTA,
-// so it may run before the cluster's first barrier completes.
+// so it may run before the cluster's first barrier completes.  `prologue` runs in
+// every thread once the first trip's loads are issued (the block-wide set-up that the
+// counter and the histogram need: it ends with a block barrier), so that set-up
+// overlaps the first round trip to memory.
 //
 // SOFT (rows of logits sampled through a softmax, read once; PROB false): keys are
 // logit keys, the positive count is the count of logits above -inf, and +inf is a bad
@@ -594,9 +598,12 @@ __device__ __forceinline__ int scan_bins_down(const T* h, int top, T kk, int lan
 // relative to its own largest logit zmax (1/T = g.vinv), the running maximum of an
 // online softmax; pass1_totals moves the masses to the CTA's maximum and the sampler to
 // the row's.  SOFT = 1 keeps no masses (paths that draw only from gathered candidates).
-template <bool VEC, bool NC, bool PROB, int SOFT = 0>
+struct NoPrologue {
+    __device__ __forceinline__ void operator()() const {}
+};
+template <bool VEC, bool NC, bool PROB, int SOFT = 0, typename PRO = NoPrologue>
 __device__ __forceinline__ void pass1(const float* __restrict__ row, Geom g, Smem sm, int hist_shift, int warp,
-                                      int lane, int& pos, bool& bad, uint32_t& kmax) {
+                                      int lane, int& pos, bool& bad, uint32_t& kmax, PRO prologue = PRO()) {
     const int spt = TB >> g.shift;  // segments per trip
     const int ntrip = (g.s1 - g.s0 + spt - 1) / spt;
     const int mask = g.seg_it() - 1;
@@ -615,6 +622,7 @@ __device__ __forceinline__ void pass1(const float* __restrict__ row, Geom g, Sme
     float4 A[TB], Bv[TB];
     int t = warp;  // the first NW trips are fixed; later ones are taken from the counter
     load_trip(t, A);
+    prologue();  // block-wide set-up, while the first trip's loads are in flight
 #pragma unroll 1
     while (t < ntrip) {
         int tn = 0;

@@ -245,49 +245,73 @@ __global__ void __launch_bounds__(NT, 3) sample_kernel(const SampleArgs a) {
     const int r = a.indices ? a.indices[b] : b;
     const bool row_ok = r >= 0 && r < a.batch_in;
     const float* row = a.probs + size_t(row_ok ? r : 0) * size_t(V);
-    const int k = a.top_k ? a.top_k[b] : 0;
-    const float tp = a.top_p ? a.top_p[b] : 1.f;
-    // The row's generator state ([explainer] RNG ownership).
-    const unsigned long long seed_b = a.seeds ? a.seeds[b] : a.seed;
-    const unsigned long long offset_b = (a.offsets ? a.offsets[b] : a.offset) + (a.offset_dev ? *a.offset_dev : 0ull);
-    const uint32_t stream_b = a.seeds ? 0u : uint32_t(b);
-    const float mp = a.min_p ? a.min_p[b] : 0.f;
-    const bool k_on = k > 0 && k < V;
-    const bool kfirst = a.order == 0 && k_on;
-    const bool need_hist = kfirst && ns >= k;
+    // The logits path picks its pass-1 variant by the row's k and needs 1/T in pass 1;
+    // the other parameters are read after pass 1 (below).
+    const int k_soft = SOFT && a.top_k ? a.top_k[b] : 0;
     const float temp = SOFT && a.temperature ? a.temperature[b] : 1.f;
+    const bool kfirst_soft = SOFT && a.order == 0 && k_soft > 0 && k_soft < V;
+    // Pass 1 counts segment maxima into the histogram in every top-k-first launch of
+    // probabilities, whatever the row's k, so that the row streams without waiting for
+    // its parameters; rows that need no top-k bound leave the counts unused.
+    const int hist_sh = (SOFT ? (kfirst_soft && ns >= k_soft) : (a.order == 0 && a.top_k != nullptr)) ? 21 : -1;
 
     // Rows of logits are read once too: pass 1 keeps, per segment, its largest logit and
     // its mass relative to it (an online softmax); the row's maximum follows from the
     // CTAs' after the barrier.
     if (SOFT) g.vinv = 1.f / temp;
 
-    // ---- a2: pass 1, the only HBM read of the row, inside a split cluster barrier
-    if (need_hist)
-        for (int i = tid; i < HBINS; i += NT) {
-            sm.hist()[i] = 0u;
-            sm.hist()[HBINS + i] = 0u;
-            reinterpret_cast<uint32_t*>(sm.lv())[i] = 0u;
+    // ---- a2: pass 1, the only HBM read of the row, inside a split cluster barrier.
+    // Its set-up runs once the first loads are in flight: the histograms cleared, the
+    // trip counter, the cluster's first arrive; then one lane copies the row's
+    // parameters into shared memory, read after the block barrier that follows pass 1.
+    auto setup = [&]() {
+        if (hist_sh >= 0)
+            for (int i = tid; i < HBINS; i += NT) {
+                sm.hist()[i] = 0u;
+                sm.hist()[HBINS + i] = 0u;
+                reinterpret_cast<uint32_t*>(sm.lv())[i] = 0u;
+            }
+        if (tid == 0) *sm.ctr() = NW;
+        __syncthreads();
+        cluster_arrive();
+        if (tid == NT - 32) {
+            uint32_t* pr = sm.prm();
+            pr[0] = uint32_t(a.top_k ? a.top_k[b] : 0);
+            pr[1] = __float_as_uint(a.top_p ? a.top_p[b] : 1.f);
+            pr[2] = __float_as_uint(a.min_p ? a.min_p[b] : 0.f);
+            // The row's generator state ([explainer] RNG ownership).
+            *reinterpret_cast<unsigned long long*>(pr + 4) = a.seeds ? a.seeds[b] : a.seed;
+            *reinterpret_cast<unsigned long long*>(pr + 6) =
+                (a.offsets ? a.offsets[b] : a.offset) + (a.offset_dev ? *a.offset_dev : 0ull);
         }
-    if (tid == 0) *sm.ctr() = NW;
-    __syncthreads();
-    cluster_arrive();
+    };
     int pos = 0;
     bool bad = false;
     uint32_t kmax = 0;
     if (row_ok) {
-        if (SOFT && kfirst)  // draws come from the gathered candidates: keys only
-            pass1<VEC, true, false, 1>(row, g, sm, need_hist ? 21 : -1, warp, lane, pos, bad, kmax);
+        if (SOFT && kfirst_soft)  // draws come from the gathered candidates: keys only
+            pass1<VEC, true, false, 1>(row, g, sm, hist_sh, warp, lane, pos, bad, kmax, setup);
         else if (SOFT)
-            pass1<VEC, true, false, 2>(row, g, sm, -1, warp, lane, pos, bad, kmax);
+            pass1<VEC, true, false, 2>(row, g, sm, -1, warp, lane, pos, bad, kmax, setup);
         else
-            pass1<VEC, true, true>(row, g, sm, need_hist ? 21 : -1, warp, lane, pos, bad, kmax);
+            pass1<VEC, true, true>(row, g, sm, hist_sh, warp, lane, pos, bad, kmax, setup);
     } else {
+        setup();
         for (int i = g.s0 + tid; i < g.s1; i += NT) {
             sm.segkey()[i] = 0u;
             sm.mass(0)[i] = 0.f;
         }
     }
+    __syncthreads();  // the row's parameters
+    const int k = int(sm.prm()[0]);
+    const float tp = __uint_as_float(sm.prm()[1]);
+    const float mp = __uint_as_float(sm.prm()[2]);
+    const unsigned long long seed_b = *reinterpret_cast<const unsigned long long*>(sm.prm() + 4);
+    const unsigned long long offset_b = *reinterpret_cast<const unsigned long long*>(sm.prm() + 6);
+    const uint32_t stream_b = a.seeds ? 0u : uint32_t(b);
+    const bool k_on = k > 0 && k < V;
+    const bool kfirst = a.order == 0 && k_on;
+    const bool need_hist = kfirst && ns >= k;
     cluster_wait();  // every CTA has started and cleared its histogram
     pass1_totals(g, sm, leader, rank, C, pos, bad, kmax, need_hist ? 21 : -1, !(SOFT && kfirst), !kfirst, warp, lane,
                  tid, SOFT && !kfirst, need_hist ? k : 0);
