@@ -136,6 +136,17 @@ def _rows(v, n: int, dtype: torch.dtype, device, name: str) -> torch.Tensor:
     return torch.full((n,), v, dtype=dtype, device=device)
 
 
+def _indices(indices, b_in: int, device):
+    """The output-row -> input-row map (None: one output row per input row) and the
+    output batch.  The kernels read it on the device, so it must live there."""
+    if indices is None:
+        return None, b_in
+    if not (isinstance(indices, torch.Tensor) and indices.dim() == 1 and indices.dtype == torch.int32
+            and indices.device == device and indices.is_contiguous()):
+        raise ValueError("indices must be a contiguous 1-D int32 tensor on the input's device")
+    return indices, indices.shape[0]
+
+
 def _order(order: Union[str, int]) -> int:
     if order in ("top_k_first", ORDER_TOP_K_FIRST):
         return ORDER_TOP_K_FIRST
@@ -154,13 +165,7 @@ def _sample(fn_name: str, probs, indices, seed, offset, params, return_rounds, o
     probs = _matrix(probs, "probs")
     b_in, V = probs.shape
     dev = probs.device
-    if indices is not None:
-        if not (isinstance(indices, torch.Tensor) and indices.dim() == 1 and indices.dtype == torch.int32
-                and indices.device == dev and indices.is_contiguous()):
-            raise ValueError("indices must be a contiguous 1-D int32 tensor on the probs' device")
-        b_out = indices.shape[0]
-    else:
-        b_out = b_in
+    indices, b_out = _indices(indices, b_in, dev)
     p_args = []
     for v, dtype, name in params:
         p_args.append(None if v is None else _rows(v, b_out, dtype, dev, name))
@@ -210,13 +215,7 @@ def top_k_top_p_sampling_rng(probs, top_k=None, top_p=None, min_p=None, order="j
     probs = _matrix(probs, "probs")
     b_in, V = probs.shape
     dev = probs.device
-    if indices is not None:
-        if not (isinstance(indices, torch.Tensor) and indices.dim() == 1 and indices.dtype == torch.int32
-                and indices.device == dev and indices.is_contiguous()):
-            raise ValueError("indices must be a contiguous 1-D int32 tensor on the probs' device")
-        b_out = indices.shape[0]
-    else:
-        b_out = b_in
+    indices, b_out = _indices(indices, b_in, dev)
 
     def u64(t, n, name):
         if t is None:
@@ -245,7 +244,7 @@ def top_k_top_p_sampling_pivots(probs, top_k=None, top_p=None, min_p=None, order
     probs = _matrix(probs, "probs")
     b_in, V = probs.shape
     dev = probs.device
-    b_out = b_in if indices is None else indices.shape[0]
+    indices, b_out = _indices(indices, b_in, dev)
     ps = [None if v is None else _rows(v, b_out, dt, dev, n)
           for v, dt, n in ((top_k, torch.int32, "top_k"), (top_p, torch.float32, "top_p"),
                            (min_p, torch.float32, "min_p"))]
@@ -263,7 +262,7 @@ def top_k_top_p_sampling_from_logits(logits, temperature=None, top_k=None, top_p
     logits = _matrix(logits, "logits")
     b_in, V = logits.shape
     dev = logits.device
-    b_out = b_in if indices is None else indices.shape[0]
+    indices, b_out = _indices(indices, b_in, dev)
     ps = [None if v is None else _rows(v, b_out, dt, dev, n)
           for v, dt, n in ((temperature, torch.float32, "temperature"), (top_k, torch.int32, "top_k"),
                            (top_p, torch.float32, "top_p"), (min_p, torch.float32, "min_p"))]
@@ -333,8 +332,8 @@ def _filter(fn_name, x, param, dtype, pname, out):
     B, V = x.shape
     p = _rows(param, B, dtype, x.device, pname)
     out = torch.empty_like(x) if out is None else _matrix(out, "out")
-    if out.shape != x.shape:
-        raise ValueError("out must have the input's shape")
+    if out.shape != x.shape or out.device != x.device:
+        raise ValueError("out must have the input's shape and device")
     valid = torch.empty(B, dtype=torch.uint8, device=x.device)
     _check(getattr(_lib(), fn_name)(_ptr(x), B, V, _ptr(p), _ptr(out), _ptr(valid), _stream()))
     return out, valid
@@ -356,8 +355,8 @@ def philox4x32_10(ctr: torch.Tensor, key: torch.Tensor) -> torch.Tensor:
     """Philox4x32-10 blocks for counters [n,4] and keys [n,2] (int32/uint32 storage)."""
     if ctr.dim() != 2 or ctr.shape[1] != 4 or key.shape != (ctr.shape[0], 2):
         raise ValueError("ctr must be [n,4] and key [n,2]")
-    if not (ctr.is_cuda and key.is_cuda and ctr.is_contiguous() and key.is_contiguous()):
-        raise ValueError("ctr and key must be contiguous CUDA tensors")
+    if not (ctr.is_cuda and key.device == ctr.device and ctr.is_contiguous() and key.is_contiguous()):
+        raise ValueError("ctr and key must be contiguous CUDA tensors on one device")
     if ctr.element_size() != 4 or key.element_size() != 4:
         raise ValueError("ctr and key must hold 32-bit words")
     out = torch.empty((ctr.shape[0], 4), dtype=torch.int32, device=ctr.device)

@@ -84,3 +84,25 @@ def test_binding_imports_without_gpu():
     assert ms.MAX_VOCAB == 2097152
     with pytest.raises(ValueError):
         ms._order("sideways")
+
+
+def test_binding_rejects_indices_the_kernels_cannot_read():
+    """The kernels read `indices` on the device: a host tensor, another dtype or a
+    strided view is refused before any call (every sampler goes through one check)."""
+    ensure_built()
+    import torch
+
+    import min_sampling_gb300 as ms
+    dev = torch.device("cuda", 0)
+    assert ms._indices(None, 7, dev) == (None, 7)
+    for bad in (torch.zeros(4, dtype=torch.int32),                  # host memory
+                torch.zeros(4, dtype=torch.int64),                  # another dtype
+                torch.zeros(8, dtype=torch.int32)[::2],             # not contiguous
+                torch.zeros((2, 2), dtype=torch.int32),             # not 1-D
+                [0, 1, 2]):
+        with pytest.raises(ValueError):
+            ms._indices(bad, 4, dev)
+    cpu = torch.device("cpu")
+    idx = torch.arange(6, dtype=torch.int32)
+    got, b_out = ms._indices(idx, 3, cpu)
+    assert got is idx and b_out == 6
