@@ -202,3 +202,30 @@ def exact_output_law(p, top_k=None, top_p=None, min_p=None, order="joint",
         return out
 
     return dict(law(row.low0, row.high0))
+
+
+def max_draws(p, top_k=None, top_p=None, min_p=None, order="joint", midpoint: str = "fp32") -> int:
+    """The largest number of draws any run of the sampler can take on this row.
+
+    The same walk over the algorithm's states (low, high) as ``exact_output_law``:
+    from a state every eligible token (p_i > low) is drawn with positive
+    probability; an accepted draw ends the path after one draw, a rejected one
+    continues from the state the three cases give.  Returns the longest path, 0 for
+    an invalid row or an empty S.  Exact rationals, so the answer does not depend on
+    summation order; ``midpoint`` as in ``sample`` ("fp32" is the kernels' rule).
+    """
+    row = _Row(p, top_k, top_p, min_p, order, exact=True)
+    if not row.valid or not row.f(row.high0):
+        return 0
+
+    @lru_cache(maxsize=None)
+    def longest(low: Fraction, high: Fraction) -> int:
+        best = 0
+        for i in range(row.V):
+            if not row.p[i] > low:
+                continue
+            nxt = three_cases(row, row.p[i], high, midpoint)
+            best = max(best, 1 if nxt is None else 1 + longest(*nxt))
+        return best
+
+    return longest(row.low0, row.high0)

@@ -167,20 +167,26 @@ def cut_value(p, top_k=None, top_p=None, min_p=None, order="joint") -> float:
     return max(cuts)
 
 
-def round_bound(p, top_k=None, top_p=None, min_p=None, order="joint") -> int:
-    """Upper bound on the number of draws of the dual-pivot sampler for one row.
+def round_bound_terms(p, top_k=None, top_p=None, min_p=None, order="joint"):
+    """The two limits on the number of draws of the dual-pivot sampler for one row.
 
-    Two facts from [blog] dual-pivot section / [explainer] "how dual pivot shrinks
-    the range": every failed round raises `low` past the drawn (rejected) token,
-    and every failed round at least halves high - low.  So the failures are at
-    most the number of rejectable tokens above the starting `low`, and at most
-    log2(high0 / (tau* - a)) (+2 for the float32 rounding of the midpoint), where
-    a is the largest rejectable value.  Draws = failures + 1.
+    Facts from [blog] dual-pivot section / [explainer] "how dual pivot shrinks the
+    range":
+      * every failed round raises `low` past the drawn (rejected) token, so the
+        failures are at most the number of rejectable tokens above the starting
+        `low` (``by_count`` = that number + 1 draws);
+      * every failed round at least halves high - low, and the round that ends
+        the search needs high - low below tau* - a (a = the largest rejectable
+        value, tau* = the cut of the acceptance test, ``cut_value``), so the
+        failures are at most log2(high0 / (tau* - a)) rounded up, plus 2 for the
+        float32 rounding of the midpoint (``by_halving`` = 3 + that log).
+    Returns (by_count, by_halving), or None when S is empty; (1, 1) when no token
+    can be rejected.
     """
     p64 = as64(p)
     S = allowed_set(p64, top_k, top_p, min_p, order)
     if S.size == 0:
-        return 0
+        return None
     V = p64.size
     desc = descending_positive(p64)
     if order == "top_k_first" and _k_active(top_k, V):
@@ -191,14 +197,21 @@ def round_bound(p, top_k=None, top_p=None, min_p=None, order="joint") -> int:
     inS[S] = True
     rejectable = pool[~inS[pool]]
     if rejectable.size == 0:
-        return 1
+        return 1, 1
     a = float(p64[rejectable].max())
     tau = cut_value(p64, top_k, top_p, min_p, order)
     hi0 = float(p64.max())
     by_count = rejectable.size + 1
     gap = tau - a
     by_halving = 3 + int(math.ceil(math.log2(hi0 / gap))) if gap > 0 else by_count
-    return int(min(by_count, by_halving))
+    return int(by_count), int(by_halving)
+
+
+def round_bound(p, top_k=None, top_p=None, min_p=None, order="joint") -> int:
+    """Upper bound on the number of draws of the dual-pivot sampler for one row:
+    the smaller of the two limits of ``round_bound_terms`` (0 when S is empty)."""
+    t = round_bound_terms(p, top_k, top_p, min_p, order)
+    return 0 if t is None else int(min(t))
 
 
 def topp_boundary_margin(p, top_k=None, top_p=None, min_p=None, order="joint") -> float:

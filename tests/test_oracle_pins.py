@@ -379,3 +379,133 @@ def test_generators_tie_free_and_deterministic():
     assert len(w5.bad_rows) == 2
     for r in w5.bad_rows:
         assert not filters.row_is_valid(w5.probs[r])
+
+
+# ---------------------------------------------------------------- round bound and cut value
+
+def _small_cases(seed, n_rows=24):
+    """(p, k, top_p, min_p, order) over small rows and parameter edges, skipping rows
+    whose top-p boundary is too close to call."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for V in (2, 3, 4, 5, 6, 7, 8):
+        for p in workloads.random_small_rows(n_rows, V, seed=seed + V, zero_prob=0.1):
+            if not (p > 0).any():
+                continue
+            for order in filters.ORDERS:
+                for _ in range(3):
+                    k = EDGE_K[rng.integers(len(EDGE_K))]
+                    tp = EDGE_P[rng.integers(len(EDGE_P))]
+                    mp = EDGE_MINP[rng.integers(len(EDGE_MINP))]
+                    if filters.topp_boundary_margin(p, k, tp, mp, order) < 1e-9:
+                        continue
+                    out.append((p, k, tp, mp, order))
+    return out
+
+
+_ROUND_CASES = None
+
+
+def _round_cases():
+    """Every case with its longest run of the sampler (the algorithm's own state walk,
+    exact rationals, float32 midpoints as the kernels compute them)."""
+    global _ROUND_CASES
+    if _ROUND_CASES is None:
+        _ROUND_CASES = [(c, dual_pivot.max_draws(*c)) for c in _small_cases(900)]
+    return _ROUND_CASES
+
+
+def _geometric_row():
+    return np.array([2.0 ** -i for i in range(1, 9)], np.float32)   # 1/2, 1/4, ..., 1/256
+
+
+def _near_flat_row():
+    return np.array([0.26, 0.25, 0.24, 0.23], np.float32)
+
+
+def _bound_pins_hold(bound) -> bool:
+    """The pins of the round bound, for a candidate `bound(p, k, top_p, min_p, order)`.
+
+    1. No run of the algorithm is longer than the bound ([blog] dual pivot: the bound
+       is a property of every path, so the longest path of the exact state walk must
+       respect it), on every small case.
+    2. Two rows worked by hand, one for each of the two limits.
+       Geometric row 1/2, 1/4, ..., 1/256 with k = 1: S = {1/2}; seven tokens can be
+       rejected, so the count limit is 7 + 1 = 8; tau* = 1/2, a = 1/4, high0 = 1/2,
+       log2(high0 / (tau* - a)) = 1, so the halving limit is 3 + 1 = 4.  The bound
+       is 4.  (Every run takes at most 2 draws: a rejected draw p_j <= 1/4 puts the
+       midpoint (p_j + 1/2) / 2 above 1/4, where f is still false, so `low` jumps past
+       every token but 1/2.)
+       Near-flat row .26, .25, .24, .23 with k = 1: three tokens can be rejected, so
+       the count limit is 4; tau* - a = .01, log2(.26 / .01) = 4.7, so the halving
+       limit is 3 + 5 = 8.  The bound is 4.
+    """
+    for c, longest in _round_cases():
+        if longest > bound(*c):
+            return False
+    return bound(_geometric_row(), 1, None, None, "joint") == 4 and \
+        bound(_near_flat_row(), 1, None, None, "joint") == 4
+
+
+def test_round_bound_covers_every_path_and_hand_rows():
+    assert len(_round_cases()) > 1000
+    assert _bound_pins_hold(filters.round_bound)
+    assert filters.round_bound_terms(_geometric_row(), 1) == (8, 4)
+    assert filters.round_bound_terms(_near_flat_row(), 1) == (4, 8)
+    assert dual_pivot.max_draws(_geometric_row(), 1) == 2
+    assert dual_pivot.max_draws(_near_flat_row(), 1) == 3
+    # The bound is not vacuous: on some cases a run reaches it.
+    assert any(longest == filters.round_bound(*c) and longest > 1 for c, longest in _round_cases())
+
+
+def test_round_bound_pins_catch_planted_mistakes():
+    """Plausible slips in the bound, each of which a pin must catch."""
+    def terms(*c):
+        return filters.round_bound_terms(*c) or (0, 0)
+
+    mutants = {
+        "max for min": lambda *c: max(terms(*c)),
+        "halving limit without the +3": lambda *c: min(terms(*c)[0], terms(*c)[1] - 3),
+        "count limit without the +1": lambda *c: min(terms(*c)[0] - 1, terms(*c)[1]),
+        "count limit alone, off by one": lambda *c: terms(*c)[0] - 1,
+    }
+    for name, bad in mutants.items():
+        assert not _bound_pins_hold(bad), name
+
+
+def _f_switches_at(c, cut_fn) -> bool:
+    """f(tau) holds at tau = cut and fails at the next float64 below it ([blog]
+    rejection sampling: the test is monotone in tau, so the cut is where it turns on)."""
+    p, k, tp, mp, order = c
+    if filters.allowed_set(p, k, tp, mp, order).size == 0:
+        return True
+    row = dual_pivot._Row(p, k, tp, mp, order, exact=False)
+    cut = cut_fn(p, k, tp, mp, order)
+    if not row.f(cut):
+        return False
+    return cut <= 0.0 or not row.f(np.nextafter(cut, -np.inf))
+
+
+def test_cut_value_is_where_the_acceptance_test_turns_on():
+    cases = _small_cases(950, n_rows=16)
+    assert len(cases) > 600
+    assert all(_f_switches_at(c, filters.cut_value) for c in cases)
+    # Planted mistakes: the smallest active cut instead of the largest; the top-p cut
+    # one rank too deep.
+    orig = filters.cut_value
+
+    def smallest_cut(p, k, tp, mp, order):
+        one = [orig(p, k, None, None, order), orig(p, None, tp, None, order), orig(p, None, None, mp, order)]
+        on = [x for x in one if x > 0]
+        return min(on) if on else 0.0
+
+    def topp_one_deeper(p, k, tp, mp, order):
+        v = orig(p, k, tp, mp, order)
+        if tp is None or not (0 < float(np.float32(tp)) < 1):
+            return v
+        vals = np.sort(p.astype(np.float64)[p > 0])[::-1]
+        below = vals[vals < v]
+        return float(below[0]) if below.size and v == orig(p, None, tp, None, order) else v
+
+    for bad in (smallest_cut, topp_one_deeper):
+        assert not all(_f_switches_at(c, bad) for c in cases), bad.__name__
