@@ -147,8 +147,8 @@ class Clocks:
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
-        self.idx = gpu_index
+    def __init__(self, device_id: str):
+        self.idx = device_id
         self.proc = None
         self.path = None
 
@@ -196,7 +196,27 @@ class Clocks:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows)}
+                "reasons": reasons, "samples": len(rows), "nvidia_smi_id": self.idx}
+
+
+def smi_device_id(local: int) -> str:
+    """The identifier nvidia-smi knows the CUDA device `local` by.  CUDA numbering
+    follows CUDA_VISIBLE_DEVICES while nvidia-smi's indices are physical, so the GPU's
+    UUID (from the CUDA runtime through torch) is used; its PCI bus id if that is not
+    available; the physical index from CUDA_VISIBLE_DEVICES as a last resort."""
+    import torch
+    props = torch.cuda.get_device_properties(local)
+    u = getattr(props, "uuid", None)
+    if u is not None:
+        u = str(u)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    bus = getattr(props, "pci_bus_id", None)
+    if bus is not None:
+        dom = getattr(props, "pci_domain_id", 0)
+        devn = getattr(props, "pci_device_id", 0)
+        return f"{dom:08X}:{bus:02X}:{devn:02X}.0"
+    vis = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+    return vis[local].strip() if local < len(vis) else str(local)
 
 
 # ---------------------------------------------------------------------------- our arm
@@ -290,7 +310,7 @@ def run_ours(args):
         nxt = warmup
         barrier()
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ctx = Clocks(local) if clocks else None
+        ctx = Clocks(smi_device_id(local)) if clocks else None
         if ctx:
             ctx.__enter__()
             t_soak = time.perf_counter() + SOAK_S

@@ -142,6 +142,10 @@ fs_status fs_top_k_top_p_sampling(const float* probs, int32_t batch_in, int32_t 
  * Row b draws Philox4x32-10 with key = seed_b and counter = (round, s_b, lo, hi) of
  * offset_b + *offset_dev, where s_b = b when `seeds` is NULL and 0 otherwise: with
  * per-request seeds a request's draws do not depend on its position in the batch.
+ * A consequence: two output rows with the same seed and the same offset draw the same
+ * numbers, hence the same token when they read the same input row.  Parallel samples
+ * of one request (several output rows mapped to one input row through `indices`) need
+ * distinct seeds or distinct offsets here; without `seeds` they differ by b.
  * Nothing is advanced by this call; see fs_advance_offset. */
 fs_status fs_top_k_top_p_sampling_rng(const float* probs, int32_t batch_in, int32_t vocab,
                                       const int32_t* indices, int32_t batch_out,

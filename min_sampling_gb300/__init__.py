@@ -110,8 +110,23 @@ def _check(status: int) -> None:
         raise FsError(msg)
 
 
-def _stream() -> ctypes.c_void_p:
-    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _run(device, fn_name: str, *args) -> None:
+    """Call a library entry with `device` made current and its current stream as the
+    last argument: the library plans and launches on the current CUDA device, so the
+    tensors' device must be the current one during the call."""
+    with torch.cuda.device(device):
+        _check(getattr(_lib(), fn_name)(*args, _stream(device)))
+
+
+def _same_device(device, **tensors) -> None:
+    """Every given tensor (None: absent) must live on `device`."""
+    for name, t in tensors.items():
+        if t is not None and t.device != device:
+            raise ValueError(f"{name} is on {t.device}, but the call's tensors are on {device}")
 
 
 def _ptr(t: Optional[torch.Tensor]) -> Optional[ctypes.c_void_p]:
@@ -174,8 +189,8 @@ def _sample(fn_name: str, probs, indices, seed, offset, params, return_rounds, o
     if order is not None:
         args.append(order)
     args += [int(seed) & (2 ** 64 - 1), int(offset) & (2 ** 64 - 1), _ptr(tok), _ptr(valid),
-             _ptr(rounds) if return_rounds else None, _stream()]
-    _check(getattr(_lib(), fn_name)(*args))
+             _ptr(rounds) if return_rounds else None]
+    _run(dev, fn_name, *args)
     return (tok, valid, rounds) if return_rounds else (tok, valid)
 
 
@@ -231,10 +246,10 @@ def top_k_top_p_sampling_rng(probs, top_k=None, top_p=None, min_p=None, order="j
           for v, dt, n in ((top_k, torch.int32, "top_k"), (top_p, torch.float32, "top_p"),
                            (min_p, torch.float32, "min_p"))]
     tok, valid, rounds = _outputs(b_out, dev)
-    _check(_lib().fs_top_k_top_p_sampling_rng(
-        _ptr(probs), b_in, V, _ptr(indices), b_out, *[_ptr(t) for t in ps], _order(order), _ptr(seeds),
-        _ptr(offsets), _ptr(offset_dev), int(seed) & (2 ** 64 - 1), int(offset) & (2 ** 64 - 1), _ptr(tok),
-        _ptr(valid), _ptr(rounds) if return_rounds else None, _stream()))
+    _run(dev, "fs_top_k_top_p_sampling_rng",
+         _ptr(probs), b_in, V, _ptr(indices), b_out, *[_ptr(t) for t in ps], _order(order), _ptr(seeds),
+         _ptr(offsets), _ptr(offset_dev), int(seed) & (2 ** 64 - 1), int(offset) & (2 ** 64 - 1), _ptr(tok),
+         _ptr(valid), _ptr(rounds) if return_rounds else None)
     return (tok, valid, rounds) if return_rounds else (tok, valid)
 
 
@@ -249,10 +264,10 @@ def top_k_top_p_sampling_pivots(probs, top_k=None, top_p=None, min_p=None, order
           for v, dt, n in ((top_k, torch.int32, "top_k"), (top_p, torch.float32, "top_p"),
                            (min_p, torch.float32, "min_p"))]
     tok, valid, rounds = _outputs(b_out, dev)
-    _check(_lib().fs_top_k_top_p_sampling_pivots(
-        _ptr(probs), b_in, V, _ptr(indices), b_out, *[_ptr(t) for t in ps], _order(order), int(pivots),
-        int(seed) & (2 ** 64 - 1), int(offset) & (2 ** 64 - 1), _ptr(tok), _ptr(valid),
-        _ptr(rounds) if return_rounds else None, _stream()))
+    _run(dev, "fs_top_k_top_p_sampling_pivots",
+         _ptr(probs), b_in, V, _ptr(indices), b_out, *[_ptr(t) for t in ps], _order(order), int(pivots),
+         int(seed) & (2 ** 64 - 1), int(offset) & (2 ** 64 - 1), _ptr(tok), _ptr(valid),
+         _ptr(rounds) if return_rounds else None)
     return (tok, valid, rounds) if return_rounds else (tok, valid)
 
 
@@ -267,10 +282,10 @@ def top_k_top_p_sampling_from_logits(logits, temperature=None, top_k=None, top_p
           for v, dt, n in ((temperature, torch.float32, "temperature"), (top_k, torch.int32, "top_k"),
                            (top_p, torch.float32, "top_p"), (min_p, torch.float32, "min_p"))]
     tok, valid, rounds = _outputs(b_out, dev)
-    _check(_lib().fs_top_k_top_p_sampling_from_logits(
-        _ptr(logits), b_in, V, _ptr(indices), b_out, *[_ptr(t) for t in ps], _order(order),
-        int(seed) & (2 ** 64 - 1), int(offset) & (2 ** 64 - 1), _ptr(tok), _ptr(valid),
-        _ptr(rounds) if return_rounds else None, _stream()))
+    _run(dev, "fs_top_k_top_p_sampling_from_logits",
+         _ptr(logits), b_in, V, _ptr(indices), b_out, *[_ptr(t) for t in ps], _order(order),
+         int(seed) & (2 ** 64 - 1), int(offset) & (2 ** 64 - 1), _ptr(tok), _ptr(valid),
+         _ptr(rounds) if return_rounds else None)
     return (tok, valid, rounds) if return_rounds else (tok, valid)
 
 
@@ -292,9 +307,9 @@ def chain_speculative_sampling(draft_probs, draft_tokens, target_probs, *, seed:
         check3(draft_probs, "draft_probs")
         if tuple(draft_probs.shape) != (B, L, V):
             raise ValueError("draft_probs must be [B, L, V] with target_probs [B, L + 1, V]")
-        if not isinstance(draft_tokens, torch.Tensor) or tuple(draft_tokens.shape) != (B, L) \
-                or draft_tokens.device != target_probs.device:
-            raise ValueError("draft_tokens must be a [B, L] tensor on the same device")
+        if not isinstance(draft_tokens, torch.Tensor) or tuple(draft_tokens.shape) != (B, L):
+            raise ValueError("draft_tokens must be a [B, L] tensor")
+        _same_device(target_probs.device, draft_probs=draft_probs, draft_tokens=draft_tokens)
         draft_tokens = draft_tokens.to(torch.int32).contiguous()
     else:
         draft_probs = draft_tokens = None
@@ -302,9 +317,9 @@ def chain_speculative_sampling(draft_probs, draft_tokens, target_probs, *, seed:
     tok = torch.empty((B, L + 1), dtype=torch.int32, device=dev)
     acc = torch.empty(B, dtype=torch.int32, device=dev)
     emi = torch.empty(B, dtype=torch.int32, device=dev)
-    _check(_lib().fs_chain_speculative_sampling(
-        _ptr(draft_probs), _ptr(draft_tokens), _ptr(target_probs), B, L, V,
-        int(seed) & (2 ** 64 - 1), int(offset) & (2 ** 64 - 1), _ptr(tok), _ptr(acc), _ptr(emi), _stream()))
+    _run(dev, "fs_chain_speculative_sampling",
+         _ptr(draft_probs), _ptr(draft_tokens), _ptr(target_probs), B, L, V,
+         int(seed) & (2 ** 64 - 1), int(offset) & (2 ** 64 - 1), _ptr(tok), _ptr(acc), _ptr(emi))
     return tok, acc, emi
 
 
@@ -324,7 +339,7 @@ def advance_offset(offset_dev, delta: int = 1) -> None:
     if not (isinstance(offset_dev, torch.Tensor) and offset_dev.dtype == torch.uint64 and offset_dev.is_cuda
             and offset_dev.numel() == 1):
         raise ValueError("offset_dev must be a CUDA uint64 tensor of one element")
-    _check(_lib().fs_advance_offset(_ptr(offset_dev), int(delta) & (2 ** 64 - 1), _stream()))
+    _run(offset_dev.device, "fs_advance_offset", _ptr(offset_dev), int(delta) & (2 ** 64 - 1))
 
 
 def _filter(fn_name, x, param, dtype, pname, out):
@@ -335,7 +350,7 @@ def _filter(fn_name, x, param, dtype, pname, out):
     if out.shape != x.shape or out.device != x.device:
         raise ValueError("out must have the input's shape and device")
     valid = torch.empty(B, dtype=torch.uint8, device=x.device)
-    _check(getattr(_lib(), fn_name)(_ptr(x), B, V, _ptr(p), _ptr(out), _ptr(valid), _stream()))
+    _run(x.device, fn_name, _ptr(x), B, V, _ptr(p), _ptr(out), _ptr(valid))
     return out, valid
 
 
@@ -360,5 +375,5 @@ def philox4x32_10(ctr: torch.Tensor, key: torch.Tensor) -> torch.Tensor:
     if ctr.element_size() != 4 or key.element_size() != 4:
         raise ValueError("ctr and key must hold 32-bit words")
     out = torch.empty((ctr.shape[0], 4), dtype=torch.int32, device=ctr.device)
-    _check(_lib().fs_philox4x32_10(_ptr(ctr), _ptr(key), ctr.shape[0], _ptr(out), _stream()))
+    _run(ctr.device, "fs_philox4x32_10", _ptr(ctr), _ptr(key), ctr.shape[0], _ptr(out))
     return out

@@ -126,3 +126,14 @@ def test_header_compiles_as_plain_c():
                         "-I", os.path.dirname(HEADER), "-o", os.devnull],
                        input=src, capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_binding_rejects_tensors_on_another_device():
+    """The binding checks that every tensor of a call lives on the call's device
+    before anything reaches the library (cpu and meta stand in for two devices)."""
+    import torch
+    from min_sampling_gb300 import _same_device
+    a = torch.zeros(3)
+    _same_device(a.device, x=a, y=None)
+    with pytest.raises(ValueError):
+        _same_device(a.device, draft_probs=a, draft_tokens=torch.zeros(3, device="meta"))

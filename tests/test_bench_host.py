@@ -49,6 +49,7 @@ def _timed_function(soak_s):
 
     cuda = types.SimpleNamespace(Event=Event, synchronize=lambda dev=None: None)
     ns = dict(torch=types.SimpleNamespace(cuda=cuda), time=time, SOAK_S=soak_s, Clocks=Clocks, local=0,
+              smi_device_id=lambda local: "GPU-stand-in",
               dev=None, stream=None, barrier=lambda: None, slowest=lambda ms, dev: ms)
     exec(code, ns)
     return ns["timed"], Event
