@@ -19,9 +19,23 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  *  - Every pointer argument is a DEVICE pointer owned by the caller, unless stated.
- *    The library allocates no memory, keeps no per-call state and may be called
- *    from several host threads at once.  Each call is asynchronous on `stream`
- *    (a cudaStream_t passed as void*; NULL is the legacy default stream).
+ *    Each call is asynchronous on `stream` (a cudaStream_t passed as void*; NULL is
+ *    the legacy default stream) and may be made from several host threads at once.
+ *  - Scratch memory.  The top-k-first samplers and fs_sampling_from_probs run as two
+ *    launches: a scan that reads every input row once, spread evenly over the GPU, and
+ *    writes a small summary of each row (a few bytes per 128 values), then one CTA per
+ *    output row that finishes the row from that summary.  The summaries live in a
+ *    scratch buffer that the library owns, one per (device, stream): calls on one
+ *    stream run in order and share it; calls on different streams do not touch each
+ *    other's.  The first call that needs more than the stream's buffer holds
+ *    allocates it (cudaMalloc, in relaxed stream-capture mode, so this may happen
+ *    while the stream is being captured; the buffer then belongs to the library, not
+ *    to the graph).  fs_workspace_reserve allocates ahead of time and
+ *    fs_release_workspaces frees every buffer.  A CUDA graph captured on a stream uses
+ *    that stream's buffer on every replay: do not replay it while other calls of
+ *    this library on that stream, or other replays of graphs captured on it, may run
+ *    at the same time.  No other call allocates, and no state but these buffers
+ *    outlives a call.
  *  - `probs` / `logits` are row-major [batch_in, vocab] float32, contiguous (row
  *    stride = vocab).  Rows are probabilities (or unnormalised non-negative scores;
  *    every filter is scale-invariant, see top-p below).
@@ -54,6 +68,7 @@
 #ifndef FS_SAMPLING_H
 #define FS_SAMPLING_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -279,6 +294,22 @@ const char* fs_last_error_string(void);
 
 /* FS_MAX_VOCAB, for bindings that cannot read the macro. */
 int32_t fs_max_vocab(void);
+
+/* Bytes of scratch that the row summaries of `batch_in` input rows of `vocab` values
+ * take (see "Scratch memory" above): per row 8 bytes per segment of the launch plan
+ * (128 values per segment up to vocab 2^19) and 16 bytes per 512 values.
+ * *bytes is a host pointer.  FS_ERR_INVALID_ARG: null bytes, batch_in < 0, vocab < 1. */
+fs_status fs_workspace_bytes(int32_t batch_in, int32_t vocab, size_t* bytes);
+
+/* Make sure the scratch buffer of the current device and `stream` holds the summaries
+ * of `batch_in` rows of `vocab` values, allocating (cudaMalloc) now if it does not.
+ * Host-side; launches nothing.  FS_ERR_CUDA if the allocation fails. */
+fs_status fs_workspace_reserve(int32_t batch_in, int32_t vocab, void* stream);
+
+/* Free every scratch buffer of the library on every device.  Only when no call of
+ * this library is in flight on any stream (and no captured graph that uses one will
+ * be replayed again); later calls allocate afresh. */
+fs_status fs_release_workspaces(void);
 
 #ifdef __cplusplus
 }

@@ -7,6 +7,7 @@
 #include <set>
 #include <tuple>
 #include <utility>
+#include <vector>
 
 #include "fs_host.h"
 
@@ -222,6 +223,49 @@ fs_status make_plan(int rows, int vocab, const void* fn, bool single_pass, Plan&
     return FS_OK;
 }
 
+// Scratch memory of the library, one buffer per (device, stream): calls on one stream
+// run in order, so they can share it; calls on different streams get different
+// buffers.  Allocated on first need and grown (to the next MiB) when a call needs
+// more; a grown-out buffer may still be read by work in flight, so it is kept until
+// fs_release_workspaces.  cudaMalloc runs in relaxed capture mode, so the first call
+// on a stream may come while that stream is being captured into a CUDA graph (the
+// buffer is allocated at capture time, outside the graph, and the graph's kernels
+// use it on every replay).
+struct WsEntry {
+    void* ptr = nullptr;
+    size_t bytes = 0;
+};
+static std::mutex g_ws_mu;
+static std::map<std::pair<int, void*>, WsEntry> g_ws;
+static std::vector<std::pair<int, void*>> g_ws_retired;
+
+fs_status workspace(size_t bytes, void* stream, void** out) {
+    *out = nullptr;
+    if (bytes == 0) return FS_OK;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    std::lock_guard<std::mutex> lock(g_ws_mu);
+    WsEntry& w = g_ws[{dev, stream}];
+    if (w.bytes < bytes) {
+        const size_t mib = size_t(1) << 20;
+        const size_t want = (bytes + mib - 1) / mib * mib;
+        cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+        e = cudaThreadExchangeStreamCaptureMode(&mode);
+        if (e != cudaSuccess) return cuda_fail(e);
+        void* p = nullptr;
+        const cudaError_t ea = cudaMalloc(&p, want);
+        e = cudaThreadExchangeStreamCaptureMode(&mode);
+        if (ea != cudaSuccess) return cuda_fail(ea);
+        if (e != cudaSuccess) return cuda_fail(e);
+        if (w.ptr) g_ws_retired.push_back({dev, w.ptr});
+        w.ptr = p;
+        w.bytes = want;
+    }
+    *out = w.ptr;
+    return FS_OK;
+}
+
 __global__ void philox_kernel(const uint32_t* __restrict__ ctr, const uint32_t* __restrict__ key, int64_t n,
                               uint32_t* __restrict__ out) {
     const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -264,6 +308,42 @@ const char* fs_status_string(int32_t status) {
 }
 
 const char* fs_last_error_string(void) { return fsd::g_last_error; }
+
+fs_status fs_workspace_bytes(int32_t batch_in, int32_t vocab, size_t* bytes) {
+    if (!bytes || batch_in < 0 || vocab < 1) return FS_ERR_INVALID_ARG;
+    if (vocab > FS_MAX_VOCAB) return FS_ERR_UNSUPPORTED;
+    *bytes = fsd::scan_workspace_bytes(batch_in, vocab);
+    return FS_OK;
+}
+
+fs_status fs_workspace_reserve(int32_t batch_in, int32_t vocab, void* stream) {
+    size_t bytes = 0;
+    const fs_status st = fs_workspace_bytes(batch_in, vocab, &bytes);
+    if (st != FS_OK) return st;
+    void* p = nullptr;
+    return fsd::workspace(bytes, stream, &p);
+}
+
+fs_status fs_release_workspaces(void) {
+    int cur = 0;
+    cudaError_t e = cudaGetDevice(&cur);
+    if (e != cudaSuccess) return fsd::cuda_fail(e);
+    std::lock_guard<std::mutex> lock(fsd::g_ws_mu);
+    std::vector<std::pair<int, void*>> all = fsd::g_ws_retired;
+    for (auto& kv : fsd::g_ws) all.push_back({kv.first.first, kv.second.ptr});
+    fs_status st = FS_OK;
+    for (auto& d : all) {
+        if (!d.second) continue;
+        e = cudaSetDevice(d.first);
+        if (e == cudaSuccess) e = cudaFree(d.second);
+        if (e != cudaSuccess && st == FS_OK) st = fsd::cuda_fail(e);
+    }
+    fsd::g_ws.clear();
+    fsd::g_ws_retired.clear();
+    e = cudaSetDevice(cur);
+    if (e != cudaSuccess && st == FS_OK) st = fsd::cuda_fail(e);
+    return st;
+}
 
 int32_t fs_max_vocab(void) { return FS_MAX_VOCAB; }
 

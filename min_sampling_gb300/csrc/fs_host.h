@@ -30,6 +30,14 @@ fs_status device_limits(int& sm_count, size_t& smem_optin);
 // with at most MAX_CLUSTER CTAs per row and at least four segments per CTA.
 fs_status make_plan(int rows, int vocab, const void* fn, bool single_pass, Plan& p, bool topp_hist = false);
 
+// The library's scratch buffer for the current device and `stream`, at least `bytes`
+// long (allocated or grown on first need; see api.cu).
+fs_status workspace(size_t bytes, void* stream, void** out);
+
+// Bytes of scratch that the row summaries of `batch_in` rows of `vocab` values take
+// (scan_kernel, sampling.cu).
+size_t scan_workspace_bytes(int batch_in, int vocab);
+
 // Opt the kernel into the device's maximum dynamic shared memory (once per device).
 fs_status prepare_kernel(const void* fn);
 

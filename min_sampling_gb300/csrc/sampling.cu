@@ -48,7 +48,193 @@ struct SampleArgs {
     int shift;                // log2(blocks per segment)
     int ns;                   // segments per row
     int nsc;                  // segments per CTA
+    // Finishing launch (FIN): the row summaries written by scan_kernel.
+    const uint32_t* skey;     // [batch_in][ls] segment maxima (order keys)
+    const float* smass;       // [batch_in][ls] segment masses (rows of probabilities)
+    const uint4* sstat;       // [batch_in][nu] per unit: mass, positives, bad flag, largest key
+    int ls;                   // words per row of skey / smass
+    int nu;                   // units per row
 };
+
+// ------------------------------------------------------------------ row summaries
+//
+// The samplers that need nothing of a row after its one read but the top of it (the
+// top-k-first order) or a single draw (no filter) run as two launches.  scan_kernel
+// reads every input row once, spread evenly over the whole GPU: the unit of work is
+// TB consecutive blocks of one row (a warp's trip, 2 KB), and warp w of the grid takes
+// units w, w + W, w + 2W, ... of the matrix in row-major order (W warps in the grid),
+// so every SM streams the same number of bytes whatever the batch.  Per unit it writes
+// each segment's largest order key and mass, and the unit's mass, positive count, bad
+// flag and largest key.  The finishing launch (sample_kernel with FIN, one CTA per
+// output row) reads the summary of its input row from L2 and goes on exactly as the
+// one-CTA cluster does after pass 1.  Nothing in scan_kernel waits on another thread.
+struct ScanArgs {
+    const float* x;           // [rows][V]
+    int rows, V, shift, ns, nu, ls;
+    uint32_t* key;            // [rows][ls]
+    float* mass;              // [rows][ls], rows of probabilities
+    uint4* stat;              // [rows][nu]
+};
+
+__host__ __device__ inline int scan_units(int V) { return (V + TB * BLK - 1) / (TB * BLK); }
+__host__ __device__ inline int scan_row_words(int ns) { return (ns + 3) & ~3; }
+
+size_t scan_workspace_bytes(int batch_in, int vocab) {
+    const int shift = seg_shift_for(vocab);
+    const int ns = (vocab + (BLK << shift) - 1) / (BLK << shift);
+    const size_t ls = size_t(scan_row_words(ns));
+    return size_t(batch_in) * (2 * ls * 4 + size_t(scan_units(vocab)) * 16);
+}
+
+// LOGITS: keys are logit keys, the positive count counts logits above -inf, +inf is a
+// bad value as well as NaN, and no masses are kept (they depend on the temperature).
+template <bool VEC, bool LOGITS>
+__global__ void __launch_bounds__(NT, 4) scan_kernel(const ScanArgs a) {
+    grid_dependency_wait();
+    allow_dependents();
+    const int lane = threadIdx.x & 31;
+    const long long total = (long long)a.rows * a.nu;
+    const long long step = (long long)gridDim.x * NW;
+    const int spu = TB >> a.shift;  // segments per unit
+    const float fill = LOGITS ? __int_as_float(0xff800000) : 0.f;
+    auto load_unit = [&](long long u, float4* v) {
+        if (u < total) {
+            const int r = int(u / a.nu), q = int(u - (long long)r * a.nu);
+            const float* row = a.x + size_t(r) * size_t(a.V);
+#pragma unroll
+            for (int j = 0; j < TB; ++j) v[j] = load4<VEC, true>(row, a.V, (q * TB + j) * BLK + lane * 4, fill);
+        } else {
+#pragma unroll
+            for (int j = 0; j < TB; ++j) v[j] = make_float4(fill, fill, fill, fill);
+        }
+    };
+    long long u = (long long)blockIdx.x * NW + (threadIdx.x >> 5);
+    float4 A[TB], Bv[TB];
+    load_unit(u, A);
+#pragma unroll 1
+    while (u < total) {
+        const long long un = u + step;
+        load_unit(un, Bv);
+        const int r = int(u / a.nu), q = int(u - (long long)r * a.nu);
+        uint32_t km[TB];
+        float s[TB];
+        int pos = 0;
+        bool bad = false;
+#pragma unroll
+        for (int j = 0; j < TB; ++j) {
+            const int base = (q * TB + j) * BLK + lane * 4;
+            uint32_t k = 0;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const float x = q_at(A[j], c);
+                if (!LOGITS) {
+                    bad |= !(x >= 0.f);
+                    k = max(k, prob_key(x));
+                    pos += x > 0.f;
+                } else {
+                    const bool in = base + c < a.V;
+                    bad |= isnan(x) || (in && x == __int_as_float(0x7f800000));
+                    pos += in && x > __int_as_float(0xff800000);
+                    k = max(k, in ? logit_key(x) : 0u);
+                }
+            }
+            km[j] = __reduce_max_sync(FULL, k);
+            s[j] = LOGITS ? 0.f : (A[j].x + A[j].y) + (A[j].z + A[j].w);
+        }
+        if (!LOGITS) {
+#pragma unroll
+            for (int m = 16; m; m >>= 1)
+#pragma unroll
+                for (int j = 0; j < TB; ++j) s[j] += __shfl_xor_sync(FULL, s[j], m);
+        }
+        // Lane l < spu: segment q * spu + l, its blocks combined in order.
+        const int sg = q * spu + lane;
+        if (lane < spu && sg < a.ns) {
+            float ss = 0.f;
+            uint32_t kk = 0;
+#pragma unroll
+            for (int j = 0; j < TB; ++j) {
+                const bool mine = (j >> a.shift) == lane;
+                ss += mine ? s[j] : 0.f;
+                kk = mine ? max(kk, km[j]) : kk;
+            }
+            a.key[size_t(r) * a.ls + sg] = kk;
+            if (!LOGITS) a.mass[size_t(r) * a.ls + sg] = ss;
+        }
+        pos = warp_sum_i(pos);
+        const unsigned anybad = __ballot_sync(FULL, bad);
+        if (lane == 0) {
+            float um = 0.f;
+            uint32_t kx = 0;
+#pragma unroll
+            for (int j = 0; j < TB; ++j) {
+                um += s[j];
+                kx = max(kx, km[j]);
+            }
+            a.stat[size_t(r) * a.nu + q] = make_uint4(__float_as_uint(um), uint32_t(pos), anybad ? 1u : 0u, kx);
+        }
+#pragma unroll
+        for (int j = 0; j < TB; ++j) A[j] = Bv[j];
+        u = un;
+    }
+}
+
+// FIN: the summary of input row r into this CTA's tables, as pass 1 and pass1_totals
+// leave them in a one-CTA cluster: segment keys (and, with `masses`, segment masses),
+// part[0] = (M; positive count, bad flag, largest key), and with `hist` the histogram
+// of the segment keys (key >> 21) in hist(), which the caller cleared.  M is the sum of
+// the unit masses in a fixed order (lane-strided, then a tree).  The summary was
+// written by the previous launch, so it is read through L2 (ld.global.cg).
+// Block-collective; the caller synchronises before the tables are read.
+__device__ __forceinline__ void load_summary(const SampleArgs& a, int r, Smem sm, bool masses, bool hist, int warp,
+                                             int lane, int tid) {
+    const uint4* key4 = reinterpret_cast<const uint4*>(a.skey + size_t(r) * a.ls);
+    const uint4* mass4 = reinterpret_cast<const uint4*>(a.smass + size_t(r) * a.ls);
+    const int n4 = a.ls >> 2;
+#pragma unroll 1
+    for (int i = tid; i < n4; i += NT) {
+        const uint4 k = __ldcg(key4 + i);
+        uint4 m = make_uint4(0u, 0u, 0u, 0u);
+        if (masses) m = __ldcg(mass4 + i);
+        const uint32_t kk[4] = {k.x, k.y, k.z, k.w};
+        const uint32_t mm[4] = {m.x, m.y, m.z, m.w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int s = 4 * i + c;
+            if (s < a.ns) {
+                sm.segkey()[s] = kk[c];
+                if (masses) sm.mass(0)[s] = __uint_as_float(mm[c]);
+                if (hist) atomicAdd(&sm.hist()[min(uint32_t(HBINS - 1), kk[c] >> 21)], 1u);
+            }
+        }
+    }
+    if (warp == 0) {
+        const uint4* st = a.sstat + size_t(r) * a.nu;
+        float ms = 0.f;
+        int p = 0;
+        bool bd = false;
+        uint32_t km = 0;
+#pragma unroll 1
+        for (int i = lane; i < a.nu; i += 32) {
+            const uint4 v = __ldcg(st + i);
+            ms += __uint_as_float(v.x);
+            p += int(v.y);
+            bd |= v.z != 0u;
+            km = max(km, v.w);
+        }
+        ms = warp_sum(ms);
+        p = warp_sum_i(p);
+        bd = __any_sync(FULL, bd);
+        km = warp_max_u(km);
+        if (lane == 0) {
+            Part& pt = sm.part()[0];
+            pt.f[0] = ms;
+            pt.u[0] = uint32_t(p);
+            pt.u[1] = bd ? 1u : 0u;
+            pt.u[2] = km;
+        }
+    }
+}
 
 // The acceptance test f(tau) ([blog] rejection sampling: count / remaining mass above
 // the pivot; [explainer] Top-k, Top-p, Min-p), from the count and the mass of the
@@ -227,8 +413,11 @@ __device__ __forceinline__ int small_rounds(const Small& s, const bool* kept, co
 
 
 
-template <bool VEC, bool SOFT>
-__global__ void __launch_bounds__(NT, 3) sample_kernel(const SampleArgs a) {
+// FIN: the finishing launch after scan_kernel, one CTA per output row (launched as
+// one-CTA clusters): the row's summary replaces pass 1, and everything after it runs
+// as in a cluster of one.
+template <bool VEC, bool SOFT, bool FIN>
+__global__ void __launch_bounds__(NT, FIN ? 2 : 3) sample_kernel(const SampleArgs a) {
     const int C = int(cluster_nctarank());
     const int rank = int(cluster_ctarank());
     const int b = int(cluster_id_x());
@@ -288,7 +477,22 @@ __global__ void __launch_bounds__(NT, 3) sample_kernel(const SampleArgs a) {
     int pos = 0;
     bool bad = false;
     uint32_t kmax = 0;
-    if (row_ok) {
+    if (FIN) {
+        // The same set-up without the cluster arrive: both histograms cleared for a
+        // top-k-first launch, the trip counter, the row's parameters.
+        if (a.order == 0 && a.top_k)
+            for (int i = tid; i < 2 * HBINS; i += NT) sm.hist()[i] = 0u;
+        if (tid == 0) *sm.ctr() = NW;
+        if (tid == NT - 32) {
+            uint32_t* pr = sm.prm();
+            pr[0] = uint32_t(a.top_k ? a.top_k[b] : 0);
+            pr[1] = __float_as_uint(a.top_p ? a.top_p[b] : 1.f);
+            pr[2] = __float_as_uint(a.min_p ? a.min_p[b] : 0.f);
+            *reinterpret_cast<unsigned long long*>(pr + 4) = a.seeds ? a.seeds[b] : a.seed;
+            *reinterpret_cast<unsigned long long*>(pr + 6) =
+                (a.offsets ? a.offsets[b] : a.offset) + (a.offset_dev ? *a.offset_dev : 0ull);
+        }
+    } else if (row_ok) {
         if (SOFT && kfirst_soft)  // draws come from the gathered candidates: keys only
             pass1<VEC, true, false, 1>(row, g, sm, hist_sh, warp, lane, pos, bad, kmax, setup);
         else if (SOFT)
@@ -312,10 +516,29 @@ __global__ void __launch_bounds__(NT, 3) sample_kernel(const SampleArgs a) {
     const bool k_on = k > 0 && k < V;
     const bool kfirst = a.order == 0 && k_on;
     const bool need_hist = kfirst && ns >= k;
-    cluster_wait();  // every CTA has started and cleared its histogram
-    pass1_totals(g, sm, leader, rank, C, pos, bad, kmax, need_hist ? 21 : -1, !(SOFT && kfirst), !kfirst, warp, lane,
-                 tid, SOFT && !kfirst, need_hist ? k : 0);
-    cluster_sync();  // the leader's segment table, every CTA's parts and histogram, are complete
+    if (FIN) {
+        if (!row_ok) {
+            for (int i = tid; i < ns; i += NT) {
+                sm.segkey()[i] = 0u;
+                sm.mass(0)[i] = 0.f;
+            }
+            if (tid == 0) sm.part()[0] = Part{};
+        } else if (SOFT && !kfirst) {
+            // Masses of logits depend on the row's temperature, which the summary does
+            // not know: this row (no top-k bound in a top-k-first launch) is read again
+            // here, from L2, as pass 1 reads it.
+            pass1<VEC, true, false, 2>(row, g, sm, -1, warp, lane, pos, bad, kmax);
+            pass1_totals(g, sm, true, 0, 1, pos, bad, kmax, -1, true, true, warp, lane, tid, true, 0);
+        } else {
+            load_summary(a, r, sm, !SOFT, need_hist, warp, lane, tid);
+        }
+        __syncthreads();  // the tables, part[0] and the histogram
+    } else {
+        cluster_wait();  // every CTA has started and cleared its histogram
+        pass1_totals(g, sm, leader, rank, C, pos, bad, kmax, need_hist ? 21 : -1, !(SOFT && kfirst), !kfirst, warp,
+                     lane, tid, SOFT && !kfirst, need_hist ? k : 0);
+        cluster_sync();  // the leader's segment table, every CTA's parts and histogram, are complete
+    }
 
     // Rows of logits: the row's largest logit m (the CTAs' maxima are logit keys in
     // part[].u[2]) and each CTA's factor exp((m_c - m) / T) from its maximum to the row's,
@@ -596,6 +819,121 @@ __global__ void __launch_bounds__(NT, 3) sample_kernel(const SampleArgs a) {
 
 // ------------------------------------------------------------------ host side
 
+#ifndef FS_SCAN_PER_SM
+#define FS_SCAN_PER_SM 3   // scan CTAs per SM
+#endif
+
+// Grid of the scan: one wave of FS_SCAN_PER_SM CTAs per SM, fewer when the matrix has
+// fewer units than the wave has warps.
+static fs_status scan_grid(long long units, int& grid) {
+    int sms = 0;
+    size_t optin = 0;
+    const fs_status st = device_limits(sms, optin);
+    if (st != FS_OK) return st;
+    const long long want = (units + NW - 1) / NW;
+    const long long wave = (long long)sms * FS_SCAN_PER_SM;
+    grid = int(want < wave ? want : wave);
+    return FS_OK;
+}
+
+template <bool LOGITS>
+static fs_status launch_scan(const float* x, int rows, int V, int shift, int ns, bool vec, void* ws, void* stream) {
+    ScanArgs s;
+    s.x = x;
+    s.rows = rows;
+    s.V = V;
+    s.shift = shift;
+    s.ns = ns;
+    s.nu = scan_units(V);
+    s.ls = scan_row_words(ns);
+    s.key = reinterpret_cast<uint32_t*>(ws);
+    s.mass = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + size_t(rows) * s.ls * 4);
+    s.stat = reinterpret_cast<uint4*>(reinterpret_cast<char*>(ws) + 2 * size_t(rows) * s.ls * 4);
+    int grid = 0;
+    fs_status st = scan_grid((long long)rows * s.nu, grid);
+    if (st != FS_OK) return st;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(grid), 1, 1);
+    cfg.blockDim = dim3(NT, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = vec ? cudaLaunchKernelEx(&cfg, scan_kernel<true, LOGITS>, s)
+                        : cudaLaunchKernelEx(&cfg, scan_kernel<false, LOGITS>, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return FS_OK;
+}
+
+// The scan of the input rows, then the finishing launch (one CTA per output row).
+static fs_status launch_scan_finish(const float* probs, int32_t batch_in, int32_t vocab, const int32_t* indices,
+                                    int32_t batch_out, const int32_t* top_k, const float* top_p, const float* min_p,
+                                    int32_t order, uint64_t seed, uint64_t offset, int32_t* out_token,
+                                    uint8_t* out_valid, int32_t* out_rounds, void* stream, const uint64_t* seeds,
+                                    const uint64_t* offsets, const uint64_t* offset_dev, int32_t pivots, bool soft,
+                                    const float* temperature, bool vec) {
+    auto fin_fn = [&]() -> void (*)(SampleArgs) {
+        if (soft) return vec ? sample_kernel<true, true, true> : sample_kernel<false, true, true>;
+        return vec ? sample_kernel<true, false, true> : sample_kernel<false, false, true>;
+    };
+    void (*fn)(SampleArgs) = fin_fn();
+    fs_status st = prepare_kernel(reinterpret_cast<const void*>(fn));
+    if (st != FS_OK) return st;
+    int sms = 0;
+    size_t optin = 0;
+    st = device_limits(sms, optin);
+    if (st != FS_OK) return st;
+    Plan p;
+    p.C = 1;
+    p.shift = seg_shift_for(vocab);
+    p.ns = (vocab + (BLK << p.shift) - 1) / (BLK << p.shift);
+    p.nsc = (p.ns + 3) & ~3;
+    p.smem = Layout(p.ns).total();
+    p.per_sm = 0;
+    if (p.smem > optin) return FS_ERR_UNSUPPORTED;
+    void* ws = nullptr;
+    if (batch_in > 0) {
+        st = workspace(scan_workspace_bytes(batch_in, vocab), stream, &ws);
+        if (st != FS_OK) return st;
+        st = soft ? launch_scan<true>(probs, batch_in, vocab, p.shift, p.ns, vec, ws, stream)
+                  : launch_scan<false>(probs, batch_in, vocab, p.shift, p.ns, vec, ws, stream);
+        if (st != FS_OK) return st;
+    }
+    SampleArgs a = {};
+    a.probs = probs;
+    a.batch_in = batch_in;
+    a.V = vocab;
+    a.indices = indices;
+    a.top_k = top_k;
+    a.top_p = top_p;
+    a.min_p = min_p;
+    a.order = order == FS_ORDER_TOP_K_FIRST ? 0 : 1;
+    a.seed = seed;
+    a.offset = offset;
+    a.seeds = reinterpret_cast<const unsigned long long*>(seeds);
+    a.offsets = reinterpret_cast<const unsigned long long*>(offsets);
+    a.offset_dev = reinterpret_cast<const unsigned long long*>(offset_dev);
+    a.single_pivot = pivots == 1 ? 1 : 0;
+    a.temperature = temperature;
+    a.out_token = out_token;
+    a.out_valid = out_valid;
+    a.out_rounds = out_rounds;
+    a.shift = p.shift;
+    a.ns = p.ns;
+    a.nsc = p.nsc;
+    a.ls = scan_row_words(p.ns);
+    a.nu = scan_units(vocab);
+    a.skey = reinterpret_cast<const uint32_t*>(ws);
+    a.smass = ws ? reinterpret_cast<const float*>(reinterpret_cast<const char*>(ws) + size_t(batch_in) * a.ls * 4)
+                 : nullptr;
+    a.sstat = ws ? reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(ws) + 2 * size_t(batch_in) * a.ls * 4)
+                 : nullptr;
+    return launch_cluster(fn, p, batch_out, stream, a);
+}
+
 static fs_status launch_sample(const float* probs, int32_t batch_in, int32_t vocab, const int32_t* indices,
                                int32_t batch_out, const int32_t* top_k, const float* top_p, const float* min_p,
                                int32_t order, uint64_t seed, uint64_t offset, int32_t* out_token, uint8_t* out_valid,
@@ -612,16 +950,23 @@ static fs_status launch_sample(const float* probs, int32_t batch_in, int32_t voc
     if (pivots != 1 && pivots != 2) return FS_ERR_INVALID_ARG;
 
     const bool vec = (vocab % 4 == 0) && ((reinterpret_cast<uintptr_t>(probs) & 15) == 0);
-    const void* fn = soft ? (vec ? reinterpret_cast<const void*>(sample_kernel<true, true>)
-                                 : reinterpret_cast<const void*>(sample_kernel<false, true>))
-                          : (vec ? reinterpret_cast<const void*>(sample_kernel<true, false>)
-                                 : reinterpret_cast<const void*>(sample_kernel<false, false>));
     // One streaming pass per row: the top-k-first order, and sampling without filters.
     const bool single_pass = (order == FS_ORDER_TOP_K_FIRST && top_k) || (!top_k && !top_p && !min_p);
+    // Those run as a scan of the input rows and a finishing launch per output row
+    // (masses of logits depend on the temperature, so sampling logits without filters
+    // stays on the clusters).
+    const bool fin = (order == FS_ORDER_TOP_K_FIRST && top_k) || (!soft && !top_k && !top_p && !min_p);
+    if (fin) return launch_scan_finish(probs, batch_in, vocab, indices, batch_out, top_k, top_p, min_p, order, seed,
+                                       offset, out_token, out_valid, out_rounds, stream, seeds, offsets, offset_dev,
+                                       pivots, soft, temperature, vec);
+    const void* fn = soft ? (vec ? reinterpret_cast<const void*>(sample_kernel<true, true, false>)
+                                 : reinterpret_cast<const void*>(sample_kernel<false, true, false>))
+                          : (vec ? reinterpret_cast<const void*>(sample_kernel<true, false, false>)
+                                 : reinterpret_cast<const void*>(sample_kernel<false, false, false>));
     Plan p;
     fs_status st = make_plan(batch_out, vocab, fn, single_pass, p);
     if (st != FS_OK) return st;
-    SampleArgs a;
+    SampleArgs a = {};
     a.probs = probs;
     a.batch_in = batch_in;
     a.V = vocab;
@@ -644,11 +989,11 @@ static fs_status launch_sample(const float* probs, int32_t batch_in, int32_t voc
     a.ns = p.ns;
     a.nsc = p.nsc;
     if (soft) {
-        if (vec) return launch_cluster(sample_kernel<true, true>, p, batch_out, stream, a);
-        return launch_cluster(sample_kernel<false, true>, p, batch_out, stream, a);
+        if (vec) return launch_cluster(sample_kernel<true, true, false>, p, batch_out, stream, a);
+        return launch_cluster(sample_kernel<false, true, false>, p, batch_out, stream, a);
     }
-    if (vec) return launch_cluster(sample_kernel<true, false>, p, batch_out, stream, a);
-    return launch_cluster(sample_kernel<false, false>, p, batch_out, stream, a);
+    if (vec) return launch_cluster(sample_kernel<true, false, false>, p, batch_out, stream, a);
+    return launch_cluster(sample_kernel<false, false, false>, p, batch_out, stream, a);
 }
 
 __global__ void advance_kernel(unsigned long long* offset_dev, unsigned long long delta) {
@@ -744,7 +1089,7 @@ fs_status fs_sampling_plan(int32_t batch_out, int32_t vocab, int32_t order, int3
     if (order != FS_ORDER_TOP_K_FIRST && order != FS_ORDER_JOINT) return FS_ERR_INVALID_ARG;
     if (vocab > FS_MAX_VOCAB) return FS_ERR_UNSUPPORTED;
     fsd::Plan p;
-    const fs_status st = fsd::make_plan(batch_out, vocab, reinterpret_cast<const void*>(fsd::sample_kernel<true, false>),
+    const fs_status st = fsd::make_plan(batch_out, vocab, reinterpret_cast<const void*>(fsd::sample_kernel<true, false, false>),
                                        order == FS_ORDER_TOP_K_FIRST, p);
     if (st != FS_OK) return st;
     *cluster = p.C;
