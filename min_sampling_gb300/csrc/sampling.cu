@@ -180,60 +180,90 @@ __global__ void __launch_bounds__(NT, 4) scan_kernel(const ScanArgs a) {
 }
 
 // FIN: the summary of input row r into this CTA's tables, as pass 1 and pass1_totals
-// leave them in a one-CTA cluster: segment keys (and, with `masses`, segment masses),
-// part[0] = (M; positive count, bad flag, largest key), and with `hist` the histogram
-// of the segment keys (key >> 21) in hist(), which the caller cleared.  M is the sum of
-// the unit masses in a fixed order (lane-strided, then a tree).  The summary was
-// written by the previous launch, so it is read through L2 (ld.global.cg).
-// Block-collective; the caller synchronises before the tables are read.
-__device__ __forceinline__ void load_summary(const SampleArgs& a, int r, Smem sm, bool masses, bool hist, int warp,
-                                             int lane, int tid) {
+// leave them in a one-CTA cluster: segment keys (and, with `masses`, segment masses)
+// and part[0] = (M; positive count, bad flag, largest key).  M is the sum of the unit
+// masses in a fixed order (thread t adds units t, t + NT, ... in turn, then a tree
+// over the lanes and the warps in order).  Every thread issues all of its loads
+// before it uses any (one round trip to L2).  The summary was written by the previous
+// launch, so it is read through L2 (ld.global.cg).  Block-collective; ends with a
+// block barrier.
+__device__ __forceinline__ void load_summary(const SampleArgs& a, int r, Smem sm, bool masses, int warp, int lane,
+                                             int tid) {
     const uint4* key4 = reinterpret_cast<const uint4*>(a.skey + size_t(r) * a.ls);
     const uint4* mass4 = reinterpret_cast<const uint4*>(a.smass + size_t(r) * a.ls);
+    const uint4* st = a.sstat + size_t(r) * a.nu;
     const int n4 = a.ls >> 2;
+    float ms = 0.f;
+    int p = 0;
+    bool bd = false;
+    uint32_t km = 0;
 #pragma unroll 1
-    for (int i = tid; i < n4; i += NT) {
-        const uint4 k = __ldcg(key4 + i);
-        uint4 m = make_uint4(0u, 0u, 0u, 0u);
-        if (masses) m = __ldcg(mass4 + i);
-        const uint32_t kk[4] = {k.x, k.y, k.z, k.w};
-        const uint32_t mm[4] = {m.x, m.y, m.z, m.w};
+    for (int i0 = 0; i0 < max(n4, a.nu); i0 += 2 * NT) {
+        uint4 k[2], m[2], v[2];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const int s = 4 * i + c;
-            if (s < a.ns) {
-                sm.segkey()[s] = kk[c];
-                if (masses) sm.mass(0)[s] = __uint_as_float(mm[c]);
-                if (hist) atomicAdd(&sm.hist()[min(uint32_t(HBINS - 1), kk[c] >> 21)], 1u);
+        for (int h = 0; h < 2; ++h) {
+            const int i = i0 + h * NT + tid;
+            k[h] = i < n4 ? __ldcg(key4 + i) : make_uint4(0u, 0u, 0u, 0u);
+            m[h] = (masses && i < n4) ? __ldcg(mass4 + i) : make_uint4(0u, 0u, 0u, 0u);
+            v[h] = i < a.nu ? __ldcg(st + i) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int i = i0 + h * NT + tid;
+            if (i < n4) {
+                const uint32_t kk[4] = {k[h].x, k[h].y, k[h].z, k[h].w};
+                const uint32_t mm[4] = {m[h].x, m[h].y, m[h].z, m[h].w};
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    if (4 * i + c < a.ns) {
+                        sm.segkey()[4 * i + c] = kk[c];
+                        if (masses) sm.mass(0)[4 * i + c] = __uint_as_float(mm[c]);
+                    }
+                }
             }
+            ms += __uint_as_float(v[h].x);
+            p += int(v[h].y);
+            bd |= v[h].z != 0u;
+            km = max(km, v[h].w);
         }
     }
-    if (warp == 0) {
-        const uint4* st = a.sstat + size_t(r) * a.nu;
-        float ms = 0.f;
-        int p = 0;
-        bool bd = false;
-        uint32_t km = 0;
+    ms = warp_sum(ms);
+    p = warp_sum_i(p);
+    bd = __any_sync(FULL, bd);
+    km = warp_max_u(km);
+    float* rf = reinterpret_cast<float*>(sm.red());
+    if (lane == 0) {
+        rf[warp] = ms;
+        sm.red()[NW + warp] = p;
+        sm.red()[2 * NW + warp] = bd ? 1 : 0;
+        sm.red()[3 * NW + warp] = int(km);
+    }
+    __syncthreads();
+    if (tid == 0) {
+        Part& pt = sm.part()[0];
+        float m = 0.f;
+        int pp = 0, b = 0;
+        uint32_t mk = 0;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            m += rf[w];
+            pp += sm.red()[NW + w];
+            b |= sm.red()[2 * NW + w];
+            mk = max(mk, uint32_t(sm.red()[3 * NW + w]));
+        }
+        pt.f[0] = m;
+        pt.u[0] = uint32_t(pp);
+        pt.u[1] = uint32_t(b);
+        pt.u[2] = mk;
+    }
+    __syncthreads();
+}
+
+// FIN: the histogram of this CTA's segment keys (key >> 21) into hist(), which the
+// caller cleared.  Block-collective; the caller synchronises before it is read.
+__device__ __forceinline__ void summary_hist(Smem sm, int ns, int tid) {
 #pragma unroll 1
-        for (int i = lane; i < a.nu; i += 32) {
-            const uint4 v = __ldcg(st + i);
-            ms += __uint_as_float(v.x);
-            p += int(v.y);
-            bd |= v.z != 0u;
-            km = max(km, v.w);
-        }
-        ms = warp_sum(ms);
-        p = warp_sum_i(p);
-        bd = __any_sync(FULL, bd);
-        km = warp_max_u(km);
-        if (lane == 0) {
-            Part& pt = sm.part()[0];
-            pt.f[0] = ms;
-            pt.u[0] = uint32_t(p);
-            pt.u[1] = bd ? 1u : 0u;
-            pt.u[2] = km;
-        }
-    }
+    for (int i = tid; i < ns; i += NT) atomicAdd(&sm.hist()[min(uint32_t(HBINS - 1), sm.segkey()[i] >> 21)], 1u);
 }
 
 // The acceptance test f(tau) ([blog] rejection sampling: count / remaining mass above
@@ -492,6 +522,9 @@ __global__ void __launch_bounds__(NT, FIN ? 2 : 3) sample_kernel(const SampleArg
             *reinterpret_cast<unsigned long long*>(pr + 6) =
                 (a.offsets ? a.offsets[b] : a.offset) + (a.offset_dev ? *a.offset_dev : 0ull);
         }
+        // The summary's loads go out with the parameters' (logit rows without a top-k
+        // bound replace the tables with a pass over the row below).
+        if (row_ok) load_summary(a, r, sm, !SOFT, warp, lane, tid);
     } else if (row_ok) {
         if (SOFT && kfirst_soft)  // draws come from the gathered candidates: keys only
             pass1<VEC, true, false, 1>(row, g, sm, hist_sh, warp, lane, pos, bad, kmax, setup);
@@ -529,8 +562,8 @@ __global__ void __launch_bounds__(NT, FIN ? 2 : 3) sample_kernel(const SampleArg
             // here, from L2, as pass 1 reads it.
             pass1<VEC, true, false, 2>(row, g, sm, -1, warp, lane, pos, bad, kmax);
             pass1_totals(g, sm, true, 0, 1, pos, bad, kmax, -1, true, true, warp, lane, tid, true, 0);
-        } else {
-            load_summary(a, r, sm, !SOFT, need_hist, warp, lane, tid);
+        } else if (need_hist) {
+            summary_hist(sm, ns, tid);  // the tables were loaded with the parameters
         }
         __syncthreads();  // the tables, part[0] and the histogram
     } else {
