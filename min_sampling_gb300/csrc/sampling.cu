@@ -51,7 +51,7 @@ struct SampleArgs {
     // Finishing launch (FIN): the row summaries written by scan_kernel.
     const uint32_t* skey;     // [batch_in][ls] segment maxima (order keys)
     const float* smass;       // [batch_in][ls] segment masses (rows of probabilities)
-    const uint4* sstat;       // [batch_in][nu] per unit: mass, positives, bad flag, largest key
+    const uint4* sstat;       // [batch_in][nu] per unit: mass, 0, bad flag, largest key
     int ls;                   // words per row of skey / smass
     int nu;                   // units per row
 };
@@ -65,7 +65,8 @@ struct SampleArgs {
 // units w, w + W, w + 2W, ... of the matrix in row-major order (W warps in the grid),
 // so every SM streams the same number of bytes whatever the batch.  Per unit it writes
 // each segment's largest order key and mass, and the unit's mass, positive count, bad
-// flag and largest key.  The finishing launch (sample_kernel with FIN, one CTA per
+// flag and largest key (no positive count: V bounds it).  The finishing launch
+// (sample_kernel with FIN, one CTA per
 // output row) reads the summary of its input row from L2 and goes on exactly as the
 // one-CTA cluster does after pass 1.  Nothing in scan_kernel waits on another thread.
 struct ScanArgs {
@@ -86,9 +87,19 @@ size_t scan_workspace_bytes(int batch_in, int vocab) {
     return size_t(batch_in) * (2 * ls * 4 + size_t(scan_units(vocab)) * 16);
 }
 
-// LOGITS: keys are logit keys, the positive count counts logits above -inf, +inf is a
-// bad value as well as NaN, and no masses are kept (they depend on the temperature).
-template <bool VEC, bool LOGITS>
+// Kinds of summary.  SCAN_KEYS (rows of probabilities, paths that draw only from
+// gathered candidates): segment maxima and unit totals.  SCAN_MASSES: segment masses
+// as well (a draw over the whole row).  SCAN_LOGITS: maxima as logit keys, no masses
+// (they depend on the temperature).
+enum : int { SCAN_KEYS = 0, SCAN_MASSES = 1, SCAN_LOGITS = 2 };
+
+// Per lane and block of four values, a few min / max / add instructions: the block's
+// largest value (its order key after the warp maximum), its smallest (a negative one
+// marks the row bad) and its sum.  A NaN passes through the sums and makes the row's
+// total NaN, which the finishing launch treats as invalid; for logits a NaN sum or a
+// +inf maximum marks the unit bad.  The unit record: mass (sum of its values, in
+// block order), 0, bad flag, largest key.
+template <bool VEC, int KIND>
 __global__ void __launch_bounds__(NT, 4) scan_kernel(const ScanArgs a) {
     grid_dependency_wait();
     allow_dependents();
@@ -96,6 +107,7 @@ __global__ void __launch_bounds__(NT, 4) scan_kernel(const ScanArgs a) {
     const long long total = (long long)a.rows * a.nu;
     const long long step = (long long)gridDim.x * NW;
     const int spu = TB >> a.shift;  // segments per unit
+    constexpr bool LOGITS = KIND == SCAN_LOGITS;
     const float fill = LOGITS ? __int_as_float(0xff800000) : 0.f;
     auto load_unit = [&](long long u, float4* v) {
         if (u < total) {
@@ -118,34 +130,34 @@ __global__ void __launch_bounds__(NT, 4) scan_kernel(const ScanArgs a) {
         const int r = int(u / a.nu), q = int(u - (long long)r * a.nu);
         uint32_t km[TB];
         float s[TB];
-        int pos = 0;
+        float lo = 0.f;
         bool bad = false;
 #pragma unroll
         for (int j = 0; j < TB; ++j) {
-            const int base = (q * TB + j) * BLK + lane * 4;
-            uint32_t k = 0;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const float x = q_at(A[j], c);
-                if (!LOGITS) {
-                    bad |= !(x >= 0.f);
-                    k = max(k, prob_key(x));
-                    pos += x > 0.f;
-                } else {
-                    const bool in = base + c < a.V;
-                    bad |= isnan(x) || (in && x == __int_as_float(0x7f800000));
-                    pos += in && x > __int_as_float(0xff800000);
-                    k = max(k, in ? logit_key(x) : 0u);
-                }
+            const float4 v = A[j];
+            const float mx = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+            s[j] = (v.x + v.y) + (v.z + v.w);
+            if (LOGITS) {
+                bad |= isnan(s[j]) || mx == __int_as_float(0x7f800000);
+                km[j] = __reduce_max_sync(FULL, logit_key(mx));
+            } else {
+                lo = fminf(lo, fminf(fminf(v.x, v.y), fminf(v.z, v.w)));
+                km[j] = __reduce_max_sync(FULL, prob_key(mx));
             }
-            km[j] = __reduce_max_sync(FULL, k);
-            s[j] = LOGITS ? 0.f : (A[j].x + A[j].y) + (A[j].z + A[j].w);
         }
-        if (!LOGITS) {
+        if (!LOGITS) bad = lo < 0.f;
+        float um = 0.f;
+        if (KIND == SCAN_MASSES) {
 #pragma unroll
             for (int m = 16; m; m >>= 1)
 #pragma unroll
                 for (int j = 0; j < TB; ++j) s[j] += __shfl_xor_sync(FULL, s[j], m);
+#pragma unroll
+            for (int j = 0; j < TB; ++j) um += s[j];
+        } else if (KIND == SCAN_KEYS) {
+#pragma unroll
+            for (int j = 0; j < TB; ++j) um += s[j];
+            um = warp_sum(um);
         }
         // Lane l < spu: segment q * spu + l, its blocks combined in order.
         const int sg = q * spu + lane;
@@ -159,19 +171,14 @@ __global__ void __launch_bounds__(NT, 4) scan_kernel(const ScanArgs a) {
                 kk = mine ? max(kk, km[j]) : kk;
             }
             a.key[size_t(r) * a.ls + sg] = kk;
-            if (!LOGITS) a.mass[size_t(r) * a.ls + sg] = ss;
+            if (KIND == SCAN_MASSES) a.mass[size_t(r) * a.ls + sg] = ss;
         }
-        pos = warp_sum_i(pos);
         const unsigned anybad = __ballot_sync(FULL, bad);
         if (lane == 0) {
-            float um = 0.f;
             uint32_t kx = 0;
 #pragma unroll
-            for (int j = 0; j < TB; ++j) {
-                um += s[j];
-                kx = max(kx, km[j]);
-            }
-            a.stat[size_t(r) * a.nu + q] = make_uint4(__float_as_uint(um), uint32_t(pos), anybad ? 1u : 0u, kx);
+            for (int j = 0; j < TB; ++j) kx = max(kx, km[j]);
+            a.stat[size_t(r) * a.nu + q] = make_uint4(__float_as_uint(um), 0u, anybad ? 1u : 0u, kx);
         }
 #pragma unroll
         for (int j = 0; j < TB; ++j) A[j] = Bv[j];
@@ -181,12 +188,12 @@ __global__ void __launch_bounds__(NT, 4) scan_kernel(const ScanArgs a) {
 
 // FIN: the summary of input row r into this CTA's tables, as pass 1 and pass1_totals
 // leave them in a one-CTA cluster: segment keys (and, with `masses`, segment masses)
-// and part[0] = (M; positive count, bad flag, largest key).  M is the sum of the unit
-// masses in a fixed order (thread t adds units t, t + NT, ... in turn, then a tree
-// over the lanes and the warps in order).  Every thread issues all of its loads
-// before it uses any (one round trip to L2).  The summary was written by the previous
-// launch, so it is read through L2 (ld.global.cg).  Block-collective; ends with a
-// block barrier.
+// and part[0] = (M; V as the bound of the positive count, bad flag, largest key).  M
+// is the sum of the unit masses in a fixed order (thread t adds units t, t + NT, ...
+// in turn, then a tree over the lanes and the warps in order).  Every thread issues
+// all of its loads before it uses any (one round trip to L2).  The summary was
+// written by the previous launch, so it is read through L2 (ld.global.cg).
+// Block-collective; ends with a block barrier.
 __device__ __forceinline__ void load_summary(const SampleArgs& a, int r, Smem sm, bool masses, int warp, int lane,
                                              int tid) {
     const uint4* key4 = reinterpret_cast<const uint4*>(a.skey + size_t(r) * a.ls);
@@ -194,7 +201,6 @@ __device__ __forceinline__ void load_summary(const SampleArgs& a, int r, Smem sm
     const uint4* st = a.sstat + size_t(r) * a.nu;
     const int n4 = a.ls >> 2;
     float ms = 0.f;
-    int p = 0;
     bool bd = false;
     uint32_t km = 0;
 #pragma unroll 1
@@ -222,37 +228,33 @@ __device__ __forceinline__ void load_summary(const SampleArgs& a, int r, Smem sm
                 }
             }
             ms += __uint_as_float(v[h].x);
-            p += int(v[h].y);
             bd |= v[h].z != 0u;
             km = max(km, v[h].w);
         }
     }
     ms = warp_sum(ms);
-    p = warp_sum_i(p);
     bd = __any_sync(FULL, bd);
     km = warp_max_u(km);
     float* rf = reinterpret_cast<float*>(sm.red());
     if (lane == 0) {
         rf[warp] = ms;
-        sm.red()[NW + warp] = p;
-        sm.red()[2 * NW + warp] = bd ? 1 : 0;
-        sm.red()[3 * NW + warp] = int(km);
+        sm.red()[NW + warp] = bd ? 1 : 0;
+        sm.red()[2 * NW + warp] = int(km);
     }
     __syncthreads();
     if (tid == 0) {
         Part& pt = sm.part()[0];
         float m = 0.f;
-        int pp = 0, b = 0;
+        int b = 0;
         uint32_t mk = 0;
 #pragma unroll
         for (int w = 0; w < NW; ++w) {
             m += rf[w];
-            pp += sm.red()[NW + w];
-            b |= sm.red()[2 * NW + w];
-            mk = max(mk, uint32_t(sm.red()[3 * NW + w]));
+            b |= sm.red()[NW + w];
+            mk = max(mk, uint32_t(sm.red()[2 * NW + w]));
         }
         pt.f[0] = m;
-        pt.u[0] = uint32_t(pp);
+        pt.u[0] = uint32_t(a.V);  // the scan counts no positives: V bounds the tokens above 0
         pt.u[1] = uint32_t(b);
         pt.u[2] = mk;
     }
@@ -447,7 +449,7 @@ __device__ __forceinline__ int small_rounds(const Small& s, const bool* kept, co
 // one-CTA clusters): the row's summary replaces pass 1, and everything after it runs
 // as in a cluster of one.
 template <bool VEC, bool SOFT, bool FIN>
-__global__ void __launch_bounds__(NT, FIN ? 2 : 3) sample_kernel(const SampleArgs a) {
+__device__ __forceinline__ void sample_row(const SampleArgs& a) {
     const int C = int(cluster_nctarank());
     const int rank = int(cluster_ctarank());
     const int b = int(cluster_id_x());
@@ -524,7 +526,7 @@ __global__ void __launch_bounds__(NT, FIN ? 2 : 3) sample_kernel(const SampleArg
         }
         // The summary's loads go out with the parameters' (logit rows without a top-k
         // bound replace the tables with a pass over the row below).
-        if (row_ok) load_summary(a, r, sm, !SOFT, warp, lane, tid);
+        if (row_ok) load_summary(a, r, sm, !SOFT && a.smass != nullptr, warp, lane, tid);
     } else if (row_ok) {
         if (SOFT && kfirst_soft)  // draws come from the gathered candidates: keys only
             pass1<VEC, true, false, 1>(row, g, sm, hist_sh, warp, lane, pos, bad, kmax, setup);
@@ -556,12 +558,17 @@ __global__ void __launch_bounds__(NT, FIN ? 2 : 3) sample_kernel(const SampleArg
                 sm.mass(0)[i] = 0.f;
             }
             if (tid == 0) sm.part()[0] = Part{};
-        } else if (SOFT && !kfirst) {
-            // Masses of logits depend on the row's temperature, which the summary does
-            // not know: this row (no top-k bound in a top-k-first launch) is read again
-            // here, from L2, as pass 1 reads it.
-            pass1<VEC, true, false, 2>(row, g, sm, -1, warp, lane, pos, bad, kmax);
-            pass1_totals(g, sm, true, 0, 1, pos, bad, kmax, -1, true, true, warp, lane, tid, true, 0);
+        } else if (!kfirst && (SOFT || !a.smass)) {
+            // A draw over the whole row needs segment masses, which this summary does not
+            // hold (masses of logits also depend on the row's temperature): this row (no
+            // top-k bound in a top-k-first launch) is read again here, from L2, as pass 1
+            // reads it.
+            if (SOFT) {
+                pass1<VEC, true, false, 2>(row, g, sm, -1, warp, lane, pos, bad, kmax);
+            } else {
+                pass1<VEC, true, true>(row, g, sm, -1, warp, lane, pos, bad, kmax);
+            }
+            pass1_totals(g, sm, true, 0, 1, pos, bad, kmax, -1, true, true, warp, lane, tid, SOFT, 0);
         } else if (need_hist) {
             summary_hist(sm, ns, tid);  // the tables were loaded with the parameters
         }
@@ -850,6 +857,234 @@ __global__ void __launch_bounds__(NT, FIN ? 2 : 3) sample_kernel(const SampleArg
     }
 }
 
+template <bool VEC, bool SOFT, bool FIN>
+__global__ void __launch_bounds__(NT, FIN ? 2 : 3) sample_kernel(const SampleArgs a) {
+    sample_row<VEC, SOFT, FIN>(a);
+}
+
+// The whole finishing path of one row, out of line: the lean top-k-first kernel's
+// fallback for rows outside its fast case.
+template <bool VEC>
+FS_COLD __device__ void sample_row_fin(const SampleArgs& a) {
+    sample_row<VEC, false, true>(a);
+}
+
+// ------------------------------------------------------------------ lean top-k-first finish
+
+// The finishing launch of the top-k-first samplers on rows of probabilities, for the
+// usual row: segments of one block (V <= 2^19), and a top-k bound L0 from the
+// histogram of the segment maxima ([explainer] filter order: the k-th largest of any
+// subset of the row, here the segment maxima, is at most the row's own) that leaves
+// at most SMALL live segments (maximum >= L0) and at most SMALL elements >= L0.  Two
+// round trips to L2 in all: (1) the row's summary with its parameters, then the
+// histogram, L0 and the live segments in index order; (2) the live segments' values,
+// and their elements >= L0 written in index order into the candidate list.  Warp 0
+// then finishes in registers exactly as the cluster's leader does: t_k and F_k among
+// the candidates, the rejection rounds ([blog] dual pivot) and the outputs.  Any other
+// row (a bad row index, no top-k filter, fewer segments than k, a larger bound or list)
+// takes the general finishing path, out of line.
+template <bool VEC>
+__global__ void __launch_bounds__(NT, 2) kfirst_kernel(const SampleArgs a) {
+    const int b = int(cluster_id_x());
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const Smem sm(a.ns);
+    const int V = a.V, ns = a.ns;
+    const KeyProb keyf;
+    grid_dependency_wait();
+    allow_dependents();
+    const int r = a.indices ? a.indices[b] : b;
+    const bool row_ok = r >= 0 && r < a.batch_in;
+    // ---- (1) parameters, the cleared histogram, the summary
+    for (int i = tid; i < HBINS; i += NT) sm.hist()[i] = 0u;
+    if (tid == NT - 32) {
+        uint32_t* pr = sm.prm();
+        pr[0] = uint32_t(a.top_k ? a.top_k[b] : 0);
+        pr[1] = __float_as_uint(a.top_p ? a.top_p[b] : 1.f);
+        pr[2] = __float_as_uint(a.min_p ? a.min_p[b] : 0.f);
+        *reinterpret_cast<unsigned long long*>(pr + 4) = a.seeds ? a.seeds[b] : a.seed;
+        *reinterpret_cast<unsigned long long*>(pr + 6) =
+            (a.offsets ? a.offsets[b] : a.offset) + (a.offset_dev ? *a.offset_dev : 0ull);
+    }
+    if (row_ok) {
+        load_summary(a, r, sm, false, warp, lane, tid);  // ends with a block barrier
+    } else {
+        __syncthreads();
+    }
+    const int k = int(sm.prm()[0]);
+    if (!row_ok || !(k > 0 && k < V) || ns < k || a.shift != 0) {
+        __syncthreads();
+        sample_row_fin<VEC>(a);
+        return;
+    }
+    // Histogram of the segment maxima (key >> 21): lanes with the same bin add once.
+#pragma unroll 1
+    for (int i0 = 0; i0 < ns; i0 += NT) {
+        const int i = i0 + tid;
+        const uint32_t bin = i < ns ? min(uint32_t(HBINS - 1), sm.segkey()[i] >> 21) : 0xffffffffu;
+        const unsigned grp = __match_any_sync(FULL, bin);
+        if (i < ns && lane == __ffs(grp) - 1) atomicAdd(&sm.hist()[bin], uint32_t(__popc(grp)));
+    }
+    __syncthreads();
+    const uint32_t maxkey = sm.part()[0].u[2];
+    if (warp == 0) {
+        uint32_t above;
+        const int B = scan_bins_down<uint32_t>(sm.hist(), int(min(uint32_t(HBINS - 1), maxkey >> 21)), uint32_t(k),
+                                               lane, above);
+        if (lane == 0) {
+            sm.bcast()[0] = max(B, 0);
+            sm.bcast()[1] = B >= 0 ? int(above + sm.hist()[B]) : INT_BIG;
+        }
+    }
+    __syncthreads();
+    if (sm.bcast()[1] > SMALL) {
+        __syncthreads();
+        sample_row_fin<VEC>(a);
+        return;
+    }
+    const uint32_t L0 = max(1u, uint32_t(sm.bcast()[0]) << 21);
+    // Live segments (maximum >= L0), in index order: each warp lists those of its
+    // contiguous share into list[] from the share's start; then lane w < NW of every
+    // warp holds warp w's count and the inclusive prefix over warps.
+    int r0, r1;
+    warp_range(ns, warp, r0, r1);
+    int nl = 0;
+#pragma unroll 1
+    for (int b0 = r0; b0 < r1; b0 += 32) {
+        const int i = b0 + lane;
+        const bool live = i < r1 && sm.segkey()[i] >= L0;
+        const unsigned bal = __ballot_sync(FULL, live);
+        if (live) sm.list()[r0 + nl + __popc(bal & ((1u << lane) - 1u))] = i;
+        nl += __popc(bal);
+    }
+    if (lane == 0) sm.red()[warp] = nl;
+    __syncthreads();
+    const int wn = lane < NW ? sm.red()[lane] : 0;
+    const int wincl = warp_incl_scan_i(wn, lane);
+    int ws0, ws1;
+    warp_range(ns, lane < NW ? lane : 0, ws0, ws1);
+    const int nlive = __shfl_sync(FULL, wincl, NW - 1);
+    // The segment of live entry j (index order).
+    auto live_seg = [&](int j) {
+        const int w = __popc(__ballot_sync(FULL, lane < NW && wincl <= j));
+        const int first = __shfl_sync(FULL, wincl - wn, w);
+        const int start = __shfl_sync(FULL, ws0, w);
+        return sm.list()[start + j - first];
+    };
+    // ---- (2) warp x loads live entries x, x + NW, ... (at most SMALL / NW each) at once.
+    constexpr int PER = SMALL / NW;
+    float4 v[PER];
+    int seg[PER];
+    const float* row = a.probs + size_t(r) * size_t(V);
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int j = warp + NW * i;
+        seg[i] = j < nlive ? live_seg(j) : 0;
+        v[i] = j < nlive ? load4<VEC, true>(row, V, seg[i] * BLK + lane * 4, 0.f) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    __syncthreads();  // every warp has read the warp counts in red[]
+    // Per live entry: its count of elements >= L0 into red[j].
+    int kc[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int j = warp + NW * i;
+        int c = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) c += keyf(q_at(v[i], q)) >= L0 && seg[i] * BLK + lane * 4 + q < V;
+        kc[i] = c;
+        const int t = warp_sum_i(c);
+        if (j < nlive && lane == 0) sm.red()[j] = t;
+    }
+    __syncthreads();
+    // Exclusive prefix of the entries' counts (lane l holds entries 4l .. 4l + 3).
+    int cnt4[4], own = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        cnt4[q] = 4 * lane + q < nlive ? sm.red()[4 * lane + q] : 0;
+        own += cnt4[q];
+    }
+    const int incl = warp_incl_scan_i(own, lane);
+    const int n = __shfl_sync(FULL, incl, 31);
+    if (n > SMALL) {
+        __syncthreads();
+        sample_row_fin<VEC>(a);
+        return;
+    }
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int j = warp + NW * i;
+        if (j < nlive) {
+            // offset of entry j: counts of the entries before it
+            const int lj = j >> 2, qj = j & 3;
+            int before = __shfl_sync(FULL, incl - own, lj);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) before += q < qj ? __shfl_sync(FULL, cnt4[q], lj) : 0;
+            int p = before + warp_incl_scan_i(kc[i], lane) - kc[i];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float x = q_at(v[i], q);
+                const int ix = seg[i] * BLK + lane * 4 + q;
+                if (keyf(x) >= L0 && ix < V) {
+                    sm.lv()[p] = x;
+                    sm.li()[p] = ix;
+                    ++p;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    // ---- warp 0: t_k, F_k, the rounds, the outputs (as the cluster's leader)
+    const float tp = __uint_as_float(sm.prm()[1]);
+    const float mp = __uint_as_float(sm.prm()[2]);
+    const unsigned long long seed_b = *reinterpret_cast<const unsigned long long*>(sm.prm() + 4);
+    const unsigned long long offset_b = *reinterpret_cast<const unsigned long long*>(sm.prm() + 6);
+    const uint32_t stream_b = a.seeds ? 0u : uint32_t(b);
+    const float M = sm.part()[0].f[0];
+    const bool any_bad = sm.part()[0].u[1] != 0u;
+    const float rowmax = __uint_as_float(maxkey);
+    Pred f;
+    f.single = a.single_pivot != 0;
+    f.k_on = true;
+    f.k = k;
+    f.p_on = tp < 1.f;
+    f.m_on = mp > 0.f;
+    f.pthr = 0.f;
+    f.t32 = 0.f;
+    bool valid = !isnan(tp) && !isnan(mp) && !any_bad && M > 0.f && M <= 3.402823466e38f;
+    if (f.m_on) {
+        f.t32 = __double2float_ru(double(mp) * double(rowmax));
+        if (!(rowmax >= f.t32)) valid = false;
+    }
+    int token = -1, rounds = 0;
+    if (valid) {
+        Small sl;
+        sl.n = n;
+#pragma unroll
+        for (int q = 0; q < SR; ++q) {
+            const int e = SR * lane + q;
+            sl.in[q] = e < n;
+            sl.x[q] = sl.in[q] ? sm.lv()[e] : 0.f;
+            sl.i[q] = sl.in[q] ? sm.li()[e] : 0;
+        }
+        const uint32_t tk = small_kth(sl, k, keyf);
+        bool kept[SR];
+        float fk = 0.f;
+#pragma unroll
+        for (int q = 0; q < SR; ++q) {
+            kept[q] = sl.in[q] && keyf(sl.x[q]) >= tk;
+            fk += kept[q] ? sl.x[q] : 0.f;
+        }
+        const float Fk = warp_sum(fk);
+        f.pthr = tp * Fk;  // top-p inside the k, measured against F_k
+        token = small_rounds(sl, kept, f, Fk, rowmax, seed_b, offset_b, stream_b, lane, rounds);
+    }
+    if (lane == 0) {
+        a.out_token[b] = token >= 0 ? token : -1;
+        a.out_valid[b] = token >= 0 ? 1 : 0;
+        if (a.out_rounds) a.out_rounds[b] = rounds;
+    }
+}
+
 // ------------------------------------------------------------------ host side
 
 #ifndef FS_SCAN_PER_SM
@@ -869,7 +1104,7 @@ static fs_status scan_grid(long long units, int& grid) {
     return FS_OK;
 }
 
-template <bool LOGITS>
+template <int KIND>
 static fs_status launch_scan(const float* x, int rows, int V, int shift, int ns, bool vec, void* ws, void* stream) {
     ScanArgs s;
     s.x = x;
@@ -895,8 +1130,8 @@ static fs_status launch_scan(const float* x, int rows, int V, int shift, int ns,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = vec ? cudaLaunchKernelEx(&cfg, scan_kernel<true, LOGITS>, s)
-                        : cudaLaunchKernelEx(&cfg, scan_kernel<false, LOGITS>, s);
+    cudaError_t e = vec ? cudaLaunchKernelEx(&cfg, scan_kernel<true, KIND>, s)
+                        : cudaLaunchKernelEx(&cfg, scan_kernel<false, KIND>, s);
     if (e != cudaSuccess) return cuda_fail(e);
     return FS_OK;
 }
@@ -908,8 +1143,10 @@ static fs_status launch_scan_finish(const float* probs, int32_t batch_in, int32_
                                     uint8_t* out_valid, int32_t* out_rounds, void* stream, const uint64_t* seeds,
                                     const uint64_t* offsets, const uint64_t* offset_dev, int32_t pivots, bool soft,
                                     const float* temperature, bool vec) {
+    const bool kfirst = order == FS_ORDER_TOP_K_FIRST && top_k;
     auto fin_fn = [&]() -> void (*)(SampleArgs) {
         if (soft) return vec ? sample_kernel<true, true, true> : sample_kernel<false, true, true>;
+        if (kfirst) return vec ? kfirst_kernel<true> : kfirst_kernel<false>;
         return vec ? sample_kernel<true, false, true> : sample_kernel<false, false, true>;
     };
     void (*fn)(SampleArgs) = fin_fn();
@@ -928,11 +1165,16 @@ static fs_status launch_scan_finish(const float* probs, int32_t batch_in, int32_
     p.per_sm = 0;
     if (p.smem > optin) return FS_ERR_UNSUPPORTED;
     void* ws = nullptr;
+    // Top-k-first launches draw from gathered candidates: no segment masses needed.
     if (batch_in > 0) {
         st = workspace(scan_workspace_bytes(batch_in, vocab), stream, &ws);
         if (st != FS_OK) return st;
-        st = soft ? launch_scan<true>(probs, batch_in, vocab, p.shift, p.ns, vec, ws, stream)
-                  : launch_scan<false>(probs, batch_in, vocab, p.shift, p.ns, vec, ws, stream);
+        if (soft)
+            st = launch_scan<SCAN_LOGITS>(probs, batch_in, vocab, p.shift, p.ns, vec, ws, stream);
+        else if (kfirst)
+            st = launch_scan<SCAN_KEYS>(probs, batch_in, vocab, p.shift, p.ns, vec, ws, stream);
+        else
+            st = launch_scan<SCAN_MASSES>(probs, batch_in, vocab, p.shift, p.ns, vec, ws, stream);
         if (st != FS_OK) return st;
     }
     SampleArgs a = {};
@@ -960,8 +1202,9 @@ static fs_status launch_scan_finish(const float* probs, int32_t batch_in, int32_
     a.ls = scan_row_words(p.ns);
     a.nu = scan_units(vocab);
     a.skey = reinterpret_cast<const uint32_t*>(ws);
-    a.smass = ws ? reinterpret_cast<const float*>(reinterpret_cast<const char*>(ws) + size_t(batch_in) * a.ls * 4)
-                 : nullptr;
+    a.smass = (ws && !soft && !kfirst)
+                  ? reinterpret_cast<const float*>(reinterpret_cast<const char*>(ws) + size_t(batch_in) * a.ls * 4)
+                  : nullptr;
     a.sstat = ws ? reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(ws) + 2 * size_t(batch_in) * a.ls * 4)
                  : nullptr;
     return launch_cluster(fn, p, batch_out, stream, a);
