@@ -64,6 +64,8 @@ def parse_args_from(argv):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-entries", action="store_true",
                     help="time only the headline step (no other entries, no pivot ablation)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other workloads (configs 2, 4 and 5; the headline at B=1)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-oracle sample")
     ap.add_argument("--profile", action="store_true",
                     help="only run the headline step (warmup + steps launches) for a profiler; prints a short line")
@@ -411,6 +413,11 @@ def run_ours(args):
         ablation["dual"]["us_per_call"] = entries["joint"]["us_per_call"]
         ablation["single"]["us_per_call"] = entries["joint_single_pivot"]["us_per_call"]
 
+    configs = None
+    if not args.no_configs and world == 1:
+        peak0, _ = measured_peak()
+        configs = time_configs(lib, dev, stream, check, timed, K, peak0, seed)
+
     # End to end through the C ABI with host buffers.
     host_p = torch.from_numpy(w.probs).pin_memory()
     host_k = top_k.cpu().pin_memory()
@@ -459,6 +466,7 @@ def run_ours(args):
         "pivot_ablation": ({"workload": "joint top-k 50 + top-p 0.9, B=64, V=151936", **ablation}
                            if ablation else None),
         "entries": entries,
+        "configs": configs,
     }
     if rank == 0 and world == 1:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
@@ -470,24 +478,101 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
 
 
+def cpu_model() -> str:
+    """The host CPU's model name from /proc/cpuinfo (or the Arm implementer / part)."""
+    try:
+        with open("/proc/cpuinfo") as fh:
+            info = fh.read().splitlines()
+    except OSError:
+        return "unknown"
+    for key in ("model name", "Model name", "cpu model"):
+        for line in info:
+            if line.lower().startswith(key.lower()) and ":" in line:
+                return line.split(":", 1)[1].strip()
+    parts = {}
+    for line in info:
+        if ":" in line:
+            k, v = (x.strip() for x in line.split(":", 1))
+            if k in ("CPU implementer", "CPU part", "CPU variant") and k not in parts:
+                parts[k] = v
+    return ", ".join(f"{k} {v}" for k, v in parts.items()) or "unknown"
+
+
+_POOL_ROWS = None
+
+
+def _pool_init(path):
+    """Worker start-up: map the matrix that the parent saved (no copy per job)."""
+    import numpy as np
+    global _POOL_ROWS
+    _POOL_ROWS = np.load(path, mmap_mode="r")
+
+
+def _oracle_rows(args):
+    """Worker: the oracle's sort-based sampler on rows [r0, r1) of the mapped matrix."""
+    import numpy as np
+
+    from oracle import baseline
+    r0, r1, k, p, seed = args
+    n = r1 - r0
+    baseline.sample_rows(np.asarray(_POOL_ROWS[r0:r1]), np.full(n, k, np.int32), np.full(n, p, np.float32), None,
+                         "top_k_first", rng=np.random.default_rng(seed))
+    return n
+
+
 def cpu_baseline(w, budget_s: float):
     """The CPU oracle (sort-based sampler) as it stands, on whole rows of the same
-    matrix, until `budget_s` of CPU time has been spent."""
+    matrix: first in this process (one thread), then in one process per host core
+    (a spawned pool, so that no worker inherits the CUDA context), each leg until about
+    half of `budget_s` is spent."""
+    import multiprocessing as mp
+
     import numpy as np
 
     from oracle import baseline
 
     rng = np.random.default_rng(0)
+    half = budget_s / 2
     t0 = time.perf_counter()
     rows = 0
-    while time.perf_counter() - t0 < budget_s and rows < 4 * B:
+    while time.perf_counter() - t0 < half and rows < 4 * B:
         r = rows % B
         baseline.sample_rows(w.probs[r:r + 1], w.top_k[r:r + 1], w.top_p[r:r + 1], None, "top_k_first", rng=rng)
         rows += 1
-    dt = time.perf_counter() - t0
-    return {"value": round(rows / dt, 3), "unit": "rows/s", "cores": 1, "kind": "oracle",
-            "sample": f"{rows} rows of the same B=64 x V=151936 matrix, one sorted-row draw each, "
-                      f"numpy single-threaded, {dt:.1f} s"}
+    dt1 = time.perf_counter() - t0
+    one = rows / dt1
+    cores = os.cpu_count() or 1
+    many, rows_n, dtn = None, 0, 0.0
+    fd, path = tempfile.mkstemp(suffix=".npy")
+    os.close(fd)
+    try:
+        np.save(path, w.probs)
+        ctx = mp.get_context("spawn")
+        k, p = int(w.top_k[0]), float(w.top_p[0])
+        with ctx.Pool(cores, initializer=_pool_init, initargs=(path,)) as pool:
+            pool.map(_oracle_rows, [(i % B, i % B + 1, k, p, i) for i in range(cores)])   # start-up, untimed
+            t0 = time.perf_counter()
+            seed = 1000
+            while time.perf_counter() - t0 < half:
+                jobs = [((seed + i) % B, (seed + i) % B + 1, k, p, seed + i) for i in range(4 * cores)]
+                seed += 4 * cores
+                rows_n += sum(pool.map(_oracle_rows, jobs, chunksize=1))
+            dtn = time.perf_counter() - t0
+        many = rows_n / dtn
+    except Exception as e:   # no process pool on this host: report the one-thread leg
+        log(f"cpu_baseline: process pool unavailable ({e}); one thread only")
+    finally:
+        os.unlink(path)
+    model = cpu_model()
+    single = {"value": round(one, 3), "cores": 1,
+              "sample": f"{rows} rows, numpy in one process, {dt1:.1f} s"}
+    if many is None:
+        return {"value": single["value"], "unit": "rows/s", "cores": 1, "kind": "oracle", "cpu_model": model,
+                "sample": f"{rows} rows of the same B=64 x V=151936 matrix, one sorted-row draw each, "
+                          f"numpy single-threaded, {dt1:.1f} s"}
+    return {"value": round(many, 3), "unit": "rows/s", "cores": cores, "kind": "oracle", "cpu_model": model,
+            "sample": f"{rows_n} rows of the same B=64 x V=151936 matrix, one sorted-row draw each, "
+                      f"{cores} spawned processes, {dtn:.1f} s", "single_thread": single}
 
 
 # ---------------------------------------------------------------------------- the other configs

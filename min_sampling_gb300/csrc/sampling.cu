@@ -188,14 +188,15 @@ __global__ void __launch_bounds__(NT, 4) scan_kernel(const ScanArgs a) {
 
 // FIN: the summary of input row r into this CTA's tables, as pass 1 and pass1_totals
 // leave them in a one-CTA cluster: segment keys (and, with `masses`, segment masses)
-// and part[0] = (M; V as the bound of the positive count, bad flag, largest key).  M
+// and part[0] = (M; V as the bound of the positive count, bad flag, largest key), and
+// with `ukey` each unit's largest key in ukey[0, nu).  M
 // is the sum of the unit masses in a fixed order (thread t adds units t, t + NT, ...
 // in turn, then a tree over the lanes and the warps in order).  Every thread issues
 // all of its loads before it uses any (one round trip to L2).  The summary was
 // written by the previous launch, so it is read through L2 (ld.global.cg).
 // Block-collective; ends with a block barrier.
 __device__ __forceinline__ void load_summary(const SampleArgs& a, int r, Smem sm, bool masses, int warp, int lane,
-                                             int tid) {
+                                             int tid, uint32_t* ukey = nullptr) {
     const uint4* key4 = reinterpret_cast<const uint4*>(a.skey + size_t(r) * a.ls);
     const uint4* mass4 = reinterpret_cast<const uint4*>(a.smass + size_t(r) * a.ls);
     const uint4* st = a.sstat + size_t(r) * a.nu;
@@ -230,6 +231,7 @@ __device__ __forceinline__ void load_summary(const SampleArgs& a, int r, Smem sm
             ms += __uint_as_float(v[h].x);
             bd |= v[h].z != 0u;
             km = max(km, v[h].w);
+            if (ukey && i < a.nu) ukey[i] = v[h].w;
         }
     }
     ms = warp_sum(ms);
@@ -872,168 +874,173 @@ FS_COLD __device__ void sample_row_fin(const SampleArgs& a) {
 // ------------------------------------------------------------------ lean top-k-first finish
 
 // The finishing launch of the top-k-first samplers on rows of probabilities, for the
-// usual row: segments of one block (V <= 2^19), and a top-k bound L0 from the
-// histogram of the segment maxima ([explainer] filter order: the k-th largest of any
-// subset of the row, here the segment maxima, is at most the row's own) that leaves
-// at most SMALL live segments (maximum >= L0) and at most SMALL elements >= L0.  Two
-// round trips to L2 in all: (1) the row's summary with its parameters, then the
-// histogram, L0 and the live segments in index order; (2) the live segments' values,
-// and their elements >= L0 written in index order into the candidate list.  Warp 0
-// then finishes in registers exactly as the cluster's leader does: t_k and F_k among
-// the candidates, the rejection rounds ([blog] dual pivot) and the outputs.  Any other
-// row (a bad row index, no top-k filter, fewer segments than k, a larger bound or list)
-// takes the general finishing path, out of line.
+// usual row.  The bound: u_k, the k-th largest of the units' maxima.  The maxima of any
+// subset of the row's elements are a subset of the row, and the k-th largest of a
+// subset is at most the row's own ([explainer] filter order: t_k is the k-th largest
+// value), so u_k <= t_k: every element >= t_k lies in a segment whose maximum is
+// >= u_k.  With one unit per four segments, about k segments qualify.  Steps, with two
+// round trips to L2 after the scan: (1) the row's summary; u_k counted exactly among
+// the unit maxima in shared memory; (2) each warp reloads the live segments (maximum
+// >= u_k) of its own contiguous share of the row, and the elements >= u_k are written
+// in index order into the candidate list; t_k is counted among the candidates by the
+// whole CTA; warp 0 then runs the rejection rounds in registers as the cluster's
+// leader does.  Any other row (a bad row index, no top-k filter, fewer units than k,
+// segments of several blocks, more than LIVE_W live segments in one warp's share or
+// more than SMALL candidates) takes the general finishing path, out of line.
+constexpr int LIVE_W = 16;   // live segments one warp holds in registers
+
 template <bool VEC>
 __global__ void __launch_bounds__(NT, 2) kfirst_kernel(const SampleArgs a) {
     const int b = int(cluster_id_x());
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const Smem sm(a.ns);
-    const int V = a.V, ns = a.ns;
+    const int V = a.V, ns = a.ns, nu = a.nu;
     const KeyProb keyf;
-    grid_dependency_wait();
-    allow_dependents();
+    uint32_t* ukey = reinterpret_cast<uint32_t*>(sm.mass(1));  // [nu] unit maxima
+    // The row index and the parameters are read before the dependency wait: they were
+    // written before the scan of this call started (the scan waits for its own
+    // predecessors before it lets this launch begin), and only the summary comes from
+    // the scan.
     const int r = a.indices ? a.indices[b] : b;
     const bool row_ok = r >= 0 && r < a.batch_in;
-    // ---- (1) parameters, the cleared histogram, the summary
-    for (int i = tid; i < HBINS; i += NT) sm.hist()[i] = 0u;
     if (tid == NT - 32) {
         uint32_t* pr = sm.prm();
         pr[0] = uint32_t(a.top_k ? a.top_k[b] : 0);
         pr[1] = __float_as_uint(a.top_p ? a.top_p[b] : 1.f);
         pr[2] = __float_as_uint(a.min_p ? a.min_p[b] : 0.f);
         *reinterpret_cast<unsigned long long*>(pr + 4) = a.seeds ? a.seeds[b] : a.seed;
-        *reinterpret_cast<unsigned long long*>(pr + 6) =
+    }
+    grid_dependency_wait();
+    allow_dependents();
+    if (tid == NT - 32) {  // a device-resident offset may be advanced by the kernel before
+        *reinterpret_cast<unsigned long long*>(sm.prm() + 6) =
             (a.offsets ? a.offsets[b] : a.offset) + (a.offset_dev ? *a.offset_dev : 0ull);
     }
+    // ---- (1) the summary; u_k
     if (row_ok) {
-        load_summary(a, r, sm, false, warp, lane, tid);  // ends with a block barrier
+        load_summary(a, r, sm, false, warp, lane, tid, ukey);  // ends with a block barrier
     } else {
         __syncthreads();
     }
     const int k = int(sm.prm()[0]);
-    if (!row_ok || !(k > 0 && k < V) || ns < k || a.shift != 0) {
+    if (!row_ok || !(k > 0 && k < V) || nu < k || nu > 2 * NT || a.shift != 0) {
         __syncthreads();
         sample_row_fin<VEC>(a);
         return;
     }
-    // Histogram of the segment maxima (key >> 21): lanes with the same bin add once.
-#pragma unroll 1
-    for (int i0 = 0; i0 < ns; i0 += NT) {
-        const int i = i0 + tid;
-        const uint32_t bin = i < ns ? min(uint32_t(HBINS - 1), sm.segkey()[i] >> 21) : 0xffffffffu;
-        const unsigned grp = __match_any_sync(FULL, bin);
-        if (i < ns && lane == __ffs(grp) - 1) atomicAdd(&sm.hist()[bin], uint32_t(__popc(grp)));
-    }
-    __syncthreads();
-    const uint32_t maxkey = sm.part()[0].u[2];
-    if (warp == 0) {
-        uint32_t above;
-        const int B = scan_bins_down<uint32_t>(sm.hist(), int(min(uint32_t(HBINS - 1), maxkey >> 21)), uint32_t(k),
-                                               lane, above);
-        if (lane == 0) {
-            sm.bcast()[0] = max(B, 0);
-            sm.bcast()[1] = B >= 0 ? int(above + sm.hist()[B]) : INT_BIG;
+    {
+        uint32_t best = 0u;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int i = tid + h * NT;
+            if (i < nu) {
+                const uint32_t mine = ukey[i];
+                int ge = 0;
+#pragma unroll 4
+                for (int j = 0; j < nu; ++j) ge += ukey[j] >= mine;
+                if (ge >= k) best = max(best, mine);
+            }
         }
+        best = warp_max_u(best);
+        if (lane == 0) sm.red()[warp] = int(best);
     }
     __syncthreads();
-    if (sm.bcast()[1] > SMALL) {
-        __syncthreads();
-        sample_row_fin<VEC>(a);
-        return;
-    }
-    const uint32_t L0 = max(1u, uint32_t(sm.bcast()[0]) << 21);
-    // Live segments (maximum >= L0), in index order: each warp lists those of its
-    // contiguous share into list[] from the share's start; then lane w < NW of every
-    // warp holds warp w's count and the inclusive prefix over warps.
+    uint32_t uk = 0u;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) uk = max(uk, uint32_t(sm.red()[w]));
+    uk = max(uk, 1u);  // zeros are never candidates
+    // ---- (2) this warp's live segments (maximum >= u_k), reloaded, in index order
     int r0, r1;
     warp_range(ns, warp, r0, r1);
     int nl = 0;
 #pragma unroll 1
     for (int b0 = r0; b0 < r1; b0 += 32) {
         const int i = b0 + lane;
-        const bool live = i < r1 && sm.segkey()[i] >= L0;
+        const bool live = i < r1 && sm.segkey()[i] >= uk;
         const unsigned bal = __ballot_sync(FULL, live);
-        if (live) sm.list()[r0 + nl + __popc(bal & ((1u << lane) - 1u))] = i;
+        if (live && nl + __popc(bal & ((1u << lane) - 1u)) < LIVE_W)
+            sm.list()[r0 + nl + __popc(bal & ((1u << lane) - 1u))] = i;
         nl += __popc(bal);
     }
-    if (lane == 0) sm.red()[warp] = nl;
-    __syncthreads();
-    const int wn = lane < NW ? sm.red()[lane] : 0;
-    const int wincl = warp_incl_scan_i(wn, lane);
-    int ws0, ws1;
-    warp_range(ns, lane < NW ? lane : 0, ws0, ws1);
-    const int nlive = __shfl_sync(FULL, wincl, NW - 1);
-    // The segment of live entry j (index order).
-    auto live_seg = [&](int j) {
-        const int w = __popc(__ballot_sync(FULL, lane < NW && wincl <= j));
-        const int first = __shfl_sync(FULL, wincl - wn, w);
-        const int start = __shfl_sync(FULL, ws0, w);
-        return sm.list()[start + j - first];
-    };
-    // ---- (2) warp x loads live entries x, x + NW, ... (at most SMALL / NW each) at once.
-    constexpr int PER = SMALL / NW;
-    float4 v[PER];
-    int seg[PER];
+    __syncwarp();
     const float* row = a.probs + size_t(r) * size_t(V);
+    float4 v[LIVE_W];
 #pragma unroll
-    for (int i = 0; i < PER; ++i) {
-        const int j = warp + NW * i;
-        seg[i] = j < nlive ? live_seg(j) : 0;
-        v[i] = j < nlive ? load4<VEC, true>(row, V, seg[i] * BLK + lane * 4, 0.f) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = 0; i < LIVE_W; ++i)
+        v[i] = i < nl ? load4<VEC, true>(row, V, sm.list()[r0 + i] * BLK + lane * 4, 0.f)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+    // Values past V were loaded as 0 and zeros are below u_k >= 1: no index check.
+    auto kept = [&](const float4& x, int q) { return keyf(q_at(x, q)) >= uk; };
+    int cnt = 0;
+#pragma unroll
+    for (int i = 0; i < LIVE_W; ++i) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) cnt += kept(v[i], q);
     }
-    __syncthreads();  // every warp has read the warp counts in red[]
-    // Per live entry: its count of elements >= L0 into red[j].
-    int kc[PER];
-#pragma unroll
-    for (int i = 0; i < PER; ++i) {
-        const int j = warp + NW * i;
-        int c = 0;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) c += keyf(q_at(v[i], q)) >= L0 && seg[i] * BLK + lane * 4 + q < V;
-        kc[i] = c;
-        const int t = warp_sum_i(c);
-        if (j < nlive && lane == 0) sm.red()[j] = t;
+    cnt = warp_sum_i(cnt);
+    __syncthreads();  // every warp is done with red[] (u_k)
+    if (lane == 0) {
+        sm.red()[warp] = cnt;
+        sm.red()[NW + warp] = nl > LIVE_W ? 1 : 0;
     }
     __syncthreads();
-    // Exclusive prefix of the entries' counts (lane l holds entries 4l .. 4l + 3).
-    int cnt4[4], own = 0;
+    int base = 0, n = 0, over = 0;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        cnt4[q] = 4 * lane + q < nlive ? sm.red()[4 * lane + q] : 0;
-        own += cnt4[q];
+    for (int w = 0; w < NW; ++w) {
+        const int c = sm.red()[w];
+        base += w < warp ? c : 0;
+        n += c;
+        over |= sm.red()[NW + w];
     }
-    const int incl = warp_incl_scan_i(own, lane);
-    const int n = __shfl_sync(FULL, incl, 31);
-    if (n > SMALL) {
+    if (over || n > SMALL) {
         __syncthreads();
         sample_row_fin<VEC>(a);
         return;
     }
+    const unsigned lt = (1u << lane) - 1u;
 #pragma unroll
-    for (int i = 0; i < PER; ++i) {
-        const int j = warp + NW * i;
-        if (j < nlive) {
-            // offset of entry j: counts of the entries before it
-            const int lj = j >> 2, qj = j & 3;
-            int before = __shfl_sync(FULL, incl - own, lj);
+    for (int i = 0; i < LIVE_W; ++i) {
+        if (i < nl) {
+            const int e0 = sm.list()[r0 + i] * BLK + lane * 4;
+            unsigned m[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) before += q < qj ? __shfl_sync(FULL, cnt4[q], lj) : 0;
-            int p = before + warp_incl_scan_i(kc[i], lane) - kc[i];
+            for (int q = 0; q < 4; ++q) m[q] = __ballot_sync(FULL, kept(v[i], q));
+            int p = base;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) p += __popc(m[q] & lt);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const float x = q_at(v[i], q);
-                const int ix = seg[i] * BLK + lane * 4 + q;
-                if (keyf(x) >= L0 && ix < V) {
-                    sm.lv()[p] = x;
-                    sm.li()[p] = ix;
+                if ((m[q] >> lane) & 1u) {
+                    sm.lv()[p] = q_at(v[i], q);
+                    sm.li()[p] = e0 + q;
                     ++p;
                 }
             }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) base += __popc(m[q]);
         }
     }
     __syncthreads();
+    // t_k: the largest candidate key with at least k candidate keys at or above it (0
+    // when there are fewer than k candidates: the row has fewer than k positives).
+    {
+        uint32_t best = 0u;
+        if (tid < n) {
+            const uint32_t mine = keyf(sm.lv()[tid]);
+            int ge = 0;
+#pragma unroll 4
+            for (int j = 0; j < n; ++j) ge += keyf(sm.lv()[j]) >= mine;
+            if (ge >= k) best = mine;
+        }
+        best = warp_max_u(best);
+        if (lane == 0) sm.red()[2 * NW + warp] = int(best);
+    }
+    __syncthreads();
     if (warp != 0) return;
-    // ---- warp 0: t_k, F_k, the rounds, the outputs (as the cluster's leader)
+    uint32_t tk = 0u;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) tk = max(tk, uint32_t(sm.red()[2 * NW + w]));
+    // ---- warp 0: F_k, the rounds, the outputs (as the cluster's leader)
     const float tp = __uint_as_float(sm.prm()[1]);
     const float mp = __uint_as_float(sm.prm()[2]);
     const unsigned long long seed_b = *reinterpret_cast<const unsigned long long*>(sm.prm() + 4);
@@ -1041,7 +1048,7 @@ __global__ void __launch_bounds__(NT, 2) kfirst_kernel(const SampleArgs a) {
     const uint32_t stream_b = a.seeds ? 0u : uint32_t(b);
     const float M = sm.part()[0].f[0];
     const bool any_bad = sm.part()[0].u[1] != 0u;
-    const float rowmax = __uint_as_float(maxkey);
+    const float rowmax = __uint_as_float(sm.part()[0].u[2]);
     Pred f;
     f.single = a.single_pivot != 0;
     f.k_on = true;
@@ -1059,24 +1066,20 @@ __global__ void __launch_bounds__(NT, 2) kfirst_kernel(const SampleArgs a) {
     if (valid) {
         Small sl;
         sl.n = n;
+        bool kp[SR];
+        float fk = 0.f;
 #pragma unroll
         for (int q = 0; q < SR; ++q) {
             const int e = SR * lane + q;
             sl.in[q] = e < n;
             sl.x[q] = sl.in[q] ? sm.lv()[e] : 0.f;
             sl.i[q] = sl.in[q] ? sm.li()[e] : 0;
-        }
-        const uint32_t tk = small_kth(sl, k, keyf);
-        bool kept[SR];
-        float fk = 0.f;
-#pragma unroll
-        for (int q = 0; q < SR; ++q) {
-            kept[q] = sl.in[q] && keyf(sl.x[q]) >= tk;
-            fk += kept[q] ? sl.x[q] : 0.f;
+            kp[q] = sl.in[q] && keyf(sl.x[q]) >= tk;
+            fk += kp[q] ? sl.x[q] : 0.f;
         }
         const float Fk = warp_sum(fk);
         f.pthr = tp * Fk;  // top-p inside the k, measured against F_k
-        token = small_rounds(sl, kept, f, Fk, rowmax, seed_b, offset_b, stream_b, lane, rounds);
+        token = small_rounds(sl, kp, f, Fk, rowmax, seed_b, offset_b, stream_b, lane, rounds);
     }
     if (lane == 0) {
         a.out_token[b] = token >= 0 ? token : -1;
