@@ -929,18 +929,27 @@ __global__ void __launch_bounds__(NT, 2) kfirst_kernel(const SampleArgs a) {
         return;
     }
     {
-        uint32_t best = 0u;
+        // Thread t counts, for units t and t + NT, the unit maxima at or above its own
+        // (16-byte broadcast reads, 32 keys per step; the keys past nu are zeros).
+        const int nu4 = (nu + 3) >> 2;
+        if (tid < 4 * nu4 - nu) ukey[nu + tid] = 0u;
+        __syncthreads();
+        const uint4* u4 = reinterpret_cast<const uint4*>(ukey);
+        const uint32_t m0 = tid < nu ? ukey[tid] : 0xffffffffu;
+        const uint32_t m1 = tid + NT < nu ? ukey[tid + NT] : 0xffffffffu;
+        int g0 = 0, g1 = 0;
+#pragma unroll 1
+        for (int j = 0; j < nu4; j += 8) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int i = tid + h * NT;
-            if (i < nu) {
-                const uint32_t mine = ukey[i];
-                int ge = 0;
-#pragma unroll 4
-                for (int j = 0; j < nu; ++j) ge += ukey[j] >= mine;
-                if (ge >= k) best = max(best, mine);
+            for (int t = 0; t < 8; ++t) {
+                const uint4 w = j + t < nu4 ? u4[j + t] : make_uint4(0u, 0u, 0u, 0u);
+                g0 += (w.x >= m0) + (w.y >= m0) + (w.z >= m0) + (w.w >= m0);
+                g1 += (w.x >= m1) + (w.y >= m1) + (w.z >= m1) + (w.w >= m1);
             }
         }
+        uint32_t best = 0u;
+        if (tid < nu && g0 >= k) best = m0;
+        if (tid + NT < nu && g1 >= k) best = max(best, m1);
         best = warp_max_u(best);
         if (lane == 0) sm.red()[warp] = int(best);
     }
@@ -1024,14 +1033,20 @@ __global__ void __launch_bounds__(NT, 2) kfirst_kernel(const SampleArgs a) {
     // t_k: the largest candidate key with at least k candidate keys at or above it (0
     // when there are fewer than k candidates: the row has fewer than k positives).
     {
-        uint32_t best = 0u;
-        if (tid < n) {
-            const uint32_t mine = keyf(sm.lv()[tid]);
-            int ge = 0;
-#pragma unroll 4
-            for (int j = 0; j < n; ++j) ge += keyf(sm.lv()[j]) >= mine;
-            if (ge >= k) best = mine;
+        // Thread t < n counts the candidates at or above candidate t (16-byte broadcast
+        // reads; candidate values are positive, so their order is that of the bits).
+        const uint4* c4 = reinterpret_cast<const uint4*>(sm.lv());
+        const uint32_t mine = tid < n ? __float_as_uint(sm.lv()[tid]) : 0xffffffffu;
+        int ge = 0;
+#pragma unroll
+        for (int t = 0; t < SMALL / 4; ++t) {
+            if (4 * t < n) {
+                const uint4 w = c4[t];
+                ge += (w.x >= mine && 4 * t + 0 < n) + (w.y >= mine && 4 * t + 1 < n) +
+                      (w.z >= mine && 4 * t + 2 < n) + (w.w >= mine && 4 * t + 3 < n);
+            }
         }
+        uint32_t best = (tid < n && ge >= k) ? mine : 0u;
         best = warp_max_u(best);
         if (lane == 0) sm.red()[2 * NW + warp] = int(best);
     }
@@ -1091,7 +1106,7 @@ __global__ void __launch_bounds__(NT, 2) kfirst_kernel(const SampleArgs a) {
 // ------------------------------------------------------------------ host side
 
 #ifndef FS_SCAN_PER_SM
-#define FS_SCAN_PER_SM 3   // scan CTAs per SM
+#define FS_SCAN_PER_SM 4   // scan CTAs per SM (the occupancy of scan_kernel: every SM gets as many)
 #endif
 
 // Grid of the scan: one wave of FS_SCAN_PER_SM CTAs per SM, fewer when the matrix has
