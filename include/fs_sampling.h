@@ -94,6 +94,7 @@ typedef enum fs_order {
 
 #define FS_MAX_VOCAB 2097152   /* largest supported vocab */
 #define FS_MAX_ROUNDS 256      /* rejection rounds before a row is reported invalid */
+#define FS_NOALLOC_SCRATCH_BYTES (8u << 20)  /* fixed scratch of fs_top_k_top_p_sampling_noalloc */
 
 /* Plain categorical sampling: one draw by inverse transform over the whole row.
  * [blog] "inverse transform sampling": u ~ U[0,1), the token k with
@@ -305,6 +306,36 @@ fs_status fs_workspace_bytes(int32_t batch_in, int32_t vocab, size_t* bytes);
  * of `batch_in` rows of `vocab` values, allocating (cudaMalloc) now if it does not.
  * Host-side; launches nothing.  FS_ERR_CUDA if the allocation fails. */
 fs_status fs_workspace_reserve(int32_t batch_in, int32_t vocab, void* stream);
+
+/* fs_top_k_top_p_sampling without any allocation (the pages have no counterpart: this
+ * is a deployment variant).  Some callers cannot let a library call cudaMalloc: a
+ * serving engine that reserves nearly all of device memory for its KV cache up front
+ * and fails or fragments on a later allocation; code that runs under a memory pool
+ * or allocator that must see every device allocation; a process that must not risk
+ * the device-wide synchronisation an allocation can cause in the middle of a decode
+ * step.  This entry takes the same arguments and gives the same results as
+ * fs_top_k_top_p_sampling, but the top-k-first order keeps its row summaries in one
+ * fixed array of FS_NOALLOC_SCRATCH_BYTES (8 MiB) that is part of the library's
+ * module image: every device that loads the library holds it until the process exits,
+ * and no call allocates or frees anything (the joint order needs no scratch at all).
+ *  - Limit: fs_workspace_bytes(batch_in, vocab) must be at most
+ *    FS_NOALLOC_SCRATCH_BYTES (for example 64 rows of 151936 values take 0.9 MB, 256
+ *    rows of 256000 values 6.1 MB); larger batches return FS_ERR_UNSUPPORTED and
+ *    fs_last_error_string() says why.
+ *  - Set-up: the first call on a device looks the array's device address up
+ *    (cudaGetSymbolAddress, which may load the module); make that first call before
+ *    any stream capture.
+ *  - Sharing: every call on every stream of a device uses the same array, and it keeps
+ *    the last call's contents.  Nothing in it needs to start at zero (each call writes
+ *    every word it later reads), but calls whose work overlaps on the GPU (other
+ *    streams, or graph replays running at the same time) race on it: order them. */
+fs_status fs_top_k_top_p_sampling_noalloc(const float* probs, int32_t batch_in, int32_t vocab,
+                                          const int32_t* indices, int32_t batch_out,
+                                          const int32_t* top_k, const float* top_p,
+                                          const float* min_p, int32_t order,
+                                          uint64_t seed, uint64_t offset,
+                                          int32_t* out_token, uint8_t* out_valid,
+                                          int32_t* out_rounds, void* stream);
 
 /* Free every scratch buffer of the library on every device.  Only when no call of
  * this library is in flight on any stream (and no captured graph that uses one will

@@ -15,6 +15,8 @@ namespace fsd {
 
 static thread_local char g_last_error[256] = "";
 
+void set_last_error(const char* msg) { std::snprintf(g_last_error, sizeof(g_last_error), "%s", msg); }
+
 fs_status cuda_fail(cudaError_t e) {
     std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
     return FS_ERR_CUDA;

@@ -22,6 +22,9 @@ struct Plan {
 // Remember a CUDA error for fs_last_error_string() and turn it into a status.
 fs_status cuda_fail(cudaError_t e);
 
+// Set the text fs_last_error_string() returns to the calling host thread.
+void set_last_error(const char* msg);
+
 // Number of SMs and the opt-in shared-memory limit of the current device.
 fs_status device_limits(int& sm_count, size_t& smem_optin);
 

@@ -22,6 +22,8 @@
 // keeps logit keys and, where draws over the whole row need them, each segment's mass
 // relative to its own largest logit (an online softmax); after the first barrier the
 // row's maximum m is known and every later read sees the weights exp((z - m) / T).
+#include <mutex>
+
 #include "fs_device.cuh"
 #include "fs_host.h"
 
@@ -1160,7 +1162,7 @@ static fs_status launch_scan_finish(const float* probs, int32_t batch_in, int32_
                                     int32_t order, uint64_t seed, uint64_t offset, int32_t* out_token,
                                     uint8_t* out_valid, int32_t* out_rounds, void* stream, const uint64_t* seeds,
                                     const uint64_t* offsets, const uint64_t* offset_dev, int32_t pivots, bool soft,
-                                    const float* temperature, bool vec) {
+                                    const float* temperature, bool vec, void* fixed_ws = nullptr) {
     const bool kfirst = order == FS_ORDER_TOP_K_FIRST && top_k;
     auto fin_fn = [&]() -> void (*)(SampleArgs) {
         if (soft) return vec ? sample_kernel<true, true, true> : sample_kernel<false, true, true>;
@@ -1185,8 +1187,12 @@ static fs_status launch_scan_finish(const float* probs, int32_t batch_in, int32_
     void* ws = nullptr;
     // Top-k-first launches draw from gathered candidates: no segment masses needed.
     if (batch_in > 0) {
-        st = workspace(scan_workspace_bytes(batch_in, vocab), stream, &ws);
-        if (st != FS_OK) return st;
+        if (fixed_ws) {
+            ws = fixed_ws;  // caller-checked to hold the summaries
+        } else {
+            st = workspace(scan_workspace_bytes(batch_in, vocab), stream, &ws);
+            if (st != FS_OK) return st;
+        }
         if (soft)
             st = launch_scan<SCAN_LOGITS>(probs, batch_in, vocab, p.shift, p.ns, vec, ws, stream);
         else if (kfirst)
@@ -1233,7 +1239,8 @@ static fs_status launch_sample(const float* probs, int32_t batch_in, int32_t voc
                                int32_t order, uint64_t seed, uint64_t offset, int32_t* out_token, uint8_t* out_valid,
                                int32_t* out_rounds, void* stream, const uint64_t* seeds = nullptr,
                                const uint64_t* offsets = nullptr, const uint64_t* offset_dev = nullptr,
-                               int32_t pivots = 2, bool soft = false, const float* temperature = nullptr) {
+                               int32_t pivots = 2, bool soft = false, const float* temperature = nullptr,
+                               void* fixed_ws = nullptr) {
     if (batch_out < 0 || batch_in < 0) return FS_ERR_INVALID_ARG;
     if (batch_out == 0) return FS_OK;
     if (!probs || !out_token || !out_valid) return FS_ERR_INVALID_ARG;
@@ -1252,7 +1259,7 @@ static fs_status launch_sample(const float* probs, int32_t batch_in, int32_t voc
     const bool fin = (order == FS_ORDER_TOP_K_FIRST && top_k) || (!soft && !top_k && !top_p && !min_p);
     if (fin) return launch_scan_finish(probs, batch_in, vocab, indices, batch_out, top_k, top_p, min_p, order, seed,
                                        offset, out_token, out_valid, out_rounds, stream, seeds, offsets, offset_dev,
-                                       pivots, soft, temperature, vec);
+                                       pivots, soft, temperature, vec, fixed_ws);
     const void* fn = soft ? (vec ? reinterpret_cast<const void*>(sample_kernel<true, true, false>)
                                  : reinterpret_cast<const void*>(sample_kernel<false, true, false>))
                           : (vec ? reinterpret_cast<const void*>(sample_kernel<true, false, false>)
@@ -1288,6 +1295,34 @@ static fs_status launch_sample(const float* probs, int32_t batch_in, int32_t voc
     }
     if (vec) return launch_cluster(sample_kernel<true, false, false>, p, batch_out, stream, a);
     return launch_cluster(sample_kernel<false, false, false>, p, batch_out, stream, a);
+}
+
+// ------------------------------------------------------------------ scratch without allocation
+//
+// For callers that may not allocate device memory: fs_top_k_top_p_sampling_noalloc keeps
+// the row summaries of its scan in this fixed array instead of the per-stream buffers.
+// It is part of the module image, so every device that loads the library holds it until
+// the process exits.  Host code cannot pass the array's name to a kernel (on the host
+// it names a stand-in, not device memory): its device address is looked up once per
+// device with cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[FS_NOALLOC_SCRATCH_BYTES];
+
+static fs_status noalloc_scratch(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= 64) return FS_ERR_UNSUPPORTED;
+    static std::mutex mu;
+    static void* addr[64] = {nullptr};
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e);
+        addr[dev] = p;
+    }
+    *out = addr[dev];
+    return FS_OK;
 }
 
 __global__ void advance_kernel(unsigned long long* offset_dev, unsigned long long delta) {
@@ -1337,6 +1372,29 @@ fs_status fs_top_k_top_p_sampling(const float* probs, int32_t batch_in, int32_t 
     if ((!top_k || !top_p) && batch_out > 0) return FS_ERR_INVALID_ARG;
     return fsd::launch_sample(probs, batch_in, vocab, indices, batch_out, top_k, top_p, min_p, order, seed, offset,
                               out_token, out_valid, out_rounds, stream);
+}
+
+fs_status fs_top_k_top_p_sampling_noalloc(const float* probs, int32_t batch_in, int32_t vocab,
+                                          const int32_t* indices, int32_t batch_out, const int32_t* top_k,
+                                          const float* top_p, const float* min_p, int32_t order, uint64_t seed,
+                                          uint64_t offset, int32_t* out_token, uint8_t* out_valid,
+                                          int32_t* out_rounds, void* stream) {
+    if ((!top_k || !top_p) && batch_out > 0) return FS_ERR_INVALID_ARG;
+    void* scratch = nullptr;
+    if (order == FS_ORDER_TOP_K_FIRST && batch_out > 0 && batch_in > 0 && vocab >= 1 && vocab <= FS_MAX_VOCAB) {
+        const size_t need = fsd::scan_workspace_bytes(batch_in, vocab);
+        if (need > size_t(FS_NOALLOC_SCRATCH_BYTES)) {
+            fsd::set_last_error("fs_top_k_top_p_sampling_noalloc: the row summaries of this batch need more than "
+                                "FS_NOALLOC_SCRATCH_BYTES of fixed scratch (see fs_workspace_bytes)");
+            return FS_ERR_UNSUPPORTED;
+        }
+        const fs_status st = fsd::noalloc_scratch(&scratch);
+        if (st != FS_OK) return st;
+    }
+    // The joint order runs on clusters and needs no scratch; nothing allocates either way.
+    return fsd::launch_sample(probs, batch_in, vocab, indices, batch_out, top_k, top_p, min_p, order, seed, offset,
+                              out_token, out_valid, out_rounds, stream, nullptr, nullptr, nullptr, 2, false, nullptr,
+                              scratch);
 }
 
 fs_status fs_top_k_top_p_sampling_rng(const float* probs, int32_t batch_in, int32_t vocab, const int32_t* indices,
