@@ -191,14 +191,15 @@ __global__ void __launch_bounds__(NT, 4) scan_kernel(const ScanArgs a) {
 // FIN: the summary of input row r into this CTA's tables, as pass 1 and pass1_totals
 // leave them in a one-CTA cluster: segment keys (and, with `masses`, segment masses)
 // and part[0] = (M; V as the bound of the positive count, bad flag, largest key), and
-// with `ukey` each unit's largest key in ukey[0, nu).  M
+// with `uhist` the histogram of the units' largest keys (key >> 21) added into uhist,
+// which the caller cleared (a block barrier orders the clear before the counts).  M
 // is the sum of the unit masses in a fixed order (thread t adds units t, t + NT, ...
 // in turn, then a tree over the lanes and the warps in order).  Every thread issues
 // all of its loads before it uses any (one round trip to L2).  The summary was
 // written by the previous launch, so it is read through L2 (ld.global.cg).
 // Block-collective; ends with a block barrier.
 __device__ __forceinline__ void load_summary(const SampleArgs& a, int r, Smem sm, bool masses, int warp, int lane,
-                                             int tid, uint32_t* ukey = nullptr) {
+                                             int tid, uint32_t* uhist = nullptr) {
     const uint4* key4 = reinterpret_cast<const uint4*>(a.skey + size_t(r) * a.ls);
     const uint4* mass4 = reinterpret_cast<const uint4*>(a.smass + size_t(r) * a.ls);
     const uint4* st = a.sstat + size_t(r) * a.nu;
@@ -216,6 +217,7 @@ __device__ __forceinline__ void load_summary(const SampleArgs& a, int r, Smem sm
             m[h] = (masses && i < n4) ? __ldcg(mass4 + i) : make_uint4(0u, 0u, 0u, 0u);
             v[h] = i < a.nu ? __ldcg(st + i) : make_uint4(0u, 0u, 0u, 0u);
         }
+        if (uhist && i0 == 0) __syncthreads();  // the caller's clear of uhist, before any count
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int i = i0 + h * NT + tid;
@@ -233,7 +235,7 @@ __device__ __forceinline__ void load_summary(const SampleArgs& a, int r, Smem sm
             ms += __uint_as_float(v[h].x);
             bd |= v[h].z != 0u;
             km = max(km, v[h].w);
-            if (ukey && i < a.nu) ukey[i] = v[h].w;
+            if (uhist && i < a.nu) atomicAdd(&uhist[min(uint32_t(HBINS - 1), v[h].w >> 21)], 1u);
         }
     }
     ms = warp_sum(ms);
@@ -876,17 +878,17 @@ FS_COLD __device__ void sample_row_fin(const SampleArgs& a) {
 // ------------------------------------------------------------------ lean top-k-first finish
 
 // The finishing launch of the top-k-first samplers on rows of probabilities, for the
-// usual row.  The bound: u_k, the k-th largest of the units' maxima.  The maxima of any
-// subset of the row's elements are a subset of the row, and the k-th largest of a
-// subset is at most the row's own ([explainer] filter order: t_k is the k-th largest
-// value), so u_k <= t_k: every element >= t_k lies in a segment whose maximum is
-// >= u_k.  With one unit per four segments, about k segments qualify.  Steps, with two
-// round trips to L2 after the scan: (1) the row's summary; u_k counted exactly among
-// the unit maxima in shared memory; (2) each warp reloads the live segments (maximum
-// >= u_k) of its own contiguous share of the row, and the elements >= u_k are written
-// in index order into the candidate list; t_k is counted among the candidates by the
-// whole CTA; warp 0 then runs the rejection rounds in registers as the cluster's
-// leader does.  Any other row (a bad row index, no top-k filter, fewer units than k,
+// usual row.  The bound uk: the lower edge of the histogram bin (key >> 21, a quarter
+// binade) that holds the k-th largest of the units' maxima.  The units' maxima are a
+// subset of the row, and the k-th largest of a subset is at most the row's own
+// ([explainer] filter order: t_k is the k-th largest value), so uk <= t_k: every
+// element >= t_k lies in a segment whose maximum is >= uk.  Steps, with two round
+// trips to L2 after the scan: (1) the row's summary, the histogram of its unit maxima
+// counted as it is unpacked, uk; (2) each warp reloads the live segments (maximum
+// >= uk) of its own contiguous share of the row, and the elements >= uk are written in
+// index order into the candidate list; t_k is counted among the candidates by the
+// warps that hold them; warp 0 then runs the rejection rounds in registers as the
+// cluster's leader does.  Any other row (a bad row index, no top-k filter, fewer units than k,
 // segments of several blocks, more than LIVE_W live segments in one warp's share or
 // more than SMALL candidates) takes the general finishing path, out of line.
 constexpr int LIVE_W = 16;   // live segments one warp holds in registers
@@ -898,7 +900,6 @@ __global__ void __launch_bounds__(NT, 2) kfirst_kernel(const SampleArgs a) {
     const Smem sm(a.ns);
     const int V = a.V, ns = a.ns, nu = a.nu;
     const KeyProb keyf;
-    uint32_t* ukey = reinterpret_cast<uint32_t*>(sm.mass(1));  // [nu] unit maxima
     // The row index and the parameters are read before the dependency wait: they were
     // written before the scan of this call started (the scan waits for its own
     // predecessors before it lets this launch begin), and only the summary comes from
@@ -912,54 +913,35 @@ __global__ void __launch_bounds__(NT, 2) kfirst_kernel(const SampleArgs a) {
         pr[2] = __float_as_uint(a.min_p ? a.min_p[b] : 0.f);
         *reinterpret_cast<unsigned long long*>(pr + 4) = a.seeds ? a.seeds[b] : a.seed;
     }
+    for (int i = tid; i < HBINS; i += NT) sm.hist()[i] = 0u;
     grid_dependency_wait();
     allow_dependents();
     if (tid == NT - 32) {  // a device-resident offset may be advanced by the kernel before
         *reinterpret_cast<unsigned long long*>(sm.prm() + 6) =
             (a.offsets ? a.offsets[b] : a.offset) + (a.offset_dev ? *a.offset_dev : 0ull);
     }
-    // ---- (1) the summary; u_k
+    // ---- (1) the summary, with the histogram of the unit maxima; the bound
     if (row_ok) {
-        load_summary(a, r, sm, false, warp, lane, tid, ukey);  // ends with a block barrier
+        load_summary(a, r, sm, false, warp, lane, tid, sm.hist());  // ends with a block barrier
     } else {
         __syncthreads();
     }
     const int k = int(sm.prm()[0]);
-    if (!row_ok || !(k > 0 && k < V) || nu < k || nu > 2 * NT || a.shift != 0) {
+    if (!row_ok || !(k > 0 && k < V) || nu < k || a.shift != 0) {
         __syncthreads();
         sample_row_fin<VEC>(a);
         return;
     }
-    {
-        // Thread t counts, for units t and t + NT, the unit maxima at or above its own
-        // (16-byte broadcast reads, 32 keys per step; the keys past nu are zeros).
-        const int nu4 = (nu + 3) >> 2;
-        if (tid < 4 * nu4 - nu) ukey[nu + tid] = 0u;
-        __syncthreads();
-        const uint4* u4 = reinterpret_cast<const uint4*>(ukey);
-        const uint32_t m0 = tid < nu ? ukey[tid] : 0xffffffffu;
-        const uint32_t m1 = tid + NT < nu ? ukey[tid + NT] : 0xffffffffu;
-        int g0 = 0, g1 = 0;
-#pragma unroll 1
-        for (int j = 0; j < nu4; j += 8) {
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                const uint4 w = j + t < nu4 ? u4[j + t] : make_uint4(0u, 0u, 0u, 0u);
-                g0 += (w.x >= m0) + (w.y >= m0) + (w.z >= m0) + (w.w >= m0);
-                g1 += (w.x >= m1) + (w.y >= m1) + (w.z >= m1) + (w.w >= m1);
-            }
-        }
-        uint32_t best = 0u;
-        if (tid < nu && g0 >= k) best = m0;
-        if (tid + NT < nu && g1 >= k) best = max(best, m1);
-        best = warp_max_u(best);
-        if (lane == 0) sm.red()[warp] = int(best);
+    if (warp == 0) {
+        // The bin holding the k-th largest unit maximum, from the top: its lower edge is
+        // at most that maximum, hence at most t_k.
+        uint32_t above;
+        const int B = scan_bins_down<uint32_t>(sm.hist(), int(min(uint32_t(HBINS - 1), sm.part()[0].u[2] >> 21)),
+                                               uint32_t(k), lane, above);
+        if (lane == 0) sm.bcast()[0] = max(B, 0);
     }
     __syncthreads();
-    uint32_t uk = 0u;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) uk = max(uk, uint32_t(sm.red()[w]));
-    uk = max(uk, 1u);  // zeros are never candidates
+    const uint32_t uk = max(1u, uint32_t(sm.bcast()[0]) << 21);  // zeros are never candidates
     // ---- (2) this warp's live segments (maximum >= u_k), reloaded, in index order
     int r0, r1;
     warp_range(ns, warp, r0, r1);
@@ -1037,19 +1019,24 @@ __global__ void __launch_bounds__(NT, 2) kfirst_kernel(const SampleArgs a) {
     {
         // Thread t < n counts the candidates at or above candidate t (16-byte broadcast
         // reads; candidate values are positive, so their order is that of the bits).
-        const uint4* c4 = reinterpret_cast<const uint4*>(sm.lv());
-        const uint32_t mine = tid < n ? __float_as_uint(sm.lv()[tid]) : 0xffffffffu;
-        int ge = 0;
+        uint32_t best = 0u;
+        if (warp * 32 < n) {  // the warps holding candidates
+            const uint4* c4 = reinterpret_cast<const uint4*>(sm.lv());
+            const uint32_t mine = tid < n ? __float_as_uint(sm.lv()[tid]) : 0xffffffffu;
+            int ge = 0;
+#pragma unroll 1
+            for (int t = 0; 4 * t < n; t += 4) {
 #pragma unroll
-        for (int t = 0; t < SMALL / 4; ++t) {
-            if (4 * t < n) {
-                const uint4 w = c4[t];
-                ge += (w.x >= mine && 4 * t + 0 < n) + (w.y >= mine && 4 * t + 1 < n) +
-                      (w.z >= mine && 4 * t + 2 < n) + (w.w >= mine && 4 * t + 3 < n);
+                for (int c = 0; c < 4; ++c) {
+                    const uint4 w = c4[t + c];  // SMALL entries are always in the list's storage
+                    const int e = 4 * (t + c);
+                    ge += (w.x >= mine && e < n) + (w.y >= mine && e + 1 < n) + (w.z >= mine && e + 2 < n) +
+                          (w.w >= mine && e + 3 < n);
+                }
             }
+            best = (tid < n && ge >= k) ? mine : 0u;
+            best = warp_max_u(best);
         }
-        uint32_t best = (tid < n && ge >= k) ? mine : 0u;
-        best = warp_max_u(best);
         if (lane == 0) sm.red()[2 * NW + warp] = int(best);
     }
     __syncthreads();
