@@ -271,12 +271,16 @@ fs_status fs_chain_speculative_sampling(const float* draft_probs, const int32_t*
 /* The launch plan of the sampling kernels for `batch_out` rows of `vocab` elements on
  * the current device.  order = FS_ORDER_TOP_K_FIRST gives the plan of the
  * top-k-first entries (fs_top_k_top_p_sampling*, order top-k-first) and of
- * fs_sampling_from_probs, which stream each row about once; FS_ORDER_JOINT that of
- * the joint order and of fs_top_k_sampling, fs_top_p_sampling and fs_min_p_sampling,
- * whose rejection rounds pass over the row several times.  Outputs (host pointers):
- * CTAs per row (*cluster), elements per segment, segments per CTA and the most CTAs
- * resident on one SM (*ctas_per_sm; below the occupancy limit when the plan caps it
- * through its shared-memory request).  Host only; nothing is launched.
+ * fs_sampling_from_probs: a scan of every row with *ctas_per_sm CTAs on every SM,
+ * then one CTA per row (*cluster = 1) that finishes the row from its summary
+ * (*segments_per_cta = the row's segments).  FS_ORDER_JOINT gives that of the joint
+ * order and of fs_top_k_sampling, fs_top_p_sampling and fs_min_p_sampling, whose
+ * rejection rounds pass over the row several times on a cluster of CTAs, for rows of
+ * probabilities that are 16-byte aligned with vocab % 4 = 0 (other rows run a
+ * scalar-load build of the same kernel).  Outputs (host pointers): CTAs per row
+ * (*cluster), elements per segment, segments per CTA and the most CTAs resident on
+ * one SM (*ctas_per_sm; below the occupancy limit when the plan caps it through its
+ * shared-memory request).  Host only; nothing is launched.
  * FS_ERR_INVALID_ARG: batch_out or vocab < 1, a null output, an unknown order. */
 fs_status fs_sampling_plan(int32_t batch_out, int32_t vocab, int32_t order, int32_t* cluster,
                            int32_t* segment_len, int32_t* segments_per_cta, int32_t* ctas_per_sm);

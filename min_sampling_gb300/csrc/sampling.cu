@@ -891,7 +891,13 @@ FS_COLD __device__ void sample_row_fin(const SampleArgs& a) {
 // cluster's leader does.  Any other row (a bad row index, no top-k filter, fewer units than k,
 // segments of several blocks, more than LIVE_W live segments in one warp's share or
 // more than SMALL candidates) takes the general finishing path, out of line.
-constexpr int LIVE_W = 16;   // live segments one warp holds in registers
+constexpr int LIVE_W = 16;   // live segments one warp stages in shared memory
+
+// Per-warp staging areas of the lean finish (NW x LIVE_W blocks), after the carve-up.
+__host__ __device__ inline size_t kfirst_smem(int ns) { return Layout(ns).total() + size_t(NW) * LIVE_W * BLK * 4; }
+__device__ __forceinline__ float* kfirst_stage(Smem sm) {
+    return reinterpret_cast<float*>(smem_raw + Layout(sm.ns).total());
+}
 
 template <bool VEC>
 __global__ void __launch_bounds__(NT, 2) kfirst_kernel(const SampleArgs a) {
@@ -942,43 +948,48 @@ __global__ void __launch_bounds__(NT, 2) kfirst_kernel(const SampleArgs a) {
     }
     __syncthreads();
     const uint32_t uk = max(1u, uint32_t(sm.bcast()[0]) << 21);  // zeros are never candidates
-    // ---- (2) this warp's live segments (maximum >= u_k), reloaded, in index order
+    // ---- (2) this warp's live segments (maximum >= uk) of its contiguous share, copied
+    // into its staging area as they are found (cp.async, one 512-byte block each), then
+    // counted and placed from shared memory.  Every loop here is rolled: this code runs
+    // once per launch, and straight-line code would be fetched line by line.
     int r0, r1;
     warp_range(ns, warp, r0, r1);
+    const float* row = a.probs + size_t(r) * size_t(V);
+    float* stg = kfirst_stage(sm) + warp * (LIVE_W * BLK);
     int nl = 0;
 #pragma unroll 1
     for (int b0 = r0; b0 < r1; b0 += 32) {
         const int i = b0 + lane;
-        const bool live = i < r1 && sm.segkey()[i] >= uk;
-        const unsigned bal = __ballot_sync(FULL, live);
-        if (live && nl + __popc(bal & ((1u << lane) - 1u)) < LIVE_W)
-            sm.list()[r0 + nl + __popc(bal & ((1u << lane) - 1u))] = i;
-        nl += __popc(bal);
+        unsigned bal = __ballot_sync(FULL, i < r1 && sm.segkey()[i] >= uk);
+#pragma unroll 1
+        while (bal) {
+            const int sg = b0 + __ffs(bal) - 1;
+            bal &= bal - 1u;
+            if (nl < LIVE_W) {
+                stage4<VEC>(stg + nl * BLK + lane * 4, row, V, sg * BLK + lane * 4);
+                if (lane == 0) sm.list()[r0 + nl] = sg;
+            }
+            ++nl;
+        }
     }
-    __syncwarp();
-    const float* row = a.probs + size_t(r) * size_t(V);
-    float4 v[LIVE_W];
-#pragma unroll
-    for (int i = 0; i < LIVE_W; ++i)
-        v[i] = i < nl ? load4<VEC, true>(row, V, sm.list()[r0 + i] * BLK + lane * 4, 0.f)
-                      : make_float4(0.f, 0.f, 0.f, 0.f);
-    // Values past V were loaded as 0 and zeros are below u_k >= 1: no index check.
-    auto kept = [&](const float4& x, int q) { return keyf(q_at(x, q)) >= uk; };
+    cp_async_commit();
+    cp_async_wait<0>();  // each lane reads back the words it copied (zeros past V)
+    const int nb = min(nl, LIVE_W);
     int cnt = 0;
-#pragma unroll
-    for (int i = 0; i < LIVE_W; ++i) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) cnt += kept(v[i], q);
+#pragma unroll 1
+    for (int i = 0; i < nb; ++i) {
+        const float4 x = *reinterpret_cast<const float4*>(stg + i * BLK + lane * 4);
+        cnt += (keyf(x.x) >= uk) + (keyf(x.y) >= uk) + (keyf(x.z) >= uk) + (keyf(x.w) >= uk);
     }
     cnt = warp_sum_i(cnt);
-    __syncthreads();  // every warp is done with red[] (u_k)
+    __syncthreads();  // every warp is done with red[] (the bound)
     if (lane == 0) {
         sm.red()[warp] = cnt;
         sm.red()[NW + warp] = nl > LIVE_W ? 1 : 0;
     }
     __syncthreads();
     int base = 0, n = 0, over = 0;
-#pragma unroll
+#pragma unroll 1
     for (int w = 0; w < NW; ++w) {
         const int c = sm.red()[w];
         base += w < warp ? c : 0;
@@ -990,27 +1001,28 @@ __global__ void __launch_bounds__(NT, 2) kfirst_kernel(const SampleArgs a) {
         sample_row_fin<VEC>(a);
         return;
     }
+    // Zeros (and the zeros past V) are below uk >= 1, so every kept value is an element.
     const unsigned lt = (1u << lane) - 1u;
-#pragma unroll
-    for (int i = 0; i < LIVE_W; ++i) {
-        if (i < nl) {
-            const int e0 = sm.list()[r0 + i] * BLK + lane * 4;
-            unsigned m[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) m[q] = __ballot_sync(FULL, kept(v[i], q));
-            int p = base;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) p += __popc(m[q] & lt);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                if ((m[q] >> lane) & 1u) {
-                    sm.lv()[p] = q_at(v[i], q);
-                    sm.li()[p] = e0 + q;
-                    ++p;
-                }
+#pragma unroll 1
+    for (int i = 0; i < nb; ++i) {
+        const float4 x = *reinterpret_cast<const float4*>(stg + i * BLK + lane * 4);
+        const int e0 = sm.list()[r0 + i] * BLK + lane * 4;
+        int p = base;
+#pragma unroll 1
+        for (int q = 0; q < 4; ++q) {
+            const float xv = q_at(x, q);
+            const unsigned m = __ballot_sync(FULL, keyf(xv) >= uk);
+            p += __popc(m & lt);
+            base += __popc(m);
+        }
+#pragma unroll 1
+        for (int q = 0; q < 4; ++q) {
+            const float xv = q_at(x, q);
+            if (keyf(xv) >= uk) {
+                sm.lv()[p] = xv;
+                sm.li()[p] = e0 + q;
+                ++p;
             }
-#pragma unroll
-            for (int q = 0; q < 4; ++q) base += __popc(m[q]);
         }
     }
     __syncthreads();
@@ -1168,7 +1180,7 @@ static fs_status launch_scan_finish(const float* probs, int32_t batch_in, int32_
     p.shift = seg_shift_for(vocab);
     p.ns = (vocab + (BLK << p.shift) - 1) / (BLK << p.shift);
     p.nsc = (p.ns + 3) & ~3;
-    p.smem = Layout(p.ns).total();
+    p.smem = (kfirst && !soft) ? kfirst_smem(p.ns) : Layout(p.ns).total();
     p.per_sm = 0;
     if (p.smem > optin) return FS_ERR_UNSUPPORTED;
     void* ws = nullptr;
@@ -1427,9 +1439,22 @@ fs_status fs_sampling_plan(int32_t batch_out, int32_t vocab, int32_t order, int3
         return FS_ERR_INVALID_ARG;
     if (order != FS_ORDER_TOP_K_FIRST && order != FS_ORDER_JOINT) return FS_ERR_INVALID_ARG;
     if (vocab > FS_MAX_VOCAB) return FS_ERR_UNSUPPORTED;
+    if (order == FS_ORDER_TOP_K_FIRST) {
+        // The scan and the finishing launch: one CTA per row finishes it from the whole
+        // row's summary; the scan keeps FS_SCAN_PER_SM CTAs on every SM.
+        const int shift = fsd::seg_shift_for(vocab);
+        *cluster = 1;
+        *segment_len = fsd::BLK << shift;
+        *segments_per_cta = (vocab + (fsd::BLK << shift) - 1) / (fsd::BLK << shift);
+        *ctas_per_sm = FS_SCAN_PER_SM;
+        return FS_OK;
+    }
+    // Clusters: the plan of rows of probabilities that are 16-byte aligned with V % 4 = 0
+    // (the other rows run a scalar-load build of the same kernel, whose occupancy can
+    // differ).
     fsd::Plan p;
     const fs_status st = fsd::make_plan(batch_out, vocab, reinterpret_cast<const void*>(fsd::sample_kernel<true, false, false>),
-                                       order == FS_ORDER_TOP_K_FIRST, p);
+                                       false, p);
     if (st != FS_OK) return st;
     *cluster = p.C;
     *segment_len = fsd::BLK << p.shift;

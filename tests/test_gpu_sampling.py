@@ -416,48 +416,52 @@ def test_refined_bound_and_long_list_law(ms):
 
 @pytest.mark.parametrize("V", [32000, 151936, 256000])
 def test_launch_plan_fits_one_wave(ms, V):
-    """The launch plans of both kinds: a cluster of 1..16 CTAs covering the row's
-    segments, at most the occupancy limit of CTAs per SM, every cluster resident at
-    once whenever C > 1 (rows x C <= SMs x CTAs per SM), and the multi-pass kind
-    never with fewer CTAs per row than the single-pass kind."""
+    """The launch plans of both kinds.  Top-k-first (scan, then one CTA per row): one
+    CTA covers the whole row's summary.  Joint (rejection rounds on a cluster): a
+    cluster of 1..16 CTAs covering the row's segments, at most the occupancy limit of
+    CTAs per SM, every cluster resident at once whenever C > 1 (rows x C <= SMs x CTAs
+    per SM)."""
     import torch
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     for B in (1, 8, 32, 64, 128, 192, 256, 4096):
-        plans = {}
+        pl = ms.sampling_plan(B, V, "top_k_first")
+        assert pl["cluster"] == 1 and 1 <= pl["ctas_per_sm"] <= 8, pl
+        assert pl["segments_per_cta"] * pl["segment_len"] >= V > (pl["segments_per_cta"] - 1) * pl["segment_len"]
+        pl = ms.sampling_plan(B, V, "joint")
+        C, per_sm = pl["cluster"], pl["ctas_per_sm"]
+        assert 1 <= C <= 16 and 1 <= per_sm <= 8, pl
+        assert C * pl["segments_per_cta"] * pl["segment_len"] >= V, pl
+        assert pl["segments_per_cta"] % 4 == 0
+        if C > 1:
+            assert B * C <= sms * per_sm, (B, pl)
         for order in ("top_k_first", "joint"):
-            pl = ms.sampling_plan(B, V, order)
-            C, per_sm = pl["cluster"], pl["ctas_per_sm"]
-            assert 1 <= C <= 16 and 1 <= per_sm <= 8, pl
-            assert C * pl["segments_per_cta"] * pl["segment_len"] >= V, pl
-            assert pl["segments_per_cta"] % 4 == 0
-            if C > 1:
-                assert B * C <= sms * per_sm, (B, pl)
-            assert ms.sampling_plan(B, V, order) == pl   # cached, stable
-            plans[order] = pl
-        assert plans["joint"]["cluster"] >= plans["top_k_first"]["cluster"], plans
+            assert ms.sampling_plan(B, V, order) == ms.sampling_plan(B, V, order)   # cached, stable
     with pytest.raises(ValueError):
         ms.sampling_plan(8, V, "sorted")
 
 
 def test_batch_sizes_and_cluster_sizes(ms):
     """Batch sizes whose launch plans use clusters of many sizes (16 down to 2 CTAs per
-    row, odd sizes included), V = 32000: top-k-first membership of every draw,
-    top-k / top-p renormalisation and the logit mask exactly as the oracle's."""
+    row, odd sizes included), V = 32000: membership of every draw in both orders (the
+    joint order on those clusters), top-k / top-p renormalisation and the logit mask
+    exactly as the oracle's."""
     import torch
     from tests.test_gpu_filters import _check_renorm, _run as run_filter
     V = 32000
     seen = set()
     for B in (3, 33, 45, 60, 77, 100, 130, 300):
-        acc = guard_accept(lambda i: [(50, 0.9, None, "top_k_first"), (None, 0.9, None, "joint")])
+        acc = guard_accept(lambda i: [(50, 0.9, None, "top_k_first"), (None, 0.9, None, "joint"),
+                                      (50, 0.9, None, "joint")])
         w = workloads.config3(batch=B, vocab=V, accept=acc, seed=9000 + B)
-        seen.add(ms.sampling_plan(B, V, "top_k_first")["cluster"])
+        seen.add(ms.sampling_plan(B, V, "joint")["cluster"])
         P = torch.from_numpy(w.probs).cuda()
         ks = np.full(B, 50, np.int32)
         ps = np.full(B, 0.9, np.float32)
-        masks, vref = allowed_masks(w.probs, ks, ps, None, "top_k_first")
-        for call in range(2):
-            tok, valid, rounds = _call(ms, "top_k_first", P, ks, ps, None, seed=B, offset=call)
-            _membership(masks, vref, tok, valid)
+        for order in ("top_k_first", "joint"):
+            masks, vref = allowed_masks(w.probs, ks, ps, None, order)
+            for call in range(2):
+                tok, valid, rounds = _call(ms, order, P, ks, ps, None, seed=B, offset=call)
+                _membership(masks, vref, tok, valid)
         out, valid = run_filter(ms, "top_k", w.probs, list(ks))
         _check_renorm(w.probs, list(ks), out, valid, filters.top_k_renorm)
         out, valid = run_filter(ms, "top_p", w.probs, list(ps))
