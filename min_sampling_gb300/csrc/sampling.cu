@@ -973,55 +973,85 @@ __global__ void __launch_bounds__(NT, 2) kfirst_kernel(const SampleArgs a) {
         }
     }
     cp_async_commit();
-    cp_async_wait<0>();  // each lane reads back the words it copied (zeros past V)
-    const int nb = min(nl, LIVE_W);
-    int cnt = 0;
-#pragma unroll 1
-    for (int i = 0; i < nb; ++i) {
-        const float4 x = *reinterpret_cast<const float4*>(stg + i * BLK + lane * 4);
-        cnt += (keyf(x.x) >= uk) + (keyf(x.y) >= uk) + (keyf(x.z) >= uk) + (keyf(x.w) >= uk);
-    }
-    cnt = warp_sum_i(cnt);
     __syncthreads();  // every warp is done with red[] (the bound)
-    if (lane == 0) {
-        sm.red()[warp] = cnt;
-        sm.red()[NW + warp] = nl > LIVE_W ? 1 : 0;
-    }
-    __syncthreads();
-    int base = 0, n = 0, over = 0;
-#pragma unroll 1
-    for (int w = 0; w < NW; ++w) {
-        const int c = sm.red()[w];
-        base += w < warp ? c : 0;
-        n += c;
-        over |= sm.red()[NW + w];
-    }
-    if (over || n > SMALL) {
+    if (lane == 0) sm.red()[warp] = nl;
+    cp_async_wait<0>();
+    __syncthreads();  // every warp's live count
+    // Staged blocks in index order: warp 0's, then warp 1's, ...; red[NW + w] = the
+    // staged blocks of warps 0..w (inclusive prefix), L = all of them.
+    const int nlw = lane < NW ? sm.red()[lane] : 0;
+    const bool over = __any_sync(FULL, nlw > LIVE_W);
+    const int bincl = warp_incl_scan_i(min(nlw, LIVE_W), lane);
+    const int L = __shfl_sync(FULL, bincl, NW - 1);
+    if (warp == 0 && lane < NW) sm.red()[NW + lane] = bincl;
+    if (over) {
         __syncthreads();
         sample_row_fin<VEC>(a);
         return;
     }
-    // Zeros (and the zeros past V) are below uk >= 1, so every kept value is an element.
-    const unsigned lt = (1u << lane) - 1u;
-#pragma unroll 1
-    for (int i = 0; i < nb; ++i) {
-        const float4 x = *reinterpret_cast<const float4*>(stg + i * BLK + lane * 4);
-        const int e0 = sm.list()[r0 + i] * BLK + lane * 4;
-        int p = base;
-#pragma unroll 1
-        for (int q = 0; q < 4; ++q) {
-            const float xv = q_at(x, q);
-            const unsigned m = __ballot_sync(FULL, keyf(xv) >= uk);
-            p += __popc(m & lt);
-            base += __popc(m);
+    __syncthreads();  // the staged blocks (each warp waited for its own copies) and red[NW..2NW)
+    // ---- candidates: one flat pass over the L x 128 staged values, fpt float4 per
+    // thread in order, then one block-wide scan of the counts gives every kept value its
+    // place in index order.  Zeros (and the zeros past V) are below uk >= 1.
+    constexpr int FPT = LIVE_W * NW * 32 / NT;  // float4 per thread at most (L <= NW x LIVE_W)
+    const int fpt = (L * 32 + NT - 1) / NT;
+    const int g0 = tid * fpt;
+    unsigned long long kmask = 0ull;  // 4 bits per float4
+    int wb = 0, wend = sm.red()[NW], wfirst = 0;  // the warp area holding flat block j
+#pragma unroll
+    for (int c = 0; c < FPT; ++c) {
+        const int g = g0 + c;  // flat float4: block j = g / 32, its float4 g % 32
+        if (c < fpt && g < L * 32) {
+            const int j = g >> 5;
+            while (j >= wend) {
+                wfirst = wend;
+                ++wb;
+                wend = sm.red()[NW + wb];
+            }
+            const float4 x = *reinterpret_cast<const float4*>(kfirst_stage(sm) + (wb * LIVE_W + j - wfirst) * BLK +
+                                                              (g & 31) * 4);
+            kmask |= (unsigned long long)((keyf(x.x) >= uk ? 1u : 0u) | (keyf(x.y) >= uk ? 2u : 0u) |
+                                          (keyf(x.z) >= uk ? 4u : 0u) | (keyf(x.w) >= uk ? 8u : 0u))
+                     << (4 * c);
         }
+    }
+    const int kc = __popcll(kmask);
+    const int kincl = warp_incl_scan_i(kc, lane);
+    if (lane == 31) sm.red()[2 * NW + warp] = kincl;
+    __syncthreads();
+    const int wt = lane < NW ? sm.red()[2 * NW + lane] : 0;
+    const int n = warp_sum_i(wt);
+    if (n > SMALL) {
+        __syncthreads();
+        sample_row_fin<VEC>(a);
+        return;
+    }
+    if (kmask) {
+        int p = kincl - kc;
+        for (int w = 0; w < warp; ++w) p += sm.red()[2 * NW + w];
+        const int per = (ns + NW - 1) / NW;  // warp w's share of the segments starts at w * per
+        wb = 0;
+        wend = sm.red()[NW];
+        wfirst = 0;
 #pragma unroll 1
-        for (int q = 0; q < 4; ++q) {
-            const float xv = q_at(x, q);
-            if (keyf(xv) >= uk) {
-                sm.lv()[p] = xv;
-                sm.li()[p] = e0 + q;
-                ++p;
+        for (int c = 0; c < fpt; ++c) {
+            const unsigned m4 = unsigned(kmask >> (4 * c)) & 15u;
+            if (!m4) continue;
+            const int g = g0 + c, j = g >> 5;
+            while (j >= wend) {
+                wfirst = wend;
+                ++wb;
+                wend = sm.red()[NW + wb];
+            }
+            const float* bx = kfirst_stage(sm) + (wb * LIVE_W + j - wfirst) * BLK + (g & 31) * 4;
+            const int e0 = sm.list()[min(ns, wb * per) + j - wfirst] * BLK + (g & 31) * 4;
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {
+                if ((m4 >> q) & 1u) {
+                    sm.lv()[p] = bx[q];
+                    sm.li()[p] = e0 + q;
+                    ++p;
+                }
             }
         }
     }
@@ -1035,17 +1065,18 @@ __global__ void __launch_bounds__(NT, 2) kfirst_kernel(const SampleArgs a) {
         if (warp * 32 < n) {  // the warps holding candidates
             const uint4* c4 = reinterpret_cast<const uint4*>(sm.lv());
             const uint32_t mine = tid < n ? __float_as_uint(sm.lv()[tid]) : 0xffffffffu;
-            int ge = 0;
+            int gc[4] = {0, 0, 0, 0};  // four independent counts
 #pragma unroll 1
             for (int t = 0; 4 * t < n; t += 4) {
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const uint4 w = c4[t + c];  // SMALL entries are always in the list's storage
                     const int e = 4 * (t + c);
-                    ge += (w.x >= mine && e < n) + (w.y >= mine && e + 1 < n) + (w.z >= mine && e + 2 < n) +
-                          (w.w >= mine && e + 3 < n);
+                    gc[c] += (w.x >= mine && e < n) + (w.y >= mine && e + 1 < n) + (w.z >= mine && e + 2 < n) +
+                             (w.w >= mine && e + 3 < n);
                 }
             }
+            const int ge = (gc[0] + gc[1]) + (gc[2] + gc[3]);
             best = (tid < n && ge >= k) ? mine : 0u;
             best = warp_max_u(best);
         }
