@@ -375,10 +375,11 @@ __device__ __forceinline__ int compact_round(Smem sm, int n_list, const Pred& f,
 // nothing eligible); the number of rounds in `rounds`.
 __device__ __forceinline__ int small_rounds(const Small& s, const bool* kept, const Pred& f, float S_low, float high,
                                             unsigned long long seed, unsigned long long offset, uint32_t b, int lane,
-                                            int& rounds) {
+                                            int& rounds, const float* u32 = nullptr) {
     float low = 0.f;
-    // Lane l holds the uniform of round l: 32 rounds of the stream at the cost of one.
-    const float u_lane = sampler_uniform(seed, offset, b, uint32_t(lane));
+    // Lane l holds the uniform of round l: 32 rounds of the stream at the cost of one
+    // (or, with u32, as another warp drew them beforehand).
+    const float u_lane = u32 ? u32[lane] : sampler_uniform(seed, offset, b, uint32_t(lane));
 #pragma unroll 1
     for (int round = 0; round < R_MAX; ++round) {
         const float u = round < 32 ? __shfl_sync(FULL, u_lane, round) : sampler_uniform(seed, offset, b, uint32_t(round));
@@ -990,82 +991,100 @@ __global__ void __launch_bounds__(NT, 2) kfirst_kernel(const SampleArgs a) {
         return;
     }
     __syncthreads();  // the staged blocks (each warp waited for its own copies) and red[NW..2NW)
-    // ---- candidates: one flat pass over the L x 128 staged values, fpt float4 per
-    // thread in order, then one block-wide scan of the counts gives every kept value its
-    // place in index order.  Zeros (and the zeros past V) are below uk >= 1.
-    constexpr int FPT = LIVE_W * NW * 32 / NT;  // float4 per thread at most (L <= NW x LIVE_W)
-    const int fpt = (L * 32 + NT - 1) / NT;
-    const int g0 = tid * fpt;
-    unsigned long long kmask = 0ull;  // 4 bits per float4
-    int wb = 0, wend = sm.red()[NW], wfirst = 0;  // the warp area holding flat block j
-#pragma unroll
-    for (int c = 0; c < FPT; ++c) {
-        const int g = g0 + c;  // flat float4: block j = g / 32, its float4 g % 32
-        if (c < fpt && g < L * 32) {
-            const int j = g >> 5;
-            while (j >= wend) {
-                wfirst = wend;
-                ++wb;
-                wend = sm.red()[NW + wb];
-            }
-            const float4 x = *reinterpret_cast<const float4*>(kfirst_stage(sm) + (wb * LIVE_W + j - wfirst) * BLK +
-                                                              (g & 31) * 4);
-            kmask |= (unsigned long long)((keyf(x.x) >= uk ? 1u : 0u) | (keyf(x.y) >= uk ? 2u : 0u) |
-                                          (keyf(x.z) >= uk ? 4u : 0u) | (keyf(x.w) >= uk ? 8u : 0u))
-                     << (4 * c);
+    // ---- candidates: the L x 128 staged values in index order, warp w taking a
+    // contiguous range of F float4 (lanes on consecutive float4: no bank conflicts);
+    // per round of 32 float4 the ballots give every kept value its place.  Zeros (and
+    // the zeros past V) are below uk >= 1.  Meanwhile warp NW - 1 draws the uniforms
+    // of the first 32 rounds.
+    const int F = (L + NW - 1) / NW * 32;  // float4 per warp
+    const int f0 = warp * F;
+    const int f1 = min(L * 32, f0 + F);
+    auto stage_at = [&](int g, int& wb, int& wend, int& wfirst) {  // flat float4 g -> its staged address
+        const int j = g >> 5;
+        while (j >= wend) {
+            wfirst = wend;
+            ++wb;
+            wend = sm.red()[NW + wb];
+        }
+        return kfirst_stage(sm) + (wb * LIVE_W + j - wfirst) * BLK + (g & 31) * 4;
+    };
+    auto kept4 = [&](const float4& x) {
+        return (keyf(x.x) >= uk ? 1u : 0u) | (keyf(x.y) >= uk ? 2u : 0u) | (keyf(x.z) >= uk ? 4u : 0u) |
+               (keyf(x.w) >= uk ? 8u : 0u);
+    };
+    int wcnt = 0;
+    unsigned hit_rounds = 0u;  // rounds of this warp's range that hold a kept value
+    {
+        int wb = 0, wend = sm.red()[NW], wfirst = 0;
+#pragma unroll 1
+        for (int g = f0, rd = 0; g < f1; g += 32, ++rd) {
+            unsigned m = 0u;
+            if (g + lane < f1) m = kept4(*reinterpret_cast<const float4*>(stage_at(g + lane, wb, wend, wfirst)));
+            const int c = __reduce_add_sync(FULL, __popc(m));
+            wcnt += c;
+            hit_rounds |= c ? (1u << rd) : 0u;
         }
     }
-    const int kc = __popcll(kmask);
-    const int kincl = warp_incl_scan_i(kc, lane);
-    if (lane == 31) sm.red()[2 * NW + warp] = kincl;
+    float* uni = reinterpret_cast<float*>(sm.mass(2));  // [32] uniforms of rounds 0..31
+    if (warp == NW - 1) {
+        const unsigned long long seed_b = *reinterpret_cast<const unsigned long long*>(sm.prm() + 4);
+        const unsigned long long offset_b = *reinterpret_cast<const unsigned long long*>(sm.prm() + 6);
+        uni[lane] = sampler_uniform(seed_b, offset_b, a.seeds ? 0u : uint32_t(b), uint32_t(lane));
+    }
+    if (lane == 0) sm.red()[2 * NW + warp] = wcnt;
     __syncthreads();
-    const int wt = lane < NW ? sm.red()[2 * NW + lane] : 0;
-    const int n = warp_sum_i(wt);
+    int n = 0, p = 0;
+#pragma unroll 1
+    for (int w = 0; w < NW; ++w) {
+        const int c = sm.red()[2 * NW + w];
+        p += w < warp ? c : 0;
+        n += c;
+    }
     if (n > SMALL) {
         __syncthreads();
         sample_row_fin<VEC>(a);
         return;
     }
-    if (kmask) {
-        int p = kincl - kc;
-        for (int w = 0; w < warp; ++w) p += sm.red()[2 * NW + w];
+    if (hit_rounds) {
         const int per = (ns + NW - 1) / NW;  // warp w's share of the segments starts at w * per
-        wb = 0;
-        wend = sm.red()[NW];
-        wfirst = 0;
+        const unsigned lt = (1u << lane) - 1u;
+        int wb = 0, wend = sm.red()[NW], wfirst = 0;
 #pragma unroll 1
-        for (int c = 0; c < fpt; ++c) {
-            const unsigned m4 = unsigned(kmask >> (4 * c)) & 15u;
-            if (!m4) continue;
-            const int g = g0 + c, j = g >> 5;
-            while (j >= wend) {
-                wfirst = wend;
-                ++wb;
-                wend = sm.red()[NW + wb];
+        for (int g = f0, rd = 0; g < f1; g += 32, ++rd) {
+            if (!((hit_rounds >> rd) & 1u)) continue;
+            unsigned m = 0u;
+            int e0 = 0;
+            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (g + lane < f1) {  // each lane's cursor only moves forward
+                x = *reinterpret_cast<const float4*>(stage_at(g + lane, wb, wend, wfirst));
+                m = kept4(x);
+                e0 = sm.list()[min(ns, wb * per) + ((g + lane) >> 5) - wfirst] * BLK + ((g + lane) & 31) * 4;
             }
-            const float* bx = kfirst_stage(sm) + (wb * LIVE_W + j - wfirst) * BLK + (g & 31) * 4;
-            const int e0 = sm.list()[min(ns, wb * per) + j - wfirst] * BLK + (g & 31) * 4;
-#pragma unroll 1
+            // index order inside the round: lane by lane, the four values of a lane in turn
+            int pos = p;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) pos += __popc(__ballot_sync(FULL, (m >> q) & 1u) & lt);
+#pragma unroll
             for (int q = 0; q < 4; ++q) {
-                if ((m4 >> q) & 1u) {
-                    sm.lv()[p] = bx[q];
-                    sm.li()[p] = e0 + q;
-                    ++p;
+                if ((m >> q) & 1u) {
+                    sm.lv()[pos] = q_at(x, q);
+                    sm.li()[pos] = e0 + q;
+                    ++pos;
                 }
             }
+            p += __reduce_add_sync(FULL, __popc(m));
         }
     }
     __syncthreads();
-    // t_k: the largest candidate key with at least k candidate keys at or above it (0
-    // when there are fewer than k candidates: the row has fewer than k positives).
-    {
-        // Thread t < n counts the candidates at or above candidate t (16-byte broadcast
-        // reads; candidate values are positive, so their order is that of the bits).
+    // t_k when more than 32 candidates lie below it: every candidate counts the
+    // candidates at or above it (warps holding candidates; four independent sums).
+    // Otherwise warp 0 finds it by taking the smallest keys away (small_kth).
+    if (n - k >= 32) {
         uint32_t best = 0u;
-        if (warp * 32 < n) {  // the warps holding candidates
+        if (warp * 32 < n) {
             const uint4* c4 = reinterpret_cast<const uint4*>(sm.lv());
             const uint32_t mine = tid < n ? __float_as_uint(sm.lv()[tid]) : 0xffffffffu;
-            int gc[4] = {0, 0, 0, 0};  // four independent counts
+            int gc[4] = {0, 0, 0, 0};
 #pragma unroll 1
             for (int t = 0; 4 * t < n; t += 4) {
 #pragma unroll
@@ -1080,13 +1099,10 @@ __global__ void __launch_bounds__(NT, 2) kfirst_kernel(const SampleArgs a) {
             best = (tid < n && ge >= k) ? mine : 0u;
             best = warp_max_u(best);
         }
-        if (lane == 0) sm.red()[2 * NW + warp] = int(best);
+        if (lane == 0) sm.red()[3 * NW + warp] = int(best);
+        __syncthreads();
     }
-    __syncthreads();
     if (warp != 0) return;
-    uint32_t tk = 0u;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) tk = max(tk, uint32_t(sm.red()[2 * NW + w]));
     // ---- warp 0: F_k, the rounds, the outputs (as the cluster's leader)
     const float tp = __uint_as_float(sm.prm()[1]);
     const float mp = __uint_as_float(sm.prm()[2]);
@@ -1113,20 +1129,30 @@ __global__ void __launch_bounds__(NT, 2) kfirst_kernel(const SampleArgs a) {
     if (valid) {
         Small sl;
         sl.n = n;
-        bool kp[SR];
-        float fk = 0.f;
 #pragma unroll
         for (int q = 0; q < SR; ++q) {
             const int e = SR * lane + q;
             sl.in[q] = e < n;
             sl.x[q] = sl.in[q] ? sm.lv()[e] : 0.f;
             sl.i[q] = sl.in[q] ? sm.li()[e] : 0;
+        }
+        uint32_t tk = 0u;
+        if (n - k >= 32) {
+#pragma unroll
+            for (int w = 0; w < NW; ++w) tk = max(tk, uint32_t(sm.red()[3 * NW + w]));
+        } else {
+            tk = small_kth(sl, k, keyf);
+        }
+        bool kp[SR];
+        float fk = 0.f;
+#pragma unroll
+        for (int q = 0; q < SR; ++q) {
             kp[q] = sl.in[q] && keyf(sl.x[q]) >= tk;
             fk += kp[q] ? sl.x[q] : 0.f;
         }
         const float Fk = warp_sum(fk);
         f.pthr = tp * Fk;  // top-p inside the k, measured against F_k
-        token = small_rounds(sl, kp, f, Fk, rowmax, seed_b, offset_b, stream_b, lane, rounds);
+        token = small_rounds(sl, kp, f, Fk, rowmax, seed_b, offset_b, stream_b, lane, rounds, uni);
     }
     if (lane == 0) {
         a.out_token[b] = token >= 0 ? token : -1;
