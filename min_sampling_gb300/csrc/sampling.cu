@@ -885,17 +885,18 @@ FS_COLD __device__ void sample_row_fin(const SampleArgs& a) {
 // ([explainer] filter order: t_k is the k-th largest value), so uk <= t_k: every
 // element >= t_k lies in a segment whose maximum is >= uk.  Steps, with two round
 // trips to L2 after the scan: (1) the row's summary, the histogram of its unit maxima
-// counted as it is unpacked, uk; (2) each warp reloads the live segments (maximum
-// >= uk) of its own contiguous share of the row, and the elements >= uk are written in
-// index order into the candidate list; t_k is counted among the candidates by the
-// warps that hold them; warp 0 then runs the rejection rounds in registers as the
-// cluster's leader does.  Any other row (a bad row index, no top-k filter, fewer units than k,
-// segments of several blocks, more than LIVE_W live segments in one warp's share or
+// counted as it is unpacked, uk; (2) the live segments (maximum >= uk) copied in index
+// order into shared memory, their elements >= uk written in index order into the
+// candidate list; then warp 0 finds t_k and runs the rejection rounds in registers as
+// the cluster's leader does.  The work is spread so that no warp runs a long chain of
+// dependent instructions: this code runs once per launch at one CTA per SM, where such
+// chains, not memory, set the time.  Any other row (a bad row index, no top-k filter,
+// fewer units than k, segments of several blocks, more than KF_LIVE live segments or
 // more than SMALL candidates) takes the general finishing path, out of line.
-constexpr int LIVE_W = 16;   // live segments one warp stages in shared memory
+constexpr int KF_LIVE = 128;  // live segments the lean finish stages in shared memory
 
-// Per-warp staging areas of the lean finish (NW x LIVE_W blocks), after the carve-up.
-__host__ __device__ inline size_t kfirst_smem(int ns) { return Layout(ns).total() + size_t(NW) * LIVE_W * BLK * 4; }
+// The staging area of the lean finish (KF_LIVE blocks), after the carve-up.
+__host__ __device__ inline size_t kfirst_smem(int ns) { return Layout(ns).total() + size_t(KF_LIVE) * BLK * 4; }
 __device__ __forceinline__ float* kfirst_stage(Smem sm) {
     return reinterpret_cast<float*>(smem_raw + Layout(sm.ns).total());
 }
@@ -949,121 +950,116 @@ __global__ void __launch_bounds__(NT, 2) kfirst_kernel(const SampleArgs a) {
     }
     __syncthreads();
     const uint32_t uk = max(1u, uint32_t(sm.bcast()[0]) << 21);  // zeros are never candidates
-    // ---- (2) this warp's live segments (maximum >= uk) of its contiguous share, copied
-    // into its staging area as they are found (cp.async, one 512-byte block each), then
-    // counted and placed from shared memory.  Every loop here is rolled: this code runs
-    // once per launch, and straight-line code would be fetched line by line.
+    // ---- (2) the live segments (maximum >= uk), copied into the staging area in index
+    // order, then the candidates.  Each warp first counts the live segments of its
+    // contiguous share, so that it knows where its copies start.
     int r0, r1;
     warp_range(ns, warp, r0, r1);
-    const float* row = a.probs + size_t(r) * size_t(V);
-    float* stg = kfirst_stage(sm) + warp * (LIVE_W * BLK);
     int nl = 0;
 #pragma unroll 1
-    for (int b0 = r0; b0 < r1; b0 += 32) {
-        const int i = b0 + lane;
-        unsigned bal = __ballot_sync(FULL, i < r1 && sm.segkey()[i] >= uk);
-#pragma unroll 1
-        while (bal) {
-            const int sg = b0 + __ffs(bal) - 1;
-            bal &= bal - 1u;
-            if (nl < LIVE_W) {
-                stage4<VEC>(stg + nl * BLK + lane * 4, row, V, sg * BLK + lane * 4);
-                if (lane == 0) sm.list()[r0 + nl] = sg;
-            }
-            ++nl;
-        }
-    }
-    cp_async_commit();
-    __syncthreads();  // every warp is done with red[] (the bound)
+    for (int b0 = r0; b0 < r1; b0 += 32)
+        nl += __popc(__ballot_sync(FULL, b0 + lane < r1 && sm.segkey()[b0 + lane] >= uk));
     if (lane == 0) sm.red()[warp] = nl;
-    cp_async_wait<0>();
-    __syncthreads();  // every warp's live count
-    // Staged blocks in index order: warp 0's, then warp 1's, ...; red[NW + w] = the
-    // staged blocks of warps 0..w (inclusive prefix), L = all of them.
-    const int nlw = lane < NW ? sm.red()[lane] : 0;
-    const bool over = __any_sync(FULL, nlw > LIVE_W);
-    const int bincl = warp_incl_scan_i(min(nlw, LIVE_W), lane);
-    const int L = __shfl_sync(FULL, bincl, NW - 1);
-    if (warp == 0 && lane < NW) sm.red()[NW + lane] = bincl;
-    if (over) {
+    __syncthreads();
+    int off = 0, L = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+        const int c = sm.red()[w];
+        off += w < warp ? c : 0;
+        L += c;
+    }
+    if (L > KF_LIVE) {
         __syncthreads();
         sample_row_fin<VEC>(a);
         return;
     }
-    __syncthreads();  // the staged blocks (each warp waited for its own copies) and red[NW..2NW)
-    // ---- candidates: the L x 128 staged values in index order, warp w taking a
-    // contiguous range of F float4 (lanes on consecutive float4: no bank conflicts);
-    // per round of 32 float4 the ballots give every kept value its place.  Zeros (and
-    // the zeros past V) are below uk >= 1.  Meanwhile warp NW - 1 draws the uniforms
-    // of the first 32 rounds.
-    const int F = (L + NW - 1) / NW * 32;  // float4 per warp
-    const int f0 = warp * F;
-    const int f1 = min(L * 32, f0 + F);
-    auto stage_at = [&](int g, int& wb, int& wend, int& wfirst) {  // flat float4 g -> its staged address
-        const int j = g >> 5;
-        while (j >= wend) {
-            wfirst = wend;
-            ++wb;
-            wend = sm.red()[NW + wb];
-        }
-        return kfirst_stage(sm) + (wb * LIVE_W + j - wfirst) * BLK + (g & 31) * 4;
-    };
-    auto kept4 = [&](const float4& x) {
-        return (keyf(x.x) >= uk ? 1u : 0u) | (keyf(x.y) >= uk ? 2u : 0u) | (keyf(x.z) >= uk ? 4u : 0u) |
-               (keyf(x.w) >= uk ? 8u : 0u);
-    };
-    int wcnt = 0;
-    unsigned hit_rounds = 0u;  // rounds of this warp's range that hold a kept value
-    {
-        int wb = 0, wend = sm.red()[NW], wfirst = 0;
+    const float* row = a.probs + size_t(r) * size_t(V);
+    float* stg = kfirst_stage(sm);
+    int* seg = reinterpret_cast<int*>(sm.list());  // [L] the staged segments, in index order
 #pragma unroll 1
-        for (int g = f0, rd = 0; g < f1; g += 32, ++rd) {
-            unsigned m = 0u;
-            if (g + lane < f1) m = kept4(*reinterpret_cast<const float4*>(stage_at(g + lane, wb, wend, wfirst)));
-            const int c = __reduce_add_sync(FULL, __popc(m));
-            wcnt += c;
-            hit_rounds |= c ? (1u << rd) : 0u;
+    for (int b0 = r0; b0 < r1; b0 += 32) {
+        unsigned bal = __ballot_sync(FULL, b0 + lane < r1 && sm.segkey()[b0 + lane] >= uk);
+#pragma unroll 1
+        while (bal) {
+            const int sg = b0 + __ffs(bal) - 1;
+            bal &= bal - 1u;
+            stage4<VEC>(stg + off * BLK + lane * 4, row, V, sg * BLK + lane * 4);
+            if (lane == 0) seg[off] = sg;
+            ++off;
         }
     }
-    float* uni = reinterpret_cast<float*>(sm.mass(2));  // [32] uniforms of rounds 0..31
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();  // every warp's copies and segment numbers
+    // Candidates: thread t takes the staged float4 t, t + NT, ... (consecutive threads on
+    // consecutive float4: no bank conflicts; the loads are independent).  Zeros (and the
+    // zeros past V) are below uk >= 1.  Round c of a warp covers float4 c * NT + 32 * warp
+    // + lane: the index order is round by round, warp by warp, lane by lane.
+    constexpr int FPT = KF_LIVE * 32 / NT;  // float4 per thread at most
+    const int g4 = L * 32;                   // staged float4
+    unsigned long long kmask = 0ull;         // 4 bits per round
+    int* rc = reinterpret_cast<int*>(sm.hist());  // [rounds x NW] counts (the histogram is done with)
+#pragma unroll
+    for (int c = 0; c < FPT; ++c) {
+        const int g = c * NT + tid;
+        if (c * NT < g4) {
+            unsigned m = 0u;
+            if (g < g4) {
+                const float4 x = *reinterpret_cast<const float4*>(stg + g * 4);
+                m = (keyf(x.x) >= uk ? 1u : 0u) | (keyf(x.y) >= uk ? 2u : 0u) | (keyf(x.z) >= uk ? 4u : 0u) |
+                    (keyf(x.w) >= uk ? 8u : 0u);
+            }
+            kmask |= (unsigned long long)m << (4 * c);
+            const int t = __reduce_add_sync(FULL, __popc(m));
+            if (lane == 0) rc[c * NW + warp] = t;
+        }
+    }
+    // Meanwhile the last warp draws the uniforms of the first 32 rounds.
+    float* uni = reinterpret_cast<float*>(sm.red()) + (REDW - 32);  // [32]
     if (warp == NW - 1) {
         const unsigned long long seed_b = *reinterpret_cast<const unsigned long long*>(sm.prm() + 4);
         const unsigned long long offset_b = *reinterpret_cast<const unsigned long long*>(sm.prm() + 6);
         uni[lane] = sampler_uniform(seed_b, offset_b, a.seeds ? 0u : uint32_t(b), uint32_t(lane));
     }
-    if (lane == 0) sm.red()[2 * NW + warp] = wcnt;
     __syncthreads();
-    int n = 0, p = 0;
-#pragma unroll 1
-    for (int w = 0; w < NW; ++w) {
-        const int c = sm.red()[2 * NW + w];
-        p += w < warp ? c : 0;
-        n += c;
+    // Exclusive prefix of the (round, warp) counts in index order, by warp 0; n = total.
+    const int nrc = ((g4 + NT - 1) / NT) * NW;  // (round, warp) counts
+    if (warp == 0) {
+        int v[4], own = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            v[q] = 4 * lane + q < nrc ? rc[4 * lane + q] : 0;
+            own += v[q];
+        }
+        const int incl = warp_incl_scan_i(own, lane);
+        int e = incl - own;
+        __syncwarp();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if (4 * lane + q < nrc) rc[4 * lane + q] = e;
+            e += v[q];
+        }
+        if (lane == 31) sm.red()[0] = incl;
     }
+    __syncthreads();
+    const int n = sm.red()[0];
     if (n > SMALL) {
         __syncthreads();
         sample_row_fin<VEC>(a);
         return;
     }
-    if (hit_rounds) {
-        const int per = (ns + NW - 1) / NW;  // warp w's share of the segments starts at w * per
-        const unsigned lt = (1u << lane) - 1u;
-        int wb = 0, wend = sm.red()[NW], wfirst = 0;
+    const unsigned lt = (1u << lane) - 1u;
 #pragma unroll 1
-        for (int g = f0, rd = 0; g < f1; g += 32, ++rd) {
-            if (!((hit_rounds >> rd) & 1u)) continue;
-            unsigned m = 0u;
-            int e0 = 0;
-            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (g + lane < f1) {  // each lane's cursor only moves forward
-                x = *reinterpret_cast<const float4*>(stage_at(g + lane, wb, wend, wfirst));
-                m = kept4(x);
-                e0 = sm.list()[min(ns, wb * per) + ((g + lane) >> 5) - wfirst] * BLK + ((g + lane) & 31) * 4;
-            }
-            // index order inside the round: lane by lane, the four values of a lane in turn
-            int pos = p;
+    for (int c = 0; c * NT < g4; ++c) {
+        const unsigned m = unsigned(kmask >> (4 * c)) & 15u;
+        if (!__any_sync(FULL, m != 0u)) continue;
+        int pos = rc[c * NW + warp];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) pos += __popc(__ballot_sync(FULL, (m >> q) & 1u) & lt);
+        for (int q = 0; q < 4; ++q) pos += __popc(__ballot_sync(FULL, (m >> q) & 1u) & lt);
+        if (m) {
+            const int g = c * NT + tid;
+            const float4 x = *reinterpret_cast<const float4*>(stg + g * 4);
+            const int e0 = seg[g >> 5] * BLK + (g & 31) * 4;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 if ((m >> q) & 1u) {
@@ -1072,7 +1068,6 @@ __global__ void __launch_bounds__(NT, 2) kfirst_kernel(const SampleArgs a) {
                     ++pos;
                 }
             }
-            p += __reduce_add_sync(FULL, __popc(m));
         }
     }
     __syncthreads();
