@@ -893,7 +893,7 @@ FS_COLD __device__ void sample_row_fin(const SampleArgs& a) {
 // chains, not memory, set the time.  Any other row (a bad row index, no top-k filter,
 // fewer units than k, segments of several blocks, more than KF_LIVE live segments or
 // more than SMALL candidates) takes the general finishing path, out of line.
-constexpr int KF_LIVE = 128;  // live segments the lean finish stages in shared memory
+constexpr int KF_LIVE = 112;  // live segments the lean finish stages (fpt = 15 float4 per thread at most)
 
 // The staging area of the lean finish (KF_LIVE blocks), after the carve-up.
 __host__ __device__ inline size_t kfirst_smem(int ns) { return Layout(ns).total() + size_t(KF_LIVE) * BLK * 4; }
@@ -991,28 +991,23 @@ __global__ void __launch_bounds__(NT, 2) kfirst_kernel(const SampleArgs a) {
     cp_async_commit();
     cp_async_wait<0>();
     __syncthreads();  // every warp's copies and segment numbers
-    // Candidates: thread t takes the staged float4 t, t + NT, ... (consecutive threads on
-    // consecutive float4: no bank conflicts; the loads are independent).  Zeros (and the
-    // zeros past V) are below uk >= 1.  Round c of a warp covers float4 c * NT + 32 * warp
-    // + lane: the index order is round by round, warp by warp, lane by lane.
-    constexpr int FPT = KF_LIVE * 32 / NT;  // float4 per thread at most
-    const int g4 = L * 32;                   // staged float4
-    unsigned long long kmask = 0ull;         // 4 bits per round
-    int* rc = reinterpret_cast<int*>(sm.hist());  // [rounds x NW] counts (the histogram is done with)
-#pragma unroll
-    for (int c = 0; c < FPT; ++c) {
-        const int g = c * NT + tid;
-        if (c * NT < g4) {
-            unsigned m = 0u;
-            if (g < g4) {
-                const float4 x = *reinterpret_cast<const float4*>(stg + g * 4);
-                m = (keyf(x.x) >= uk ? 1u : 0u) | (keyf(x.y) >= uk ? 2u : 0u) | (keyf(x.z) >= uk ? 4u : 0u) |
-                    (keyf(x.w) >= uk ? 8u : 0u);
-            }
-            kmask |= (unsigned long long)m << (4 * c);
-            const int t = __reduce_add_sync(FULL, __popc(m));
-            if (lane == 0) rc[c * NW + warp] = t;
-        }
+    // Candidates: thread t takes fpt consecutive staged float4 (fpt odd: the eight lanes
+    // of a 16-byte access phase then touch eight different bank groups), one block-wide
+    // scan of the counts gives every kept value its place in index order.  Rolled loops
+    // and few instructions: this code runs once per launch.  Zeros (and the zeros past
+    // V) are below uk >= 1; for values >= 0, key >= uk is x >= the float of uk.
+    const float ukf = __uint_as_float(uk);
+    const int g4 = L * 32;  // staged float4
+    const int fpt = ((g4 + NT - 1) / NT) | 1;
+    const int g0 = min(g4, tid * fpt), g1 = min(g4, g0 + fpt);
+    const float4* stg4 = reinterpret_cast<const float4*>(stg);
+    unsigned long long kmask = 0ull;  // 4 bits per float4 of the thread's range (fpt <= 17)
+#pragma unroll 1
+    for (int g = g0; g < g1; ++g) {
+        const float4 x = stg4[g];
+        const unsigned m = (x.x >= ukf ? 1u : 0u) | (x.y >= ukf ? 2u : 0u) | (x.z >= ukf ? 4u : 0u) |
+                           (x.w >= ukf ? 8u : 0u);
+        kmask |= (unsigned long long)m << (4 * (g - g0));
     }
     // Meanwhile the last warp draws the uniforms of the first 32 rounds.
     float* uni = reinterpret_cast<float*>(sm.red()) + (REDW - 32);  // [32]
@@ -1021,60 +1016,33 @@ __global__ void __launch_bounds__(NT, 2) kfirst_kernel(const SampleArgs a) {
         const unsigned long long offset_b = *reinterpret_cast<const unsigned long long*>(sm.prm() + 6);
         uni[lane] = sampler_uniform(seed_b, offset_b, a.seeds ? 0u : uint32_t(b), uint32_t(lane));
     }
+    const int kc = __popcll(kmask);
+    const int kincl = warp_incl_scan_i(kc, lane);
+    if (lane == 31) sm.red()[warp] = kincl;
     __syncthreads();
-    // Exclusive prefix of the (round, warp) counts in index order, by warp 0; n = total.
-    const int nrc = ((g4 + NT - 1) / NT) * NW;  // (round, warp) counts
-    if (warp == 0) {
-        int v[4], own = 0;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            v[q] = 4 * lane + q < nrc ? rc[4 * lane + q] : 0;
-            own += v[q];
-        }
-        const int incl = warp_incl_scan_i(own, lane);
-        int e = incl - own;
-        __syncwarp();
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            if (4 * lane + q < nrc) rc[4 * lane + q] = e;
-            e += v[q];
-        }
-        if (lane == 31) sm.red()[0] = incl;
-    }
-    __syncthreads();
-    const int n = sm.red()[0];
+    const int wtot = lane < NW ? sm.red()[lane] : 0;
+    const int wincl = warp_incl_scan_i(wtot, lane);
+    const int n = __shfl_sync(FULL, wincl, NW - 1);
     if (n > SMALL) {
         __syncthreads();
         sample_row_fin<VEC>(a);
         return;
     }
-    const unsigned lt = (1u << lane) - 1u;
+    int pos = __shfl_sync(FULL, wincl - wtot, warp) + kincl - kc;
 #pragma unroll 1
-    for (int c = 0; c * NT < g4; ++c) {
-        const unsigned m = unsigned(kmask >> (4 * c)) & 15u;
-        if (!__any_sync(FULL, m != 0u)) continue;
-        int pos = rc[c * NW + warp];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) pos += __popc(__ballot_sync(FULL, (m >> q) & 1u) & lt);
-        if (m) {
-            const int g = c * NT + tid;
-            const float4 x = *reinterpret_cast<const float4*>(stg + g * 4);
-            const int e0 = seg[g >> 5] * BLK + (g & 31) * 4;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                if ((m >> q) & 1u) {
-                    sm.lv()[pos] = q_at(x, q);
-                    sm.li()[pos] = e0 + q;
-                    ++pos;
-                }
-            }
-        }
+    while (kmask) {
+        const int bit = __ffsll(kmask) - 1;
+        kmask &= kmask - 1ull;
+        const int g = g0 + (bit >> 2), q = bit & 3;
+        sm.lv()[pos] = stg[4 * g + q];
+        sm.li()[pos] = seg[g >> 5] * BLK + (g & 31) * 4 + q;
+        ++pos;
     }
     __syncthreads();
-    // t_k when more than 32 candidates lie below it: every candidate counts the
-    // candidates at or above it (warps holding candidates; four independent sums).
-    // Otherwise warp 0 finds it by taking the smallest keys away (small_kth).
-    if (n - k >= 32) {
+    // t_k: every candidate counts the candidates at or above it (the warps holding
+    // candidates; broadcast reads, four independent sums); the largest with at least k
+    // is t_k (0 when there are fewer than k: the row has fewer than k positives).
+    {
         uint32_t best = 0u;
         if (warp * 32 < n) {
             const uint4* c4 = reinterpret_cast<const uint4*>(sm.lv());
@@ -1132,12 +1100,8 @@ __global__ void __launch_bounds__(NT, 2) kfirst_kernel(const SampleArgs a) {
             sl.i[q] = sl.in[q] ? sm.li()[e] : 0;
         }
         uint32_t tk = 0u;
-        if (n - k >= 32) {
 #pragma unroll
-            for (int w = 0; w < NW; ++w) tk = max(tk, uint32_t(sm.red()[3 * NW + w]));
-        } else {
-            tk = small_kth(sl, k, keyf);
-        }
+        for (int w = 0; w < NW; ++w) tk = max(tk, uint32_t(sm.red()[3 * NW + w]));
         bool kp[SR];
         float fk = 0.f;
 #pragma unroll
