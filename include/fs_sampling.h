@@ -31,7 +31,9 @@
  *    allocates it (cudaMalloc, in relaxed stream-capture mode, so this may happen
  *    while the stream is being captured; the buffer then belongs to the library, not
  *    to the graph).  fs_workspace_reserve allocates ahead of time and
- *    fs_release_workspaces frees every buffer.  A CUDA graph captured on a stream uses
+ *    fs_release_workspaces frees every buffer.  A new buffer is set to zero on `stream`
+ *    (the scan's claim counters in it must start at zero; each call leaves them at
+ *    zero).  A CUDA graph captured on a stream uses
  *    that stream's buffer on every replay: do not replay it while other calls of
  *    this library on that stream, or other replays of graphs captured on it, may run
  *    at the same time.  No other call allocates, and no state but these buffers
@@ -330,9 +332,11 @@ fs_status fs_workspace_reserve(int32_t batch_in, int32_t vocab, void* stream);
  *    (cudaGetSymbolAddress, which may load the module); make that first call before
  *    any stream capture.
  *  - Sharing: every call on every stream of a device uses the same array, and it keeps
- *    the last call's contents.  Nothing in it needs to start at zero (each call writes
- *    every word it later reads), but calls whose work overlaps on the GPU (other
- *    streams, or graph replays running at the same time) race on it: order them. */
+ *    the last call's contents.  Each call first sets the scan's 16 claim counters in it
+ *    to zero (an asynchronous memset on `stream`, which allocates nothing); every
+ *    other word it reads it has written itself.  Calls whose work overlaps on the GPU
+ *    (other streams, or graph replays running at the same time) race on it: order
+ *    them. */
 fs_status fs_top_k_top_p_sampling_noalloc(const float* probs, int32_t batch_in, int32_t vocab,
                                           const int32_t* indices, int32_t batch_out,
                                           const int32_t* top_k, const float* top_p,

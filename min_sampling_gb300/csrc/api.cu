@@ -260,6 +260,13 @@ fs_status workspace(size_t bytes, void* stream, void** out) {
         e = cudaThreadExchangeStreamCaptureMode(&mode);
         if (ea != cudaSuccess) return cuda_fail(ea);
         if (e != cudaSuccess) return cuda_fail(e);
+        // A new buffer starts at zero: the scan's claim counters must be zero at launch
+        // (each finishing launch sets them back to zero afterwards).
+        e = cudaMemsetAsync(p, 0, want, static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) {
+            cudaFree(p);
+            return cuda_fail(e);
+        }
         if (w.ptr) g_ws_retired.push_back({dev, w.ptr});
         w.ptr = p;
         w.bytes = want;

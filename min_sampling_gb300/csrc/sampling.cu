@@ -56,6 +56,7 @@ struct SampleArgs {
     const uint4* sstat;       // [batch_in][nu] per unit: mass, 0, bad flag, largest key
     int ls;                   // words per row of skey / smass
     int nu;                   // units per row
+    unsigned* sctr;           // the scan's claim counters, set back to zero by output row 0
 };
 
 // ------------------------------------------------------------------ row summaries
@@ -77,7 +78,17 @@ struct ScanArgs {
     uint32_t* key;            // [rows][ls]
     float* mass;              // [rows][ls], rows of probabilities
     uint4* stat;              // [rows][nu]
+    unsigned* ctr;            // [SCAN_CTRS] claim counters of the last units (zero at launch)
+    long long ustatic;        // units [0, ustatic) are dealt round-robin; the rest are claimed
+    int slice;                // claimed units per counter
 };
+
+// The last fifth of the units is not dealt but claimed: warps that finish their share
+// early (SMs that happen to stream faster) take more.  The claimed units are cut into
+// SCAN_CTRS slices, each with its own counter, and warp w claims from slice w % SCAN_CTRS
+// only (one atomic per claimed unit, one more when its slice is used up); the finishing
+// launch sets the counters back to zero once the scan is complete.
+constexpr int SCAN_CTRS = 16;
 
 __host__ __device__ inline int scan_units(int V) { return (V + TB * BLK - 1) / (TB * BLK); }
 __host__ __device__ inline int scan_row_words(int ns) { return (ns + 3) & ~3; }
@@ -86,7 +97,7 @@ size_t scan_workspace_bytes(int batch_in, int vocab) {
     const int shift = seg_shift_for(vocab);
     const int ns = (vocab + (BLK << shift) - 1) / (BLK << shift);
     const size_t ls = size_t(scan_row_words(ns));
-    return size_t(batch_in) * (2 * ls * 4 + size_t(scan_units(vocab)) * 16);
+    return size_t(batch_in) * (2 * ls * 4 + size_t(scan_units(vocab)) * 16) + SCAN_CTRS * sizeof(unsigned);
 }
 
 // Kinds of summary.  SCAN_KEYS (rows of probabilities, paths that draw only from
@@ -122,12 +133,25 @@ __global__ void __launch_bounds__(NT, 4) scan_kernel(const ScanArgs a) {
             for (int j = 0; j < TB; ++j) v[j] = make_float4(fill, fill, fill, fill);
         }
     };
-    long long u = (long long)blockIdx.x * NW + (threadIdx.x >> 5);
+    const long long gw = (long long)blockIdx.x * NW + (threadIdx.x >> 5);
+    const int home = int(gw % SCAN_CTRS);  // the warps of one counter are spread over every SM
+    // The next claimed unit of this warp's counter (total once it is used up);
+    // warp-collective.
+    auto claim = [&]() -> long long {
+        long long c = total;
+        if (lane == 0) {
+            const unsigned i = atomicAdd(&a.ctr[home], 1u);
+            const long long uu = a.ustatic + (long long)home * a.slice + i;
+            if (i < unsigned(a.slice) && uu < total) c = uu;
+        }
+        return __shfl_sync(FULL, c, 0);
+    };
+    long long u = gw < a.ustatic ? gw : claim();
     float4 A[TB], Bv[TB];
     load_unit(u, A);
 #pragma unroll 1
     while (u < total) {
-        const long long un = u + step;
+        const long long un = (u < a.ustatic && u + step < a.ustatic) ? u + step : claim();
         load_unit(un, Bv);
         const int r = int(u / a.nu), q = int(u - (long long)r * a.nu);
         uint32_t km[TB];
@@ -469,6 +493,7 @@ __device__ __forceinline__ void sample_row(const SampleArgs& a) {
 
     grid_dependency_wait();
     allow_dependents();
+    if (FIN && b == 0 && tid < SCAN_CTRS && a.sctr) a.sctr[tid] = 0u;  // the scan is complete
     // ---- a1: row map and parameters (every CTA reads them)
     const int r = a.indices ? a.indices[b] : b;
     const bool row_ok = r >= 0 && r < a.batch_in;
@@ -924,6 +949,7 @@ __global__ void __launch_bounds__(NT, 2) kfirst_kernel(const SampleArgs a) {
     for (int i = tid; i < HBINS; i += NT) sm.hist()[i] = 0u;
     grid_dependency_wait();
     allow_dependents();
+    if (b == 0 && tid < SCAN_CTRS && a.sctr) a.sctr[tid] = 0u;  // the scan is complete
     if (tid == NT - 32) {  // a device-resident offset may be advanced by the kernel before
         *reinterpret_cast<unsigned long long*>(sm.prm() + 6) =
             (a.offsets ? a.offsets[b] : a.offset) + (a.offset_dev ? *a.offset_dev : 0ull);
@@ -1152,8 +1178,13 @@ static fs_status launch_scan(const float* x, int rows, int V, int shift, int ns,
     s.key = reinterpret_cast<uint32_t*>(ws);
     s.mass = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + size_t(rows) * s.ls * 4);
     s.stat = reinterpret_cast<uint4*>(reinterpret_cast<char*>(ws) + 2 * size_t(rows) * s.ls * 4);
+    s.ctr = reinterpret_cast<unsigned*>(reinterpret_cast<char*>(ws) + scan_workspace_bytes(rows, V) -
+                                        SCAN_CTRS * sizeof(unsigned));
+    const long long total = (long long)rows * s.nu;
+    s.ustatic = total - total / 5;
+    s.slice = int((total - s.ustatic + SCAN_CTRS - 1) / SCAN_CTRS);
     int grid = 0;
-    fs_status st = scan_grid((long long)rows * s.nu, grid);
+    fs_status st = scan_grid(total, grid);
     if (st != FS_OK) return st;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(grid), 1, 1);
@@ -1246,6 +1277,9 @@ static fs_status launch_scan_finish(const float* probs, int32_t batch_in, int32_
                   : nullptr;
     a.sstat = ws ? reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(ws) + 2 * size_t(batch_in) * a.ls * 4)
                  : nullptr;
+    a.sctr = ws ? reinterpret_cast<unsigned*>(reinterpret_cast<char*>(ws) + scan_workspace_bytes(batch_in, vocab) -
+                                              SCAN_CTRS * sizeof(unsigned))
+                : nullptr;
     return launch_cluster(fn, p, batch_out, stream, a);
 }
 
@@ -1405,6 +1439,10 @@ fs_status fs_top_k_top_p_sampling_noalloc(const float* probs, int32_t batch_in, 
         }
         const fs_status st = fsd::noalloc_scratch(&scratch);
         if (st != FS_OK) return st;
+        // The scan's claim counters (the last words of its scratch) start at zero.
+        const cudaError_t e = cudaMemsetAsync(static_cast<char*>(scratch) + need - fsd::SCAN_CTRS * sizeof(unsigned), 0,
+                                              fsd::SCAN_CTRS * sizeof(unsigned), static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return fsd::cuda_fail(e);
     }
     // The joint order runs on clusters and needs no scratch; nothing allocates either way.
     return fsd::launch_sample(probs, batch_in, vocab, indices, batch_out, top_k, top_p, min_p, order, seed, offset,
