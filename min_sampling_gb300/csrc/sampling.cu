@@ -89,6 +89,10 @@ struct ScanArgs {
 // only (one atomic per claimed unit, one more when its slice is used up); the finishing
 // launch sets the counters back to zero once the scan is complete.
 constexpr int SCAN_CTRS = 16;
+// The scratch layout: the counters first (at a fixed place whatever the shape, so that
+// a buffer reused for another shape still finds them at zero), then the segment keys,
+// the segment masses and the unit records.
+constexpr size_t SCAN_HEAD = 256;
 
 __host__ __device__ inline int scan_units(int V) { return (V + TB * BLK - 1) / (TB * BLK); }
 __host__ __device__ inline int scan_row_words(int ns) { return (ns + 3) & ~3; }
@@ -97,7 +101,7 @@ size_t scan_workspace_bytes(int batch_in, int vocab) {
     const int shift = seg_shift_for(vocab);
     const int ns = (vocab + (BLK << shift) - 1) / (BLK << shift);
     const size_t ls = size_t(scan_row_words(ns));
-    return size_t(batch_in) * (2 * ls * 4 + size_t(scan_units(vocab)) * 16) + SCAN_CTRS * sizeof(unsigned);
+    return SCAN_HEAD + size_t(batch_in) * (2 * ls * 4 + size_t(scan_units(vocab)) * 16);
 }
 
 // Kinds of summary.  SCAN_KEYS (rows of probabilities, paths that draw only from
@@ -135,23 +139,36 @@ __global__ void __launch_bounds__(NT, 4) scan_kernel(const ScanArgs a) {
     };
     const long long gw = (long long)blockIdx.x * NW + (threadIdx.x >> 5);
     const int home = int(gw % SCAN_CTRS);  // the warps of one counter are spread over every SM
-    // The next claimed unit of this warp's counter (total once it is used up);
-    // warp-collective.
-    auto claim = [&]() -> long long {
-        long long c = total;
-        if (lane == 0) {
-            const unsigned i = atomicAdd(&a.ctr[home], 1u);
-            const long long uu = a.ustatic + (long long)home * a.slice + i;
-            if (i < unsigned(a.slice) && uu < total) c = uu;
-        }
-        return __shfl_sync(FULL, c, 0);
+    // This warp's units: its dealt ones gw, gw + step, ... below ustatic, then claims.  A
+    // claim's atomic is issued one unit ahead (lane 0) and read at the next call, so its
+    // round trip overlaps the unit being streamed.  Warp-collective.
+    long long s_next = gw;
+    bool pending = false;
+    unsigned pend = 0u;
+    auto issue = [&]() {
+        if (lane == 0) pend = atomicAdd(&a.ctr[home], 1u);
+        pending = true;
     };
-    long long u = gw < a.ustatic ? gw : claim();
+    auto next_unit = [&]() -> long long {
+        if (s_next < a.ustatic) {
+            const long long r = s_next;
+            s_next += step;
+            if (s_next >= a.ustatic && !pending) issue();
+            return r;
+        }
+        if (!pending) issue();
+        const long long uu = a.ustatic + (long long)home * a.slice + pend;
+        const long long r = __shfl_sync(FULL, (pend < unsigned(a.slice) && uu < total) ? uu : total, 0);
+        pending = false;
+        if (r < total) issue();
+        return r;
+    };
+    long long u = next_unit();
     float4 A[TB], Bv[TB];
     load_unit(u, A);
 #pragma unroll 1
     while (u < total) {
-        const long long un = (u < a.ustatic && u + step < a.ustatic) ? u + step : claim();
+        const long long un = next_unit();
         load_unit(un, Bv);
         const int r = int(u / a.nu), q = int(u - (long long)r * a.nu);
         uint32_t km[TB];
@@ -1175,11 +1192,11 @@ static fs_status launch_scan(const float* x, int rows, int V, int shift, int ns,
     s.ns = ns;
     s.nu = scan_units(V);
     s.ls = scan_row_words(ns);
-    s.key = reinterpret_cast<uint32_t*>(ws);
-    s.mass = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + size_t(rows) * s.ls * 4);
-    s.stat = reinterpret_cast<uint4*>(reinterpret_cast<char*>(ws) + 2 * size_t(rows) * s.ls * 4);
-    s.ctr = reinterpret_cast<unsigned*>(reinterpret_cast<char*>(ws) + scan_workspace_bytes(rows, V) -
-                                        SCAN_CTRS * sizeof(unsigned));
+    char* body = reinterpret_cast<char*>(ws) + SCAN_HEAD;
+    s.key = reinterpret_cast<uint32_t*>(body);
+    s.mass = reinterpret_cast<float*>(body + size_t(rows) * s.ls * 4);
+    s.stat = reinterpret_cast<uint4*>(body + 2 * size_t(rows) * s.ls * 4);
+    s.ctr = reinterpret_cast<unsigned*>(ws);
     const long long total = (long long)rows * s.nu;
     s.ustatic = total - total / 5;
     s.slice = int((total - s.ustatic + SCAN_CTRS - 1) / SCAN_CTRS);
@@ -1271,15 +1288,11 @@ static fs_status launch_scan_finish(const float* probs, int32_t batch_in, int32_
     a.nsc = p.nsc;
     a.ls = scan_row_words(p.ns);
     a.nu = scan_units(vocab);
-    a.skey = reinterpret_cast<const uint32_t*>(ws);
-    a.smass = (ws && !soft && !kfirst)
-                  ? reinterpret_cast<const float*>(reinterpret_cast<const char*>(ws) + size_t(batch_in) * a.ls * 4)
-                  : nullptr;
-    a.sstat = ws ? reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(ws) + 2 * size_t(batch_in) * a.ls * 4)
-                 : nullptr;
-    a.sctr = ws ? reinterpret_cast<unsigned*>(reinterpret_cast<char*>(ws) + scan_workspace_bytes(batch_in, vocab) -
-                                              SCAN_CTRS * sizeof(unsigned))
-                : nullptr;
+    const char* body = ws ? reinterpret_cast<const char*>(ws) + SCAN_HEAD : nullptr;
+    a.skey = ws ? reinterpret_cast<const uint32_t*>(body) : nullptr;
+    a.smass = (ws && !soft && !kfirst) ? reinterpret_cast<const float*>(body + size_t(batch_in) * a.ls * 4) : nullptr;
+    a.sstat = ws ? reinterpret_cast<const uint4*>(body + 2 * size_t(batch_in) * a.ls * 4) : nullptr;
+    a.sctr = reinterpret_cast<unsigned*>(ws);
     return launch_cluster(fn, p, batch_out, stream, a);
 }
 
@@ -1439,9 +1452,9 @@ fs_status fs_top_k_top_p_sampling_noalloc(const float* probs, int32_t batch_in, 
         }
         const fs_status st = fsd::noalloc_scratch(&scratch);
         if (st != FS_OK) return st;
-        // The scan's claim counters (the last words of its scratch) start at zero.
-        const cudaError_t e = cudaMemsetAsync(static_cast<char*>(scratch) + need - fsd::SCAN_CTRS * sizeof(unsigned), 0,
-                                              fsd::SCAN_CTRS * sizeof(unsigned), static_cast<cudaStream_t>(stream));
+        // The scan's claim counters (the first words of its scratch) start at zero.
+        const cudaError_t e = cudaMemsetAsync(scratch, 0, fsd::SCAN_CTRS * sizeof(unsigned),
+                                              static_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) return fsd::cuda_fail(e);
     }
     // The joint order runs on clusters and needs no scratch; nothing allocates either way.
