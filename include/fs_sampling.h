@@ -303,7 +303,7 @@ const char* fs_last_error_string(void);
 int32_t fs_max_vocab(void);
 
 /* Bytes of scratch that the row summaries of `batch_in` input rows of `vocab` values
- * take (see "Scratch memory" above): 256 bytes of counters, then per row 8 bytes per
+ * take (see "Scratch memory" above): 2 KB of counters, then per row 8 bytes per
  * segment of the launch plan (128 values per segment up to vocab 2^19) and 16 bytes per
  * 512 values.
  * *bytes is a host pointer.  FS_ERR_INVALID_ARG: null bytes, batch_in < 0, vocab < 1. */

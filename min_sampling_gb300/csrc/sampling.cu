@@ -78,7 +78,7 @@ struct ScanArgs {
     uint32_t* key;            // [rows][ls]
     float* mass;              // [rows][ls], rows of probabilities
     uint4* stat;              // [rows][nu]
-    unsigned* ctr;            // [SCAN_CTRS] claim counters of the last units (zero at launch)
+    unsigned* ctr;            // claim counters of the last units, SCAN_CTR_STRIDE words apart (zero at launch)
     long long ustatic;        // units [0, ustatic) are dealt round-robin; the rest are claimed
     int slice;                // claimed units per counter
 };
@@ -92,7 +92,8 @@ constexpr int SCAN_CTRS = 16;
 // The scratch layout: the counters first (at a fixed place whatever the shape, so that
 // a buffer reused for another shape still finds them at zero), then the segment keys,
 // the segment masses and the unit records.
-constexpr size_t SCAN_HEAD = 256;
+constexpr int SCAN_CTR_STRIDE = 32;  // words between counters: one 128-byte line each (different L2 slices)
+constexpr size_t SCAN_HEAD = size_t(SCAN_CTRS) * SCAN_CTR_STRIDE * 4;
 
 __host__ __device__ inline int scan_units(int V) { return (V + TB * BLK - 1) / (TB * BLK); }
 __host__ __device__ inline int scan_row_words(int ns) { return (ns + 3) & ~3; }
@@ -146,7 +147,7 @@ __global__ void __launch_bounds__(NT, 4) scan_kernel(const ScanArgs a) {
     bool pending = false;
     unsigned pend = 0u;
     auto issue = [&]() {
-        if (lane == 0) pend = atomicAdd(&a.ctr[home], 1u);
+        if (lane == 0) pend = atomicAdd(&a.ctr[home * SCAN_CTR_STRIDE], 1u);
         pending = true;
     };
     auto next_unit = [&]() -> long long {
@@ -510,7 +511,7 @@ __device__ __forceinline__ void sample_row(const SampleArgs& a) {
 
     grid_dependency_wait();
     allow_dependents();
-    if (FIN && b == 0 && tid < SCAN_CTRS && a.sctr) a.sctr[tid] = 0u;  // the scan is complete
+    if (FIN && b == 0 && tid < SCAN_CTRS && a.sctr) a.sctr[tid * SCAN_CTR_STRIDE] = 0u;  // the scan is complete
     // ---- a1: row map and parameters (every CTA reads them)
     const int r = a.indices ? a.indices[b] : b;
     const bool row_ok = r >= 0 && r < a.batch_in;
@@ -966,7 +967,7 @@ __global__ void __launch_bounds__(NT, 2) kfirst_kernel(const SampleArgs a) {
     for (int i = tid; i < HBINS; i += NT) sm.hist()[i] = 0u;
     grid_dependency_wait();
     allow_dependents();
-    if (b == 0 && tid < SCAN_CTRS && a.sctr) a.sctr[tid] = 0u;  // the scan is complete
+    if (b == 0 && tid < SCAN_CTRS && a.sctr) a.sctr[tid * SCAN_CTR_STRIDE] = 0u;  // the scan is complete
     if (tid == NT - 32) {  // a device-resident offset may be advanced by the kernel before
         *reinterpret_cast<unsigned long long*>(sm.prm() + 6) =
             (a.offsets ? a.offsets[b] : a.offset) + (a.offset_dev ? *a.offset_dev : 0ull);
@@ -1453,8 +1454,7 @@ fs_status fs_top_k_top_p_sampling_noalloc(const float* probs, int32_t batch_in, 
         const fs_status st = fsd::noalloc_scratch(&scratch);
         if (st != FS_OK) return st;
         // The scan's claim counters (the first words of its scratch) start at zero.
-        const cudaError_t e = cudaMemsetAsync(scratch, 0, fsd::SCAN_CTRS * sizeof(unsigned),
-                                              static_cast<cudaStream_t>(stream));
+        const cudaError_t e = cudaMemsetAsync(scratch, 0, fsd::SCAN_HEAD, static_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) return fsd::cuda_fail(e);
     }
     // The joint order runs on clusters and needs no scratch; nothing allocates either way.
