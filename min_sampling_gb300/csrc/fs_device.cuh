@@ -1470,6 +1470,60 @@ __device__ __forceinline__ unsigned long long locate_in_segment(const float* __r
     return pack_jx(last_j, last_x);
 }
 
+// The same guarded locate over nb consecutive blocks from block b0 of the row (a unit
+// of the scan), warp-collective: the first element with x > low whose running sum
+// passes t, else the last element with x > low (-1 if none), packed with its value.
+template <bool VEC>
+__device__ __forceinline__ unsigned long long locate_in_blocks(const float* __restrict__ row, int V, int b0, int nb,
+                                                               float low, float t, int lane) {
+    float run = 0.f;
+    int last_j = -1;
+    float last_x = 0.f;
+#pragma unroll 1
+    for (int it = 0; it < nb; ++it) {
+        const int base = (b0 + it) * BLK + lane * 4;
+        const float4 v = load4<VEC, true>(row, V, base, 0.f);
+        float w[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float x = q_at(v, q);
+            w[q] = x > low ? x : 0.f;
+        }
+        const float lsum = (w[0] + w[1]) + (w[2] + w[3]);
+        const bool any = (w[0] > 0.f) | (w[1] > 0.f) | (w[2] > 0.f) | (w[3] > 0.f);
+        const float incl = warp_incl_scan(lsum, lane);
+        const unsigned hit = __ballot_sync(FULL, any && (run + incl > t));
+        const unsigned elig = __ballot_sync(FULL, any);
+        if (elig) {
+            const int l = 31 - __clz(elig);
+            int lq = 0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (w[q] > 0.f) lq = q;
+            const int lq_l = __shfl_sync(FULL, lq, l);
+            last_j = __shfl_sync(FULL, base, l) + lq_l;
+            last_x = __shfl_sync(FULL, q_at(v, lq), l);
+        }
+        if (hit) {
+            const int l = __ffs(hit) - 1;
+            int pq = -1, lastq = 0;
+            float acc = run + (incl - lsum);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (w[q] > 0.f) {
+                    acc += w[q];
+                    lastq = q;
+                    if (pq < 0 && acc > t) pq = q;
+                }
+            }
+            if (pq < 0) pq = lastq;
+            return pack_jx(__shfl_sync(FULL, base + pq, l), __shfl_sync(FULL, q_at(v, pq), l));
+        }
+        run += __shfl_sync(FULL, incl, 31);
+    }
+    return pack_jx(last_j, last_x);
+}
+
 // First segment in [a, b) whose running mass over mass[] exceeds t; if none, the last
 // segment with positive mass (-1 if none).  Packed with the mass before it.
 // Warp-collective.

@@ -234,14 +234,16 @@ __global__ void __launch_bounds__(NT, 4) scan_kernel(const ScanArgs a) {
 // leave them in a one-CTA cluster: segment keys (and, with `masses`, segment masses)
 // and part[0] = (M; V as the bound of the positive count, bad flag, largest key), and
 // with `uhist` the histogram of the units' largest keys (key >> 21) added into uhist,
-// which the caller cleared (a block barrier orders the clear before the counts).  M
+// which the caller cleared (a block barrier orders the clear before the counts), and
+// with `umass` / `ukey` each unit's mass and largest key.  M
 // is the sum of the unit masses in a fixed order (thread t adds units t, t + NT, ...
 // in turn, then a tree over the lanes and the warps in order).  Every thread issues
 // all of its loads before it uses any (one round trip to L2).  The summary was
 // written by the previous launch, so it is read through L2 (ld.global.cg).
 // Block-collective; ends with a block barrier.
 __device__ __forceinline__ void load_summary(const SampleArgs& a, int r, Smem sm, bool masses, int warp, int lane,
-                                             int tid, uint32_t* uhist = nullptr) {
+                                             int tid, uint32_t* uhist = nullptr, float* umass = nullptr,
+                                             uint32_t* ukey = nullptr) {
     const uint4* key4 = reinterpret_cast<const uint4*>(a.skey + size_t(r) * a.ls);
     const uint4* mass4 = reinterpret_cast<const uint4*>(a.smass + size_t(r) * a.ls);
     const uint4* st = a.sstat + size_t(r) * a.nu;
@@ -278,6 +280,10 @@ __device__ __forceinline__ void load_summary(const SampleArgs& a, int r, Smem sm
             bd |= v[h].z != 0u;
             km = max(km, v[h].w);
             if (uhist && i < a.nu) atomicAdd(&uhist[min(uint32_t(HBINS - 1), v[h].w >> 21)], 1u);
+            if (umass && i < a.nu) {
+                umass[i] = __uint_as_float(v[h].x);
+                ukey[i] = v[h].w;
+            }
         }
     }
     ms = warp_sum(ms);
@@ -936,6 +942,222 @@ FS_COLD __device__ void sample_row_fin(const SampleArgs& a) {
 // chains, not memory, set the time.  Any other row (a bad row index, no top-k filter,
 // fewer units than k, segments of several blocks, more than KF_LIVE live segments or
 // more than SMALL candidates) takes the general finishing path, out of line.
+// ------------------------------------------------------------------ lean joint finish
+
+// Each unit's mass above `low` (a pass over the row, from L2, by the whole CTA): warp w
+// takes a contiguous share of the units, two units' loads in flight; units whose
+// largest key is at most low's are not read (mass 0).  Returns the total, summed in a
+// fixed order (each warp its share in order, then the warps in order).  Block-collective.
+template <bool VEC>
+__device__ __forceinline__ float unit_pass(const float* __restrict__ row, int V, int nu, float low, float* umass,
+                                           const uint32_t* ukey, Smem sm, int warp, int lane) {
+    const uint32_t klow = prob_key(low);
+    int u0, u1;
+    warp_range(nu, warp, u0, u1);
+    auto load = [&](int u, float4* v) {
+        const bool on = u < u1 && ukey[u] > klow;
+#pragma unroll
+        for (int j = 0; j < TB; ++j)
+            v[j] = on ? load4<VEC, true>(row, V, (u * TB + j) * BLK + lane * 4, 0.f) : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    float4 A[TB], Bv[TB];
+    load(u0, A);
+#pragma unroll 1
+    for (int u = u0; u < u1; ++u) {
+        load(u + 1, Bv);
+        float sacc = 0.f;
+#pragma unroll
+        for (int j = 0; j < TB; ++j)
+            sacc += ((A[j].x > low ? A[j].x : 0.f) + (A[j].y > low ? A[j].y : 0.f)) +
+                    ((A[j].z > low ? A[j].z : 0.f) + (A[j].w > low ? A[j].w : 0.f));
+        sacc = warp_sum(sacc);
+        if (lane == 0) umass[u] = sacc;
+#pragma unroll
+        for (int j = 0; j < TB; ++j) A[j] = Bv[j];
+    }
+    __syncwarp();
+    const float ws = warp_ordered_sum(umass, u0, u1, lane);
+    float* rf = reinterpret_cast<float*>(sm.red()) + 64;
+    if (lane == 0) rf[warp] = ws;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) tot += rf[w];
+    __syncthreads();
+    return tot;
+}
+
+// The unit holding target t in the running sum of umass[0, nu) (index order): the first
+// unit with positive mass whose running sum passes t, else the last unit with positive
+// mass (-1 if none) ([blog] implementation details: the scan is not monotone in floating
+// point, so the pick is forced onto an eligible unit).  `before` = the running sum up to
+// it.  Thread t sums a contiguous range; one block scan.  Block-collective.
+__device__ __forceinline__ int locate_unit(const float* umass, int nu, float t, Smem sm, int tid, int warp, int lane,
+                                           float& before) {
+    const int c = (nu + NT - 1) / NT;
+    const int a0 = min(nu, tid * c), a1 = min(nu, a0 + c);
+    float own = 0.f;
+#pragma unroll 1
+    for (int i = a0; i < a1; ++i) own += umass[i];
+    const float incl = warp_incl_scan(own, lane);
+    float* rf = reinterpret_cast<float*>(sm.red()) + 64;
+    int* ri = sm.red() + 80;
+    if (lane == 31) rf[warp] = incl;
+    if (tid == 0) {
+        ri[0] = INT_BIG;  // first hit
+        ri[1] = -1;       // last positive unit
+    }
+    __syncthreads();
+    float wbase = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) wbase += w < warp ? rf[w] : 0.f;
+    float run = wbase + incl - own;
+    int hit = INT_BIG, lastpos = -1;
+#pragma unroll 1
+    for (int i = a0; i < a1; ++i) {
+        const float m = umass[i];
+        if (m > 0.f) {
+            lastpos = i;
+            if (hit == INT_BIG && run + m > t) hit = i;
+        }
+        run += m;
+    }
+    if (hit != INT_BIG) atomicMin(&ri[0], hit);
+    if (lastpos >= 0) atomicMax(&ri[1], lastpos);
+    __syncthreads();
+    const int pick = ri[0] != INT_BIG ? ri[0] : ri[1];
+    if (pick >= a0 && pick < a1) {  // the owner of the pick writes the sum before it
+        float bsum = wbase + incl - own;
+        for (int i = a0; i < pick; ++i) bsum += umass[i];
+        rf[8] = bsum;
+    }
+    __syncthreads();
+    before = rf[8];
+    __syncthreads();
+    return pick;
+}
+
+// The rejection rounds of the joint order ([blog] dual-pivot rejection sampling) for a
+// row whose top-k bound uk <= t_k leaves n >= k candidates, all in the list lv/li[0, n)
+// (every element >= uk, in index order).  f(tau) needs the count and mass above tau only
+// for tau >= uk, and every element above such a tau is in the list; below uk at least n
+// >= k elements lie above tau, so f fails there without a reduction.  While `low` >= uk
+// the draw is over the list; below uk it needs each unit's mass above low, from the
+// summary for low = 0 and from a pass over the row (unit_pass) after a round that leaves
+// low below uk.  Block-collective; thread 0 writes the outputs.
+template <bool VEC>
+__device__ __forceinline__ void joint_rounds(const SampleArgs& a, Smem sm, const float* row, int b, int k, uint32_t uk,
+                                             int n, const float* uni, float* umass, const uint32_t* ukey, int tid,
+                                             int warp, int lane) {
+    const float tp = __uint_as_float(sm.prm()[1]);
+    const float mp = __uint_as_float(sm.prm()[2]);
+    const unsigned long long seed_b = *reinterpret_cast<const unsigned long long*>(sm.prm() + 4);
+    const unsigned long long offset_b = *reinterpret_cast<const unsigned long long*>(sm.prm() + 6);
+    const uint32_t stream_b = a.seeds ? 0u : uint32_t(b);
+    const float M = sm.part()[0].f[0];
+    const bool any_bad = sm.part()[0].u[1] != 0u;
+    const float rowmax = __uint_as_float(sm.part()[0].u[2]);
+    Pred f;
+    f.single = a.single_pivot != 0;
+    f.k_on = true;
+    f.k = k;
+    f.p_on = tp < 1.f;
+    f.m_on = mp > 0.f;
+    f.pthr = tp * M;
+    f.t32 = 0.f;
+    bool valid = !isnan(tp) && !isnan(mp) && !any_bad && M > 0.f && M <= 3.402823466e38f;
+    if (f.m_on) {
+        f.t32 = __double2float_ru(double(mp) * double(rowmax));
+        if (!(rowmax >= f.t32)) valid = false;
+    }
+    const float ukf = __uint_as_float(uk);
+    int* st = sm.red() + 88;                                   // [4] round results (ints)
+    float* sf = reinterpret_cast<float*>(sm.red()) + 92;      // [4] round results (floats)
+    float low = 0.f, high = rowmax, S_low = M;
+    bool listmode = false;  // low = 0 < uk
+    int token = -1, rounds = 0;
+#pragma unroll 1
+    for (int round = 0; valid && round < R_MAX; ++round) {
+        const float u = round < 32 ? uni[round] : sampler_uniform(seed_b, offset_b, stream_b, uint32_t(round));
+        const float t = u * S_low;
+        // ---- draw ([blog] inverse transform over the tokens above low)
+        if (listmode) {
+            if (warp == 0) {
+                const int e = locate_in_list(sm.lv(), n, low, t, lane);
+                if (lane == 0) {
+                    st[0] = e >= 0 ? sm.li()[e] : -1;
+                    sf[0] = e >= 0 ? sm.lv()[e] : 0.f;
+                }
+            }
+        } else {
+            float before = 0.f;
+            const int un = locate_unit(umass, a.nu, t, sm, tid, warp, lane, before);
+            if (warp == 0) {
+                unsigned long long jx = pack_jx(-1, 0.f);
+                if (un >= 0) jx = locate_in_blocks<VEC>(row, a.V, un * TB, TB, low, fmaxf(t - before, 0.f), lane);
+                if (lane == 0) {
+                    st[0] = unpack_j(jx);
+                    sf[0] = unpack_x(jx);
+                }
+            }
+        }
+        __syncthreads();
+        const int j = st[0];
+        const float pivot1 = sf[0];
+        if (j < 0) break;
+        const float pivot2 = f.pivot2(pivot1, high);
+        // ---- f at both pivots, from the list when the pivot is >= uk ([blog] dual pivot)
+        if (warp == 0) {
+            float m1 = 0.f, m2 = 0.f;
+            int c1 = 0, c2 = 0;
+            for (int i = lane; i < n; i += 32) {
+                const float x = sm.lv()[i];
+                const bool g1 = x > pivot1, g2 = x > pivot2;
+                m1 += g1 ? x : 0.f;
+                m2 += g2 ? x : 0.f;
+                c1 += g1;
+                c2 += g2;
+            }
+            m1 = warp_sum(m1);
+            m2 = warp_sum(m2);
+            c1 = warp_sum_i(c1);
+            c2 = warp_sum_i(c2);
+            const bool f1 = pivot1 >= ukf && f(c1, m1, pivot1);
+            const bool f2 = pivot2 >= ukf && f(c2, m2, pivot2);
+            if (lane == 0) {
+                st[1] = f1 ? 1 : (f2 ? 2 : 3);
+                sf[1] = m1;
+                sf[2] = m2;
+            }
+        }
+        __syncthreads();
+        const int kase = st[1];
+        const float m1 = sf[1], m2 = sf[2];
+        __syncthreads();
+        if (kase == 1) {
+            token = j;
+            rounds = round + 1;
+            break;
+        }
+        if (kase == 2) {
+            low = pivot1;
+            high = pivot2;
+            S_low = m1;
+        } else {
+            low = pivot2;
+            S_low = m2;
+        }
+        listmode = low >= ukf;
+        if (!listmode) S_low = unit_pass<VEC>(row, a.V, a.nu, low, umass, ukey, sm, warp, lane);
+        if (round == R_MAX - 1) rounds = R_MAX;
+    }
+    if (tid == 0) {
+        a.out_token[b] = token >= 0 ? token : -1;
+        a.out_valid[b] = token >= 0 ? 1 : 0;
+        if (a.out_rounds) a.out_rounds[b] = token >= 0 ? rounds : (valid ? R_MAX : 0);
+    }
+}
+
 constexpr int KF_LIVE = 112;  // live segments the lean finish stages (fpt = 15 float4 per thread at most)
 
 // The staging area of the lean finish (KF_LIVE blocks), after the carve-up.
@@ -944,7 +1166,7 @@ __device__ __forceinline__ float* kfirst_stage(Smem sm) {
     return reinterpret_cast<float*>(smem_raw + Layout(sm.ns).total());
 }
 
-template <bool VEC>
+template <bool VEC, bool JOINT>
 __global__ void __launch_bounds__(NT, 2) kfirst_kernel(const SampleArgs a) {
     const int b = int(cluster_id_x());
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -974,7 +1196,8 @@ __global__ void __launch_bounds__(NT, 2) kfirst_kernel(const SampleArgs a) {
     }
     // ---- (1) the summary, with the histogram of the unit maxima; the bound
     if (row_ok) {
-        load_summary(a, r, sm, false, warp, lane, tid, sm.hist());  // ends with a block barrier
+        load_summary(a, r, sm, false, warp, lane, tid, sm.hist(), JOINT ? sm.mass(1) : nullptr,
+                     JOINT ? reinterpret_cast<uint32_t*>(sm.mass(2)) : nullptr);  // ends with a block barrier
     } else {
         __syncthreads();
     }
@@ -1067,7 +1290,7 @@ __global__ void __launch_bounds__(NT, 2) kfirst_kernel(const SampleArgs a) {
     const int wtot = lane < NW ? sm.red()[lane] : 0;
     const int wincl = warp_incl_scan_i(wtot, lane);
     const int n = __shfl_sync(FULL, wincl, NW - 1);
-    if (n > SMALL) {
+    if (n > SMALL || (JOINT && n < k)) {  // joint: below uk, f must fail for lack of k
         __syncthreads();
         sample_row_fin<VEC>(a);
         return;
@@ -1083,6 +1306,11 @@ __global__ void __launch_bounds__(NT, 2) kfirst_kernel(const SampleArgs a) {
         ++pos;
     }
     __syncthreads();
+    if (JOINT) {
+        joint_rounds<VEC>(a, sm, row, b, k, uk, n, uni, sm.mass(1), reinterpret_cast<const uint32_t*>(sm.mass(2)), tid,
+                          warp, lane);
+        return;
+    }
     // t_k: every candidate counts the candidates at or above it (the warps holding
     // candidates; broadcast reads, four independent sums); the largest with at least k
     // is t_k (0 when there are fewer than k: the row has fewer than k positives).
@@ -1228,9 +1456,11 @@ static fs_status launch_scan_finish(const float* probs, int32_t batch_in, int32_
                                     const uint64_t* offsets, const uint64_t* offset_dev, int32_t pivots, bool soft,
                                     const float* temperature, bool vec, void* fixed_ws = nullptr) {
     const bool kfirst = order == FS_ORDER_TOP_K_FIRST && top_k;
+    const bool kjoint = !soft && order == FS_ORDER_JOINT && top_k;
     auto fin_fn = [&]() -> void (*)(SampleArgs) {
         if (soft) return vec ? sample_kernel<true, true, true> : sample_kernel<false, true, true>;
-        if (kfirst) return vec ? kfirst_kernel<true> : kfirst_kernel<false>;
+        if (kfirst) return vec ? kfirst_kernel<true, false> : kfirst_kernel<false, false>;
+        if (kjoint) return vec ? kfirst_kernel<true, true> : kfirst_kernel<false, true>;
         return vec ? sample_kernel<true, false, true> : sample_kernel<false, false, true>;
     };
     void (*fn)(SampleArgs) = fin_fn();
@@ -1245,7 +1475,7 @@ static fs_status launch_scan_finish(const float* probs, int32_t batch_in, int32_
     p.shift = seg_shift_for(vocab);
     p.ns = (vocab + (BLK << p.shift) - 1) / (BLK << p.shift);
     p.nsc = (p.ns + 3) & ~3;
-    p.smem = (kfirst && !soft) ? kfirst_smem(p.ns) : Layout(p.ns).total();
+    p.smem = ((kfirst || kjoint) && !soft) ? kfirst_smem(p.ns) : Layout(p.ns).total();
     p.per_sm = 0;
     if (p.smem > optin) return FS_ERR_UNSUPPORTED;
     void* ws = nullptr;
@@ -1291,7 +1521,7 @@ static fs_status launch_scan_finish(const float* probs, int32_t batch_in, int32_
     a.nu = scan_units(vocab);
     const char* body = ws ? reinterpret_cast<const char*>(ws) + SCAN_HEAD : nullptr;
     a.skey = ws ? reinterpret_cast<const uint32_t*>(body) : nullptr;
-    a.smass = (ws && !soft && !kfirst) ? reinterpret_cast<const float*>(body + size_t(batch_in) * a.ls * 4) : nullptr;
+    a.smass = (ws && !soft && !kfirst) ? reinterpret_cast<const float*>(body + size_t(batch_in) * a.ls * 4) : nullptr;  // joint and unfiltered: segment masses
     a.sstat = ws ? reinterpret_cast<const uint4*>(body + 2 * size_t(batch_in) * a.ls * 4) : nullptr;
     a.sctr = reinterpret_cast<unsigned*>(ws);
     return launch_cluster(fn, p, batch_out, stream, a);
@@ -1319,7 +1549,8 @@ static fs_status launch_sample(const float* probs, int32_t batch_in, int32_t voc
     // Those run as a scan of the input rows and a finishing launch per output row
     // (masses of logits depend on the temperature, so sampling logits without filters
     // stays on the clusters).
-    const bool fin = (order == FS_ORDER_TOP_K_FIRST && top_k) || (!soft && !top_k && !top_p && !min_p);
+    const bool fin = (order == FS_ORDER_TOP_K_FIRST && top_k) || (!soft && !top_k && !top_p && !min_p) ||
+                     (!soft && order == FS_ORDER_JOINT && top_k);
     if (fin) return launch_scan_finish(probs, batch_in, vocab, indices, batch_out, top_k, top_p, min_p, order, seed,
                                        offset, out_token, out_valid, out_rounds, stream, seeds, offsets, offset_dev,
                                        pivots, soft, temperature, vec, fixed_ws);
