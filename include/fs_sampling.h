@@ -21,10 +21,12 @@
  *  - Every pointer argument is a DEVICE pointer owned by the caller, unless stated.
  *    Each call is asynchronous on `stream` (a cudaStream_t passed as void*; NULL is
  *    the legacy default stream) and may be made from several host threads at once.
- *  - Scratch memory.  The top-k-first samplers and fs_sampling_from_probs run as two
- *    launches: a scan that reads every input row once, spread evenly over the GPU, and
- *    writes a small summary of each row (a few bytes per 128 values), then one CTA per
- *    output row that finishes the row from that summary.  The summaries live in a
+ *  - Scratch memory.  The top-k-first samplers, the joint order with a top-k filter
+ *    on rows of probabilities (fs_top_k_top_p_sampling*, fs_top_k_sampling) and
+ *    fs_sampling_from_probs run as two launches: a scan that reads every input row
+ *    once, spread evenly over the GPU, and writes a small summary of each row (a few
+ *    bytes per 128 values; the joint order adds one byte per 4 values), then one CTA
+ *    per output row that finishes the row from that summary.  The summaries live in a
  *    scratch buffer that the library owns, one per (device, stream): calls on one
  *    stream run in order and share it; calls on different streams do not touch each
  *    other's.  The first call that needs more than the stream's buffer holds
@@ -275,9 +277,10 @@ fs_status fs_chain_speculative_sampling(const float* draft_probs, const int32_t*
  * top-k-first entries (fs_top_k_top_p_sampling*, order top-k-first) and of
  * fs_sampling_from_probs: a scan of every row with *ctas_per_sm CTAs on every SM,
  * then one CTA per row (*cluster = 1) that finishes the row from its summary
- * (*segments_per_cta = the row's segments).  FS_ORDER_JOINT gives that of the joint
- * order and of fs_top_k_sampling, fs_top_p_sampling and fs_min_p_sampling, whose
- * rejection rounds pass over the row several times on a cluster of CTAs, for rows of
+ * (*segments_per_cta = the row's segments); the joint order with a top-k filter on
+ * rows of probabilities runs the same two launches.  FS_ORDER_JOINT gives the plan of
+ * the cluster kernel: fs_top_p_sampling and fs_min_p_sampling, whose rejection rounds
+ * pass over the row several times on a cluster of CTAs, for rows of
  * probabilities that are 16-byte aligned with vocab % 4 = 0 (other rows run a
  * scalar-load build of the same kernel).  Outputs (host pointers): CTAs per row
  * (*cluster), elements per segment, segments per CTA and the most CTAs resident on
@@ -303,9 +306,9 @@ const char* fs_last_error_string(void);
 int32_t fs_max_vocab(void);
 
 /* Bytes of scratch that the row summaries of `batch_in` input rows of `vocab` values
- * take (see "Scratch memory" above): 2 KB of counters, then per row 8 bytes per
- * segment of the launch plan (128 values per segment up to vocab 2^19) and 16 bytes per
- * 512 values.
+ * take on the path that needs the most (see "Scratch memory" above): 2 KB of counters,
+ * then per row 8 bytes per segment of the launch plan (128 values per segment up to
+ * vocab 2^19), 16 bytes per 512 values and, for the joint order, 1 byte per 4 values.
  * *bytes is a host pointer.  FS_ERR_INVALID_ARG: null bytes, batch_in < 0, vocab < 1. */
 fs_status fs_workspace_bytes(int32_t batch_in, int32_t vocab, size_t* bytes);
 
@@ -321,14 +324,15 @@ fs_status fs_workspace_reserve(int32_t batch_in, int32_t vocab, void* stream);
  * or allocator that must see every device allocation; a process that must not risk
  * the device-wide synchronisation an allocation can cause in the middle of a decode
  * step.  This entry takes the same arguments and gives the same results as
- * fs_top_k_top_p_sampling, but the top-k-first order keeps its row summaries in one
- * fixed array of FS_NOALLOC_SCRATCH_BYTES (8 MiB) that is part of the library's
- * module image: every device that loads the library holds it until the process exits,
- * and no call allocates or frees anything (the joint order needs no scratch at all).
- *  - Limit: fs_workspace_bytes(batch_in, vocab) must be at most
- *    FS_NOALLOC_SCRATCH_BYTES (for example 64 rows of 151936 values take 0.9 MB, 256
- *    rows of 256000 values 6.1 MB); larger batches return FS_ERR_UNSUPPORTED and
- *    fs_last_error_string() says why.
+ * fs_top_k_top_p_sampling, but both orders keep their row summaries in one fixed
+ * array of FS_NOALLOC_SCRATCH_BYTES (8 MiB) that is part of the library's module
+ * image: every device that loads the library holds it until the process exits, and no
+ * call allocates or frees anything.
+ *  - Limit: the summaries of the call must fit FS_NOALLOC_SCRATCH_BYTES: 64 rows of
+ *    151936 values take 0.9 MB in the top-k-first order and 3.3 MB in the joint order
+ *    (which adds one byte per 4 values), 256 rows of 256000 values 6.1 MB in the
+ *    top-k-first order (too many for the joint order); larger batches return
+ *    FS_ERR_UNSUPPORTED and fs_last_error_string() says why.
  *  - Set-up: the first call on a device looks the array's device address up
  *    (cudaGetSymbolAddress, which may load the module); make that first call before
  *    any stream capture.

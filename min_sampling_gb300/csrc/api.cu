@@ -321,7 +321,7 @@ const char* fs_last_error_string(void) { return fsd::g_last_error; }
 fs_status fs_workspace_bytes(int32_t batch_in, int32_t vocab, size_t* bytes) {
     if (!bytes || batch_in < 0 || vocab < 1) return FS_ERR_INVALID_ARG;
     if (vocab > FS_MAX_VOCAB) return FS_ERR_UNSUPPORTED;
-    *bytes = fsd::scan_workspace_bytes(batch_in, vocab);
+    *bytes = fsd::scan_workspace_bytes(batch_in, vocab, true);
     return FS_OK;
 }
 

@@ -1470,57 +1470,71 @@ __device__ __forceinline__ unsigned long long locate_in_segment(const float* __r
     return pack_jx(last_j, last_x);
 }
 
-// The same guarded locate over nb consecutive blocks from block b0 of the row (a unit
-// of the scan), warp-collective: the first element with x > low whose running sum
-// passes t, else the last element with x > low (-1 if none), packed with its value.
+// One block of the guarded locate ([blog] implementation details): the lane's four
+// values v are elements base .. base + 3 of the row (the lanes in index order) and are
+// eligible when above low.  Returns true, with the pick packed in jx, when the running
+// sum passes t inside the block; otherwise adds the block's eligible mass to run and
+// remembers its last eligible element.  Warp-collective.
+__device__ __forceinline__ bool locate_step(const float4& v, int base, float low, float t, float& run, int& last_j,
+                                            float& last_x, unsigned long long& jx, int lane) {
+    float w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float x = q_at(v, q);
+        w[q] = x > low ? x : 0.f;
+    }
+    const float lsum = (w[0] + w[1]) + (w[2] + w[3]);
+    const bool any = (w[0] > 0.f) | (w[1] > 0.f) | (w[2] > 0.f) | (w[3] > 0.f);
+    const float incl = warp_incl_scan(lsum, lane);
+    const unsigned hit = __ballot_sync(FULL, any && (run + incl > t));
+    const unsigned elig = __ballot_sync(FULL, any);
+    if (elig) {
+        const int l = 31 - __clz(elig);
+        int lq = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (w[q] > 0.f) lq = q;
+        const int lq_l = __shfl_sync(FULL, lq, l);
+        last_j = __shfl_sync(FULL, base, l) + lq_l;
+        last_x = __shfl_sync(FULL, q_at(v, lq), l);
+    }
+    if (hit) {
+        const int l = __ffs(hit) - 1;
+        int pq = -1, lastq = 0;
+        float acc = run + (incl - lsum);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if (w[q] > 0.f) {
+                acc += w[q];
+                lastq = q;
+                if (pq < 0 && acc > t) pq = q;
+            }
+        }
+        if (pq < 0) pq = lastq;
+        jx = pack_jx(__shfl_sync(FULL, base + pq, l), __shfl_sync(FULL, q_at(v, pq), l));
+        return true;
+    }
+    run += __shfl_sync(FULL, incl, 31);
+    return false;
+}
+
+// The guarded locate over the TB blocks of unit un of the row (a unit of the scan):
+// the first element above low whose running sum passes t, else the last element above
+// low (-1 if none), packed with its value.  Every block's load is issued before the
+// first is scanned.  Warp-collective.
 template <bool VEC>
-__device__ __forceinline__ unsigned long long locate_in_blocks(const float* __restrict__ row, int V, int b0, int nb,
-                                                               float low, float t, int lane) {
+__device__ __forceinline__ unsigned long long locate_in_unit(const float* __restrict__ row, int V, int un, float low,
+                                                             float t, int lane) {
+    float4 v[TB];
+#pragma unroll
+    for (int j = 0; j < TB; ++j) v[j] = load4<VEC, true>(row, V, (un * TB + j) * BLK + lane * 4, 0.f);
     float run = 0.f;
     int last_j = -1;
     float last_x = 0.f;
-#pragma unroll 1
-    for (int it = 0; it < nb; ++it) {
-        const int base = (b0 + it) * BLK + lane * 4;
-        const float4 v = load4<VEC, true>(row, V, base, 0.f);
-        float w[4];
+    unsigned long long jx = 0ull;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float x = q_at(v, q);
-            w[q] = x > low ? x : 0.f;
-        }
-        const float lsum = (w[0] + w[1]) + (w[2] + w[3]);
-        const bool any = (w[0] > 0.f) | (w[1] > 0.f) | (w[2] > 0.f) | (w[3] > 0.f);
-        const float incl = warp_incl_scan(lsum, lane);
-        const unsigned hit = __ballot_sync(FULL, any && (run + incl > t));
-        const unsigned elig = __ballot_sync(FULL, any);
-        if (elig) {
-            const int l = 31 - __clz(elig);
-            int lq = 0;
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                if (w[q] > 0.f) lq = q;
-            const int lq_l = __shfl_sync(FULL, lq, l);
-            last_j = __shfl_sync(FULL, base, l) + lq_l;
-            last_x = __shfl_sync(FULL, q_at(v, lq), l);
-        }
-        if (hit) {
-            const int l = __ffs(hit) - 1;
-            int pq = -1, lastq = 0;
-            float acc = run + (incl - lsum);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                if (w[q] > 0.f) {
-                    acc += w[q];
-                    lastq = q;
-                    if (pq < 0 && acc > t) pq = q;
-                }
-            }
-            if (pq < 0) pq = lastq;
-            return pack_jx(__shfl_sync(FULL, base + pq, l), __shfl_sync(FULL, q_at(v, pq), l));
-        }
-        run += __shfl_sync(FULL, incl, 31);
-    }
+    for (int j = 0; j < TB; ++j)
+        if (locate_step(v[j], (un * TB + j) * BLK + lane * 4, low, t, run, last_j, last_x, jx, lane)) return jx;
     return pack_jx(last_j, last_x);
 }
 

@@ -38,8 +38,8 @@ fs_status make_plan(int rows, int vocab, const void* fn, bool single_pass, Plan&
 fs_status workspace(size_t bytes, void* stream, void** out);
 
 // Bytes of scratch that the row summaries of `batch_in` rows of `vocab` values take
-// (scan_kernel, sampling.cu).
-size_t scan_workspace_bytes(int batch_in, int vocab);
+// (scan_kernel, sampling.cu); `codes`: with the joint order's run codes.
+size_t scan_workspace_bytes(int batch_in, int vocab, bool codes);
 
 // Opt the kernel into the device's maximum dynamic shared memory (once per device).
 fs_status prepare_kernel(const void* fn);

@@ -54,9 +54,14 @@ struct SampleArgs {
     const uint32_t* skey;     // [batch_in][ls] segment maxima (order keys)
     const float* smass;       // [batch_in][ls] segment masses (rows of probabilities)
     const uint4* sstat;       // [batch_in][nu] per unit: mass, 0, bad flag, largest key
+    const uint32_t* scode;    // [batch_in][nu][32] run codes (SCAN_JOINT), nullable
     int ls;                   // words per row of skey / smass
     int nu;                   // units per row
     unsigned* sctr;           // the scan's claim counters, set back to zero by output row 0
+    // Joint-order finish (kjoint_kernel): 1 = the whole row is staged in shared memory;
+    // 0 = candidate list, then a list of the elements above low of a.jy4 float4 runs.
+    int jmode;
+    int jy4;
 };
 
 // ------------------------------------------------------------------ row summaries
@@ -78,6 +83,8 @@ struct ScanArgs {
     uint32_t* key;            // [rows][ls]
     float* mass;              // [rows][ls], rows of probabilities
     uint4* stat;              // [rows][nu]
+    uint32_t* code;           // [rows][nu][32] SCAN_JOINT: lane l's word of unit q holds in byte j the code of
+                              // run (q TB + j) 32 + l (the float4 of elements 4 times that)
     unsigned* ctr;            // claim counters of the last units, SCAN_CTR_STRIDE words apart (zero at launch)
     long long ustatic;        // units [0, ustatic) are dealt round-robin; the rest are claimed
     int slice;                // claimed units per counter
@@ -91,25 +98,29 @@ struct ScanArgs {
 constexpr int SCAN_CTRS = 16;
 // The scratch layout: the counters first (at a fixed place whatever the shape, so that
 // a buffer reused for another shape still finds them at zero), then the segment keys,
-// the segment masses and the unit records.
+// the segment masses, the unit records and the run codes.
 constexpr int SCAN_CTR_STRIDE = 32;  // words between counters: one 128-byte line each (different L2 slices)
 constexpr size_t SCAN_HEAD = size_t(SCAN_CTRS) * SCAN_CTR_STRIDE * 4;
 
 __host__ __device__ inline int scan_units(int V) { return (V + TB * BLK - 1) / (TB * BLK); }
 __host__ __device__ inline int scan_row_words(int ns) { return (ns + 3) & ~3; }
 
-size_t scan_workspace_bytes(int batch_in, int vocab) {
+size_t scan_workspace_bytes(int batch_in, int vocab, bool codes) {
     const int shift = seg_shift_for(vocab);
     const int ns = (vocab + (BLK << shift) - 1) / (BLK << shift);
     const size_t ls = size_t(scan_row_words(ns));
-    return SCAN_HEAD + size_t(batch_in) * (2 * ls * 4 + size_t(scan_units(vocab)) * 16);
+    return SCAN_HEAD + size_t(batch_in) * (2 * ls * 4 + size_t(scan_units(vocab)) * (16 + (codes ? 32 * 4 : 0)));
 }
 
 // Kinds of summary.  SCAN_KEYS (rows of probabilities, paths that draw only from
 // gathered candidates): segment maxima and unit totals.  SCAN_MASSES: segment masses
 // as well (a draw over the whole row).  SCAN_LOGITS: maxima as logit keys, no masses
-// (they depend on the temperature).
-enum : int { SCAN_KEYS = 0, SCAN_MASSES = 1, SCAN_LOGITS = 2 };
+// (they depend on the temperature).  SCAN_JOINT: SCAN_MASSES and a one-byte code of
+// every float4 run, min(255, key of its largest value >> 22) (the binade and its top
+// mantissa bit, saturated): a run with an element above x has a code at least x's, so
+// a pass for the elements above x reads the codes and only the runs they admit.
+enum : int { SCAN_KEYS = 0, SCAN_MASSES = 1, SCAN_LOGITS = 2, SCAN_JOINT = 3 };
+__host__ __device__ inline uint32_t run_code(uint32_t key) { return min(255u, key >> 22); }
 
 // Per lane and block of four values, a few min / max / add instructions: the block's
 // largest value (its order key after the warp maximum), its smallest (a negative one
@@ -126,6 +137,7 @@ __global__ void __launch_bounds__(NT, 4) scan_kernel(const ScanArgs a) {
     const long long step = (long long)gridDim.x * NW;
     const int spu = TB >> a.shift;  // segments per unit
     constexpr bool LOGITS = KIND == SCAN_LOGITS;
+    constexpr bool MASSES = KIND == SCAN_MASSES || KIND == SCAN_JOINT;
     const float fill = LOGITS ? __int_as_float(0xff800000) : 0.f;
     auto load_unit = [&](long long u, float4* v) {
         if (u < total) {
@@ -176,10 +188,12 @@ __global__ void __launch_bounds__(NT, 4) scan_kernel(const ScanArgs a) {
         float s[TB];
         float lo = 0.f;
         bool bad = false;
+        uint32_t cw = 0u;  // SCAN_JOINT: the lane's four run codes
 #pragma unroll
         for (int j = 0; j < TB; ++j) {
             const float4 v = A[j];
             const float mx = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+            if (KIND == SCAN_JOINT) cw |= run_code(prob_key(mx)) << (8 * j);
             s[j] = (v.x + v.y) + (v.z + v.w);
             if (LOGITS) {
                 bad |= isnan(s[j]) || mx == __int_as_float(0x7f800000);
@@ -191,7 +205,8 @@ __global__ void __launch_bounds__(NT, 4) scan_kernel(const ScanArgs a) {
         }
         if (!LOGITS) bad = lo < 0.f;
         float um = 0.f;
-        if (KIND == SCAN_MASSES) {
+        if (KIND == SCAN_JOINT) a.code[(size_t(r) * a.nu + q) * 32 + lane] = cw;
+        if (MASSES) {
 #pragma unroll
             for (int m = 16; m; m >>= 1)
 #pragma unroll
@@ -215,7 +230,7 @@ __global__ void __launch_bounds__(NT, 4) scan_kernel(const ScanArgs a) {
                 kk = mine ? max(kk, km[j]) : kk;
             }
             a.key[size_t(r) * a.ls + sg] = kk;
-            if (KIND == SCAN_MASSES) a.mass[size_t(r) * a.ls + sg] = ss;
+            if (MASSES) a.mass[size_t(r) * a.ls + sg] = ss;
         }
         const unsigned anybad = __ballot_sync(FULL, bad);
         if (lane == 0) {
@@ -235,7 +250,8 @@ __global__ void __launch_bounds__(NT, 4) scan_kernel(const ScanArgs a) {
 // and part[0] = (M; V as the bound of the positive count, bad flag, largest key), and
 // with `uhist` the histogram of the units' largest keys (key >> 21) added into uhist,
 // which the caller cleared (a block barrier orders the clear before the counts), and
-// with `umass` / `ukey` each unit's mass and largest key.  M
+// with `umass` / `ukey` each unit's mass and largest key, with `shist` the histogram of
+// the segments' keys (key >> 21) added into shist, cleared by the caller as uhist.  M
 // is the sum of the unit masses in a fixed order (thread t adds units t, t + NT, ...
 // in turn, then a tree over the lanes and the warps in order).  Every thread issues
 // all of its loads before it uses any (one round trip to L2).  The summary was
@@ -243,7 +259,7 @@ __global__ void __launch_bounds__(NT, 4) scan_kernel(const ScanArgs a) {
 // Block-collective; ends with a block barrier.
 __device__ __forceinline__ void load_summary(const SampleArgs& a, int r, Smem sm, bool masses, int warp, int lane,
                                              int tid, uint32_t* uhist = nullptr, float* umass = nullptr,
-                                             uint32_t* ukey = nullptr) {
+                                             uint32_t* ukey = nullptr, uint32_t* shist = nullptr) {
     const uint4* key4 = reinterpret_cast<const uint4*>(a.skey + size_t(r) * a.ls);
     const uint4* mass4 = reinterpret_cast<const uint4*>(a.smass + size_t(r) * a.ls);
     const uint4* st = a.sstat + size_t(r) * a.nu;
@@ -261,7 +277,7 @@ __device__ __forceinline__ void load_summary(const SampleArgs& a, int r, Smem sm
             m[h] = (masses && i < n4) ? __ldcg(mass4 + i) : make_uint4(0u, 0u, 0u, 0u);
             v[h] = i < a.nu ? __ldcg(st + i) : make_uint4(0u, 0u, 0u, 0u);
         }
-        if (uhist && i0 == 0) __syncthreads();  // the caller's clear of uhist, before any count
+        if ((uhist || shist) && i0 == 0) __syncthreads();  // the caller's clear of the histogram, before any count
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int i = i0 + h * NT + tid;
@@ -273,6 +289,7 @@ __device__ __forceinline__ void load_summary(const SampleArgs& a, int r, Smem sm
                     if (4 * i + c < a.ns) {
                         sm.segkey()[4 * i + c] = kk[c];
                         if (masses) sm.mass(0)[4 * i + c] = __uint_as_float(mm[c]);
+                        if (shist) atomicAdd(&shist[min(uint32_t(HBINS - 1), kk[c] >> 21)], 1u);
                     }
                 }
             }
@@ -942,222 +959,6 @@ FS_COLD __device__ void sample_row_fin(const SampleArgs& a) {
 // chains, not memory, set the time.  Any other row (a bad row index, no top-k filter,
 // fewer units than k, segments of several blocks, more than KF_LIVE live segments or
 // more than SMALL candidates) takes the general finishing path, out of line.
-// ------------------------------------------------------------------ lean joint finish
-
-// Each unit's mass above `low` (a pass over the row, from L2, by the whole CTA): warp w
-// takes a contiguous share of the units, two units' loads in flight; units whose
-// largest key is at most low's are not read (mass 0).  Returns the total, summed in a
-// fixed order (each warp its share in order, then the warps in order).  Block-collective.
-template <bool VEC>
-__device__ __forceinline__ float unit_pass(const float* __restrict__ row, int V, int nu, float low, float* umass,
-                                           const uint32_t* ukey, Smem sm, int warp, int lane) {
-    const uint32_t klow = prob_key(low);
-    int u0, u1;
-    warp_range(nu, warp, u0, u1);
-    auto load = [&](int u, float4* v) {
-        const bool on = u < u1 && ukey[u] > klow;
-#pragma unroll
-        for (int j = 0; j < TB; ++j)
-            v[j] = on ? load4<VEC, true>(row, V, (u * TB + j) * BLK + lane * 4, 0.f) : make_float4(0.f, 0.f, 0.f, 0.f);
-    };
-    float4 A[TB], Bv[TB];
-    load(u0, A);
-#pragma unroll 1
-    for (int u = u0; u < u1; ++u) {
-        load(u + 1, Bv);
-        float sacc = 0.f;
-#pragma unroll
-        for (int j = 0; j < TB; ++j)
-            sacc += ((A[j].x > low ? A[j].x : 0.f) + (A[j].y > low ? A[j].y : 0.f)) +
-                    ((A[j].z > low ? A[j].z : 0.f) + (A[j].w > low ? A[j].w : 0.f));
-        sacc = warp_sum(sacc);
-        if (lane == 0) umass[u] = sacc;
-#pragma unroll
-        for (int j = 0; j < TB; ++j) A[j] = Bv[j];
-    }
-    __syncwarp();
-    const float ws = warp_ordered_sum(umass, u0, u1, lane);
-    float* rf = reinterpret_cast<float*>(sm.red()) + 64;
-    if (lane == 0) rf[warp] = ws;
-    __syncthreads();
-    float tot = 0.f;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) tot += rf[w];
-    __syncthreads();
-    return tot;
-}
-
-// The unit holding target t in the running sum of umass[0, nu) (index order): the first
-// unit with positive mass whose running sum passes t, else the last unit with positive
-// mass (-1 if none) ([blog] implementation details: the scan is not monotone in floating
-// point, so the pick is forced onto an eligible unit).  `before` = the running sum up to
-// it.  Thread t sums a contiguous range; one block scan.  Block-collective.
-__device__ __forceinline__ int locate_unit(const float* umass, int nu, float t, Smem sm, int tid, int warp, int lane,
-                                           float& before) {
-    const int c = (nu + NT - 1) / NT;
-    const int a0 = min(nu, tid * c), a1 = min(nu, a0 + c);
-    float own = 0.f;
-#pragma unroll 1
-    for (int i = a0; i < a1; ++i) own += umass[i];
-    const float incl = warp_incl_scan(own, lane);
-    float* rf = reinterpret_cast<float*>(sm.red()) + 64;
-    int* ri = sm.red() + 80;
-    if (lane == 31) rf[warp] = incl;
-    if (tid == 0) {
-        ri[0] = INT_BIG;  // first hit
-        ri[1] = -1;       // last positive unit
-    }
-    __syncthreads();
-    float wbase = 0.f;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) wbase += w < warp ? rf[w] : 0.f;
-    float run = wbase + incl - own;
-    int hit = INT_BIG, lastpos = -1;
-#pragma unroll 1
-    for (int i = a0; i < a1; ++i) {
-        const float m = umass[i];
-        if (m > 0.f) {
-            lastpos = i;
-            if (hit == INT_BIG && run + m > t) hit = i;
-        }
-        run += m;
-    }
-    if (hit != INT_BIG) atomicMin(&ri[0], hit);
-    if (lastpos >= 0) atomicMax(&ri[1], lastpos);
-    __syncthreads();
-    const int pick = ri[0] != INT_BIG ? ri[0] : ri[1];
-    if (pick >= a0 && pick < a1) {  // the owner of the pick writes the sum before it
-        float bsum = wbase + incl - own;
-        for (int i = a0; i < pick; ++i) bsum += umass[i];
-        rf[8] = bsum;
-    }
-    __syncthreads();
-    before = rf[8];
-    __syncthreads();
-    return pick;
-}
-
-// The rejection rounds of the joint order ([blog] dual-pivot rejection sampling) for a
-// row whose top-k bound uk <= t_k leaves n >= k candidates, all in the list lv/li[0, n)
-// (every element >= uk, in index order).  f(tau) needs the count and mass above tau only
-// for tau >= uk, and every element above such a tau is in the list; below uk at least n
-// >= k elements lie above tau, so f fails there without a reduction.  While `low` >= uk
-// the draw is over the list; below uk it needs each unit's mass above low, from the
-// summary for low = 0 and from a pass over the row (unit_pass) after a round that leaves
-// low below uk.  Block-collective; thread 0 writes the outputs.
-template <bool VEC>
-__device__ __forceinline__ void joint_rounds(const SampleArgs& a, Smem sm, const float* row, int b, int k, uint32_t uk,
-                                             int n, const float* uni, float* umass, const uint32_t* ukey, int tid,
-                                             int warp, int lane) {
-    const float tp = __uint_as_float(sm.prm()[1]);
-    const float mp = __uint_as_float(sm.prm()[2]);
-    const unsigned long long seed_b = *reinterpret_cast<const unsigned long long*>(sm.prm() + 4);
-    const unsigned long long offset_b = *reinterpret_cast<const unsigned long long*>(sm.prm() + 6);
-    const uint32_t stream_b = a.seeds ? 0u : uint32_t(b);
-    const float M = sm.part()[0].f[0];
-    const bool any_bad = sm.part()[0].u[1] != 0u;
-    const float rowmax = __uint_as_float(sm.part()[0].u[2]);
-    Pred f;
-    f.single = a.single_pivot != 0;
-    f.k_on = true;
-    f.k = k;
-    f.p_on = tp < 1.f;
-    f.m_on = mp > 0.f;
-    f.pthr = tp * M;
-    f.t32 = 0.f;
-    bool valid = !isnan(tp) && !isnan(mp) && !any_bad && M > 0.f && M <= 3.402823466e38f;
-    if (f.m_on) {
-        f.t32 = __double2float_ru(double(mp) * double(rowmax));
-        if (!(rowmax >= f.t32)) valid = false;
-    }
-    const float ukf = __uint_as_float(uk);
-    int* st = sm.red() + 88;                                   // [4] round results (ints)
-    float* sf = reinterpret_cast<float*>(sm.red()) + 92;      // [4] round results (floats)
-    float low = 0.f, high = rowmax, S_low = M;
-    bool listmode = false;  // low = 0 < uk
-    int token = -1, rounds = 0;
-#pragma unroll 1
-    for (int round = 0; valid && round < R_MAX; ++round) {
-        const float u = round < 32 ? uni[round] : sampler_uniform(seed_b, offset_b, stream_b, uint32_t(round));
-        const float t = u * S_low;
-        // ---- draw ([blog] inverse transform over the tokens above low)
-        if (listmode) {
-            if (warp == 0) {
-                const int e = locate_in_list(sm.lv(), n, low, t, lane);
-                if (lane == 0) {
-                    st[0] = e >= 0 ? sm.li()[e] : -1;
-                    sf[0] = e >= 0 ? sm.lv()[e] : 0.f;
-                }
-            }
-        } else {
-            float before = 0.f;
-            const int un = locate_unit(umass, a.nu, t, sm, tid, warp, lane, before);
-            if (warp == 0) {
-                unsigned long long jx = pack_jx(-1, 0.f);
-                if (un >= 0) jx = locate_in_blocks<VEC>(row, a.V, un * TB, TB, low, fmaxf(t - before, 0.f), lane);
-                if (lane == 0) {
-                    st[0] = unpack_j(jx);
-                    sf[0] = unpack_x(jx);
-                }
-            }
-        }
-        __syncthreads();
-        const int j = st[0];
-        const float pivot1 = sf[0];
-        if (j < 0) break;
-        const float pivot2 = f.pivot2(pivot1, high);
-        // ---- f at both pivots, from the list when the pivot is >= uk ([blog] dual pivot)
-        if (warp == 0) {
-            float m1 = 0.f, m2 = 0.f;
-            int c1 = 0, c2 = 0;
-            for (int i = lane; i < n; i += 32) {
-                const float x = sm.lv()[i];
-                const bool g1 = x > pivot1, g2 = x > pivot2;
-                m1 += g1 ? x : 0.f;
-                m2 += g2 ? x : 0.f;
-                c1 += g1;
-                c2 += g2;
-            }
-            m1 = warp_sum(m1);
-            m2 = warp_sum(m2);
-            c1 = warp_sum_i(c1);
-            c2 = warp_sum_i(c2);
-            const bool f1 = pivot1 >= ukf && f(c1, m1, pivot1);
-            const bool f2 = pivot2 >= ukf && f(c2, m2, pivot2);
-            if (lane == 0) {
-                st[1] = f1 ? 1 : (f2 ? 2 : 3);
-                sf[1] = m1;
-                sf[2] = m2;
-            }
-        }
-        __syncthreads();
-        const int kase = st[1];
-        const float m1 = sf[1], m2 = sf[2];
-        __syncthreads();
-        if (kase == 1) {
-            token = j;
-            rounds = round + 1;
-            break;
-        }
-        if (kase == 2) {
-            low = pivot1;
-            high = pivot2;
-            S_low = m1;
-        } else {
-            low = pivot2;
-            S_low = m2;
-        }
-        listmode = low >= ukf;
-        if (!listmode) S_low = unit_pass<VEC>(row, a.V, a.nu, low, umass, ukey, sm, warp, lane);
-        if (round == R_MAX - 1) rounds = R_MAX;
-    }
-    if (tid == 0) {
-        a.out_token[b] = token >= 0 ? token : -1;
-        a.out_valid[b] = token >= 0 ? 1 : 0;
-        if (a.out_rounds) a.out_rounds[b] = token >= 0 ? rounds : (valid ? R_MAX : 0);
-    }
-}
-
 constexpr int KF_LIVE = 112;  // live segments the lean finish stages (fpt = 15 float4 per thread at most)
 
 // The staging area of the lean finish (KF_LIVE blocks), after the carve-up.
@@ -1166,7 +967,7 @@ __device__ __forceinline__ float* kfirst_stage(Smem sm) {
     return reinterpret_cast<float*>(smem_raw + Layout(sm.ns).total());
 }
 
-template <bool VEC, bool JOINT>
+template <bool VEC>
 __global__ void __launch_bounds__(NT, 2) kfirst_kernel(const SampleArgs a) {
     const int b = int(cluster_id_x());
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1196,8 +997,7 @@ __global__ void __launch_bounds__(NT, 2) kfirst_kernel(const SampleArgs a) {
     }
     // ---- (1) the summary, with the histogram of the unit maxima; the bound
     if (row_ok) {
-        load_summary(a, r, sm, false, warp, lane, tid, sm.hist(), JOINT ? sm.mass(1) : nullptr,
-                     JOINT ? reinterpret_cast<uint32_t*>(sm.mass(2)) : nullptr);  // ends with a block barrier
+        load_summary(a, r, sm, false, warp, lane, tid, sm.hist());  // ends with a block barrier
     } else {
         __syncthreads();
     }
@@ -1290,7 +1090,7 @@ __global__ void __launch_bounds__(NT, 2) kfirst_kernel(const SampleArgs a) {
     const int wtot = lane < NW ? sm.red()[lane] : 0;
     const int wincl = warp_incl_scan_i(wtot, lane);
     const int n = __shfl_sync(FULL, wincl, NW - 1);
-    if (n > SMALL || (JOINT && n < k)) {  // joint: below uk, f must fail for lack of k
+    if (n > SMALL) {
         __syncthreads();
         sample_row_fin<VEC>(a);
         return;
@@ -1306,11 +1106,6 @@ __global__ void __launch_bounds__(NT, 2) kfirst_kernel(const SampleArgs a) {
         ++pos;
     }
     __syncthreads();
-    if (JOINT) {
-        joint_rounds<VEC>(a, sm, row, b, k, uk, n, uni, sm.mass(1), reinterpret_cast<const uint32_t*>(sm.mass(2)), tid,
-                          warp, lane);
-        return;
-    }
     // t_k: every candidate counts the candidates at or above it (the warps holding
     // candidates; broadcast reads, four independent sums); the largest with at least k
     // is t_k (0 when there are fewer than k: the row has fewer than k positives).
@@ -1392,6 +1187,730 @@ __global__ void __launch_bounds__(NT, 2) kfirst_kernel(const SampleArgs a) {
     }
 }
 
+// ------------------------------------------------------------------ lean joint finish
+//
+// The finishing launch of the joint order with a top-k filter on rows of
+// probabilities, one CTA per output row.  Each round ([blog] dual-pivot rejection
+// sampling) needs a draw over {p > low} in index order and the count and mass above
+// both pivots.  Both come from a list in shared memory whenever the list holds every
+// element above `low` (above the pivot, for f):
+//  * jmode 1 (rows that fit the shared memory): the whole row, staged once;
+//  * jmode 0: first the candidates, the elements at or above uk, the lower edge of the
+//    histogram bin (key >> 21) that holds the k-th largest block maximum, so that
+//    uk <= t_k (the block maxima are a subset of the row; [explainer] filter order).
+//    Below uk at least k elements lie above any threshold, so f fails there without a
+//    count.  A draw while low < uk needs each unit's mass above low: the scan's unit
+//    masses while low = 0, else one pass over the row through L2, which also copies
+//    every float4 run that holds an element above low into the second list; from then
+//    on every round runs on that list, since low never decreases.  If the second list
+//    overflows, the next draw below its threshold passes over the row again.
+// A list is a sequence of float4 runs of the row in index order (with the index of
+// each run's first element, or implied), cut into chunks of 32 runs; the pass that
+// evaluates f gives every chunk's mass above both pivots, which is the table of the
+// next round's draw.  Other rows (a bad row index, segments of several blocks, in
+// jmode 0 an invalid k, fewer blocks than k, or a candidate list that overflows or
+// counts fewer than k elements) take the general finishing path, out of line.
+
+constexpr int JCH = 512;   // chunks of a list, at most
+constexpr int JX4 = 1024;  // runs of the candidate list (JX4 / NW per warp)
+
+// The area after the carve-up: the two chunk-mass tables, the chunk bases (run
+// offsets) and the chunk maxima, JCH words each; then, in jmode 1, the row; in jmode 0
+// the candidate list (JX4 runs and their indices) and the second list (jy4 runs and
+// their indices).
+__host__ __device__ inline size_t jtab_off(int ns) { return Layout(ns).total(); }
+__host__ __device__ inline size_t jx_off(int ns) { return jtab_off(ns) + 4 * size_t(JCH) * 4; }
+__host__ __device__ inline size_t jy_off(int ns) { return jx_off(ns) + size_t(JX4) * 20; }
+
+// A list of runs: chunk c is v4[jb[c] .. jb[c] + 32).
+struct JList {
+    const float4* v4;
+    const int* ix;  // element index of each run's .x (nullptr: run i holds elements 4 i .. 4 i + 3)
+    int nch;        // chunks
+    float lo;       // every element above lo is in the list
+};
+
+__device__ __forceinline__ unsigned lanes_below(int lane) { return (1u << lane) - 1u; }
+
+// Appends the lane's run v (elements base .. base + 3) to a warp's slice s4 / si when
+// one of its values is above thr, the warp's runs in lane order.  wn counts the warp's
+// runs, past the slice's capacity cap too (nothing is written there).  Warp-collective.
+__device__ __forceinline__ void append_run(const float4& v, int base, float thr, float4* s4, int* si, int cap, int& wn,
+                                           int lane) {
+    const bool any = (v.x > thr) | (v.y > thr) | (v.z > thr) | (v.w > thr);
+    const unsigned bal = __ballot_sync(FULL, any);
+    const int pos = wn + __popc(bal & lanes_below(lane));
+    if (any && pos < cap) {
+        s4[pos] = v;
+        si[pos] = base;
+    }
+    wn += __popc(bal);
+}
+
+// Closes a list kept in slices (warp w's wn_w runs from run w * cap on): each slice
+// padded with zero runs to whole chunks, the chunk bases jb in slice order and the
+// chunk maxima jk.  Returns the chunk count, or -1 with the tables untouched when a
+// slice overflowed or the chunks exceed JCH.  Block-collective.
+__device__ __forceinline__ int close_list(float4* v4, int cap, int wn, int* jb, float* jk, Smem sm, int warp,
+                                          int lane) {
+    int* rw = sm.red() + 56;  // [NW]
+    if (lane == 0) rw[warp] = wn;
+    __syncthreads();
+    int before = 0, total = 0;
+    bool over = false;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+        const int c = rw[w];
+        over |= c > cap;
+        const int nc = (min(c, cap) + 31) >> 5;
+        before += w < warp ? nc : 0;
+        total += nc;
+    }
+    __syncthreads();  // every thread has read rw
+    if (over || total > JCH) return -1;
+    const int nc = (wn + 31) >> 5;
+    float4* s4 = v4 + size_t(warp) * cap;
+    for (int e = wn + lane; e < nc * 32; e += 32) s4[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+    __syncwarp();
+#pragma unroll 1
+    for (int i = 0; i < nc; ++i) {
+        const float4 v = s4[32 * i + lane];
+        const uint32_t m = warp_max_u(prob_key(fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w))));
+        if (lane == 0) {
+            jb[before + i] = warp * cap + 32 * i;
+            jk[before + i] = __uint_as_float(m);
+        }
+    }
+    __syncthreads();
+    return total;
+}
+
+// Every chunk's mass above t1 (m1c) and above t2 (m2c), and the totals: the masses
+// summed in a fixed order, the counts exact.  A chunk whose largest value is at most
+// min(t1, t2) holds nothing above either and is not read.  When more than DENSE
+// threads own a chunk to read, thread c takes chunk c (and c + NT): its 32 runs in an
+// order rotated by the lane, so that the eight lanes of an access phase read eight
+// different bank groups, and no shuffles; otherwise warp w takes chunks w, w + NW, ...
+// four at a time, one run per lane, the four chunks' reductions interleaved.  Each
+// thread (warp) adds its chunks in order, then the warps in order.  Block-collective;
+// every thread gets the totals.
+constexpr int DENSE = 64;
+__device__ __forceinline__ void chunk_pass(const JList& L, const int* jb, const float* jk, float t1, float t2,
+                                           float* m1c, float* m2c, Smem sm, int tid, int warp, int lane, float& m1,
+                                           float& m2, int& c1, int& c2) {
+    const float tmin = fminf(t1, t2);
+    bool own = false;
+    for (int c = tid; c < L.nch; c += NT) own |= jk[c] > tmin;
+    const bool dense = __syncthreads_count(own) > DENSE;
+    float s1 = 0.f, s2 = 0.f;
+    int n1 = 0, n2 = 0;
+    if (dense) {
+#pragma unroll 1
+        for (int c = tid; c < L.nch; c += NT) {
+            float a1 = 0.f, a2 = 0.f, b1 = 0.f, b2 = 0.f;
+            int k1 = 0, k2 = 0;
+            if (jk[c] > tmin) {
+                const float4* q = L.v4 + jb[c];
+#pragma unroll 4
+                for (int i = 0; i < 32; ++i) {
+                    const float4 v = q[(i + lane) & 31];
+                    a1 += (v.x > t1 ? v.x : 0.f) + (v.y > t1 ? v.y : 0.f);
+                    b1 += (v.z > t1 ? v.z : 0.f) + (v.w > t1 ? v.w : 0.f);
+                    a2 += (v.x > t2 ? v.x : 0.f) + (v.y > t2 ? v.y : 0.f);
+                    b2 += (v.z > t2 ? v.z : 0.f) + (v.w > t2 ? v.w : 0.f);
+                    k1 += int(v.x > t1) + int(v.y > t1) + int(v.z > t1) + int(v.w > t1);
+                    k2 += int(v.x > t2) + int(v.y > t2) + int(v.z > t2) + int(v.w > t2);
+                }
+            }
+            m1c[c] = a1 + b1;
+            m2c[c] = a2 + b2;
+            s1 += a1 + b1;
+            s2 += a2 + b2;
+            n1 += k1;
+            n2 += k2;
+        }
+        s1 = warp_sum(s1);
+        s2 = warp_sum(s2);
+        n1 = warp_sum_i(n1);
+        n2 = warp_sum_i(n2);
+    } else {
+#pragma unroll 1
+        for (int c0 = warp; c0 < L.nch; c0 += 4 * NW) {
+            bool act[4];
+            bool any = false;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int c = c0 + i * NW;
+                act[i] = c < L.nch && jk[c] > tmin;
+                any |= act[i];
+            }
+            float a1[4] = {0.f, 0.f, 0.f, 0.f}, a2[4] = {0.f, 0.f, 0.f, 0.f};
+            int k1[4] = {0, 0, 0, 0}, k2[4] = {0, 0, 0, 0};
+            if (any) {  // warp-uniform
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float4 v = act[i] ? L.v4[jb[c0 + i * NW] + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+                    a1[i] = ((v.x > t1 ? v.x : 0.f) + (v.y > t1 ? v.y : 0.f)) +
+                            ((v.z > t1 ? v.z : 0.f) + (v.w > t1 ? v.w : 0.f));
+                    a2[i] = ((v.x > t2 ? v.x : 0.f) + (v.y > t2 ? v.y : 0.f)) +
+                            ((v.z > t2 ? v.z : 0.f) + (v.w > t2 ? v.w : 0.f));
+                    k1[i] = int(v.x > t1) + int(v.y > t1) + int(v.z > t1) + int(v.w > t1);
+                    k2[i] = int(v.x > t2) + int(v.y > t2) + int(v.z > t2) + int(v.w > t2);
+                }
+#pragma unroll
+                for (int m = 16; m; m >>= 1) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        a1[i] += __shfl_xor_sync(FULL, a1[i], m);
+                        a2[i] += __shfl_xor_sync(FULL, a2[i], m);
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    k1[i] = __reduce_add_sync(FULL, k1[i]);
+                    k2[i] = __reduce_add_sync(FULL, k2[i]);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int c = c0 + i * NW;
+                if (c < L.nch) {
+                    if (lane == 0) {
+                        m1c[c] = a1[i];
+                        m2c[c] = a2[i];
+                    }
+                    s1 += a1[i];
+                    s2 += a2[i];
+                    n1 += k1[i];
+                    n2 += k2[i];
+                }
+            }
+        }
+    }
+    float* rf = reinterpret_cast<float*>(sm.red()) + 24;  // [NW] s1, [NW] s2
+    int* ri = sm.red() + 24 + 2 * NW;                     // [NW] n1, [NW] n2
+    if (lane == 0) {
+        rf[warp] = s1;
+        rf[NW + warp] = s2;
+        ri[warp] = n1;
+        ri[NW + warp] = n2;
+    }
+    __syncthreads();
+    m1 = 0.f;
+    m2 = 0.f;
+    c1 = 0;
+    c2 = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+        m1 += rf[w];
+        m2 += rf[NW + w];
+        c1 += ri[w];
+        c2 += ri[NW + w];
+    }
+    __syncthreads();
+}
+
+// Warp w's contiguous share of the units, streamed through a ring of four register
+// buffers: three units' loads are in flight while one is handed to op(u, v, i) (i =
+// u - u turn's first, a constant), and done(u) follows every fourth unit (units past the share are zeros, not read).  A
+// unit whose largest key is at most klow is not read either (zeros).  Warp-collective.
+template <bool VEC, typename Op, typename Done>
+__device__ __forceinline__ void stream_units(const float* __restrict__ row, int V, int u0, int u1, const uint32_t* ukey,
+                                             uint32_t klow, int lane, Op op, Done done) {
+    auto load1 = [&](int u, float4* v) {
+        const bool on = u < u1 && ukey[u] > klow;
+#pragma unroll
+        for (int j = 0; j < TB; ++j)
+            v[j] = on ? load4<VEC, true>(row, V, (u * TB + j) * BLK + lane * 4, 0.f) : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    float4 R0[TB], R1[TB], R2[TB], R3[TB];
+    load1(u0, R0);
+    load1(u0 + 1, R1);
+    load1(u0 + 2, R2);
+#pragma unroll 1
+    for (int u = u0; u < u1; u += 4) {
+        load1(u + 3, R3);
+        op(u, R0, 0);
+        load1(u + 4, R0);
+        op(u + 1, R1, 1);
+        load1(u + 5, R1);
+        op(u + 2, R2, 2);
+        load1(u + 6, R2);
+        op(u + 3, R3, 3);
+        done(u);
+    }
+}
+
+// Every run of the row that holds an element above low, appended in index order to
+// warp w's slice [w * ys, (w + 1) * ys) of the second list (wn: the warp's run count;
+// above ys the slice overflowed), from the row's run codes (SCAN_JOINT): (1) the code
+// words of the warp's share of the units (one word per lane and unit, copied into
+// shared memory first) admit the runs whose code is at least low's, and their element
+// indices go in index order into the slice's index array; (2) the admitted runs are
+// read through L2, 32 per lane group and eight groups in flight, and those with an
+// element above low are kept in place (a kept run never moves past its own slot).  A
+// unit whose largest key is at most low's admits nothing.  Warp-collective.
+template <bool VEC>
+__device__ __forceinline__ void compact_pass(const float* __restrict__ row, int V, int nu, float low,
+                                             const uint32_t* __restrict__ code, const uint32_t* ukey, float4* y4,
+                                             int* yi, int ys, int& wn, int warp, int lane) {
+    int u0, u1;
+    warp_range(nu, warp, u0, u1);
+    float4* s4 = y4 + size_t(warp) * ys;
+    int* si = yi + size_t(warp) * ys;
+    const uint32_t klow = prob_key(low);
+    const uint32_t clow = run_code(klow);
+    const unsigned below = lanes_below(lane);
+    // The code words go first into the slice's value array (free until step 2), one
+    // round trip per batch of ys / 8 units.
+    uint32_t* cw = reinterpret_cast<uint32_t*>(s4);
+    const int ucap = ys / 8;
+    int n = 0;
+#pragma unroll 1
+    for (int ub = u0; ub < u1; ub += ucap) {
+        const int ue = min(u1, ub + ucap);
+        const float* src = reinterpret_cast<const float*>(code + size_t(ub) * 32);
+#pragma unroll 1
+        for (int q = lane; q < (ue - ub) * 8; q += 32) cp_async16(reinterpret_cast<float*>(cw) + q * 4, src + q * 4, 16);
+        cp_async_commit();
+        cp_async_wait<0>();
+        __syncwarp();
+#pragma unroll 4
+        for (int u = ub; u < ue; ++u) {
+            const uint32_t cur = cw[(u - ub) * 32 + lane];
+            const bool on = ukey[u] > klow;
+            bool adm[TB];
+            unsigned bal[TB];
+#pragma unroll
+            for (int j = 0; j < TB; ++j) {
+                adm[j] = on && ((cur >> (8 * j)) & 0xffu) >= clow;
+                bal[j] = __ballot_sync(FULL, adm[j]);
+            }
+            int base = n;
+#pragma unroll
+            for (int j = 0; j < TB; ++j) {
+                const int pos = base + __popc(bal[j] & below);
+                if (adm[j] && pos < ys) si[pos] = ((u * TB + j) * 32 + lane) * 4;
+                base += __popc(bal[j]);
+            }
+            n = base;
+        }
+        __syncwarp();
+    }
+    if (n > ys) {
+        wn = n;
+        return;
+    }
+    __syncwarp();
+    constexpr int G = 8;  // groups of 32 admitted runs in flight
+    int m = 0;
+#pragma unroll 1
+    for (int c0 = 0; c0 < n; c0 += G * 32) {
+        float4 v[G];
+        int e[G];
+        bool in[G];
+#pragma unroll
+        for (int i = 0; i < G; ++i) {
+            const int c = c0 + i * 32 + lane;
+            in[i] = c < n;
+            e[i] = in[i] ? si[c] : 0;
+            v[i] = in[i] ? load4<VEC, true>(row, V, e[i], 0.f) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        __syncwarp();  // every lane has read its indices before any lane writes
+#pragma unroll
+        for (int i = 0; i < G; ++i) {
+            const bool keep = in[i] && fmaxf(fmaxf(v[i].x, v[i].y), fmaxf(v[i].z, v[i].w)) > low;
+            const unsigned bal = __ballot_sync(FULL, keep);
+            const int pos = m + __popc(bal & below);
+            if (keep) {
+                s4[pos] = v[i];
+                si[pos] = e[i];
+            }
+            m += __popc(bal);
+        }
+        __syncwarp();
+    }
+    wn = m;
+}
+
+// Each unit's mass above low (umass; a unit whose largest key is at most low's is 0)
+// and the total in a fixed order (returned), one pass through L2; the four units' warp
+// sums of a turn are interleaved.  Block-collective.
+template <bool VEC>
+__device__ __forceinline__ float mass_pass(const float* __restrict__ row, int V, int nu, float low, float* umass,
+                                           const uint32_t* ukey, Smem sm, int warp, int lane) {
+    int u0, u1;
+    warp_range(nu, warp, u0, u1);
+    float sm4[4];
+    stream_units<VEC>(row, V, u0, u1, ukey, prob_key(low), lane,
+        [&](int, const float4* v, int i) {
+            float sacc = 0.f;
+#pragma unroll
+            for (int j = 0; j < TB; ++j)
+                sacc += ((v[j].x > low ? v[j].x : 0.f) + (v[j].y > low ? v[j].y : 0.f)) +
+                        ((v[j].z > low ? v[j].z : 0.f) + (v[j].w > low ? v[j].w : 0.f));
+            sm4[i] = sacc;
+        },
+        [&](int u) {
+#pragma unroll
+            for (int m = 16; m; m >>= 1) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) sm4[i] += __shfl_xor_sync(FULL, sm4[i], m);
+            }
+            if (lane == 0) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (u + i < u1) umass[u + i] = sm4[i];
+            }
+        });
+    __syncwarp();
+    const float ws = warp_ordered_sum(umass, u0, u1, lane);
+    float* rf = reinterpret_cast<float*>(sm.red()) + 24;
+    if (lane == 0) rf[warp] = ws;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) tot += rf[w];
+    __syncthreads();
+    return tot;
+}
+
+// The guarded locate inside chunk c of a list (one run per lane, in index order).
+// Warp-collective.
+__device__ __forceinline__ unsigned long long locate_in_chunk(const JList& L, const int* jb, int c, float low, float t,
+                                                              int lane) {
+    const int run = jb[c] + lane;
+    const float4 v = L.v4[run];
+    const int base = L.ix ? L.ix[run] : 4 * run;
+    float rs = 0.f;
+    int last_j = -1;
+    float last_x = 0.f;
+    unsigned long long jx = 0ull;
+    if (locate_step(v, base, low, t, rs, last_j, last_x, jx, lane)) return jx;
+    return pack_jx(last_j, last_x);
+}
+
+// The entry holding target t in the running sum of m[0, n) (index order), by one warp:
+// lane l walks a contiguous range from the sum before it (one warp scan of the ranges'
+// sums).  The first entry with positive mass whose running sum passes t, else the last
+// entry with positive mass (-1 if none) ([blog] implementation details: the running sum
+// is not monotone in floating point, so the pick is forced onto an eligible entry);
+// `before` = the running sum before it.  Warp-collective.
+__device__ __forceinline__ int locate_entry_warp(const float* m, int n, float t, int lane, float& before) {
+    const int per = (n + 31) >> 5;
+    const int a0 = min(n, lane * per), a1 = min(n, a0 + per);
+    float own = 0.f;
+#pragma unroll 4
+    for (int i = a0; i < a1; ++i) own += m[i];
+    const float incl = warp_incl_scan(own, lane);
+    float run = incl - own;
+    int hit = -1, lastpos = -1;
+    float hit_before = 0.f, last_before = 0.f;
+#pragma unroll 1
+    for (int i = a0; i < a1; ++i) {
+        const float x = m[i];
+        if (x > 0.f) {
+            if (hit < 0 && run + x > t) {
+                hit = i;
+                hit_before = run;
+            }
+            lastpos = i;
+            last_before = run;
+        }
+        run += x;
+    }
+    const unsigned hb = __ballot_sync(FULL, hit >= 0);
+    if (hb) {
+        const int l = __ffs(hb) - 1;
+        before = __shfl_sync(FULL, hit_before, l);
+        return __shfl_sync(FULL, hit, l);
+    }
+    const unsigned pb = __ballot_sync(FULL, lastpos >= 0);
+    if (!pb) {
+        before = 0.f;
+        return -1;
+    }
+    const int l = 31 - __clz(pb);
+    before = __shfl_sync(FULL, last_before, l);
+    return __shfl_sync(FULL, lastpos, l);
+}
+
+template <bool VEC>
+__global__ void __launch_bounds__(NT, 1) kjoint_kernel(const SampleArgs a) {
+    const int b = int(cluster_id_x());
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const Smem sm(a.ns);
+    const int V = a.V, ns = a.ns, nu = a.nu;
+    const bool full = a.jmode != 0;
+    // The row index and the parameters are read before the dependency wait (written
+    // before the scan of this call started); only the summary comes from the scan.
+    const int r = a.indices ? a.indices[b] : b;
+    const bool row_ok = r >= 0 && r < a.batch_in;
+    if (tid == NT - 32) {
+        uint32_t* pr = sm.prm();
+        pr[0] = uint32_t(a.top_k ? a.top_k[b] : 0);
+        pr[1] = __float_as_uint(a.top_p ? a.top_p[b] : 1.f);
+        pr[2] = __float_as_uint(a.min_p ? a.min_p[b] : 0.f);
+        *reinterpret_cast<unsigned long long*>(pr + 4) = a.seeds ? a.seeds[b] : a.seed;
+    }
+    if (!full)
+        for (int i = tid; i < HBINS; i += NT) sm.hist()[i] = 0u;
+    const float* row = a.probs + size_t(row_ok ? r : 0) * size_t(V);
+    if (full && row_ok) {
+        // The whole row into shared memory (its blocks become the chunks), issued before
+        // the wait: the input rows were written before the scan of this call started.
+        float* stg = sm.at<float>(jx_off(ns));
+#pragma unroll 1
+        for (int c = warp; c < ns; c += NW) stage4<VEC>(stg + c * BLK + lane * 4, row, V, c * BLK + lane * 4);
+        cp_async_commit();
+    }
+    grid_dependency_wait();
+    allow_dependents();
+    if (b == 0 && tid < SCAN_CTRS && a.sctr) a.sctr[tid * SCAN_CTR_STRIDE] = 0u;  // the scan is complete
+    if (tid == NT - 32) {  // a device-resident offset may be advanced by the kernel before
+        *reinterpret_cast<unsigned long long*>(sm.prm() + 6) =
+            (a.offsets ? a.offsets[b] : a.offset) + (a.offset_dev ? *a.offset_dev : 0ull);
+    }
+    float* umass = sm.mass(1);
+    uint32_t* ukey = reinterpret_cast<uint32_t*>(sm.mass(2));
+    // ---- the summary: in jmode 1 with the segment masses (the first draw's table), in
+    // jmode 0 with the unit masses and keys and the histogram of the block maxima
+    if (row_ok) {
+        if (full)
+            load_summary(a, r, sm, true, warp, lane, tid);
+        else
+            load_summary(a, r, sm, false, warp, lane, tid, nullptr, umass, ukey, sm.hist());
+    } else {
+        __syncthreads();
+    }
+    const int k = int(sm.prm()[0]);
+    const bool k_on = k > 0 && k < V;
+    if (!row_ok || a.shift != 0 || (!full && (!k_on || ns < k))) {
+        cp_async_wait<0>();
+        __syncthreads();
+        sample_row_fin<VEC>(a);
+        return;
+    }
+    const unsigned long long seed_b = *reinterpret_cast<const unsigned long long*>(sm.prm() + 4);
+    const unsigned long long offset_b = *reinterpret_cast<const unsigned long long*>(sm.prm() + 6);
+    const uint32_t stream_b = a.seeds ? 0u : uint32_t(b);
+    float* uni = reinterpret_cast<float*>(sm.red()) + (REDW - 32);  // [32] the uniforms of rounds 0..31
+    if (warp == NW - 1) uni[lane] = sampler_uniform(seed_b, offset_b, stream_b, uint32_t(lane));
+    float* jm0 = sm.at<float>(jtab_off(ns));
+    float* jm1 = jm0 + JCH;
+    int* jb = reinterpret_cast<int*>(jm0 + 2 * JCH);
+    float* jk = jm0 + 3 * JCH;
+    JList L;
+    const float* cur = nullptr;  // each chunk's mass above low, while low >= L.lo
+    float4* y4 = nullptr;
+    int* yi = nullptr;
+    const int ys = a.jy4 / NW;  // runs per warp slice of the second list (a multiple of 32)
+    if (full) {
+        float4* v4 = sm.at<float4>(jx_off(ns));
+        for (int c = tid; c < ns; c += NT) {
+            jb[c] = 32 * c;
+            jk[c] = __uint_as_float(sm.segkey()[c]);
+        }
+        cp_async_wait<0>();
+        __syncthreads();
+        L.v4 = v4;
+        L.ix = nullptr;
+        L.nch = ns;
+        L.lo = 0.f;
+        cur = sm.mass(0);
+    } else {
+        // ---- uk; the live blocks (largest value >= uk) copied in index order into the
+        // second list's area (one round trip to L2), then each warp appends the runs of its
+        // own live blocks that hold a candidate
+        if (warp == 0) {
+            uint32_t above;
+            const int B = scan_bins_down<uint32_t>(sm.hist(), int(min(uint32_t(HBINS - 1), sm.part()[0].u[2] >> 21)),
+                                                   uint32_t(k), lane, above);
+            if (lane == 0) sm.bcast()[0] = max(B, 0);
+        }
+        __syncthreads();
+        const uint32_t uk = max(1u, uint32_t(sm.bcast()[0]) << 21);  // zeros are never candidates
+        const float lo = __uint_as_float(uk - 1u);                    // x > lo  <=>  x >= the float of uk
+        int r0, r1;
+        warp_range(ns, warp, r0, r1);
+        int nl = 0;
+#pragma unroll 1
+        for (int b0 = r0; b0 < r1; b0 += 32)
+            nl += __popc(__ballot_sync(FULL, b0 + lane < r1 && sm.segkey()[b0 + lane] >= uk));
+        if (lane == 0) sm.red()[warp] = nl;
+        __syncthreads();
+        int off = 0, nlive = 0;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            const int c = sm.red()[w];
+            off += w < warp ? c : 0;
+            nlive += c;
+        }
+        const int yblocks = int((size_t(a.jy4) * 20) / (BLK * 4));
+        if (nlive > yblocks) {
+            __syncthreads();
+            sample_row_fin<VEC>(a);
+            return;
+        }
+        float* stg = sm.at<float>(jy_off(ns));
+        int* seg = sm.list();  // [nlive] the staged blocks, in index order
+        const int off0 = off;
+#pragma unroll 1
+        for (int b0 = r0; b0 < r1; b0 += 32) {
+            unsigned bal = __ballot_sync(FULL, b0 + lane < r1 && sm.segkey()[b0 + lane] >= uk);
+#pragma unroll 1
+            while (bal) {
+                const int sg = b0 + __ffs(bal) - 1;
+                bal &= bal - 1u;
+                stage4<VEC>(stg + off * BLK + lane * 4, row, V, sg * BLK + lane * 4);
+                if (lane == 0) seg[off] = sg;
+                ++off;
+            }
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+        __syncthreads();  // every warp's copies and block numbers
+        float4* x4 = sm.at<float4>(jx_off(ns));
+        int* xi = sm.at<int>(jx_off(ns) + size_t(JX4) * 16);
+        constexpr int XS = JX4 / NW;
+        int wn = 0, cnt = 0;
+        const float4* stg4 = reinterpret_cast<const float4*>(stg);
+#pragma unroll 1
+        for (int q = off0; q < off0 + nl; ++q) {
+            const float4 v = stg4[q * 32 + lane];
+            append_run(v, seg[q] * BLK + lane * 4, lo, x4 + warp * XS, xi + warp * XS, XS, wn, lane);
+            cnt += int(v.x > lo) + int(v.y > lo) + int(v.z > lo) + int(v.w > lo);
+        }
+        cnt = warp_sum_i(cnt);
+        if (lane == 0) sm.red()[warp] = cnt;  // words 0 .. NW: no other use after the summary
+        const int nch = close_list(x4, XS, wn, jb, jk, sm, warp, lane);  // its barriers publish the counts
+        int n = 0;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) n += sm.red()[w];
+        if (nch < 0 || n < k) {
+            __syncthreads();
+            sample_row_fin<VEC>(a);
+            return;
+        }
+        L.v4 = x4;
+        L.ix = xi;
+        L.nch = nch;
+        L.lo = lo;
+        y4 = sm.at<float4>(jy_off(ns));
+        yi = sm.at<int>(jy_off(ns) + size_t(a.jy4) * 16);
+    }
+    // ---- the rounds ([blog] dual-pivot rejection sampling)
+    const float tp = __uint_as_float(sm.prm()[1]);
+    const float mp = __uint_as_float(sm.prm()[2]);
+    const float M = sm.part()[0].f[0];
+    const bool any_bad = sm.part()[0].u[1] != 0u;
+    const float rowmax = __uint_as_float(sm.part()[0].u[2]);
+    Pred f;
+    f.single = a.single_pivot != 0;
+    f.k_on = k_on;
+    f.k = k;
+    f.p_on = tp < 1.f;
+    f.m_on = mp > 0.f;
+    f.pthr = tp * M;
+    f.t32 = 0.f;
+    bool valid = !isnan(tp) && !isnan(mp) && !any_bad && M > 0.f && M <= 3.402823466e38f;
+    if (f.m_on) {
+        f.t32 = __double2float_ru(double(mp) * double(rowmax));
+        if (!(rowmax >= f.t32)) valid = false;
+    }
+    int* st = sm.red() + 88;                               // [4] round results (ints)
+    float* sf = reinterpret_cast<float*>(sm.red()) + 92;  // [4] round results (floats)
+    float low = 0.f, high = rowmax, S_low = M;
+    if (!full && L.lo <= 0.f) {  // every positive element is a candidate: the list serves from the first draw
+        float m2 = 0.f;
+        int c1 = 0, c2 = 0;
+        chunk_pass(L, jb, jk, 0.f, 0.f, jm0, jm1, sm, tid, warp, lane, S_low, m2, c1, c2);
+        cur = jm0;
+    }
+    int token = -1, rounds = 0;
+#pragma unroll 1
+    for (int round = 0; valid && round < R_MAX; ++round) {
+        const float u = round < 32 ? uni[round] : sampler_uniform(seed_b, offset_b, stream_b, uint32_t(round));
+        // ---- below the list's threshold after the first round: one pass through L2 copies
+        // every run above low into the second list, whose chunk masses above low are then
+        // this draw's table; if that list overflows, the pass gives each unit's mass above low
+        if (low < L.lo && round > 0) {
+            int nch = -1;
+            if (ys >= 32) {
+                int wn = 0;
+                compact_pass<VEC>(row, V, nu, low, a.scode + size_t(r) * nu * 32, ukey, y4, yi, ys, wn, warp, lane);
+                nch = close_list(y4, ys, wn, jb, jk, sm, warp, lane);
+            }
+            if (nch >= 0) {
+                L.v4 = y4;
+                L.ix = yi;
+                L.nch = nch;
+                L.lo = low;
+                float m2 = 0.f;
+                int c1 = 0, c2 = 0;
+                chunk_pass(L, jb, jk, low, low, jm0, jm1, sm, tid, warp, lane, S_low, m2, c1, c2);
+                cur = jm0;
+            } else {
+                S_low = mass_pass<VEC>(row, V, nu, low, umass, ukey, sm, warp, lane);
+            }
+        }
+        // ---- draw j by inverse transform over the tokens above low ([blog]): from the
+        // list's chunk masses, else from the unit masses and the unit read through L2
+        if (warp == 0) {
+            const float t = u * S_low;
+            float before = 0.f;
+            unsigned long long jx = pack_jx(-1, 0.f);
+            if (low >= L.lo) {
+                const int c = locate_entry_warp(cur, L.nch, t, lane, before);
+                if (c >= 0) jx = locate_in_chunk(L, jb, c, low, fmaxf(t - before, 0.f), lane);
+            } else {
+                const int un = locate_entry_warp(umass, nu, t, lane, before);
+                if (un >= 0) jx = locate_in_unit<VEC>(row, V, un, low, fmaxf(t - before, 0.f), lane);
+            }
+            if (lane == 0) {
+                st[0] = unpack_j(jx);
+                sf[0] = unpack_x(jx);
+            }
+        }
+        __syncthreads();
+        const int j = st[0];
+        const float pivot1 = sf[0];
+        if (j < 0) break;
+        const float pivot2 = f.pivot2(pivot1, high);
+        // ---- f at both pivots: from the list at or above its threshold, else false
+        int kase = 3;
+        float m1 = 0.f, m2 = 0.f;
+        if (fmaxf(pivot1, pivot2) >= L.lo) {
+            int c1 = 0, c2 = 0;
+            chunk_pass(L, jb, jk, pivot1, pivot2, jm0, jm1, sm, tid, warp, lane, m1, m2, c1, c2);
+            const bool f1 = pivot1 >= L.lo && f(c1, m1, pivot1);
+            const bool f2 = pivot2 >= L.lo && f(c2, m2, pivot2);
+            kase = f1 ? 1 : (f2 ? 2 : 3);
+        }
+        if (kase == 1) {
+            token = j;
+            rounds = round + 1;
+            break;
+        }
+        if (kase == 2) {
+            low = pivot1;
+            high = pivot2;
+            S_low = m1;
+            cur = jm0;
+        } else {
+            low = pivot2;
+            S_low = m2;
+            cur = jm1;
+        }
+        if (round == R_MAX - 1) rounds = R_MAX;
+    }
+    if (tid == 0) {
+        a.out_token[b] = token >= 0 ? token : -1;
+        a.out_valid[b] = token >= 0 ? 1 : 0;
+        if (a.out_rounds) a.out_rounds[b] = token >= 0 ? rounds : (valid ? R_MAX : 0);
+    }
+}
+
 // ------------------------------------------------------------------ host side
 
 #ifndef FS_SCAN_PER_SM
@@ -1425,6 +1944,7 @@ static fs_status launch_scan(const float* x, int rows, int V, int shift, int ns,
     s.key = reinterpret_cast<uint32_t*>(body);
     s.mass = reinterpret_cast<float*>(body + size_t(rows) * s.ls * 4);
     s.stat = reinterpret_cast<uint4*>(body + 2 * size_t(rows) * s.ls * 4);
+    s.code = reinterpret_cast<uint32_t*>(body + 2 * size_t(rows) * s.ls * 4 + size_t(rows) * s.nu * 16);
     s.ctr = reinterpret_cast<unsigned*>(ws);
     const long long total = (long long)rows * s.nu;
     s.ustatic = total - total / 5;
@@ -1459,8 +1979,8 @@ static fs_status launch_scan_finish(const float* probs, int32_t batch_in, int32_
     const bool kjoint = !soft && order == FS_ORDER_JOINT && top_k;
     auto fin_fn = [&]() -> void (*)(SampleArgs) {
         if (soft) return vec ? sample_kernel<true, true, true> : sample_kernel<false, true, true>;
-        if (kfirst) return vec ? kfirst_kernel<true, false> : kfirst_kernel<false, false>;
-        if (kjoint) return vec ? kfirst_kernel<true, true> : kfirst_kernel<false, true>;
+        if (kfirst) return vec ? kfirst_kernel<true> : kfirst_kernel<false>;
+        if (kjoint) return vec ? kjoint_kernel<true> : kjoint_kernel<false>;
         return vec ? sample_kernel<true, false, true> : sample_kernel<false, false, true>;
     };
     void (*fn)(SampleArgs) = fin_fn();
@@ -1475,22 +1995,41 @@ static fs_status launch_scan_finish(const float* probs, int32_t batch_in, int32_
     p.shift = seg_shift_for(vocab);
     p.ns = (vocab + (BLK << p.shift) - 1) / (BLK << p.shift);
     p.nsc = (p.ns + 3) & ~3;
-    p.smem = ((kfirst || kjoint) && !soft) ? kfirst_smem(p.ns) : Layout(p.ns).total();
+    p.smem = (kfirst && !soft) ? kfirst_smem(p.ns) : Layout(p.ns).total();
+    int jmode = 0, jy4 = 0;
+    if (kjoint) {
+        // The whole row when it fits beside the tables; else the candidate list and, in
+        // the rest of the device's limit, the second list (whole chunks per warp).
+        const size_t row_end = jx_off(p.ns) + size_t(p.ns) * BLK * 4;
+        if (p.shift == 0 && p.ns <= JCH && row_end <= optin) {
+            jmode = 1;
+            p.smem = row_end;
+        } else {
+            p.smem = optin;
+            if (optin > jy_off(p.ns)) {
+                constexpr size_t quantum = size_t(NW) * 32;
+                jy4 = int((optin - jy_off(p.ns)) / 20 / quantum * quantum);
+                if (jy4 > JCH * 32) jy4 = JCH * 32;  // its chunks fit the table
+            }
+        }
+    }
     p.per_sm = 0;
-    if (p.smem > optin) return FS_ERR_UNSUPPORTED;
+    if (p.smem > optin || (kjoint && p.smem < jy_off(p.ns) && jmode == 0)) return FS_ERR_UNSUPPORTED;
     void* ws = nullptr;
     // Top-k-first launches draw from gathered candidates: no segment masses needed.
     if (batch_in > 0) {
         if (fixed_ws) {
             ws = fixed_ws;  // caller-checked to hold the summaries
         } else {
-            st = workspace(scan_workspace_bytes(batch_in, vocab), stream, &ws);
+            st = workspace(scan_workspace_bytes(batch_in, vocab, kjoint), stream, &ws);
             if (st != FS_OK) return st;
         }
         if (soft)
             st = launch_scan<SCAN_LOGITS>(probs, batch_in, vocab, p.shift, p.ns, vec, ws, stream);
         else if (kfirst)
             st = launch_scan<SCAN_KEYS>(probs, batch_in, vocab, p.shift, p.ns, vec, ws, stream);
+        else if (kjoint)
+            st = launch_scan<SCAN_JOINT>(probs, batch_in, vocab, p.shift, p.ns, vec, ws, stream);
         else
             st = launch_scan<SCAN_MASSES>(probs, batch_in, vocab, p.shift, p.ns, vec, ws, stream);
         if (st != FS_OK) return st;
@@ -1523,7 +2062,12 @@ static fs_status launch_scan_finish(const float* probs, int32_t batch_in, int32_
     a.skey = ws ? reinterpret_cast<const uint32_t*>(body) : nullptr;
     a.smass = (ws && !soft && !kfirst) ? reinterpret_cast<const float*>(body + size_t(batch_in) * a.ls * 4) : nullptr;  // joint and unfiltered: segment masses
     a.sstat = ws ? reinterpret_cast<const uint4*>(body + 2 * size_t(batch_in) * a.ls * 4) : nullptr;
+    a.scode = (ws && kjoint) ? reinterpret_cast<const uint32_t*>(body + 2 * size_t(batch_in) * a.ls * 4 +
+                                                                  size_t(batch_in) * a.nu * 16)
+                             : nullptr;
     a.sctr = reinterpret_cast<unsigned*>(ws);
+    a.jmode = jmode;
+    a.jy4 = jy4;
     return launch_cluster(fn, p, batch_out, stream, a);
 }
 
@@ -1675,8 +2219,10 @@ fs_status fs_top_k_top_p_sampling_noalloc(const float* probs, int32_t batch_in, 
                                           int32_t* out_rounds, void* stream) {
     if ((!top_k || !top_p) && batch_out > 0) return FS_ERR_INVALID_ARG;
     void* scratch = nullptr;
-    if (order == FS_ORDER_TOP_K_FIRST && batch_out > 0 && batch_in > 0 && vocab >= 1 && vocab <= FS_MAX_VOCAB) {
-        const size_t need = fsd::scan_workspace_bytes(batch_in, vocab);
+    // Both orders run as the scan and a finishing launch here (top_k is given); the joint
+    // order's summaries also hold the run codes.
+    if (batch_out > 0 && batch_in > 0 && vocab >= 1 && vocab <= FS_MAX_VOCAB) {
+        const size_t need = fsd::scan_workspace_bytes(batch_in, vocab, order == FS_ORDER_JOINT);
         if (need > size_t(FS_NOALLOC_SCRATCH_BYTES)) {
             fsd::set_last_error("fs_top_k_top_p_sampling_noalloc: the row summaries of this batch need more than "
                                 "FS_NOALLOC_SCRATCH_BYTES of fixed scratch (see fs_workspace_bytes)");
@@ -1688,7 +2234,6 @@ fs_status fs_top_k_top_p_sampling_noalloc(const float* probs, int32_t batch_in, 
         const cudaError_t e = cudaMemsetAsync(scratch, 0, fsd::SCAN_HEAD, static_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) return fsd::cuda_fail(e);
     }
-    // The joint order runs on clusters and needs no scratch; nothing allocates either way.
     return fsd::launch_sample(probs, batch_in, vocab, indices, batch_out, top_k, top_p, min_p, order, seed, offset,
                               out_token, out_valid, out_rounds, stream, nullptr, nullptr, nullptr, 2, false, nullptr,
                               scratch);

@@ -44,22 +44,23 @@ def test_noalloc_entry_matches_the_allocating_entry():
     p = torch.from_numpy(w.top_p).to(dev)
     stream = P(torch.cuda.current_stream(dev).cuda_stream)
 
-    def run(name, offset):
+    def run(name, order, offset):
         tok = torch.full((B,), -7, dtype=torch.int32, device=dev)
         val = torch.full((B,), 7, dtype=torch.uint8, device=dev)
         rnd = torch.full((B,), -7, dtype=torch.int32, device=dev)
-        st = getattr(so, name)(P(x.data_ptr()), B, V, None, B, P(k.data_ptr()), P(p.data_ptr()), None, 0,
+        st = getattr(so, name)(P(x.data_ptr()), B, V, None, B, P(k.data_ptr()), P(p.data_ptr()), None, order,
                                1234, offset, P(tok.data_ptr()), P(val.data_ptr()), P(rnd.data_ptr()), stream)
         assert st == 0, (name, st, so.fs_last_error_string())
         torch.cuda.synchronize(dev)
         return tok.cpu().numpy(), val.cpu().numpy(), rnd.cpu().numpy()
 
-    for offset in (5, 6):   # two calls in a row on each entry
-        ref = run("fs_top_k_top_p_sampling", offset)
-        got = run("fs_top_k_top_p_sampling_noalloc", offset)
-        for a, b in zip(ref, got):
-            assert np.array_equal(a, b), offset
-        assert got[1].all() and (got[0] >= 0).all() and (got[2] >= 1).all()
+    for order in (0, 1):          # top-k-first, joint: both keep their summaries in the fixed array
+        for offset in (5, 6):     # two calls in a row on each entry
+            ref = run("fs_top_k_top_p_sampling", order, offset)
+            got = run("fs_top_k_top_p_sampling_noalloc", order, offset)
+            for a, b in zip(ref, got):
+                assert np.array_equal(a, b), (order, offset)
+            assert got[1].all() and (got[0] >= 0).all() and (got[2] >= 1).all()
 
 
 def test_noalloc_entry_rejects_batches_beyond_its_scratch():
