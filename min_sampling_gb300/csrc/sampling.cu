@@ -1719,10 +1719,24 @@ __global__ void __launch_bounds__(NT, 1) kjoint_kernel(const SampleArgs a) {
         L.lo = 0.f;
         cur = sm.mass(0);
     } else {
+        // ---- the first draw, by warp 0 while the others build the candidate list: over
+        // the whole row (low = 0), from the scan's unit masses and one read of the unit.
+        // It is used when the first round runs below the list's threshold (uk > 1).
+        if (warp == 0) {
+            const float t = sampler_uniform(seed_b, offset_b, stream_b, 0u) * sm.part()[0].f[0];
+            float before = 0.f;
+            const int un = locate_entry_warp(umass, nu, t, lane, before);
+            unsigned long long jx = pack_jx(-1, 0.f);
+            if (un >= 0) jx = locate_in_unit<VEC>(row, V, un, 0.f, fmaxf(t - before, 0.f), lane);
+            if (lane == 0) {
+                sm.red()[88] = unpack_j(jx);
+                reinterpret_cast<float*>(sm.red())[92] = unpack_x(jx);
+            }
+        }
         // ---- uk; the live blocks (largest value >= uk) copied in index order into the
         // second list's area (one round trip to L2), then each warp appends the runs of its
         // own live blocks that hold a candidate
-        if (warp == 0) {
+        if (warp == 1) {
             uint32_t above;
             const int B = scan_bins_down<uint32_t>(sm.hist(), int(min(uint32_t(HBINS - 1), sm.part()[0].u[2] >> 21)),
                                                    uint32_t(k), lane, above);
@@ -1855,8 +1869,9 @@ __global__ void __launch_bounds__(NT, 1) kjoint_kernel(const SampleArgs a) {
             }
         }
         // ---- draw j by inverse transform over the tokens above low ([blog]): from the
-        // list's chunk masses, else from the unit masses and the unit read through L2
-        if (warp == 0) {
+        // list's chunk masses, else from the unit masses and the unit read through L2 (the
+        // first round's below-threshold draw was made during the set-up)
+        if (warp == 0 && !(round == 0 && low < L.lo)) {
             const float t = u * S_low;
             float before = 0.f;
             unsigned long long jx = pack_jx(-1, 0.f);
