@@ -277,8 +277,9 @@ fs_status fs_chain_speculative_sampling(const float* draft_probs, const int32_t*
  * top-k-first entries (fs_top_k_top_p_sampling*, order top-k-first) and of
  * fs_sampling_from_probs: a scan of every row with *ctas_per_sm CTAs on every SM,
  * then one CTA per row (*cluster = 1) that finishes the row from its summary
- * (*segments_per_cta = the row's segments); the joint order with a top-k filter on
- * rows of probabilities runs the same two launches.  FS_ORDER_JOINT gives the plan of
+ * (*segments_per_cta = the row's segments; fs_sampling_from_probs finishes with one
+ * warp per row); the joint order with a top-k filter on rows of probabilities runs
+ * the same two launches.  FS_ORDER_JOINT gives the plan of
  * the cluster kernel: fs_top_p_sampling and fs_min_p_sampling, whose rejection rounds
  * pass over the row several times on a cluster of CTAs, for rows of
  * probabilities that are 16-byte aligned with vocab % 4 = 0 (other rows run a

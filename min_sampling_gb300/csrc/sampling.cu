@@ -58,6 +58,7 @@ struct SampleArgs {
     int ls;                   // words per row of skey / smass
     int nu;                   // units per row
     unsigned* sctr;           // the scan's claim counters, set back to zero by output row 0
+    int nout;                 // output rows (kdraw_kernel: one warp per output row)
     // Joint-order finish (kjoint_kernel): 1 = the whole row is staged in shared memory;
     // 0 = candidate list, then a list of the elements above low of a.jy4 float4 runs.
     int jmode;
@@ -1926,6 +1927,112 @@ __global__ void __launch_bounds__(NT, 1) kjoint_kernel(const SampleArgs a) {
     }
 }
 
+// ------------------------------------------------------------------ lean draw (no filter)
+//
+// The finishing launch of sampling without filters on rows of probabilities, one warp
+// per output row.  With no filter f holds at every pivot, so the first draw of the
+// rejection sampler is the sample ([blog] dual-pivot rejection sampling: accept j when
+// f(p_j) holds): the inverse transform over the whole row ([blog] inverse transform
+// sampling), from the scan's unit masses (lane l sums a contiguous range of units; one
+// warp scan gives M and every range's start), the guarded pick of the unit, then the
+// element inside the unit read through L2.  Two round trips to L2 after the scan.
+template <bool VEC>
+__global__ void __launch_bounds__(NT) kdraw_kernel(const SampleArgs a) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = int(blockIdx.x) * NW + warp;
+    const bool in_range = b < a.nout;
+    // Read before the dependency wait: written before the scan of this call started.
+    const int r = in_range ? (a.indices ? a.indices[b] : b) : -1;
+    const unsigned long long seed_b = in_range ? (a.seeds ? a.seeds[b] : a.seed) : 0ull;
+    grid_dependency_wait();
+    allow_dependents();
+    if (b == 0 && lane < SCAN_CTRS && a.sctr) a.sctr[lane * SCAN_CTR_STRIDE] = 0u;  // the scan is complete
+    if (!in_range) return;
+    const unsigned long long offset_b =
+        (a.offsets ? a.offsets[b] : a.offset) + (a.offset_dev ? *a.offset_dev : 0ull);
+    const uint32_t stream_b = a.seeds ? 0u : uint32_t(b);
+    const int nu = a.nu;
+    int token = -1;
+    bool valid = false;
+    if (r >= 0 && r < a.batch_in) {
+        const uint4* st = a.sstat + size_t(r) * nu;
+        const int per = (nu + 31) >> 5;
+        const int a0 = min(nu, lane * per), a1 = min(nu, a0 + per);
+        // The lane's unit masses in registers (KD units at a time, every load issued
+        // before the first is used); ranges longer than KD are read again for the walk.
+        constexpr int KD = 16;
+        float um[KD];
+        float own = 0.f;
+        bool bad = false;
+#pragma unroll 1
+        for (int c0 = a0; c0 < a1; c0 += KD) {
+#pragma unroll
+            for (int q = 0; q < KD; ++q) {
+                const uint4 v = c0 + q < a1 ? __ldcg(st + c0 + q) : make_uint4(0u, 0u, 0u, 0u);
+                um[q] = __uint_as_float(v.x);
+                bad |= v.z != 0u;
+            }
+#pragma unroll
+            for (int q = 0; q < KD; ++q) own += um[q];
+        }
+        const float incl = warp_incl_scan(own, lane);
+        const float M = __shfl_sync(FULL, incl, 31);
+        bad = __any_sync(FULL, bad);
+        valid = !bad && M > 0.f && M <= 3.402823466e38f;
+        if (valid) {
+            const float t = sampler_uniform(seed_b, offset_b, stream_b, 0u) * M;
+            // the first unit with positive mass whose running sum passes t, else the last
+            // unit with positive mass (the sum is not monotone in floating point)
+            float run = incl - own;
+            int hit = -1, lastpos = -1;
+            float hit_before = 0.f, last_before = 0.f;
+            const bool in_regs = a1 - a0 <= KD;
+#pragma unroll 1
+            for (int c0 = a0; c0 < a1; c0 += KD) {
+                if (!in_regs) {
+#pragma unroll
+                    for (int q = 0; q < KD; ++q) um[q] = c0 + q < a1 ? __uint_as_float(__ldcg(&st[c0 + q].x)) : 0.f;
+                }
+#pragma unroll
+                for (int q = 0; q < KD; ++q) {
+                    const float m = um[q];
+                    if (c0 + q < a1 && m > 0.f) {
+                        if (hit < 0 && run + m > t) {
+                            hit = c0 + q;
+                            hit_before = run;
+                        }
+                        lastpos = c0 + q;
+                        last_before = run;
+                    }
+                    run += m;
+                }
+            }
+            const unsigned hb = __ballot_sync(FULL, hit >= 0);
+            const unsigned pb = __ballot_sync(FULL, lastpos >= 0);
+            int un = -1;
+            float before = 0.f;
+            if (hb) {
+                const int l = __ffs(hb) - 1;
+                un = __shfl_sync(FULL, hit, l);
+                before = __shfl_sync(FULL, hit_before, l);
+            } else if (pb) {
+                const int l = 31 - __clz(pb);
+                un = __shfl_sync(FULL, lastpos, l);
+                before = __shfl_sync(FULL, last_before, l);
+            }
+            if (un >= 0) {
+                const float* row = a.probs + size_t(r) * size_t(a.V);
+                token = unpack_j(locate_in_unit<VEC>(row, a.V, un, 0.f, fmaxf(t - before, 0.f), lane));
+            }
+        }
+    }
+    if (lane == 0) {
+        a.out_token[b] = token >= 0 ? token : -1;
+        a.out_valid[b] = token >= 0 ? 1 : 0;
+        if (a.out_rounds) a.out_rounds[b] = token >= 0 ? 1 : (valid ? R_MAX : 0);
+    }
+}
+
 // ------------------------------------------------------------------ host side
 
 #ifndef FS_SCAN_PER_SM
@@ -1992,10 +2099,12 @@ static fs_status launch_scan_finish(const float* probs, int32_t batch_in, int32_
                                     const float* temperature, bool vec, void* fixed_ws = nullptr) {
     const bool kfirst = order == FS_ORDER_TOP_K_FIRST && top_k;
     const bool kjoint = !soft && order == FS_ORDER_JOINT && top_k;
+    const bool kdraw = !soft && !top_k && !top_p && !min_p;  // no filter: the first draw is the sample
     auto fin_fn = [&]() -> void (*)(SampleArgs) {
         if (soft) return vec ? sample_kernel<true, true, true> : sample_kernel<false, true, true>;
         if (kfirst) return vec ? kfirst_kernel<true> : kfirst_kernel<false>;
         if (kjoint) return vec ? kjoint_kernel<true> : kjoint_kernel<false>;
+        if (kdraw) return vec ? kdraw_kernel<true> : kdraw_kernel<false>;
         return vec ? sample_kernel<true, false, true> : sample_kernel<false, false, true>;
     };
     void (*fn)(SampleArgs) = fin_fn();
@@ -2083,6 +2192,11 @@ static fs_status launch_scan_finish(const float* probs, int32_t batch_in, int32_
     a.sctr = reinterpret_cast<unsigned*>(ws);
     a.jmode = jmode;
     a.jy4 = jy4;
+    a.nout = batch_out;
+    if (kdraw) {  // one warp per output row, no shared memory
+        p.smem = 0;
+        return launch_cluster(fn, p, (batch_out + NW - 1) / NW, stream, a);
+    }
     return launch_cluster(fn, p, batch_out, stream, a);
 }
 
