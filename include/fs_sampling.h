@@ -21,9 +21,10 @@
  *  - Every pointer argument is a DEVICE pointer owned by the caller, unless stated.
  *    Each call is asynchronous on `stream` (a cudaStream_t passed as void*; NULL is
  *    the legacy default stream) and may be made from several host threads at once.
- *  - Scratch memory.  The top-k-first samplers, the joint order with a top-k filter
- *    on rows of probabilities (fs_top_k_top_p_sampling*, fs_top_k_sampling) and
- *    fs_sampling_from_probs run as two launches: a scan that reads every input row
+ *  - Scratch memory.  The top-k-first samplers, the joint order with a top-k or a
+ *    min-p filter on rows of probabilities (fs_top_k_top_p_sampling*,
+ *    fs_top_k_sampling, fs_min_p_sampling) and fs_sampling_from_probs run as two
+ *    launches: a scan that reads every input row
  *    once, spread evenly over the GPU, and writes a small summary of each row (a few
  *    bytes per 128 values; the joint order adds one byte per 4 values), then one CTA
  *    per output row that finishes the row from that summary.  The summaries live in a
@@ -278,10 +279,10 @@ fs_status fs_chain_speculative_sampling(const float* draft_probs, const int32_t*
  * fs_sampling_from_probs: a scan of every row with *ctas_per_sm CTAs on every SM,
  * then one CTA per row (*cluster = 1) that finishes the row from its summary
  * (*segments_per_cta = the row's segments; fs_sampling_from_probs finishes with one
- * warp per row); the joint order with a top-k filter on rows of probabilities runs
- * the same two launches.  FS_ORDER_JOINT gives the plan of
- * the cluster kernel: fs_top_p_sampling and fs_min_p_sampling, whose rejection rounds
- * pass over the row several times on a cluster of CTAs, for rows of
+ * warp per row); the joint order with a top-k or a min-p filter on rows of
+ * probabilities (fs_top_k_sampling, fs_min_p_sampling) runs the same two launches.
+ * FS_ORDER_JOINT gives the plan of the cluster kernel: fs_top_p_sampling, whose
+ * rejection rounds pass over the row several times on a cluster of CTAs, for rows of
  * probabilities that are 16-byte aligned with vocab % 4 = 0 (other rows run a
  * scalar-load build of the same kernel).  Outputs (host pointers): CTAs per row
  * (*cluster), elements per segment, segments per CTA and the most CTAs resident on

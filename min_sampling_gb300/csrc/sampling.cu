@@ -1686,7 +1686,10 @@ __global__ void __launch_bounds__(NT, 1) kjoint_kernel(const SampleArgs a) {
     }
     const int k = int(sm.prm()[0]);
     const bool k_on = k > 0 && k < V;
-    if (!row_ok || a.shift != 0 || (!full && (!k_on || ns < k))) {
+    const float mp_row = __uint_as_float(sm.prm()[2]);
+    const bool m_on = mp_row > 0.f;  // a min-p filter: f fails below min_p * max
+    // jmode 0 needs a threshold below which f fails: the top-k bound (ns >= k) or min-p
+    if (!row_ok || a.shift != 0 || (!full && !(k_on && ns >= k) && !m_on)) {
         cp_async_wait<0>();
         __syncthreads();
         sample_row_fin<VEC>(a);
@@ -1737,15 +1740,22 @@ __global__ void __launch_bounds__(NT, 1) kjoint_kernel(const SampleArgs a) {
         // ---- uk; the live blocks (largest value >= uk) copied in index order into the
         // second list's area (one round trip to L2), then each warp appends the runs of its
         // own live blocks that hold a candidate
-        if (warp == 1) {
+        const bool kb = k_on && ns >= k;  // the top-k bound is available
+        if (warp == 1 && kb) {
             uint32_t above;
             const int B = scan_bins_down<uint32_t>(sm.hist(), int(min(uint32_t(HBINS - 1), sm.part()[0].u[2] >> 21)),
                                                    uint32_t(k), lane, above);
             if (lane == 0) sm.bcast()[0] = max(B, 0);
         }
         __syncthreads();
-        const uint32_t uk = max(1u, uint32_t(sm.bcast()[0]) << 21);  // zeros are never candidates
-        const float lo = __uint_as_float(uk - 1u);                    // x > lo  <=>  x >= the float of uk
+        // uk: the larger of the top-k bound and the min-p threshold (the float32 of
+        // min_p * max rounded up, as f takes it), below either of which f fails.
+        const uint32_t uk_k = kb ? max(1u, uint32_t(sm.bcast()[0]) << 21) : 0u;
+        const uint32_t uk_m =
+            m_on ? prob_key(__double2float_ru(double(mp_row) * double(__uint_as_float(sm.part()[0].u[2])))) : 0u;
+        const uint32_t uk = max(1u, max(uk_k, uk_m));  // zeros are never candidates
+        const bool by_min_p = m_on && uk_m >= uk_k;     // f fails below uk by min-p, whatever the count
+        const float lo = __uint_as_float(uk - 1u);      // x > lo  <=>  x >= the float of uk
         int r0, r1;
         warp_range(ns, warp, r0, r1);
         int nl = 0;
@@ -1802,7 +1812,7 @@ __global__ void __launch_bounds__(NT, 1) kjoint_kernel(const SampleArgs a) {
         int n = 0;
 #pragma unroll
         for (int w = 0; w < NW; ++w) n += sm.red()[w];
-        if (nch < 0 || n < k) {
+        if (nch < 0 || (!by_min_p && n < k)) {
             __syncthreads();
             sample_row_fin<VEC>(a);
             return;
@@ -2098,7 +2108,7 @@ static fs_status launch_scan_finish(const float* probs, int32_t batch_in, int32_
                                     const uint64_t* offsets, const uint64_t* offset_dev, int32_t pivots, bool soft,
                                     const float* temperature, bool vec, void* fixed_ws = nullptr) {
     const bool kfirst = order == FS_ORDER_TOP_K_FIRST && top_k;
-    const bool kjoint = !soft && order == FS_ORDER_JOINT && top_k;
+    const bool kjoint = !soft && order == FS_ORDER_JOINT && (top_k || min_p);
     const bool kdraw = !soft && !top_k && !top_p && !min_p;  // no filter: the first draw is the sample
     auto fin_fn = [&]() -> void (*)(SampleArgs) {
         if (soft) return vec ? sample_kernel<true, true, true> : sample_kernel<false, true, true>;
@@ -2223,7 +2233,7 @@ static fs_status launch_sample(const float* probs, int32_t batch_in, int32_t voc
     // (masses of logits depend on the temperature, so sampling logits without filters
     // stays on the clusters).
     const bool fin = (order == FS_ORDER_TOP_K_FIRST && top_k) || (!soft && !top_k && !top_p && !min_p) ||
-                     (!soft && order == FS_ORDER_JOINT && top_k);
+                     (!soft && order == FS_ORDER_JOINT && (top_k || min_p));
     if (fin) return launch_scan_finish(probs, batch_in, vocab, indices, batch_out, top_k, top_p, min_p, order, seed,
                                        offset, out_token, out_valid, out_rounds, stream, seeds, offsets, offset_dev,
                                        pivots, soft, temperature, vec, fixed_ws);
