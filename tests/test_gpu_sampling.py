@@ -340,6 +340,36 @@ def test_misaligned_rows_and_large_k_first(ms):
             _membership(masks, vref, tok, valid)
 
 
+def test_misaligned_long_rows_on_the_two_launch_finishes(ms):
+    """Scalar loads on the finishing launches: a base address off the 16-byte grid and
+    V % 4 != 0, with rows long enough for the joint finish's candidate list and second
+    list (not the whole row on chip).  Joint top-k + top-p, min-p (its threshold bounds
+    the candidates) and sampling without filters; every draw in S over several calls,
+    and 16 parallel samples of every row through `indices`."""
+    import torch
+    acc = guard_accept(lambda i: [(50, 0.9, None, "joint")])
+    w = workloads.config3(batch=8, vocab=100003, accept=acc, with_logits=False)
+    flat = torch.empty(w.probs.size + 1, dtype=torch.float32, device="cuda")
+    flat[1:] = torch.from_numpy(w.probs.reshape(-1)).cuda()
+    P = flat[1:].view(w.probs.shape)
+    ks = np.full(8, 50, np.int32)
+    ps = np.full(8, 0.9, np.float32)
+    mps = np.full(8, 0.1, np.float32)
+    cases = [("joint", ks, ps, None), ("min_p", None, None, mps), ("from_probs", None, None, None)]
+    for entry, k, p, mp in cases:
+        oa = _oracle_args(entry, k, p, mp)
+        masks, vref = allowed_masks(w.probs, oa[0], oa[1], oa[2], oa[3])
+        for call in range(3):
+            tok, valid, rounds = _call(ms, entry, P, k, p, mp, seed=13, offset=call)
+            _membership(masks, vref, tok, valid)
+        idx = np.repeat(np.arange(8, dtype=np.int32), 16)
+        kk = None if k is None else k[idx]
+        pp = None if p is None else p[idx]
+        mm = None if mp is None else mp[idx]
+        tok, valid, _ = _call(ms, entry, P, kk, pp, mm, indices=idx, seed=17, offset=4)
+        _membership(masks[idx], vref[idx], tok, valid)
+
+
 def test_single_pivot_ablation(ms):
     """The one-pivot rule ([blog] rejection sampling) through the ablation entry: the
     same law (TV, chi-square, every draw in S), the oracle's one-pivot run replayed on
