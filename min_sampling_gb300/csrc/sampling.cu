@@ -2150,7 +2150,8 @@ static fs_status launch_scan_finish(const float* probs, int32_t batch_in, int32_
     p.per_sm = 0;
     if (p.smem > optin || (kjoint && p.smem < jy_off(p.ns) && jmode == 0)) return FS_ERR_UNSUPPORTED;
     void* ws = nullptr;
-    // Top-k-first launches draw from gathered candidates: no segment masses needed.
+    // Top-k-first launches draw from gathered candidates and unfiltered ones from the unit
+    // records: no segment masses needed.
     if (batch_in > 0) {
         if (fixed_ws) {
             ws = fixed_ws;  // caller-checked to hold the summaries
@@ -2160,7 +2161,7 @@ static fs_status launch_scan_finish(const float* probs, int32_t batch_in, int32_
         }
         if (soft)
             st = launch_scan<SCAN_LOGITS>(probs, batch_in, vocab, p.shift, p.ns, vec, ws, stream);
-        else if (kfirst)
+        else if (kfirst || kdraw)  // kdraw reads only the unit records
             st = launch_scan<SCAN_KEYS>(probs, batch_in, vocab, p.shift, p.ns, vec, ws, stream);
         else if (kjoint)
             st = launch_scan<SCAN_JOINT>(probs, batch_in, vocab, p.shift, p.ns, vec, ws, stream);
@@ -2194,7 +2195,8 @@ static fs_status launch_scan_finish(const float* probs, int32_t batch_in, int32_
     a.nu = scan_units(vocab);
     const char* body = ws ? reinterpret_cast<const char*>(ws) + SCAN_HEAD : nullptr;
     a.skey = ws ? reinterpret_cast<const uint32_t*>(body) : nullptr;
-    a.smass = (ws && !soft && !kfirst) ? reinterpret_cast<const float*>(body + size_t(batch_in) * a.ls * 4) : nullptr;  // joint and unfiltered: segment masses
+    a.smass = (ws && !soft && !kfirst && !kdraw) ? reinterpret_cast<const float*>(body + size_t(batch_in) * a.ls * 4)
+                                                 : nullptr;  // the joint order: segment masses
     a.sstat = ws ? reinterpret_cast<const uint4*>(body + 2 * size_t(batch_in) * a.ls * 4) : nullptr;
     a.scode = (ws && kjoint) ? reinterpret_cast<const uint32_t*>(body + 2 * size_t(batch_in) * a.ls * 4 +
                                                                   size_t(batch_in) * a.nu * 16)
