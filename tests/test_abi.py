@@ -137,3 +137,43 @@ def test_binding_rejects_tensors_on_another_device():
     _same_device(a.device, x=a, y=None)
     with pytest.raises(ValueError):
         _same_device(a.device, draft_probs=a, draft_tokens=torch.zeros(3, device="meta"))
+
+
+def test_workspace_bytes_follow_the_documented_layout(so):
+    """fs_workspace_bytes: 2 KB of counters, then per row 8 bytes per segment of the
+    plan (rounded up to 4 segments), 16 bytes per 512 values and, for the joint
+    order's run codes, one byte per 4 values (per 512-value unit, 128 bytes)."""
+    f = so.fs_workspace_bytes
+    f.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t)]
+    f.restype = ctypes.c_int
+
+    def expect(B, V):
+        shift = 0 if V <= 4096 * 128 else (1 if V <= 4096 * 256 else 2)
+        seg = 128 << shift
+        ns = (V + seg - 1) // seg
+        ls = (ns + 3) // 4 * 4
+        nu = (V + 511) // 512
+        return 2048 + B * (2 * ls * 4 + nu * (16 + 128))
+
+    for B, V in ((1, 1), (64, 151936), (256, 256000), (3, 32000), (5, 600001)):
+        out = ctypes.c_size_t(0)
+        assert f(B, V, ctypes.byref(out)) == 0
+        assert out.value == expect(B, V), (B, V)
+    out = ctypes.c_size_t(0)
+    f(64, 151936, ctypes.byref(out))
+    assert abs(out.value / 1e6 - 3.35) < 0.01   # the header's example: 3.3 MB in the joint order
+
+
+def test_noalloc_rejects_a_joint_batch_that_fits_only_top_k_first(so):
+    """256 rows of 256000 values: 6.1 MB of summaries top-k-first (within the fixed
+    array), 22.5 MB with the joint order's run codes (rejected before any CUDA call)."""
+    f = so.fs_top_k_top_p_sampling_noalloc
+    P = ctypes.c_void_p
+    f.argtypes = [P, ctypes.c_int32, ctypes.c_int32, P, ctypes.c_int32, P, P, P, ctypes.c_int32, ctypes.c_uint64,
+                  ctypes.c_uint64, P, P, P, P]
+    f.restype = ctypes.c_int
+    so.fs_last_error_string.restype = ctypes.c_char_p
+    fake = P(0x1000)   # never dereferenced: the size check comes first
+    st = f(fake, 256, 256000, None, 256, fake, fake, None, 1, 1, 2, fake, fake, None, None)
+    assert st == 2
+    assert b"FS_NOALLOC_SCRATCH_BYTES" in so.fs_last_error_string()
