@@ -1,7 +1,14 @@
 // Dual-pivot rejection sampler (sm_103a).
 //
-// One thread-block cluster per output row; see fs_device.cuh for the execution model.
-// Steps, in the order the pages give them:
+// Two execution models.  The top-k-first samplers, the joint order with a top-k or a
+// min-p filter and sampling without filters, on rows of probabilities, run as a scan
+// of every input row spread evenly over the GPU (scan_kernel, writing a small summary
+// of each row) and one finishing launch (kfirst_kernel, kjoint_kernel: one CTA per
+// output row; kdraw_kernel: one warp per output row); see the sections below.  The
+// other samplers run on one thread-block cluster per output row (sample_kernel; see
+// fs_device.cuh for its execution model), and so do the rows the lean finishes hand
+// over (the cluster code with a cluster of one, after the scan).
+// The cluster sampler's steps, in the order the pages give them:
 //   pass 1   every CTA reads its share of the row once; the leader ends up with every
 //            segment's maximum key and mass, each CTA's mass, the row total M, the
 //            positive count and a NaN/negative flag;
@@ -1190,26 +1197,29 @@ __global__ void __launch_bounds__(NT, 2) kfirst_kernel(const SampleArgs a) {
 
 // ------------------------------------------------------------------ lean joint finish
 //
-// The finishing launch of the joint order with a top-k filter on rows of
+// The finishing launch of the joint order with a top-k or a min-p filter on rows of
 // probabilities, one CTA per output row.  Each round ([blog] dual-pivot rejection
 // sampling) needs a draw over {p > low} in index order and the count and mass above
 // both pivots.  Both come from a list in shared memory whenever the list holds every
 // element above `low` (above the pivot, for f):
 //  * jmode 1 (rows that fit the shared memory): the whole row, staged once;
-//  * jmode 0: first the candidates, the elements at or above uk, the lower edge of the
-//    histogram bin (key >> 21) that holds the k-th largest block maximum, so that
-//    uk <= t_k (the block maxima are a subset of the row; [explainer] filter order).
-//    Below uk at least k elements lie above any threshold, so f fails there without a
-//    count.  A draw while low < uk needs each unit's mass above low: the scan's unit
-//    masses while low = 0, else one pass over the row through L2, which also copies
-//    every float4 run that holds an element above low into the second list; from then
-//    on every round runs on that list, since low never decreases.  If the second list
-//    overflows, the next draw below its threshold passes over the row again.
+//  * jmode 0: first the candidates, the elements at or above uk, the larger of the
+//    lower edge of the histogram bin (key >> 21) that holds the k-th largest block
+//    maximum (so that uk <= t_k: the block maxima are a subset of the row;
+//    [explainer] filter order) and the min-p threshold.  Below uk f fails without a
+//    count: at least k elements lie above any threshold there, or min-p fails.  A draw
+//    while low < uk needs each unit's mass above low: the scan's unit masses while
+//    low = 0 (that draw is made by warp 0 during the set-up), else one pass over the
+//    row through L2, which also copies every float4 run that holds an element above
+//    low into the second list; from then on every round runs on that list, since low
+//    never decreases.  If the second list overflows, the next draw below its
+//    threshold passes over the row again.
 // A list is a sequence of float4 runs of the row in index order (with the index of
 // each run's first element, or implied), cut into chunks of 32 runs; the pass that
 // evaluates f gives every chunk's mass above both pivots, which is the table of the
 // next round's draw.  Other rows (a bad row index, segments of several blocks, in
-// jmode 0 an invalid k, fewer blocks than k, or a candidate list that overflows or
+// jmode 0 neither a top-k bound (a valid k, at most as many as the blocks) nor
+// min-p, or a candidate list that overflows or, bounded by the top-k bound alone,
 // counts fewer than k elements) take the general finishing path, out of line.
 
 constexpr int JCH = 512;   // chunks of a list, at most
